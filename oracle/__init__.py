@@ -1,0 +1,351 @@
+"""CPU oracle for the recurrent-state hot path -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline / reference
+legs of ``bench.py`` import this package.  The product library never does, and
+this package never imports the product library: the two share no code.
+
+The arithmetic lives in ``rs_oracle.c`` (plain C loops, IEEE binary32,
+``-ffp-contract=off``); this module only builds it with gcc and marshals numpy
+arrays through ctypes.  Page citations are in the C source.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "rs_oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
+# Each result below depends on these flags: no contraction of a*b+c into an
+# FMA, no fast-math reassociation, IEEE division and rounding.
+CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+          "-fno-unsafe-math-optimizations", "-fPIC", "-shared"]
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``rs_oracle.c`` into ``_build/liboracle.so`` (gcc)."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+    subprocess.check_call(["gcc", *CFLAGS, _SRC, "-o", tmp, "-lm"])
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = ctypes.CDLL(build())
+            _declare(_lib)
+        return _lib
+
+
+def build_variant(source: str, out_path: str) -> str:
+    """Compile an edited copy of the oracle source (used by the mutation test
+    that checks the pins catch planted mistakes)."""
+    src = out_path + ".c"
+    with open(src, "w") as f:
+        f.write(source)
+    subprocess.check_call(["gcc", *CFLAGS, src, "-o", out_path, "-lm"])
+    return out_path
+
+
+class use_library:
+    """Context manager: route every call of this module through another build
+    of the oracle (a planted-mistake variant), then restore the real one."""
+
+    def __init__(self, path: str):
+        self.path = path
+
+    def __enter__(self):
+        global _lib
+        self._saved = lib()
+        variant = ctypes.CDLL(self.path)
+        _declare(variant)
+        with _lock:
+            _lib = variant
+        return self
+
+    def __exit__(self, *exc):
+        global _lib
+        with _lock:
+            _lib = self._saved
+        return False
+
+
+def source() -> str:
+    with open(_SRC) as f:
+        return f.read()
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+_I64 = ctypes.c_int64
+
+
+def _declare(L):
+    L.orc_step_tile_f32.argtypes = [_I, _I, _P, _P, _P, _P, _P, _I, _F, _P]
+    L.orc_step_tile_f32.restype = None
+    L.orc_row_scale.argtypes = [_I, _P]
+    L.orc_row_scale.restype = _F
+    L.orc_quant_code.argtypes = [_F, _F]
+    L.orc_quant_code.restype = ctypes.c_int8
+    L.orc_quantise_row.argtypes = [_I, _P, _P, _P]
+    L.orc_dequantise_row.argtypes = [_I, _P, _F, _P]
+    L.orc_mixed_tile_bytes.argtypes = [_I, _I, _I]
+    L.orc_mixed_tile_bytes.restype = ctypes.c_size_t
+    L.orc_mixed_unpack.argtypes = [_I, _I, _I, _P, _P]
+    L.orc_mixed_pack.argtypes = [_I, _I, _I, _P, _P]
+    L.orc_convert_f32_to_mixed.argtypes = [_I, _I, _I, _P, _P, _P]
+    L.orc_convert_f32_to_mixed.restype = _I
+    L.orc_convert_mixed_to_f32.argtypes = [_I, _I, _I, _P, _P, _P]
+    L.orc_convert_mixed_to_f32.restype = _I
+    L.orc_decode_f32.argtypes = [_I, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P, _P,
+                                 _P, _P, _P, _I, _I]
+    L.orc_decode_f32.restype = _I
+    L.orc_decode_mixed.argtypes = [_I, _I, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P,
+                                   _P, _P, _P, _P, _P, _I, _I]
+    L.orc_decode_mixed.restype = _I
+    L.orc_replay_f32.argtypes = [_I, _I, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P,
+                                 _P, _P, _P, _P, _P, _I, _I]
+    L.orc_replay_f32.restype = _I
+    L.orc_replay_mixed.argtypes = [_I, _I, _I, _I, _I, _I, _I, _I, _P, _I, _P, _P,
+                                   _P, _P, _P, _P, _P, _P, _P, _I, _I]
+    L.orc_replay_mixed.restype = _I
+    L.orc_plan_offsets.argtypes = [_I, _I, _I, _I, _P, _P]
+    L.orc_ckpt_pack.argtypes = [_I, _I, _I, _I, _I, _P, _P, _I64, _I, _P, _P, _I,
+                                _P, _I]
+    L.orc_ckpt_pack.restype = _I
+    L.orc_ckpt_restore.argtypes = [_I, _I, _I, _I, _I, _P, _P, _I, _P, _P, _I64,
+                                   _I, _P, _I]
+    L.orc_ckpt_restore.restype = _I
+
+
+# --------------------------------------------------------------------------
+# numpy marshalling helpers
+# --------------------------------------------------------------------------
+def _c(a: np.ndarray, dtype) -> np.ndarray:
+    if a.dtype != dtype or not a.flags["C_CONTIGUOUS"]:
+        raise TypeError(f"expected C-contiguous {np.dtype(dtype)}, got {a.dtype}")
+    return a
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def step_tile(S, q, k, v, a, beta, want_o=True):
+    """One decode step on one tile, in place on ``S`` [dk][dv] (float32).
+    ``a`` is a float32 scalar array of shape () / (1,) for GDN or (dk,) for KDA."""
+    dk, dv = S.shape
+    _c(S, np.float32)
+    q = np.ascontiguousarray(q, np.float32)
+    k = np.ascontiguousarray(k, np.float32)
+    v = np.ascontiguousarray(v, np.float32)
+    a = np.ascontiguousarray(np.atleast_1d(a), np.float32)
+    o = np.zeros(dv, np.float32) if want_o else None
+    lib().orc_step_tile_f32(dk, dv, _ptr(S), _ptr(q), _ptr(k), _ptr(v), _ptr(a),
+                            0 if a.size == 1 else 1, float(np.float32(beta)), _ptr(o))
+    return o
+
+
+def row_scale(x):
+    x = np.ascontiguousarray(x, np.float32)
+    return np.float32(lib().orc_row_scale(x.size, _ptr(x)))
+
+
+def quantise_row(x):
+    x = np.ascontiguousarray(x, np.float32)
+    codes = np.zeros(x.size, np.int8)
+    s = np.zeros(1, np.float32)
+    lib().orc_quantise_row(x.size, _ptr(x), _ptr(codes), _ptr(s))
+    return codes, s[0]
+
+
+def dequantise_row(codes, s):
+    codes = np.ascontiguousarray(codes, np.int8)
+    x = np.zeros(codes.size, np.float32)
+    lib().orc_dequantise_row(codes.size, _ptr(codes), float(np.float32(s)), _ptr(x))
+    return x
+
+
+def mixed_tile_bytes(dk, dv, khi):
+    return int(lib().orc_mixed_tile_bytes(dk, dv, khi))
+
+
+def mixed_unpack(tile, dk, dv, khi):
+    tile = _c(np.ascontiguousarray(tile), np.uint8)
+    T = np.zeros((dk, dv), np.float32)
+    lib().orc_mixed_unpack(dk, dv, khi, _ptr(tile), _ptr(T))
+    return T
+
+
+def mixed_pack(T, khi):
+    T = _c(np.ascontiguousarray(T), np.float32)
+    dk, dv = T.shape
+    tile = np.zeros(mixed_tile_bytes(dk, dv, khi), np.uint8)
+    lib().orc_mixed_pack(dk, dv, khi, _ptr(T), _ptr(tile))
+    return tile
+
+
+def convert_f32_to_mixed(S, khi, pi):
+    """Logical FP32 head ``S`` [dk][dv] -> mixed tile bytes with row map ``pi``."""
+    S = _c(np.ascontiguousarray(S), np.float32)
+    dk, dv = S.shape
+    pi = np.ascontiguousarray(pi, np.int16)
+    tile = np.zeros(mixed_tile_bytes(dk, dv, khi), np.uint8)
+    assert lib().orc_convert_f32_to_mixed(dk, dv, khi, _ptr(pi), _ptr(S), _ptr(tile)) == 0
+    return tile
+
+
+def convert_mixed_to_f32(tile, dk, dv, khi, pi):
+    tile = _c(np.ascontiguousarray(tile), np.uint8)
+    pi = np.ascontiguousarray(pi, np.int16)
+    S = np.zeros((dk, dv), np.float32)
+    assert lib().orc_convert_mixed_to_f32(dk, dv, khi, _ptr(pi), _ptr(tile), _ptr(S)) == 0
+    return S
+
+
+def convert_pool_f32_to_mixed(pool, khi, pi):
+    """[..., Hv, dk, dv] float32 -> [..., Hv, tile_bytes] uint8; pi [Hv][dk]."""
+    *lead, Hv, dk, dv = pool.shape
+    flat = pool.reshape(-1, Hv, dk, dv)
+    out = np.zeros((flat.shape[0], Hv, mixed_tile_bytes(dk, dv, khi)), np.uint8)
+    for s in range(flat.shape[0]):
+        for h in range(Hv):
+            out[s, h] = convert_f32_to_mixed(np.ascontiguousarray(flat[s, h]), khi, pi[h])
+    return out.reshape(*lead, Hv, out.shape[-1])
+
+
+def convert_pool_mixed_to_f32(pool, dk, dv, khi, pi):
+    *lead, Hv, tb = pool.shape
+    flat = pool.reshape(-1, Hv, tb)
+    out = np.zeros((flat.shape[0], Hv, dk, dv), np.float32)
+    for s in range(flat.shape[0]):
+        for h in range(Hv):
+            out[s, h] = convert_mixed_to_f32(np.ascontiguousarray(flat[s, h]), dk, dv, khi, pi[h])
+    return out.reshape(*lead, Hv, dk, dv)
+
+
+def decode_f32(pool, slot_idx, q, k, v, alpha, beta, o=None, per_channel=None,
+               items=None):
+    """Batched FP32 decode step in place on ``pool`` [n_slots][Hv][dk][dv].
+    q, k: [B][Hk][dk]; v: [B][Hv][dv]; alpha: [B][Hv] or [B][Hv][dk];
+    beta: [B][Hv].  Returns (o [B][Hv][dv], status bits)."""
+    _c(pool, np.float32)
+    n_slots, Hv, dk, dv = pool.shape
+    B, Hk, _ = q.shape
+    if per_channel is None:
+        per_channel = alpha.ndim == 3
+    if o is None:
+        o = np.zeros((B, Hv, dv), np.float32)
+    lo, hi = items if items is not None else (0, B * Hv)
+    st = lib().orc_decode_f32(B, Hk, Hv, dk, dv, int(per_channel), _ptr(pool), n_slots,
+                              _ptr(_c(slot_idx, np.int32)), _ptr(_c(q, np.float32)),
+                              _ptr(_c(k, np.float32)), _ptr(_c(v, np.float32)),
+                              _ptr(_c(alpha, np.float32)), _ptr(_c(beta, np.float32)),
+                              _ptr(_c(o, np.float32)), lo, hi)
+    return o, st
+
+
+def decode_mixed(pool, slot_idx, pi, khi, dk, dv, q, k, v, alpha, beta, o=None,
+                 per_channel=None, items=None):
+    """Batched mixed-layout decode in place on ``pool`` [n_slots][Hv][tile_bytes]."""
+    _c(pool, np.uint8)
+    n_slots, Hv, tb = pool.shape
+    assert tb == mixed_tile_bytes(dk, dv, khi)
+    B, Hk, _ = q.shape
+    if per_channel is None:
+        per_channel = alpha.ndim == 3
+    if o is None:
+        o = np.zeros((B, Hv, dv), np.float32)
+    lo, hi = items if items is not None else (0, B * Hv)
+    st = lib().orc_decode_mixed(B, Hk, Hv, dk, dv, khi, int(per_channel), _ptr(pool),
+                                n_slots, _ptr(_c(slot_idx, np.int32)),
+                                _ptr(_c(pi, np.int16)), _ptr(_c(q, np.float32)),
+                                _ptr(_c(k, np.float32)), _ptr(_c(v, np.float32)),
+                                _ptr(_c(alpha, np.float32)), _ptr(_c(beta, np.float32)),
+                                _ptr(_c(o, np.float32)), lo, hi)
+    return o, st
+
+
+def replay_f32(pool, slot_idx, n_accept, q, k, v, alpha, beta, o=None,
+               per_channel=None, items=None):
+    """Spec replay on the FP32 pool. Inputs are [B][T_max][...]."""
+    _c(pool, np.float32)
+    n_slots, Hv, dk, dv = pool.shape
+    B, T_max, Hk, _ = q.shape
+    if per_channel is None:
+        per_channel = alpha.ndim == 4
+    if o is None:
+        o = np.zeros((B, T_max, Hv, dv), np.float32)
+    lo, hi = items if items is not None else (0, B * Hv)
+    st = lib().orc_replay_f32(B, T_max, Hk, Hv, dk, dv, int(per_channel), _ptr(pool),
+                              n_slots, _ptr(_c(slot_idx, np.int32)),
+                              _ptr(_c(n_accept, np.int32)), _ptr(_c(q, np.float32)),
+                              _ptr(_c(k, np.float32)), _ptr(_c(v, np.float32)),
+                              _ptr(_c(alpha, np.float32)), _ptr(_c(beta, np.float32)),
+                              _ptr(_c(o, np.float32)), lo, hi)
+    return o, st
+
+
+def replay_mixed(pool, slot_idx, n_accept, pi, khi, dk, dv, q, k, v, alpha, beta,
+                 o=None, per_channel=None, items=None):
+    _c(pool, np.uint8)
+    n_slots, Hv, tb = pool.shape
+    assert tb == mixed_tile_bytes(dk, dv, khi)
+    B, T_max, Hk, _ = q.shape
+    if per_channel is None:
+        per_channel = alpha.ndim == 4
+    if o is None:
+        o = np.zeros((B, T_max, Hv, dv), np.float32)
+    lo, hi = items if items is not None else (0, B * Hv)
+    st = lib().orc_replay_mixed(B, T_max, Hk, Hv, dk, dv, khi, int(per_channel),
+                                _ptr(pool), n_slots, _ptr(_c(slot_idx, np.int32)),
+                                _ptr(_c(n_accept, np.int32)), _ptr(_c(pi, np.int16)),
+                                _ptr(_c(q, np.float32)), _ptr(_c(k, np.float32)),
+                                _ptr(_c(v, np.float32)), _ptr(_c(alpha, np.float32)),
+                                _ptr(_c(beta, np.float32)), _ptr(_c(o, np.float32)), lo, hi)
+    return o, st
+
+
+def plan_offsets(keep, Hv, dk, unit):
+    """o_0..o_L for keep [L][n_units] (uint8)."""
+    keep = _c(np.ascontiguousarray(keep, np.uint8), np.uint8)
+    L = keep.shape[0]
+    off = np.zeros(L + 1, np.int64)
+    lib().orc_plan_offsets(L, Hv, dk, unit, _ptr(keep), _ptr(off))
+    return off
+
+
+def ckpt_pack(keep, unit, pool, src_slots, dst_slots, ckpt):
+    """pool: [L][n_slots][Hv][dk][dv] float32; ckpt: [n_ckpt][total_units*unit_bytes] uint8."""
+    keep = _c(np.ascontiguousarray(keep, np.uint8), np.uint8)
+    L, n_slots, Hv, dk, dv = pool.shape
+    st = lib().orc_ckpt_pack(L, Hv, dk, dv, unit, _ptr(keep), _ptr(_c(pool, np.float32)),
+                             pool.strides[0], n_slots, _ptr(_c(src_slots, np.int32)),
+                             _ptr(_c(dst_slots, np.int32)), len(src_slots),
+                             _ptr(_c(ckpt, np.uint8)), ckpt.shape[0])
+    return st
+
+
+def ckpt_restore(keep, unit, ckpt, src_slots, pool, dst_slots):
+    keep = _c(np.ascontiguousarray(keep, np.uint8), np.uint8)
+    L, n_slots, Hv, dk, dv = pool.shape
+    st = lib().orc_ckpt_restore(L, Hv, dk, dv, unit, _ptr(keep), _ptr(_c(ckpt, np.uint8)),
+                                ckpt.shape[0], _ptr(_c(src_slots, np.int32)),
+                                _ptr(_c(pool, np.float32)), pool.strides[0], n_slots,
+                                _ptr(_c(dst_slots, np.int32)), len(src_slots))
+    return st

@@ -1,0 +1,473 @@
+/*
+ * rs_oracle.c -- plain, slow CPU oracle for the recurrent-state hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or calls
+ * this file: only the tests, the smoke check and the benchmark's CPU-baseline
+ * leg do.  It shares no code, header, table or helper with the CUDA library.
+ *
+ * Sources (pages, cited by title and section):
+ *   [dasc] "dasc: Decay-Aware State Compression for Hybrid Linear-Attention
+ *          Serving" (arXiv 2608.30386).
+ *   [DAMP] "DAMP: Decay-Aware Mixed-Precision Recurrent-State Quantization"
+ *          (arXiv 2608.27513).
+ *   [SRA]  "Serving recurrent attention" (Kimi K3 explainer, section 22).
+ *
+ * Arithmetic: IEEE binary32, round to nearest even, no flush to zero, built
+ * with -ffp-contract=off so that every '*' and '+' rounds on its own.  Where a
+ * fused multiply-add is meant it is written as fmaf() (correctly rounded by
+ * the C library), so the order and the roundings of every result below are
+ * fixed by this source alone.
+ *
+ * Orientation ([DAMP] §3.1): per head the state S has dk rows (key channels)
+ * of dv values each, row-major, S[u*dv + v].  One decode step is
+ *     S <- diag(a) S;   p = S^T k;   e = v - p;   S <- S + beta k e^T;
+ *     o = S^T q  (read from the updated state, [DAMP] §3.1 Eq. 1).
+ * Expanding [DAMP] §3.1 Eq. 2, (I - beta k k^T) Lambda S + beta k v^T, gives
+ * exactly these lines; [dasc] §3.1 Eq. 1 is the same map on S^T.
+ *
+ * Reading fixed here (the pages leave the floating-point order open):
+ *   - the decay is one multiply per element, S[u][v] * a[u];
+ *   - both reductions over u run in ascending u, starting from +0.0f, each
+ *     term accumulated with one fused multiply-add, p = fmaf(S[u][v], k[u], p);
+ *   - the rank-1 write is S[u][v] = fmaf(beta*k[u], e[v], S[u][v]) with the
+ *     product beta*k[u] rounded first.
+ *
+ * Status bits returned by the batched entry points (same meaning as the
+ * device status word of the library, defined independently here):
+ *   1 = a slot index out of range (that item is skipped),
+ *   2 = an accepted-token count out of range (that item is skipped),
+ *   4 = a checkpoint slot out of range (that item is skipped).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stddef.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_MAX_D 256
+
+/* ------------------------------------------------------------------------ */
+/* One decode step on one state tile (rows in the order given).             */
+/* a_stride = 0 gives one decay for the whole head (GDN, [DAMP] §3.1:        */
+/* Lambda = alpha I); a_stride = 1 gives one decay per key channel (KDA,     */
+/* Lambda = diag(exp g)).  o may be NULL.                                    */
+/* ------------------------------------------------------------------------ */
+void orc_step_tile_f32(int dk, int dv, float *S, const float *q, const float *k,
+                       const float *v, const float *a, int a_stride, float beta,
+                       float *o)
+{
+    float e[ORC_MAX_D];
+    int u, c;
+
+    /* S <- diag(a) S */
+    for (u = 0; u < dk; ++u) {
+        float au = a[(size_t)u * (size_t)a_stride];
+        for (c = 0; c < dv; ++c)
+            S[(size_t)u * dv + c] = S[(size_t)u * dv + c] * au;
+    }
+    /* prediction p = S^T k, error e = v - p */
+    for (c = 0; c < dv; ++c) {
+        float p = 0.0f;
+        for (u = 0; u < dk; ++u)
+            p = fmaf(S[(size_t)u * dv + c], k[u], p);
+        e[c] = v[c] - p;
+    }
+    /* rank-1 delta-rule write S <- S + beta k e^T */
+    for (u = 0; u < dk; ++u) {
+        float bk = beta * k[u];
+        for (c = 0; c < dv; ++c)
+            S[(size_t)u * dv + c] = fmaf(bk, e[c], S[(size_t)u * dv + c]);
+    }
+    /* readout o = S^T q on the updated state */
+    if (o) {
+        for (c = 0; c < dv; ++c) {
+            float acc = 0.0f;
+            for (u = 0; u < dk; ++u)
+                acc = fmaf(S[(size_t)u * dv + c], q[u], acc);
+            o[c] = acc;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Symmetric INT8 row quantiser ([DAMP] §3.2 Eq. 5-6 with b = 8, "x a row of */
+/* S"; floor, clip and FP32 arithmetic as in [dasc] Appendix E.1 Eq. 8).     */
+/*   a = max_v |x_v|            (a NaN anywhere makes a NaN)                 */
+/*   s = max(a, 1e-8) / 127     (fmaxf: a NaN a gives the floor)             */
+/*   c_v = clip(round_half_even(x_v / s), -127, 127)                        */
+/* Dequantised value: c * s, one FP32 multiply.                              */
+/* ------------------------------------------------------------------------ */
+float orc_row_scale(int n, const float *x)
+{
+    float a = 0.0f;
+    int i;
+    for (i = 0; i < n; ++i) {
+        float ax = fabsf(x[i]);
+        if (isnan(ax) || ax > a)
+            a = ax;
+    }
+    return fmaxf(a, 1e-8f) / 127.0f;
+}
+
+int8_t orc_quant_code(float x, float s)
+{
+    float r = rintf(x / s);          /* default rounding: half to even */
+    r = fminf(fmaxf(r, -127.0f), 127.0f);
+    return (int8_t)r;
+}
+
+void orc_quantise_row(int n, const float *x, int8_t *codes, float *scale)
+{
+    float s = orc_row_scale(n, x);
+    int i;
+    for (i = 0; i < n; ++i)
+        codes[i] = orc_quant_code(x[i], s);
+    *scale = s;
+}
+
+void orc_dequantise_row(int n, const int8_t *codes, float s, float *x)
+{
+    int i;
+    for (i = 0; i < n; ++i)
+        x[i] = (float)codes[i] * s;
+}
+
+/* FP16 storage of a high-precision row: round to nearest even, overflow to
+ * infinity (IEEE binary16 through the compiler's _Float16). */
+static uint16_t f32_to_f16_bits(float x)
+{
+    _Float16 h = (_Float16)x;
+    uint16_t b;
+    memcpy(&b, &h, 2);
+    return b;
+}
+
+static float f16_bits_to_f32(uint16_t b)
+{
+    _Float16 h;
+    memcpy(&h, &b, 2);
+    return (float)h;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Mixed-precision head tile ([DAMP] §5.2 and Appendix A.4, with one scale   */
+/* per INT8 row as in [DAMP] §3.2):                                          */
+/*   bytes [0, 2*khi*dv)              : rows 0..khi-1 as FP16                */
+/*   bytes [.., + (dk-khi)*dv)        : rows khi..dk-1 as INT8 codes         */
+/*   bytes [.., + 4*(dk-khi))         : one FP32 scale per INT8 row          */
+/* Rows are physical rows of the permuted state T = P_K S ([DAMP] Appendix   */
+/* A.3 Eq. 17, value scaling and value reordering not applied).              */
+/* ------------------------------------------------------------------------ */
+size_t orc_mixed_tile_bytes(int dk, int dv, int khi)
+{
+    return (size_t)2 * khi * dv + (size_t)(dk - khi) * dv + (size_t)4 * (dk - khi);
+}
+
+void orc_mixed_unpack(int dk, int dv, int khi, const uint8_t *tile, float *T)
+{
+    const uint8_t *hi = tile;
+    const int8_t *lo = (const int8_t *)(tile + (size_t)2 * khi * dv);
+    const uint8_t *sc = tile + (size_t)2 * khi * dv + (size_t)(dk - khi) * dv;
+    int r, c;
+    for (r = 0; r < khi; ++r)
+        for (c = 0; c < dv; ++c) {
+            uint16_t b;
+            memcpy(&b, hi + ((size_t)r * dv + c) * 2, 2);
+            T[(size_t)r * dv + c] = f16_bits_to_f32(b);
+        }
+    for (r = khi; r < dk; ++r) {
+        float s;
+        memcpy(&s, sc + (size_t)(r - khi) * 4, 4);
+        orc_dequantise_row(dv, lo + (size_t)(r - khi) * dv, s, T + (size_t)r * dv);
+    }
+}
+
+void orc_mixed_pack(int dk, int dv, int khi, const float *T, uint8_t *tile)
+{
+    uint8_t *hi = tile;
+    int8_t *lo = (int8_t *)(tile + (size_t)2 * khi * dv);
+    uint8_t *sc = tile + (size_t)2 * khi * dv + (size_t)(dk - khi) * dv;
+    int r, c;
+    for (r = 0; r < khi; ++r)
+        for (c = 0; c < dv; ++c) {
+            uint16_t b = f32_to_f16_bits(T[(size_t)r * dv + c]);
+            memcpy(hi + ((size_t)r * dv + c) * 2, &b, 2);
+        }
+    for (r = khi; r < dk; ++r) {
+        float s;
+        orc_quantise_row(dv, T + (size_t)r * dv, lo + (size_t)(r - khi) * dv, &s);
+        memcpy(sc + (size_t)(r - khi) * 4, &s, 4);
+    }
+}
+
+/* Logical FP32 head S (rows = key channels) <-> mixed tile with row map pi:
+ * physical row r holds logical channel pi[r] ([DAMP] Appendix A.2, last step
+ * of Algorithm 1; Appendix A.3 Eq. 17). */
+int orc_convert_f32_to_mixed(int dk, int dv, int khi, const int16_t *pi,
+                             const float *S, uint8_t *tile)
+{
+    float *T = (float *)malloc((size_t)dk * dv * 4);
+    int r;
+    if (!T) return -1;
+    for (r = 0; r < dk; ++r)
+        memcpy(T + (size_t)r * dv, S + (size_t)pi[r] * dv, (size_t)dv * 4);
+    orc_mixed_pack(dk, dv, khi, T, tile);
+    free(T);
+    return 0;
+}
+
+int orc_convert_mixed_to_f32(int dk, int dv, int khi, const int16_t *pi,
+                             const uint8_t *tile, float *S)
+{
+    float *T = (float *)malloc((size_t)dk * dv * 4);
+    int r;
+    if (!T) return -1;
+    orc_mixed_unpack(dk, dv, khi, tile, T);
+    for (r = 0; r < dk; ++r)
+        memcpy(S + (size_t)pi[r] * dv, T + (size_t)r * dv, (size_t)dv * 4);
+    free(T);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Batched decode over a pool.                                               */
+/* Pool (one layer): [n_slots][Hv][head_bytes]; item = b*Hv + h, b < B.      */
+/* Value head h reads q, k of key head g = h / (Hv/Hk): the Hv/Hk adjacent   */
+/* value heads share one key head ([dasc] Appendix B.1).                     */
+/* q, k: [B][Hk][dk] f32; v: [B][Hv][dv]; alpha: [B][Hv] (per_channel = 0)   */
+/* or [B][Hv][dk] (per_channel = 1); beta: [B][Hv]; o: [B][Hv][dv] or NULL.  */
+/* Items [item_begin, item_end) are processed, so callers may split work.   */
+/* ------------------------------------------------------------------------ */
+static int key_head(int h, int Hk, int Hv) { return h / (Hv / Hk); }
+
+int orc_decode_f32(int B, int Hk, int Hv, int dk, int dv, int per_channel,
+                   float *pool, int n_slots, const int32_t *slot_idx,
+                   const float *q, const float *k, const float *v,
+                   const float *alpha, const float *beta, float *o,
+                   int item_begin, int item_end)
+{
+    int status = 0, it;
+    (void)B;
+    for (it = item_begin; it < item_end; ++it) {
+        int b = it / Hv, h = it % Hv, g = key_head(h, Hk, Hv);
+        int32_t slot = slot_idx[b];
+        float *S;
+        const float *a;
+        if (slot < 0 || slot >= n_slots) { status |= 1; continue; }
+        S = pool + ((size_t)slot * Hv + h) * (size_t)dk * dv;
+        a = per_channel ? alpha + ((size_t)b * Hv + h) * dk : alpha + (size_t)b * Hv + h;
+        orc_step_tile_f32(dk, dv, S,
+                          q + ((size_t)b * Hk + g) * dk, k + ((size_t)b * Hk + g) * dk,
+                          v + ((size_t)b * Hv + h) * dv, a, per_channel ? 1 : 0,
+                          beta[(size_t)b * Hv + h],
+                          o ? o + ((size_t)b * Hv + h) * dv : NULL);
+    }
+    return status;
+}
+
+/* Mixed-layout decode: dequantise once, one FP32 step in the permuted
+ * coordinates of [DAMP] Appendix A.3 Eq. 18 (inputs gathered by pi, the sums
+ * over physical rows in ascending row order), requantise once and write back
+ * ([DAMP] Appendix A.4 "Fused decoding").  pi: [Hv][dk]. */
+int orc_decode_mixed(int B, int Hk, int Hv, int dk, int dv, int khi, int per_channel,
+                     uint8_t *pool, int n_slots, const int32_t *slot_idx,
+                     const int16_t *pi, const float *q, const float *k, const float *v,
+                     const float *alpha, const float *beta, float *o,
+                     int item_begin, int item_end)
+{
+    float *T = (float *)malloc((size_t)dk * dv * 4);
+    float qp[ORC_MAX_D], kp[ORC_MAX_D], ap[ORC_MAX_D];
+    size_t tb = orc_mixed_tile_bytes(dk, dv, khi);
+    int status = 0, it, r;
+    (void)B;
+    if (!T) return -1;
+    for (it = item_begin; it < item_end; ++it) {
+        int b = it / Hv, h = it % Hv, g = key_head(h, Hk, Hv);
+        int32_t slot = slot_idx[b];
+        const int16_t *ph = pi + (size_t)h * dk;
+        const float *qh = q + ((size_t)b * Hk + g) * dk, *kh = k + ((size_t)b * Hk + g) * dk;
+        uint8_t *tile;
+        if (slot < 0 || slot >= n_slots) { status |= 1; continue; }
+        tile = pool + ((size_t)slot * Hv + h) * tb;
+        for (r = 0; r < dk; ++r) {
+            qp[r] = qh[ph[r]];
+            kp[r] = kh[ph[r]];
+            ap[r] = per_channel ? alpha[((size_t)b * Hv + h) * dk + ph[r]]
+                                : alpha[(size_t)b * Hv + h];
+        }
+        orc_mixed_unpack(dk, dv, khi, tile, T);
+        orc_step_tile_f32(dk, dv, T, qp, kp, v + ((size_t)b * Hv + h) * dv, ap, 1,
+                          beta[(size_t)b * Hv + h],
+                          o ? o + ((size_t)b * Hv + h) * dv : NULL);
+        orc_mixed_pack(dk, dv, khi, T, tile);
+    }
+    free(T);
+    return status;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Speculative-token replay ([SRA] "Speculative decoding without state       */
+/* snapshots"): the inputs of T_max logged draft tokens are kept; for each   */
+/* sequence the first n_accept[b] of them are replayed on the state, which   */
+/* is loaded (and dequantised) once and stored (and requantised) once.       */
+/* Inputs are [B][T_max][...] versions of the decode inputs; o is            */
+/* [B][T_max][Hv][dv] or NULL, rows t >= n_accept[b] are not written.        */
+/* ------------------------------------------------------------------------ */
+int orc_replay_f32(int B, int T_max, int Hk, int Hv, int dk, int dv, int per_channel,
+                   float *pool, int n_slots, const int32_t *slot_idx, const int32_t *n_accept,
+                   const float *q, const float *k, const float *v,
+                   const float *alpha, const float *beta, float *o,
+                   int item_begin, int item_end)
+{
+    int status = 0, it, t;
+    (void)B;
+    for (it = item_begin; it < item_end; ++it) {
+        int b = it / Hv, h = it % Hv, g = key_head(h, Hk, Hv);
+        int32_t slot = slot_idx[b], n = n_accept[b];
+        float *S;
+        if (slot < 0 || slot >= n_slots) { status |= 1; continue; }
+        if (n < 0 || n > T_max) { status |= 2; continue; }
+        S = pool + ((size_t)slot * Hv + h) * (size_t)dk * dv;
+        for (t = 0; t < n; ++t) {
+            size_t bt = (size_t)b * T_max + t;
+            const float *a = per_channel ? alpha + (bt * Hv + h) * dk : alpha + bt * Hv + h;
+            orc_step_tile_f32(dk, dv, S, q + (bt * Hk + g) * dk, k + (bt * Hk + g) * dk,
+                              v + (bt * Hv + h) * dv, a, per_channel ? 1 : 0,
+                              beta[bt * Hv + h], o ? o + (bt * Hv + h) * dv : NULL);
+        }
+    }
+    return status;
+}
+
+int orc_replay_mixed(int B, int T_max, int Hk, int Hv, int dk, int dv, int khi, int per_channel,
+                     uint8_t *pool, int n_slots, const int32_t *slot_idx, const int32_t *n_accept,
+                     const int16_t *pi, const float *q, const float *k, const float *v,
+                     const float *alpha, const float *beta, float *o,
+                     int item_begin, int item_end)
+{
+    float *T = (float *)malloc((size_t)dk * dv * 4);
+    float qp[ORC_MAX_D], kp[ORC_MAX_D], ap[ORC_MAX_D];
+    size_t tb = orc_mixed_tile_bytes(dk, dv, khi);
+    int status = 0, it, t, r;
+    (void)B;
+    if (!T) return -1;
+    for (it = item_begin; it < item_end; ++it) {
+        int b = it / Hv, h = it % Hv, g = key_head(h, Hk, Hv);
+        int32_t slot = slot_idx[b], n = n_accept[b];
+        const int16_t *ph = pi + (size_t)h * dk;
+        uint8_t *tile;
+        if (slot < 0 || slot >= n_slots) { status |= 1; continue; }
+        if (n < 0 || n > T_max) { status |= 2; continue; }
+        if (n == 0) continue;            /* nothing accepted: state untouched */
+        tile = pool + ((size_t)slot * Hv + h) * tb;
+        orc_mixed_unpack(dk, dv, khi, tile, T);
+        for (t = 0; t < n; ++t) {
+            size_t bt = (size_t)b * T_max + t;
+            const float *qh = q + (bt * Hk + g) * dk, *kh = k + (bt * Hk + g) * dk;
+            for (r = 0; r < dk; ++r) {
+                qp[r] = qh[ph[r]];
+                kp[r] = kh[ph[r]];
+                ap[r] = per_channel ? alpha[(bt * Hv + h) * dk + ph[r]] : alpha[bt * Hv + h];
+            }
+            orc_step_tile_f32(dk, dv, T, qp, kp, v + (bt * Hv + h) * dv, ap, 1,
+                              beta[bt * Hv + h], o ? o + (bt * Hv + h) * dv : NULL);
+        }
+        orc_mixed_pack(dk, dv, khi, T, tile);
+    }
+    free(T);
+    return status;
+}
+
+/* ------------------------------------------------------------------------ */
+/* dasc checkpoints ([dasc] §4.1 and Appendix B "Ragged (Scheme 2)").        */
+/* A unit is one head (GDN, unit = 0) or one (head, key channel) row of dv   */
+/* values (KDA, unit = 1) of the FP32 state.  keep: [L][n_units] of 0/1.     */
+/* r_l = retained units of layer l; offsets o_0 = 0, o_l = o_{l-1} + r_l;    */
+/* layer l's units occupy packed positions [o_{l-1}, o_l), in ascending unit */
+/* order.  Pool: [L][slots][Hv][dk*dv*4] with layer stride layer_stride      */
+/* bytes; checkpoint pool: [ckpt_slots][o_L][unit_bytes].                    */
+/* ------------------------------------------------------------------------ */
+static size_t unit_bytes_of(int unit, int dk, int dv)
+{
+    return unit ? (size_t)dv * 4 : (size_t)dk * dv * 4;
+}
+
+static int units_per_layer(int unit, int Hv, int dk)
+{
+    return unit ? Hv * dk : Hv;
+}
+
+/* offsets[0..L]: o_0 = 0, o_l = o_{l-1} + r_l */
+void orc_plan_offsets(int L, int Hv, int dk, int unit, const uint8_t *keep, int64_t *offsets)
+{
+    int n = units_per_layer(unit, Hv, dk), l, x;
+    offsets[0] = 0;
+    for (l = 1; l <= L; ++l) {
+        int64_t r = 0;
+        for (x = 0; x < n; ++x)
+            r += keep[(size_t)(l - 1) * n + x] ? 1 : 0;
+        offsets[l] = offsets[l - 1] + r;
+    }
+}
+
+int orc_ckpt_pack(int L, int Hv, int dk, int dv, int unit, const uint8_t *keep,
+                  const uint8_t *pool, int64_t layer_stride, int n_pool_slots,
+                  const int32_t *src_slots, const int32_t *dst_ckpt_slots, int n,
+                  uint8_t *ckpt, int n_ckpt_slots)
+{
+    int64_t off[1025];
+    int nu = units_per_layer(unit, Hv, dk), i, l, x;
+    size_t ub = unit_bytes_of(unit, dk, dv), slot_bytes = (size_t)Hv * dk * dv * 4;
+    int status = 0;
+    if (L > 1024) return -1;
+    orc_plan_offsets(L, Hv, dk, unit, keep, off);
+    for (i = 0; i < n; ++i) {
+        int32_t s = src_slots[i], d = dst_ckpt_slots[i];
+        if (s < 0 || s >= n_pool_slots) { status |= 1; continue; }
+        if (d < 0 || d >= n_ckpt_slots) { status |= 4; continue; }
+        for (l = 0; l < L; ++l) {
+            int64_t j = 0;
+            for (x = 0; x < nu; ++x) {
+                if (!keep[(size_t)l * nu + x]) continue;
+                memcpy(ckpt + ((size_t)d * off[L] + (size_t)(off[l] + j)) * ub,
+                       pool + (size_t)l * layer_stride + (size_t)s * slot_bytes + (size_t)x * ub,
+                       ub);
+                ++j;
+            }
+        }
+    }
+    return status;
+}
+
+/* dasc-nr restore ([dasc] §4.2): retained units are loaded exactly, omitted
+ * units are left at zero (+0.0, all bytes 0x00). */
+int orc_ckpt_restore(int L, int Hv, int dk, int dv, int unit, const uint8_t *keep,
+                     const uint8_t *ckpt, int n_ckpt_slots, const int32_t *src_ckpt_slots,
+                     uint8_t *pool, int64_t layer_stride, int n_pool_slots,
+                     const int32_t *dst_slots, int n)
+{
+    int64_t off[1025];
+    int nu = units_per_layer(unit, Hv, dk), i, l, x;
+    size_t ub = unit_bytes_of(unit, dk, dv), slot_bytes = (size_t)Hv * dk * dv * 4;
+    int status = 0;
+    if (L > 1024) return -1;
+    orc_plan_offsets(L, Hv, dk, unit, keep, off);
+    for (i = 0; i < n; ++i) {
+        int32_t s = src_ckpt_slots[i], d = dst_slots[i];
+        if (s < 0 || s >= n_ckpt_slots) { status |= 4; continue; }
+        if (d < 0 || d >= n_pool_slots) { status |= 1; continue; }
+        for (l = 0; l < L; ++l) {
+            int64_t j = 0;
+            for (x = 0; x < nu; ++x) {
+                uint8_t *dst = pool + (size_t)l * layer_stride + (size_t)d * slot_bytes + (size_t)x * ub;
+                if (keep[(size_t)l * nu + x]) {
+                    memcpy(dst, ckpt + ((size_t)s * off[L] + (size_t)(off[l] + j)) * ub, ub);
+                    ++j;
+                } else {
+                    memset(dst, 0, ub);
+                }
+            }
+        }
+    }
+    return status;
+}
