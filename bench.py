@@ -1,0 +1,505 @@
+#!/usr/bin/env python
+"""Benchmark of the recurrent-state decode step on GB300.
+
+Headline workload (one "step" = one batched decode step = 8,192 state
+updates): GDN, batch 256, 16 q/k heads shared by 32 value heads, dk = dv =
+128, FP32 states, bf16 q/k/v, per-token per-head decay, 64 consecutive
+steps of synthetic inputs cycled.  Metric: state updates per second (whole
+job, all ranks) and the decode kernel's achieved HBM bandwidth against the
+measured copy bandwidth.
+
+Also reported, each on its own workload: the KDA FP32 step, the KDA mixed
+FP16/INT8 step, mixed-layout speculative replay (1..8 accepted tokens), and
+dasc checkpoint pack / restore (36 layers x 64 checkpoints).
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+N > 1 runs under torch.distributed.run, one rank per GPU, each rank an
+independent replica (the decode path shards by sequence with no exchange).
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures as cf
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from recurrent_state_gb300 import inputs as gen  # noqa: E402
+
+METRIC = "state-updates/sec and achieved HBM GB/s (% of GB300 peak) at batch 256"
+UNIT = "state-updates/s"
+GDN = dict(B=256, Hk=16, Hv=32, d=128)
+KDA = dict(B=256, Hk=32, Hv=32, d=128)
+BENCH_STEPS_DATA = 64   # distinct input steps, cycled
+
+
+# --------------------------------------------------------------------------
+# algorithmic bytes (what the step must move at minimum)
+# --------------------------------------------------------------------------
+def decode_bytes(B, Hk, Hv, d, head_bytes, in_size, per_channel, o_size=4, tokens=1):
+    state = 2 * B * Hv * head_bytes
+    qk = 2 * B * Hk * d * in_size * tokens
+    v = B * Hv * d * in_size * tokens
+    alpha = B * Hv * (d if per_channel else 1) * 4 * tokens
+    beta = B * Hv * 4 * tokens
+    o = B * Hv * d * o_size * tokens
+    return state + qk + v + alpha + beta + o
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_sources_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "recurrent_state_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_key):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(kernel_key)
+    if not e or e.get("sources") != kernel_sources_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# --------------------------------------------------------------------------
+# clocks sampled during the timed region
+# --------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,utilization.gpu,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            self.path = f"/tmp/rs_clocks_{os.getpid()}.csv"
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        rows = []
+        if self.path and os.path.exists(self.path):
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        loaded = [r for r in rows if (num(r[3]) or 0) > 0] or rows
+        sm = [num(r[1]) for r in loaded if num(r[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in loaded for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": num(rows[0][2]), "reasons": reasons, "samples": len(loaded)}
+
+
+# --------------------------------------------------------------------------
+# the oracle as CPU baseline (host cores, bounded sample)
+# --------------------------------------------------------------------------
+class OracleSample:
+    """The oracle's GDN decode step on host threads over a bounded sample of
+    the B=256 workload's (sequence, head) items."""
+
+    def __init__(self):
+        import oracle as orc
+        self.orc = orc
+        self.w = gen.decode_workload(steps=1, per_channel=False, in_dtype="bf16", seed=0, **GDN)
+        self.items = GDN["B"] * GDN["Hv"]
+        self.pool = self.w.state0.copy()
+        self.o = np.zeros((GDN["B"], GDN["Hv"], GDN["d"]), np.float32)
+        self.threads = os.cpu_count() or 1
+        w = self.w
+        self.args = (w.q[0], w.k[0], w.v[0], w.alpha[0], w.beta[0])
+        t0 = time.perf_counter()
+        orc.decode_f32(self.pool, w.slot_idx, *self.args, items=(0, 16))
+        self.per_item = (time.perf_counter() - t0) / 16
+
+    def size_for(self, seconds):
+        n = int(seconds * self.threads / max(self.per_item, 1e-9))
+        return int(min(self.items, max(self.threads, n)))
+
+    def run(self, n_items):
+        bounds = np.linspace(0, n_items, self.threads + 1).astype(int)
+
+        def work(i):
+            self.orc.decode_f32(self.pool, self.w.slot_idx, *self.args, o=self.o,
+                                items=(int(bounds[i]), int(bounds[i + 1])))
+        t0 = time.perf_counter()
+        with cf.ThreadPoolExecutor(max_workers=self.threads) as ex:
+            list(ex.map(work, range(self.threads)))
+        return time.perf_counter() - t0
+
+    def describe(self, n_items):
+        return (f"{n_items} of the {self.items} (sequence, head) state updates of one GDN decode "
+                f"step (B=256, Hv=32, d=128), split over {self.threads} threads")
+
+
+def cpu_baseline(target_seconds=12.0):
+    s = OracleSample()
+    n = s.size_for(target_seconds)
+    dt = s.run(n)
+    return {"value": n / dt, "unit": UNIT, "cores": s.threads, "kind": "oracle",
+            "sample": s.describe(n), "seconds": dt}
+
+
+# --------------------------------------------------------------------------
+# GPU measurement
+# --------------------------------------------------------------------------
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import recurrent_state_gb300 as rs
+    from recurrent_state_gb300 import build as rsbuild
+
+    if rank == 0 or not os.path.exists(rsbuild.LIB_PATH):
+        rsbuild.build()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream()
+    peak, peak_kind = measured_peaks()
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    def to_bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    # ---------------- headline: GDN decode, FP32 state --------------------
+    w = gen.decode_workload(steps=BENCH_STEPS_DATA, per_channel=False, in_dtype="bf16",
+                            seed=rank, **GDN)
+    lay = rs.Layout("fp32", GDN["d"], GDN["Hv"], GDN["Hk"])
+    pool = to_dev(w.state0)
+    slots = to_dev(w.slot_idx)
+    q, k, v = to_bf16(w.q_bits), to_bf16(w.k_bits), to_bf16(w.v_bits)
+    al, be = to_dev(w.alpha), to_dev(w.beta)
+    o = torch.empty((GDN["B"], GDN["Hv"], GDN["d"]), device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step(i):
+        t = i % BENCH_STEPS_DATA
+        rs.gdn_decode_update(lay, pool, slots, q[t], k[t], v[t], al[t], be[t], o=o, status=status)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clk:
+        _barrier(world)
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(args.warmup + i)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        _barrier(world)
+    dt = ev0.elapsed_time(ev1) / 1e3
+    dt_max = _max_over_ranks(dt, world)
+    assert int(status.item()) == 0
+    updates = GDN["B"] * GDN["Hv"]
+    alg = decode_bytes(GDN["B"], GDN["Hk"], GDN["Hv"], GDN["d"], lay.head_bytes, 2, False)
+    per_launch = dt / args.steps
+    achieved = alg / per_launch / 1e9
+
+    # ---------------- e2e: host buffers through the C ABI ----------------
+    qh = torch.from_numpy(w.q_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    kh = torch.from_numpy(w.k_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    vh = torch.from_numpy(w.v_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    ah = torch.from_numpy(w.alpha).pin_memory()
+    bh = torch.from_numpy(w.beta).pin_memory()
+    oh = torch.empty((GDN["B"], GDN["Hv"], GDN["d"]), dtype=torch.float32).pin_memory()
+    qs, ks, vs = torch.empty_like(q[0]), torch.empty_like(k[0]), torch.empty_like(v[0])
+    as_, bs = torch.empty_like(al[0]), torch.empty_like(be[0])
+
+    def e2e_step(i):
+        t = i % BENCH_STEPS_DATA
+        qs.copy_(qh[t], non_blocking=True)
+        ks.copy_(kh[t], non_blocking=True)
+        vs.copy_(vh[t], non_blocking=True)
+        as_.copy_(ah[t], non_blocking=True)
+        bs.copy_(bh[t], non_blocking=True)
+        rs.gdn_decode_update(lay, pool, slots, qs, ks, vs, as_, bs, o=o)
+        oh.copy_(o, non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    _barrier(world)
+    ev0.record(stream)
+    for i in range(args.steps):
+        e2e_step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    e2e_dt = _max_over_ranks(ev0.elapsed_time(ev1) / 1e3, world)
+    h2d = (qs.numel() + ks.numel() + vs.numel()) * 2 + (as_.numel() + bs.numel()) * 4
+    d2h = o.numel() * 4
+
+    result = {
+        "metric": METRIC, "value": world * args.steps * updates / dt_max, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt_max / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "GDN decode step, B=256, Hk=16, Hv=32, dk=dv=128, FP32 state, "
+                               "bf16 q/k/v, 64 input steps cycled",
+                   "global_batch": GDN["B"] * world, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (512 MiB state pool per rank)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "traffic": profiled_traffic("step_gdn_f32_b256"),
+                     "algorithmic_bytes_per_launch": alg,
+                     "kernel": "rs::step_kernel<128, FP32, GDN>"},
+        "e2e": {"value": world * args.steps * updates / e2e_dt, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
+    del pool, q, k, v, al, be
+    torch.cuda.empty_cache()
+    if not args.skip_extra:
+        result["kernels"] = extra_kernels(args, rs, torch, dev, peak, world)
+    if rank == 0 and not args.no_cpu:
+        result["cpu_baseline"] = cpu_baseline()
+    return result
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _time(torch, fn, iters, warm=3):
+    for i in range(warm):
+        fn(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(iters):
+        fn(warm + i)
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / 1e3 / iters
+
+
+def extra_kernels(args, rs, torch, dev, peak, world):
+    """The other hot-path kernels, each timed alone on its own workload."""
+    out = {}
+    iters = max(10, min(args.steps, 200))
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    def to_bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    nsteps = 8
+    w = gen.decode_workload(steps=nsteps, per_channel=True, in_dtype="bf16", seed=1,
+                            horizon=(2.0, 8192.0), **KDA)
+    q, k, v = to_bf16(w.q_bits), to_bf16(w.k_bits), to_bf16(w.v_bits)
+    al, be = to_dev(w.alpha), to_dev(w.beta)
+    slots = to_dev(w.slot_idx)
+    o = torch.empty((KDA["B"], KDA["Hv"], KDA["d"]), device=dev)
+    f32 = rs.Layout("fp32", 128, KDA["Hv"], KDA["Hk"])
+    hi = gen.hi_rows(KDA["Hv"], 128, 16, seed=1)
+    mix = rs.Layout("mixed", 128, KDA["Hv"], KDA["Hk"], k_hi=16, hi_rows=hi)
+    pool = to_dev(w.state0)
+    mpool = mix.empty_pool(KDA["B"], device=dev)
+    rs.state_convert(f32, pool, mix, mpool, torch.arange(KDA["B"], dtype=torch.int32, device=dev))
+
+    def rec(name, sec, alg, updates, extra=None):
+        gbs = alg / sec / 1e9
+        out[name] = {"ms": sec * 1e3, "GB/s": gbs, "frac_of_peak": gbs / peak,
+                     "algorithmic_bytes": alg, "state_updates_per_s": updates / sec if updates else None}
+        if extra:
+            out[name].update(extra)
+
+    sec = _time(torch, lambda i: rs.kda_decode_update(f32, pool, slots, q[i % nsteps], k[i % nsteps],
+                                                      v[i % nsteps], al[i % nsteps], be[i % nsteps], o=o),
+                iters)
+    rec("kda_decode_fp32_b256", sec,
+        decode_bytes(256, 32, 32, 128, f32.head_bytes, 2, True), 256 * 32)
+    sec = _time(torch, lambda i: rs.kda_decode_update(mix, mpool, slots, q[i % nsteps], k[i % nsteps],
+                                                      v[i % nsteps], al[i % nsteps], be[i % nsteps], o=o),
+                iters)
+    rec("kda_decode_mixed_b256", sec,
+        decode_bytes(256, 32, 32, 128, mix.head_bytes, 2, True), 256 * 32)
+    al_g = al[..., 0].contiguous()  # one decay per (sequence, head) for the GDN form
+    sec = _time(torch, lambda i: rs.gdn_decode_update(mix, mpool, slots, q[i % nsteps], k[i % nsteps],
+                                                      v[i % nsteps], al_g[i % nsteps], be[i % nsteps],
+                                                      o=o),
+                iters)
+    rec("gdn_decode_mixed_b256_h32", sec,
+        decode_bytes(256, 32, 32, 128, mix.head_bytes, 2, False), 256 * 32)
+    # replay, T_max = 8, n_accept uniform 1..8
+    T = 8
+    n_acc = gen.n_accept(256, T, seed=1)
+    tok = int(n_acc.sum())
+
+    def bt(x):
+        return np.ascontiguousarray(np.swapaxes(x[:T], 0, 1))
+    rq, rk, rv = to_bf16(bt(w.q_bits)), to_bf16(bt(w.k_bits)), to_bf16(bt(w.v_bits))
+    ra, rb = to_dev(bt(w.alpha)), to_dev(bt(w.beta))
+    ro = torch.empty((256, T, 32, 128), device=dev)
+    nd = to_dev(n_acc)
+    sec = _time(torch, lambda i: rs.spec_replay_update(mix, True, mpool, slots, nd, rq, rk, rv, ra, rb,
+                                                       o=ro), iters)
+    per_tok = (2 * 32 * 128 * 2 + 32 * 128 * 2 + 32 * 128 * 4 + 32 * 4 + 32 * 128 * 4)
+    alg = 2 * 256 * 32 * mix.head_bytes + tok * per_tok
+    rec("kda_replay_mixed_b256_T8", sec, alg, tok * 32,
+        {"accepted_tokens": tok, "n_accept": "uniform 1..8"})
+    sec = _time(torch, lambda i: rs.spec_replay_update(f32, True, pool, slots, nd, rq, rk, rv, ra, rb,
+                                                       o=ro), iters)
+    alg = 2 * 256 * 32 * f32.head_bytes + tok * per_tok
+    rec("kda_replay_fp32_b256_T8", sec, alg, tok * 32, {"accepted_tokens": tok})
+    del pool, mpool, q, k, v, al, be, rq, rk, rv, ra, rb, ro
+    torch.cuda.empty_cache()
+
+    # dasc pack / restore: 36 layers, 64 checkpoints, 64 pool slots
+    for unit, p, name in ((0, 0.5, "gdn"), (1, 0.45, "kda")):
+        L, nslot, Hv, d, n = 36, 64, 32, 128, 64
+        keep = gen.keep_mask(L, Hv if unit == 0 else Hv * d, p, seed=unit)
+        src, dst = gen.ckpt_slots(nslot, n, seed=unit)
+        lay = rs.Layout("fp32", d, Hv, 1)
+        plan = rs.Plan(lay, keep, "head" if unit == 0 else "channel").upload()
+        big = torch.empty((L, nslot, Hv, d, d), device=dev)
+        big.normal_()
+        ckpt = plan.empty_ckpt_pool(n, device=dev)
+        sd, dd = to_dev(src), to_dev(dst)
+        kept_bytes = int(plan.offsets[-1]) * plan.unit_bytes * n
+        full_bytes = L * Hv * d * d * 4 * n
+        sec = _time(torch, lambda i: rs.ckpt_pack(plan, big, sd, dd, ckpt), max(5, iters // 10))
+        rec(f"ckpt_pack_{name}", sec, 2 * kept_bytes, 0,
+            {"checkpoints_per_s": n / sec, "C_temp": keep.size / max(int(keep.sum()), 1)})
+        sec = _time(torch, lambda i: rs.ckpt_restore(plan, ckpt, dd, big, sd), max(5, iters // 10))
+        rec(f"ckpt_restore_{name}", sec, kept_bytes + full_bytes, 0, {"checkpoints_per_s": n / sec})
+        del big, ckpt
+        torch.cuda.empty_cache()
+    return out
+
+
+# --------------------------------------------------------------------------
+# reference arm: the oracle on host cores
+# --------------------------------------------------------------------------
+def run_reference(args, budget_seconds=100.0):
+    s = OracleSample()
+    total = args.warmup + args.steps
+    n = s.size_for(budget_seconds / total)
+    for _ in range(args.warmup):
+        s.run(n)
+    t_all = 0.0
+    for _ in range(args.steps):
+        t_all += s.run(n)
+    value = n * args.steps / t_all
+    updates = GDN["B"] * GDN["Hv"]
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": updates / value * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": "GDN decode step, B=256, Hk=16, Hv=32, dk=dv=128, FP32 state, "
+                               "bf16 q/k/v", "global_batch": GDN["B"], "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": s.threads, "kind": "oracle",
+                         "sample": s.describe(n) + " per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--skip-extra", action="store_true", help="headline workload only")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return 0
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

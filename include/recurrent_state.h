@@ -1,0 +1,264 @@
+/*
+ * recurrent_state.h -- C ABI of the GB300 recurrent-state library.
+ *
+ * The library runs the batched decode-step update of gated delta-rule linear
+ * attention on one GPU (sm_103a), for GDN (one decay per head) and KDA (one
+ * decay per key channel), with FP32 or mixed FP16/INT8 state storage,
+ * speculative-token replay, and ragged dasc checkpoint pack/restore.
+ *
+ * Pages cited (by title and section):
+ *   [dasc] "dasc: Decay-Aware State Compression for Hybrid Linear-Attention
+ *          Serving" (arXiv 2608.30386).
+ *   [DAMP] "DAMP: Decay-Aware Mixed-Precision Recurrent-State Quantization"
+ *          (arXiv 2608.27513).
+ *   [SRA]  "Serving recurrent attention" (Kimi K3 explainer, section 22).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Every call returns an rs_status.  No C++ exception crosses this ABI.
+ * - Pointers named "device" must point to memory of the current CUDA device,
+ *   16-byte aligned, contiguous in the layout stated; RS_ERR_MISALIGNED
+ *   otherwise.  Pointers named "host" are read during the call only.
+ * - The caller owns every device buffer, every stream and every event.  The
+ *   library owns only the rs_layout and rs_plan objects it creates (host
+ *   memory, plus the device tables of an uploaded plan).  Decode, replay,
+ *   convert, pack and restore never allocate and never synchronise: they
+ *   enqueue kernels on `stream` (a cudaStream_t; NULL = legacy default
+ *   stream) and return.
+ * - Host-side validation failures return before any launch and modify
+ *   nothing.
+ * - Index errors that can only be seen on the device (a slot index out of
+ *   range, an accepted-token count out of range) skip the affected item and
+ *   OR a bit into the caller's int32 device status word `status` (may be
+ *   NULL).  Nothing traps, nothing hangs; read the word after the stream
+ *   completes.  Every on-chip pipeline wait is bounded; a wait that runs out
+ *   sets RS_DEV_PIPE_TIMEOUT and the kernel returns.
+ * - Slot indices within one call must be distinct (two items that name the
+ *   same slot race on it).
+ *
+ * State layouts (one linear-attention layer; a pool is [slots][Hv][head])
+ * ----------------------------------------------------------------------
+ * RS_LAYOUT_FP32: head = float32 S[dk][dv], row u = key channel u ([DAMP]
+ *   §3.1: S in R^{dk x dv}, row S_{t,u} per key channel), 4*dk*dv bytes.
+ * RS_LAYOUT_MIXED_FP16_INT8 ([DAMP] §5.2, Appendix A.4; one FP32 scale per
+ *   INT8 row as in [DAMP] §3.2 Eq. 5-6): head = the permuted state T = P_K S
+ *   ([DAMP] Appendix A.3 Eq. 17) stored as
+ *     fp16  rows 0..k_hi-1           [k_hi][dv]       2*k_hi*dv bytes
+ *     int8  rows k_hi..dk-1          [dk-k_hi][dv]    (dk-k_hi)*dv bytes
+ *     fp32  one scale per INT8 row   [dk-k_hi]        4*(dk-k_hi) bytes
+ *   (18,880 bytes at dk = dv = 128, k_hi = 16).  Physical row r holds key
+ *   channel pi[r]: the k_hi selected channels in ascending order, then the
+ *   rest in ascending order ([DAMP] Appendix A.2, Algorithm 1, last step).
+ *   INT8 rows use a = max_v |x_v| (NaN if any x_v is NaN),
+ *   s = max(a, 1e-8)/127, c = clip(round_half_even(x/s), -127, 127), with the
+ *   maximum, the division and the rounding in IEEE FP32 ([dasc] Appendix E.1
+ *   Eq. 8); dequantised value c*s.  FP16 rows round to nearest even.
+ *
+ * Decode step (per sequence b and value head h; [DAMP] §3.1 Eq. 1-2,
+ * equivalently [dasc] §3.1 Eq. 1 on the transposed state):
+ *     S <- diag(alpha) S
+ *     p = S^T k,   e = v - p
+ *     S <- S + beta k e^T
+ *     o = S^T q                          (o reads the updated state)
+ * FP32 evaluation order (fixed so results are reproducible bit for bit):
+ * decay = one multiply per element; both sums over key channels run in
+ * ascending physical row order from +0.0, one fused multiply-add per term;
+ * the write is fmaf(beta*k[u], e[v], S[u][v]) with beta*k[u] rounded first.
+ * Value head h reads q and k of key head h / (Hv/Hk): the Hv/Hk adjacent
+ * value heads share one key head ([dasc] Appendix B.1).  The kernels take q
+ * and k as given (the model L2-normalises them upstream, [DAMP] §3.1).
+ * Mixed layout: each step dequantises once, updates and reads out in FP32,
+ * requantises once and writes back ([DAMP] Appendix A.4 "Fused decoding");
+ * o is read from the FP32 updated state before requantisation.
+ */
+#ifndef RECURRENT_STATE_H
+#define RECURRENT_STATE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes (return values) -------------------------------------- */
+typedef int32_t rs_status;
+#define RS_OK                0
+#define RS_ERR_INVALID_ARG  (-1)  /* bad size, NULL pointer, unknown enum   */
+#define RS_ERR_UNSUPPORTED  (-2)  /* valid but not built (e.g. dk = 96)     */
+#define RS_ERR_MISALIGNED   (-3)  /* a device pointer not 16-byte aligned   */
+#define RS_ERR_CUDA         (-4)  /* a CUDA runtime call failed (see below) */
+
+/* ---- device status word bits (OR-ed by kernels into *status) ----------- */
+#define RS_DEV_BAD_SLOT       1   /* a pool slot index outside [0, n_slots) */
+#define RS_DEV_BAD_ACCEPT     2   /* n_accept[b] outside [0, T_max]         */
+#define RS_DEV_BAD_CKPT_SLOT  4   /* a checkpoint slot outside its pool     */
+#define RS_DEV_PIPE_TIMEOUT   8   /* an on-chip pipeline wait ran out       */
+
+/* ---- enums ------------------------------------------------------------- */
+#define RS_LAYOUT_FP32             0
+#define RS_LAYOUT_MIXED_FP16_INT8  1
+
+#define RS_F32   0
+#define RS_BF16  1
+#define RS_F16   2
+
+#define RS_UNIT_HEAD     0   /* GDN checkpoint unit: one head state        */
+#define RS_UNIT_CHANNEL  1   /* KDA checkpoint unit: one key-channel row   */
+
+/* ---- opaque objects ---------------------------------------------------- */
+typedef struct rs_layout rs_layout;
+typedef struct rs_plan rs_plan;
+
+typedef struct {
+    int32_t kind;          /* RS_LAYOUT_FP32 or RS_LAYOUT_MIXED_FP16_INT8   */
+    int32_t dk;            /* key channels per head (64 or 128)            */
+    int32_t dv;            /* values per key channel; must equal dk        */
+    int32_t num_v_heads;   /* Hv: state heads per layer                    */
+    int32_t num_qk_heads;  /* Hk: q/k heads; Hv % Hk == 0                  */
+    int32_t k_hi;          /* FP16 rows per head (mixed layout), else 0    */
+} rs_layout_params;
+
+/* Human-readable text for a status code (static storage). */
+const char *rs_status_string(rs_status s);
+
+/* Text of the last CUDA error seen by this thread in the library ("" if none). */
+const char *rs_last_cuda_error(void);
+
+/* Library version, e.g. "0.1.0". */
+const char *rs_version(void);
+
+/* ---- layout descriptors (host only; no CUDA call) ---------------------- */
+
+/* Create a state-pool layout.  hi_rows (host, may be NULL for the FP32
+ * layout) holds, per value head, the k_hi selected key channels
+ * ([DAMP] §5.1 "Budgeted selection": the same count for every head); order
+ * within a head does not matter, duplicates are rejected.  *out receives a
+ * library-owned object; free it with rs_layout_destroy. */
+rs_status rs_layout_create(rs_layout **out, const rs_layout_params *p,
+                           const int16_t *hi_rows /* host [Hv][k_hi] */);
+rs_status rs_layout_destroy(rs_layout *l);
+
+/* Bytes of one head state in this layout (65,536 or 18,880 at d = 128). */
+rs_status rs_layout_head_bytes(const rs_layout *l, size_t *bytes);
+
+/* The row map pi (physical row -> key channel) per head, host [Hv][dk]. */
+rs_status rs_layout_row_map(const rs_layout *l, int16_t *pi);
+
+/* Storage cost per state value in bits, scales included ([DAMP] Table 1
+ * "Avg. bits"): 32 for FP32, (16*k_hi*dv + 8*(dk-k_hi)*dv + 32*(dk-k_hi))
+ * / (dk*dv) for the mixed layout. */
+rs_status rs_layout_bits_per_value(const rs_layout *l, double *bits);
+
+/* ---- decode-step updates ----------------------------------------------- */
+
+/* GDN decode step, one scalar decay per (sequence, value head)
+ * ([DAMP] §3.1: Lambda = alpha I).
+ *   pool      device  [n_slots][Hv][head_bytes]   state of one layer, in place
+ *   slot_idx  device  int32 [B]                   pool slot of sequence b
+ *   q, k      device  in_dtype [B][Hk][dk]
+ *   v         device  in_dtype [B][Hv][dv]
+ *   alpha     device  float [B][Hv]               decay in (0, 1]
+ *   beta      device  float [B][Hv]               write strength
+ *   o         device  out_dtype [B][Hv][dv]        readout (may be NULL)
+ *   status    device  int32 (may be NULL)
+ * in_dtype: RS_F32, RS_BF16 or RS_F16; out_dtype: RS_F32 or RS_BF16.
+ * B = 0 is a no-op. */
+rs_status rs_gdn_decode_update(const rs_layout *l, void *pool, int64_t n_slots,
+                               const int32_t *slot_idx, int32_t B,
+                               const void *q, const void *k, const void *v,
+                               int32_t in_dtype, const float *alpha, const float *beta,
+                               void *o, int32_t out_dtype, int32_t *status,
+                               void *stream);
+
+/* KDA decode step, one decay per key channel ([DAMP] §3.1:
+ * Lambda = diag(exp g); [dasc] §3.1 Eq. 1, alpha in (0,1)^dk).  As above,
+ * except alpha is device float [B][Hv][dk], indexed by key channel (not by
+ * physical row). */
+rs_status rs_kda_decode_update(const rs_layout *l, void *pool, int64_t n_slots,
+                               const int32_t *slot_idx, int32_t B,
+                               const void *q, const void *k, const void *v,
+                               int32_t in_dtype, const float *alpha, const float *beta,
+                               void *o, int32_t out_dtype, int32_t *status,
+                               void *stream);
+
+/* Speculative-token replay ([SRA] "Speculative decoding without state
+ * snapshots"): the projected inputs of T_max draft tokens were logged; for
+ * each sequence b the first n_accept[b] of them are replayed on the state,
+ * which is read (and dequantised) once, kept on chip across the tokens, and
+ * written (and requantised) once.  To add the target model's bonus token,
+ * log it as one more token.  With the FP32 layout the result equals
+ * n_accept[b] decode steps bit for bit.
+ *   per_channel_decay  0 = GDN (alpha [B][T_max][Hv]),
+ *                      1 = KDA (alpha [B][T_max][Hv][dk])
+ *   T_max     1..8
+ *   n_accept  device int32 [B]; 0 leaves the state untouched
+ *   q, k      device in_dtype [B][T_max][Hk][dk]; v [B][T_max][Hv][dv]
+ *   beta      device float [B][T_max][Hv]
+ *   o         device out_dtype [B][T_max][Hv][dv] or NULL; rows t >= n_accept[b]
+ *             are not written. */
+rs_status rs_spec_replay_update(const rs_layout *l, int32_t per_channel_decay,
+                                void *pool, int64_t n_slots, const int32_t *slot_idx,
+                                int32_t B, int32_t T_max, const int32_t *n_accept,
+                                const void *q, const void *k, const void *v,
+                                int32_t in_dtype, const float *alpha, const float *beta,
+                                void *o, int32_t out_dtype, int32_t *status,
+                                void *stream);
+
+/* Convert n slots between two layouts of the same shape (FP32 -> mixed
+ * quantises with the rules above; mixed -> FP32 dequantises and un-permutes
+ * rows; same kind copies).  slots: device int32 [n], used as both source and
+ * destination slot. */
+rs_status rs_state_convert(const rs_layout *src_l, const void *src_pool,
+                           const rs_layout *dst_l, void *dst_pool, int64_t n_slots,
+                           const int32_t *slots, int32_t n, int32_t *status,
+                           void *stream);
+
+/* ---- dasc checkpoint plans and pack / restore --------------------------- */
+
+/* Selection plan ([dasc] §4.1): keep (host uint8 [L][n_units], 0/1) marks
+ * the retained units of each of num_layers layers.  unit = RS_UNIT_HEAD
+ * (GDN: n_units = Hv, unit = one head, 4*dk*dv bytes) or RS_UNIT_CHANNEL
+ * (KDA: n_units = Hv*dk, unit = row (h, u) of dv floats).  Only the FP32
+ * layout is packed.  Host only: offsets o_0 = 0, o_l = o_{l-1} + r_l
+ * ([dasc] Appendix B "Ragged (Scheme 2)") are computed here. */
+rs_status rs_plan_create(rs_plan **out, const rs_layout *l, int32_t num_layers,
+                         int32_t unit, const uint8_t *keep);
+rs_status rs_plan_destroy(rs_plan *p);
+
+/* offsets: host int64 [L+1] (o_0..o_L, in units); unit_bytes: bytes per unit.
+ * Checkpoint slot size is o_L * unit_bytes. */
+rs_status rs_plan_offsets(const rs_plan *p, int64_t *offsets, int64_t *unit_bytes);
+
+/* Copy the plan's index tables to the current device (allocates them once
+ * per plan; [dasc] Appendix B.2: masks and offsets are precomputed once and
+ * reused).  Required before pack/restore; synchronous. */
+rs_status rs_plan_upload(rs_plan *p);
+
+/* Pack ([dasc] §4.1, Appendix B): for each i < n, copy the retained units of
+ * every layer of pool slot src_slots[i] into checkpoint slot
+ * dst_ckpt_slots[i], layer l at units [o_{l-1}, o_l), ascending unit order.
+ *   pool         device  [L] x (layer_stride_bytes apart) x [n_pool_slots][Hv][head]
+ *   ckpt_pool    device  [n_ckpt_slots][o_L * unit_bytes] (may be NULL when o_L = 0)
+ *   src_slots, dst_ckpt_slots  device int32 [n]   */
+rs_status rs_ckpt_pack(const rs_plan *p, const void *pool, int64_t layer_stride_bytes,
+                       int64_t n_pool_slots, const int32_t *src_slots,
+                       const int32_t *dst_ckpt_slots, int32_t n, void *ckpt_pool,
+                       int64_t n_ckpt_slots, int32_t *status, void *stream);
+
+/* Restore, dasc-nr ([dasc] §4.2; [SRA] "One pool, two cache types": restore
+ * the immutable checkpoint into the request's private running state): for
+ * each i < n, every unit of every layer of pool slot dst_slots[i] is written,
+ * retained units from checkpoint slot src_ckpt_slots[i], omitted units as
+ * +0.0 (all bytes zero). */
+rs_status rs_ckpt_restore(const rs_plan *p, const void *ckpt_pool, int64_t n_ckpt_slots,
+                          const int32_t *src_ckpt_slots, void *pool,
+                          int64_t layer_stride_bytes, int64_t n_pool_slots,
+                          const int32_t *dst_slots, int32_t n, int32_t *status,
+                          void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RECURRENT_STATE_H */

@@ -1,0 +1,87 @@
+// rs_convert.cu -- FP32 <-> mixed FP16/INT8 state conversion (DAMP §5.2,
+// Appendix A.3 Eq. 17, Appendix A.4), and same-layout slot copies.
+//
+// One CTA of D threads per (slot, head) tile; thread v owns column v.
+// FP32 -> mixed: physical row r of the mixed tile takes logical key channel
+// pi[r]; the rows are requantised by the same routine as the decode kernel.
+// Mixed -> FP32: dequantise and write each physical row back to its logical
+// channel.  Used to initialise and inspect mixed pools, not on the decode path.
+#include "rs_step.cuh"
+#include "../../include/recurrent_state.h"
+
+namespace rs {
+
+namespace {
+
+template <int D, int KH>
+__global__ void __launch_bounds__(D) convert_kernel(const __grid_constant__ ConvertParamsPi P) {
+    constexpr int kMixedBytes = 2 * KH * D + (D - KH) * D + 4 * (D - KH);
+    constexpr int kF32Bytes = D * D * 4;
+    __shared__ float red[(D / 32) * D];
+    __shared__ float2 sy[D];
+    __shared__ uint8_t pi_s[D];
+    const int tid = threadIdx.x, lane = tid & 31, wig = tid >> 5;
+    const int i = blockIdx.x / P.Hv, h = blockIdx.x - (blockIdx.x / P.Hv) * P.Hv;
+    const int32_t slot = P.slots[i];
+    if (slot < 0 || (int64_t)slot >= P.n_slots) {
+        if (tid == 0 && P.status) atomicOr(P.status, RS_DEV_BAD_SLOT);
+        return;
+    }
+    pi_s[tid] = P.pi[h * D + tid];
+    __syncthreads();
+    const size_t tile = (size_t)slot * P.Hv + h;
+    float x[D];
+    if (P.to_mixed) {
+        const float *src = static_cast<const float *>(P.src) + tile * (D * D);
+#pragma unroll
+        for (int r = 0; r < D; ++r) x[r] = src[(int)pi_s[r] * D + tid];
+        mixed_requant_store<D, KH>(x, static_cast<uint8_t *>(P.dst) + tile * kMixedBytes, red, sy,
+                                   tid, lane, wig, 0);
+    } else {
+        mixed_dequant<D, KH>(static_cast<const uint8_t *>(P.src) + tile * kMixedBytes, tid, x);
+        float *dst = static_cast<float *>(P.dst) + tile * (D * D);
+#pragma unroll
+        for (int r = 0; r < D; ++r) dst[(int)pi_s[r] * D + tid] = x[r];
+    }
+    (void)kF32Bytes;
+}
+
+// Same-layout copy of whole heads: 16-byte vectors, one CTA per (slot, head).
+__global__ void copy_heads_kernel(const uint8_t *src, uint8_t *dst, int64_t head_bytes,
+                                  const int32_t *slots, int64_t n_slots, int32_t Hv,
+                                  int32_t *status) {
+    const int i = blockIdx.x / Hv, h = blockIdx.x - (blockIdx.x / Hv) * Hv;
+    const int32_t slot = slots[i];
+    if (slot < 0 || (int64_t)slot >= n_slots) {
+        if (threadIdx.x == 0 && status) atomicOr(status, RS_DEV_BAD_SLOT);
+        return;
+    }
+    const size_t off = ((size_t)slot * Hv + h) * head_bytes;
+    const uint4 *s4 = reinterpret_cast<const uint4 *>(src + off);
+    uint4 *d4 = reinterpret_cast<uint4 *>(dst + off);
+    for (int64_t j = threadIdx.x; j < head_bytes / 16; j += blockDim.x) d4[j] = s4[j];
+}
+
+}  // namespace
+
+cudaError_t launch_convert(int D, int khi, ConvertParamsPi &P, cudaStream_t s) {
+    if (P.n == 0) return cudaSuccess;
+    const unsigned grid = (unsigned)P.n * (unsigned)P.Hv;
+    if (D == 128 && khi == 16) {
+        convert_kernel<128, 16><<<grid, 128, 0, s>>>(P);
+        return cudaGetLastError();
+    }
+    return cudaErrorNotSupported;
+}
+
+cudaError_t launch_copy_heads(const void *src, void *dst, int64_t head_bytes, const int32_t *slots,
+                              int32_t n, int64_t n_slots, int32_t Hv, int32_t *status,
+                              cudaStream_t s) {
+    if (n == 0) return cudaSuccess;
+    copy_heads_kernel<<<(unsigned)n * (unsigned)Hv, 256, 0, s>>>(
+        static_cast<const uint8_t *>(src), static_cast<uint8_t *>(dst), head_bytes, slots, n_slots,
+        Hv, status);
+    return cudaGetLastError();
+}
+
+}  // namespace rs

@@ -1,0 +1,99 @@
+// rs_internal.h -- launch parameters and launcher entry points shared by the
+// host-side C ABI (rs_api.cu) and the kernel translation units.  Not part of
+// the public interface.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace rs {
+
+constexpr int kMaxTokens = 8;        // replay window (draft tokens per call)
+constexpr int kStepThreads = 384;    // threads per CTA of the step kernel
+constexpr int kMaxRowMap = 8192;     // bytes of row maps carried in the launch params
+
+struct StepParams {
+    void *pool;
+    int64_t n_slots;
+    const int32_t *slot_idx;
+    const int32_t *n_accept;   // replay only
+    const void *q;
+    const void *k;
+    const void *v;
+    const float *alpha;
+    const float *beta;
+    void *o;
+    int32_t *status;
+    int32_t B, Hk, Hv, T_max;
+    int32_t replay;            // 0: one token per item; 1: n_accept[b] tokens
+    int32_t header_bytes;      // shared memory before the per-group regions
+    int32_t region_bytes;      // shared memory per group
+};
+
+// Mixed layout: the row map pi (physical row -> key channel), [Hv][D] bytes,
+// travels with the launch so the library needs no device allocation for it.
+struct StepParamsPi : StepParams {
+    uint8_t pi[kMaxRowMap];
+};
+
+struct StepLaunch {
+    int D;          // 64 or 128
+    int khi;        // -1 = FP32 layout, else FP16 rows of the mixed layout
+    bool kda;
+    int in_dt;      // RS_F32 / RS_BF16 / RS_F16
+    int out_dt;     // RS_F32 / RS_BF16
+};
+
+// Defined in rs_step_*.cu (one translation unit each, compiled in parallel).
+// They return cudaErrorNotSupported for a combination that is not built.
+cudaError_t launch_step_f32_d64(const StepLaunch &L, StepParams &P, cudaStream_t s);
+cudaError_t launch_step_f32_d128(const StepLaunch &L, StepParams &P, cudaStream_t s);
+cudaError_t launch_step_mixed_decode(const StepLaunch &L, StepParamsPi &P, cudaStream_t s);
+cudaError_t launch_step_mixed_replay(const StepLaunch &L, StepParamsPi &P, cudaStream_t s);
+
+// rs_convert.cu
+struct ConvertParams {
+    const void *src;
+    void *dst;
+    int64_t n_slots;
+    const int32_t *slots;
+    int32_t *status;
+    int32_t n, Hv;
+    int32_t to_mixed;          // 1: FP32 -> mixed, 0: mixed -> FP32
+};
+struct ConvertParamsPi : ConvertParams {
+    uint8_t pi[kMaxRowMap];
+};
+cudaError_t launch_convert(int D, int khi, ConvertParamsPi &P, cudaStream_t s);
+cudaError_t launch_copy_heads(const void *src, void *dst, int64_t head_bytes, const int32_t *slots,
+                              int32_t n, int64_t n_slots, int32_t Hv, int32_t *status,
+                              cudaStream_t s);
+
+// rs_ckpt.cu
+struct CkptParams {
+    const uint8_t *src;
+    uint8_t *dst;
+    int64_t layer_stride;      // bytes between layers of the pool
+    int64_t slot_bytes;        // bytes of one slot of one layer (Hv heads)
+    int64_t ckpt_slot_bytes;   // o_L * unit_bytes
+    int64_t unit_bytes;
+    int64_t n_pool_slots, n_ckpt_slots;
+    int64_t n_kept;            // o_L
+    int64_t n_all;             // L * n_units
+    const int32_t *kept_unit;  // [n_kept]  (layer << 20) | unit, packed order
+    const int32_t *all_pidx;   // [n_all]   packed index or -1 (restore)
+    const int32_t *pool_slots; // [n]
+    const int32_t *ckpt_slots; // [n]
+    int32_t *status;
+    int32_t n;
+    int32_t units_per_layer;
+};
+cudaError_t launch_ckpt_pack(const CkptParams &P, cudaStream_t s);
+cudaError_t launch_ckpt_restore(const CkptParams &P, cudaStream_t s);
+
+// Per-device cached attributes.
+int device_sm_count();
+int device_max_smem_optin();
+
+}  // namespace rs
