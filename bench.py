@@ -187,11 +187,15 @@ class OracleSample:
 
 
 def cpu_baseline(target_seconds=12.0):
+    """About target_seconds of oracle work: repeated passes over (a sample of)
+    the batch's items, timed as a whole."""
     s = OracleSample()
     n = s.size_for(target_seconds)
-    dt = s.run(n)
-    return {"value": n / dt, "unit": UNIT, "cores": s.threads, "kind": "oracle",
-            "sample": s.describe(n), "seconds": dt}
+    per_pass = max(n * s.per_item / s.threads, 1e-6)
+    passes = max(1, int(round(target_seconds / per_pass)))
+    dt = sum(s.run(n) for _ in range(passes))
+    return {"value": n * passes / dt, "unit": UNIT, "cores": s.threads, "kind": "oracle",
+            "sample": f"{passes} pass(es) over " + s.describe(n), "seconds": dt}
 
 
 # --------------------------------------------------------------------------
@@ -332,6 +336,7 @@ def _max_over_ranks(x, world):
 
 
 def _time(torch, fn, iters, warm=3):
+    warm = max(3, warm)
     for i in range(warm):
         fn(i)
     torch.cuda.synchronize()
@@ -344,30 +349,22 @@ def _time(torch, fn, iters, warm=3):
     return e0.elapsed_time(e1) / 1e3 / iters
 
 
-def extra_kernels(args, rs, torch, dev, peak, world):
+EXTRA = ("kda_fp32", "kda_mixed", "gdn_mixed", "replay_mixed", "replay_fp32",
+         "pack_gdn", "restore_gdn", "pack_kda", "restore_kda")
+
+
+def extra_kernels(args, rs, torch, dev, peak, world, only=None):
     """The other hot-path kernels, each timed alone on its own workload."""
     out = {}
-    iters = max(10, min(args.steps, 200))
+    iters = max(3, min(args.steps, 200))
+    warm = max(3, min(args.warmup, 10))
+    want = set(only) if only else set(EXTRA)
 
     def to_dev(a):
         return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
     def to_bf16(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
-
-    nsteps = 8
-    w = gen.decode_workload(steps=nsteps, per_channel=True, in_dtype="bf16", seed=1,
-                            horizon=(2.0, 8192.0), **KDA)
-    q, k, v = to_bf16(w.q_bits), to_bf16(w.k_bits), to_bf16(w.v_bits)
-    al, be = to_dev(w.alpha), to_dev(w.beta)
-    slots = to_dev(w.slot_idx)
-    o = torch.empty((KDA["B"], KDA["Hv"], KDA["d"]), device=dev)
-    f32 = rs.Layout("fp32", 128, KDA["Hv"], KDA["Hk"])
-    hi = gen.hi_rows(KDA["Hv"], 128, 16, seed=1)
-    mix = rs.Layout("mixed", 128, KDA["Hv"], KDA["Hk"], k_hi=16, hi_rows=hi)
-    pool = to_dev(w.state0)
-    mpool = mix.empty_pool(KDA["B"], device=dev)
-    rs.state_convert(f32, pool, mix, mpool, torch.arange(KDA["B"], dtype=torch.int32, device=dev))
 
     def rec(name, sec, alg, updates, extra=None):
         gbs = alg / sec / 1e9
@@ -376,49 +373,68 @@ def extra_kernels(args, rs, torch, dev, peak, world):
         if extra:
             out[name].update(extra)
 
-    sec = _time(torch, lambda i: rs.kda_decode_update(f32, pool, slots, q[i % nsteps], k[i % nsteps],
-                                                      v[i % nsteps], al[i % nsteps], be[i % nsteps], o=o),
-                iters)
-    rec("kda_decode_fp32_b256", sec,
-        decode_bytes(256, 32, 32, 128, f32.head_bytes, 2, True), 256 * 32)
-    sec = _time(torch, lambda i: rs.kda_decode_update(mix, mpool, slots, q[i % nsteps], k[i % nsteps],
-                                                      v[i % nsteps], al[i % nsteps], be[i % nsteps], o=o),
-                iters)
-    rec("kda_decode_mixed_b256", sec,
-        decode_bytes(256, 32, 32, 128, mix.head_bytes, 2, True), 256 * 32)
-    al_g = al[..., 0].contiguous()  # one decay per (sequence, head) for the GDN form
-    sec = _time(torch, lambda i: rs.gdn_decode_update(mix, mpool, slots, q[i % nsteps], k[i % nsteps],
-                                                      v[i % nsteps], al_g[i % nsteps], be[i % nsteps],
-                                                      o=o),
-                iters)
-    rec("gdn_decode_mixed_b256_h32", sec,
-        decode_bytes(256, 32, 32, 128, mix.head_bytes, 2, False), 256 * 32)
-    # replay, T_max = 8, n_accept uniform 1..8
-    T = 8
-    n_acc = gen.n_accept(256, T, seed=1)
-    tok = int(n_acc.sum())
+    if want & {"kda_fp32", "kda_mixed", "gdn_mixed", "replay_mixed", "replay_fp32"}:
+        nsteps = 8
+        w = gen.decode_workload(steps=nsteps, per_channel=True, in_dtype="bf16", seed=1,
+                                horizon=(2.0, 8192.0), **KDA)
+        q, k, v = to_bf16(w.q_bits), to_bf16(w.k_bits), to_bf16(w.v_bits)
+        al, be = to_dev(w.alpha), to_dev(w.beta)
+        slots = to_dev(w.slot_idx)
+        o = torch.empty((KDA["B"], KDA["Hv"], KDA["d"]), device=dev)
+        f32 = rs.Layout("fp32", 128, KDA["Hv"], KDA["Hk"])
+        hi = gen.hi_rows(KDA["Hv"], 128, 16, seed=1)
+        mix = rs.Layout("mixed", 128, KDA["Hv"], KDA["Hk"], k_hi=16, hi_rows=hi)
+        pool = to_dev(w.state0)
+        mpool = mix.empty_pool(KDA["B"], device=dev)
+        rs.state_convert(f32, pool, mix, mpool, torch.arange(KDA["B"], dtype=torch.int32, device=dev))
+        if "kda_fp32" in want:
+            sec = _time(torch, lambda i: rs.kda_decode_update(
+                f32, pool, slots, q[i % nsteps], k[i % nsteps], v[i % nsteps], al[i % nsteps],
+                be[i % nsteps], o=o), iters, warm)
+            rec("kda_decode_fp32_b256", sec, decode_bytes(256, 32, 32, 128, f32.head_bytes, 2, True),
+                256 * 32)
+        if "kda_mixed" in want:
+            sec = _time(torch, lambda i: rs.kda_decode_update(
+                mix, mpool, slots, q[i % nsteps], k[i % nsteps], v[i % nsteps], al[i % nsteps],
+                be[i % nsteps], o=o), iters, warm)
+            rec("kda_decode_mixed_b256", sec, decode_bytes(256, 32, 32, 128, mix.head_bytes, 2, True),
+                256 * 32)
+        if "gdn_mixed" in want:
+            al_g = al[..., 0].contiguous()  # one decay per (sequence, head) for the GDN form
+            sec = _time(torch, lambda i: rs.gdn_decode_update(
+                mix, mpool, slots, q[i % nsteps], k[i % nsteps], v[i % nsteps], al_g[i % nsteps],
+                be[i % nsteps], o=o), iters, warm)
+            rec("gdn_decode_mixed_b256_h32", sec,
+                decode_bytes(256, 32, 32, 128, mix.head_bytes, 2, False), 256 * 32)
+        if want & {"replay_mixed", "replay_fp32"}:
+            T = 8
+            n_acc = gen.n_accept(256, T, seed=1)
+            tok = int(n_acc.sum())
 
-    def bt(x):
-        return np.ascontiguousarray(np.swapaxes(x[:T], 0, 1))
-    rq, rk, rv = to_bf16(bt(w.q_bits)), to_bf16(bt(w.k_bits)), to_bf16(bt(w.v_bits))
-    ra, rb = to_dev(bt(w.alpha)), to_dev(bt(w.beta))
-    ro = torch.empty((256, T, 32, 128), device=dev)
-    nd = to_dev(n_acc)
-    sec = _time(torch, lambda i: rs.spec_replay_update(mix, True, mpool, slots, nd, rq, rk, rv, ra, rb,
-                                                       o=ro), iters)
-    per_tok = (2 * 32 * 128 * 2 + 32 * 128 * 2 + 32 * 128 * 4 + 32 * 4 + 32 * 128 * 4)
-    alg = 2 * 256 * 32 * mix.head_bytes + tok * per_tok
-    rec("kda_replay_mixed_b256_T8", sec, alg, tok * 32,
-        {"accepted_tokens": tok, "n_accept": "uniform 1..8"})
-    sec = _time(torch, lambda i: rs.spec_replay_update(f32, True, pool, slots, nd, rq, rk, rv, ra, rb,
-                                                       o=ro), iters)
-    alg = 2 * 256 * 32 * f32.head_bytes + tok * per_tok
-    rec("kda_replay_fp32_b256_T8", sec, alg, tok * 32, {"accepted_tokens": tok})
-    del pool, mpool, q, k, v, al, be, rq, rk, rv, ra, rb, ro
-    torch.cuda.empty_cache()
+            def bt(x):
+                return np.ascontiguousarray(np.swapaxes(x[:T], 0, 1))
+            rq, rk, rv = to_bf16(bt(w.q_bits)), to_bf16(bt(w.k_bits)), to_bf16(bt(w.v_bits))
+            ra, rb = to_dev(bt(w.alpha)), to_dev(bt(w.beta))
+            ro = torch.empty((256, T, 32, 128), device=dev)
+            nd = to_dev(n_acc)
+            per_tok = 2 * 32 * 128 * 2 + 32 * 128 * 2 + 32 * 128 * 4 + 32 * 4 + 32 * 128 * 4
+            if "replay_mixed" in want:
+                sec = _time(torch, lambda i: rs.spec_replay_update(
+                    mix, True, mpool, slots, nd, rq, rk, rv, ra, rb, o=ro), iters, warm)
+                rec("kda_replay_mixed_b256_T8", sec, 2 * 256 * 32 * mix.head_bytes + tok * per_tok,
+                    tok * 32, {"accepted_tokens": tok, "n_accept": "uniform 1..8"})
+            if "replay_fp32" in want:
+                sec = _time(torch, lambda i: rs.spec_replay_update(
+                    f32, True, pool, slots, nd, rq, rk, rv, ra, rb, o=ro), iters, warm)
+                rec("kda_replay_fp32_b256_T8", sec, 2 * 256 * 32 * f32.head_bytes + tok * per_tok,
+                    tok * 32, {"accepted_tokens": tok})
+        del pool, mpool
+        torch.cuda.empty_cache()
 
     # dasc pack / restore: 36 layers, 64 checkpoints, 64 pool slots
     for unit, p, name in ((0, 0.5, "gdn"), (1, 0.45, "kda")):
+        if not want & {f"pack_{name}", f"restore_{name}"}:
+            continue
         L, nslot, Hv, d, n = 36, 64, 32, 128, 64
         keep = gen.keep_mask(L, Hv if unit == 0 else Hv * d, p, seed=unit)
         src, dst = gen.ckpt_slots(nslot, n, seed=unit)
@@ -430,11 +446,15 @@ def extra_kernels(args, rs, torch, dev, peak, world):
         sd, dd = to_dev(src), to_dev(dst)
         kept_bytes = int(plan.offsets[-1]) * plan.unit_bytes * n
         full_bytes = L * Hv * d * d * 4 * n
-        sec = _time(torch, lambda i: rs.ckpt_pack(plan, big, sd, dd, ckpt), max(5, iters // 10))
-        rec(f"ckpt_pack_{name}", sec, 2 * kept_bytes, 0,
-            {"checkpoints_per_s": n / sec, "C_temp": keep.size / max(int(keep.sum()), 1)})
-        sec = _time(torch, lambda i: rs.ckpt_restore(plan, ckpt, dd, big, sd), max(5, iters // 10))
-        rec(f"ckpt_restore_{name}", sec, kept_bytes + full_bytes, 0, {"checkpoints_per_s": n / sec})
+        rs.ckpt_pack(plan, big, sd, dd, ckpt)
+        if f"pack_{name}" in want:
+            sec = _time(torch, lambda i: rs.ckpt_pack(plan, big, sd, dd, ckpt), max(3, iters // 10), warm)
+            rec(f"ckpt_pack_{name}", sec, 2 * kept_bytes, 0,
+                {"checkpoints_per_s": n / sec, "C_temp": keep.size / max(int(keep.sum()), 1)})
+        if f"restore_{name}" in want:
+            sec = _time(torch, lambda i: rs.ckpt_restore(plan, ckpt, dd, big, sd), max(3, iters // 10),
+                        warm)
+            rec(f"ckpt_restore_{name}", sec, kept_bytes + full_bytes, 0, {"checkpoints_per_s": n / sec})
         del big, ckpt
         torch.cuda.empty_cache()
     return out
@@ -475,6 +495,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--skip-extra", action="store_true", help="headline workload only")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
+    ap.add_argument("--only", default=None,
+                    help="comma list of secondary kernels to time alone (" + ",".join(EXTRA) + ")")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -486,6 +508,20 @@ def main():
             print(json.dumps(run_reference(args)), flush=True)
         return 0
 
+    if args.only:
+        import torch
+        import recurrent_state_gb300 as rs
+        from recurrent_state_gb300 import build as rsbuild
+        rsbuild.build()
+        names = [x for x in args.only.split(",") if x]
+        bad = [x for x in names if x not in EXTRA]
+        if bad:
+            raise SystemExit(f"unknown kernel(s) {bad}; choose from {EXTRA}")
+        torch.cuda.set_device(local_rank)
+        res = extra_kernels(args, rs, torch, torch.device("cuda", local_rank), measured_peaks()[0],
+                            1, only=names)
+        print(json.dumps({"only": res}), flush=True)
+        return 0
     if world > 1:
         import torch
         import torch.distributed as dist

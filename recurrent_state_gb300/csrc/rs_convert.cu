@@ -16,9 +16,9 @@ namespace {
 template <int D, int KH>
 __global__ void __launch_bounds__(D) convert_kernel(const __grid_constant__ ConvertParamsPi P) {
     constexpr int kMixedBytes = 2 * KH * D + (D - KH) * D + 4 * (D - KH);
-    constexpr int kF32Bytes = D * D * 4;
     __shared__ float red[(D / 32) * D];
-    __shared__ float2 sy[D];
+    __shared__ __align__(16) float2 sy[D];
+    __shared__ __align__(16) uint8_t out[kMixedBytes];
     __shared__ uint8_t pi_s[D];
     const int tid = threadIdx.x, lane = tid & 31, wig = tid >> 5;
     const int i = blockIdx.x / P.Hv, h = blockIdx.x - (blockIdx.x / P.Hv) * P.Hv;
@@ -30,20 +30,26 @@ __global__ void __launch_bounds__(D) convert_kernel(const __grid_constant__ Conv
     pi_s[tid] = P.pi[h * D + tid];
     __syncthreads();
     const size_t tile = (size_t)slot * P.Hv + h;
-    float x[D];
+    float2 x[D / 2];
     if (P.to_mixed) {
         const float *src = static_cast<const float *>(P.src) + tile * (D * D);
 #pragma unroll
-        for (int r = 0; r < D; ++r) x[r] = src[(int)pi_s[r] * D + tid];
-        mixed_requant_store<D, KH>(x, static_cast<uint8_t *>(P.dst) + tile * kMixedBytes, red, sy,
-                                   tid, lane, wig, 0);
+        for (int j = 0; j < D / 2; ++j)
+            x[j] = make_float2(src[(int)pi_s[2 * j] * D + tid], src[(int)pi_s[2 * j + 1] * D + tid]);
+        mixed_requant_smem<D, KH>(x, out, red, sy, tid, lane, wig, 0, [] {});
+        __syncthreads();
+        uint4 *dst4 = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(P.dst) + tile * kMixedBytes);
+        const uint4 *src4 = reinterpret_cast<const uint4 *>(out);
+        for (int j = tid; j < kMixedBytes / 16; j += D) dst4[j] = src4[j];
     } else {
         mixed_dequant<D, KH>(static_cast<const uint8_t *>(P.src) + tile * kMixedBytes, tid, x);
         float *dst = static_cast<float *>(P.dst) + tile * (D * D);
 #pragma unroll
-        for (int r = 0; r < D; ++r) dst[(int)pi_s[r] * D + tid] = x[r];
+        for (int j = 0; j < D / 2; ++j) {
+            dst[(int)pi_s[2 * j] * D + tid] = x[j].x;
+            dst[(int)pi_s[2 * j + 1] * D + tid] = x[j].y;
+        }
     }
-    (void)kF32Bytes;
 }
 
 // Same-layout copy of whole heads: 16-byte vectors, one CTA per (slot, head).

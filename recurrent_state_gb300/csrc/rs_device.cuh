@@ -71,6 +71,29 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// 1-D bulk copy shared -> global (async proxy), tracked as a bulk group of
+// the issuing thread.  Addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_s2g(void *dst, const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                 "r"(smem_addr(src)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_store_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Wait until every committed bulk store of this thread has finished reading
+// its shared-memory source (the buffer may then be rewritten).
+__device__ __forceinline__ void bulk_store_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Wait until every committed bulk store of this thread has completed.
+__device__ __forceinline__ void bulk_store_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // Barrier over `count` threads (a multiple of 32) of this CTA, id 1..15.
 __device__ __forceinline__ void group_sync(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
@@ -93,7 +116,7 @@ __device__ __forceinline__ bool group_sync_or(uint32_t id, uint32_t count, bool 
 // max over the warp of |x|, NaN if any lane holds a NaN.
 __device__ __forceinline__ float warp_max_abs_nan(float x) {
     float r;
-    asm volatile("redux.sync.max.abs.NaN.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
+    asm("redux.sync.max.abs.NaN.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
     return r;
 }
 
