@@ -42,17 +42,23 @@
  *   §3.1: S in R^{dk x dv}, row S_{t,u} per key channel), 4*dk*dv bytes.
  * RS_LAYOUT_MIXED_FP16_INT8 ([DAMP] §5.2, Appendix A.4; one FP32 scale per
  *   INT8 row as in [DAMP] §3.2 Eq. 5-6): head = the permuted state T = P_K S
- *   ([DAMP] Appendix A.3 Eq. 17) stored as
- *     fp16  rows 0..k_hi-1           [k_hi][dv]       2*k_hi*dv bytes
- *     int8  rows k_hi..dk-1          [dk-k_hi][dv]    (dk-k_hi)*dv bytes
- *     fp32  one scale per INT8 row   [dk-k_hi]        4*(dk-k_hi) bytes
- *   (18,880 bytes at dk = dv = 128, k_hi = 16).  Physical row r holds key
+ *   ([DAMP] Appendix A.3 Eq. 17) stored as three contiguous regions
+ *     fp16  rows 0..k_hi-1           2*k_hi*dv bytes
+ *     int8  rows k_hi..dk-1          (dk-k_hi)*dv bytes
+ *     fp32  one scale per INT8 row   4*(dk-k_hi) bytes, row order
+ *   (18,880 bytes at dk = dv = 128, k_hi = 16).  Inside the fp16 and int8
+ *   regions rows are interleaved by 32-bit word so that one word holds one
+ *   column of 2 fp16 rows or of 4 int8 rows: fp16 value (r, c) is half
+ *   ((r/2)*dv + c)*2 + r%2; int8 value (r, c) is byte ((q/4)*dv + c)*4 + q%4
+ *   with q = r - k_hi (k_hi a multiple of 4).  Physical row r holds key
  *   channel pi[r]: the k_hi selected channels in ascending order, then the
  *   rest in ascending order ([DAMP] Appendix A.2, Algorithm 1, last step).
  *   INT8 rows use a = max_v |x_v| (NaN if any x_v is NaN),
  *   s = max(a, 1e-8)/127, c = clip(round_half_even(x/s), -127, 127), with the
  *   maximum, the division and the rounding in IEEE FP32 ([dasc] Appendix E.1
- *   Eq. 8); dequantised value c*s.  FP16 rows round to nearest even.
+ *   Eq. 8); dequantised value c*s.  FP16 rows round to nearest even.  A NaN
+ *   state value stays a NaN (its payload bits are unspecified); its INT8 code
+ *   is -127.
  *
  * Decode step (per sequence b and value head h; [DAMP] §3.1 Eq. 1-2,
  * equivalently [dasc] §3.1 Eq. 1 on the transposed state):

@@ -157,45 +157,69 @@ static float f16_bits_to_f32(uint16_t b)
 /*   bytes [.., + 4*(dk-khi))         : one FP32 scale per INT8 row          */
 /* Rows are physical rows of the permuted state T = P_K S ([DAMP] Appendix   */
 /* A.3 Eq. 17, value scaling and value reordering not applied).              */
+/* The pages fix that the two regions are contiguous so that they can be     */
+/* moved with vector loads and stores ([DAMP] Appendix A.4); the order of    */
+/* the values inside a region is left open.  Reading fixed here: rows are    */
+/* interleaved by the width of one 32-bit word, so the values of one column  */
+/* in 2 consecutive FP16 rows (or 4 consecutive INT8 rows) share a word:     */
+/*   FP16 value (r, c), r < khi:  half index ((r/2)*dv + c)*2 + r%2           */
+/*   INT8 value (r, c), r >= khi: byte index ((q/4)*dv + c)*4 + q%4, q = r-khi */
+/* (khi a multiple of 4).                                                    */
 /* ------------------------------------------------------------------------ */
 size_t orc_mixed_tile_bytes(int dk, int dv, int khi)
 {
     return (size_t)2 * khi * dv + (size_t)(dk - khi) * dv + (size_t)4 * (dk - khi);
 }
 
+static size_t hi_offset(int dv, int r, int c)   /* byte offset in the FP16 region */
+{
+    return (((size_t)(r / 2) * dv + c) * 2 + (size_t)(r % 2)) * 2;
+}
+
+static size_t lo_offset(int dv, int q, int c)   /* byte offset in the INT8 region */
+{
+    return ((size_t)(q / 4) * dv + c) * 4 + (size_t)(q % 4);
+}
+
 void orc_mixed_unpack(int dk, int dv, int khi, const uint8_t *tile, float *T)
 {
     const uint8_t *hi = tile;
-    const int8_t *lo = (const int8_t *)(tile + (size_t)2 * khi * dv);
+    const uint8_t *lo = tile + (size_t)2 * khi * dv;
     const uint8_t *sc = tile + (size_t)2 * khi * dv + (size_t)(dk - khi) * dv;
+    int8_t row[ORC_MAX_D];
     int r, c;
     for (r = 0; r < khi; ++r)
         for (c = 0; c < dv; ++c) {
             uint16_t b;
-            memcpy(&b, hi + ((size_t)r * dv + c) * 2, 2);
+            memcpy(&b, hi + hi_offset(dv, r, c), 2);
             T[(size_t)r * dv + c] = f16_bits_to_f32(b);
         }
     for (r = khi; r < dk; ++r) {
         float s;
         memcpy(&s, sc + (size_t)(r - khi) * 4, 4);
-        orc_dequantise_row(dv, lo + (size_t)(r - khi) * dv, s, T + (size_t)r * dv);
+        for (c = 0; c < dv; ++c)
+            row[c] = (int8_t)lo[lo_offset(dv, r - khi, c)];
+        orc_dequantise_row(dv, row, s, T + (size_t)r * dv);
     }
 }
 
 void orc_mixed_pack(int dk, int dv, int khi, const float *T, uint8_t *tile)
 {
     uint8_t *hi = tile;
-    int8_t *lo = (int8_t *)(tile + (size_t)2 * khi * dv);
+    uint8_t *lo = tile + (size_t)2 * khi * dv;
     uint8_t *sc = tile + (size_t)2 * khi * dv + (size_t)(dk - khi) * dv;
+    int8_t row[ORC_MAX_D];
     int r, c;
     for (r = 0; r < khi; ++r)
         for (c = 0; c < dv; ++c) {
             uint16_t b = f32_to_f16_bits(T[(size_t)r * dv + c]);
-            memcpy(hi + ((size_t)r * dv + c) * 2, &b, 2);
+            memcpy(hi + hi_offset(dv, r, c), &b, 2);
         }
     for (r = khi; r < dk; ++r) {
         float s;
-        orc_quantise_row(dv, T + (size_t)r * dv, lo + (size_t)(r - khi) * dv, &s);
+        orc_quantise_row(dv, T + (size_t)r * dv, row, &s);
+        for (c = 0; c < dv; ++c)
+            lo[lo_offset(dv, r - khi, c)] = (uint8_t)row[c];
         memcpy(sc + (size_t)(r - khi) * 4, &s, 4);
     }
 }

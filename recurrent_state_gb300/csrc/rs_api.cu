@@ -126,7 +126,7 @@ rs_status rs_layout_create(rs_layout **out, const rs_layout_params *p, const int
             for (int r = 0; r < dk; ++r) l->pi[(size_t)h * dk + r] = (int16_t)r;
         l->head_bytes = (size_t)4 * dk * p->dv;
     } else {
-        if (p->k_hi < 0 || p->k_hi > dk || !hi_rows) { delete l; return RS_ERR_INVALID_ARG; }
+        if (p->k_hi < 0 || p->k_hi > dk || (p->k_hi % 4) != 0 || !hi_rows) { delete l; return RS_ERR_INVALID_ARG; }
         if ((size_t)Hv * dk > (size_t)rs::kMaxRowMap) { delete l; return RS_ERR_UNSUPPORTED; }
         std::vector<uint8_t> seen(dk);
         for (int h = 0; h < Hv; ++h) {

@@ -17,7 +17,10 @@ template <int D, int KH>
 __global__ void __launch_bounds__(D) convert_kernel(const __grid_constant__ ConvertParamsPi P) {
     constexpr int kMixedBytes = 2 * KH * D + (D - KH) * D + 4 * (D - KH);
     __shared__ float red[(D / 32) * D];
-    __shared__ __align__(16) float2 sy[D];
+    __shared__ __align__(16) float scl[D];
+    __shared__ __align__(16) float nscl[D];
+    __shared__ __align__(16) float rcp[D];
+    __shared__ int flag;
     __shared__ __align__(16) uint8_t out[kMixedBytes];
     __shared__ uint8_t pi_s[D];
     const int tid = threadIdx.x, lane = tid & 31, wig = tid >> 5;
@@ -28,6 +31,7 @@ __global__ void __launch_bounds__(D) convert_kernel(const __grid_constant__ Conv
         return;
     }
     pi_s[tid] = P.pi[h * D + tid];
+    if (tid == 0) flag = 0;
     __syncthreads();
     const size_t tile = (size_t)slot * P.Hv + h;
     float2 x[D / 2];
@@ -36,7 +40,7 @@ __global__ void __launch_bounds__(D) convert_kernel(const __grid_constant__ Conv
 #pragma unroll
         for (int j = 0; j < D / 2; ++j)
             x[j] = make_float2(src[(int)pi_s[2 * j] * D + tid], src[(int)pi_s[2 * j + 1] * D + tid]);
-        mixed_requant_smem<D, KH>(x, out, red, sy, tid, lane, wig, 0, [] {});
+        mixed_requant_smem<D, KH>(x, out, red, scl, nscl, rcp, &flag, tid, lane, wig, 0, [] {});
         __syncthreads();
         uint4 *dst4 = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(P.dst) + tile * kMixedBytes);
         const uint4 *src4 = reinterpret_cast<const uint4 *>(out);

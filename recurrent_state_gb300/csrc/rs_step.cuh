@@ -9,9 +9,10 @@
 //     sequential FMA chains in ascending row order inside one thread, which
 //     reproduces the oracle's FP32 evaluation order exactly;
 //   * the decay and the rank-1 write are elementwise on registers; the column
-//     is held as row pairs, and the dequantise / requantise arithmetic of the
-//     mixed layout runs as paired FP32 instructions (mul/add/fma .f32x2), two
-//     rows per instruction, each lane rounded on its own;
+//     is held as row pairs so these, and the dequantise / requantise
+//     arithmetic of the mixed layout, run as paired FP32 instructions
+//     (mul/add/fma .f32x2), two rows per instruction, each lane rounded on
+//     its own;
 //   * a replay keeps the state on chip across tokens ("Serving recurrent
 //     attention", speculative decoding without state snapshots).
 // The tile and the token inputs arrive through a 1-D bulk TMA copy
@@ -26,11 +27,16 @@
 // FP32 scale per row are dequantised into the registers, updated in FP32, and
 // requantised in the same pass; the per-row absmax is a warp max-reduction
 // (redux.sync) plus a combine over the group's warps in shared memory.  The
-// INT8 code is round_half_even(x / s) with x / s the IEEE quotient: the
-// kernel computes q0 = x * rcp_rn(s); since |q0 - fl(x/s)| <= 3 * 2^-24 *
-// |x/s| < 2^-15 for |x/s| <= 127.0001, every q0 farther than 2^-15 from a
-// half-integer rounds like fl(x/s); the rest (about 6e-5 of the values) take
-// the exact IEEE division.
+// INT8 code is round_half_even(x / s) with x / s the IEEE quotient RN(x/s).
+// The kernel forms that quotient without a division: with y = rcp_rn(s)
+// (correctly rounded), q0 = RN(x*y), r0 = RN(x - q0*s), q1 = RN(q0 + r0*y)
+// is a faithful quotient, and one more correction r1 = RN(x - q1*s),
+// q = RN(q1 + r1*y) is exactly RN(x/s) by Markstein's theorem (P. Markstein,
+// "Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. Res. Dev. 34(1), 1990; the remainders are exact FMA
+// results).  The preconditions hold whenever |x/s| >= 1/4 (no underflow);
+// below that every quotient rounds to code 0 anyway.  Rows whose absmax is
+// not finite take the oracle's literal IEEE-division path.
 #pragma once
 
 #include <cstdint>
@@ -59,7 +65,7 @@ struct StepShape {
     __host__ __device__ static constexpr int region_bytes(int T) {
         int r = stage_bytes(T);
         r += T * kRowVecs * D * 4;
-        if (kMixed) r += kWarps * D * 4 + D * 8 + kStatePad;  // absmax partials, (s, 1/s), out tile
+        if (kMixed) r += kWarps * D * 4 + D * 12 + 128 + kStatePad;  // partials, s/-s/1/s, flag, out tile
         return (r + 127) / 128 * 128;
     }
 };
@@ -69,73 +75,88 @@ __device__ __forceinline__ void report(int32_t *status, int32_t bits) {
 }
 
 constexpr float kRound = 12582912.0f;            // 1.5 * 2^23: x + kRound - kRound = rint(x)
-constexpr float kNearHalf = 0.499969482421875f;  // 0.5 - 2^-15
+constexpr float kCodeBias = 8388736.0f;          // 2^23 + 128
 
-// Exact INT8 code for one value on the slow path (IEEE division).
+// Byte layout of a mixed tile (rows interleaved by 32-bit word inside each
+// region; see the header): FP16 value (r, c) is half ((r/2)*D + c)*2 + r%2,
+// INT8 value (r, c) is byte ((q/4)*D + c)*4 + q%4 with q = r - KH.  Thread c
+// of a group therefore moves one column of 2 FP16 rows or 4 INT8 rows with a
+// single 32-bit shared-memory access.
+
+// Exact INT8 code for one value (IEEE division), the oracle's definition.
 __device__ __forceinline__ uint32_t quant_exact(float x, float s) {
     float r = rintf(__fdiv_rn(x, s));
     r = fminf(fmaxf(r, -127.0f), 127.0f);
-    return static_cast<uint32_t>(static_cast<int32_t>(r));
+    return static_cast<uint32_t>(static_cast<int32_t>(r)) & 0xffu;
 }
 
-// INT8 codes of two values x (rows r, r+1) with scales s and reciprocals
-// y = rcp_rn(s) (NaN marks a row whose absmax is not finite).  The low byte
-// of each result is the two's-complement code.
-__device__ __forceinline__ void quant_pair(float2 x, float2 s, float2 y, uint32_t &c0,
-                                           uint32_t &c1) {
-    const float2 q0 = __fmul2_rn(x, y);
-    const float2 m = __fadd2_rn(q0, make_float2(kRound, kRound));
-    const float2 rr = __fadd2_rn(m, make_float2(-kRound, -kRound));
-    const float2 t = __ffma2_rn(rr, make_float2(-1.0f, -1.0f), q0);  // q0 - rint(q0), exact
-    float tm;
-    asm("max.NaN.f32 %0, %1, %2;" : "=f"(tm) : "f"(fabsf(t.x)), "f"(fabsf(t.y)));
-    if (tm < kNearHalf) {
-        c0 = __float_as_uint(m.x);
-        c1 = __float_as_uint(m.y);
-    } else {
-        c0 = quant_exact(x.x, s.x);
-        c1 = quant_exact(x.y, s.y);
-    }
+// INT8 codes of four values (one column of rows 4q..4q+3) of finite rows
+// with scales s, negated scales ns = -s and reciprocals y = rcp_rn(s):
+// q = RN(x/s) by two FMA corrections (see the top of this file), then
+// round-half-even through the 1.5 * 2^23 addend; the low byte of each sum is
+// the two's-complement code.  |q| <= 127.00002, so no clamp is needed.
+__device__ __forceinline__ uint32_t quant_quad(float2 x01, float2 x23, float4 ns, float4 y) {
+    const float2 y01 = make_float2(y.x, y.y), y23 = make_float2(y.z, y.w);
+    const float2 n01 = make_float2(ns.x, ns.y), n23 = make_float2(ns.z, ns.w);
+    float2 q01 = __fmul2_rn(x01, y01);
+    float2 q23 = __fmul2_rn(x23, y23);
+    q01 = __ffma2_rn(__ffma2_rn(q01, n01, x01), y01, q01);
+    q23 = __ffma2_rn(__ffma2_rn(q23, n23, x23), y23, q23);
+    q01 = __ffma2_rn(__ffma2_rn(q01, n01, x01), y01, q01);
+    q23 = __ffma2_rn(__ffma2_rn(q23, n23, x23), y23, q23);
+    const float2 m01 = __fadd2_rn(q01, make_float2(kRound, kRound));
+    const float2 m23 = __fadd2_rn(q23, make_float2(kRound, kRound));
+    const uint32_t lo2 = __byte_perm(__float_as_uint(m01.x), __float_as_uint(m01.y), 0x0040);
+    const uint32_t hi2 = __byte_perm(__float_as_uint(m23.x), __float_as_uint(m23.y), 0x0040);
+    return __byte_perm(lo2, hi2, 0x5410);
+}
+
+__device__ __forceinline__ uint32_t quant_quad_exact(float2 x01, float2 x23, float4 s) {
+    return quant_exact(x01.x, s.x) | (quant_exact(x01.y, s.y) << 8) |
+           (quant_exact(x23.x, s.z) << 16) | (quant_exact(x23.y, s.w) << 24);
 }
 
 // Dequantise column tid of a mixed tile (shared or global memory) into row
-// pairs xs[j] = rows (2j, 2j+1).  int8 -> float uses the exact magic-number
-// form (c + 0x4B400000 as float) - 1.5 * 2^23 instead of a conversion.
+// pairs xs[j] = rows (2j, 2j+1).  int8 -> float is exact without a
+// conversion instruction: the code byte, offset by 128, becomes the low
+// mantissa byte of 2^23 and the bias is subtracted.
 template <int D, int KH>
 __device__ __forceinline__ void mixed_dequant(const uint8_t *tile, int tid, float2 (&xs)[D / 2]) {
-    const __half *hi = reinterpret_cast<const __half *>(tile);
-    const int8_t *lo = reinterpret_cast<const int8_t *>(tile + 2 * KH * D);
+    const __half2 *hi = reinterpret_cast<const __half2 *>(tile);
+    const uint32_t *lo = reinterpret_cast<const uint32_t *>(tile + 2 * KH * D);
     const float4 *sc4 = reinterpret_cast<const float4 *>(tile + 2 * KH * D + (D - KH) * D);
 #pragma unroll
-    for (int j = 0; j < KH / 2; ++j)
-        xs[j] = make_float2(__half2float(hi[(2 * j) * D + tid]), __half2float(hi[(2 * j + 1) * D + tid]));
+    for (int j = 0; j < KH / 2; ++j) xs[j] = __half22float2(hi[j * D + tid]);
 #pragma unroll
-    for (int j = KH / 2; j < D / 2; j += 2) {  // four INT8 rows per step: one float4 of scales
-        const int r = 2 * j - KH;
-        const float4 s4 = sc4[r / 4];
-        const int c0 = lo[(r + 0) * D + tid], c1 = lo[(r + 1) * D + tid];
-        const int c2 = lo[(r + 2) * D + tid], c3 = lo[(r + 3) * D + tid];
-        const float2 f01 = __fadd2_rn(make_float2(__int_as_float(c0 + 0x4B400000), __int_as_float(c1 + 0x4B400000)),
-                                      make_float2(-kRound, -kRound));
-        const float2 f23 = __fadd2_rn(make_float2(__int_as_float(c2 + 0x4B400000), __int_as_float(c3 + 0x4B400000)),
-                                      make_float2(-kRound, -kRound));
-        xs[j] = __fmul2_rn(f01, make_float2(s4.x, s4.y));
-        xs[j + 1] = __fmul2_rn(f23, make_float2(s4.z, s4.w));
+    for (int qd = 0; qd < (D - KH) / 4; ++qd) {
+        const uint32_t w = lo[qd * D + tid] ^ 0x80808080u;
+        const float4 s4 = sc4[qd];
+        const float f0 = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540));
+        const float f1 = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7541));
+        const float f2 = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7542));
+        const float f3 = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7543));
+        const float2 c01 = __fadd2_rn(make_float2(f0, f1), make_float2(-kCodeBias, -kCodeBias));
+        const float2 c23 = __fadd2_rn(make_float2(f2, f3), make_float2(-kCodeBias, -kCodeBias));
+        xs[KH / 2 + 2 * qd] = __fmul2_rn(c01, make_float2(s4.x, s4.y));
+        xs[KH / 2 + 2 * qd + 1] = __fmul2_rn(c23, make_float2(s4.z, s4.w));
     }
 }
 
 // Requantise the FP32 column (row pairs xs, thread tid of a group of D
 // threads, warp wig, lane lane) into a mixed tile assembled at `out` in
-// shared memory (same byte layout as a pool tile).  red ([D/32][D] floats)
-// and sy ([D] float2) are group-private scratch; bar_id/D name the group
-// barrier.  `before_write` runs on every thread after the absmax phase and
-// before the group barrier that precedes the first write into `out`.
-// Matches the oracle's quantiser bit for bit.
+// shared memory (same byte layout as a pool tile).  red ([D/32][D] floats),
+// sc, nsc and rc ([D] floats each: row scale, its negation, its reciprocal)
+// and flag (one int, zero on entry) are group-private scratch; bar_id/D name
+// the group barrier.  `before_write`
+// runs on every thread after the absmax phase and before the group barrier
+// that precedes the first write into `out`.  Bit-exact with the oracle.
 template <int D, int KH, typename F>
 __device__ __forceinline__ void mixed_requant_smem(const float2 (&xs)[D / 2], uint8_t *out, float *red,
-                                                   float2 *sy, int tid, int lane, int wig,
-                                                   uint32_t bar_id, F before_write) {
+                                                   float *sc, float *nsc, float *rc, int *flag,
+                                                   int tid, int lane, int wig, uint32_t bar_id,
+                                                   F before_write) {
     constexpr int W = D / 32;
+    constexpr int NQ = (D - KH) / 4;
     static_assert(KH % 4 == 0 && (D - KH) % 4 == 0, "row blocks of four");
     // per-row absmax: one warp max-reduction per row; lane (r & 31) keeps row r
     float mine[D / 32];
@@ -159,26 +180,38 @@ __device__ __forceinline__ void mixed_requant_smem(const float2 (&xs)[D / 2], ui
         for (int w = 1; w < W; ++w) ab = max(ab, __float_as_uint(red[w * D + tid]));
         const float a = __uint_as_float(ab);  // >= 0, or NaN (largest bit pattern)
         const float s = __fdiv_rn(fmaxf(a, 1e-8f), 127.0f);
-        const bool finite = ab < 0x7f800000u;
-        sy[tid] = make_float2(s, finite ? __frcp_rn(s) : __int_as_float(0x7fc00000));
+        sc[tid] = s;
+        nsc[tid] = -s;
+        rc[tid] = __frcp_rn(s);
+        if (ab >= 0x7f800000u) *flag = 1;  // absmax inf or NaN: exact path for the tile
         reinterpret_cast<float *>(out + 2 * KH * D + (D - KH) * D)[tid - KH] = s;
     }
     group_sync(bar_id, D);
-    __half *hi = reinterpret_cast<__half *>(out);
+    __half2 *hi = reinterpret_cast<__half2 *>(out);
 #pragma unroll
-    for (int j = 0; j < KH / 2; ++j) {
-        hi[(2 * j) * D + tid] = __float2half_rn(xs[j].x);
-        hi[(2 * j + 1) * D + tid] = __float2half_rn(xs[j].y);
-    }
-    uint8_t *lo = out + 2 * KH * D;
-    const float4 *sy4 = reinterpret_cast<const float4 *>(sy);
+    for (int j = 0; j < KH / 2; ++j) hi[j * D + tid] = __floats2half2_rn(xs[j].x, xs[j].y);
+    uint32_t *lo = reinterpret_cast<uint32_t *>(out + 2 * KH * D);
+    if (*flag == 0) {
+        const float4 *rc4 = reinterpret_cast<const float4 *>(rc + KH);
+        const float4 *ns4 = reinterpret_cast<const float4 *>(nsc + KH);
 #pragma unroll
-    for (int j = KH / 2; j < D / 2; ++j) {
-        const float4 v = sy4[j];  // s_r, y_r, s_{r+1}, y_{r+1} for r = 2j
-        uint32_t c0, c1;
-        quant_pair(xs[j], make_float2(v.x, v.z), make_float2(v.y, v.w), c0, c1);
-        lo[(2 * j - KH) * D + tid] = static_cast<uint8_t>(c0 & 0xffu);
-        lo[(2 * j + 1 - KH) * D + tid] = static_cast<uint8_t>(c1 & 0xffu);
+        for (int qd = 0; qd < NQ; ++qd)
+            lo[qd * D + tid] = quant_quad(xs[KH / 2 + 2 * qd], xs[KH / 2 + 2 * qd + 1], ns4[qd], rc4[qd]);
+    } else {
+        const float4 *sc4 = reinterpret_cast<const float4 *>(sc + KH);
+#pragma unroll 1
+        for (int qd = 0; qd < NQ; ++qd) {
+            // dynamic row index: this cold path reads the column back from
+            // the scratch copy instead of indexing the register array
+            float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int k = 0; k < NQ; ++k)
+                if (k == qd) {
+                    a01 = xs[KH / 2 + 2 * k];
+                    a23 = xs[KH / 2 + 2 * k + 1];
+                }
+            lo[qd * D + tid] = quant_quad_exact(a01, a23, sc4[qd]);
+        }
     }
 }
 
@@ -206,8 +239,11 @@ __global__ void __launch_bounds__(kStepThreads, 1)
     float *rowv = reinterpret_cast<float *>(region + S::stage_bytes(T));
     // rowv layout per token t: [K | BK | Q | V | A?] each D floats
     float *red = rowv + T * S::kRowVecs * D;                        // [kWarps][D]   (mixed)
-    float2 *sy = reinterpret_cast<float2 *>(red + S::kWarps * D);   // [D]           (mixed)
-    uint8_t *outt = reinterpret_cast<uint8_t *>(sy + D);            // out tile      (mixed)
+    float *scl = red + S::kWarps * D;                               // [D] row scales
+    float *nscl = scl + D;                                          // [D] -scales
+    float *rcp = nscl + D;                                          // [D] reciprocals
+    int *flag = reinterpret_cast<int *>(rcp + D);                   // non-finite row seen
+    uint8_t *outt = reinterpret_cast<uint8_t *>(rcp + D + 32);      // out tile      (mixed)
 
     if (threadIdx.x < G) mbar_init(&bars[threadIdx.x], 1);
     if constexpr (MIXED)
@@ -346,13 +382,11 @@ __global__ void __launch_bounds__(kStepThreads, 1)
                 float4 aa;
                 if (KDA) aa = *reinterpret_cast<const float4 *>(rv + 4 * D + 2 * j);
                 else aa = make_float4(a_s, a_s, a_s, a_s);
-                x[j].x = __fmul_rn(x[j].x, aa.x);
+                x[j] = __fmul2_rn(x[j], make_float2(aa.x, aa.y));
+                x[j + 1] = __fmul2_rn(x[j + 1], make_float2(aa.z, aa.w));
                 p = __fmaf_rn(x[j].x, kk.x, p);
-                x[j].y = __fmul_rn(x[j].y, aa.y);
                 p = __fmaf_rn(x[j].y, kk.y, p);
-                x[j + 1].x = __fmul_rn(x[j + 1].x, aa.z);
                 p = __fmaf_rn(x[j + 1].x, kk.z, p);
-                x[j + 1].y = __fmul_rn(x[j + 1].y, aa.w);
                 p = __fmaf_rn(x[j + 1].y, kk.w, p);
             }
             const float e = __fsub_rn(rv[3 * D + tid], p);
@@ -362,13 +396,11 @@ __global__ void __launch_bounds__(kStepThreads, 1)
             for (int j = 0; j < DP; j += 2) {
                 const float4 bk = *reinterpret_cast<const float4 *>(rv + D + 2 * j);
                 const float4 qq = *reinterpret_cast<const float4 *>(rv + 2 * D + 2 * j);
-                x[j].x = __fmaf_rn(bk.x, e, x[j].x);
+                x[j] = __ffma2_rn(make_float2(bk.x, bk.y), make_float2(e, e), x[j]);
+                x[j + 1] = __ffma2_rn(make_float2(bk.z, bk.w), make_float2(e, e), x[j + 1]);
                 o = __fmaf_rn(x[j].x, qq.x, o);
-                x[j].y = __fmaf_rn(bk.y, e, x[j].y);
                 o = __fmaf_rn(x[j].y, qq.y, o);
-                x[j + 1].x = __fmaf_rn(bk.z, e, x[j + 1].x);
                 o = __fmaf_rn(x[j + 1].x, qq.z, o);
-                x[j + 1].y = __fmaf_rn(bk.w, e, x[j + 1].y);
                 o = __fmaf_rn(x[j + 1].y, qq.w, o);
             }
             if (P.o) {
@@ -387,8 +419,11 @@ __global__ void __launch_bounds__(kStepThreads, 1)
                 st[(2 * j + 1) * D + tid] = x[j].y;
             }
         } else {
-            mixed_requant_smem<D, KH>(x, outt, red, sy, tid, lane, wig, bar_id, [&] {
-                if (tid == 0) bulk_store_wait_read();  // the previous tile's store has read `outt`
+            mixed_requant_smem<D, KH>(x, outt, red, scl, nscl, rcp, flag, tid, lane, wig, bar_id, [&] {
+                if (tid == 0) {
+                    bulk_store_wait_read();  // the previous tile's store has read `outt`
+                    *flag = 0;
+                }
             });
             fence_proxy_async_smem();  // this thread's writes to `outt` before the bulk store
             group_sync(bar_id, D);

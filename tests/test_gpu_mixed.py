@@ -186,3 +186,51 @@ def test_replay_bad_accept_count_reported():
     after = host(pool)
     for b in (1, 2):
         assert same_bits(after[w.slot_idx[b]], before[w.slot_idx[b]])
+
+
+def adversarial_rows(n_heads, seed):
+    """FP32 heads whose INT8 rows put many x/s within a few ulps of, or
+    exactly on, a half-integer (x = (n + 1/2) s nudged by 0..3 ulps; scales
+    that are powers of two give exact ties), plus rows holding NaN / inf."""
+    g = gen.rng(seed)
+    S = np.zeros((n_heads, D, D), np.float32)
+    for h in range(n_heads):
+        for r in range(D):
+            e = int(g.integers(-20, 4))
+            a = np.float32(127.0 * 2.0 ** e) if r % 3 == 0 else np.float32(g.uniform(0.05, 3.0))
+            s = np.float32(np.float32(max(a, np.float32(1e-8))) / np.float32(127.0))
+            n = g.integers(-126, 126, D).astype(np.float32)
+            x = ((n + np.float32(0.5)) * s).astype(np.float32)
+            nudge = g.integers(-3, 4, D)
+            x = np.array([np.nextafter(xi, np.float32(np.inf) if k > 0 else np.float32(-np.inf))
+                          if k else xi for xi, k in zip(x, nudge)], np.float32)
+            for _ in range(2):
+                x = np.where(nudge > 1, np.nextafter(x, np.float32(np.inf)), x)
+                x = np.where(nudge < -1, np.nextafter(x, np.float32(-np.inf)), x)
+            x[0] = a                      # the row's absmax
+            x = np.clip(x, -a, a).astype(np.float32)
+            S[h, r] = x
+    S[0, 20, 5] = np.nan
+    S[0, 21, 7] = np.inf
+    S[0, 22, 9] = -np.inf
+    S[0, 22, 10] = np.nan
+    S[1, 40, :] = 0.0
+    return S
+
+
+def test_quantiser_rounding_near_half_integers():
+    Hv = 4
+    f32, mix, pi = layouts(Hv, Hv, seed=12)
+    state = adversarial_rows(3 * Hv, 12).reshape(3, Hv, D, D)
+    g = host(to_mixed_gpu(f32, mix, state))
+    ref = orc.convert_pool_f32_to_mixed(state, KHI, pi)
+    # INT8 codes and scales: every byte.  FP16 rows: every bit, except that a
+    # NaN only has to stay a NaN (its payload bits are not part of the format).
+    hb = 2 * KHI * D
+    assert same_bits(g[..., hb:], ref[..., hb:])
+    hg = g[..., :hb].copy().view(np.float16)
+    hr = ref[..., :hb].copy().view(np.float16)
+    nan = np.isnan(hr)
+    assert np.array_equal(np.isnan(hg), nan)
+    assert np.array_equal(hg.view(np.uint16)[~nan], hr.view(np.uint16)[~nan])
+    assert nan.sum() >= 1  # the NaN planted in an FP16 row survives

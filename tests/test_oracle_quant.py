@@ -80,33 +80,54 @@ def test_nan_row_reading():
     assert codes.tolist() == [127, -127, -25, 0]
 
 
+def hi_region(tile, khi, dv):
+    """FP16 rows [khi][dv] from the FP16 region (row pairs interleaved)."""
+    h = tile[: 2 * khi * dv].view(np.uint16).reshape(khi // 2, dv, 2)
+    return np.ascontiguousarray(h.transpose(0, 2, 1).reshape(khi, dv))
+
+
+def lo_region(tile, dk, khi, dv):
+    """INT8 rows [dk-khi][dv] from the INT8 region (row quads interleaved)."""
+    n = (dk - khi) * dv
+    b = tile[2 * khi * dv: 2 * khi * dv + n].view(np.int8).reshape((dk - khi) // 4, dv, 4)
+    return np.ascontiguousarray(b.transpose(0, 2, 1).reshape(dk - khi, dv))
+
+
 def test_fp16_rows_match_ieee_half():
     """FP16 rows round to nearest even like numpy's IEEE float16 conversion."""
     g = gen.rng(13)
-    dk, dv, khi = 8, 32, 3
+    dk, dv, khi = 8, 32, 4
     T = (g.standard_normal((dk, dv)) * 10.0 ** g.uniform(-3, 4, (dk, 1))).astype(np.float32)
     T[0, :4] = [65504.0, 65520.0, -70000.0, 6e-8]  # max, overflow to inf, tiny
     tile = orc.mixed_pack(T, khi)
-    hi = tile[: 2 * khi * dv].view(np.uint16).reshape(khi, dv)
+    hi = hi_region(tile, khi, dv)
     assert np.array_equal(hi, T[:khi].astype(np.float16).view(np.uint16))
     back = orc.mixed_unpack(tile, dk, dv, khi)
     assert np.array_equal(back[:khi], T[:khi].astype(np.float16).astype(np.float32))
 
 
 def test_mixed_tile_layout_and_size():
-    """16 FP16 rows + 112 INT8 rows + 112 FP32 row scales at d = 128."""
+    """16 FP16 rows + 112 INT8 rows + 112 FP32 row scales at d = 128; inside
+    the regions, one 32-bit word holds one column of 2 FP16 rows or of 4
+    INT8 rows."""
     dk = dv = 128
     khi = 16
     assert orc.mixed_tile_bytes(dk, dv, khi) == 16 * 128 * 2 + 112 * 128 + 112 * 4 == 18880
     g = gen.rng(14)
     T = g.standard_normal((dk, dv)).astype(np.float32)
     tile = orc.mixed_pack(T, khi)
-    lo = tile[4096:4096 + 112 * 128].view(np.int8).reshape(112, 128)
+    lo = lo_region(tile, dk, khi, dv)
     sc = tile[4096 + 112 * 128:].view(np.float32)
     for r in range(khi, dk):
         c, s = orc.quantise_row(T[r])
         assert np.array_equal(lo[r - khi], c)
         assert sc[r - khi] == s
+    # the word holding column 5 of INT8 rows khi+4 .. khi+7
+    w = tile[4096 + (1 * 128 + 5) * 4: 4096 + (1 * 128 + 5) * 4 + 4].view(np.int8)
+    assert np.array_equal(w, lo[4:8, 5])
+    # the word holding column 9 of FP16 rows 2, 3
+    hw = tile[(1 * 128 + 9) * 4: (1 * 128 + 9) * 4 + 4].view(np.uint16)
+    assert np.array_equal(hw, T[2:4, 9].astype(np.float16).view(np.uint16))
 
 
 def test_convert_places_logical_rows():
