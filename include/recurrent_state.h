@@ -263,6 +263,29 @@ rs_status rs_ckpt_restore(const rs_plan *p, const void *ckpt_pool, int64_t n_ckp
                           const int32_t *dst_slots, int32_t n, int32_t *status,
                           void *stream);
 
+/* Pack for callers that cannot allocate device memory.  The pages have no
+ * counterpart to this call; it exists for integrations such as a serving
+ * engine that reserves a fixed share of HBM for its own pools when it starts
+ * and must not allocate afterwards, or a caller on a latency-critical path
+ * that cannot afford the device-wide synchronisation of cudaFree.
+ * Same arguments, layout and result as rs_ckpt_pack, but the plan needs no
+ * rs_plan_upload: the plan's index table is copied (cudaMemcpyAsync on
+ * `stream`) into a fixed array that the library holds in device memory, and
+ * nothing is allocated or freed.  Limits and behaviour:
+ *   - the plan may retain at most 262,144 units per checkpoint (o_L); a
+ *     larger plan returns RS_ERR_UNSUPPORTED before any work;
+ *   - the array (1 MiB) lives on every GPU that loads the library until the
+ *     process exits;
+ *   - the first call on a device looks up the array's device address; make
+ *     that first call before any stream capture begins;
+ *   - all calls share the one array, which keeps the last call's table:
+ *     calls whose work overlaps on the GPU (on different streams) race and
+ *     must be ordered by the caller. */
+rs_status rs_ckpt_pack_noalloc(const rs_plan *p, const void *pool, int64_t layer_stride_bytes,
+                               int64_t n_pool_slots, const int32_t *src_slots,
+                               const int32_t *dst_ckpt_slots, int32_t n, void *ckpt_pool,
+                               int64_t n_ckpt_slots, int32_t *status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

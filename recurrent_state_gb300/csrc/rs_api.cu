@@ -20,17 +20,6 @@ struct rs_layout {
     size_t head_bytes;
 };
 
-struct rs_plan {
-    int32_t L, unit, Hv, dk, dv, nu;
-    size_t head_bytes;
-    int64_t unit_bytes;
-    std::vector<int64_t> offsets;     // o_0..o_L
-    std::vector<int32_t> kept_unit;   // packed order: (layer << 20) | unit
-    std::vector<int32_t> all_pidx;    // [L * nu]: packed index or -1
-    int device = -1;
-    int32_t *d_kept = nullptr;
-    int32_t *d_all = nullptr;
-};
 
 namespace {
 
