@@ -349,7 +349,7 @@ def _time(torch, fn, iters, warm=3):
     return e0.elapsed_time(e1) / 1e3 / iters
 
 
-EXTRA = ("kda_fp32", "kda_mixed", "gdn_mixed", "replay_mixed", "replay_fp32",
+EXTRA = ("gdn_fp32", "kda_fp32", "kda_mixed", "gdn_mixed", "replay_mixed", "replay_fp32",
          "pack_gdn", "restore_gdn", "pack_kda", "restore_kda")
 
 
@@ -373,60 +373,78 @@ def extra_kernels(args, rs, torch, dev, peak, world, only=None):
         if extra:
             out[name].update(extra)
 
+    B = getattr(args, "batch", None) or 256
+    if "gdn_fp32" in want:
+        nsteps = 8
+        g_cfg = dict(GDN, B=B)
+        w = gen.decode_workload(steps=nsteps, per_channel=False, in_dtype="bf16", seed=2, **g_cfg)
+        lay = rs.Layout("fp32", 128, GDN["Hv"], GDN["Hk"])
+        pool = to_dev(w.state0)
+        q, k, v = to_bf16(w.q_bits), to_bf16(w.k_bits), to_bf16(w.v_bits)
+        al, be, slots = to_dev(w.alpha), to_dev(w.beta), to_dev(w.slot_idx)
+        o = torch.empty((B, GDN["Hv"], 128), device=dev)
+        sec = _time(torch, lambda i: rs.gdn_decode_update(
+            lay, pool, slots, q[i % nsteps], k[i % nsteps], v[i % nsteps], al[i % nsteps],
+            be[i % nsteps], o=o), iters, warm)
+        rec(f"gdn_decode_fp32_b{B}", sec, decode_bytes(B, 16, 32, 128, lay.head_bytes, 2, False),
+            B * 32)
+        del pool, q, k, v
+        torch.cuda.empty_cache()
+    KDA_B = dict(KDA, B=B)
     if want & {"kda_fp32", "kda_mixed", "gdn_mixed", "replay_mixed", "replay_fp32"}:
         nsteps = 8
         w = gen.decode_workload(steps=nsteps, per_channel=True, in_dtype="bf16", seed=1,
-                                horizon=(2.0, 8192.0), **KDA)
+                                horizon=(2.0, 8192.0), **KDA_B)
         q, k, v = to_bf16(w.q_bits), to_bf16(w.k_bits), to_bf16(w.v_bits)
         al, be = to_dev(w.alpha), to_dev(w.beta)
         slots = to_dev(w.slot_idx)
-        o = torch.empty((KDA["B"], KDA["Hv"], KDA["d"]), device=dev)
+        o = torch.empty((B, KDA["Hv"], KDA["d"]), device=dev)
         f32 = rs.Layout("fp32", 128, KDA["Hv"], KDA["Hk"])
         hi = gen.hi_rows(KDA["Hv"], 128, 16, seed=1)
         mix = rs.Layout("mixed", 128, KDA["Hv"], KDA["Hk"], k_hi=16, hi_rows=hi)
         pool = to_dev(w.state0)
-        mpool = mix.empty_pool(KDA["B"], device=dev)
-        rs.state_convert(f32, pool, mix, mpool, torch.arange(KDA["B"], dtype=torch.int32, device=dev))
+        mpool = mix.empty_pool(B, device=dev)
+        rs.state_convert(f32, pool, mix, mpool, torch.arange(B, dtype=torch.int32, device=dev))
         if "kda_fp32" in want:
             sec = _time(torch, lambda i: rs.kda_decode_update(
                 f32, pool, slots, q[i % nsteps], k[i % nsteps], v[i % nsteps], al[i % nsteps],
                 be[i % nsteps], o=o), iters, warm)
-            rec("kda_decode_fp32_b256", sec, decode_bytes(256, 32, 32, 128, f32.head_bytes, 2, True),
-                256 * 32)
+            rec(f"kda_decode_fp32_b{B}", sec, decode_bytes(B, 32, 32, 128, f32.head_bytes, 2, True),
+                B * 32)
         if "kda_mixed" in want:
             sec = _time(torch, lambda i: rs.kda_decode_update(
                 mix, mpool, slots, q[i % nsteps], k[i % nsteps], v[i % nsteps], al[i % nsteps],
                 be[i % nsteps], o=o), iters, warm)
-            rec("kda_decode_mixed_b256", sec, decode_bytes(256, 32, 32, 128, mix.head_bytes, 2, True),
-                256 * 32)
+            rec(f"kda_decode_mixed_b{B}", sec, decode_bytes(B, 32, 32, 128, mix.head_bytes, 2, True),
+                B * 32)
         if "gdn_mixed" in want:
             al_g = al[..., 0].contiguous()  # one decay per (sequence, head) for the GDN form
             sec = _time(torch, lambda i: rs.gdn_decode_update(
                 mix, mpool, slots, q[i % nsteps], k[i % nsteps], v[i % nsteps], al_g[i % nsteps],
                 be[i % nsteps], o=o), iters, warm)
-            rec("gdn_decode_mixed_b256_h32", sec,
-                decode_bytes(256, 32, 32, 128, mix.head_bytes, 2, False), 256 * 32)
+            rec(f"gdn_decode_mixed_b{B}_h32", sec,
+                decode_bytes(B, 32, 32, 128, mix.head_bytes, 2, False), B * 32)
         if want & {"replay_mixed", "replay_fp32"}:
             T = 8
-            n_acc = gen.n_accept(256, T, seed=1)
+            n_acc = gen.n_accept(B, T, seed=1)
             tok = int(n_acc.sum())
 
             def bt(x):
                 return np.ascontiguousarray(np.swapaxes(x[:T], 0, 1))
             rq, rk, rv = to_bf16(bt(w.q_bits)), to_bf16(bt(w.k_bits)), to_bf16(bt(w.v_bits))
             ra, rb = to_dev(bt(w.alpha)), to_dev(bt(w.beta))
-            ro = torch.empty((256, T, 32, 128), device=dev)
+            ro = torch.empty((B, T, 32, 128), device=dev)
             nd = to_dev(n_acc)
             per_tok = 2 * 32 * 128 * 2 + 32 * 128 * 2 + 32 * 128 * 4 + 32 * 4 + 32 * 128 * 4
             if "replay_mixed" in want:
                 sec = _time(torch, lambda i: rs.spec_replay_update(
                     mix, True, mpool, slots, nd, rq, rk, rv, ra, rb, o=ro), iters, warm)
-                rec("kda_replay_mixed_b256_T8", sec, 2 * 256 * 32 * mix.head_bytes + tok * per_tok,
+                rec(f"kda_replay_mixed_b{B}_T8", sec, 2 * B * 32 * mix.head_bytes + tok * per_tok,
                     tok * 32, {"accepted_tokens": tok, "n_accept": "uniform 1..8"})
             if "replay_fp32" in want:
                 sec = _time(torch, lambda i: rs.spec_replay_update(
                     f32, True, pool, slots, nd, rq, rk, rv, ra, rb, o=ro), iters, warm)
-                rec("kda_replay_fp32_b256_T8", sec, 2 * 256 * 32 * f32.head_bytes + tok * per_tok,
+                rec(f"kda_replay_fp32_b{B}_T8", sec, 2 * B * 32 * f32.head_bytes + tok * per_tok,
                     tok * 32, {"accepted_tokens": tok})
         del pool, mpool
         torch.cuda.empty_cache()
@@ -435,7 +453,8 @@ def extra_kernels(args, rs, torch, dev, peak, world, only=None):
     for unit, p, name in ((0, 0.5, "gdn"), (1, 0.45, "kda")):
         if not want & {f"pack_{name}", f"restore_{name}"}:
             continue
-        L, nslot, Hv, d, n = 36, 64, 32, 128, 64
+        nslot = n = getattr(args, "slots", None) or 64
+        L, Hv, d = 36, 32, 128
         keep = gen.keep_mask(L, Hv if unit == 0 else Hv * d, p, seed=unit)
         src, dst = gen.ckpt_slots(nslot, n, seed=unit)
         lay = rs.Layout("fp32", d, Hv, 1)
@@ -495,6 +514,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--skip-extra", action="store_true", help="headline workload only")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="batch of the decode kernels in --only mode (default 256)")
+    ap.add_argument("--slots", type=int, default=None,
+                    help="pool slots and checkpoints of the pack/restore kernels (default 64)")
     ap.add_argument("--only", default=None,
                     help="comma list of secondary kernels to time alone (" + ",".join(EXTRA) + ")")
     args = ap.parse_args()

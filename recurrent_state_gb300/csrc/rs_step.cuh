@@ -142,33 +142,32 @@ __device__ __forceinline__ void mixed_dequant(const uint8_t *tile, int tid, floa
     }
 }
 
+// Per-row absmax bookkeeping: after a warp max-reduction of rows 2j and
+// 2j+1, lane (r & 31) keeps the maximum of row r in mine[r >> 5].
+template <int D>
+__device__ __forceinline__ void absmax_pair(float2 xv, int j, int lane, float (&mine)[D / 32]) {
+    const float m0 = warp_max_abs_nan(xv.x);
+    const float m1 = warp_max_abs_nan(xv.y);
+    mine[(2 * j) >> 5] = lane == ((2 * j) & 31) ? m0 : mine[(2 * j) >> 5];
+    mine[(2 * j + 1) >> 5] = lane == ((2 * j + 1) & 31) ? m1 : mine[(2 * j + 1) >> 5];
+}
+
 // Requantise the FP32 column (row pairs xs, thread tid of a group of D
 // threads, warp wig, lane lane) into a mixed tile assembled at `out` in
-// shared memory (same byte layout as a pool tile).  red ([D/32][D] floats),
-// sc, nsc and rc ([D] floats each: row scale, its negation, its reciprocal)
-// and flag (one int, zero on entry) are group-private scratch; bar_id/D name
-// the group barrier.  `before_write`
-// runs on every thread after the absmax phase and before the group barrier
+// shared memory (same byte layout as a pool tile), given the warp's per-row
+// maxima in mine (see absmax_pair).  red ([D/32][D] floats), sc, nsc and rc
+// ([D] floats each: row scale, its negation, its reciprocal) and flag (one
+// int, zero on entry) are group-private scratch; bar_id/D name the group
+// barrier.  `before_write` runs on every thread before the group barrier
 // that precedes the first write into `out`.  Bit-exact with the oracle.
 template <int D, int KH, typename F>
-__device__ __forceinline__ void mixed_requant_smem(const float2 (&xs)[D / 2], uint8_t *out, float *red,
-                                                   float *sc, float *nsc, float *rc, int *flag,
-                                                   int tid, int lane, int wig, uint32_t bar_id,
-                                                   F before_write) {
+__device__ __forceinline__ void mixed_requant_from_max(const float2 (&xs)[D / 2], const float (&mine)[D / 32],
+                                                       uint8_t *out, float *red, float *sc, float *nsc,
+                                                       float *rc, int *flag, int tid, int lane, int wig,
+                                                       uint32_t bar_id, F before_write) {
     constexpr int W = D / 32;
     constexpr int NQ = (D - KH) / 4;
     static_assert(KH % 4 == 0 && (D - KH) % 4 == 0, "row blocks of four");
-    // per-row absmax: one warp max-reduction per row; lane (r & 31) keeps row r
-    float mine[D / 32];
-#pragma unroll
-    for (int k = 0; k < D / 32; ++k) mine[k] = 0.0f;
-#pragma unroll
-    for (int j = KH / 2; j < D / 2; ++j) {
-        const float m0 = warp_max_abs_nan(xs[j].x);
-        const float m1 = warp_max_abs_nan(xs[j].y);
-        if (lane == ((2 * j) & 31)) mine[(2 * j) >> 5] = m0;
-        if (lane == ((2 * j + 1) & 31)) mine[(2 * j + 1) >> 5] = m1;
-    }
 #pragma unroll
     for (int k = 0; k < D / 32; ++k)
         if (32 * k + lane >= KH) red[wig * D + 32 * k + lane] = mine[k];
@@ -201,8 +200,8 @@ __device__ __forceinline__ void mixed_requant_smem(const float2 (&xs)[D / 2], ui
         const float4 *sc4 = reinterpret_cast<const float4 *>(sc + KH);
 #pragma unroll 1
         for (int qd = 0; qd < NQ; ++qd) {
-            // dynamic row index: this cold path reads the column back from
-            // the scratch copy instead of indexing the register array
+            // dynamic quad index on this cold path: select the pair from the
+            // register array without indexing it dynamically
             float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int k = 0; k < NQ; ++k)
@@ -212,6 +211,48 @@ __device__ __forceinline__ void mixed_requant_smem(const float2 (&xs)[D / 2], ui
                 }
             lo[qd * D + tid] = quant_quad_exact(a01, a23, sc4[qd]);
         }
+    }
+}
+
+// Same, collecting the per-row maxima first (for callers that did not fuse
+// the reductions into the update pass).
+template <int D, int KH, typename F>
+__device__ __forceinline__ void mixed_requant_smem(const float2 (&xs)[D / 2], uint8_t *out, float *red,
+                                                   float *sc, float *nsc, float *rc, int *flag,
+                                                   int tid, int lane, int wig, uint32_t bar_id,
+                                                   F before_write) {
+    float mine[D / 32];
+#pragma unroll
+    for (int k = 0; k < D / 32; ++k) mine[k] = 0.0f;
+#pragma unroll
+    for (int j = KH / 2; j < D / 2; ++j) absmax_pair<D>(xs[j], j, lane, mine);
+    mixed_requant_from_max<D, KH>(xs, mine, out, red, sc, nsc, rc, flag, tid, lane, wig, bar_id,
+                                  before_write);
+}
+
+// Dequantise rows 4q..4q+3 (q counted from row 0) of column tid of a mixed
+// tile into two row pairs.
+template <int D, int KH>
+__device__ __forceinline__ void mixed_dequant_quad(const uint8_t *tile, int q, int tid, float2 &x01,
+                                                   float2 &x23) {
+    if (4 * q < KH) {
+        const __half2 *hi = reinterpret_cast<const __half2 *>(tile);
+        x01 = __half22float2(hi[(2 * q) * D + tid]);
+        x23 = __half22float2(hi[(2 * q + 1) * D + tid]);
+    } else {
+        const int qd = q - KH / 4;
+        const uint32_t *lo = reinterpret_cast<const uint32_t *>(tile + 2 * KH * D);
+        const float4 *sc4 = reinterpret_cast<const float4 *>(tile + 2 * KH * D + (D - KH) * D);
+        const uint32_t w = lo[qd * D + tid] ^ 0x80808080u;
+        const float4 s4 = sc4[qd];
+        const float f0 = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540));
+        const float f1 = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7541));
+        const float f2 = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7542));
+        const float f3 = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7543));
+        x01 = __fmul2_rn(__fadd2_rn(make_float2(f0, f1), make_float2(-kCodeBias, -kCodeBias)),
+                         make_float2(s4.x, s4.y));
+        x23 = __fmul2_rn(__fadd2_rn(make_float2(f2, f3), make_float2(-kCodeBias, -kCodeBias)),
+                         make_float2(s4.z, s4.w));
     }
 }
 
@@ -330,8 +371,91 @@ __global__ void __launch_bounds__(kStepThreads, 1)
         }
         phase ^= 1u;
 
-        // ---- state tile -> registers (row pairs) --------------------------
         float2 x[DP];
+        if constexpr (MIXED && MAXT == 1) {
+            // Single decode step on the mixed layout: dequantisation is fused
+            // into the decay/prediction pass and the per-row maxima into the
+            // update/readout pass, so the two FMA chains always have
+            // independent work beside them.
+            {
+                const int src = (int)pi_s[h * D + tid];
+                const uint8_t *tb = stage + S::kStatePad;
+                const float kf = load_as_f32<TI>(reinterpret_cast<const TI *>(tb) + src);
+                rowv[tid] = kf;
+                rowv[D + tid] = __fmul_rn(beta_r[0], kf);
+                rowv[2 * D + tid] = load_as_f32<TI>(reinterpret_cast<const TI *>(tb + S::kVecBytes) + src);
+                rowv[3 * D + tid] = load_as_f32<TI>(reinterpret_cast<const TI *>(tb + 2 * S::kVecBytes) + tid);
+                if (KDA) rowv[4 * D + tid] = reinterpret_cast<const float *>(tb + 3 * S::kVecBytes)[src];
+            }
+            group_sync(bar_id, D);  // row vectors visible
+            const float *rv = rowv;
+            const float a_s = alpha_r[0];
+            float p = 0.0f;
+#pragma unroll
+            for (int j = 0; j < DP; j += 2) {
+                float2 x0, x1;
+                mixed_dequant_quad<D, KH>(stage, j / 2, tid, x0, x1);
+                const float4 kk = *reinterpret_cast<const float4 *>(rv + 2 * j);
+                float4 aa;
+                if (KDA) aa = *reinterpret_cast<const float4 *>(rv + 4 * D + 2 * j);
+                else aa = make_float4(a_s, a_s, a_s, a_s);
+                x0 = __fmul2_rn(x0, make_float2(aa.x, aa.y));
+                x1 = __fmul2_rn(x1, make_float2(aa.z, aa.w));
+                p = __fmaf_rn(x0.x, kk.x, p);
+                p = __fmaf_rn(x0.y, kk.y, p);
+                p = __fmaf_rn(x1.x, kk.z, p);
+                p = __fmaf_rn(x1.y, kk.w, p);
+                x[j] = x0;
+                x[j + 1] = x1;
+            }
+            group_sync(bar_id, D);  // stage fully read
+            if (tid == 0) {
+                fence_proxy_async_smem();
+                issue(nxt, nxt_slot, nxt_n);  // the stage now belongs to the next tile
+            }
+            const float e = __fsub_rn(rv[3 * D + tid], p);
+            float o = 0.0f;
+            float mine[D / 32];
+#pragma unroll
+            for (int k = 0; k < D / 32; ++k) mine[k] = 0.0f;
+#pragma unroll
+            for (int j = 0; j < DP; j += 2) {
+                const float4 bk = *reinterpret_cast<const float4 *>(rv + D + 2 * j);
+                const float4 qq = *reinterpret_cast<const float4 *>(rv + 2 * D + 2 * j);
+                x[j] = __ffma2_rn(make_float2(bk.x, bk.y), make_float2(e, e), x[j]);
+                x[j + 1] = __ffma2_rn(make_float2(bk.z, bk.w), make_float2(e, e), x[j + 1]);
+                o = __fmaf_rn(x[j].x, qq.x, o);
+                o = __fmaf_rn(x[j].y, qq.y, o);
+                o = __fmaf_rn(x[j + 1].x, qq.z, o);
+                o = __fmaf_rn(x[j + 1].y, qq.w, o);
+                if (2 * j >= KH) {
+                    absmax_pair<D>(x[j], j, lane, mine);
+                    absmax_pair<D>(x[j + 1], j + 1, lane, mine);
+                }
+            }
+            if (P.o) {
+                TO *og = static_cast<TO *>(P.o);
+                store_from_f32<TO>(og + ((size_t)b * Hv + h) * D + tid, o);
+            }
+            uint8_t *tile = pool + ((size_t)slot * Hv + h) * S::kStateBytes;
+            mixed_requant_from_max<D, KH>(x, mine, outt, red, scl, nscl, rcp, flag, tid, lane, wig,
+                                          bar_id, [&] {
+                                              if (tid == 0) {
+                                                  bulk_store_wait_read();  // previous store has read `outt`
+                                                  *flag = 0;
+                                              }
+                                          });
+            fence_proxy_async_smem();  // this thread's writes to `outt` before the bulk store
+            group_sync(bar_id, D);
+            if (tid == 0) {
+                bulk_s2g(tile, outt, S::kStateBytes);
+                bulk_store_commit();
+            }
+            group_sync(bar_id, D);  // row vectors / partials free for the next item
+            continue;
+        }
+
+        // ---- state tile -> registers (row pairs) --------------------------
         if constexpr (!MIXED) {
             const float *st = reinterpret_cast<const float *>(stage);
 #pragma unroll
