@@ -292,7 +292,7 @@ def run_ours(args, rank, world, local_rank):
     d2h = o.numel() * 4
 
     result = {
-        "metric": METRIC, "value": world * args.steps * updates / dt_max, "unit": UNIT,
+        "metric": METRIC, "value": job_value(world, args.steps, updates, dt_max), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt_max / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
@@ -305,7 +305,7 @@ def run_ours(args, rank, world, local_rank):
                      "traffic": profiled_traffic("step_gdn_f32_b256"),
                      "algorithmic_bytes_per_launch": alg,
                      "kernel": "rs::step_kernel<128, FP32, GDN>"},
-        "e2e": {"value": world * args.steps * updates / e2e_dt, "unit": UNIT,
+        "e2e": {"value": job_value(world, args.steps, updates, e2e_dt), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps,
         "clocks": clk.summary(),
@@ -326,13 +326,21 @@ def _barrier(world):
 
 
 def _max_over_ranks(x, world):
+    """Largest value over the ranks (the elapsed time of the slowest rank)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_value(world, steps, units_per_step, dt_max):
+    """Whole-job throughput: the units all ranks processed over the slowest
+    rank's time (every rank runs its own replica of the workload)."""
+    return world * steps * units_per_step / dt_max
 
 
 def _time(torch, fn, iters, warm=3):
