@@ -24,7 +24,10 @@ struct rs_plan {
 namespace rs {
 
 constexpr int kMaxTokens = 8;        // replay window (draft tokens per call)
-constexpr int kStepThreads = 384;    // threads per CTA of the step kernel
+constexpr int kStepThreads = 384;    // threads per CTA of the step kernel (single token)
+// Replay keeps the state live across a runtime token loop: two groups per CTA
+// leave it the registers it needs (255 per thread) without spilling.
+constexpr int step_threads(int max_tokens) { return max_tokens > 1 ? 256 : kStepThreads; }
 constexpr int kMaxRowMap = 8192;     // bytes of row maps carried in the launch params
 
 struct StepParams {

@@ -64,7 +64,7 @@ struct StepShape {
     __host__ __device__ static constexpr int stage_bytes(int T) { return (kStatePad + T * kTokBytes + 127) / 128 * 128; }
     __host__ __device__ static constexpr int region_bytes(int T) {
         int r = stage_bytes(T);
-        r += T * kRowVecs * D * 4;
+        r += T * kRowVecs * D * 4 + 32;  // row vectors, per-token decays (replay)
         if (kMixed) r += kWarps * D * 4 + D * 12 + 128 + kStatePad;  // partials, s/-s/1/s, flag, out tile
         return (r + 127) / 128 * 128;
     }
@@ -257,7 +257,7 @@ __device__ __forceinline__ void mixed_dequant_quad(const uint8_t *tile, int q, i
 }
 
 template <int D, int KHI, bool KDA, int MAXT, typename TI, typename TO, typename PT>
-__global__ void __launch_bounds__(kStepThreads, 1)
+__global__ void __launch_bounds__(step_threads(MAXT), 1)
     step_kernel(const __grid_constant__ PT P) {
     using S = StepShape<D, KHI, KDA, TI>;
     constexpr bool MIXED = S::kMixed;
@@ -279,7 +279,8 @@ __global__ void __launch_bounds__(kStepThreads, 1)
     uint8_t *stage = region;
     float *rowv = reinterpret_cast<float *>(region + S::stage_bytes(T));
     // rowv layout per token t: [K | BK | Q | V | A?] each D floats
-    float *red = rowv + T * S::kRowVecs * D;                        // [kWarps][D]   (mixed)
+    float *tok_alpha = rowv + T * S::kRowVecs * D;                  // [8] GDN decays (replay)
+    float *red = tok_alpha + 8;                                     // [kWarps][D]   (mixed)
     float *scl = red + S::kWarps * D;                               // [D] row scales
     float *nscl = scl + D;                                          // [D] -scales
     float *rcp = nscl + D;                                          // [D] reciprocals
@@ -347,17 +348,13 @@ __global__ void __launch_bounds__(kStepThreads, 1)
             }
             continue;
         }
-        // Scalars of this item, loaded before the wait so their latency hides.
-        float beta_r[MAXT], alpha_r[MAXT];
-#pragma unroll
-        for (int t = 0; t < MAXT; ++t) {
-            beta_r[t] = 0.0f;
-            alpha_r[t] = 0.0f;
-            if (t < n) {
-                const size_t bt = (size_t)b * T + t;
-                beta_r[t] = P.beta[bt * Hv + h];
-                if (!KDA) alpha_r[t] = P.alpha[bt * Hv + h];
-            }
+        // Scalars of a single-token item, loaded before the wait so their
+        // latency hides.  Replay instances read them while building the row
+        // vectors instead, keeping registers for the state.
+        float beta0 = 0.0f, alpha0 = 0.0f;
+        if constexpr (MAXT == 1) {
+            beta0 = P.beta[(size_t)b * Hv + h];
+            if (!KDA) alpha0 = P.alpha[(size_t)b * Hv + h];
         }
 
         bool got = mbar_wait_bounded(bar, phase);
@@ -382,14 +379,14 @@ __global__ void __launch_bounds__(kStepThreads, 1)
                 const uint8_t *tb = stage + S::kStatePad;
                 const float kf = load_as_f32<TI>(reinterpret_cast<const TI *>(tb) + src);
                 rowv[tid] = kf;
-                rowv[D + tid] = __fmul_rn(beta_r[0], kf);
+                rowv[D + tid] = __fmul_rn(beta0, kf);
                 rowv[2 * D + tid] = load_as_f32<TI>(reinterpret_cast<const TI *>(tb + S::kVecBytes) + src);
                 rowv[3 * D + tid] = load_as_f32<TI>(reinterpret_cast<const TI *>(tb + 2 * S::kVecBytes) + tid);
                 if (KDA) rowv[4 * D + tid] = reinterpret_cast<const float *>(tb + 3 * S::kVecBytes)[src];
             }
             group_sync(bar_id, D);  // row vectors visible
             const float *rv = rowv;
-            const float a_s = alpha_r[0];
+            const float a_s = alpha0;
             float p = 0.0f;
 #pragma unroll
             for (int j = 0; j < DP; j += 2) {
@@ -473,10 +470,9 @@ __global__ void __launch_bounds__(kStepThreads, 1)
             const TI *vt = reinterpret_cast<const TI *>(tb + 2 * S::kVecBytes);
             float *rv = rowv + t * S::kRowVecs * D;
             const float kf = load_as_f32<TI>(kt + src);
-            float bt = 0.0f;
-#pragma unroll
-            for (int tt = 0; tt < MAXT; ++tt)
-                if (tt == t) bt = beta_r[tt];
+            const size_t bti = ((size_t)b * T + t) * Hv + h;
+            const float bt = MAXT == 1 ? beta0 : P.beta[bti];
+            if (!KDA && MAXT > 1 && tid == 0) tok_alpha[t] = P.alpha[bti];
             rv[tid] = kf;
             rv[D + tid] = __fmul_rn(bt, kf);
             rv[2 * D + tid] = load_as_f32<TI>(qt + src);
@@ -494,10 +490,7 @@ __global__ void __launch_bounds__(kStepThreads, 1)
         const int ntok = MAXT == 1 ? 1 : n;  // decode instances: one token, known at compile time
         for (int t = 0; t < ntok; ++t) {
             const float *rv = rowv + t * S::kRowVecs * D;
-            float a_s = 0.0f;
-#pragma unroll
-            for (int tt = 0; tt < MAXT; ++tt)
-                if (tt == t) a_s = alpha_r[tt];
+            const float a_s = KDA ? 0.0f : (MAXT == 1 ? alpha0 : tok_alpha[t]);
             // S <- diag(alpha) S ;  p = S^T k  (ascending rows)
             float p = 0.0f;
 #pragma unroll

@@ -14,7 +14,7 @@ cudaError_t run(StepParamsPi &P, cudaStream_t s) {
     const int region = Sh::region_bytes(P.T_max);
     const int header = 128 + (P.Hv * D + 127) / 128 * 128;
     const int smax = device_max_smem_optin();
-    int G = kStepThreads / D;
+    int G = step_threads(MAXT) / D;
     while (G > 1 && header + G * region > smax) --G;
     if (header + G * region > smax) return cudaErrorNotSupported;
     const int groups_needed = (P.B * P.Hv + G - 1) / G;
