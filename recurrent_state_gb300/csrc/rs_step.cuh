@@ -369,135 +369,61 @@ __global__ void __launch_bounds__(step_threads(MAXT), 1)
         phase ^= 1u;
 
         float2 x[DP];
-        if constexpr (MIXED && MAXT == 1) {
-            // Single decode step on the mixed layout: dequantisation is fused
-            // into the decay/prediction pass and the per-row maxima into the
-            // update/readout pass, so the two FMA chains always have
-            // independent work beside them.
-            {
-                const int src = (int)pi_s[h * D + tid];
-                const uint8_t *tb = stage + S::kStatePad;
-                const float kf = load_as_f32<TI>(reinterpret_cast<const TI *>(tb) + src);
-                rowv[tid] = kf;
-                rowv[D + tid] = __fmul_rn(beta0, kf);
-                rowv[2 * D + tid] = load_as_f32<TI>(reinterpret_cast<const TI *>(tb + S::kVecBytes) + src);
-                rowv[3 * D + tid] = load_as_f32<TI>(reinterpret_cast<const TI *>(tb + 2 * S::kVecBytes) + tid);
-                if (KDA) rowv[4 * D + tid] = reinterpret_cast<const float *>(tb + 3 * S::kVecBytes)[src];
-            }
-            group_sync(bar_id, D);  // row vectors visible
-            const float *rv = rowv;
-            const float a_s = alpha0;
-            float p = 0.0f;
+        if constexpr (!MIXED) {
+            // FP32 tile -> registers, then the stage can be refilled early.
+            const float *st = reinterpret_cast<const float *>(stage);
 #pragma unroll
-            for (int j = 0; j < DP; j += 2) {
-                float2 x0, x1;
-                mixed_dequant_quad<D, KH>(stage, j / 2, tid, x0, x1);
-                const float4 kk = *reinterpret_cast<const float4 *>(rv + 2 * j);
-                float4 aa;
-                if (KDA) aa = *reinterpret_cast<const float4 *>(rv + 4 * D + 2 * j);
-                else aa = make_float4(a_s, a_s, a_s, a_s);
-                x0 = __fmul2_rn(x0, make_float2(aa.x, aa.y));
-                x1 = __fmul2_rn(x1, make_float2(aa.z, aa.w));
-                p = __fmaf_rn(x0.x, kk.x, p);
-                p = __fmaf_rn(x0.y, kk.y, p);
-                p = __fmaf_rn(x1.x, kk.z, p);
-                p = __fmaf_rn(x1.y, kk.w, p);
-                x[j] = x0;
-                x[j + 1] = x1;
+            for (int j = 0; j < DP; ++j) x[j] = make_float2(st[(2 * j) * D + tid], st[(2 * j + 1) * D + tid]);
+        }
+
+        // ---- token inputs -> per-row vectors (row u built by thread u) -----
+        const int ntok = MAXT == 1 ? 1 : n;  // decode instances: one token, known at compile time
+        {
+            const int src = MIXED ? (int)pi_s[h * D + tid] : tid;
+            for (int t = 0; t < ntok; ++t) {
+                const uint8_t *tb = stage + S::kStatePad + t * S::kTokBytes;
+                const TI *kt = reinterpret_cast<const TI *>(tb);
+                const TI *qt = reinterpret_cast<const TI *>(tb + S::kVecBytes);
+                const TI *vt = reinterpret_cast<const TI *>(tb + 2 * S::kVecBytes);
+                float *rv = rowv + t * S::kRowVecs * D;
+                const float kf = load_as_f32<TI>(kt + src);
+                const size_t bti = ((size_t)b * T + t) * Hv + h;
+                const float bt = MAXT == 1 ? beta0 : P.beta[bti];
+                if (!KDA && MAXT > 1 && tid == 0) tok_alpha[t] = P.alpha[bti];
+                rv[tid] = kf;
+                rv[D + tid] = __fmul_rn(bt, kf);
+                rv[2 * D + tid] = load_as_f32<TI>(qt + src);
+                rv[3 * D + tid] = load_as_f32<TI>(vt + tid);  // value coordinates: no row map
+                if (KDA) rv[4 * D + tid] = reinterpret_cast<const float *>(tb + 3 * S::kVecBytes)[src];
             }
-            group_sync(bar_id, D);  // stage fully read
+        }
+        group_sync(bar_id, D);  // row vectors visible (FP32: stage fully read)
+        if constexpr (!MIXED) {
             if (tid == 0) {
                 fence_proxy_async_smem();
                 issue(nxt, nxt_slot, nxt_n);  // the stage now belongs to the next tile
             }
-            const float e = __fsub_rn(rv[3 * D + tid], p);
-            float o = 0.0f;
-            float mine[D / 32];
+        }
+        auto decay_of = [&](int t) -> float {
+            return KDA ? 0.0f : (MAXT == 1 ? alpha0 : tok_alpha[t]);
+        };
+
+        TO *og = static_cast<TO *>(P.o);
+        float mine[D / 32];
 #pragma unroll
-            for (int k = 0; k < D / 32; ++k) mine[k] = 0.0f;
-#pragma unroll
-            for (int j = 0; j < DP; j += 2) {
-                const float4 bk = *reinterpret_cast<const float4 *>(rv + D + 2 * j);
-                const float4 qq = *reinterpret_cast<const float4 *>(rv + 2 * D + 2 * j);
-                x[j] = __ffma2_rn(make_float2(bk.x, bk.y), make_float2(e, e), x[j]);
-                x[j + 1] = __ffma2_rn(make_float2(bk.z, bk.w), make_float2(e, e), x[j + 1]);
-                o = __fmaf_rn(x[j].x, qq.x, o);
-                o = __fmaf_rn(x[j].y, qq.y, o);
-                o = __fmaf_rn(x[j + 1].x, qq.z, o);
-                o = __fmaf_rn(x[j + 1].y, qq.w, o);
-                if (2 * j >= KH) {
-                    absmax_pair<D>(x[j], j, lane, mine);
-                    absmax_pair<D>(x[j + 1], j + 1, lane, mine);
-                }
-            }
-            if (P.o) {
-                TO *og = static_cast<TO *>(P.o);
-                store_from_f32<TO>(og + ((size_t)b * Hv + h) * D + tid, o);
-            }
-            uint8_t *tile = pool + ((size_t)slot * Hv + h) * S::kStateBytes;
-            mixed_requant_from_max<D, KH>(x, mine, outt, red, scl, nscl, rcp, flag, tid, lane, wig,
-                                          bar_id, [&] {
-                                              if (tid == 0) {
-                                                  bulk_store_wait_read();  // previous store has read `outt`
-                                                  *flag = 0;
-                                              }
-                                          });
-            fence_proxy_async_smem();  // this thread's writes to `outt` before the bulk store
-            group_sync(bar_id, D);
-            if (tid == 0) {
-                bulk_s2g(tile, outt, S::kStateBytes);
-                bulk_store_commit();
-            }
-            group_sync(bar_id, D);  // row vectors / partials free for the next item
-            continue;
-        }
-
-        // ---- state tile -> registers (row pairs) --------------------------
-        if constexpr (!MIXED) {
-            const float *st = reinterpret_cast<const float *>(stage);
-#pragma unroll
-            for (int j = 0; j < DP; ++j) x[j] = make_float2(st[(2 * j) * D + tid], st[(2 * j + 1) * D + tid]);
-        } else {
-            mixed_dequant<D, KH>(stage, tid, x);
-        }
-
-        // ---- token inputs -> per-row vectors (row u built by thread u) -----
-        const int src = MIXED ? (int)pi_s[h * D + tid] : tid;
-        for (int t = 0; t < n; ++t) {
-            const uint8_t *tb = stage + S::kStatePad + t * S::kTokBytes;
-            const TI *kt = reinterpret_cast<const TI *>(tb);
-            const TI *qt = reinterpret_cast<const TI *>(tb + S::kVecBytes);
-            const TI *vt = reinterpret_cast<const TI *>(tb + 2 * S::kVecBytes);
-            float *rv = rowv + t * S::kRowVecs * D;
-            const float kf = load_as_f32<TI>(kt + src);
-            const size_t bti = ((size_t)b * T + t) * Hv + h;
-            const float bt = MAXT == 1 ? beta0 : P.beta[bti];
-            if (!KDA && MAXT > 1 && tid == 0) tok_alpha[t] = P.alpha[bti];
-            rv[tid] = kf;
-            rv[D + tid] = __fmul_rn(bt, kf);
-            rv[2 * D + tid] = load_as_f32<TI>(qt + src);
-            rv[3 * D + tid] = load_as_f32<TI>(vt + tid);  // value coordinates: no row map
-            if (KDA) rv[4 * D + tid] = reinterpret_cast<const float *>(tb + 3 * S::kVecBytes)[src];
-        }
-        group_sync(bar_id, D);  // stage fully read, row vectors visible
-
-        if (tid == 0) {
-            fence_proxy_async_smem();
-            issue(nxt, nxt_slot, nxt_n);  // the stage now belongs to the next tile
-        }
-
-        // ---- the recurrence, token by token, state in registers -----------
-        const int ntok = MAXT == 1 ? 1 : n;  // decode instances: one token, known at compile time
-        for (int t = 0; t < ntok; ++t) {
-            const float *rv = rowv + t * S::kRowVecs * D;
-            const float a_s = KDA ? 0.0f : (MAXT == 1 ? alpha0 : tok_alpha[t]);
-            // S <- diag(alpha) S ;  p = S^T k  (ascending rows)
+        for (int k = 0; k < D / 32; ++k) mine[k] = 0.0f;
+        if constexpr (MAXT == 1) {
+            // ---- one token: decay and prediction (mixed: fused with the
+            // dequantisation), then write and readout (mixed: fused with the
+            // per-row maxima), so each FMA chain has independent work beside it
             float p = 0.0f;
+            const float a_s = decay_of(0);
 #pragma unroll
             for (int j = 0; j < DP; j += 2) {
-                const float4 kk = *reinterpret_cast<const float4 *>(rv + 2 * j);
+                if constexpr (MIXED) mixed_dequant_quad<D, KH>(stage, j / 2, tid, x[j], x[j + 1]);
+                const float4 kk = *reinterpret_cast<const float4 *>(rowv + 2 * j);
                 float4 aa;
-                if (KDA) aa = *reinterpret_cast<const float4 *>(rv + 4 * D + 2 * j);
+                if (KDA) aa = *reinterpret_cast<const float4 *>(rowv + 4 * D + 2 * j);
                 else aa = make_float4(a_s, a_s, a_s, a_s);
                 x[j] = __fmul2_rn(x[j], make_float2(aa.x, aa.y));
                 x[j + 1] = __fmul2_rn(x[j + 1], make_float2(aa.z, aa.w));
@@ -506,23 +432,78 @@ __global__ void __launch_bounds__(step_threads(MAXT), 1)
                 p = __fmaf_rn(x[j + 1].x, kk.z, p);
                 p = __fmaf_rn(x[j + 1].y, kk.w, p);
             }
-            const float e = __fsub_rn(rv[3 * D + tid], p);
-            // S <- S + beta k e^T ;  o = S^T q  (ascending rows)
+            if constexpr (MIXED) {
+                group_sync(bar_id, D);  // stage fully read
+                if (tid == 0) {
+                    fence_proxy_async_smem();
+                    issue(nxt, nxt_slot, nxt_n);  // the stage now belongs to the next tile
+                }
+            }
+            const float e = __fsub_rn(rowv[3 * D + tid], p);
             float o = 0.0f;
 #pragma unroll
             for (int j = 0; j < DP; j += 2) {
-                const float4 bk = *reinterpret_cast<const float4 *>(rv + D + 2 * j);
-                const float4 qq = *reinterpret_cast<const float4 *>(rv + 2 * D + 2 * j);
+                const float4 bk = *reinterpret_cast<const float4 *>(rowv + D + 2 * j);
+                const float4 qq = *reinterpret_cast<const float4 *>(rowv + 2 * D + 2 * j);
                 x[j] = __ffma2_rn(make_float2(bk.x, bk.y), make_float2(e, e), x[j]);
                 x[j + 1] = __ffma2_rn(make_float2(bk.z, bk.w), make_float2(e, e), x[j + 1]);
                 o = __fmaf_rn(x[j].x, qq.x, o);
                 o = __fmaf_rn(x[j].y, qq.y, o);
                 o = __fmaf_rn(x[j + 1].x, qq.z, o);
                 o = __fmaf_rn(x[j + 1].y, qq.w, o);
+                if constexpr (MIXED) {
+                    if (2 * j >= KH) {  // row maxima beside the readout chain
+                        absmax_pair<D>(x[j], j, lane, mine);
+                        absmax_pair<D>(x[j + 1], j + 1, lane, mine);
+                    }
+                }
             }
-            if (P.o) {
-                TO *og = static_cast<TO *>(P.o);
-                store_from_f32<TO>(og + (((size_t)b * T + t) * Hv + h) * D + tid, o);
+            if (og) store_from_f32<TO>(og + ((size_t)b * Hv + h) * D + tid, o);
+        } else {
+            // ---- replay: the state stays in registers across the tokens
+            if constexpr (MIXED) {
+                mixed_dequant<D, KH>(stage, tid, x);
+                group_sync(bar_id, D);  // stage fully read
+                if (tid == 0) {
+                    fence_proxy_async_smem();
+                    issue(nxt, nxt_slot, nxt_n);  // the stage now belongs to the next tile
+                }
+            }
+            for (int t = 0; t < ntok; ++t) {
+                const float *rv = rowv + t * S::kRowVecs * D;
+                const float a_s = decay_of(t);
+                float p = 0.0f;
+#pragma unroll
+                for (int j = 0; j < DP; j += 2) {
+                    const float4 kk = *reinterpret_cast<const float4 *>(rv + 2 * j);
+                    float4 aa;
+                    if (KDA) aa = *reinterpret_cast<const float4 *>(rv + 4 * D + 2 * j);
+                    else aa = make_float4(a_s, a_s, a_s, a_s);
+                    x[j] = __fmul2_rn(x[j], make_float2(aa.x, aa.y));
+                    x[j + 1] = __fmul2_rn(x[j + 1], make_float2(aa.z, aa.w));
+                    p = __fmaf_rn(x[j].x, kk.x, p);
+                    p = __fmaf_rn(x[j].y, kk.y, p);
+                    p = __fmaf_rn(x[j + 1].x, kk.z, p);
+                    p = __fmaf_rn(x[j + 1].y, kk.w, p);
+                }
+                const float e = __fsub_rn(rv[3 * D + tid], p);
+                float o = 0.0f;
+#pragma unroll
+                for (int j = 0; j < DP; j += 2) {
+                    const float4 bk = *reinterpret_cast<const float4 *>(rv + D + 2 * j);
+                    const float4 qq = *reinterpret_cast<const float4 *>(rv + 2 * D + 2 * j);
+                    x[j] = __ffma2_rn(make_float2(bk.x, bk.y), make_float2(e, e), x[j]);
+                    x[j + 1] = __ffma2_rn(make_float2(bk.z, bk.w), make_float2(e, e), x[j + 1]);
+                    o = __fmaf_rn(x[j].x, qq.x, o);
+                    o = __fmaf_rn(x[j].y, qq.y, o);
+                    o = __fmaf_rn(x[j + 1].x, qq.z, o);
+                    o = __fmaf_rn(x[j + 1].y, qq.w, o);
+                }
+                if (og) store_from_f32<TO>(og + (((size_t)b * T + t) * Hv + h) * D + tid, o);
+            }
+            if constexpr (MIXED) {
+#pragma unroll
+                for (int j = KH / 2; j < DP; ++j) absmax_pair<D>(x[j], j, lane, mine);
             }
         }
 
@@ -536,12 +517,13 @@ __global__ void __launch_bounds__(step_threads(MAXT), 1)
                 st[(2 * j + 1) * D + tid] = x[j].y;
             }
         } else {
-            mixed_requant_smem<D, KH>(x, outt, red, scl, nscl, rcp, flag, tid, lane, wig, bar_id, [&] {
-                if (tid == 0) {
-                    bulk_store_wait_read();  // the previous tile's store has read `outt`
-                    *flag = 0;
-                }
-            });
+            mixed_requant_from_max<D, KH>(x, mine, outt, red, scl, nscl, rcp, flag, tid, lane, wig,
+                                          bar_id, [&] {
+                                              if (tid == 0) {
+                                                  bulk_store_wait_read();  // previous store has read `outt`
+                                                  *flag = 0;
+                                              }
+                                          });
             fence_proxy_async_smem();  // this thread's writes to `outt` before the bulk store
             group_sync(bar_id, D);
             if (tid == 0) {
