@@ -211,6 +211,7 @@ static rs_status step_common(const rs_layout *l, bool kda, bool replay, void *po
         P.replay = replay ? 1 : 0;
         P.header_bytes = 0;
         P.region_bytes = 0;
+        P.stages = 0;
     };
     cudaError_t e;
     if (l->p.kind == RS_LAYOUT_FP32) {

@@ -46,6 +46,7 @@ struct StepParams {
     int32_t replay;            // 0: one token per item; 1: n_accept[b] tokens
     int32_t header_bytes;      // shared memory before the per-group regions
     int32_t region_bytes;      // shared memory per group
+    int32_t stages;            // stage ring length (kernels that take one)
 };
 
 // Mixed layout: the row map pi (physical row -> key channel), [Hv][D] bytes,

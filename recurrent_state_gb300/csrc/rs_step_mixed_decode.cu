@@ -1,6 +1,7 @@
-// rs_step_mixed_decode.cu -- instantiations of the step kernel for the mixed
-// FP16/INT8 layout (dk = dv = 128, 16 FP16 rows per head), single decode steps.
-#include "rs_step.cuh"
+// rs_step_mixed_decode.cu -- single decode steps on the mixed FP16/INT8
+// layout (dk = dv = 128, 16 FP16 rows per head): one warp per tile over a
+// ring of shared-memory stages (rs_mixed_decode.cuh).
+#include "rs_mixed_decode.cuh"
 #include "../../include/recurrent_state.h"
 
 namespace rs {
@@ -9,24 +10,31 @@ namespace {
 
 template <int D, int KHI, bool KDA, int MAXT, typename TI, typename TO>
 cudaError_t run(StepParamsPi &P, cudaStream_t s) {
-    using Sh = StepShape<D, KHI, KDA, TI>;
-    auto kern = step_kernel<D, KHI, KDA, MAXT, TI, TO, StepParamsPi>;
-    const int region = Sh::region_bytes(P.T_max);
-    const int header = 128 + (P.Hv * D + 127) / 128 * 128;
+    static_assert(MAXT == 1, "single decode steps");
+    using Sh = MixedWarpShape<D, KHI, KDA, TI>;
+    auto kern = mixed_decode_kernel<D, KHI, KDA, TI, TO>;
+    const int header = Sh::kHeader + (P.Hv * D + 127) / 128 * 128;
     const int smax = device_max_smem_optin();
-    int G = step_threads(MAXT) / D;
-    while (G > 1 && header + G * region > smax) --G;
-    if (header + G * region > smax) return cudaErrorNotSupported;
-    const int groups_needed = (P.B * P.Hv + G - 1) / G;
+    // W warps and a ring of NS > W stages in the shared memory there is
+    int W = kMixedWarps, NS = 0;
+    for (; W >= 1; --W) {
+        const int avail = smax - header - W * Sh::kWarpBytes;
+        NS = avail > 0 ? avail / Sh::kStage : 0;
+        if (NS > kMixedMaxStages) NS = kMixedMaxStages;
+        if (NS >= W + 1) break;
+    }
+    if (W < 1) return cudaErrorNotSupported;
+    const int items = P.B * P.Hv;
     int grid = device_sm_count();
-    if (grid > groups_needed) grid = groups_needed;
+    if (grid > items) grid = items;
     if (grid < 1) grid = 1;
     P.header_bytes = header;
-    P.region_bytes = region;
-    const int smem = header + G * region;
+    P.region_bytes = Sh::kStage;
+    P.stages = NS;
+    const int smem = header + W * Sh::kWarpBytes + NS * Sh::kStage;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, G * D, smem, s>>>(P);
+    kern<<<grid, W * 32, smem, s>>>(P);
     return cudaGetLastError();
 }
 

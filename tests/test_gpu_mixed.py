@@ -234,3 +234,77 @@ def test_quantiser_rounding_near_half_integers():
     assert np.array_equal(np.isnan(hg), nan)
     assert np.array_equal(hg.view(np.uint16)[~nan], hr.view(np.uint16)[~nan])
     assert nan.sum() >= 1  # the NaN planted in an FP16 row survives
+
+
+@pytest.mark.parametrize("per_channel", [True, False])
+def test_mixed_decode_small_batch_bad_slots(per_channel):
+    """Fewer tiles than streaming multiprocessors, two of them with slots out
+    of range: those are skipped and reported (status bit 1), the rest match
+    the oracle bit for bit."""
+    B, Hk, Hv = 6, 2, 4
+    f32, mix, pi = layouts(Hv, Hk, seed=8)
+    w = gen.decode_workload(B=B, Hk=Hk, Hv=Hv, d=D, steps=1, per_channel=per_channel,
+                            in_dtype="bf16", seed=8, n_slots=9)
+    w.slot_idx[2] = 9
+    w.slot_idx[4] = -1
+    ref = orc.convert_pool_f32_to_mixed(w.state0, KHI, pi)
+    pool = dev(ref)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q, k, v, a, b = step_inputs(w, 0)
+    o = torch.full((B, Hv, D), 7.0, device="cuda")
+    fn = rs.kda_decode_update if per_channel else rs.gdn_decode_update
+    fn(mix, pool, dev(w.slot_idx), q, k, v, a, b, o=o, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 1
+    oh = host(o)
+    assert np.all(oh[[2, 4]] == 7.0)
+    ok = np.array([0, 1, 3, 5])
+    o_r, st = orc.decode_mixed(ref, w.slot_idx[ok], pi, KHI, D, D, w.q[0][ok], w.k[0][ok],
+                               w.v[0][ok], w.alpha[0][ok], w.beta[0][ok])
+    assert st == 0
+    assert same_bits(oh[ok], o_r)
+    assert same_bits(host(pool), ref)
+
+
+def nan_aware_same(g, r):
+    gn, rn = np.isnan(g), np.isnan(r)
+    return np.array_equal(gn, rn) and np.array_equal(g[~gn].view(np.uint32), r[~rn].view(np.uint32))
+
+
+def test_mixed_decode_nonfinite_state():
+    """A NaN in an FP16 row spreads through the prediction to its whole
+    column, and an infinite INT8 scale makes its row infinite: every INT8
+    block of those tiles then takes the literal-division path.  INT8 codes
+    and scales must match every byte; FP16 rows and o match up to NaN
+    payloads."""
+    B, Hv = 4, 4
+    f32, mix, pi = layouts(Hv, Hv, seed=9)
+    for per_channel in (True, False):
+        w = gen.decode_workload(B=B, Hk=Hv, Hv=Hv, d=D, steps=1, per_channel=per_channel,
+                                in_dtype="bf16", seed=9)
+        ref = orc.convert_pool_f32_to_mixed(w.state0, KHI, pi)
+        s0, s1 = w.slot_idx[0], w.slot_idx[1]
+        r, c = 3, 10                               # FP16 row 3, column 10 of head 1
+        off = 2 * (((r // 2) * D + c) * 2 + r % 2)
+        ref[s0, 1, off:off + 2] = np.array([0x7E00], np.uint16).view(np.uint8)
+        sc = 2 * KHI * D + (D - KHI) * D + 4 * 5  # INT8 row 5's scale in head 0
+        ref[s1, 0, sc:sc + 4] = np.array([np.inf], np.float32).view(np.uint8)
+        pool = dev(ref)
+        q, k, v, a, b = step_inputs(w, 0)
+        o = torch.empty((B, Hv, D), device="cuda")
+        fn = rs.kda_decode_update if per_channel else rs.gdn_decode_update
+        fn(mix, pool, dev(w.slot_idx), q, k, v, a, b, o=o)
+        o_r, st = orc.decode_mixed(ref, w.slot_idx, pi, KHI, D, D, w.q[0], w.k[0], w.v[0],
+                                   w.alpha[0], w.beta[0])
+        assert st == 0
+        assert np.isnan(o_r).any()
+        assert nan_aware_same(host(o), o_r)
+        g = host(pool)
+        hb = 2 * KHI * D
+        assert same_bits(g[..., hb:], ref[..., hb:])
+        hg = g[..., :hb].copy().view(np.float16)
+        hr = ref[..., :hb].copy().view(np.float16)
+        nan = np.isnan(hr)
+        assert nan.sum() >= KHI  # the NaN column of head 1, all its FP16 rows
+        assert np.array_equal(np.isnan(hg), nan)
+        assert np.array_equal(hg.view(np.uint16)[~nan], hr.view(np.uint16)[~nan])
