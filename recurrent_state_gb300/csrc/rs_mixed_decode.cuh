@@ -1,17 +1,19 @@
 // rs_mixed_decode.cuh -- single-token decode on the mixed FP16/INT8 layout
 // (DAMP §5.2 and Appendix A.4: one fused load, dequantise, update, readout,
-// requantise and store per step), one warp per state tile.
+// requantise and store per step).
 //
-// Lane l of a warp owns the four adjacent columns 4l..4l+3 of the tile, so
-//   * one 16-byte shared load brings a column quad of a word row (4 INT8 rows
-//     or 2 FP16 rows per column), and every per-element operation runs as a
-//     paired FP32 instruction (mul/add/fma .f32x2) over two columns of one
-//     row -- including the two reductions over key channels, which stay
-//     sequential ascending-row FMA chains per column, exactly the oracle's
-//     evaluation order;
-//   * the per-row absmax of the requantisation is a max over the lane's four
-//     values plus one warp max-reduction (redux.sync): no shared-memory
-//     combine and no barrier beyond the warp.
+// A state tile is worked on by WPT warps (one or two); lane l of tile warp t
+// owns the CPL = D / (32 WPT) adjacent columns starting at CPL (32 t + l), so
+//   * one 8- or 16-byte shared load brings a lane's columns of a word row
+//     (4 INT8 rows or 2 FP16 rows per column), and every per-element
+//     operation runs as a paired FP32 instruction (mul/add/fma .f32x2) over
+//     two columns of one row -- including the two reductions over key
+//     channels, which stay sequential ascending-row FMA chains per column,
+//     exactly the oracle's evaluation order;
+//   * the per-row absmax of the requantisation is a max over the lane's
+//     values, one warp max-reduction (redux.sync) and, with two warps per
+//     tile, one exchange of the 16 partial maxima of a block through shared
+//     memory.
 // The packed tile (18,880 B at d = 128) is worked on in place in its
 // shared-memory stage: pass 1 dequantises and decays each row and runs the
 // prediction chain p = S^T k; pass 2 repeats the dequantisation and decay
@@ -19,28 +21,28 @@
 // x += RN(beta k) e^T, runs the readout chain o = S^T q, and requantises in
 // blocks of 16 rows (FP16 rows round to nearest even; INT8 rows get a new
 // scale from the block's absmax and an exact RN(x/s) code, as in
-// rs_step.cuh).  Lane 0 then bulk-stores the tile.
+// rs_step.cuh).  One thread then bulk-stores the tile.
 //
-// A CTA runs W warps over a ring of NS > W stages.  Its tiles are numbered
-// j = 0, 1, ... (tile blockIdx.x + j * gridDim.x of the launch); tile j uses
-// stage j mod NS and warp j mod W.  The warp that finishes tile j issues the
-// bulk copy of tile j + NS into the stage it has just released, so the copy
-// of a tile starts NS - W tiles ahead of the warp that takes it.  A use
-// counter per stage, written before each copy is issued, tells a warp that
-// its copy was issued before it waits on the stage's mbarrier parity (tiles
-// are taken by different warps, so the parity alone could alias).  Every wait
-// is bounded and reports RS_DEV_PIPE_TIMEOUT.
+// A CTA runs P = W / WPT tile slots over a ring of NS > P stages.  Its tiles
+// are numbered j = 0, 1, ... (tile blockIdx.x + j * gridDim.x of the
+// launch); tile j uses stage j mod NS and tile slot j mod P.  The slot that
+// finishes tile j issues the bulk copy of tile j + NS into the stage it has
+// just released, so the copy of a tile starts NS - P tiles ahead of the slot
+// that takes it.  A use counter per stage, written before each copy is
+// issued, tells a slot that its copy was issued before it waits on the
+// stage's mbarrier parity (tiles are taken by different slots, so the parity
+// alone could alias).  Every wait is bounded and reports RS_DEV_PIPE_TIMEOUT.
 #pragma once
 
 #include "rs_step.cuh"
 
 namespace rs {
 
-constexpr int kMixedWarps = 8;       // warps per CTA
 constexpr int kMixedMaxStages = 16;  // stage ring length limit (mbarriers in the header)
 
-template <int D, int KH, bool KDA, typename TI>
+template <int D, int KH, bool KDA, typename TI, int WPT>
 struct MixedWarpShape {
+    static constexpr int kCols = D / (32 * WPT);  // columns per lane
     static constexpr int kStateBytes = 2 * KH * D + (D - KH) * D + 4 * (D - KH);
     static constexpr int kStatePad = (kStateBytes + 127) / 128 * 128;
     static constexpr int kVecBytes = D * (int)sizeof(TI);
@@ -48,8 +50,10 @@ struct MixedWarpShape {
     static constexpr int kStage = (kStatePad + kTokBytes + 127) / 128 * 128;
     static constexpr int kRowVecs = KDA ? 4 : 3;  // K, BK, Q (+ A), floats in row order
     static constexpr int kBlock = 16;             // rows per requantisation block
-    // per warp: row vectors, then -s and 1/s of the current block
-    static constexpr int kWarpBytes = (kRowVecs * D * 4 + 2 * kBlock * 4 + 127) / 128 * 128;
+    // per tile slot: row vectors, partial row maxima [2][WPT][kBlock], and
+    // per warp -s and 1/s of the current block
+    static constexpr int kSlotBytes =
+        (kRowVecs * D * 4 + 2 * WPT * kBlock * 4 + WPT * 2 * kBlock * 4 + 127) / 128 * 128;
     static constexpr int kHeader = 256;  // mbarriers [NS], use counters [NS] at +128
 };
 
@@ -65,38 +69,100 @@ __device__ __forceinline__ float max_abs4_nan(float2 a, float2 b) {
     return r;
 }
 
+__device__ __forceinline__ float max_abs2_nan(float2 a) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(fabsf(a.x)), "f"(fabsf(a.y)));
+    return r;
+}
+
+__device__ __forceinline__ float max_nan(float a, float b) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-// Rows 4q..4q+3 of a lane's columns: x[i][0] = columns (c0, c1) of row
-// 4q+i, x[i][1] = columns (c2, c3).
-struct Quad {
-    float2 x[4][2];
+// RN(a / 127) for a >= 1e-8 or a = +inf, without a division: q0 = RN(a y)
+// with y = RN(1/127), one exact-remainder correction q = RN(q0 + RN(a - q0
+// 127) y) (Markstein's correction step).  Checked against the IEEE quotient
+// for every finite FP32 a >= 1e-8; +inf is passed through.
+__device__ __forceinline__ float div127(float a) {
+    constexpr float y = 1.0f / 127.0f;
+    const float q0 = __fmul_rn(a, y);
+    const float q = __fmaf_rn(__fmaf_rn(-q0, 127.0f, a), y, q0);
+    return a == __int_as_float(0x7f800000) ? a : q;
+}
+
+// A lane's CPL words of one word row (CPL = 2 or 4), 8- or 16-byte aligned.
+template <int N> __device__ __forceinline__ void lds_words(const uint32_t *p, uint32_t (&w)[N]) {
+    if constexpr (N == 4) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(p);
+        w[0] = v.x, w[1] = v.y, w[2] = v.z, w[3] = v.w;
+    } else {
+        const uint2 v = *reinterpret_cast<const uint2 *>(p);
+        w[0] = v.x, w[1] = v.y;
+    }
+}
+template <int N> __device__ __forceinline__ void sts_words(uint32_t *p, const uint32_t (&w)[N]) {
+    if constexpr (N == 4) *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+    else *reinterpret_cast<uint2 *>(p) = make_uint2(w[0], w[1]);
+}
+
+// Rows 4q..4q+3 of a lane's columns: x[i][k] = columns (2k, 2k+1) of the
+// lane's columns in row 4q+i.
+template <int CPL> struct Quad {
+    float2 x[4][CPL / 2];
 };
 
-template <int D, int KH, bool KDA, typename TI, typename TO>
-__global__ void __launch_bounds__(kMixedWarps * 32, 1)
+// INT8 words of a lane's columns for rows 4q..4q+3 with scales s, by the
+// literal IEEE division: the path of blocks whose absmax is not finite.  Out
+// of line, so that the common path carries a call and nothing else of it.
+template <int CPL> __device__ __noinline__ void quant_rows_exact(Quad<CPL> X, float4 s, uint32_t *dst) {
+    const float sr[4] = {s.x, s.y, s.z, s.w};
+    uint32_t wd[CPL];
+#pragma unroll
+    for (int t = 0; t < CPL; ++t) wd[t] = 0u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int k = 0; k < CPL / 2; ++k) {
+            wd[2 * k] |= quant_exact(X.x[i][k].x, sr[i]) << (8 * i);
+            wd[2 * k + 1] |= quant_exact(X.x[i][k].y, sr[i]) << (8 * i);
+        }
+    sts_words<CPL>(dst, wd);
+}
+
+template <int D, int KH, bool KDA, typename TI, typename TO, int WPT>
+__global__ void __launch_bounds__(256 * WPT, 1)
     mixed_decode_kernel(const __grid_constant__ StepParamsPi P) {
-    using S = MixedWarpShape<D, KH, KDA, TI>;
-    static_assert(D == 128, "four columns per lane");
+    using S = MixedWarpShape<D, KH, KDA, TI, WPT>;
+    constexpr int CPL = S::kCols;
+    constexpr int NP = CPL / 2;  // column pairs per lane
+    static_assert(CPL == 2 || CPL == 4, "two or four columns per lane");
     static_assert((D - KH) % S::kBlock == 0 && KH % 4 == 0, "INT8 rows fill whole blocks");
-    constexpr int NQ = D / 4;  // 16-byte column quads per word row
 
     extern __shared__ __align__(128) uint8_t smem[];
     const int W = blockDim.x >> 5;
+    const int NSLOT = W / WPT;
     const int w = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int ps = w / WPT;               // tile slot
+    const int wt = w - ps * WPT;          // warp within the tile
+    const int tt = wt * 32 + lane;        // thread within the tile
+    const int c0 = CPL * tt;              // first column of this lane
     const int NS = P.stages;
     const int Hv = P.Hv, Hk = P.Hk;
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
     volatile int32_t *useq = reinterpret_cast<volatile int32_t *>(smem + 128);
     uint8_t *pi_s = smem + S::kHeader;
-    float *wv = reinterpret_cast<float *>(smem + P.header_bytes + (size_t)w * S::kWarpBytes);
-    float *nsc = wv + S::kRowVecs * D;  // -s of the block's rows
-    float *ysc = nsc + S::kBlock;       // 1/s of the block's rows
-    uint8_t *stages = smem + P.header_bytes + (size_t)W * S::kWarpBytes;
+    float *wv = reinterpret_cast<float *>(smem + P.header_bytes + (size_t)ps * S::kSlotBytes);
+    float *part = wv + S::kRowVecs * D;                       // [2][WPT][kBlock]
+    float *nsc = part + 2 * WPT * S::kBlock + wt * 2 * S::kBlock;  // -s [kBlock], 1/s [kBlock]
+    uint8_t *stages = smem + P.header_bytes + (size_t)NSLOT * S::kSlotBytes;
 
     if (threadIdx.x < NS) {
         mbar_init(&bars[threadIdx.x], 1);
@@ -105,6 +171,11 @@ __global__ void __launch_bounds__(kMixedWarps * 32, 1)
     for (int i = threadIdx.x; i < Hv * D; i += blockDim.x) pi_s[i] = P.pi[i];
     fence_mbar_init();
     __syncthreads();
+
+    auto tile_sync = [&]() {
+        if constexpr (WPT == 1) __syncwarp();
+        else group_sync(1 + ps, 32 * WPT);
+    };
 
     const int items = P.B * Hv;
     const int grid = gridDim.x;
@@ -147,14 +218,15 @@ __global__ void __launch_bounds__(kMixedWarps * 32, 1)
     // write strength (and GDN decay) of a tile, read one tile ahead
     auto tile_beta = [&](int it) -> float { return it < items ? P.beta[it] : 0.0f; };
     auto tile_alpha = [&](int it) -> float { return (!KDA && it < items) ? P.alpha[it] : 0.0f; };
-    float nbeta = tile_beta(item_of(w)), nalpha = tile_alpha(item_of(w));
+    float nbeta = tile_beta(item_of(ps)), nalpha = tile_alpha(item_of(ps));
+    const bool l0 = lane & 1, l1 = lane & 2, l2 = lane & 4, l3 = lane & 8;
 
-    for (int j = w;; j += W) {
+    for (int j = ps;; j += NSLOT) {
         const int it = item_of(j);
         if (it >= items) break;
         const float beta0 = nbeta, alpha0 = nalpha;
-        nbeta = tile_beta(item_of(j + W));
-        nalpha = tile_alpha(item_of(j + W));
+        nbeta = tile_beta(item_of(j + NSLOT));
+        nalpha = tile_alpha(item_of(j + NSLOT));
         const int s = j % NS;
         const int32_t use = j / NS;
 
@@ -169,8 +241,11 @@ __global__ void __launch_bounds__(kMixedWarps * 32, 1)
         }
         ok = ok && (mbar_wait_bounded(&bars[s], (uint32_t)use & 1u) ||
                     mbar_wait_bounded(&bars[s], (uint32_t)use & 1u));
-        if (!__all_sync(0xffffffffu, ok)) {
-            if (lane == 0) {
+        bool failed;
+        if constexpr (WPT == 1) failed = !__all_sync(0xffffffffu, ok);
+        else failed = group_sync_or(1 + ps, 32 * WPT, !ok);
+        if (failed) {
+            if (tt == 0) {
                 report(P.status, 8);
                 bulk_store_wait_all();
             }
@@ -179,7 +254,7 @@ __global__ void __launch_bounds__(kMixedWarps * 32, 1)
         const int b = it / Hv, h = it - b * Hv;
         const int32_t slot = P.slot_idx[b];
         if (!slot_ok(slot)) {
-            if (lane == 0) {
+            if (tt == 0) {
                 report(P.status, 1);
                 issue(j + NS);
             }
@@ -189,168 +264,191 @@ __global__ void __launch_bounds__(kMixedWarps * 32, 1)
         uint8_t *st = stages + (size_t)s * S::kStage;
         const uint8_t *tb = st + S::kStatePad;
 
-        // ---- row vectors in physical row order: lane l builds rows 4l..4l+3
+        // ---- row vectors in physical row order: thread tt builds rows
+        // CPL tt .. CPL tt + CPL - 1
         {
-            const uint32_t src4 = *reinterpret_cast<const uint32_t *>(pi_s + h * D + 4 * lane);
-            float kk[4], bk[4], qq[4], aa[4];
+            uint32_t srcs;
+            if constexpr (CPL == 4) srcs = *reinterpret_cast<const uint32_t *>(pi_s + h * D + c0);
+            else srcs = *reinterpret_cast<const uint16_t *>(pi_s + h * D + c0);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int src = (src4 >> (8 * i)) & 0xff;
-                kk[i] = load_as_f32<TI>(reinterpret_cast<const TI *>(tb) + src);
-                bk[i] = __fmul_rn(beta0, kk[i]);
-                qq[i] = load_as_f32<TI>(reinterpret_cast<const TI *>(tb + S::kVecBytes) + src);
-                aa[i] = KDA ? reinterpret_cast<const float *>(tb + 3 * S::kVecBytes)[src] : 0.0f;
+            for (int i = 0; i < CPL; ++i) {
+                const int src = (srcs >> (8 * i)) & 0xff;
+                const float kf = load_as_f32<TI>(reinterpret_cast<const TI *>(tb) + src);
+                wv[c0 + i] = kf;
+                wv[D + c0 + i] = __fmul_rn(beta0, kf);
+                wv[2 * D + c0 + i] = load_as_f32<TI>(reinterpret_cast<const TI *>(tb + S::kVecBytes) + src);
+                if (KDA) wv[3 * D + c0 + i] = reinterpret_cast<const float *>(tb + 3 * S::kVecBytes)[src];
             }
-            reinterpret_cast<float4 *>(wv)[lane] = make_float4(kk[0], kk[1], kk[2], kk[3]);
-            reinterpret_cast<float4 *>(wv + D)[lane] = make_float4(bk[0], bk[1], bk[2], bk[3]);
-            reinterpret_cast<float4 *>(wv + 2 * D)[lane] = make_float4(qq[0], qq[1], qq[2], qq[3]);
-            if (KDA) reinterpret_cast<float4 *>(wv + 3 * D)[lane] = make_float4(aa[0], aa[1], aa[2], aa[3]);
         }
-        float vv[4];
+        float vv[CPL];
 #pragma unroll
-        for (int t = 0; t < 4; ++t)
-            vv[t] = load_as_f32<TI>(reinterpret_cast<const TI *>(tb + 2 * S::kVecBytes) + 4 * lane + t);
-        __syncwarp();
+        for (int t = 0; t < CPL; ++t)
+            vv[t] = load_as_f32<TI>(reinterpret_cast<const TI *>(tb + 2 * S::kVecBytes) + c0 + t);
+        tile_sync();
 
         const float4 *K4 = reinterpret_cast<const float4 *>(wv);
         const float4 *BK4 = reinterpret_cast<const float4 *>(wv + D);
         const float4 *Q4 = reinterpret_cast<const float4 *>(wv + 2 * D);
         const float4 *A4 = reinterpret_cast<const float4 *>(wv + 3 * D);
-        uint4 *hi4 = reinterpret_cast<uint4 *>(st);               // [KH/2][NQ]
-        uint4 *lo4 = reinterpret_cast<uint4 *>(st + 2 * KH * D);  // [(D-KH)/4][NQ]
+        uint32_t *hiw = reinterpret_cast<uint32_t *>(st);               // FP16 pairs [KH/2][D]
+        uint32_t *low = reinterpret_cast<uint32_t *>(st + 2 * KH * D);  // INT8 quads [(D-KH)/4][D]
         float *scales = reinterpret_cast<float *>(st + 2 * KH * D + (D - KH) * D);
         const float4 *sc4 = reinterpret_cast<const float4 *>(scales);
 
-        auto decay = [&](int q, Quad &X) {  // rows 4q..4q+3 times their decay
+        auto decay = [&](int q, Quad<CPL> &X) {  // rows 4q..4q+3 times their decay
             const float4 a = KDA ? A4[q] : make_float4(alpha0, alpha0, alpha0, alpha0);
             const float ar[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                X.x[i][0] = __fmul2_rn(X.x[i][0], make_float2(ar[i], ar[i]));
-                X.x[i][1] = __fmul2_rn(X.x[i][1], make_float2(ar[i], ar[i]));
-            }
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int k = 0; k < NP; ++k) X.x[i][k] = __fmul2_rn(X.x[i][k], make_float2(ar[i], ar[i]));
         };
-        auto load_hi = [&](int q, Quad &X) {  // FP16 rows 4q..4q+3, decayed
+        auto load_hi = [&](int q, Quad<CPL> &X) {  // FP16 rows 4q..4q+3, decayed
 #pragma unroll
             for (int pr = 0; pr < 2; ++pr) {
-                const uint4 hw = hi4[(2 * q + pr) * NQ + lane];
-                const __half2 h0 = *reinterpret_cast<const __half2 *>(&hw.x);
-                const __half2 h1 = *reinterpret_cast<const __half2 *>(&hw.y);
-                const __half2 h2 = *reinterpret_cast<const __half2 *>(&hw.z);
-                const __half2 h3 = *reinterpret_cast<const __half2 *>(&hw.w);
-                X.x[2 * pr][0] = make_float2(__low2float(h0), __low2float(h1));
-                X.x[2 * pr][1] = make_float2(__low2float(h2), __low2float(h3));
-                X.x[2 * pr + 1][0] = make_float2(__high2float(h0), __high2float(h1));
-                X.x[2 * pr + 1][1] = make_float2(__high2float(h2), __high2float(h3));
+                uint32_t wd[CPL];
+                lds_words<CPL>(hiw + (2 * q + pr) * D + c0, wd);
+#pragma unroll
+                for (int k = 0; k < NP; ++k) {
+                    const __half2 ha = *reinterpret_cast<const __half2 *>(&wd[2 * k]);
+                    const __half2 hb = *reinterpret_cast<const __half2 *>(&wd[2 * k + 1]);
+                    X.x[2 * pr][k] = make_float2(__low2float(ha), __low2float(hb));
+                    X.x[2 * pr + 1][k] = make_float2(__high2float(ha), __high2float(hb));
+                }
             }
             decay(q, X);
         };
-        auto load_lo = [&](int qd, Quad &X) {  // INT8 rows KH+4qd .. KH+4qd+3, decayed
-            const uint4 wr = lo4[qd * NQ + lane];
-            const uint32_t wd[4] = {wr.x ^ 0x80808080u, wr.y ^ 0x80808080u, wr.z ^ 0x80808080u,
-                                    wr.w ^ 0x80808080u};
+        auto load_lo = [&](int qd, Quad<CPL> &X) {  // INT8 rows KH+4qd .. KH+4qd+3, decayed
+            uint32_t wd[CPL];
+            lds_words<CPL>(low + qd * D + c0, wd);
+#pragma unroll
+            for (int t = 0; t < CPL; ++t) wd[t] ^= 0x80808080u;
             const float4 s4 = sc4[qd];
             const float sr[4] = {s4.x, s4.y, s4.z, s4.w};
             const float2 nb = make_float2(-kCodeBias, -kCodeBias);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const uint32_t sel = 0x7540u + (uint32_t)i;
-                const float f0 = __uint_as_float(__byte_perm(wd[0], 0x4B000000u, sel));
-                const float f1 = __uint_as_float(__byte_perm(wd[1], 0x4B000000u, sel));
-                const float f2 = __uint_as_float(__byte_perm(wd[2], 0x4B000000u, sel));
-                const float f3 = __uint_as_float(__byte_perm(wd[3], 0x4B000000u, sel));
-                X.x[i][0] = __fmul2_rn(__fadd2_rn(make_float2(f0, f1), nb), make_float2(sr[i], sr[i]));
-                X.x[i][1] = __fmul2_rn(__fadd2_rn(make_float2(f2, f3), nb), make_float2(sr[i], sr[i]));
+#pragma unroll
+                for (int k = 0; k < NP; ++k) {
+                    const float fa = __uint_as_float(__byte_perm(wd[2 * k], 0x4B000000u, sel));
+                    const float fb = __uint_as_float(__byte_perm(wd[2 * k + 1], 0x4B000000u, sel));
+                    X.x[i][k] = __fmul2_rn(__fadd2_rn(make_float2(fa, fb), nb), make_float2(sr[i], sr[i]));
+                }
             }
             decay(KH / 4 + qd, X);
         };
-        auto predict = [&](int q, const Quad &X, float2 &p01, float2 &p23) {
+        auto predict = [&](int q, const Quad<CPL> &X, float2 (&p)[NP]) {
             const float4 k4 = K4[q];
             const float kr[4] = {k4.x, k4.y, k4.z, k4.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                p01 = __ffma2_rn(X.x[i][0], make_float2(kr[i], kr[i]), p01);
-                p23 = __ffma2_rn(X.x[i][1], make_float2(kr[i], kr[i]), p23);
-            }
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int k = 0; k < NP; ++k) p[k] = __ffma2_rn(X.x[i][k], make_float2(kr[i], kr[i]), p[k]);
         };
-        auto write_read = [&](int q, Quad &X, float2 e01, float2 e23, float2 &o01, float2 &o23) {
+        auto write_read = [&](int q, Quad<CPL> &X, const float2 (&e)[NP], float2 (&o)[NP]) {
             const float4 b4 = BK4[q];
             const float4 q4 = Q4[q];
             const float br[4] = {b4.x, b4.y, b4.z, b4.w};
             const float qr[4] = {q4.x, q4.y, q4.z, q4.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                X.x[i][0] = __ffma2_rn(make_float2(br[i], br[i]), e01, X.x[i][0]);
-                X.x[i][1] = __ffma2_rn(make_float2(br[i], br[i]), e23, X.x[i][1]);
-                o01 = __ffma2_rn(X.x[i][0], make_float2(qr[i], qr[i]), o01);
-                o23 = __ffma2_rn(X.x[i][1], make_float2(qr[i], qr[i]), o23);
-            }
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int k = 0; k < NP; ++k) {
+                    X.x[i][k] = __ffma2_rn(make_float2(br[i], br[i]), e[k], X.x[i][k]);
+                    o[k] = __ffma2_rn(X.x[i][k], make_float2(qr[i], qr[i]), o[k]);
+                }
         };
 
         // ---- pass 1: decay and prediction p = S^T k (ascending rows) -------
-        float2 p01 = make_float2(0.0f, 0.0f), p23 = make_float2(0.0f, 0.0f);
+        float2 p[NP];
+#pragma unroll
+        for (int k = 0; k < NP; ++k) p[k] = make_float2(0.0f, 0.0f);
 #pragma unroll
         for (int q = 0; q < KH / 4; ++q) {
-            Quad X;
+            Quad<CPL> X;
             load_hi(q, X);
-            predict(q, X, p01, p23);
+            predict(q, X, p);
         }
 #pragma unroll 4
         for (int qd = 0; qd < (D - KH) / 4; ++qd) {
-            Quad X;
+            Quad<CPL> X;
             load_lo(qd, X);
-            predict(KH / 4 + qd, X, p01, p23);
+            predict(KH / 4 + qd, X, p);
         }
-        const float2 e01 = make_float2(__fsub_rn(vv[0], p01.x), __fsub_rn(vv[1], p01.y));
-        const float2 e23 = make_float2(__fsub_rn(vv[2], p23.x), __fsub_rn(vv[3], p23.y));
+        float2 e[NP], o[NP];
+#pragma unroll
+        for (int k = 0; k < NP; ++k) {
+            e[k] = make_float2(__fsub_rn(vv[2 * k], p[k].x), __fsub_rn(vv[2 * k + 1], p[k].y));
+            o[k] = make_float2(0.0f, 0.0f);
+        }
 
         // ---- pass 2: write, readout, requantise ---------------------------
-        float2 o01 = make_float2(0.0f, 0.0f), o23 = make_float2(0.0f, 0.0f);
 #pragma unroll
         for (int q = 0; q < KH / 4; ++q) {  // FP16 rows: round to nearest even, in place
-            Quad X;
+            Quad<CPL> X;
             load_hi(q, X);
-            write_read(q, X, e01, e23, o01, o23);
+            write_read(q, X, e, o);
 #pragma unroll
             for (int pr = 0; pr < 2; ++pr) {
-                const __half2 h0 = __floats2half2_rn(X.x[2 * pr][0].x, X.x[2 * pr + 1][0].x);
-                const __half2 h1 = __floats2half2_rn(X.x[2 * pr][0].y, X.x[2 * pr + 1][0].y);
-                const __half2 h2 = __floats2half2_rn(X.x[2 * pr][1].x, X.x[2 * pr + 1][1].x);
-                const __half2 h3 = __floats2half2_rn(X.x[2 * pr][1].y, X.x[2 * pr + 1][1].y);
-                uint4 hw;
-                hw.x = *reinterpret_cast<const uint32_t *>(&h0);
-                hw.y = *reinterpret_cast<const uint32_t *>(&h1);
-                hw.z = *reinterpret_cast<const uint32_t *>(&h2);
-                hw.w = *reinterpret_cast<const uint32_t *>(&h3);
-                hi4[(2 * q + pr) * NQ + lane] = hw;
+                uint32_t wd[CPL];
+#pragma unroll
+                for (int k = 0; k < NP; ++k) {
+                    const __half2 ha = __floats2half2_rn(X.x[2 * pr][k].x, X.x[2 * pr + 1][k].x);
+                    const __half2 hb = __floats2half2_rn(X.x[2 * pr][k].y, X.x[2 * pr + 1][k].y);
+                    wd[2 * k] = *reinterpret_cast<const uint32_t *>(&ha);
+                    wd[2 * k + 1] = *reinterpret_cast<const uint32_t *>(&hb);
+                }
+                sts_words<CPL>(hiw + (2 * q + pr) * D + c0, wd);
             }
         }
         constexpr int QB = S::kBlock / 4;  // quads per block
 #pragma unroll 1
         for (int blk = 0; blk < (D - KH) / S::kBlock; ++blk) {  // INT8 rows
             const int q0 = blk * QB;
-            Quad X[QB];
+            Quad<CPL> X[QB];
 #pragma unroll
             for (int qq = 0; qq < QB; ++qq) {
                 load_lo(q0 + qq, X[qq]);
-                write_read(KH / 4 + q0 + qq, X[qq], e01, e23, o01, o23);
+                write_read(KH / 4 + q0 + qq, X[qq], e, o);
             }
-            // per-row absmax over the warp's 128 columns; lane r keeps row r
-            float mine = 0.0f;
+            // per-row absmax of the block; a select tree on the lane bits
+            // leaves row r's maximum over the warp's columns in lane r
+            float r[S::kBlock];
 #pragma unroll
             for (int qq = 0; qq < QB; ++qq)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const float r = warp_max_abs_nan(max_abs4_nan(X[qq].x[i][0], X[qq].x[i][1]));
-                    mine = lane == 4 * qq + i ? r : mine;
+                    float m;
+                    if constexpr (NP == 2) m = max_abs4_nan(X[qq].x[i][0], X[qq].x[i][1]);
+                    else m = max_abs2_nan(X[qq].x[i][0]);
+                    r[4 * qq + i] = warp_max_abs_nan(m);
                 }
-            __syncwarp();  // every lane has read the block's old scales
+            float t8[8], t4[4], t2[2];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) t8[i] = l0 ? r[2 * i + 1] : r[2 * i];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) t4[i] = l1 ? t8[2 * i + 1] : t8[2 * i];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) t2[i] = l2 ? t4[2 * i + 1] : t4[2 * i];
+            float mine = l3 ? t2[1] : t2[0];
+            if constexpr (WPT > 1) {  // combine the tile's warps (every warp gets the same maxima)
+                float *pb = part + (blk & 1) * WPT * S::kBlock;
+                if (lane < S::kBlock) pb[wt * S::kBlock + lane] = mine;
+                tile_sync();  // also: every warp has read the block's old scales
+                if (lane < S::kBlock)
+#pragma unroll
+                    for (int u = 0; u < WPT; ++u)
+                        if (u != wt) mine = max_nan(mine, pb[u * S::kBlock + lane]);
+            } else {
+                __syncwarp();  // every lane has read the block's old scales
+            }
             bool nonfinite = false;
             if (lane < S::kBlock) {
-                const float sv = __fdiv_rn(fmaxf(mine, 1e-8f), 127.0f);
+                const float sv = div127(fmaxf(mine, 1e-8f));
                 nsc[lane] = -sv;
-                ysc[lane] = __frcp_rn(sv);
-                scales[blk * S::kBlock + lane] = sv;
+                nsc[S::kBlock + lane] = __frcp_rn(sv);
+                if (wt == 0) scales[blk * S::kBlock + lane] = sv;
                 nonfinite = !(mine <= 3.402823466e38f);  // absmax inf or NaN
             }
             __syncwarp();
@@ -359,61 +457,55 @@ __global__ void __launch_bounds__(kMixedWarps * 32, 1)
 #pragma unroll
                 for (int qq = 0; qq < QB; ++qq) {
                     const float4 n4 = reinterpret_cast<const float4 *>(nsc)[qq];
-                    const float4 y4 = reinterpret_cast<const float4 *>(ysc)[qq];
+                    const float4 y4 = reinterpret_cast<const float4 *>(nsc + S::kBlock)[qq];
                     const float nr[4] = {n4.x, n4.y, n4.z, n4.w};
                     const float yr[4] = {y4.x, y4.y, y4.z, y4.w};
-                    uint32_t mb[4][4];  // [row][column]: RN(x/s) + 1.5 * 2^23
+                    uint32_t mb[4][CPL];  // [row][column]: RN(x/s) + 1.5 * 2^23
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
 #pragma unroll
-                        for (int hf = 0; hf < 2; ++hf) {
-                            const float2 x = X[qq].x[i][hf];
+                        for (int k = 0; k < NP; ++k) {
+                            const float2 x = X[qq].x[i][k];
                             const float2 y = make_float2(yr[i], yr[i]);
                             const float2 n = make_float2(nr[i], nr[i]);
                             float2 t = __fmul2_rn(x, y);
                             t = __ffma2_rn(__ffma2_rn(t, n, x), y, t);
                             t = __ffma2_rn(__ffma2_rn(t, n, x), y, t);
                             t = __fadd2_rn(t, make_float2(kRound, kRound));
-                            mb[i][2 * hf] = __float_as_uint(t.x);
-                            mb[i][2 * hf + 1] = __float_as_uint(t.y);
+                            mb[i][2 * k] = __float_as_uint(t.x);
+                            mb[i][2 * k + 1] = __float_as_uint(t.y);
                         }
                     }
-                    uint32_t wd[4];
+                    uint32_t wd[CPL];
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
+                    for (int c = 0; c < CPL; ++c)
                         wd[c] = __byte_perm(__byte_perm(mb[0][c], mb[1][c], 0x0040),
                                             __byte_perm(mb[2][c], mb[3][c], 0x0040), 0x5410);
-                    lo4[(q0 + qq) * NQ + lane] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+                    sts_words<CPL>(low + (q0 + qq) * D + c0, wd);
                 }
             } else {  // absmax inf or NaN somewhere in the block: literal IEEE division
 #pragma unroll
-                for (int qq = 0; qq < QB; ++qq) {
-                    uint32_t wd[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float sv = -nsc[4 * qq + i];
-                        wd[0] |= quant_exact(X[qq].x[i][0].x, sv) << (8 * i);
-                        wd[1] |= quant_exact(X[qq].x[i][0].y, sv) << (8 * i);
-                        wd[2] |= quant_exact(X[qq].x[i][1].x, sv) << (8 * i);
-                        wd[3] |= quant_exact(X[qq].x[i][1].y, sv) << (8 * i);
-                    }
-                    lo4[(q0 + qq) * NQ + lane] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
-                }
+                for (int qq = 0; qq < QB; ++qq)
+                    quant_rows_exact<CPL>(X[qq],
+                                          make_float4(-nsc[4 * qq], -nsc[4 * qq + 1], -nsc[4 * qq + 2],
+                                                      -nsc[4 * qq + 3]),
+                                          low + (q0 + qq) * D + c0);
             }
             __syncwarp();  // -s and 1/s are rewritten by the next block
         }
         if (P.o) {
-            TO *og = static_cast<TO *>(P.o) + ((size_t)b * Hv + h) * D + 4 * lane;
-            store_from_f32<TO>(og, o01.x);
-            store_from_f32<TO>(og + 1, o01.y);
-            store_from_f32<TO>(og + 2, o23.x);
-            store_from_f32<TO>(og + 3, o23.y);
+            TO *og = static_cast<TO *>(P.o) + ((size_t)b * Hv + h) * D + c0;
+#pragma unroll
+            for (int k = 0; k < NP; ++k) {
+                store_from_f32<TO>(og + 2 * k, o[k].x);
+                store_from_f32<TO>(og + 2 * k + 1, o[k].y);
+            }
         }
 
         // ---- store the tile; the stage then takes tile j + NS ---------------
         fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
+        tile_sync();
+        if (tt == 0) {
             bulk_s2g(pool + ((size_t)slot * Hv + h) * S::kStateBytes, st, S::kStateBytes);
             bulk_store_commit();
             bulk_store_wait_read();
@@ -421,7 +513,7 @@ __global__ void __launch_bounds__(kMixedWarps * 32, 1)
         }
         __syncwarp();
     }
-    if (lane == 0) bulk_store_wait_all();
+    if (tt == 0) bulk_store_wait_all();
 }
 
 }  // namespace rs

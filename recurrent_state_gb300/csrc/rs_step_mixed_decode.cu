@@ -1,5 +1,5 @@
 // rs_step_mixed_decode.cu -- single decode steps on the mixed FP16/INT8
-// layout (dk = dv = 128, 16 FP16 rows per head): one warp per tile over a
+// layout (dk = dv = 128, 16 FP16 rows per head): a warp pair per tile over a
 // ring of shared-memory stages (rs_mixed_decode.cuh).
 #include "rs_mixed_decode.cuh"
 #include "../../include/recurrent_state.h"
@@ -8,22 +8,27 @@ namespace rs {
 
 namespace {
 
+// warps per tile: 2 (two columns per lane, 16 warps per CTA) or 1 (four)
+constexpr int kMixedWpt = 2;
+constexpr int kMixedSlots = 8;  // tile slots per CTA
+
 template <int D, int KHI, bool KDA, int MAXT, typename TI, typename TO>
 cudaError_t run(StepParamsPi &P, cudaStream_t s) {
     static_assert(MAXT == 1, "single decode steps");
-    using Sh = MixedWarpShape<D, KHI, KDA, TI>;
-    auto kern = mixed_decode_kernel<D, KHI, KDA, TI, TO>;
+    using Sh = MixedWarpShape<D, KHI, KDA, TI, kMixedWpt>;
+    auto kern = mixed_decode_kernel<D, KHI, KDA, TI, TO, kMixedWpt>;
     const int header = Sh::kHeader + (P.Hv * D + 127) / 128 * 128;
     const int smax = device_max_smem_optin();
-    // W warps and a ring of NS > W stages in the shared memory there is
-    int W = kMixedWarps, NS = 0;
-    for (; W >= 1; --W) {
-        const int avail = smax - header - W * Sh::kWarpBytes;
+    // NSLOT tile slots and a ring of NS > NSLOT stages in the shared memory there is
+    int NSLOT = kMixedSlots, NS = 0;
+    for (; NSLOT >= 1; --NSLOT) {
+        const int avail = smax - header - NSLOT * Sh::kSlotBytes;
         NS = avail > 0 ? avail / Sh::kStage : 0;
         if (NS > kMixedMaxStages) NS = kMixedMaxStages;
-        if (NS >= W + 1) break;
+        if (NS >= NSLOT + 1) break;
     }
-    if (W < 1) return cudaErrorNotSupported;
+    if (NSLOT < 1) return cudaErrorNotSupported;
+    const int W = NSLOT * kMixedWpt;
     const int items = P.B * P.Hv;
     int grid = device_sm_count();
     if (grid > items) grid = items;
@@ -31,7 +36,7 @@ cudaError_t run(StepParamsPi &P, cudaStream_t s) {
     P.header_bytes = header;
     P.region_bytes = Sh::kStage;
     P.stages = NS;
-    const int smem = header + W * Sh::kWarpBytes + NS * Sh::kStage;
+    const int smem = header + NSLOT * Sh::kSlotBytes + NS * Sh::kStage;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, W * 32, smem, s>>>(P);
