@@ -64,10 +64,14 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+# sources of the headline kernel (the FP32 step kernel at d = 128)
+HEADLINE_SOURCES = ("rs_device.cuh", "rs_internal.h", "rs_step.cuh", "rs_step_f32_d128.cu")
+
+
 def kernel_sources_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "recurrent_state_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in HEADLINE_SOURCES:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]

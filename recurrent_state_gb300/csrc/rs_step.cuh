@@ -64,7 +64,7 @@ struct StepShape {
     __host__ __device__ static constexpr int stage_bytes(int T) { return (kStatePad + T * kTokBytes + 127) / 128 * 128; }
     __host__ __device__ static constexpr int region_bytes(int T) {
         int r = stage_bytes(T);
-        r += T * kRowVecs * D * 4 + 32;  // row vectors, per-token decays (replay)
+        r += T * kRowVecs * D * 4 + 64;  // row vectors, per-token decays and strengths (replay)
         if (kMixed) r += kWarps * D * 4 + D * 12 + 128 + kStatePad;  // partials, s/-s/1/s, flag, out tile
         return (r + 127) / 128 * 128;
     }
@@ -280,7 +280,8 @@ __global__ void __launch_bounds__(step_threads(MAXT), 1)
     float *rowv = reinterpret_cast<float *>(region + S::stage_bytes(T));
     // rowv layout per token t: [K | BK | Q | V | A?] each D floats
     float *tok_alpha = rowv + T * S::kRowVecs * D;                  // [8] GDN decays (replay)
-    float *red = tok_alpha + 8;                                     // [kWarps][D]   (mixed)
+    float *tok_beta = tok_alpha + 8;                                // [8] write strengths (replay)
+    float *red = tok_beta + 8;                                      // [kWarps][D]   (mixed)
     float *scl = red + S::kWarps * D;                               // [D] row scales
     float *nscl = scl + D;                                          // [D] -scales
     float *rcp = nscl + D;                                          // [D] reciprocals
@@ -326,10 +327,25 @@ __global__ void __launch_bounds__(step_threads(MAXT), 1)
         }
     };
 
+    // Replay: thread t < n of the group holds token t's write strength (and
+    // GDN decay) of the next item in registers, loaded one item ahead; they
+    // reach shared memory at the start of that item.
+    auto tok_scalars = [&](int it, int32_t n, float &bt, float &at) {
+        bt = 0.0f;
+        at = 0.0f;
+        if (MAXT > 1 && tid < n && it < items) {
+            const size_t bti = ((size_t)(it / Hv) * T + tid) * Hv + (it - (it / Hv) * Hv);
+            bt = P.beta[bti];
+            if (!KDA) at = P.alpha[bti];
+        }
+    };
+
     int item = blockIdx.x * G + grp;
     int32_t cur_slot = item_slot(item), cur_n = item_n(item);
     if (tid == 0) issue(item, cur_slot, cur_n);
     uint32_t phase = 0;
+    float cur_bt, cur_at;
+    tok_scalars(item, cur_n, cur_bt, cur_at);
 
     for (; item < items; item += gstride) {
         const int b = item / Hv, h = item - (item / Hv) * Hv;
@@ -338,6 +354,14 @@ __global__ void __launch_bounds__(step_threads(MAXT), 1)
         const int32_t slot = cur_slot, n = cur_n;
         cur_slot = nxt_slot;
         cur_n = nxt_n;
+        if (MAXT > 1 && tid < MAXT) {  // visible after the barrier below
+            tok_beta[tid] = cur_bt;
+            tok_alpha[tid] = cur_at;
+        }
+        if constexpr (MAXT > 1) {
+            const int32_t nn = (nxt_n >= 0 && nxt_n <= T) ? nxt_n : 0;
+            tok_scalars(nxt, nn, cur_bt, cur_at);
+        }
         const bool slot_ok = slot >= 0 && (int64_t)slot < P.n_slots;
         const bool n_ok = n >= 0 && n <= T;
         if (!slot_ok || !n_ok || n == 0) {
@@ -349,8 +373,7 @@ __global__ void __launch_bounds__(step_threads(MAXT), 1)
             continue;
         }
         // Scalars of a single-token item, loaded before the wait so their
-        // latency hides.  Replay instances read them while building the row
-        // vectors instead, keeping registers for the state.
+        // latency hides.  Replay instances took theirs one item ahead.
         float beta0 = 0.0f, alpha0 = 0.0f;
         if constexpr (MAXT == 1) {
             beta0 = P.beta[(size_t)b * Hv + h];
@@ -387,9 +410,7 @@ __global__ void __launch_bounds__(step_threads(MAXT), 1)
                 const TI *vt = reinterpret_cast<const TI *>(tb + 2 * S::kVecBytes);
                 float *rv = rowv + t * S::kRowVecs * D;
                 const float kf = load_as_f32<TI>(kt + src);
-                const size_t bti = ((size_t)b * T + t) * Hv + h;
-                const float bt = MAXT == 1 ? beta0 : P.beta[bti];
-                if (!KDA && MAXT > 1 && tid == 0) tok_alpha[t] = P.alpha[bti];
+                const float bt = MAXT == 1 ? beta0 : tok_beta[t];
                 rv[tid] = kf;
                 rv[D + tid] = __fmul_rn(bt, kf);
                 rv[2 * D + tid] = load_as_f32<TI>(qt + src);
