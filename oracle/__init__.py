@@ -131,6 +131,18 @@ def _declare(L):
     L.orc_ckpt_restore.argtypes = [_I, _I, _I, _I, _I, _P, _P, _I, _P, _P, _I64,
                                    _I, _P, _I]
     L.orc_ckpt_restore.restype = _I
+    L.orc_ckpt_pack_heads.argtypes = [_I, _I, _I64, _P, _P, _I64, _I, _P, _P, _I, _P, _I]
+    L.orc_ckpt_pack_heads.restype = _I
+    L.orc_ckpt_restore_heads.argtypes = [_I, _I, _I64, _P, _P, _I, _P, _P, _I64, _I, _P, _I]
+    L.orc_ckpt_restore_heads.restype = _I
+    L.orc_ckpt_int8_codes_bytes.argtypes = [_I64, _I, _I]
+    L.orc_ckpt_int8_codes_bytes.restype = _I64
+    L.orc_ckpt_int8_slot_bytes.argtypes = [_I64, _I, _I]
+    L.orc_ckpt_int8_slot_bytes.restype = _I64
+    L.orc_ckpt_pack_int8.argtypes = [_I, _I, _I, _I, _I, _P, _P, _I64, _I, _P, _P, _I, _P, _I]
+    L.orc_ckpt_pack_int8.restype = _I
+    L.orc_ckpt_restore_int8.argtypes = [_I, _I, _I, _I, _I, _P, _P, _I, _P, _P, _I64, _I, _P, _I]
+    L.orc_ckpt_restore_int8.restype = _I
 
 
 # --------------------------------------------------------------------------
@@ -349,3 +361,50 @@ def ckpt_restore(keep, unit, ckpt, src_slots, pool, dst_slots):
                                 _ptr(_c(pool, np.float32)), pool.strides[0], n_slots,
                                 _ptr(_c(dst_slots, np.int32)), len(src_slots))
     return st
+
+
+def ckpt_pack_heads(keep, pool, src_slots, dst_slots, ckpt):
+    """Whole-head checkpoint of a packed pool: pool [L][n_slots][Hv][head_bytes]
+    uint8, keep [L][Hv]; ckpt [n_ckpt][o_L * head_bytes] uint8."""
+    keep = _c(np.ascontiguousarray(keep, np.uint8), np.uint8)
+    L, n_slots, Hv, hb = pool.shape
+    return lib().orc_ckpt_pack_heads(L, Hv, hb, _ptr(keep), _ptr(_c(pool, np.uint8)), pool.strides[0],
+                                     n_slots, _ptr(_c(src_slots, np.int32)),
+                                     _ptr(_c(dst_slots, np.int32)), len(src_slots),
+                                     _ptr(_c(ckpt, np.uint8)), ckpt.shape[0])
+
+
+def ckpt_restore_heads(keep, ckpt, src_slots, pool, dst_slots):
+    keep = _c(np.ascontiguousarray(keep, np.uint8), np.uint8)
+    L, n_slots, Hv, hb = pool.shape
+    return lib().orc_ckpt_restore_heads(L, Hv, hb, _ptr(keep), _ptr(_c(ckpt, np.uint8)), ckpt.shape[0],
+                                        _ptr(_c(src_slots, np.int32)), _ptr(_c(pool, np.uint8)),
+                                        pool.strides[0], n_slots, _ptr(_c(dst_slots, np.int32)),
+                                        len(src_slots))
+
+
+def ckpt_int8_layout(n_kept, unit, dk, dv):
+    """(codes bytes, slot bytes) of one INT8 checkpoint slot."""
+    rows = 1 if unit else dk
+    return (lib().orc_ckpt_int8_codes_bytes(n_kept, rows, dv),
+            lib().orc_ckpt_int8_slot_bytes(n_kept, rows, dv))
+
+
+def ckpt_pack_int8(keep, unit, pool, src_slots, dst_slots, ckpt):
+    """INT8 checkpoint of an FP32 pool [L][n_slots][Hv][dk][dv]; ckpt
+    [n_ckpt][slot_bytes] uint8 (codes, then scales)."""
+    keep = _c(np.ascontiguousarray(keep, np.uint8), np.uint8)
+    L, n_slots, Hv, dk, dv = pool.shape
+    return lib().orc_ckpt_pack_int8(L, Hv, dk, dv, unit, _ptr(keep), _ptr(_c(pool, np.float32)),
+                                    pool.strides[0] // 4, n_slots, _ptr(_c(src_slots, np.int32)),
+                                    _ptr(_c(dst_slots, np.int32)), len(src_slots),
+                                    _ptr(_c(ckpt, np.uint8)), ckpt.shape[0])
+
+
+def ckpt_restore_int8(keep, unit, ckpt, src_slots, pool, dst_slots):
+    keep = _c(np.ascontiguousarray(keep, np.uint8), np.uint8)
+    L, n_slots, Hv, dk, dv = pool.shape
+    return lib().orc_ckpt_restore_int8(L, Hv, dk, dv, unit, _ptr(keep), _ptr(_c(ckpt, np.uint8)),
+                                       ckpt.shape[0], _ptr(_c(src_slots, np.int32)),
+                                       _ptr(_c(pool, np.float32)), pool.strides[0] // 4, n_slots,
+                                       _ptr(_c(dst_slots, np.int32)), len(src_slots))

@@ -495,3 +495,175 @@ int orc_ckpt_restore(int L, int Hv, int dk, int dv, int unit, const uint8_t *kee
     }
     return status;
 }
+
+/* ---------------------------------------------------------------------------
+ * Checkpoints of whole packed heads ([DAMP] §5.2 layout, [dasc] §4.1 Scheme 2
+ * ragged packing): a unit is one head of head_bytes bytes (a mixed tile with
+ * its FP16 rows, INT8 codes and scales, copied verbatim).  Same order and
+ * offsets as orc_ckpt_pack with head units; restore writes zero bytes to
+ * omitted heads, which decode as the zero state.
+ * ------------------------------------------------------------------------- */
+int orc_ckpt_pack_heads(int L, int Hv, int64_t head_bytes, const uint8_t *keep,
+                        const uint8_t *pool, int64_t layer_stride, int n_pool_slots,
+                        const int32_t *src_slots, const int32_t *dst_ckpt_slots, int n,
+                        uint8_t *ckpt, int n_ckpt_slots)
+{
+    int64_t off[1025];
+    size_t ub = (size_t)head_bytes, slot_bytes = (size_t)Hv * ub;
+    int status = 0, i, l, x;
+    if (L > 1024) return -1;
+    orc_plan_offsets(L, Hv, 1, 0, keep, off);
+    for (i = 0; i < n; ++i) {
+        int32_t s = src_slots[i], d = dst_ckpt_slots[i];
+        if (s < 0 || s >= n_pool_slots) { status |= 1; continue; }
+        if (d < 0 || d >= n_ckpt_slots) { status |= 4; continue; }
+        for (l = 0; l < L; ++l) {
+            int64_t j = 0;
+            for (x = 0; x < Hv; ++x) {
+                if (!keep[(size_t)l * Hv + x]) continue;
+                memcpy(ckpt + ((size_t)d * off[L] + (size_t)(off[l] + j)) * ub,
+                       pool + (size_t)l * layer_stride + (size_t)s * slot_bytes + (size_t)x * ub, ub);
+                ++j;
+            }
+        }
+    }
+    return status;
+}
+
+int orc_ckpt_restore_heads(int L, int Hv, int64_t head_bytes, const uint8_t *keep,
+                           const uint8_t *ckpt, int n_ckpt_slots, const int32_t *src_ckpt_slots,
+                           uint8_t *pool, int64_t layer_stride, int n_pool_slots,
+                           const int32_t *dst_slots, int n)
+{
+    int64_t off[1025];
+    size_t ub = (size_t)head_bytes, slot_bytes = (size_t)Hv * ub;
+    int status = 0, i, l, x;
+    if (L > 1024) return -1;
+    orc_plan_offsets(L, Hv, 1, 0, keep, off);
+    for (i = 0; i < n; ++i) {
+        int32_t s = src_ckpt_slots[i], d = dst_slots[i];
+        if (s < 0 || s >= n_ckpt_slots) { status |= 4; continue; }
+        if (d < 0 || d >= n_pool_slots) { status |= 1; continue; }
+        for (l = 0; l < L; ++l) {
+            int64_t j = 0;
+            for (x = 0; x < Hv; ++x) {
+                uint8_t *dst = pool + (size_t)l * layer_stride + (size_t)d * slot_bytes + (size_t)x * ub;
+                if (keep[(size_t)l * Hv + x]) {
+                    memcpy(dst, ckpt + ((size_t)s * off[L] + (size_t)(off[l] + j)) * ub, ub);
+                    ++j;
+                } else {
+                    memset(dst, 0, ub);
+                }
+            }
+        }
+    }
+    return status;
+}
+
+/* ---------------------------------------------------------------------------
+ * INT8 state checkpoint ([dasc] Appendix E.1, Eq. 8): the retained units of
+ * an FP32 state are quantised once at insertion and dequantised once on reuse.
+ * One scale per (layer, head, key channel), shared over dv: in this oracle's
+ * orientation (rows = key channels) that is one scale per row, the same
+ * symmetric quantiser as the mixed layout's INT8 rows (orc_quantise_row).
+ *
+ * A unit covers R rows of dv values: R = dk for a head (GDN), R = 1 for a
+ * key channel (KDA).  Checkpoint slot layout (reading fixed here; the pages
+ * give the format, not the byte order):
+ *     codes  [o_L][R][dv]  int8, units in packed order (orc_plan_offsets),
+ *     scales [o_L][R]      float32,
+ * the scales starting right after the codes; a slot occupies
+ * orc_ckpt_int8_slot_bytes() bytes (codes + scales, rounded up to 16).
+ * Restore: omitted units are +0.0; retained rows are codes[v] * scale.
+ * ------------------------------------------------------------------------- */
+int64_t orc_ckpt_int8_codes_bytes(int64_t n_kept, int rows, int dv)
+{
+    return n_kept * rows * dv;
+}
+
+int64_t orc_ckpt_int8_slot_bytes(int64_t n_kept, int rows, int dv)
+{
+    int64_t b = n_kept * rows * ((int64_t)dv + 4);
+    return (b + 15) / 16 * 16;
+}
+
+int orc_ckpt_pack_int8(int L, int Hv, int dk, int dv, int unit, const uint8_t *keep,
+                       const float *pool, int64_t layer_stride_floats, int n_pool_slots,
+                       const int32_t *src_slots, const int32_t *dst_ckpt_slots, int n,
+                       uint8_t *ckpt, int n_ckpt_slots)
+{
+    int64_t off[1025];
+    int nu = units_per_layer(unit, Hv, dk), R = unit ? 1 : dk, i, l, x, r;
+    size_t slot_floats = (size_t)Hv * dk * dv;
+    int64_t sb, cb;
+    int status = 0;
+    if (L > 1024) return -1;
+    orc_plan_offsets(L, Hv, dk, unit, keep, off);
+    sb = orc_ckpt_int8_slot_bytes(off[L], R, dv);
+    cb = orc_ckpt_int8_codes_bytes(off[L], R, dv);
+    for (i = 0; i < n; ++i) {
+        int32_t s = src_slots[i], d = dst_ckpt_slots[i];
+        if (s < 0 || s >= n_pool_slots) { status |= 1; continue; }
+        if (d < 0 || d >= n_ckpt_slots) { status |= 4; continue; }
+        for (l = 0; l < L; ++l) {
+            int64_t j = 0;
+            for (x = 0; x < nu; ++x) {
+                const float *src;
+                if (!keep[(size_t)l * nu + x]) continue;
+                /* unit x: head x (R = dk rows) or row x of the slot (R = 1) */
+                src = pool + (size_t)l * layer_stride_floats + (size_t)s * slot_floats
+                      + (size_t)x * R * dv;
+                for (r = 0; r < R; ++r) {
+                    int64_t row = (off[l] + j) * R + r;
+                    int8_t *codes = (int8_t *)(ckpt + (size_t)d * sb + (size_t)row * dv);
+                    float sc;
+                    orc_quantise_row(dv, src + (size_t)r * dv, codes, &sc);
+                    memcpy(ckpt + (size_t)d * sb + (size_t)cb + (size_t)row * 4, &sc, 4);
+                }
+                ++j;
+            }
+        }
+    }
+    return status;
+}
+
+int orc_ckpt_restore_int8(int L, int Hv, int dk, int dv, int unit, const uint8_t *keep,
+                          const uint8_t *ckpt, int n_ckpt_slots, const int32_t *src_ckpt_slots,
+                          float *pool, int64_t layer_stride_floats, int n_pool_slots,
+                          const int32_t *dst_slots, int n)
+{
+    int64_t off[1025];
+    int nu = units_per_layer(unit, Hv, dk), R = unit ? 1 : dk, i, l, x, r;
+    size_t slot_floats = (size_t)Hv * dk * dv;
+    int64_t sb, cb;
+    int status = 0;
+    if (L > 1024) return -1;
+    orc_plan_offsets(L, Hv, dk, unit, keep, off);
+    sb = orc_ckpt_int8_slot_bytes(off[L], R, dv);
+    cb = orc_ckpt_int8_codes_bytes(off[L], R, dv);
+    for (i = 0; i < n; ++i) {
+        int32_t s = src_ckpt_slots[i], d = dst_slots[i];
+        if (s < 0 || s >= n_ckpt_slots) { status |= 4; continue; }
+        if (d < 0 || d >= n_pool_slots) { status |= 1; continue; }
+        for (l = 0; l < L; ++l) {
+            int64_t j = 0;
+            for (x = 0; x < nu; ++x) {
+                float *dst = pool + (size_t)l * layer_stride_floats + (size_t)d * slot_floats
+                             + (size_t)x * R * dv;
+                if (!keep[(size_t)l * nu + x]) {
+                    memset(dst, 0, (size_t)R * dv * 4);
+                    continue;
+                }
+                for (r = 0; r < R; ++r) {
+                    int64_t row = (off[l] + j) * R + r;
+                    float sc;
+                    memcpy(&sc, ckpt + (size_t)s * sb + (size_t)cb + (size_t)row * 4, 4);
+                    orc_dequantise_row(dv, (const int8_t *)(ckpt + (size_t)s * sb + (size_t)row * dv),
+                                       sc, dst + (size_t)r * dv);
+                }
+                ++j;
+            }
+        }
+    }
+    return status;
+}

@@ -19,6 +19,7 @@ import oracle as orc
 from recurrent_state_gb300 import inputs as gen
 
 from . import test_oracle_ckpt as ck
+from . import test_oracle_ckpt_int8 as i8
 from . import test_oracle_mixed as mx
 from . import test_oracle_quant as qt
 from . import test_oracle_recurrence as rc
@@ -47,6 +48,9 @@ CHECKS = [
     ("mixed_perm", mx.test_permutation_is_applied_to_inputs),
     ("mixed_bound", lambda: mx.test_mixed_step_within_local_quantisation_error(True)),
     ("mixed_replay", lambda: mx.test_mixed_replay_requantises_once(True)),
+    ("int8_closed", lambda: i8.test_constant_rows_closed_form_and_order(1)),
+    ("int8_roundtrip", lambda: i8.test_roundtrip_error_bound_and_zero_fill(0)),
+    ("heads", i8.test_whole_head_pack_matches_fp32_pack),
 ]
 
 READOUT_BLOCK = """    /* readout o = S^T q on the updated state */
@@ -99,6 +103,14 @@ MUTATIONS = {
          "            orc_mixed_unpack(dk, dv, khi, tile, T);\n        }\n"
          "        orc_mixed_pack(dk, dv, khi, T, tile);")],
     "replay_skips_first": [("for (t = 0; t < n; ++t) {", "for (t = 1; t < n; ++t) {")],
+    "int8_scale_per_unit": [
+        ("memcpy(ckpt + (size_t)d * sb + (size_t)cb + (size_t)row * 4, &sc, 4);",
+         "memcpy(ckpt + (size_t)d * sb + (size_t)cb + (size_t)(off[l] + j) * 4, &sc, 4);")],
+    "int8_restore_no_zero_fill": [("memset(dst, 0, (size_t)R * dv * 4);", "(void)dst;")],
+    "int8_dequant_unscaled": [("                                       sc, dst + (size_t)r * dv);",
+                               "                                       1.0f, dst + (size_t)r * dv);")],
+    "heads_unit_is_fp32_head": [("size_t ub = (size_t)head_bytes, slot_bytes = (size_t)Hv * ub;\n    int status = 0, i, l, x;\n    if (L > 1024) return -1;\n    orc_plan_offsets(L, Hv, 1, 0, keep, off);\n    for (i = 0; i < n; ++i) {\n        int32_t s = src_slots[i]",
+                                 "size_t ub = (size_t)head_bytes, slot_bytes = (size_t)Hv * ub * 2;\n    int status = 0, i, l, x;\n    if (L > 1024) return -1;\n    orc_plan_offsets(L, Hv, 1, 0, keep, off);\n    for (i = 0; i < n; ++i) {\n        int32_t s = src_slots[i]")],
 }
 
 
