@@ -362,7 +362,8 @@ def _time(torch, fn, iters, warm=3):
 
 
 EXTRA = ("gdn_fp32", "kda_fp32", "kda_mixed", "gdn_mixed", "replay_mixed", "replay_fp32",
-         "pack_gdn", "restore_gdn", "pack_kda", "restore_kda")
+         "pack_gdn", "restore_gdn", "pack_kda", "restore_kda", "pack_int8_gdn", "restore_int8_gdn",
+         "pack_int8_kda", "restore_int8_kda", "pack_mixed", "restore_mixed")
 
 
 def extra_kernels(args, rs, torch, dev, peak, world, only=None):
@@ -463,7 +464,7 @@ def extra_kernels(args, rs, torch, dev, peak, world, only=None):
 
     # dasc pack / restore: 36 layers, 64 checkpoints, 64 pool slots
     for unit, p, name in ((0, 0.5, "gdn"), (1, 0.45, "kda")):
-        if not want & {f"pack_{name}", f"restore_{name}"}:
+        if not want & {f"pack_{name}", f"restore_{name}", f"pack_int8_{name}", f"restore_int8_{name}"}:
             continue
         nslot = n = getattr(args, "slots", None) or 64
         L, Hv, d = 36, 32, 128
@@ -486,6 +487,47 @@ def extra_kernels(args, rs, torch, dev, peak, world, only=None):
             sec = _time(torch, lambda i: rs.ckpt_restore(plan, ckpt, dd, big, sd), max(3, iters // 10),
                         warm)
             rec(f"ckpt_restore_{name}", sec, kept_bytes + full_bytes, 0, {"checkpoints_per_s": n / sec})
+        del ckpt
+        # dasc INT8 checkpoint of the same plan: quantise at pack, dequantise at restore
+        if want & {f"pack_int8_{name}", f"restore_int8_{name}"}:
+            ck8 = plan.empty_int8_ckpt_pool(n, device=dev)
+            rows = plan.int8_codes_bytes // d
+            int8_bytes = (plan.int8_codes_bytes + 4 * rows) * n
+            kept_f32 = rows * d * 4 * n
+            rs.ckpt_pack_int8(plan, big, sd, dd, ck8)
+            if f"pack_int8_{name}" in want:
+                sec = _time(torch, lambda i: rs.ckpt_pack_int8(plan, big, sd, dd, ck8), max(3, iters // 10),
+                            warm)
+                rec(f"ckpt_pack_int8_{name}", sec, kept_f32 + int8_bytes, 0,
+                    {"checkpoints_per_s": n / sec, "bytes_vs_fp32": kept_f32 / int8_bytes})
+            if f"restore_int8_{name}" in want:
+                sec = _time(torch, lambda i: rs.ckpt_restore_int8(plan, ck8, dd, big, sd),
+                            max(3, iters // 10), warm)
+                rec(f"ckpt_restore_int8_{name}", sec, int8_bytes + full_bytes, 0, {"checkpoints_per_s": n / sec})
+            del ck8
+        del big
+        torch.cuda.empty_cache()
+    # whole mixed FP16/INT8 heads (18,880 B) in and out of checkpoints
+    if want & {"pack_mixed", "restore_mixed"}:
+        nslot = n = getattr(args, "slots", None) or 64
+        L, Hv, d = 36, 32, 128
+        keep = gen.keep_mask(L, Hv, 0.5, seed=0)
+        src, dst = gen.ckpt_slots(nslot, n, seed=0)
+        hi = gen.hi_rows(Hv, d, 16, seed=1)
+        mix = rs.Layout("mixed", d, Hv, Hv, k_hi=16, hi_rows=hi)
+        plan = rs.Plan(mix, keep, "head").upload()
+        big = torch.randint(0, 255, (L, nslot, Hv, mix.head_bytes), dtype=torch.uint8, device=dev)
+        ckpt = plan.empty_ckpt_pool(n, device=dev)
+        sd, dd = to_dev(src), to_dev(dst)
+        kept_bytes = int(plan.offsets[-1]) * plan.unit_bytes * n
+        full_bytes = L * Hv * mix.head_bytes * n
+        rs.ckpt_pack(plan, big, sd, dd, ckpt)
+        if "pack_mixed" in want:
+            sec = _time(torch, lambda i: rs.ckpt_pack(plan, big, sd, dd, ckpt), max(3, iters // 10), warm)
+            rec("ckpt_pack_mixed_gdn", sec, 2 * kept_bytes, 0, {"checkpoints_per_s": n / sec})
+        if "restore_mixed" in want:
+            sec = _time(torch, lambda i: rs.ckpt_restore(plan, ckpt, dd, big, sd), max(3, iters // 10), warm)
+            rec("ckpt_restore_mixed_gdn", sec, kept_bytes + full_bytes, 0, {"checkpoints_per_s": n / sec})
         del big, ckpt
         torch.cuda.empty_cache()
     return out

@@ -224,10 +224,14 @@ rs_status rs_state_convert(const rs_layout *src_l, const void *src_pool,
 
 /* Selection plan ([dasc] §4.1): keep (host uint8 [L][n_units], 0/1) marks
  * the retained units of each of num_layers layers.  unit = RS_UNIT_HEAD
- * (GDN: n_units = Hv, unit = one head, 4*dk*dv bytes) or RS_UNIT_CHANNEL
- * (KDA: n_units = Hv*dk, unit = row (h, u) of dv floats).  Only the FP32
- * layout is packed.  Host only: offsets o_0 = 0, o_l = o_{l-1} + r_l
- * ([dasc] Appendix B "Ragged (Scheme 2)") are computed here. */
+ * (GDN: n_units = Hv, unit = one head of the layout's head bytes) or
+ * RS_UNIT_CHANNEL (KDA: n_units = Hv*dk, unit = row (h, u) of dv floats).
+ * FP32 layouts take either unit.  A mixed FP16/INT8 layout ([DAMP] §5.2)
+ * takes head units only: a head is copied verbatim with its FP16 rows, INT8
+ * rows and scales; its rows are interleaved by word, so a key channel is not
+ * a unit of its own (RS_ERR_UNSUPPORTED).  Host only: offsets o_0 = 0,
+ * o_l = o_{l-1} + r_l ([dasc] Appendix B "Ragged (Scheme 2)") are computed
+ * here. */
 rs_status rs_plan_create(rs_plan **out, const rs_layout *l, int32_t num_layers,
                          int32_t unit, const uint8_t *keep);
 rs_status rs_plan_destroy(rs_plan *p);
@@ -285,6 +289,41 @@ rs_status rs_ckpt_pack_noalloc(const rs_plan *p, const void *pool, int64_t layer
                                int64_t n_pool_slots, const int32_t *src_slots,
                                const int32_t *dst_ckpt_slots, int32_t n, void *ckpt_pool,
                                int64_t n_ckpt_slots, int32_t *status, void *stream);
+
+/* ---- dasc INT8 state checkpoint ------------------------------------------
+ * [dasc] Appendix E.1 Eq. 8: an FP32 state is quantised once when the
+ * checkpoint is written and dequantised once when it is reused.  Each row of
+ * a retained unit (key channel u of head h: the [dasc] scale index (l, h, k)
+ * shared over dv) gets a = max_v |S[u][v]|, s = max(a, 1e-8) / 127 and codes
+ * clip(round_half_even(S / s), -127, 127) (FP32 maximum, division and
+ * rounding; a NaN absmax takes the 1e-8 floor, as in the mixed layout);
+ * reuse writes S^ = code * s.  The plan must be on an FP32 layout; units are
+ * those of the plan (a head: dk rows; a key channel: 1 row).
+ *
+ * Checkpoint slot layout:
+ *   codes  int8  [o_L][rows_per_unit][dv]   units in packed order
+ *   scales f32   [o_L][rows_per_unit]       from byte codes_bytes on
+ * and the slot is slot_bytes = codes + scales rounded up to 16 bytes (16,896
+ * B per 128 x 128 head, 3.88x smaller than FP32). */
+rs_status rs_ckpt_int8_bytes(const rs_plan *p, int64_t *codes_bytes, int64_t *slot_bytes);
+
+/* INT8 pack: as rs_ckpt_pack (same slots, order, status bits and argument
+ * rules), quantising each retained row into checkpoint slot
+ * dst_ckpt_slots[i] of ckpt_pool (device, [n_ckpt_slots][slot_bytes]).
+ * Requires rs_plan_upload and dv = 64 or 128. */
+rs_status rs_ckpt_pack_int8(const rs_plan *p, const void *pool, int64_t layer_stride_bytes,
+                            int64_t n_pool_slots, const int32_t *src_slots,
+                            const int32_t *dst_ckpt_slots, int32_t n, void *ckpt_pool,
+                            int64_t n_ckpt_slots, int32_t *status, void *stream);
+
+/* INT8 restore, dasc-nr: every row of every layer of pool slot dst_slots[i]
+ * is written, retained rows dequantised from checkpoint slot
+ * src_ckpt_slots[i], omitted rows +0.0. */
+rs_status rs_ckpt_restore_int8(const rs_plan *p, const void *ckpt_pool, int64_t n_ckpt_slots,
+                               const int32_t *src_ckpt_slots, void *pool,
+                               int64_t layer_stride_bytes, int64_t n_pool_slots,
+                               const int32_t *dst_slots, int32_t n, int32_t *status,
+                               void *stream);
 
 #ifdef __cplusplus
 }

@@ -2,7 +2,7 @@
 
 Batched decode-step update of gated delta-rule linear attention (GDN and KDA)
 on FP32 or mixed FP16/INT8 state pools, speculative-token replay, and ragged
-dasc checkpoint pack/restore.  Every step runs in the CUDA library built from
+dasc checkpoint pack/restore (verbatim units, or the INT8 checkpoint).  Every step runs in the CUDA library built from
 ``csrc/`` and reached through the C ABI of ``include/recurrent_state.h``;
 this package only marshals torch tensors into that ABI (PyTorch provides
 device memory and streams).
@@ -16,13 +16,14 @@ import importlib
 
 __all__ = [
     "Layout", "Plan", "gdn_decode_update", "kda_decode_update", "spec_replay_update",
-    "state_convert", "ckpt_pack", "ckpt_restore", "RsError", "build", "inputs",
+    "state_convert", "ckpt_pack", "ckpt_restore", "ckpt_pack_int8", "ckpt_restore_int8", "RsError",
+    "build", "inputs",
 ]
 
 _LAZY = {
     "Layout": "api", "Plan": "api", "gdn_decode_update": "api", "kda_decode_update": "api",
     "spec_replay_update": "api", "state_convert": "api", "ckpt_pack": "api",
-    "ckpt_restore": "api", "RsError": "_abi",
+    "ckpt_restore": "api", "ckpt_pack_int8": "api", "ckpt_restore_int8": "api", "RsError": "_abi",
 }
 
 

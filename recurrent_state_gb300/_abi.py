@@ -35,6 +35,7 @@ EXPORTS = (
     "rs_gdn_decode_update", "rs_kda_decode_update", "rs_spec_replay_update", "rs_state_convert",
     "rs_plan_create", "rs_plan_destroy", "rs_plan_offsets", "rs_plan_upload",
     "rs_ckpt_pack", "rs_ckpt_restore", "rs_ckpt_pack_noalloc",
+    "rs_ckpt_int8_bytes", "rs_ckpt_pack_int8", "rs_ckpt_restore_int8",
 )
 
 
@@ -101,6 +102,9 @@ def _declare(L):
     L.rs_ckpt_pack.argtypes = [_P, _P, _I64, _I64, _P, _P, _I32, _P, _I64, _P, _P]
     L.rs_ckpt_restore.argtypes = [_P, _P, _I64, _P, _P, _I64, _I64, _P, _I32, _P, _P]
     L.rs_ckpt_pack_noalloc.argtypes = [_P, _P, _I64, _I64, _P, _P, _I32, _P, _I64, _P, _P]
+    L.rs_ckpt_int8_bytes.argtypes = [_P, _P, _P]
+    L.rs_ckpt_pack_int8.argtypes = [_P, _P, _I64, _I64, _P, _P, _I32, _P, _I64, _P, _P]
+    L.rs_ckpt_restore_int8.argtypes = [_P, _P, _I64, _P, _P, _I64, _I64, _P, _I32, _P, _P]
     for name in EXPORTS:
         if name not in ("rs_status_string", "rs_last_cuda_error", "rs_version"):
             getattr(L, name).restype = _I32

@@ -167,7 +167,8 @@ def state_convert(src_layout, src_pool, dst_layout, dst_pool, slots, status=None
 
 
 class Plan:
-    """A dasc selection plan (``rs_plan``) over an FP32 layout."""
+    """A dasc selection plan (``rs_plan``): head or key-channel units of an
+    FP32 layout, or head units of a mixed layout."""
 
     def __init__(self, layout: Layout, keep: np.ndarray, unit: str):
         keep = np.ascontiguousarray(keep, np.uint8)
@@ -185,6 +186,11 @@ class Plan:
         self.unit_bytes = int(ub.value)
         self.ckpt_slot_bytes = int(off[-1]) * self.unit_bytes
         self._uploaded = False
+        self.int8_codes_bytes = self.int8_slot_bytes = None
+        if layout.kind == _abi.RS_LAYOUT_FP32:
+            cb, sb = ctypes.c_int64(), ctypes.c_int64()
+            check(_abi.lib().rs_ckpt_int8_bytes(h, ctypes.byref(cb), ctypes.byref(sb)), "rs_ckpt_int8_bytes")
+            self.int8_codes_bytes, self.int8_slot_bytes = int(cb.value), int(sb.value)
 
     def upload(self):
         check(_abi.lib().rs_plan_upload(self._h), "rs_plan_upload")
@@ -193,6 +199,10 @@ class Plan:
 
     def empty_ckpt_pool(self, n_ckpt_slots: int, device="cuda") -> torch.Tensor:
         return torch.empty((n_ckpt_slots, self.ckpt_slot_bytes), dtype=torch.uint8, device=device)
+
+    def empty_int8_ckpt_pool(self, n_ckpt_slots: int, device="cuda") -> torch.Tensor:
+        """INT8 checkpoint slots: codes [o_L][rows][dv] int8, then scales f32."""
+        return torch.empty((n_ckpt_slots, self.int8_slot_bytes), dtype=torch.uint8, device=device)
 
     def __del__(self):
         h = getattr(self, "_h", None)
@@ -234,3 +244,29 @@ def ckpt_restore(plan: Plan, ckpt_pool, src_ckpt_slots, pool, dst_slots, status=
                                      _ptr(src_ckpt_slots), _ptr(pool), stride, n_pool,
                                      _ptr(dst_slots), dst_slots.numel(), _ptr(status),
                                      _stream(stream)), "rs_ckpt_restore")
+
+
+def ckpt_pack_int8(plan: Plan, pool, src_slots, dst_ckpt_slots, ckpt_pool, status=None, stream=None):
+    """dasc INT8 checkpoint: quantise the retained rows of FP32 pool slots."""
+    n_pool, stride = _layer_pool(pool, plan.layout)
+    _dev(src_slots, "src_slots", torch.int32)
+    _dev(dst_ckpt_slots, "dst_ckpt_slots", torch.int32)
+    _dev(ckpt_pool, "ckpt_pool")
+    _dev(status, "status", torch.int32)
+    check(_abi.lib().rs_ckpt_pack_int8(plan._h, _ptr(pool), stride, n_pool, _ptr(src_slots),
+                                       _ptr(dst_ckpt_slots), src_slots.numel(), _ptr(ckpt_pool),
+                                       ckpt_pool.shape[0], _ptr(status), _stream(stream)),
+          "rs_ckpt_pack_int8")
+
+
+def ckpt_restore_int8(plan: Plan, ckpt_pool, src_ckpt_slots, pool, dst_slots, status=None, stream=None):
+    """dasc INT8 checkpoint reuse: dequantise into FP32 pool slots, omitted rows zero."""
+    n_pool, stride = _layer_pool(pool, plan.layout)
+    _dev(src_ckpt_slots, "src_ckpt_slots", torch.int32)
+    _dev(dst_slots, "dst_slots", torch.int32)
+    _dev(ckpt_pool, "ckpt_pool")
+    _dev(status, "status", torch.int32)
+    check(_abi.lib().rs_ckpt_restore_int8(plan._h, _ptr(ckpt_pool), ckpt_pool.shape[0],
+                                          _ptr(src_ckpt_slots), _ptr(pool), stride, n_pool,
+                                          _ptr(dst_slots), dst_slots.numel(), _ptr(status),
+                                          _stream(stream)), "rs_ckpt_restore_int8")

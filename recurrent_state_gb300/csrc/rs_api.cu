@@ -13,6 +13,7 @@
 
 #include "../../include/recurrent_state.h"
 #include "rs_internal.h"
+#include "rs_ckpt_int8.h"
 
 struct rs_layout {
     rs_layout_params p;
@@ -300,7 +301,7 @@ rs_status rs_plan_create(rs_plan **out, const rs_layout *l, int32_t num_layers, 
     if (!out || !l || !keep || num_layers <= 0 || num_layers >= 2048) return RS_ERR_INVALID_ARG;
     *out = nullptr;
     if (unit != RS_UNIT_HEAD && unit != RS_UNIT_CHANNEL) return RS_ERR_INVALID_ARG;
-    if (l->p.kind != RS_LAYOUT_FP32) return RS_ERR_UNSUPPORTED;
+    if (l->p.kind != RS_LAYOUT_FP32 && unit != RS_UNIT_HEAD) return RS_ERR_UNSUPPORTED;
     rs_plan *p = new (std::nothrow) rs_plan;
     if (!p) return RS_ERR_INVALID_ARG;
     p->L = num_layers;
@@ -427,6 +428,84 @@ rs_status rs_ckpt_restore(const rs_plan *p, const void *ckpt_pool, int64_t n_ckp
                           void *stream) {
     return ckpt_common(p, false, ckpt_pool, pool, layer_stride_bytes, n_pool_slots, n_ckpt_slots,
                        dst_slots, src_ckpt_slots, n, status, stream);
+}
+
+static int64_t int8_rows_per_unit(const rs_plan *p) { return p->unit == RS_UNIT_HEAD ? p->dk : 1; }
+// A plan on the FP32 layout: its heads are dk x dv floats (a mixed head is smaller).
+static bool plan_fp32(const rs_plan *p) { return p->head_bytes == (size_t)p->dk * p->dv * 4; }
+
+rs_status rs_ckpt_int8_bytes(const rs_plan *p, int64_t *codes_bytes, int64_t *slot_bytes) {
+    if (!p) return RS_ERR_INVALID_ARG;
+    if (!plan_fp32(p)) return RS_ERR_UNSUPPORTED;
+    const int64_t rows = p->offsets.back() * int8_rows_per_unit(p);
+    if (codes_bytes) *codes_bytes = rows * p->dv;
+    if (slot_bytes) *slot_bytes = (rows * (p->dv + 4) + 15) / 16 * 16;
+    return RS_OK;
+}
+
+static rs_status ckpt_int8_common(const rs_plan *p, bool pack, const void *src, void *dst,
+                                  int64_t layer_stride_bytes, int64_t n_pool_slots, int64_t n_ckpt_slots,
+                                  const int32_t *pool_slots, const int32_t *ckpt_slots, int32_t n,
+                                  int32_t *status, void *stream) {
+    if (!p || n < 0 || n_pool_slots < 0 || n_ckpt_slots < 0) return RS_ERR_INVALID_ARG;
+    if (!plan_fp32(p) || (p->dv != 64 && p->dv != 128)) return RS_ERR_UNSUPPORTED;
+    if (n == 0) return RS_OK;
+    const bool empty_ckpt = p->offsets.back() == 0;
+    const void *ckpt_ptr = pack ? static_cast<const void *>(dst) : src;
+    const void *pool_ptr = pack ? src : static_cast<const void *>(dst);
+    if (!pool_ptr || !pool_slots || !ckpt_slots || (!ckpt_ptr && !empty_ckpt)) return RS_ERR_INVALID_ARG;
+    if (!aligned16(pool_ptr) || !aligned16(ckpt_ptr) || (layer_stride_bytes & 15)) return RS_ERR_MISALIGNED;
+    const int64_t slot_bytes = (int64_t)p->Hv * (int64_t)p->head_bytes;
+    if (p->L > 1 && layer_stride_bytes < slot_bytes * n_pool_slots) return RS_ERR_INVALID_ARG;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (p->device != dev) return RS_ERR_INVALID_ARG;  // rs_plan_upload first
+    int64_t codes = 0, sb = 0;
+    rs_ckpt_int8_bytes(p, &codes, &sb);
+    int rows_log2 = 0;
+    while ((int64_t(1) << rows_log2) < int8_rows_per_unit(p)) ++rows_log2;
+    if ((int64_t(1) << rows_log2) != int8_rows_per_unit(p)) return RS_ERR_UNSUPPORTED;
+    rs::Int8CkptParams P;
+    P.src = static_cast<const uint8_t *>(src);
+    P.dst = static_cast<uint8_t *>(dst);
+    P.layer_stride = layer_stride_bytes;
+    P.slot_bytes = slot_bytes;
+    P.unit_bytes = p->unit_bytes;
+    P.ckpt_slot_bytes = sb;
+    P.codes_bytes = codes;
+    P.n_pool_slots = n_pool_slots;
+    P.n_ckpt_slots = n_ckpt_slots;
+    P.n_kept = p->offsets.back();
+    P.n_all = (int64_t)p->L * p->nu;
+    P.kept_unit = p->d_kept;
+    P.all_pidx = p->d_all;
+    P.pool_slots = pool_slots;
+    P.ckpt_slots = ckpt_slots;
+    P.status = status;
+    P.n = n;
+    P.units_per_layer = p->nu;
+    P.rows_log2 = rows_log2;
+    P.dv = p->dv;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = pack ? rs::launch_ckpt_pack_int8(P, s) : rs::launch_ckpt_restore_int8(P, s);
+    if (e != cudaSuccess) return launch_fail(e);
+    return RS_OK;
+}
+
+rs_status rs_ckpt_pack_int8(const rs_plan *p, const void *pool, int64_t layer_stride_bytes,
+                            int64_t n_pool_slots, const int32_t *src_slots, const int32_t *dst_ckpt_slots,
+                            int32_t n, void *ckpt_pool, int64_t n_ckpt_slots, int32_t *status,
+                            void *stream) {
+    return ckpt_int8_common(p, true, pool, ckpt_pool, layer_stride_bytes, n_pool_slots, n_ckpt_slots,
+                            src_slots, dst_ckpt_slots, n, status, stream);
+}
+
+rs_status rs_ckpt_restore_int8(const rs_plan *p, const void *ckpt_pool, int64_t n_ckpt_slots,
+                               const int32_t *src_ckpt_slots, void *pool, int64_t layer_stride_bytes,
+                               int64_t n_pool_slots, const int32_t *dst_slots, int32_t n,
+                               int32_t *status, void *stream) {
+    return ckpt_int8_common(p, false, ckpt_pool, pool, layer_stride_bytes, n_pool_slots, n_ckpt_slots,
+                            dst_slots, src_ckpt_slots, n, status, stream);
 }
 
 }  // extern "C"

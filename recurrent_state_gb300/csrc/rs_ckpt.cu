@@ -7,8 +7,10 @@
 // units from the checkpoint and omitted units as +0.0.
 //
 // Both kernels are plain streaming copies.  The work is cut into 512-byte
-// chunks (a whole KDA unit at dv = 128, 1/128 of a GDN head); a warp moves
-// one chunk per step with one 16-byte load and one 16-byte store per lane,
+// chunks (a whole KDA unit at dv = 128, 1/128 of a GDN head, the last chunk
+// of a unit possibly shorter: a mixed FP16/INT8 head of 18,880 B is 36
+// chunks and 448 B); a warp moves one chunk per step with one 16-byte load
+// and one 16-byte store per lane,
 // and each warp keeps kChunks chunks in flight so that enough bytes are
 // outstanding per SM to cover HBM latency.  Pack reads ragged source units
 // and writes the checkpoint contiguously; restore walks the destination
@@ -43,12 +45,28 @@ __device__ __forceinline__ void st_stream(uint4 *p, uint4 v) {
                  : "memory");
 }
 
+// Unit and chunk within the unit of a flat chunk index: a shift when the
+// chunks per unit are a power of two, else a division.
+struct Split {
+    uint32_t cpu;  // chunks per unit
+    int log2cpu;   // log2(cpu), or -1
+};
+__device__ __forceinline__ void split(uint32_t cc, Split sp, uint32_t &unit, uint32_t &part) {
+    if (sp.log2cpu >= 0) {
+        unit = cc >> sp.log2cpu;
+        part = cc & ((1u << sp.log2cpu) - 1u);
+    } else {
+        unit = cc / sp.cpu;
+        part = cc - unit * sp.cpu;
+    }
+}
+
 // Chunk cc (within checkpoint i) of the pack: cc = j * cpu + part.
 __device__ __forceinline__ Chunk pack_chunk(const CkptParams &P, int32_t s, int32_t d, uint32_t cc,
-                                            int log2cpu, int lanes, int lane) {
+                                            Split sp, int lane) {
     Chunk ch;
-    const uint32_t j = cc >> log2cpu;
-    const uint32_t part = cc & ((1u << log2cpu) - 1u);
+    uint32_t j, part;
+    split(cc, sp, j, part);
     const int32_t ku = __ldg(P.kept_unit + j);
     const int64_t l = ku >> 20, x = ku & 0xfffff;
     const int64_t off = (int64_t)part * kChunkBytes + (int64_t)lane * 16;
@@ -56,16 +74,16 @@ __device__ __forceinline__ Chunk pack_chunk(const CkptParams &P, int32_t s, int3
                                              x * P.unit_bytes + off);
     ch.dst = reinterpret_cast<uint4 *>(P.dst + (int64_t)d * P.ckpt_slot_bytes +
                                        (int64_t)j * P.unit_bytes + off);
-    ch.active = lane < lanes;
+    ch.active = off < P.unit_bytes;
     return ch;
 }
 
 // Chunk cc (within slot i) of the restore: cc = u * cpu + part, u = l * nu + x.
 __device__ __forceinline__ Chunk restore_chunk(const CkptParams &P, int32_t s, int32_t d, uint32_t cc,
-                                               int log2cpu, int lanes, int lane) {
+                                               Split sp, int lane) {
     Chunk ch;
-    const uint32_t u = cc >> log2cpu;
-    const uint32_t part = cc & ((1u << log2cpu) - 1u);
+    uint32_t u, part;
+    split(cc, sp, u, part);
     const uint32_t l = u / (uint32_t)P.units_per_layer;
     const uint32_t x = u - l * (uint32_t)P.units_per_layer;
     const int32_t pidx = __ldg(P.all_pidx + u);
@@ -75,14 +93,14 @@ __device__ __forceinline__ Chunk restore_chunk(const CkptParams &P, int32_t s, i
     ch.src = pidx >= 0 ? reinterpret_cast<const uint4 *>(P.src + (int64_t)s * P.ckpt_slot_bytes +
                                                          (int64_t)pidx * P.unit_bytes + off)
                        : nullptr;
-    ch.active = lane < lanes;
+    ch.active = off < P.unit_bytes;
     return ch;
 }
 
 // grid.y walks the n (slot, checkpoint) pairs; grid.x the chunks of one pair.
 template <bool PACK>
 __global__ void __launch_bounds__(256) ckpt_kernel(const __grid_constant__ CkptParams P,
-                                                   uint32_t chunks_per_pair, int log2cpu, int lanes) {
+                                                   uint32_t chunks_per_pair, Split sp) {
     const int lane = threadIdx.x & 31;
     const int i = blockIdx.y;
     const int32_t ps = P.pool_slots[i], cs = P.ckpt_slots[i];
@@ -103,8 +121,7 @@ __global__ void __launch_bounds__(256) ckpt_kernel(const __grid_constant__ CkptP
             const uint32_t cc = base + k;
             ch[k] = Chunk{nullptr, nullptr, false};
             if (cc < chunks_per_pair)
-                ch[k] = PACK ? pack_chunk(P, ps, cs, cc, log2cpu, lanes, lane)
-                             : restore_chunk(P, cs, ps, cc, log2cpu, lanes, lane);
+                ch[k] = PACK ? pack_chunk(P, ps, cs, cc, sp, lane) : restore_chunk(P, cs, ps, cc, sp, lane);
         }
 #pragma unroll
         for (int k = 0; k < kChunks; ++k) {
@@ -118,11 +135,11 @@ __global__ void __launch_bounds__(256) ckpt_kernel(const __grid_constant__ CkptP
 }
 
 cudaError_t launch(const CkptParams &P, bool pack, cudaStream_t s) {
-    const int64_t cpu = P.unit_bytes >= kChunkBytes ? P.unit_bytes / kChunkBytes : 1;
-    const int lanes = P.unit_bytes >= kChunkBytes ? 32 : (int)(P.unit_bytes / 16);
+    if (P.unit_bytes <= 0 || (P.unit_bytes & 15)) return cudaErrorNotSupported;
+    const int64_t cpu = (P.unit_bytes + kChunkBytes - 1) / kChunkBytes;
     int log2cpu = 0;
     while ((1ll << log2cpu) < cpu) ++log2cpu;
-    if ((1ll << log2cpu) != cpu) return cudaErrorNotSupported;
+    if ((1ll << log2cpu) != cpu) log2cpu = -1;
     const int64_t units = pack ? P.n_kept : P.n_all;
     const int64_t per_pair = units * cpu;
     if (per_pair >= (1ll << 31) || P.n > 65535) return cudaErrorNotSupported;
@@ -134,10 +151,11 @@ cudaError_t launch(const CkptParams &P, bool pack, cudaStream_t s) {
     if (cap < 1) cap = 1;
     if (bx > cap) bx = cap;
     dim3 grid((unsigned)bx, (unsigned)P.n);
+    const Split sp{(uint32_t)cpu, log2cpu};
     if (pack)
-        ckpt_kernel<true><<<grid, 256, 0, s>>>(P, (uint32_t)per_pair, log2cpu, lanes);
+        ckpt_kernel<true><<<grid, 256, 0, s>>>(P, (uint32_t)per_pair, sp);
     else
-        ckpt_kernel<false><<<grid, 256, 0, s>>>(P, (uint32_t)per_pair, log2cpu, lanes);
+        ckpt_kernel<false><<<grid, 256, 0, s>>>(P, (uint32_t)per_pair, sp);
     return cudaGetLastError();
 }
 

@@ -34,7 +34,7 @@
 // alone could alias).  Every wait is bounded and reports RS_DEV_PIPE_TIMEOUT.
 #pragma once
 
-#include "rs_step.cuh"
+#include "rs_quant.cuh"
 
 namespace rs {
 
@@ -83,17 +83,6 @@ __device__ __forceinline__ float max_nan(float a, float b) {
 
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
-// RN(a / 127) for a >= 1e-8 or a = +inf, without a division: q0 = RN(a y)
-// with y = RN(1/127), one exact-remainder correction q = RN(q0 + RN(a - q0
-// 127) y) (Markstein's correction step).  Checked against the IEEE quotient
-// for every finite FP32 a >= 1e-8; +inf is passed through.
-__device__ __forceinline__ float div127(float a) {
-    constexpr float y = 1.0f / 127.0f;
-    const float q0 = __fmul_rn(a, y);
-    const float q = __fmaf_rn(__fmaf_rn(-q0, 127.0f, a), y, q0);
-    return a == __int_as_float(0x7f800000) ? a : q;
 }
 
 // A lane's CPL words of one word row (CPL = 2 or 4), 8- or 16-byte aligned.

@@ -181,3 +181,34 @@ def test_plan_offsets_match_golden_and_oracle(L):
 def test_status_strings(L):
     for s in (0, -1, -2, -3, -4):
         assert L.rs_status_string(s).decode()
+
+
+def test_mixed_head_plans_and_int8_checkpoint_sizes(L):
+    """Mixed layouts take head units (a packed head is one unit); INT8
+    checkpoint slots hold codes then one FP32 scale per row (dasc Appendix
+    E.1), sizes agreeing with the oracle's."""
+    Hv, d = 4, 128
+    hi = np.stack([np.arange(16, dtype=np.int16) * 3 + h for h in range(Hv)])
+    st, mix = make_layout(L, _abi.RS_LAYOUT_MIXED_FP16_INT8, dk=d, Hv=Hv, Hk=Hv, k_hi=16, hi=hi)
+    assert st == 0
+    keep = gen.keep_mask(3, Hv, 0.5, seed=1)
+    ph = ctypes.c_void_p()
+    assert L.rs_plan_create(ctypes.byref(ph), mix, 3, _abi.RS_UNIT_HEAD, keep.ctypes.data) == 0
+    off = np.zeros(4, np.int64)
+    ub = ctypes.c_int64()
+    assert L.rs_plan_offsets(ph, off.ctypes.data, ctypes.byref(ub)) == 0
+    assert ub.value == 18880 and off[-1] == keep.sum()
+    cb, sb = ctypes.c_int64(), ctypes.c_int64()
+    assert L.rs_ckpt_int8_bytes(ph, ctypes.byref(cb), ctypes.byref(sb)) == _abi.RS_ERR_UNSUPPORTED
+    L.rs_plan_destroy(ph)
+    keep_c = gen.keep_mask(3, Hv * d, 0.5, seed=2)
+    assert L.rs_plan_create(ctypes.byref(ph), mix, 3, _abi.RS_UNIT_CHANNEL, keep_c.ctypes.data) == \
+        _abi.RS_ERR_UNSUPPORTED
+    L.rs_layout_destroy(mix)
+    st, f32 = make_layout(L, _abi.RS_LAYOUT_FP32, dk=d, Hv=Hv, Hk=Hv)
+    for unit, kp in ((_abi.RS_UNIT_HEAD, keep), (_abi.RS_UNIT_CHANNEL, keep_c)):
+        assert L.rs_plan_create(ctypes.byref(ph), f32, 3, unit, kp.ctypes.data) == 0
+        assert L.rs_ckpt_int8_bytes(ph, ctypes.byref(cb), ctypes.byref(sb)) == 0
+        assert (cb.value, sb.value) == orc.ckpt_int8_layout(int(kp.sum()), unit, d, d)
+        L.rs_plan_destroy(ph)
+    L.rs_layout_destroy(f32)
