@@ -58,6 +58,18 @@ def same_bits(a: np.ndarray, b: np.ndarray) -> bool:
     return a.shape == b.shape and np.array_equal(a.view(np.uint8), b.view(np.uint8))
 
 
+def same_bits_nan(a: np.ndarray, b: np.ndarray) -> bool:
+    """Bit equality of float32 arrays, except that a NaN only has to meet a
+    NaN: the payload of a NaN produced by arithmetic (0 * inf) is the
+    hardware's and not part of the result."""
+    a = np.ascontiguousarray(a, np.float32)
+    b = np.ascontiguousarray(b, np.float32)
+    if a.shape != b.shape:
+        return False
+    na, nb = np.isnan(a), np.isnan(b)
+    return np.array_equal(na, nb) and np.array_equal(a[~na].view(np.uint32), b[~nb].view(np.uint32))
+
+
 def max_rel(x: np.ndarray, ref: np.ndarray) -> float:
     """max over tiles of ||x - ref||_inf / ||ref||_inf, tiles = last two axes
     (or the last axis for vectors)."""
