@@ -325,6 +325,55 @@ rs_status rs_ckpt_restore_int8(const rs_plan *p, const void *ckpt_pool, int64_t 
                                const int32_t *dst_slots, int32_t n, int32_t *status,
                                void *stream);
 
+/* ---- selection-plan builders (host only, offline) ------------------------
+ * These compute the inputs of rs_plan_create (keep masks) and of
+ * rs_layout_create (FP16 channel sets) from model weights and calibration
+ * trajectories.  Host memory only; no device work; fp64 arithmetic from FP32
+ * inputs, except that the quantisation error uses the FP32 storage
+ * quantiser itself.  NULL pointers with a zero count are allowed. */
+
+#define RS_GATE_STD 0   /* g = -exp(A_log) * softplus(a_s + d)             */
+#define RS_GATE_K3  1   /* g = -5 * sigmoid(exp(A_log) * (a_s + d)) (safe) */
+
+/* [dasc] §3.3 Eq. 2-3: static log-decay g_s of each unit from its learned
+ * log-scale A_log[u] and decay bias d_bias[u] (host float [n_units]) with
+ * the model-wide representative gate input a_s (the page uses -0.3 for the
+ * standard gate, 0.8 for the Kimi-K3 safe gate), and the static retention
+ * horizon H[u] = ln(epsilon) / g_s (host double [n_units]; the page uses
+ * epsilon = 1e-3).  A unit is a GDN head or a KDA (head, key channel). */
+rs_status rs_dasc_horizons(int32_t gate, const float *A_log, const float *d_bias, int64_t n_units,
+                           double a_s, double epsilon, double *H);
+
+/* [dasc] §4.1: keep[u] = 1 when H[u] > W_max (retained, global unit), else 0
+ * (omitted, local).  The result is one layer's row of rs_plan_create's keep. */
+rs_status rs_dasc_keep(const double *H, int64_t n_units, double W_max, uint8_t *keep);
+
+/* [dasc] §4.2 Eq. 7: suffix-refresh window of dasc-wr.  For each omitted
+ * unit (keep[u] = 0), W_u = clamp(next_pow2(H[u]), 4, W_max) with
+ * next_pow2(x) = 2^ceil(log2 x) (x > 0; 4 for x = 0); *W_replay = min(
+ * n_prefix, max W_u), or 0 when no unit is omitted.  W_max >= 4. */
+rs_status rs_dasc_refresh_window(const double *H, const uint8_t *keep, int64_t n_units, int64_t W_max,
+                                 int64_t n_prefix, int64_t *W_replay);
+
+/* [DAMP] §5.1 Eq. 14-15: accumulated-error risk of each key channel of one
+ * (layer, head).  states: host float [n_anchors][dk][dv], calibration
+ * states at the scoring anchors (DAMP orientation, row = key channel);
+ * decays: host float [n_anchors][horizon][dk], the decay factors a_{t+r,u}
+ * of the horizon updates that follow each anchor.  C[u] (host double [dk]) =
+ * mean over anchors of e_u * (1 + sum_{j=1..horizon} prod_{r<=j} a_r^2) with
+ * e_u = sum_v (Q(S)[u][v] - S[u][v])^2 and Q the storage quantiser (one INT8
+ * scale per row, as in rs_layout_create's INT8 rows). */
+rs_status rs_damp_risk_scores(const float *states, const float *decays, int32_t n_anchors, int32_t dk,
+                              int32_t dv, int32_t horizon, double *C);
+
+/* [DAMP] §5.1 budgeted selection: for each of n_heads heads, the k_hi key
+ * channels with the largest C (host double [n_heads][dk]); equal scores
+ * rank the lower channel first; each head's channels are written in
+ * ascending order to hi_rows (host int16 [n_heads][k_hi]) -- the format
+ * rs_layout_create takes.  A NaN score is an error. */
+rs_status rs_damp_select_hi_rows(const double *C, int32_t n_heads, int32_t dk, int32_t k_hi,
+                                 int16_t *hi_rows);
+
 #ifdef __cplusplus
 }
 #endif

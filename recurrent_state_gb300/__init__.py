@@ -17,7 +17,7 @@ import importlib
 __all__ = [
     "Layout", "Plan", "gdn_decode_update", "kda_decode_update", "spec_replay_update",
     "state_convert", "ckpt_pack", "ckpt_restore", "ckpt_pack_int8", "ckpt_restore_int8", "RsError",
-    "build", "inputs",
+    "build", "inputs", "plans",
 ]
 
 _LAZY = {
@@ -31,6 +31,6 @@ def __getattr__(name):
     if name in _LAZY:
         mod = importlib.import_module(f".{_LAZY[name]}", __name__)
         return getattr(mod, name)
-    if name in ("build", "inputs", "api", "_abi"):
+    if name in ("build", "inputs", "api", "_abi", "plans"):
         return importlib.import_module(f".{name}", __name__)
     raise AttributeError(name)

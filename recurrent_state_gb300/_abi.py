@@ -26,6 +26,7 @@ RS_LAYOUT_FP32 = 0
 RS_LAYOUT_MIXED_FP16_INT8 = 1
 RS_F32, RS_BF16, RS_F16 = 0, 1, 2
 RS_UNIT_HEAD, RS_UNIT_CHANNEL = 0, 1
+RS_GATE_STD, RS_GATE_K3 = 0, 1
 
 # Every function the header declares, for the symbol-table test.
 EXPORTS = (
@@ -36,6 +37,8 @@ EXPORTS = (
     "rs_plan_create", "rs_plan_destroy", "rs_plan_offsets", "rs_plan_upload",
     "rs_ckpt_pack", "rs_ckpt_restore", "rs_ckpt_pack_noalloc",
     "rs_ckpt_int8_bytes", "rs_ckpt_pack_int8", "rs_ckpt_restore_int8",
+    "rs_dasc_horizons", "rs_dasc_keep", "rs_dasc_refresh_window", "rs_damp_risk_scores",
+    "rs_damp_select_hi_rows",
 )
 
 
@@ -105,6 +108,11 @@ def _declare(L):
     L.rs_ckpt_int8_bytes.argtypes = [_P, _P, _P]
     L.rs_ckpt_pack_int8.argtypes = [_P, _P, _I64, _I64, _P, _P, _I32, _P, _I64, _P, _P]
     L.rs_ckpt_restore_int8.argtypes = [_P, _P, _I64, _P, _P, _I64, _I64, _P, _I32, _P, _P]
+    L.rs_dasc_horizons.argtypes = [_I32, _P, _P, _I64, ctypes.c_double, ctypes.c_double, _P]
+    L.rs_dasc_keep.argtypes = [_P, _I64, ctypes.c_double, _P]
+    L.rs_dasc_refresh_window.argtypes = [_P, _P, _I64, _I64, _I64, _P]
+    L.rs_damp_risk_scores.argtypes = [_P, _P, _I32, _I32, _I32, _I32, _P]
+    L.rs_damp_select_hi_rows.argtypes = [_P, _I32, _I32, _I32, _P]
     for name in EXPORTS:
         if name not in ("rs_status_string", "rs_last_cuda_error", "rs_version"):
             getattr(L, name).restype = _I32

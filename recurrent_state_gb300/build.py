@@ -24,8 +24,10 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # --fmad=false: no a*b+c contraction anywhere; the kernels spell out every
 # fused multiply-add they mean, so FP32 results match the CPU oracle bit for
 # bit.  IEEE division and square root are the nvcc defaults (no fast math).
+# -ffp-contract=off does the same for the host compiler (Arm gcc contracts by
+# default).
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "--fmad=false", "-std=c++17", "-Xcompiler", "-fPIC",
-                     "-I", os.path.join(ROOT, "include")]
+                     "-Xcompiler", "-ffp-contract=off", "-I", os.path.join(ROOT, "include")]
 
 
 def nvcc() -> str:
