@@ -131,6 +131,20 @@ def _declare(L):
     L.orc_ckpt_restore.argtypes = [_I, _I, _I, _I, _I, _P, _P, _I, _P, _P, _I64,
                                    _I, _P, _I]
     L.orc_ckpt_restore.restype = _I
+    L.orc_damp_tile_bytes.argtypes = [_I, _I, _I, _I]
+    L.orc_damp_tile_bytes.restype = ctypes.c_size_t
+    L.orc_damp_unpack.argtypes = [_I, _I, _I, _I, _P, _P]
+    L.orc_damp_pack.argtypes = [_I, _I, _I, _I, _P, _P]
+    L.orc_convert_f32_to_damp.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P]
+    L.orc_convert_f32_to_damp.restype = _I
+    L.orc_convert_damp_to_f32.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P]
+    L.orc_convert_damp_to_f32.restype = _I
+    L.orc_decode_damp.argtypes = [_I, _I, _I, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P, _P, _P, _P,
+                                  _P, _P, _P, _I, _I]
+    L.orc_decode_damp.restype = _I
+    L.orc_replay_damp.argtypes = [_I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P, _P, _P,
+                                  _P, _P, _P, _P, _P, _I, _I]
+    L.orc_replay_damp.restype = _I
     L.orc_ckpt_pack_heads.argtypes = [_I, _I, _I64, _P, _P, _I64, _I, _P, _P, _I, _P, _I]
     L.orc_ckpt_pack_heads.restype = _I
     L.orc_ckpt_restore_heads.argtypes = [_I, _I, _I64, _P, _P, _I, _P, _P, _I64, _I, _P, _I]
@@ -408,3 +422,96 @@ def ckpt_restore_int8(keep, unit, ckpt, src_slots, pool, dst_slots):
                                        ckpt.shape[0], _ptr(_c(src_slots, np.int32)),
                                        _ptr(_c(pool, np.float32)), pool.strides[0] // 4, n_slots,
                                        _ptr(_c(dst_slots, np.int32)), len(src_slots))
+
+
+# --------------------------------------------------------------------------
+# DAMP-exact storage: INT8 groups along dv, value scaling (DAMP Appendix A.1,
+# A.3 Eq. 17-18, A.4)
+# --------------------------------------------------------------------------
+def damp_tile_bytes(dk, dv, khi, group):
+    return int(lib().orc_damp_tile_bytes(dk, dv, khi, group))
+
+
+def damp_unpack(tile, dk, dv, khi, group):
+    tile = _c(np.ascontiguousarray(tile), np.uint8)
+    T = np.zeros((dk, dv), np.float32)
+    lib().orc_damp_unpack(dk, dv, khi, group, _ptr(tile), _ptr(T))
+    return T
+
+
+def damp_pack(T, khi, group):
+    T = _c(np.ascontiguousarray(T), np.float32)
+    dk, dv = T.shape
+    tile = np.zeros(damp_tile_bytes(dk, dv, khi, group), np.uint8)
+    lib().orc_damp_pack(dk, dv, khi, group, _ptr(T), _ptr(tile))
+    return tile
+
+
+def convert_pool_f32_to_damp(pool, khi, group, pi, cs):
+    """[..., Hv, dk, dv] float32 -> [..., Hv, tile_bytes] uint8; pi [Hv][dk],
+    cs [Hv][dv] value-scaling factors."""
+    *lead, Hv, dk, dv = pool.shape
+    flat = pool.reshape(-1, Hv, dk, dv)
+    pi = np.ascontiguousarray(pi, np.int16)
+    cs = _c(np.ascontiguousarray(cs, np.float32), np.float32)
+    out = np.zeros((flat.shape[0], Hv, damp_tile_bytes(dk, dv, khi, group)), np.uint8)
+    for s in range(flat.shape[0]):
+        for h in range(Hv):
+            S = np.ascontiguousarray(flat[s, h])
+            assert lib().orc_convert_f32_to_damp(dk, dv, khi, group, _ptr(pi[h]), _ptr(cs[h]), _ptr(S),
+                                                 _ptr(out[s, h])) == 0
+    return out.reshape(*lead, Hv, out.shape[-1])
+
+
+def convert_pool_damp_to_f32(pool, dk, dv, khi, group, pi, cs):
+    *lead, Hv, tb = pool.shape
+    flat = np.ascontiguousarray(pool.reshape(-1, Hv, tb))
+    pi = np.ascontiguousarray(pi, np.int16)
+    cs = _c(np.ascontiguousarray(cs, np.float32), np.float32)
+    out = np.zeros((flat.shape[0], Hv, dk, dv), np.float32)
+    for s in range(flat.shape[0]):
+        for h in range(Hv):
+            assert lib().orc_convert_damp_to_f32(dk, dv, khi, group, _ptr(pi[h]), _ptr(cs[h]),
+                                                 _ptr(flat[s, h]), _ptr(out[s, h])) == 0
+    return out.reshape(*lead, Hv, dk, dv)
+
+
+def decode_damp(pool, slot_idx, pi, cs, khi, group, dk, dv, q, k, v, alpha, beta, o=None,
+                per_channel=None, items=None):
+    """Batched DAMP-exact decode in place on ``pool`` [n_slots][Hv][tile_bytes]."""
+    _c(pool, np.uint8)
+    n_slots, Hv, tb = pool.shape
+    assert tb == damp_tile_bytes(dk, dv, khi, group)
+    B, Hk, _ = q.shape
+    if per_channel is None:
+        per_channel = alpha.ndim == 3
+    if o is None:
+        o = np.zeros((B, Hv, dv), np.float32)
+    lo, hi = items if items is not None else (0, B * Hv)
+    st = lib().orc_decode_damp(B, Hk, Hv, dk, dv, khi, group, int(per_channel), _ptr(pool), n_slots,
+                               _ptr(_c(slot_idx, np.int32)), _ptr(_c(pi, np.int16)),
+                               _ptr(_c(cs, np.float32)), _ptr(_c(q, np.float32)),
+                               _ptr(_c(k, np.float32)), _ptr(_c(v, np.float32)),
+                               _ptr(_c(alpha, np.float32)), _ptr(_c(beta, np.float32)),
+                               _ptr(_c(o, np.float32)), lo, hi)
+    return o, st
+
+
+def replay_damp(pool, slot_idx, n_accept, pi, cs, khi, group, dk, dv, q, k, v, alpha, beta, o=None,
+                per_channel=None, items=None):
+    _c(pool, np.uint8)
+    n_slots, Hv, tb = pool.shape
+    assert tb == damp_tile_bytes(dk, dv, khi, group)
+    B, T_max, Hk, _ = q.shape
+    if per_channel is None:
+        per_channel = alpha.ndim == 4
+    if o is None:
+        o = np.zeros((B, T_max, Hv, dv), np.float32)
+    lo, hi = items if items is not None else (0, B * Hv)
+    st = lib().orc_replay_damp(B, T_max, Hk, Hv, dk, dv, khi, group, int(per_channel), _ptr(pool),
+                               n_slots, _ptr(_c(slot_idx, np.int32)), _ptr(_c(n_accept, np.int32)),
+                               _ptr(_c(pi, np.int16)), _ptr(_c(cs, np.float32)), _ptr(_c(q, np.float32)),
+                               _ptr(_c(k, np.float32)), _ptr(_c(v, np.float32)),
+                               _ptr(_c(alpha, np.float32)), _ptr(_c(beta, np.float32)),
+                               _ptr(_c(o, np.float32)), lo, hi)
+    return o, st

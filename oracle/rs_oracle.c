@@ -667,3 +667,191 @@ int orc_ckpt_restore_int8(int L, int Hv, int dk, int dv, int unit, const uint8_t
     }
     return status;
 }
+
+/* ---------------------------------------------------------------------------
+ * DAMP-exact storage ([DAMP] Appendix A.1 "Integer formats" and "Value
+ * scaling and reordering", A.3 Eq. 17-18, A.4 "State storage"):
+ *   - INT8 rows are quantised in groups of `group` consecutive values along
+ *     dv, one FP32 scale per group (the page's group is 32), with the same
+ *     symmetric quantiser as above (orc_quantise_row on each group);
+ *   - the stored state is T = P_K S D_c^{-1} P_V^T.  The model produces its
+ *     value coordinates already in P_V order (A.3: the projections are
+ *     rearranged offline), so here the value order is taken as given and
+ *     cs[c] = c'_c are the scaling factors in that order (D'_c);
+ *   - the step runs on T in the transformed coordinates (Eq. 18): v' =
+ *     D'_c^{-1} v (v[c] / cs[c], one IEEE division), the delta-rule update
+ *     as in orc_step_tile_f32, and o = D'_c T^T q' (cs[c] * o'[c]).
+ * Tile: FP16 and INT8 regions as in the one-scale-per-row tile (same word
+ * interleave), then the scales [dk - khi][dv / group] row-major.  With
+ * group = dv and cs = 1 this is exactly the one-scale-per-row layout.
+ * ------------------------------------------------------------------------- */
+size_t orc_damp_tile_bytes(int dk, int dv, int khi, int group)
+{
+    return (size_t)2 * khi * dv + (size_t)(dk - khi) * dv + (size_t)4 * (dk - khi) * (dv / group);
+}
+
+void orc_damp_unpack(int dk, int dv, int khi, int group, const uint8_t *tile, float *T)
+{
+    const uint8_t *hi = tile;
+    const uint8_t *lo = tile + (size_t)2 * khi * dv;
+    const uint8_t *sc = tile + (size_t)2 * khi * dv + (size_t)(dk - khi) * dv;
+    int ng = dv / group, r, c, gi;
+    int8_t row[ORC_MAX_D];
+    for (r = 0; r < khi; ++r)
+        for (c = 0; c < dv; ++c) {
+            uint16_t b;
+            memcpy(&b, hi + hi_offset(dv, r, c), 2);
+            T[(size_t)r * dv + c] = f16_bits_to_f32(b);
+        }
+    for (r = khi; r < dk; ++r) {
+        for (c = 0; c < dv; ++c)
+            row[c] = (int8_t)lo[lo_offset(dv, r - khi, c)];
+        for (gi = 0; gi < ng; ++gi) {
+            float s;
+            memcpy(&s, sc + ((size_t)(r - khi) * ng + gi) * 4, 4);
+            orc_dequantise_row(group, row + gi * group, s, T + (size_t)r * dv + gi * group);
+        }
+    }
+}
+
+void orc_damp_pack(int dk, int dv, int khi, int group, const float *T, uint8_t *tile)
+{
+    uint8_t *hi = tile;
+    uint8_t *lo = tile + (size_t)2 * khi * dv;
+    uint8_t *sc = tile + (size_t)2 * khi * dv + (size_t)(dk - khi) * dv;
+    int ng = dv / group, r, c, gi;
+    int8_t row[ORC_MAX_D];
+    for (r = 0; r < khi; ++r)
+        for (c = 0; c < dv; ++c) {
+            uint16_t b = f32_to_f16_bits(T[(size_t)r * dv + c]);
+            memcpy(hi + hi_offset(dv, r, c), &b, 2);
+        }
+    for (r = khi; r < dk; ++r) {
+        for (gi = 0; gi < ng; ++gi) {
+            float s;
+            orc_quantise_row(group, T + (size_t)r * dv + gi * group, row + gi * group, &s);
+            memcpy(sc + ((size_t)(r - khi) * ng + gi) * 4, &s, 4);
+        }
+        for (c = 0; c < dv; ++c)
+            lo[lo_offset(dv, r - khi, c)] = (uint8_t)row[c];
+    }
+}
+
+/* S (logical rows, value order as produced) <-> tile: T[r][c] = S[pi[r]][c]
+ * / cs[c] ([DAMP] Appendix A.3 Eq. 17), and back S[pi[r]][c] = T[r][c] * cs[c]. */
+int orc_convert_f32_to_damp(int dk, int dv, int khi, int group, const int16_t *pi, const float *cs,
+                            const float *S, uint8_t *tile)
+{
+    float *T = (float *)malloc((size_t)dk * dv * 4);
+    int r, c;
+    if (!T) return -1;
+    for (r = 0; r < dk; ++r)
+        for (c = 0; c < dv; ++c)
+            T[(size_t)r * dv + c] = S[(size_t)pi[r] * dv + c] / cs[c];
+    orc_damp_pack(dk, dv, khi, group, T, tile);
+    free(T);
+    return 0;
+}
+
+int orc_convert_damp_to_f32(int dk, int dv, int khi, int group, const int16_t *pi, const float *cs,
+                            const uint8_t *tile, float *S)
+{
+    float *T = (float *)malloc((size_t)dk * dv * 4);
+    int r, c;
+    if (!T) return -1;
+    orc_damp_unpack(dk, dv, khi, group, tile, T);
+    for (r = 0; r < dk; ++r)
+        for (c = 0; c < dv; ++c)
+            S[(size_t)pi[r] * dv + c] = T[(size_t)r * dv + c] * cs[c];
+    free(T);
+    return 0;
+}
+
+/* One transformed step on T ([DAMP] Appendix A.3 Eq. 18). */
+static void damp_step(int dk, int dv, float *T, const float *qp, const float *kp, const float *v,
+                      const float *cs, const float *ap, float beta, float *o)
+{
+    float vp[ORC_MAX_D], op[ORC_MAX_D];
+    int c;
+    for (c = 0; c < dv; ++c)
+        vp[c] = v[c] / cs[c];
+    orc_step_tile_f32(dk, dv, T, qp, kp, vp, ap, 1, beta, o ? op : NULL);
+    if (o)
+        for (c = 0; c < dv; ++c)
+            o[c] = cs[c] * op[c];
+}
+
+/* Batched decode / replay on DAMP tiles: as orc_decode_mixed and
+ * orc_replay_mixed, with group-wise INT8 scales and value scaling; cs is
+ * [Hv][dv] (one vector per head). */
+int orc_decode_damp(int B, int Hk, int Hv, int dk, int dv, int khi, int group, int per_channel,
+                    uint8_t *pool, int n_slots, const int32_t *slot_idx, const int16_t *pi,
+                    const float *cs, const float *q, const float *k, const float *v,
+                    const float *alpha, const float *beta, float *o, int item_begin, int item_end)
+{
+    float *T = (float *)malloc((size_t)dk * dv * 4);
+    float qp[ORC_MAX_D], kp[ORC_MAX_D], ap[ORC_MAX_D];
+    size_t tb = orc_damp_tile_bytes(dk, dv, khi, group);
+    int status = 0, it, r;
+    (void)B;
+    if (!T) return -1;
+    for (it = item_begin; it < item_end; ++it) {
+        int b = it / Hv, h = it % Hv, g = key_head(h, Hk, Hv);
+        int32_t slot = slot_idx[b];
+        const int16_t *ph = pi + (size_t)h * dk;
+        const float *qh = q + ((size_t)b * Hk + g) * dk, *kh = k + ((size_t)b * Hk + g) * dk;
+        uint8_t *tile;
+        if (slot < 0 || slot >= n_slots) { status |= 1; continue; }
+        tile = pool + ((size_t)slot * Hv + h) * tb;
+        for (r = 0; r < dk; ++r) {
+            qp[r] = qh[ph[r]];
+            kp[r] = kh[ph[r]];
+            ap[r] = per_channel ? alpha[((size_t)b * Hv + h) * dk + ph[r]] : alpha[(size_t)b * Hv + h];
+        }
+        orc_damp_unpack(dk, dv, khi, group, tile, T);
+        damp_step(dk, dv, T, qp, kp, v + ((size_t)b * Hv + h) * dv, cs + (size_t)h * dv, ap,
+                  beta[(size_t)b * Hv + h], o ? o + ((size_t)b * Hv + h) * dv : NULL);
+        orc_damp_pack(dk, dv, khi, group, T, tile);
+    }
+    free(T);
+    return status;
+}
+
+int orc_replay_damp(int B, int T_max, int Hk, int Hv, int dk, int dv, int khi, int group,
+                    int per_channel, uint8_t *pool, int n_slots, const int32_t *slot_idx,
+                    const int32_t *n_accept, const int16_t *pi, const float *cs, const float *q,
+                    const float *k, const float *v, const float *alpha, const float *beta, float *o,
+                    int item_begin, int item_end)
+{
+    float *T = (float *)malloc((size_t)dk * dv * 4);
+    float qp[ORC_MAX_D], kp[ORC_MAX_D], ap[ORC_MAX_D];
+    size_t tb = orc_damp_tile_bytes(dk, dv, khi, group);
+    int status = 0, it, t, r;
+    (void)B;
+    if (!T) return -1;
+    for (it = item_begin; it < item_end; ++it) {
+        int b = it / Hv, h = it % Hv, g = key_head(h, Hk, Hv);
+        int32_t slot = slot_idx[b], n = n_accept[b];
+        const int16_t *ph = pi + (size_t)h * dk;
+        uint8_t *tile;
+        if (slot < 0 || slot >= n_slots) { status |= 1; continue; }
+        if (n < 0 || n > T_max) { status |= 2; continue; }
+        if (n == 0) continue;
+        tile = pool + ((size_t)slot * Hv + h) * tb;
+        orc_damp_unpack(dk, dv, khi, group, tile, T);
+        for (t = 0; t < n; ++t) {
+            size_t bt = (size_t)b * T_max + t;
+            const float *qh = q + (bt * Hk + g) * dk, *kh = k + (bt * Hk + g) * dk;
+            for (r = 0; r < dk; ++r) {
+                qp[r] = qh[ph[r]];
+                kp[r] = kh[ph[r]];
+                ap[r] = per_channel ? alpha[(bt * Hv + h) * dk + ph[r]] : alpha[bt * Hv + h];
+            }
+            damp_step(dk, dv, T, qp, kp, v + (bt * Hv + h) * dv, cs + (size_t)h * dv, ap,
+                      beta[bt * Hv + h], o ? o + (bt * Hv + h) * dv : NULL);
+        }
+        orc_damp_pack(dk, dv, khi, group, T, tile);
+    }
+    free(T);
+    return status;
+}

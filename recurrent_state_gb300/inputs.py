@@ -187,3 +187,15 @@ def ckpt_slots(n_pool_slots: int, n: int, seed: int = 0):
 def random_pool(shape, seed: int = 0, std: float = 0.1) -> np.ndarray:
     g = rng(seed + 17)
     return (g.standard_normal(shape, dtype=np.float32) * np.float32(std)).astype(np.float32)
+
+
+def value_scales(Hv: int, dv: int, seed: int = 0, group: int = 0, pow2: bool = False) -> np.ndarray:
+    """Value-scaling factors c' > 0 per (head, value dimension), float32
+    [Hv][dv] (DAMP Appendix A.1 "Value scaling and reordering", calibrated
+    offline; synthetic here): log-uniform in [1/4, 4], or, with ``pow2``, one
+    power of two 2^k (k in -3..3) per group of ``group`` consecutive values."""
+    g = rng(seed + 4099)
+    if pow2:
+        k = g.integers(-3, 4, (Hv, dv // group))
+        return np.repeat(np.ldexp(np.float32(1.0), k).astype(np.float32), group, axis=1)
+    return np.exp(g.uniform(np.log(0.25), np.log(4.0), (Hv, dv))).astype(np.float32)

@@ -20,6 +20,7 @@ from recurrent_state_gb300 import inputs as gen
 
 from . import test_oracle_ckpt as ck
 from . import test_oracle_ckpt_int8 as i8
+from . import test_oracle_damp as dm
 from . import test_oracle_mixed as mx
 from . import test_oracle_quant as qt
 from . import test_oracle_recurrence as rc
@@ -51,6 +52,10 @@ CHECKS = [
     ("int8_closed", lambda: i8.test_constant_rows_closed_form_and_order(1)),
     ("int8_roundtrip", lambda: i8.test_roundtrip_error_bound_and_zero_fill(0)),
     ("heads", i8.test_whole_head_pack_matches_fp32_pack),
+    ("damp_groups", dm.test_constant_groups_closed_form),
+    ("damp_bound", dm.test_group_error_bound),
+    ("damp_pow2", lambda: dm.test_pow2_value_scaling_equivariance(True)),
+    ("damp_fp64", dm.test_transformed_step_matches_original_map_fp64),
 ]
 
 READOUT_BLOCK = """    /* readout o = S^T q on the updated state */
@@ -109,6 +114,12 @@ MUTATIONS = {
     "int8_restore_no_zero_fill": [("memset(dst, 0, (size_t)R * dv * 4);", "(void)dst;")],
     "int8_dequant_unscaled": [("                                       sc, dst + (size_t)r * dv);",
                                "                                       1.0f, dst + (size_t)r * dv);")],
+    "damp_value_scale_multiplied": [("vp[c] = v[c] / cs[c];", "vp[c] = v[c] * cs[c];")],
+    "damp_readout_unscaled": [("o[c] = cs[c] * op[c];", "o[c] = op[c];")],
+    "damp_group_scale_index": [("memcpy(&s, sc + ((size_t)(r - khi) * ng + gi) * 4, 4);",
+                                "memcpy(&s, sc + ((size_t)(r - khi) * ng) * 4, 4);")],
+    "damp_convert_multiplies": [("T[(size_t)r * dv + c] = S[(size_t)pi[r] * dv + c] / cs[c];",
+                                 "T[(size_t)r * dv + c] = S[(size_t)pi[r] * dv + c] * cs[c];")],
     "heads_unit_is_fp32_head": [("size_t ub = (size_t)head_bytes, slot_bytes = (size_t)Hv * ub;\n    int status = 0, i, l, x;\n    if (L > 1024) return -1;\n    orc_plan_offsets(L, Hv, 1, 0, keep, off);\n    for (i = 0; i < n; ++i) {\n        int32_t s = src_slots[i]",
                                  "size_t ub = (size_t)head_bytes, slot_bytes = (size_t)Hv * ub * 2;\n    int status = 0, i, l, x;\n    if (L > 1024) return -1;\n    orc_plan_offsets(L, Hv, 1, 0, keep, off);\n    for (i = 0; i < n; ++i) {\n        int32_t s = src_slots[i]")],
 }
