@@ -143,6 +143,25 @@ const char *rs_version(void);
  * library-owned object; free it with rs_layout_destroy. */
 rs_status rs_layout_create(rs_layout **out, const rs_layout_params *p,
                            const int16_t *hi_rows /* host [Hv][k_hi] */);
+/* DAMP-exact storage ([DAMP] Appendix A.1 "Integer formats" and "Value
+ * scaling and reordering", A.3 Eq. 17-18, A.4): a mixed layout (kind
+ * RS_LAYOUT_MIXED_FP16_INT8, hi_rows as in rs_layout_create) whose INT8 rows
+ * are quantised in groups of `group` consecutive values along dv with one
+ * FP32 scale per group (the page's 32; only 32 is built), and whose state is
+ * stored in value-scaled coordinates T = P_K S D_c^{-1}.  value_scales: host
+ * float [Hv][dv], c'_v > 0 and finite, in the value order the model produces
+ * (the value reordering P_V is absorbed into the projections, [DAMP] A.3);
+ * NULL means all ones.  The library copies them.  Decode computes v' = v / c'
+ * (IEEE division), the step of rs_gdn/kda_decode_update on T, and returns
+ * o = c' (T^T q') -- the page's o' = D'_c T^T q'.
+ * Tile: the FP16 and INT8 regions of the one-scale-per-row layout (same word
+ * interleave), then scales [dk - k_hi][dv / group] f32 row-major: 20,224 B at
+ * d = 128, k_hi = 16 (9.875 bits per value).  rs_state_convert converts FP32
+ * states (S in logical rows) to and from it; checkpoint plans take its heads
+ * as units.  Speculative replay on this layout is not built
+ * (RS_ERR_UNSUPPORTED); Hv * dv <= 4096. */
+rs_status rs_layout_create_damp(rs_layout **out, const rs_layout_params *p, const int16_t *hi_rows,
+                                int32_t group, const float *value_scales);
 rs_status rs_layout_destroy(rs_layout *l);
 
 /* Bytes of one head state in this layout (65,536 or 18,880 at d = 128). */

@@ -31,7 +31,7 @@ RS_GATE_STD, RS_GATE_K3 = 0, 1
 # Every function the header declares, for the symbol-table test.
 EXPORTS = (
     "rs_status_string", "rs_last_cuda_error", "rs_version",
-    "rs_layout_create", "rs_layout_destroy", "rs_layout_head_bytes", "rs_layout_row_map",
+    "rs_layout_create", "rs_layout_create_damp", "rs_layout_destroy", "rs_layout_head_bytes", "rs_layout_row_map",
     "rs_layout_bits_per_value",
     "rs_gdn_decode_update", "rs_kda_decode_update", "rs_spec_replay_update", "rs_state_convert",
     "rs_plan_create", "rs_plan_destroy", "rs_plan_offsets", "rs_plan_upload",
@@ -106,6 +106,7 @@ def _declare(L):
     L.rs_ckpt_restore.argtypes = [_P, _P, _I64, _P, _P, _I64, _I64, _P, _I32, _P, _P]
     L.rs_ckpt_pack_noalloc.argtypes = [_P, _P, _I64, _I64, _P, _P, _I32, _P, _I64, _P, _P]
     L.rs_ckpt_int8_bytes.argtypes = [_P, _P, _P]
+    L.rs_layout_create_damp.argtypes = [ctypes.POINTER(_P), ctypes.POINTER(LayoutParams), _P, _I32, _P]
     L.rs_ckpt_pack_int8.argtypes = [_P, _P, _I64, _I64, _P, _P, _I32, _P, _I64, _P, _P]
     L.rs_ckpt_restore_int8.argtypes = [_P, _P, _I64, _P, _P, _I64, _I64, _P, _I32, _P, _P]
     L.rs_dasc_horizons.argtypes = [_I32, _P, _P, _I64, ctypes.c_double, ctypes.c_double, _P]

@@ -43,8 +43,13 @@ class Layout:
     """A state-pool layout (``rs_layout``)."""
 
     def __init__(self, kind: str, dk: int, num_v_heads: int, num_qk_heads: int,
-                 k_hi: int = 0, hi_rows=None, dv: int | None = None):
-        self.kind = {"fp32": _abi.RS_LAYOUT_FP32, "mixed": _abi.RS_LAYOUT_MIXED_FP16_INT8}[kind]
+                 k_hi: int = 0, hi_rows=None, dv: int | None = None, group: int = 32,
+                 value_scales=None):
+        """kind: "fp32", "mixed" (one INT8 scale per row) or "damp" (DAMP-exact:
+        INT8 groups of ``group`` values along dv and value-scaling factors
+        ``value_scales`` [Hv][dv], default all ones)."""
+        self.kind = {"fp32": _abi.RS_LAYOUT_FP32, "mixed": _abi.RS_LAYOUT_MIXED_FP16_INT8,
+                     "damp": _abi.RS_LAYOUT_MIXED_FP16_INT8}[kind]
         self.kind_name = kind
         self.dk, self.dv = dk, dv or dk
         self.Hv, self.Hk, self.k_hi = num_v_heads, num_qk_heads, k_hi
@@ -53,8 +58,20 @@ class Layout:
         if hi_rows is not None:
             hr = np.ascontiguousarray(hi_rows, np.int16)
         h = ctypes.c_void_p()
-        check(_abi.lib().rs_layout_create(ctypes.byref(h), ctypes.byref(p),
-                                          None if hr is None else hr.ctypes.data), "rs_layout_create")
+        if kind == "damp":
+            cs = None
+            if value_scales is not None:
+                cs = np.ascontiguousarray(value_scales, np.float32)
+                if cs.shape != (num_v_heads, self.dv):
+                    raise ValueError("value_scales must be [Hv][dv]")
+            self.value_scales = cs
+            check(_abi.lib().rs_layout_create_damp(ctypes.byref(h), ctypes.byref(p),
+                                                   None if hr is None else hr.ctypes.data, group,
+                                                   None if cs is None else cs.ctypes.data),
+                  "rs_layout_create_damp")
+        else:
+            check(_abi.lib().rs_layout_create(ctypes.byref(h), ctypes.byref(p),
+                                              None if hr is None else hr.ctypes.data), "rs_layout_create")
         self._h = h
         nb = ctypes.c_size_t()
         check(_abi.lib().rs_layout_head_bytes(h, ctypes.byref(nb)))

@@ -2,6 +2,8 @@
 // layout and plan objects, argument validation, status codes, and dispatch to
 // the kernel launchers.  No exception crosses the ABI; every entry point
 // returns an rs_status.
+#include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -14,11 +16,14 @@
 #include "../../include/recurrent_state.h"
 #include "rs_internal.h"
 #include "rs_ckpt_int8.h"
+#include "rs_damp.h"
 
 struct rs_layout {
     rs_layout_params p;
     std::vector<int16_t> pi;  // [Hv][dk], physical row -> key channel
     size_t head_bytes;
+    int32_t group = 0;        // DAMP-exact layout: values per INT8 scale group (0: one scale per row)
+    std::vector<float> cs;    // DAMP-exact layout: value-scaling factors [Hv][dv]
 };
 
 
@@ -139,6 +144,29 @@ rs_status rs_layout_create(rs_layout **out, const rs_layout_params *p, const int
     return RS_OK;
 }
 
+rs_status rs_layout_create_damp(rs_layout **out, const rs_layout_params *p, const int16_t *hi_rows,
+                                int32_t group, const float *value_scales) {
+    if (!out || !p) return RS_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (p->kind != RS_LAYOUT_MIXED_FP16_INT8 || group <= 0 || p->dv % group != 0) return RS_ERR_INVALID_ARG;
+    if (group != rs::kDampGroup) return RS_ERR_UNSUPPORTED;
+    if ((size_t)p->num_v_heads * p->dv > (size_t)rs::kMaxValueScales) return RS_ERR_UNSUPPORTED;
+    const size_t ncs = (size_t)p->num_v_heads * (size_t)(p->dv > 0 ? p->dv : 0);
+    if (value_scales)
+        for (size_t i = 0; i < ncs; ++i)
+            if (!(value_scales[i] > 0.0f) || !std::isfinite(value_scales[i])) return RS_ERR_INVALID_ARG;
+    rs_layout *l = nullptr;
+    const rs_status st = rs_layout_create(&l, p, hi_rows);
+    if (st != RS_OK) return st;
+    l->group = group;
+    l->cs.assign(ncs, 1.0f);
+    if (value_scales) std::copy(value_scales, value_scales + ncs, l->cs.begin());
+    l->head_bytes = (size_t)2 * p->k_hi * p->dv + (size_t)(p->dk - p->k_hi) * p->dv +
+                    (size_t)4 * (p->dk - p->k_hi) * (p->dv / group);
+    *out = l;
+    return RS_OK;
+}
+
 rs_status rs_layout_destroy(rs_layout *l) {
     delete l;
     return RS_OK;
@@ -220,11 +248,20 @@ static rs_status step_common(const rs_layout *l, bool kda, bool replay, void *po
         fill(P);
         e = D == 128 ? rs::launch_step_f32_d128(L, P, s) : rs::launch_step_f32_d64(L, P, s);
     } else {
-        static thread_local rs::StepParamsPi P;
-        fill(P);
-        for (size_t i = 0; i < l->pi.size(); ++i) P.pi[i] = (uint8_t)l->pi[i];
-        e = (replay || T_max > 1) ? rs::launch_step_mixed_replay(L, P, s)
-                                  : rs::launch_step_mixed_decode(L, P, s);
+        if (l->group) {  // DAMP-exact layout: single decode steps
+            if (replay || T_max > 1) return RS_ERR_UNSUPPORTED;
+            static thread_local rs::StepParamsDamp P;
+            fill(P);
+            for (size_t i = 0; i < l->pi.size(); ++i) P.pi[i] = (uint8_t)l->pi[i];
+            std::copy(l->cs.begin(), l->cs.end(), P.cs);
+            e = rs::launch_step_damp_decode(L, P, s);
+        } else {
+            static thread_local rs::StepParamsPi P;
+            fill(P);
+            for (size_t i = 0; i < l->pi.size(); ++i) P.pi[i] = (uint8_t)l->pi[i];
+            e = (replay || T_max > 1) ? rs::launch_step_mixed_replay(L, P, s)
+                                      : rs::launch_step_mixed_decode(L, P, s);
+        }
     }
     if (e != cudaSuccess) return launch_fail(e);
     return RS_OK;
@@ -271,12 +308,29 @@ rs_status rs_state_convert(const rs_layout *src_l, const void *src_pool, const r
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (a.kind == b.kind) {
-        if (a.kind == RS_LAYOUT_MIXED_FP16_INT8 && (a.k_hi != b.k_hi || src_l->pi != dst_l->pi))
+        if (a.kind == RS_LAYOUT_MIXED_FP16_INT8 &&
+            (a.k_hi != b.k_hi || src_l->pi != dst_l->pi || src_l->group != dst_l->group || src_l->cs != dst_l->cs))
             return RS_ERR_UNSUPPORTED;
         e = rs::launch_copy_heads(src_pool, dst_pool, (int64_t)src_l->head_bytes, slots, n, n_slots,
                                   a.num_v_heads, status, s);
     } else {
         const rs_layout *mixed = a.kind == RS_LAYOUT_MIXED_FP16_INT8 ? src_l : dst_l;
+        if (mixed->group) {  // DAMP-exact layout
+            static thread_local rs::ConvertParamsDamp P;
+            P.src = src_pool;
+            P.dst = dst_pool;
+            P.n_slots = n_slots;
+            P.slots = slots;
+            P.status = status;
+            P.n = n;
+            P.Hv = a.num_v_heads;
+            P.to_mixed = b.kind == RS_LAYOUT_MIXED_FP16_INT8 ? 1 : 0;
+            for (size_t i = 0; i < mixed->pi.size(); ++i) P.pi[i] = (uint8_t)mixed->pi[i];
+            std::copy(mixed->cs.begin(), mixed->cs.end(), P.cs);
+            e = rs::launch_convert_damp(a.dk, mixed->p.k_hi, P, s);
+            if (e != cudaSuccess) return launch_fail(e);
+            return RS_OK;
+        }
         static thread_local rs::ConvertParamsPi P;
         P.src = src_pool;
         P.dst = dst_pool;
