@@ -361,7 +361,7 @@ def _time(torch, fn, iters, warm=3):
     return e0.elapsed_time(e1) / 1e3 / iters
 
 
-EXTRA = ("gdn_fp32", "kda_fp32", "kda_mixed", "gdn_mixed", "replay_mixed", "replay_fp32",
+EXTRA = ("gdn_fp32", "kda_fp32", "kda_mixed", "gdn_mixed", "kda_damp", "replay_mixed", "replay_fp32",
          "pack_gdn", "restore_gdn", "pack_kda", "restore_kda", "pack_int8_gdn", "restore_int8_gdn",
          "pack_int8_kda", "restore_int8_kda", "pack_mixed", "restore_mixed")
 
@@ -404,7 +404,7 @@ def extra_kernels(args, rs, torch, dev, peak, world, only=None):
         del pool, q, k, v
         torch.cuda.empty_cache()
     KDA_B = dict(KDA, B=B)
-    if want & {"kda_fp32", "kda_mixed", "gdn_mixed", "replay_mixed", "replay_fp32"}:
+    if want & {"kda_fp32", "kda_mixed", "gdn_mixed", "kda_damp", "replay_mixed", "replay_fp32"}:
         nsteps = 8
         w = gen.decode_workload(steps=nsteps, per_channel=True, in_dtype="bf16", seed=1,
                                 horizon=(2.0, 8192.0), **KDA_B)
@@ -437,6 +437,18 @@ def extra_kernels(args, rs, torch, dev, peak, world, only=None):
                 be[i % nsteps], o=o), iters, warm)
             rec(f"gdn_decode_mixed_b{B}_h32", sec,
                 decode_bytes(B, 32, 32, 128, mix.head_bytes, 2, False), B * 32)
+        if "kda_damp" in want:
+            # DAMP-exact storage: INT8 groups of 32 along dv, value scaling
+            damp = rs.Layout("damp", 128, KDA["Hv"], KDA["Hk"], k_hi=16, hi_rows=hi,
+                             value_scales=gen.value_scales(KDA["Hv"], 128, seed=1))
+            dpool = damp.empty_pool(B, device=dev)
+            rs.state_convert(f32, pool, damp, dpool, torch.arange(B, dtype=torch.int32, device=dev))
+            sec = _time(torch, lambda i: rs.kda_decode_update(
+                damp, dpool, slots, q[i % nsteps], k[i % nsteps], v[i % nsteps], al[i % nsteps],
+                be[i % nsteps], o=o), iters, warm)
+            rec(f"kda_decode_damp_g32_b{B}", sec, decode_bytes(B, 32, 32, 128, damp.head_bytes, 2, True),
+                B * 32, {"bits_per_value": damp.bits_per_value()})
+            del dpool
         if want & {"replay_mixed", "replay_fp32"}:
             T = 8
             n_acc = gen.n_accept(B, T, seed=1)
