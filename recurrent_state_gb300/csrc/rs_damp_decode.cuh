@@ -28,8 +28,9 @@ struct DampShape {
     static constexpr int kStage = (kStatePad + kTokBytes + 127) / 128 * 128;
     static constexpr int kRowVecs = KDA ? 4 : 3;
     static constexpr int kBlock = 16;
-    // per tile slot: row vectors; per warp: -s and 1/s of the block's rows for its two groups
-    static constexpr int kSlotBytes = (kRowVecs * D * 4 + 2 * 4 * 2 * kBlock + 127) / 128 * 128;
+    // per tile slot: row vectors; per warp (two): -s and 1/s of the block's rows for its two groups
+    static constexpr int kWarpScratch = 4 * kBlock * 4;
+    static constexpr int kSlotBytes = (kRowVecs * D * 4 + 2 * kWarpScratch + 127) / 128 * 128;
     static constexpr int kHeader = 256;
 };
 
