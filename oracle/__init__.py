@@ -103,6 +103,29 @@ def _declare(L):
     L.orc_quant_code.argtypes = [_F, _F]
     L.orc_quant_code.restype = ctypes.c_int8
     L.orc_quantise_row.argtypes = [_I, _P, _P, _P]
+    L.orc_quant_code_rcp.argtypes = [_F, _F]
+    L.orc_quant_code_rcp.restype = ctypes.c_int8
+    L.orc_quantise_row_m.argtypes = [_I, _P, _I, _P, _P]
+    L.orc_mixed_pack_m.argtypes = [_I, _I, _I, _I, _P, _P]
+    L.orc_mixed_unpack_decayed.argtypes = [_I, _I, _I, _P, _P, _P]
+    L.orc_convert_f32_to_mixed_m.argtypes = [_I, _I, _I, _I, _P, _P, _P]
+    L.orc_convert_f32_to_mixed_m.restype = _I
+    L.orc_decode_mixed_m.argtypes = [_I, _I, _I, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P,
+                                     _P, _P, _P, _P, _P, _I, _I]
+    L.orc_decode_mixed_m.restype = _I
+    L.orc_replay_mixed_m.argtypes = [_I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _I, _P, _P,
+                                     _P, _P, _P, _P, _P, _P, _P, _I, _I]
+    L.orc_replay_mixed_m.restype = _I
+    L.orc_damp_pack_m.argtypes = [_I, _I, _I, _I, _I, _P, _P]
+    L.orc_damp_unpack_decayed.argtypes = [_I, _I, _I, _I, _P, _P, _P]
+    L.orc_convert_f32_to_damp_m.argtypes = [_I, _I, _I, _I, _I, _P, _P, _P, _P]
+    L.orc_convert_f32_to_damp_m.restype = _I
+    L.orc_decode_damp_m.argtypes = [_I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P, _P,
+                                    _P, _P, _P, _P, _P, _I, _I]
+    L.orc_decode_damp_m.restype = _I
+    L.orc_replay_damp_m.argtypes = [_I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P,
+                                    _P, _P, _P, _P, _P, _P, _P, _I, _I]
+    L.orc_replay_damp_m.restype = _I
     L.orc_dequantise_row.argtypes = [_I, _P, _F, _P]
     L.orc_mixed_tile_bytes.argtypes = [_I, _I, _I]
     L.orc_mixed_tile_bytes.restype = ctypes.c_size_t
@@ -192,12 +215,19 @@ def row_scale(x):
     return np.float32(lib().orc_row_scale(x.size, _ptr(x)))
 
 
-def quantise_row(x):
+def quantise_row(x, mode=0):
+    """Codes and scale of one INT8 row; ``mode`` 0 (IEEE quotient) or 1 (fused
+    reciprocal arithmetic, see ``orc_quant_code_rcp`` in the C source)."""
     x = np.ascontiguousarray(x, np.float32)
     codes = np.zeros(x.size, np.int8)
     s = np.zeros(1, np.float32)
-    lib().orc_quantise_row(x.size, _ptr(x), _ptr(codes), _ptr(s))
+    lib().orc_quantise_row_m(x.size, _ptr(x), int(mode), _ptr(codes), _ptr(s))
     return codes, s[0]
+
+
+def quant_code_rcp(x, y):
+    """Mode-1 code of ``x`` given y = RN(1/s)."""
+    return int(lib().orc_quant_code_rcp(float(np.float32(x)), float(np.float32(y))))
 
 
 def dequantise_row(codes, s):
@@ -218,21 +248,30 @@ def mixed_unpack(tile, dk, dv, khi):
     return T
 
 
-def mixed_pack(T, khi):
+def mixed_pack(T, khi, mode=0):
     T = _c(np.ascontiguousarray(T), np.float32)
     dk, dv = T.shape
     tile = np.zeros(mixed_tile_bytes(dk, dv, khi), np.uint8)
-    lib().orc_mixed_pack(dk, dv, khi, _ptr(T), _ptr(tile))
+    lib().orc_mixed_pack_m(dk, dv, khi, int(mode), _ptr(T), _ptr(tile))
     return tile
 
 
-def convert_f32_to_mixed(S, khi, pi):
+def mixed_unpack_decayed(tile, dk, dv, khi, a):
+    """Mode-1 dequantise-and-decay of a tile with per-row decays ``a`` [dk]."""
+    tile = _c(np.ascontiguousarray(tile), np.uint8)
+    a = np.ascontiguousarray(a, np.float32)
+    T = np.zeros((dk, dv), np.float32)
+    lib().orc_mixed_unpack_decayed(dk, dv, khi, _ptr(tile), _ptr(a), _ptr(T))
+    return T
+
+
+def convert_f32_to_mixed(S, khi, pi, mode=0):
     """Logical FP32 head ``S`` [dk][dv] -> mixed tile bytes with row map ``pi``."""
     S = _c(np.ascontiguousarray(S), np.float32)
     dk, dv = S.shape
     pi = np.ascontiguousarray(pi, np.int16)
     tile = np.zeros(mixed_tile_bytes(dk, dv, khi), np.uint8)
-    assert lib().orc_convert_f32_to_mixed(dk, dv, khi, _ptr(pi), _ptr(S), _ptr(tile)) == 0
+    assert lib().orc_convert_f32_to_mixed_m(dk, dv, khi, int(mode), _ptr(pi), _ptr(S), _ptr(tile)) == 0
     return tile
 
 
@@ -244,14 +283,14 @@ def convert_mixed_to_f32(tile, dk, dv, khi, pi):
     return S
 
 
-def convert_pool_f32_to_mixed(pool, khi, pi):
+def convert_pool_f32_to_mixed(pool, khi, pi, mode=0):
     """[..., Hv, dk, dv] float32 -> [..., Hv, tile_bytes] uint8; pi [Hv][dk]."""
     *lead, Hv, dk, dv = pool.shape
     flat = pool.reshape(-1, Hv, dk, dv)
     out = np.zeros((flat.shape[0], Hv, mixed_tile_bytes(dk, dv, khi)), np.uint8)
     for s in range(flat.shape[0]):
         for h in range(Hv):
-            out[s, h] = convert_f32_to_mixed(np.ascontiguousarray(flat[s, h]), khi, pi[h])
+            out[s, h] = convert_f32_to_mixed(np.ascontiguousarray(flat[s, h]), khi, pi[h], mode)
     return out.reshape(*lead, Hv, out.shape[-1])
 
 
@@ -287,8 +326,9 @@ def decode_f32(pool, slot_idx, q, k, v, alpha, beta, o=None, per_channel=None,
 
 
 def decode_mixed(pool, slot_idx, pi, khi, dk, dv, q, k, v, alpha, beta, o=None,
-                 per_channel=None, items=None):
-    """Batched mixed-layout decode in place on ``pool`` [n_slots][Hv][tile_bytes]."""
+                 per_channel=None, items=None, mode=0):
+    """Batched mixed-layout decode in place on ``pool`` [n_slots][Hv][tile_bytes];
+    ``mode`` selects the requantisation arithmetic (0 IEEE, 1 fused)."""
     _c(pool, np.uint8)
     n_slots, Hv, tb = pool.shape
     assert tb == mixed_tile_bytes(dk, dv, khi)
@@ -298,7 +338,7 @@ def decode_mixed(pool, slot_idx, pi, khi, dk, dv, q, k, v, alpha, beta, o=None,
     if o is None:
         o = np.zeros((B, Hv, dv), np.float32)
     lo, hi = items if items is not None else (0, B * Hv)
-    st = lib().orc_decode_mixed(B, Hk, Hv, dk, dv, khi, int(per_channel), _ptr(pool),
+    st = lib().orc_decode_mixed_m(B, Hk, Hv, dk, dv, khi, int(per_channel), int(mode), _ptr(pool),
                                 n_slots, _ptr(_c(slot_idx, np.int32)),
                                 _ptr(_c(pi, np.int16)), _ptr(_c(q, np.float32)),
                                 _ptr(_c(k, np.float32)), _ptr(_c(v, np.float32)),
@@ -328,7 +368,7 @@ def replay_f32(pool, slot_idx, n_accept, q, k, v, alpha, beta, o=None,
 
 
 def replay_mixed(pool, slot_idx, n_accept, pi, khi, dk, dv, q, k, v, alpha, beta,
-                 o=None, per_channel=None, items=None):
+                 o=None, per_channel=None, items=None, mode=0):
     _c(pool, np.uint8)
     n_slots, Hv, tb = pool.shape
     assert tb == mixed_tile_bytes(dk, dv, khi)
@@ -338,7 +378,7 @@ def replay_mixed(pool, slot_idx, n_accept, pi, khi, dk, dv, q, k, v, alpha, beta
     if o is None:
         o = np.zeros((B, T_max, Hv, dv), np.float32)
     lo, hi = items if items is not None else (0, B * Hv)
-    st = lib().orc_replay_mixed(B, T_max, Hk, Hv, dk, dv, khi, int(per_channel),
+    st = lib().orc_replay_mixed_m(B, T_max, Hk, Hv, dk, dv, khi, int(per_channel), int(mode),
                                 _ptr(pool), n_slots, _ptr(_c(slot_idx, np.int32)),
                                 _ptr(_c(n_accept, np.int32)), _ptr(_c(pi, np.int16)),
                                 _ptr(_c(q, np.float32)), _ptr(_c(k, np.float32)),
@@ -439,15 +479,23 @@ def damp_unpack(tile, dk, dv, khi, group):
     return T
 
 
-def damp_pack(T, khi, group):
+def damp_pack(T, khi, group, mode=0):
     T = _c(np.ascontiguousarray(T), np.float32)
     dk, dv = T.shape
     tile = np.zeros(damp_tile_bytes(dk, dv, khi, group), np.uint8)
-    lib().orc_damp_pack(dk, dv, khi, group, _ptr(T), _ptr(tile))
+    lib().orc_damp_pack_m(dk, dv, khi, group, int(mode), _ptr(T), _ptr(tile))
     return tile
 
 
-def convert_pool_f32_to_damp(pool, khi, group, pi, cs):
+def damp_unpack_decayed(tile, dk, dv, khi, group, a):
+    tile = _c(np.ascontiguousarray(tile), np.uint8)
+    a = np.ascontiguousarray(a, np.float32)
+    T = np.zeros((dk, dv), np.float32)
+    lib().orc_damp_unpack_decayed(dk, dv, khi, group, _ptr(tile), _ptr(a), _ptr(T))
+    return T
+
+
+def convert_pool_f32_to_damp(pool, khi, group, pi, cs, mode=0):
     """[..., Hv, dk, dv] float32 -> [..., Hv, tile_bytes] uint8; pi [Hv][dk],
     cs [Hv][dv] value-scaling factors."""
     *lead, Hv, dk, dv = pool.shape
@@ -458,8 +506,8 @@ def convert_pool_f32_to_damp(pool, khi, group, pi, cs):
     for s in range(flat.shape[0]):
         for h in range(Hv):
             S = np.ascontiguousarray(flat[s, h])
-            assert lib().orc_convert_f32_to_damp(dk, dv, khi, group, _ptr(pi[h]), _ptr(cs[h]), _ptr(S),
-                                                 _ptr(out[s, h])) == 0
+            assert lib().orc_convert_f32_to_damp_m(dk, dv, khi, group, int(mode), _ptr(pi[h]),
+                                                   _ptr(cs[h]), _ptr(S), _ptr(out[s, h])) == 0
     return out.reshape(*lead, Hv, out.shape[-1])
 
 
@@ -477,7 +525,7 @@ def convert_pool_damp_to_f32(pool, dk, dv, khi, group, pi, cs):
 
 
 def decode_damp(pool, slot_idx, pi, cs, khi, group, dk, dv, q, k, v, alpha, beta, o=None,
-                per_channel=None, items=None):
+                per_channel=None, items=None, mode=0):
     """Batched DAMP-exact decode in place on ``pool`` [n_slots][Hv][tile_bytes]."""
     _c(pool, np.uint8)
     n_slots, Hv, tb = pool.shape
@@ -488,7 +536,8 @@ def decode_damp(pool, slot_idx, pi, cs, khi, group, dk, dv, q, k, v, alpha, beta
     if o is None:
         o = np.zeros((B, Hv, dv), np.float32)
     lo, hi = items if items is not None else (0, B * Hv)
-    st = lib().orc_decode_damp(B, Hk, Hv, dk, dv, khi, group, int(per_channel), _ptr(pool), n_slots,
+    st = lib().orc_decode_damp_m(B, Hk, Hv, dk, dv, khi, group, int(per_channel), int(mode), _ptr(pool),
+                                 n_slots,
                                _ptr(_c(slot_idx, np.int32)), _ptr(_c(pi, np.int16)),
                                _ptr(_c(cs, np.float32)), _ptr(_c(q, np.float32)),
                                _ptr(_c(k, np.float32)), _ptr(_c(v, np.float32)),
@@ -498,7 +547,7 @@ def decode_damp(pool, slot_idx, pi, cs, khi, group, dk, dv, q, k, v, alpha, beta
 
 
 def replay_damp(pool, slot_idx, n_accept, pi, cs, khi, group, dk, dv, q, k, v, alpha, beta, o=None,
-                per_channel=None, items=None):
+                per_channel=None, items=None, mode=0):
     _c(pool, np.uint8)
     n_slots, Hv, tb = pool.shape
     assert tb == damp_tile_bytes(dk, dv, khi, group)
@@ -508,7 +557,8 @@ def replay_damp(pool, slot_idx, n_accept, pi, cs, khi, group, dk, dv, q, k, v, a
     if o is None:
         o = np.zeros((B, T_max, Hv, dv), np.float32)
     lo, hi = items if items is not None else (0, B * Hv)
-    st = lib().orc_replay_damp(B, T_max, Hk, Hv, dk, dv, khi, group, int(per_channel), _ptr(pool),
+    st = lib().orc_replay_damp_m(B, T_max, Hk, Hv, dk, dv, khi, group, int(per_channel), int(mode),
+                                 _ptr(pool),
                                n_slots, _ptr(_c(slot_idx, np.int32)), _ptr(_c(n_accept, np.int32)),
                                _ptr(_c(pi, np.int16)), _ptr(_c(cs, np.float32)), _ptr(_c(q, np.float32)),
                                _ptr(_c(k, np.float32)), _ptr(_c(v, np.float32)),

@@ -38,6 +38,7 @@
  *   2 = an accepted-token count out of range (that item is skipped),
  *   4 = a checkpoint slot out of range (that item is skipped).
  */
+#include <float.h>
 #include <math.h>
 #include <stdint.h>
 #include <stddef.h>
@@ -97,7 +98,7 @@ void orc_step_tile_f32(int dk, int dv, float *S, const float *q, const float *k,
 /*   c_v = clip(round_half_even(x_v / s), -127, 127)                        */
 /* Dequantised value: c * s, one FP32 multiply.                              */
 /* ------------------------------------------------------------------------ */
-float orc_row_scale(int n, const float *x)
+static float row_absmax(int n, const float *x)
 {
     float a = 0.0f;
     int i;
@@ -106,7 +107,12 @@ float orc_row_scale(int n, const float *x)
         if (isnan(ax) || ax > a)
             a = ax;
     }
-    return fmaxf(a, 1e-8f) / 127.0f;
+    return a;
+}
+
+float orc_row_scale(int n, const float *x)
+{
+    return fmaxf(row_absmax(n, x), 1e-8f) / 127.0f;
 }
 
 int8_t orc_quant_code(float x, float s)
@@ -130,6 +136,50 @@ void orc_dequantise_row(int n, const int8_t *codes, float s, float *x)
     int i;
     for (i = 0; i < n; ++i)
         x[i] = (float)codes[i] * s;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Fused requantisation arithmetic (mode 1) of the mixed layouts.  The pages */
+/* fix the quantiser (s = max(a, 1e-8)/127, code = round(x/s) clipped to     */
+/* +-127, FP32) and the step (dequantise, decay, update, requantise), not    */
+/* how a kernel evaluates x/s or where the decay's rounding falls.  Mode 0   */
+/* (above and in the step) takes the IEEE quotient and decays the            */
+/* dequantised value.  Mode 1 is the reading a division-free kernel          */
+/* implements, with the same scale s:                                        */
+/*   - code = the integer nearest to the exact product x * RN(1/s), ties to  */
+/*     even (the quotient through the correctly rounded reciprocal, rounded  */
+/*     once); rows whose absmax is inf or NaN keep the IEEE quotient;        */
+/*   - a step that decays a dequantised INT8 row multiplies the row's scale: */
+/*     x = c * RN(s * a_u), since diag(a) diag(s) C = diag(a s) C ([DAMP]    */
+/*     §3.1 Lambda applied to the dequantised state of §3.2 Eq. 6); FP16 rows */
+/*     are decayed as in mode 0, x = RN(h * a_u).                            */
+/* A mode-1 code differs from the mode-0 code only where x/s lies within a   */
+/* few units of 2^-24 |x/s| of a half-integer (the spec allowance is   */
+/* 1e-6 max(1, |x/s|)).                                                      */
+/* ------------------------------------------------------------------------ */
+int8_t orc_quant_code_rcp(float x, float y)
+{
+    /* a product of two binary32 values is exact in binary64 */
+    double r = rint((double)x * (double)y);
+    if (r > 127.0) r = 127.0;
+    if (r < -127.0) r = -127.0;
+    return (int8_t)r;
+}
+
+void orc_quantise_row_m(int n, const float *x, int mode, int8_t *codes, float *scale)
+{
+    float a = row_absmax(n, x);
+    float s = orc_row_scale(n, x);
+    int i;
+    if (mode == 1 && a <= FLT_MAX) {
+        float y = 1.0f / s;
+        for (i = 0; i < n; ++i)
+            codes[i] = orc_quant_code_rcp(x[i], y);
+    } else {
+        for (i = 0; i < n; ++i)
+            codes[i] = orc_quant_code(x[i], s);
+    }
+    *scale = s;
 }
 
 /* FP16 storage of a high-precision row: round to nearest even, overflow to
@@ -203,7 +253,7 @@ void orc_mixed_unpack(int dk, int dv, int khi, const uint8_t *tile, float *T)
     }
 }
 
-void orc_mixed_pack(int dk, int dv, int khi, const float *T, uint8_t *tile)
+void orc_mixed_pack_m(int dk, int dv, int khi, int mode, const float *T, uint8_t *tile)
 {
     uint8_t *hi = tile;
     uint8_t *lo = tile + (size_t)2 * khi * dv;
@@ -217,27 +267,62 @@ void orc_mixed_pack(int dk, int dv, int khi, const float *T, uint8_t *tile)
         }
     for (r = khi; r < dk; ++r) {
         float s;
-        orc_quantise_row(dv, T + (size_t)r * dv, row, &s);
+        orc_quantise_row_m(dv, T + (size_t)r * dv, mode, row, &s);
         for (c = 0; c < dv; ++c)
             lo[lo_offset(dv, r - khi, c)] = (uint8_t)row[c];
         memcpy(sc + (size_t)(r - khi) * 4, &s, 4);
     }
 }
 
+void orc_mixed_pack(int dk, int dv, int khi, const float *T, uint8_t *tile)
+{
+    orc_mixed_pack_m(dk, dv, khi, 0, T, tile);
+}
+
+/* Mode 1: dequantise and decay in one (see above): FP16 row r gives
+ * h * a[r], INT8 row r gives c * RN(s_r * a[r]). */
+void orc_mixed_unpack_decayed(int dk, int dv, int khi, const uint8_t *tile, const float *a, float *T)
+{
+    const uint8_t *hi = tile;
+    const uint8_t *lo = tile + (size_t)2 * khi * dv;
+    const uint8_t *sc = tile + (size_t)2 * khi * dv + (size_t)(dk - khi) * dv;
+    int8_t row[ORC_MAX_D];
+    int r, c;
+    for (r = 0; r < khi; ++r)
+        for (c = 0; c < dv; ++c) {
+            uint16_t b;
+            memcpy(&b, hi + hi_offset(dv, r, c), 2);
+            T[(size_t)r * dv + c] = f16_bits_to_f32(b) * a[r];
+        }
+    for (r = khi; r < dk; ++r) {
+        float s;
+        memcpy(&s, sc + (size_t)(r - khi) * 4, 4);
+        for (c = 0; c < dv; ++c)
+            row[c] = (int8_t)lo[lo_offset(dv, r - khi, c)];
+        orc_dequantise_row(dv, row, s * a[r], T + (size_t)r * dv);
+    }
+}
+
 /* Logical FP32 head S (rows = key channels) <-> mixed tile with row map pi:
  * physical row r holds logical channel pi[r] ([DAMP] Appendix A.2, last step
  * of Algorithm 1; Appendix A.3 Eq. 17). */
-int orc_convert_f32_to_mixed(int dk, int dv, int khi, const int16_t *pi,
-                             const float *S, uint8_t *tile)
+int orc_convert_f32_to_mixed_m(int dk, int dv, int khi, int mode, const int16_t *pi,
+                               const float *S, uint8_t *tile)
 {
     float *T = (float *)malloc((size_t)dk * dv * 4);
     int r;
     if (!T) return -1;
     for (r = 0; r < dk; ++r)
         memcpy(T + (size_t)r * dv, S + (size_t)pi[r] * dv, (size_t)dv * 4);
-    orc_mixed_pack(dk, dv, khi, T, tile);
+    orc_mixed_pack_m(dk, dv, khi, mode, T, tile);
     free(T);
     return 0;
+}
+
+int orc_convert_f32_to_mixed(int dk, int dv, int khi, const int16_t *pi,
+                             const float *S, uint8_t *tile)
+{
+    return orc_convert_f32_to_mixed_m(dk, dv, khi, 0, pi, S, tile);
 }
 
 int orc_convert_mixed_to_f32(int dk, int dv, int khi, const int16_t *pi,
@@ -292,12 +377,16 @@ int orc_decode_f32(int B, int Hk, int Hv, int dk, int dv, int per_channel,
 /* Mixed-layout decode: dequantise once, one FP32 step in the permuted
  * coordinates of [DAMP] Appendix A.3 Eq. 18 (inputs gathered by pi, the sums
  * over physical rows in ascending row order), requantise once and write back
- * ([DAMP] Appendix A.4 "Fused decoding").  pi: [Hv][dk]. */
-int orc_decode_mixed(int B, int Hk, int Hv, int dk, int dv, int khi, int per_channel,
-                     uint8_t *pool, int n_slots, const int32_t *slot_idx,
-                     const int16_t *pi, const float *q, const float *k, const float *v,
-                     const float *alpha, const float *beta, float *o,
-                     int item_begin, int item_end)
+ * ([DAMP] Appendix A.4 "Fused decoding").  pi: [Hv][dk].  mode: 0 or 1, the
+ * requantisation arithmetic (see orc_quant_code_rcp); in mode 1 the decay is
+ * applied while dequantising and the step itself decays by 1 (exact). */
+static const float k_one = 1.0f;
+
+int orc_decode_mixed_m(int B, int Hk, int Hv, int dk, int dv, int khi, int per_channel, int mode,
+                       uint8_t *pool, int n_slots, const int32_t *slot_idx,
+                       const int16_t *pi, const float *q, const float *k, const float *v,
+                       const float *alpha, const float *beta, float *o,
+                       int item_begin, int item_end)
 {
     float *T = (float *)malloc((size_t)dk * dv * 4);
     float qp[ORC_MAX_D], kp[ORC_MAX_D], ap[ORC_MAX_D];
@@ -319,14 +408,31 @@ int orc_decode_mixed(int B, int Hk, int Hv, int dk, int dv, int khi, int per_cha
             ap[r] = per_channel ? alpha[((size_t)b * Hv + h) * dk + ph[r]]
                                 : alpha[(size_t)b * Hv + h];
         }
-        orc_mixed_unpack(dk, dv, khi, tile, T);
-        orc_step_tile_f32(dk, dv, T, qp, kp, v + ((size_t)b * Hv + h) * dv, ap, 1,
-                          beta[(size_t)b * Hv + h],
-                          o ? o + ((size_t)b * Hv + h) * dv : NULL);
-        orc_mixed_pack(dk, dv, khi, T, tile);
+        if (mode == 1) {
+            orc_mixed_unpack_decayed(dk, dv, khi, tile, ap, T);
+            orc_step_tile_f32(dk, dv, T, qp, kp, v + ((size_t)b * Hv + h) * dv, &k_one, 0,
+                              beta[(size_t)b * Hv + h],
+                              o ? o + ((size_t)b * Hv + h) * dv : NULL);
+        } else {
+            orc_mixed_unpack(dk, dv, khi, tile, T);
+            orc_step_tile_f32(dk, dv, T, qp, kp, v + ((size_t)b * Hv + h) * dv, ap, 1,
+                              beta[(size_t)b * Hv + h],
+                              o ? o + ((size_t)b * Hv + h) * dv : NULL);
+        }
+        orc_mixed_pack_m(dk, dv, khi, mode, T, tile);
     }
     free(T);
     return status;
+}
+
+int orc_decode_mixed(int B, int Hk, int Hv, int dk, int dv, int khi, int per_channel,
+                     uint8_t *pool, int n_slots, const int32_t *slot_idx,
+                     const int16_t *pi, const float *q, const float *k, const float *v,
+                     const float *alpha, const float *beta, float *o,
+                     int item_begin, int item_end)
+{
+    return orc_decode_mixed_m(B, Hk, Hv, dk, dv, khi, per_channel, 0, pool, n_slots, slot_idx, pi,
+                              q, k, v, alpha, beta, o, item_begin, item_end);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -363,11 +469,13 @@ int orc_replay_f32(int B, int T_max, int Hk, int Hv, int dk, int dv, int per_cha
     return status;
 }
 
-int orc_replay_mixed(int B, int T_max, int Hk, int Hv, int dk, int dv, int khi, int per_channel,
-                     uint8_t *pool, int n_slots, const int32_t *slot_idx, const int32_t *n_accept,
-                     const int16_t *pi, const float *q, const float *k, const float *v,
-                     const float *alpha, const float *beta, float *o,
-                     int item_begin, int item_end)
+/* mode as in orc_decode_mixed_m: in mode 1 the first token's decay is
+ * applied while dequantising, so one replayed token equals one decode step. */
+int orc_replay_mixed_m(int B, int T_max, int Hk, int Hv, int dk, int dv, int khi, int per_channel,
+                       int mode, uint8_t *pool, int n_slots, const int32_t *slot_idx,
+                       const int32_t *n_accept, const int16_t *pi, const float *q, const float *k,
+                       const float *v, const float *alpha, const float *beta, float *o,
+                       int item_begin, int item_end)
 {
     float *T = (float *)malloc((size_t)dk * dv * 4);
     float qp[ORC_MAX_D], kp[ORC_MAX_D], ap[ORC_MAX_D];
@@ -384,7 +492,6 @@ int orc_replay_mixed(int B, int T_max, int Hk, int Hv, int dk, int dv, int khi, 
         if (n < 0 || n > T_max) { status |= 2; continue; }
         if (n == 0) continue;            /* nothing accepted: state untouched */
         tile = pool + ((size_t)slot * Hv + h) * tb;
-        orc_mixed_unpack(dk, dv, khi, tile, T);
         for (t = 0; t < n; ++t) {
             size_t bt = (size_t)b * T_max + t;
             const float *qh = q + (bt * Hk + g) * dk, *kh = k + (bt * Hk + g) * dk;
@@ -393,13 +500,31 @@ int orc_replay_mixed(int B, int T_max, int Hk, int Hv, int dk, int dv, int khi, 
                 kp[r] = kh[ph[r]];
                 ap[r] = per_channel ? alpha[(bt * Hv + h) * dk + ph[r]] : alpha[bt * Hv + h];
             }
+            if (t == 0 && mode == 1) {
+                orc_mixed_unpack_decayed(dk, dv, khi, tile, ap, T);
+                orc_step_tile_f32(dk, dv, T, qp, kp, v + (bt * Hv + h) * dv, &k_one, 0,
+                                  beta[bt * Hv + h], o ? o + (bt * Hv + h) * dv : NULL);
+                continue;
+            }
+            if (t == 0)
+                orc_mixed_unpack(dk, dv, khi, tile, T);
             orc_step_tile_f32(dk, dv, T, qp, kp, v + (bt * Hv + h) * dv, ap, 1,
                               beta[bt * Hv + h], o ? o + (bt * Hv + h) * dv : NULL);
         }
-        orc_mixed_pack(dk, dv, khi, T, tile);
+        orc_mixed_pack_m(dk, dv, khi, mode, T, tile);
     }
     free(T);
     return status;
+}
+
+int orc_replay_mixed(int B, int T_max, int Hk, int Hv, int dk, int dv, int khi, int per_channel,
+                     uint8_t *pool, int n_slots, const int32_t *slot_idx, const int32_t *n_accept,
+                     const int16_t *pi, const float *q, const float *k, const float *v,
+                     const float *alpha, const float *beta, float *o,
+                     int item_begin, int item_end)
+{
+    return orc_replay_mixed_m(B, T_max, Hk, Hv, dk, dv, khi, per_channel, 0, pool, n_slots, slot_idx,
+                              n_accept, pi, q, k, v, alpha, beta, o, item_begin, item_end);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -714,7 +839,7 @@ void orc_damp_unpack(int dk, int dv, int khi, int group, const uint8_t *tile, fl
     }
 }
 
-void orc_damp_pack(int dk, int dv, int khi, int group, const float *T, uint8_t *tile)
+void orc_damp_pack_m(int dk, int dv, int khi, int group, int mode, const float *T, uint8_t *tile)
 {
     uint8_t *hi = tile;
     uint8_t *lo = tile + (size_t)2 * khi * dv;
@@ -729,7 +854,7 @@ void orc_damp_pack(int dk, int dv, int khi, int group, const float *T, uint8_t *
     for (r = khi; r < dk; ++r) {
         for (gi = 0; gi < ng; ++gi) {
             float s;
-            orc_quantise_row(group, T + (size_t)r * dv + gi * group, row + gi * group, &s);
+            orc_quantise_row_m(group, T + (size_t)r * dv + gi * group, mode, row + gi * group, &s);
             memcpy(sc + ((size_t)(r - khi) * ng + gi) * 4, &s, 4);
         }
         for (c = 0; c < dv; ++c)
@@ -737,10 +862,42 @@ void orc_damp_pack(int dk, int dv, int khi, int group, const float *T, uint8_t *
     }
 }
 
+void orc_damp_pack(int dk, int dv, int khi, int group, const float *T, uint8_t *tile)
+{
+    orc_damp_pack_m(dk, dv, khi, group, 0, T, tile);
+}
+
+/* Mode 1 (see orc_quant_code_rcp): dequantise and decay in one; the decay of
+ * INT8 row r multiplies each of its group scales, c * RN(s_g * a[r]). */
+void orc_damp_unpack_decayed(int dk, int dv, int khi, int group, const uint8_t *tile, const float *a,
+                             float *T)
+{
+    const uint8_t *hi = tile;
+    const uint8_t *lo = tile + (size_t)2 * khi * dv;
+    const uint8_t *sc = tile + (size_t)2 * khi * dv + (size_t)(dk - khi) * dv;
+    int ng = dv / group, r, c, gi;
+    int8_t row[ORC_MAX_D];
+    for (r = 0; r < khi; ++r)
+        for (c = 0; c < dv; ++c) {
+            uint16_t b;
+            memcpy(&b, hi + hi_offset(dv, r, c), 2);
+            T[(size_t)r * dv + c] = f16_bits_to_f32(b) * a[r];
+        }
+    for (r = khi; r < dk; ++r) {
+        for (c = 0; c < dv; ++c)
+            row[c] = (int8_t)lo[lo_offset(dv, r - khi, c)];
+        for (gi = 0; gi < ng; ++gi) {
+            float s;
+            memcpy(&s, sc + ((size_t)(r - khi) * ng + gi) * 4, 4);
+            orc_dequantise_row(group, row + gi * group, s * a[r], T + (size_t)r * dv + gi * group);
+        }
+    }
+}
+
 /* S (logical rows, value order as produced) <-> tile: T[r][c] = S[pi[r]][c]
  * / cs[c] ([DAMP] Appendix A.3 Eq. 17), and back S[pi[r]][c] = T[r][c] * cs[c]. */
-int orc_convert_f32_to_damp(int dk, int dv, int khi, int group, const int16_t *pi, const float *cs,
-                            const float *S, uint8_t *tile)
+int orc_convert_f32_to_damp_m(int dk, int dv, int khi, int group, int mode, const int16_t *pi,
+                              const float *cs, const float *S, uint8_t *tile)
 {
     float *T = (float *)malloc((size_t)dk * dv * 4);
     int r, c;
@@ -748,9 +905,15 @@ int orc_convert_f32_to_damp(int dk, int dv, int khi, int group, const int16_t *p
     for (r = 0; r < dk; ++r)
         for (c = 0; c < dv; ++c)
             T[(size_t)r * dv + c] = S[(size_t)pi[r] * dv + c] / cs[c];
-    orc_damp_pack(dk, dv, khi, group, T, tile);
+    orc_damp_pack_m(dk, dv, khi, group, mode, T, tile);
     free(T);
     return 0;
+}
+
+int orc_convert_f32_to_damp(int dk, int dv, int khi, int group, const int16_t *pi, const float *cs,
+                            const float *S, uint8_t *tile)
+{
+    return orc_convert_f32_to_damp_m(dk, dv, khi, group, 0, pi, cs, S, tile);
 }
 
 int orc_convert_damp_to_f32(int dk, int dv, int khi, int group, const int16_t *pi, const float *cs,
@@ -769,25 +932,26 @@ int orc_convert_damp_to_f32(int dk, int dv, int khi, int group, const int16_t *p
 
 /* One transformed step on T ([DAMP] Appendix A.3 Eq. 18). */
 static void damp_step(int dk, int dv, float *T, const float *qp, const float *kp, const float *v,
-                      const float *cs, const float *ap, float beta, float *o)
+                      const float *cs, const float *ap, int a_stride, float beta, float *o)
 {
     float vp[ORC_MAX_D], op[ORC_MAX_D];
     int c;
     for (c = 0; c < dv; ++c)
         vp[c] = v[c] / cs[c];
-    orc_step_tile_f32(dk, dv, T, qp, kp, vp, ap, 1, beta, o ? op : NULL);
+    orc_step_tile_f32(dk, dv, T, qp, kp, vp, ap, a_stride, beta, o ? op : NULL);
     if (o)
         for (c = 0; c < dv; ++c)
             o[c] = cs[c] * op[c];
 }
 
-/* Batched decode / replay on DAMP tiles: as orc_decode_mixed and
- * orc_replay_mixed, with group-wise INT8 scales and value scaling; cs is
+/* Batched decode / replay on DAMP tiles: as orc_decode_mixed_m and
+ * orc_replay_mixed_m, with group-wise INT8 scales and value scaling; cs is
  * [Hv][dv] (one vector per head). */
-int orc_decode_damp(int B, int Hk, int Hv, int dk, int dv, int khi, int group, int per_channel,
-                    uint8_t *pool, int n_slots, const int32_t *slot_idx, const int16_t *pi,
-                    const float *cs, const float *q, const float *k, const float *v,
-                    const float *alpha, const float *beta, float *o, int item_begin, int item_end)
+int orc_decode_damp_m(int B, int Hk, int Hv, int dk, int dv, int khi, int group, int per_channel,
+                      int mode, uint8_t *pool, int n_slots, const int32_t *slot_idx,
+                      const int16_t *pi, const float *cs, const float *q, const float *k,
+                      const float *v, const float *alpha, const float *beta, float *o,
+                      int item_begin, int item_end)
 {
     float *T = (float *)malloc((size_t)dk * dv * 4);
     float qp[ORC_MAX_D], kp[ORC_MAX_D], ap[ORC_MAX_D];
@@ -808,20 +972,35 @@ int orc_decode_damp(int B, int Hk, int Hv, int dk, int dv, int khi, int group, i
             kp[r] = kh[ph[r]];
             ap[r] = per_channel ? alpha[((size_t)b * Hv + h) * dk + ph[r]] : alpha[(size_t)b * Hv + h];
         }
-        orc_damp_unpack(dk, dv, khi, group, tile, T);
-        damp_step(dk, dv, T, qp, kp, v + ((size_t)b * Hv + h) * dv, cs + (size_t)h * dv, ap,
-                  beta[(size_t)b * Hv + h], o ? o + ((size_t)b * Hv + h) * dv : NULL);
-        orc_damp_pack(dk, dv, khi, group, T, tile);
+        if (mode == 1) {
+            orc_damp_unpack_decayed(dk, dv, khi, group, tile, ap, T);
+            damp_step(dk, dv, T, qp, kp, v + ((size_t)b * Hv + h) * dv, cs + (size_t)h * dv, &k_one,
+                      0, beta[(size_t)b * Hv + h], o ? o + ((size_t)b * Hv + h) * dv : NULL);
+        } else {
+            orc_damp_unpack(dk, dv, khi, group, tile, T);
+            damp_step(dk, dv, T, qp, kp, v + ((size_t)b * Hv + h) * dv, cs + (size_t)h * dv, ap, 1,
+                      beta[(size_t)b * Hv + h], o ? o + ((size_t)b * Hv + h) * dv : NULL);
+        }
+        orc_damp_pack_m(dk, dv, khi, group, mode, T, tile);
     }
     free(T);
     return status;
 }
 
-int orc_replay_damp(int B, int T_max, int Hk, int Hv, int dk, int dv, int khi, int group,
-                    int per_channel, uint8_t *pool, int n_slots, const int32_t *slot_idx,
-                    const int32_t *n_accept, const int16_t *pi, const float *cs, const float *q,
-                    const float *k, const float *v, const float *alpha, const float *beta, float *o,
-                    int item_begin, int item_end)
+int orc_decode_damp(int B, int Hk, int Hv, int dk, int dv, int khi, int group, int per_channel,
+                    uint8_t *pool, int n_slots, const int32_t *slot_idx, const int16_t *pi,
+                    const float *cs, const float *q, const float *k, const float *v,
+                    const float *alpha, const float *beta, float *o, int item_begin, int item_end)
+{
+    return orc_decode_damp_m(B, Hk, Hv, dk, dv, khi, group, per_channel, 0, pool, n_slots, slot_idx,
+                             pi, cs, q, k, v, alpha, beta, o, item_begin, item_end);
+}
+
+int orc_replay_damp_m(int B, int T_max, int Hk, int Hv, int dk, int dv, int khi, int group,
+                      int per_channel, int mode, uint8_t *pool, int n_slots, const int32_t *slot_idx,
+                      const int32_t *n_accept, const int16_t *pi, const float *cs, const float *q,
+                      const float *k, const float *v, const float *alpha, const float *beta, float *o,
+                      int item_begin, int item_end)
 {
     float *T = (float *)malloc((size_t)dk * dv * 4);
     float qp[ORC_MAX_D], kp[ORC_MAX_D], ap[ORC_MAX_D];
@@ -838,7 +1017,6 @@ int orc_replay_damp(int B, int T_max, int Hk, int Hv, int dk, int dv, int khi, i
         if (n < 0 || n > T_max) { status |= 2; continue; }
         if (n == 0) continue;
         tile = pool + ((size_t)slot * Hv + h) * tb;
-        orc_damp_unpack(dk, dv, khi, group, tile, T);
         for (t = 0; t < n; ++t) {
             size_t bt = (size_t)b * T_max + t;
             const float *qh = q + (bt * Hk + g) * dk, *kh = k + (bt * Hk + g) * dk;
@@ -847,11 +1025,29 @@ int orc_replay_damp(int B, int T_max, int Hk, int Hv, int dk, int dv, int khi, i
                 kp[r] = kh[ph[r]];
                 ap[r] = per_channel ? alpha[(bt * Hv + h) * dk + ph[r]] : alpha[bt * Hv + h];
             }
-            damp_step(dk, dv, T, qp, kp, v + (bt * Hv + h) * dv, cs + (size_t)h * dv, ap,
+            if (t == 0 && mode == 1) {
+                orc_damp_unpack_decayed(dk, dv, khi, group, tile, ap, T);
+                damp_step(dk, dv, T, qp, kp, v + (bt * Hv + h) * dv, cs + (size_t)h * dv, &k_one, 0,
+                          beta[bt * Hv + h], o ? o + (bt * Hv + h) * dv : NULL);
+                continue;
+            }
+            if (t == 0)
+                orc_damp_unpack(dk, dv, khi, group, tile, T);
+            damp_step(dk, dv, T, qp, kp, v + (bt * Hv + h) * dv, cs + (size_t)h * dv, ap, 1,
                       beta[bt * Hv + h], o ? o + (bt * Hv + h) * dv : NULL);
         }
-        orc_damp_pack(dk, dv, khi, group, T, tile);
+        orc_damp_pack_m(dk, dv, khi, group, mode, T, tile);
     }
     free(T);
     return status;
+}
+
+int orc_replay_damp(int B, int T_max, int Hk, int Hv, int dk, int dv, int khi, int group,
+                    int per_channel, uint8_t *pool, int n_slots, const int32_t *slot_idx,
+                    const int32_t *n_accept, const int16_t *pi, const float *cs, const float *q,
+                    const float *k, const float *v, const float *alpha, const float *beta, float *o,
+                    int item_begin, int item_end)
+{
+    return orc_replay_damp_m(B, T_max, Hk, Hv, dk, dv, khi, group, per_channel, 0, pool, n_slots,
+                             slot_idx, n_accept, pi, cs, q, k, v, alpha, beta, o, item_begin, item_end);
 }

@@ -21,6 +21,7 @@ from recurrent_state_gb300 import inputs as gen
 from . import test_oracle_ckpt as ck
 from . import test_oracle_ckpt_int8 as i8
 from . import test_oracle_damp as dm
+from . import test_oracle_fused as fz
 from . import test_oracle_mixed as mx
 from . import test_oracle_quant as qt
 from . import test_oracle_recurrence as rc
@@ -56,6 +57,13 @@ CHECKS = [
     ("damp_bound", dm.test_group_error_bound),
     ("damp_pow2", lambda: dm.test_pow2_value_scaling_equivariance(True)),
     ("damp_fp64", dm.test_transformed_step_matches_original_map_fp64),
+    ("fused_code", fz.test_rcp_code_is_nearest_integer_to_exact_product),
+    ("fused_once", fz.test_rcp_code_rounds_the_exact_product_once),
+    ("fused_constructed", fz.test_constructed_row_where_the_modes_differ),
+    ("fused_unpack", fz.test_unpack_decayed_matches_numpy_float32),
+    ("fused_bound", lambda: fz.test_fused_step_within_local_quantisation_error(True)),
+    ("fused_replay", lambda: fz.test_fused_replay_one_equals_decode(True)),
+    ("damp_fused_unpack", fz.test_damp_unpack_decayed_matches_numpy_float32),
 ]
 
 READOUT_BLOCK = """    /* readout o = S^T q on the updated state */
@@ -92,7 +100,8 @@ MUTATIONS = {
     "readout_before_write": [(WRITE_BLOCK + READOUT_BLOCK, READOUT_BLOCK + WRITE_BLOCK)],
     "gqa_modulo": [("{ return h / (Hv / Hk); }", "{ return h % Hk; }")],
     "round_half_away": [("float r = rintf(x / s);", "float r = roundf(x / s);")],
-    "scale_128": [("return fmaxf(a, 1e-8f) / 127.0f;", "return fmaxf(a, 1e-8f) / 128.0f;")],
+    "scale_128": [("return fmaxf(row_absmax(n, x), 1e-8f) / 127.0f;",
+                   "return fmaxf(row_absmax(n, x), 1e-8f) / 128.0f;")],
     "abs_dropped": [("float ax = fabsf(x[i]);", "float ax = x[i];")],
     "offsets_not_cumulative": [("offsets[l] = offsets[l - 1] + r;", "offsets[l] = r;")],
     "pack_reversed_in_layer": [
@@ -103,10 +112,25 @@ MUTATIONS = {
     "mixed_alpha_unpermuted": [("? alpha[((size_t)b * Hv + h) * dk + ph[r]]",
                                 "? alpha[((size_t)b * Hv + h) * dk + r]")],
     "replay_requant_each_token": [
-        ("NULL);\n        }\n        orc_mixed_pack(dk, dv, khi, T, tile);",
-         "NULL);\n            orc_mixed_pack(dk, dv, khi, T, tile);\n"
+        ("beta[bt * Hv + h], o ? o + (bt * Hv + h) * dv : NULL);\n        }\n"
+         "        orc_mixed_pack_m(dk, dv, khi, mode, T, tile);",
+         "beta[bt * Hv + h], o ? o + (bt * Hv + h) * dv : NULL);\n"
+         "            orc_mixed_pack_m(dk, dv, khi, mode, T, tile);\n"
          "            orc_mixed_unpack(dk, dv, khi, tile, T);\n        }\n"
-         "        orc_mixed_pack(dk, dv, khi, T, tile);")],
+         "        orc_mixed_pack_m(dk, dv, khi, mode, T, tile);")],
+    "fused_decay_twice": [("&k_one, 0,\n                              beta[(size_t)b * Hv + h],",
+                           "ap, 1,\n                              beta[(size_t)b * Hv + h],")],
+    "fused_double_rounding": [("double r = rint((double)x * (double)y);",
+                               "double r = rint((double)(x * y));")],
+    "fused_mode_ignored": [("if (mode == 1 && a <= FLT_MAX) {", "if (0) {")],
+    "fused_int8_decay_dropped": [("orc_dequantise_row(dv, row, s * a[r], T + (size_t)r * dv);",
+                                  "orc_dequantise_row(dv, row, s, T + (size_t)r * dv);")],
+    "fused_replay_first_decayed_twice": [
+        ("&k_one, 0,\n                                  beta[bt * Hv + h]",
+         "ap, 1,\n                                  beta[bt * Hv + h]")],
+    "damp_fused_group_decay_dropped": [
+        ("orc_dequantise_row(group, row + gi * group, s * a[r], T + (size_t)r * dv + gi * group);",
+         "orc_dequantise_row(group, row + gi * group, s, T + (size_t)r * dv + gi * group);")],
     "replay_skips_first": [("for (t = 0; t < n; ++t) {", "for (t = 1; t < n; ++t) {")],
     "int8_scale_per_unit": [
         ("memcpy(ckpt + (size_t)d * sb + (size_t)cb + (size_t)row * 4, &sc, 4);",
