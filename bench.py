@@ -362,6 +362,7 @@ def _time(torch, fn, iters, warm=3):
 
 
 EXTRA = ("gdn_fp32", "kda_fp32", "kda_mixed", "gdn_mixed", "kda_damp", "replay_mixed", "replay_fp32",
+         "kda_mixed_fused", "gdn_mixed_fused", "kda_damp_fused", "replay_mixed_fused",
          "pack_gdn", "restore_gdn", "pack_kda", "restore_kda", "pack_int8_gdn", "restore_int8_gdn",
          "pack_int8_kda", "restore_int8_kda", "pack_mixed", "restore_mixed")
 
@@ -404,7 +405,9 @@ def extra_kernels(args, rs, torch, dev, peak, world, only=None):
         del pool, q, k, v
         torch.cuda.empty_cache()
     KDA_B = dict(KDA, B=B)
-    if want & {"kda_fp32", "kda_mixed", "gdn_mixed", "kda_damp", "replay_mixed", "replay_fp32"}:
+    MIXED_KEYS = {"kda_fp32", "kda_mixed", "gdn_mixed", "kda_damp", "replay_mixed", "replay_fp32",
+                  "kda_mixed_fused", "gdn_mixed_fused", "kda_damp_fused", "replay_mixed_fused"}
+    if want & MIXED_KEYS:
         nsteps = 8
         w = gen.decode_workload(steps=nsteps, per_channel=True, in_dtype="bf16", seed=1,
                                 horizon=(2.0, 8192.0), **KDA_B)
@@ -415,6 +418,8 @@ def extra_kernels(args, rs, torch, dev, peak, world, only=None):
         f32 = rs.Layout("fp32", 128, KDA["Hv"], KDA["Hk"])
         hi = gen.hi_rows(KDA["Hv"], 128, 16, seed=1)
         mix = rs.Layout("mixed", 128, KDA["Hv"], KDA["Hk"], k_hi=16, hi_rows=hi)
+        # the same pool format with the fused requantisation arithmetic
+        mixf = rs.Layout("mixed", 128, KDA["Hv"], KDA["Hk"], k_hi=16, hi_rows=hi, quant="fused")
         pool = to_dev(w.state0)
         mpool = mix.empty_pool(B, device=dev)
         rs.state_convert(f32, pool, mix, mpool, torch.arange(B, dtype=torch.int32, device=dev))
@@ -430,26 +435,42 @@ def extra_kernels(args, rs, torch, dev, peak, world, only=None):
                 be[i % nsteps], o=o), iters, warm)
             rec(f"kda_decode_mixed_b{B}", sec, decode_bytes(B, 32, 32, 128, mix.head_bytes, 2, True),
                 B * 32)
+        if "kda_mixed_fused" in want:
+            sec = _time(torch, lambda i: rs.kda_decode_update(
+                mixf, mpool, slots, q[i % nsteps], k[i % nsteps], v[i % nsteps], al[i % nsteps],
+                be[i % nsteps], o=o), iters, warm)
+            rec(f"kda_decode_mixed_fused_b{B}", sec, decode_bytes(B, 32, 32, 128, mix.head_bytes, 2, True),
+                B * 32, {"quant": "fused"})
+        al_g = al[..., 0].contiguous()  # one decay per (sequence, head) for the GDN form
         if "gdn_mixed" in want:
-            al_g = al[..., 0].contiguous()  # one decay per (sequence, head) for the GDN form
             sec = _time(torch, lambda i: rs.gdn_decode_update(
                 mix, mpool, slots, q[i % nsteps], k[i % nsteps], v[i % nsteps], al_g[i % nsteps],
                 be[i % nsteps], o=o), iters, warm)
             rec(f"gdn_decode_mixed_b{B}_h32", sec,
                 decode_bytes(B, 32, 32, 128, mix.head_bytes, 2, False), B * 32)
-        if "kda_damp" in want:
+        if "gdn_mixed_fused" in want:
+            sec = _time(torch, lambda i: rs.gdn_decode_update(
+                mixf, mpool, slots, q[i % nsteps], k[i % nsteps], v[i % nsteps], al_g[i % nsteps],
+                be[i % nsteps], o=o), iters, warm)
+            rec(f"gdn_decode_mixed_fused_b{B}_h32", sec,
+                decode_bytes(B, 32, 32, 128, mix.head_bytes, 2, False), B * 32, {"quant": "fused"})
+        for dkey, quant in (("kda_damp", "ieee"), ("kda_damp_fused", "fused")):
+            if dkey not in want:
+                continue
             # DAMP-exact storage: INT8 groups of 32 along dv, value scaling
             damp = rs.Layout("damp", 128, KDA["Hv"], KDA["Hk"], k_hi=16, hi_rows=hi,
-                             value_scales=gen.value_scales(KDA["Hv"], 128, seed=1))
+                             value_scales=gen.value_scales(KDA["Hv"], 128, seed=1), quant=quant)
             dpool = damp.empty_pool(B, device=dev)
             rs.state_convert(f32, pool, damp, dpool, torch.arange(B, dtype=torch.int32, device=dev))
             sec = _time(torch, lambda i: rs.kda_decode_update(
                 damp, dpool, slots, q[i % nsteps], k[i % nsteps], v[i % nsteps], al[i % nsteps],
                 be[i % nsteps], o=o), iters, warm)
-            rec(f"kda_decode_damp_g32_b{B}", sec, decode_bytes(B, 32, 32, 128, damp.head_bytes, 2, True),
-                B * 32, {"bits_per_value": damp.bits_per_value()})
+            suffix = "_fused" if quant == "fused" else ""
+            rec(f"kda_decode_damp_g32{suffix}_b{B}", sec,
+                decode_bytes(B, 32, 32, 128, damp.head_bytes, 2, True), B * 32,
+                {"bits_per_value": damp.bits_per_value(), "quant": quant})
             del dpool
-        if want & {"replay_mixed", "replay_fp32"}:
+        if want & {"replay_mixed", "replay_fp32", "replay_mixed_fused"}:
             T = 8
             n_acc = gen.n_accept(B, T, seed=1)
             tok = int(n_acc.sum())
@@ -466,6 +487,11 @@ def extra_kernels(args, rs, torch, dev, peak, world, only=None):
                     mix, True, mpool, slots, nd, rq, rk, rv, ra, rb, o=ro), iters, warm)
                 rec(f"kda_replay_mixed_b{B}_T8", sec, 2 * B * 32 * mix.head_bytes + tok * per_tok,
                     tok * 32, {"accepted_tokens": tok, "n_accept": "uniform 1..8"})
+            if "replay_mixed_fused" in want:
+                sec = _time(torch, lambda i: rs.spec_replay_update(
+                    mixf, True, mpool, slots, nd, rq, rk, rv, ra, rb, o=ro), iters, warm)
+                rec(f"kda_replay_mixed_fused_b{B}_T8", sec, 2 * B * 32 * mix.head_bytes + tok * per_tok,
+                    tok * 32, {"accepted_tokens": tok, "n_accept": "uniform 1..8", "quant": "fused"})
             if "replay_fp32" in want:
                 sec = _time(torch, lambda i: rs.spec_replay_update(
                     f32, True, pool, slots, nd, rq, rk, rv, ra, rb, o=ro), iters, warm)

@@ -109,6 +109,9 @@ typedef int32_t rs_status;
 #define RS_BF16  1
 #define RS_F16   2
 
+#define RS_QUANT_IEEE    0   /* mixed layouts: IEEE quotient (default)     */
+#define RS_QUANT_FUSED   1   /* mixed layouts: division-free arithmetic    */
+
 #define RS_UNIT_HEAD     0   /* GDN checkpoint unit: one head state        */
 #define RS_UNIT_CHANNEL  1   /* KDA checkpoint unit: one key-channel row   */
 
@@ -163,6 +166,29 @@ rs_status rs_layout_create(rs_layout **out, const rs_layout_params *p,
 rs_status rs_layout_create_damp(rs_layout **out, const rs_layout_params *p, const int16_t *hi_rows,
                                 int32_t group, const float *value_scales);
 rs_status rs_layout_destroy(rs_layout *l);
+
+/* Requantisation arithmetic of a mixed layout (either kind of
+ * rs_layout_create or rs_layout_create_damp).  The pages fix the quantiser
+ * (s = max(a, 1e-8)/127, code = round(x/s) clipped to +-127, FP32: [DAMP]
+ * §3.2 Eq. 5-6, [dasc] Appendix E.1 Eq. 8) and the fused step ([DAMP]
+ * Appendix A.4: dequantise, decay and update in FP32, requantise), not how
+ * x/s is evaluated or where the decay's rounding falls.
+ *   RS_QUANT_IEEE  (default) code = clip(round_half_even(x/s)) with the IEEE
+ *                  FP32 quotient; a step decays the dequantised value,
+ *                  RN(RN(c*s) * a).
+ *   RS_QUANT_FUSED the code is the integer nearest to the exact product
+ *                  x * RN(1/s), ties to even (rows or groups whose absmax is
+ *                  inf or NaN keep the IEEE quotient); a step decays an INT8
+ *                  row through its scale, c * RN(s * a_u) (diag(a) diag(s) C
+ *                  = diag(a s) C).  FP16 rows are as in RS_QUANT_IEEE.
+ * The two agree on every scale and every FP16 value given the same FP32
+ * state; a code may differ by one where x/s lies within about 2^-23 |x/s|
+ * of a half-integer.  The stored format is the same: a pool may be used
+ * with either mode.  The mode applies to decode, replay and FP32 -> mixed
+ * conversion.  RS_ERR_INVALID_ARG for an unknown mode or RS_QUANT_FUSED on
+ * an FP32 layout. */
+rs_status rs_layout_set_quant(rs_layout *l, int32_t mode);
+rs_status rs_layout_quant(const rs_layout *l, int32_t *mode);
 
 /* Bytes of one head state in this layout (65,536 or 18,880 at d = 128). */
 rs_status rs_layout_head_bytes(const rs_layout *l, size_t *bytes);

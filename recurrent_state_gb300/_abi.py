@@ -27,12 +27,13 @@ RS_LAYOUT_MIXED_FP16_INT8 = 1
 RS_F32, RS_BF16, RS_F16 = 0, 1, 2
 RS_UNIT_HEAD, RS_UNIT_CHANNEL = 0, 1
 RS_GATE_STD, RS_GATE_K3 = 0, 1
+RS_QUANT_IEEE, RS_QUANT_FUSED = 0, 1
 
 # Every function the header declares, for the symbol-table test.
 EXPORTS = (
     "rs_status_string", "rs_last_cuda_error", "rs_version",
     "rs_layout_create", "rs_layout_create_damp", "rs_layout_destroy", "rs_layout_head_bytes", "rs_layout_row_map",
-    "rs_layout_bits_per_value",
+    "rs_layout_bits_per_value", "rs_layout_set_quant", "rs_layout_quant",
     "rs_gdn_decode_update", "rs_kda_decode_update", "rs_spec_replay_update", "rs_state_convert",
     "rs_plan_create", "rs_plan_destroy", "rs_plan_offsets", "rs_plan_upload",
     "rs_ckpt_pack", "rs_ckpt_restore", "rs_ckpt_pack_noalloc",
@@ -92,6 +93,8 @@ def _declare(L):
     L.rs_layout_head_bytes.argtypes = [_P, ctypes.POINTER(ctypes.c_size_t)]
     L.rs_layout_row_map.argtypes = [_P, _P]
     L.rs_layout_bits_per_value.argtypes = [_P, ctypes.POINTER(ctypes.c_double)]
+    L.rs_layout_set_quant.argtypes = [_P, _I32]
+    L.rs_layout_quant.argtypes = [_P, ctypes.POINTER(_I32)]
     step = [_P, _P, _I64, _P, _I32, _P, _P, _P, _I32, _P, _P, _P, _I32, _P, _P]
     L.rs_gdn_decode_update.argtypes = step
     L.rs_kda_decode_update.argtypes = step

@@ -44,10 +44,12 @@ class Layout:
 
     def __init__(self, kind: str, dk: int, num_v_heads: int, num_qk_heads: int,
                  k_hi: int = 0, hi_rows=None, dv: int | None = None, group: int = 32,
-                 value_scales=None):
+                 value_scales=None, quant: str = "ieee"):
         """kind: "fp32", "mixed" (one INT8 scale per row) or "damp" (DAMP-exact:
         INT8 groups of ``group`` values along dv and value-scaling factors
-        ``value_scales`` [Hv][dv], default all ones)."""
+        ``value_scales`` [Hv][dv], default all ones).  quant: the requantisation
+        arithmetic of a mixed layout, "ieee" (RS_QUANT_IEEE) or "fused"
+        (RS_QUANT_FUSED)."""
         self.kind = {"fp32": _abi.RS_LAYOUT_FP32, "mixed": _abi.RS_LAYOUT_MIXED_FP16_INT8,
                      "damp": _abi.RS_LAYOUT_MIXED_FP16_INT8}[kind]
         self.kind_name = kind
@@ -73,6 +75,10 @@ class Layout:
             check(_abi.lib().rs_layout_create(ctypes.byref(h), ctypes.byref(p),
                                               None if hr is None else hr.ctypes.data), "rs_layout_create")
         self._h = h
+        self.quant = quant
+        check(_abi.lib().rs_layout_set_quant(h, {"ieee": _abi.RS_QUANT_IEEE,
+                                                  "fused": _abi.RS_QUANT_FUSED}[quant]),
+              "rs_layout_set_quant")
         nb = ctypes.c_size_t()
         check(_abi.lib().rs_layout_head_bytes(h, ctypes.byref(nb)))
         self.head_bytes = int(nb.value)

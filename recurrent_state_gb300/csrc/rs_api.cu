@@ -24,6 +24,7 @@ struct rs_layout {
     size_t head_bytes;
     int32_t group = 0;        // DAMP-exact layout: values per INT8 scale group (0: one scale per row)
     std::vector<float> cs;    // DAMP-exact layout: value-scaling factors [Hv][dv]
+    int32_t quant = RS_QUANT_IEEE;  // requantisation arithmetic of a mixed layout
 };
 
 
@@ -167,6 +168,19 @@ rs_status rs_layout_create_damp(rs_layout **out, const rs_layout_params *p, cons
     return RS_OK;
 }
 
+rs_status rs_layout_set_quant(rs_layout *l, int32_t mode) {
+    if (!l || (mode != RS_QUANT_IEEE && mode != RS_QUANT_FUSED)) return RS_ERR_INVALID_ARG;
+    if (l->p.kind == RS_LAYOUT_FP32 && mode != RS_QUANT_IEEE) return RS_ERR_INVALID_ARG;
+    l->quant = mode;
+    return RS_OK;
+}
+
+rs_status rs_layout_quant(const rs_layout *l, int32_t *mode) {
+    if (!l || !mode) return RS_ERR_INVALID_ARG;
+    *mode = l->quant;
+    return RS_OK;
+}
+
 rs_status rs_layout_destroy(rs_layout *l) {
     delete l;
     return RS_OK;
@@ -219,6 +233,7 @@ static rs_status step_common(const rs_layout *l, bool kda, bool replay, void *po
     L.kda = kda;
     L.in_dt = in_dtype;
     L.out_dt = out_dtype;
+    L.fused = l->p.kind != RS_LAYOUT_FP32 && l->quant == RS_QUANT_FUSED;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     auto fill = [&](rs::StepParams &P) {
@@ -325,6 +340,7 @@ rs_status rs_state_convert(const rs_layout *src_l, const void *src_pool, const r
             P.n = n;
             P.Hv = a.num_v_heads;
             P.to_mixed = b.kind == RS_LAYOUT_MIXED_FP16_INT8 ? 1 : 0;
+            P.fused = mixed->quant == RS_QUANT_FUSED ? 1 : 0;
             for (size_t i = 0; i < mixed->pi.size(); ++i) P.pi[i] = (uint8_t)mixed->pi[i];
             std::copy(mixed->cs.begin(), mixed->cs.end(), P.cs);
             e = rs::launch_convert_damp(a.dk, mixed->p.k_hi, P, s);
@@ -340,6 +356,7 @@ rs_status rs_state_convert(const rs_layout *src_l, const void *src_pool, const r
         P.n = n;
         P.Hv = a.num_v_heads;
         P.to_mixed = b.kind == RS_LAYOUT_MIXED_FP16_INT8 ? 1 : 0;
+        P.fused = mixed->quant == RS_QUANT_FUSED ? 1 : 0;
         for (size_t i = 0; i < mixed->pi.size(); ++i) P.pi[i] = (uint8_t)mixed->pi[i];
         e = rs::launch_convert(a.dk, mixed->p.k_hi, P, s);
     }

@@ -3,7 +3,8 @@
 //
 // One CTA of D threads per (slot, head) tile; thread v owns column v.
 // FP32 -> mixed: physical row r of the mixed tile takes logical key channel
-// pi[r]; the rows are requantised by the same routine as the decode kernel.
+// pi[r]; the rows are requantised by the same routine as the replay kernel,
+// in the IEEE or the fused arithmetic of the destination layout.
 // Mixed -> FP32: dequantise and write each physical row back to its logical
 // channel.  Used to initialise and inspect mixed pools, not on the decode path.
 #include "rs_step.cuh"
@@ -13,7 +14,7 @@ namespace rs {
 
 namespace {
 
-template <int D, int KH>
+template <int D, int KH, bool FUSED>
 __global__ void __launch_bounds__(D) convert_kernel(const __grid_constant__ ConvertParamsPi P) {
     constexpr int kMixedBytes = 2 * KH * D + (D - KH) * D + 4 * (D - KH);
     __shared__ float red[(D / 32) * D];
@@ -40,7 +41,7 @@ __global__ void __launch_bounds__(D) convert_kernel(const __grid_constant__ Conv
 #pragma unroll
         for (int j = 0; j < D / 2; ++j)
             x[j] = make_float2(src[(int)pi_s[2 * j] * D + tid], src[(int)pi_s[2 * j + 1] * D + tid]);
-        mixed_requant_smem<D, KH>(x, out, red, scl, nscl, rcp, &flag, tid, lane, wig, 0, [] {});
+        mixed_requant_smem<D, KH, FUSED>(x, out, red, scl, nscl, rcp, &flag, tid, lane, wig, 0, [] {});
         __syncthreads();
         uint4 *dst4 = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(P.dst) + tile * kMixedBytes);
         const uint4 *src4 = reinterpret_cast<const uint4 *>(out);
@@ -78,7 +79,8 @@ cudaError_t launch_convert(int D, int khi, ConvertParamsPi &P, cudaStream_t s) {
     if (P.n == 0) return cudaSuccess;
     const unsigned grid = (unsigned)P.n * (unsigned)P.Hv;
     if (D == 128 && khi == 16) {
-        convert_kernel<128, 16><<<grid, 128, 0, s>>>(P);
+        if (P.fused) convert_kernel<128, 16, true><<<grid, 128, 0, s>>>(P);
+        else convert_kernel<128, 16, false><<<grid, 128, 0, s>>>(P);
         return cudaGetLastError();
     }
     return cudaErrorNotSupported;

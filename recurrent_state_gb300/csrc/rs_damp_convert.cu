@@ -3,7 +3,9 @@
 // key channel pi[r], each value is divided by its value-scaling factor c'_v,
 // FP16 rows round to nearest even and INT8 rows are quantised in groups of 32
 // values (one warp per group: the absmax is one warp max-reduction) with the
-// literal IEEE quotient.  DAMP -> FP32: dequantise, multiply by c'_v, write the
+// literal IEEE quotient, or with the fused arithmetic's one-rounding product
+// x * RN(1/s) when the destination layout asks for it (groups whose absmax is
+// inf or NaN keep the quotient).  DAMP -> FP32: dequantise, multiply by c'_v, write the
 // logical row.  One CTA of D threads per (slot, head), thread v on column v.
 // Used to initialise and inspect pools, not on the decode path.
 #include "rs_damp.h"
@@ -14,7 +16,7 @@ namespace rs {
 
 namespace {
 
-template <int D, int KH>
+template <int D, int KH, bool FUSED>
 __global__ void __launch_bounds__(D) damp_convert_kernel(const __grid_constant__ ConvertParamsDamp P) {
     constexpr int NG = D / kDampGroup;
     constexpr int kBytes = 2 * KH * D + (D - KH) * D + 4 * (D - KH) * NG;
@@ -45,7 +47,10 @@ __global__ void __launch_bounds__(D) damp_convert_kernel(const __grid_constant__
                 const int q = r - KH;
                 const float a = warp_max_abs_nan(x);  // one group = one warp
                 const float s = __fdiv_rn(fmaxf(a, 1e-8f), 127.0f);
-                lo[((q / 4) * D + tid) * 4 + (q % 4)] = (uint8_t)quant_exact(x, s);
+                uint32_t code;
+                if constexpr (FUSED) code = quant_rcp_or_exact(x, s, a <= 3.402823466e38f ? __frcp_rn(s) : 0.0f);
+                else code = quant_exact(x, s);
+                lo[((q / 4) * D + tid) * 4 + (q % 4)] = (uint8_t)code;
                 if (lane == 0) sc[q * NG + grp] = s;
             }
         }
@@ -78,8 +83,12 @@ __global__ void __launch_bounds__(D) damp_convert_kernel(const __grid_constant__
 cudaError_t launch_convert_damp(int D, int khi, ConvertParamsDamp &P, cudaStream_t s) {
     if (P.n == 0) return cudaSuccess;
     const unsigned grid = (unsigned)P.n * (unsigned)P.Hv;
-    if (D == 128 && khi == 16) damp_convert_kernel<128, 16><<<grid, 128, 0, s>>>(P);
-    else return cudaErrorNotSupported;
+    if (D == 128 && khi == 16) {
+        if (P.fused) damp_convert_kernel<128, 16, true><<<grid, 128, 0, s>>>(P);
+        else damp_convert_kernel<128, 16, false><<<grid, 128, 0, s>>>(P);
+    } else {
+        return cudaErrorNotSupported;
+    }
     return cudaGetLastError();
 }
 

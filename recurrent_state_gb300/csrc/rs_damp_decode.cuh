@@ -11,6 +11,11 @@
 // c'_v enter as v' = v / c' before the prediction error and o = c' o' after
 // the readout chain.  Every value is computed with the same operations in the
 // same order as the oracle's transformed step.
+// Fused arithmetic (FUSED): when the row vectors are built, each INT8 row's
+// group scales in the stage are multiplied by the row's decay in place
+// (RN(s_g a_u); the tile's new scales overwrite them in pass 2), so the
+// passes dequantise with c * RN(s_g a_u) and no decay multiply; each new code
+// is one fused multiply-add, the integer nearest to x * RN(1/s).
 #pragma once
 
 #include "rs_damp.h"
@@ -34,7 +39,7 @@ struct DampShape {
     static constexpr int kHeader = 256;
 };
 
-template <int D, int KH, bool KDA, typename TI, typename TO>
+template <int D, int KH, bool KDA, typename TI, typename TO, bool FUSED>
 __global__ void __launch_bounds__(512, 1) damp_decode_kernel(const __grid_constant__ StepParamsDamp P) {
     using S = DampShape<D, KH, KDA, TI>;
     constexpr int WPT = 2;
@@ -160,7 +165,17 @@ __global__ void __launch_bounds__(512, 1) damp_decode_kernel(const __grid_consta
                 wv[2 * tt + i] = kf;
                 wv[D + 2 * tt + i] = __fmul_rn(beta0, kf);
                 wv[2 * D + 2 * tt + i] = load_as_f32<TI>(reinterpret_cast<const TI *>(tb + S::kVecBytes) + src);
-                if (KDA) wv[3 * D + 2 * tt + i] = reinterpret_cast<const float *>(tb + 3 * S::kVecBytes)[src];
+                const float ar = KDA ? reinterpret_cast<const float *>(tb + 3 * S::kVecBytes)[src] : alpha0;
+                if (KDA) wv[3 * D + 2 * tt + i] = ar;
+                if constexpr (FUSED) {  // decay folded into the row's group scales
+                    const int r = 2 * tt + i;
+                    if (r >= KH) {
+                        float4 *g4 = reinterpret_cast<float4 *>(st + 2 * KH * D + (D - KH) * D) + (r - KH);
+                        const float4 sg = *g4;
+                        *g4 = make_float4(__fmul_rn(sg.x, ar), __fmul_rn(sg.y, ar), __fmul_rn(sg.z, ar),
+                                          __fmul_rn(sg.w, ar));
+                    }
+                }
             }
         }
         // value-scaling factors of this lane's columns; v' = v / c'
@@ -206,7 +221,7 @@ __global__ void __launch_bounds__(512, 1) damp_decode_kernel(const __grid_consta
                 const float fb = __uint_as_float(__byte_perm(wb, 0x4B000000u, sel));
                 x[i] = __fmul2_rn(__fadd2_rn(make_float2(fa, fb), nb), s2);
             }
-            decay(KH / 4 + qd, x);
+            if constexpr (!FUSED) decay(KH / 4 + qd, x);
         };
         auto predict = [&](int q, const float2 (&x)[4], float2 &p) {
             const float4 k4 = K4[q];
@@ -293,10 +308,12 @@ __global__ void __launch_bounds__(512, 1) damp_decode_kernel(const __grid_consta
                 const float sa = row_scale_from_absmax(ma), sb = row_scale_from_absmax(mb);
                 nsc[lane] = -sa;
                 nsc[S::kBlock + lane] = -sb;
-                nsc[2 * S::kBlock + lane] = __frcp_rn(sa);
-                nsc[3 * S::kBlock + lane] = __frcp_rn(sb);
+                const bool bad_a = !(ma <= 3.402823466e38f), bad_b = !(mb <= 3.402823466e38f);
+                // fused arithmetic: y = 0 marks a group whose absmax is inf or NaN
+                nsc[2 * S::kBlock + lane] = (FUSED && bad_a) ? 0.0f : __frcp_rn(sa);
+                nsc[3 * S::kBlock + lane] = (FUSED && bad_b) ? 0.0f : __frcp_rn(sb);
                 *reinterpret_cast<float2 *>(scales + (blk * S::kBlock + lane) * NG + 2 * wt) = make_float2(sa, sb);
-                nonfinite = !(ma <= 3.402823466e38f) || !(mb <= 3.402823466e38f);
+                nonfinite = bad_a || bad_b;
             }
             __syncwarp();
             nonfinite = __any_sync(0xffffffffu, nonfinite);
@@ -314,11 +331,16 @@ __global__ void __launch_bounds__(512, 1) damp_decode_kernel(const __grid_consta
                     for (int i = 0; i < 4; ++i) {
                         const float2 x = X[qq][i];
                         const float2 y = make_float2(ya[i], yb[i]);
-                        const float2 n = make_float2(na[i], nbv[i]);
-                        float2 t = __fmul2_rn(x, y);
-                        t = __ffma2_rn(__ffma2_rn(t, n, x), y, t);
-                        t = __ffma2_rn(__ffma2_rn(t, n, x), y, t);
-                        t = __fadd2_rn(t, make_float2(kRound, kRound));
+                        float2 t;
+                        if constexpr (FUSED) {  // integer nearest to x y, rounded once
+                            t = __ffma2_rn(x, y, make_float2(kRound, kRound));
+                        } else {                // RN(x / s), then rounded to an integer
+                            const float2 n = make_float2(na[i], nbv[i]);
+                            t = __fmul2_rn(x, y);
+                            t = __ffma2_rn(__ffma2_rn(t, n, x), y, t);
+                            t = __ffma2_rn(__ffma2_rn(t, n, x), y, t);
+                            t = __fadd2_rn(t, make_float2(kRound, kRound));
+                        }
                         mA[i] = __float_as_uint(t.x);
                         mB[i] = __float_as_uint(t.y);
                     }
@@ -333,8 +355,14 @@ __global__ void __launch_bounds__(512, 1) damp_decode_kernel(const __grid_consta
                     uint32_t wa = 0, wb = 0;
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        wa |= quant_exact(X[qq][i].x, -nsc[4 * qq + i]) << (8 * i);
-                        wb |= quant_exact(X[qq][i].y, -nsc[S::kBlock + 4 * qq + i]) << (8 * i);
+                        const float s_a = -nsc[4 * qq + i], s_b = -nsc[S::kBlock + 4 * qq + i];
+                        if constexpr (FUSED) {
+                            wa |= quant_rcp_or_exact(X[qq][i].x, s_a, nsc[2 * S::kBlock + 4 * qq + i]) << (8 * i);
+                            wb |= quant_rcp_or_exact(X[qq][i].y, s_b, nsc[3 * S::kBlock + 4 * qq + i]) << (8 * i);
+                        } else {
+                            wa |= quant_exact(X[qq][i].x, s_a) << (8 * i);
+                            wb |= quant_exact(X[qq][i].y, s_b) << (8 * i);
+                        }
                     }
                     low[(q0 + qq) * D + cA] = wa;
                     low[(q0 + qq) * D + cB] = wb;

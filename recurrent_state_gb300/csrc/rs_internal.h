@@ -61,6 +61,7 @@ struct StepLaunch {
     bool kda;
     int in_dt;      // RS_F32 / RS_BF16 / RS_F16
     int out_dt;     // RS_F32 / RS_BF16
+    bool fused;     // mixed layouts: RS_QUANT_FUSED arithmetic
 };
 
 // Defined in rs_step_*.cu (one translation unit each, compiled in parallel).
@@ -79,6 +80,7 @@ struct ConvertParams {
     int32_t *status;
     int32_t n, Hv;
     int32_t to_mixed;          // 1: FP32 -> mixed, 0: mixed -> FP32
+    int32_t fused;             // FP32 -> mixed: RS_QUANT_FUSED codes
 };
 struct ConvertParamsPi : ConvertParams {
     uint8_t pi[kMaxRowMap];

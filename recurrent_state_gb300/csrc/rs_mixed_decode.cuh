@@ -22,6 +22,10 @@
 // blocks of 16 rows (FP16 rows round to nearest even; INT8 rows get a new
 // scale from the block's absmax and an exact RN(x/s) code, as in
 // rs_step.cuh).  One thread then bulk-stores the tile.
+// With the fused arithmetic (FUSED) the decay of INT8 row u is applied to
+// its scale when the row vectors are built (RN(s_u a_u), so dequantising is
+// c * RN(s_u a_u) and needs no decay multiply), and each new code is one
+// fused multiply-add, the integer nearest to x * RN(1/s).
 //
 // A CTA runs P = W / WPT tile slots over a ring of NS > P stages.  Its tiles
 // are numbered j = 0, 1, ... (tile blockIdx.x + j * gridDim.x of the
@@ -40,7 +44,7 @@ namespace rs {
 
 constexpr int kMixedMaxStages = 16;  // stage ring length limit (mbarriers in the header)
 
-template <int D, int KH, bool KDA, typename TI, int WPT>
+template <int D, int KH, bool KDA, typename TI, int WPT, bool FUSED = false>
 struct MixedWarpShape {
     static constexpr int kCols = D / (32 * WPT);  // columns per lane
     static constexpr int kStateBytes = 2 * KH * D + (D - KH) * D + 4 * (D - KH);
@@ -48,7 +52,9 @@ struct MixedWarpShape {
     static constexpr int kVecBytes = D * (int)sizeof(TI);
     static constexpr int kTokBytes = 3 * kVecBytes + (KDA ? D * 4 : 0);  // k, q, v (+ alpha)
     static constexpr int kStage = (kStatePad + kTokBytes + 127) / 128 * 128;
-    static constexpr int kRowVecs = KDA ? 4 : 3;  // K, BK, Q (+ A), floats in row order
+    // K, BK, Q (+ A: the decay of each row; fused: RN(s_u a_u) for INT8 rows),
+    // floats in row order
+    static constexpr int kRowVecs = (KDA || FUSED) ? 4 : 3;
     static constexpr int kBlock = 16;             // rows per requantisation block
     // per tile slot: row vectors, partial row maxima [2][WPT][kBlock], and
     // per warp -s and 1/s of the current block
@@ -109,8 +115,12 @@ template <int CPL> struct Quad {
 // INT8 words of a lane's columns for rows 4q..4q+3 with scales s, by the
 // literal IEEE division: the path of blocks whose absmax is not finite.  Out
 // of line, so that the common path carries a call and nothing else of it.
-template <int CPL> __device__ __noinline__ void quant_rows_exact(Quad<CPL> X, float4 s, uint32_t *dst) {
+// Fused arithmetic: rows with a finite absmax (reciprocal y != 0) keep the
+// one-rounding product code, the others take the IEEE quotient.
+template <int CPL, bool FUSED>
+__device__ __noinline__ void quant_rows_exact(Quad<CPL> X, float4 s, float4 y, uint32_t *dst) {
     const float sr[4] = {s.x, s.y, s.z, s.w};
+    const float yr[4] = {y.x, y.y, y.z, y.w};
     uint32_t wd[CPL];
 #pragma unroll
     for (int t = 0; t < CPL; ++t) wd[t] = 0u;
@@ -118,16 +128,21 @@ template <int CPL> __device__ __noinline__ void quant_rows_exact(Quad<CPL> X, fl
     for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int k = 0; k < CPL / 2; ++k) {
-            wd[2 * k] |= quant_exact(X.x[i][k].x, sr[i]) << (8 * i);
-            wd[2 * k + 1] |= quant_exact(X.x[i][k].y, sr[i]) << (8 * i);
+            if constexpr (FUSED) {
+                wd[2 * k] |= quant_rcp_or_exact(X.x[i][k].x, sr[i], yr[i]) << (8 * i);
+                wd[2 * k + 1] |= quant_rcp_or_exact(X.x[i][k].y, sr[i], yr[i]) << (8 * i);
+            } else {
+                wd[2 * k] |= quant_exact(X.x[i][k].x, sr[i]) << (8 * i);
+                wd[2 * k + 1] |= quant_exact(X.x[i][k].y, sr[i]) << (8 * i);
+            }
         }
     sts_words<CPL>(dst, wd);
 }
 
-template <int D, int KH, bool KDA, typename TI, typename TO, int WPT>
+template <int D, int KH, bool KDA, typename TI, typename TO, int WPT, bool FUSED>
 __global__ void __launch_bounds__(256 * WPT, 1)
     mixed_decode_kernel(const __grid_constant__ StepParamsPi P) {
-    using S = MixedWarpShape<D, KH, KDA, TI, WPT>;
+    using S = MixedWarpShape<D, KH, KDA, TI, WPT, FUSED>;
     constexpr int CPL = S::kCols;
     constexpr int NP = CPL / 2;  // column pairs per lane
     static_assert(CPL == 2 || CPL == 4, "two or four columns per lane");
@@ -266,7 +281,14 @@ __global__ void __launch_bounds__(256 * WPT, 1)
                 wv[c0 + i] = kf;
                 wv[D + c0 + i] = __fmul_rn(beta0, kf);
                 wv[2 * D + c0 + i] = load_as_f32<TI>(reinterpret_cast<const TI *>(tb + S::kVecBytes) + src);
-                if (KDA) wv[3 * D + c0 + i] = reinterpret_cast<const float *>(tb + 3 * S::kVecBytes)[src];
+                if constexpr (FUSED) {
+                    const float ar = KDA ? reinterpret_cast<const float *>(tb + 3 * S::kVecBytes)[src] : alpha0;
+                    const int r = c0 + i;
+                    const float *scl = reinterpret_cast<const float *>(st + 2 * KH * D + (D - KH) * D);
+                    wv[3 * D + r] = r < KH ? ar : __fmul_rn(scl[r - KH], ar);
+                } else if (KDA) {
+                    wv[3 * D + c0 + i] = reinterpret_cast<const float *>(tb + 3 * S::kVecBytes)[src];
+                }
             }
         }
         float vv[CPL];
@@ -285,7 +307,7 @@ __global__ void __launch_bounds__(256 * WPT, 1)
         const float4 *sc4 = reinterpret_cast<const float4 *>(scales);
 
         auto decay = [&](int q, Quad<CPL> &X) {  // rows 4q..4q+3 times their decay
-            const float4 a = KDA ? A4[q] : make_float4(alpha0, alpha0, alpha0, alpha0);
+            const float4 a = (KDA || FUSED) ? A4[q] : make_float4(alpha0, alpha0, alpha0, alpha0);
             const float ar[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i)
@@ -312,7 +334,8 @@ __global__ void __launch_bounds__(256 * WPT, 1)
             lds_words<CPL>(low + qd * D + c0, wd);
 #pragma unroll
             for (int t = 0; t < CPL; ++t) wd[t] ^= 0x80808080u;
-            const float4 s4 = sc4[qd];
+            // fused: the decayed scales RN(s a) of the row vectors; otherwise the stored scales
+            const float4 s4 = FUSED ? A4[KH / 4 + qd] : sc4[qd];
             const float sr[4] = {s4.x, s4.y, s4.z, s4.w};
             const float2 nb = make_float2(-kCodeBias, -kCodeBias);
 #pragma unroll
@@ -325,7 +348,7 @@ __global__ void __launch_bounds__(256 * WPT, 1)
                     X.x[i][k] = __fmul2_rn(__fadd2_rn(make_float2(fa, fb), nb), make_float2(sr[i], sr[i]));
                 }
             }
-            decay(KH / 4 + qd, X);
+            if constexpr (!FUSED) decay(KH / 4 + qd, X);
         };
         auto predict = [&](int q, const Quad<CPL> &X, float2 (&p)[NP]) {
             const float4 k4 = K4[q];
@@ -435,10 +458,11 @@ __global__ void __launch_bounds__(256 * WPT, 1)
             bool nonfinite = false;
             if (lane < S::kBlock) {
                 const float sv = div127(fmaxf(mine, 1e-8f));
-                nsc[lane] = -sv;
-                nsc[S::kBlock + lane] = __frcp_rn(sv);
-                if (wt == 0) scales[blk * S::kBlock + lane] = sv;
                 nonfinite = !(mine <= 3.402823466e38f);  // absmax inf or NaN
+                nsc[lane] = -sv;
+                // fused arithmetic: y = 0 marks a row whose absmax is inf or NaN
+                nsc[S::kBlock + lane] = (FUSED && nonfinite) ? 0.0f : __frcp_rn(sv);
+                if (wt == 0) scales[blk * S::kBlock + lane] = sv;
             }
             __syncwarp();
             nonfinite = __any_sync(0xffffffffu, nonfinite);
@@ -456,11 +480,16 @@ __global__ void __launch_bounds__(256 * WPT, 1)
                         for (int k = 0; k < NP; ++k) {
                             const float2 x = X[qq].x[i][k];
                             const float2 y = make_float2(yr[i], yr[i]);
-                            const float2 n = make_float2(nr[i], nr[i]);
-                            float2 t = __fmul2_rn(x, y);
-                            t = __ffma2_rn(__ffma2_rn(t, n, x), y, t);
-                            t = __ffma2_rn(__ffma2_rn(t, n, x), y, t);
-                            t = __fadd2_rn(t, make_float2(kRound, kRound));
+                            float2 t;
+                            if constexpr (FUSED) {  // integer nearest to x y, rounded once
+                                t = __ffma2_rn(x, y, make_float2(kRound, kRound));
+                            } else {                // RN(x / s), then rounded to an integer
+                                const float2 n = make_float2(nr[i], nr[i]);
+                                t = __fmul2_rn(x, y);
+                                t = __ffma2_rn(__ffma2_rn(t, n, x), y, t);
+                                t = __ffma2_rn(__ffma2_rn(t, n, x), y, t);
+                                t = __fadd2_rn(t, make_float2(kRound, kRound));
+                            }
                             mb[i][2 * k] = __float_as_uint(t.x);
                             mb[i][2 * k + 1] = __float_as_uint(t.y);
                         }
@@ -475,10 +504,9 @@ __global__ void __launch_bounds__(256 * WPT, 1)
             } else {  // absmax inf or NaN somewhere in the block: literal IEEE division
 #pragma unroll
                 for (int qq = 0; qq < QB; ++qq)
-                    quant_rows_exact<CPL>(X[qq],
-                                          make_float4(-nsc[4 * qq], -nsc[4 * qq + 1], -nsc[4 * qq + 2],
-                                                      -nsc[4 * qq + 3]),
-                                          low + (q0 + qq) * D + c0);
+                    quant_rows_exact<CPL, FUSED>(
+                        X[qq], make_float4(-nsc[4 * qq], -nsc[4 * qq + 1], -nsc[4 * qq + 2], -nsc[4 * qq + 3]),
+                        reinterpret_cast<const float4 *>(nsc + S::kBlock)[qq], low + (q0 + qq) * D + c0);
             }
             __syncwarp();  // -s and 1/s are rewritten by the next block
         }

@@ -116,6 +116,34 @@ __device__ __forceinline__ uint32_t quant_quad_exact(float2 x01, float2 x23, flo
            (quant_exact(x23.x, s.z) << 16) | (quant_exact(x23.y, s.w) << 24);
 }
 
+// Fused arithmetic (RS_QUANT_FUSED): the code is the integer nearest to the
+// exact product x * y, y = RN(1/s), rounded once -- the fused multiply-add
+// x * y + 1.5 * 2^23 leaves it in the low mantissa bits (|x y| < 127.5, so
+// the sum stays in [2^23, 2^24) where the spacing is 1).  The low byte of the
+// sum is the two's-complement code.
+__device__ __forceinline__ uint32_t quant_quad_rcp(float2 x01, float2 x23, float4 y) {
+    const float2 m01 = __ffma2_rn(x01, make_float2(y.x, y.y), make_float2(kRound, kRound));
+    const float2 m23 = __ffma2_rn(x23, make_float2(y.z, y.w), make_float2(kRound, kRound));
+    const uint32_t lo2 = __byte_perm(__float_as_uint(m01.x), __float_as_uint(m01.y), 0x0040);
+    const uint32_t hi2 = __byte_perm(__float_as_uint(m23.x), __float_as_uint(m23.y), 0x0040);
+    return __byte_perm(lo2, hi2, 0x5410);
+}
+
+// One fused-arithmetic code of a row whose reciprocal is y, or -- for a row
+// whose absmax is inf or NaN, marked by y = 0 -- the IEEE quotient by s.
+__device__ __forceinline__ uint32_t quant_rcp_or_exact(float x, float s, float y) {
+    return y != 0.0f ? (__float_as_uint(__fmaf_rn(x, y, kRound)) & 0xffu) : quant_exact(x, s);
+}
+
+template <bool FUSED>
+__device__ __forceinline__ uint32_t quant_quad_cold(float2 x01, float2 x23, float4 s, float4 y) {
+    if constexpr (FUSED)
+        return quant_rcp_or_exact(x01.x, s.x, y.x) | (quant_rcp_or_exact(x01.y, s.y, y.y) << 8) |
+               (quant_rcp_or_exact(x23.x, s.z, y.z) << 16) | (quant_rcp_or_exact(x23.y, s.w, y.w) << 24);
+    else
+        return quant_quad_exact(x01, x23, s);
+}
+
 // Dequantise column tid of a mixed tile (shared or global memory) into row
 // pairs xs[j] = rows (2j, 2j+1).  int8 -> float is exact without a
 // conversion instruction: the code byte, offset by 128, becomes the low
@@ -159,8 +187,9 @@ __device__ __forceinline__ void absmax_pair(float2 xv, int j, int lane, float (&
 // ([D] floats each: row scale, its negation, its reciprocal) and flag (one
 // int, zero on entry) are group-private scratch; bar_id/D name the group
 // barrier.  `before_write` runs on every thread before the group barrier
-// that precedes the first write into `out`.  Bit-exact with the oracle.
-template <int D, int KH, typename F>
+// that precedes the first write into `out`.  Bit-exact with the oracle, in
+// the IEEE (FUSED = false) or the fused arithmetic.
+template <int D, int KH, bool FUSED, typename F>
 __device__ __forceinline__ void mixed_requant_from_max(const float2 (&xs)[D / 2], const float (&mine)[D / 32],
                                                        uint8_t *out, float *red, float *sc, float *nsc,
                                                        float *rc, int *flag, int tid, int lane, int wig,
@@ -181,7 +210,8 @@ __device__ __forceinline__ void mixed_requant_from_max(const float2 (&xs)[D / 2]
         const float s = __fdiv_rn(fmaxf(a, 1e-8f), 127.0f);
         sc[tid] = s;
         nsc[tid] = -s;
-        rc[tid] = __frcp_rn(s);
+        // fused arithmetic: y = 0 marks a row whose absmax is inf or NaN
+        rc[tid] = (FUSED && ab >= 0x7f800000u) ? 0.0f : __frcp_rn(s);
         if (ab >= 0x7f800000u) *flag = 1;  // absmax inf or NaN: exact path for the tile
         reinterpret_cast<float *>(out + 2 * KH * D + (D - KH) * D)[tid - KH] = s;
     }
@@ -194,10 +224,15 @@ __device__ __forceinline__ void mixed_requant_from_max(const float2 (&xs)[D / 2]
         const float4 *rc4 = reinterpret_cast<const float4 *>(rc + KH);
         const float4 *ns4 = reinterpret_cast<const float4 *>(nsc + KH);
 #pragma unroll
-        for (int qd = 0; qd < NQ; ++qd)
-            lo[qd * D + tid] = quant_quad(xs[KH / 2 + 2 * qd], xs[KH / 2 + 2 * qd + 1], ns4[qd], rc4[qd]);
+        for (int qd = 0; qd < NQ; ++qd) {
+            if constexpr (FUSED)
+                lo[qd * D + tid] = quant_quad_rcp(xs[KH / 2 + 2 * qd], xs[KH / 2 + 2 * qd + 1], rc4[qd]);
+            else
+                lo[qd * D + tid] = quant_quad(xs[KH / 2 + 2 * qd], xs[KH / 2 + 2 * qd + 1], ns4[qd], rc4[qd]);
+        }
     } else {
         const float4 *sc4 = reinterpret_cast<const float4 *>(sc + KH);
+        const float4 *rc4 = reinterpret_cast<const float4 *>(rc + KH);
 #pragma unroll 1
         for (int qd = 0; qd < NQ; ++qd) {
             // dynamic quad index on this cold path: select the pair from the
@@ -209,14 +244,14 @@ __device__ __forceinline__ void mixed_requant_from_max(const float2 (&xs)[D / 2]
                     a01 = xs[KH / 2 + 2 * k];
                     a23 = xs[KH / 2 + 2 * k + 1];
                 }
-            lo[qd * D + tid] = quant_quad_exact(a01, a23, sc4[qd]);
+            lo[qd * D + tid] = quant_quad_cold<FUSED>(a01, a23, sc4[qd], rc4[qd]);
         }
     }
 }
 
 // Same, collecting the per-row maxima first (for callers that did not fuse
 // the reductions into the update pass).
-template <int D, int KH, typename F>
+template <int D, int KH, bool FUSED, typename F>
 __device__ __forceinline__ void mixed_requant_smem(const float2 (&xs)[D / 2], uint8_t *out, float *red,
                                                    float *sc, float *nsc, float *rc, int *flag,
                                                    int tid, int lane, int wig, uint32_t bar_id,
@@ -226,8 +261,8 @@ __device__ __forceinline__ void mixed_requant_smem(const float2 (&xs)[D / 2], ui
     for (int k = 0; k < D / 32; ++k) mine[k] = 0.0f;
 #pragma unroll
     for (int j = KH / 2; j < D / 2; ++j) absmax_pair<D>(xs[j], j, lane, mine);
-    mixed_requant_from_max<D, KH>(xs, mine, out, red, sc, nsc, rc, flag, tid, lane, wig, bar_id,
-                                  before_write);
+    mixed_requant_from_max<D, KH, FUSED>(xs, mine, out, red, sc, nsc, rc, flag, tid, lane, wig, bar_id,
+                                         before_write);
 }
 
 // Dequantise rows 4q..4q+3 (q counted from row 0) of column tid of a mixed
@@ -256,7 +291,7 @@ __device__ __forceinline__ void mixed_dequant_quad(const uint8_t *tile, int q, i
     }
 }
 
-template <int D, int KHI, bool KDA, int MAXT, typename TI, typename TO, typename PT>
+template <int D, int KHI, bool KDA, int MAXT, typename TI, typename TO, typename PT, bool FUSED = false>
 __global__ void __launch_bounds__(step_threads(MAXT), 1)
     step_kernel(const __grid_constant__ PT P) {
     using S = StepShape<D, KHI, KDA, TI>;
@@ -399,6 +434,9 @@ __global__ void __launch_bounds__(step_threads(MAXT), 1)
             for (int j = 0; j < DP; ++j) x[j] = make_float2(st[(2 * j) * D + tid], st[(2 * j + 1) * D + tid]);
         }
 
+        auto decay_of = [&](int t) -> float {
+            return KDA ? 0.0f : (MAXT == 1 ? alpha0 : tok_alpha[t]);
+        };
         // ---- token inputs -> per-row vectors (row u built by thread u) -----
         const int ntok = MAXT == 1 ? 1 : n;  // decode instances: one token, known at compile time
         {
@@ -415,7 +453,17 @@ __global__ void __launch_bounds__(step_threads(MAXT), 1)
                 rv[D + tid] = __fmul_rn(bt, kf);
                 rv[2 * D + tid] = load_as_f32<TI>(qt + src);
                 rv[3 * D + tid] = load_as_f32<TI>(vt + tid);  // value coordinates: no row map
-                if (KDA) rv[4 * D + tid] = reinterpret_cast<const float *>(tb + 3 * S::kVecBytes)[src];
+                const float at = KDA ? reinterpret_cast<const float *>(tb + 3 * S::kVecBytes)[src] : decay_of(t);
+                if (KDA) rv[4 * D + tid] = at;
+                if constexpr (MIXED && FUSED && MAXT > 1) {
+                    // fused arithmetic: the first token's decay of INT8 row tid goes
+                    // into the row's scale in the stage, RN(s a); dequantising then
+                    // gives c * RN(s a) and token 0 skips that row's decay
+                    if (t == 0 && tid >= KH) {
+                        float *scl_st = reinterpret_cast<float *>(stage + 2 * KH * D + (D - KH) * D);
+                        scl_st[tid - KH] = __fmul_rn(scl_st[tid - KH], at);
+                    }
+                }
             }
         }
         group_sync(bar_id, D);  // row vectors visible (FP32: stage fully read)
@@ -425,9 +473,6 @@ __global__ void __launch_bounds__(step_threads(MAXT), 1)
                 issue(nxt, nxt_slot, nxt_n);  // the stage now belongs to the next tile
             }
         }
-        auto decay_of = [&](int t) -> float {
-            return KDA ? 0.0f : (MAXT == 1 ? alpha0 : tok_alpha[t]);
-        };
 
         TO *og = static_cast<TO *>(P.o);
         float mine[D / 32];
@@ -493,6 +538,8 @@ __global__ void __launch_bounds__(step_threads(MAXT), 1)
             for (int t = 0; t < ntok; ++t) {
                 const float *rv = rowv + t * S::kRowVecs * D;
                 const float a_s = decay_of(t);
+                // fused arithmetic: token 0's decay of the INT8 rows is in their scales
+                const bool dec_lo = !(MIXED && FUSED) || t > 0;
                 float p = 0.0f;
 #pragma unroll
                 for (int j = 0; j < DP; j += 2) {
@@ -500,6 +547,7 @@ __global__ void __launch_bounds__(step_threads(MAXT), 1)
                     float4 aa;
                     if (KDA) aa = *reinterpret_cast<const float4 *>(rv + 4 * D + 2 * j);
                     else aa = make_float4(a_s, a_s, a_s, a_s);
+                    if (2 * j >= KH && !dec_lo) aa = make_float4(1.0f, 1.0f, 1.0f, 1.0f);  // x * 1 = x
                     x[j] = __fmul2_rn(x[j], make_float2(aa.x, aa.y));
                     x[j + 1] = __fmul2_rn(x[j + 1], make_float2(aa.z, aa.w));
                     p = __fmaf_rn(x[j].x, kk.x, p);
@@ -538,8 +586,8 @@ __global__ void __launch_bounds__(step_threads(MAXT), 1)
                 st[(2 * j + 1) * D + tid] = x[j].y;
             }
         } else {
-            mixed_requant_from_max<D, KH>(x, mine, outt, red, scl, nscl, rcp, flag, tid, lane, wig,
-                                          bar_id, [&] {
+            mixed_requant_from_max<D, KH, FUSED>(x, mine, outt, red, scl, nscl, rcp, flag, tid, lane, wig,
+                                                 bar_id, [&] {
                                               if (tid == 0) {
                                                   bulk_store_wait_read();  // previous store has read `outt`
                                                   *flag = 0;

@@ -12,11 +12,10 @@ namespace {
 constexpr int kMixedWpt = 2;
 constexpr int kMixedSlots = 8;  // tile slots per CTA
 
-template <int D, int KHI, bool KDA, int MAXT, typename TI, typename TO>
+template <int D, int KHI, bool KDA, typename TI, typename TO, bool FUSED>
 cudaError_t run(StepParamsPi &P, cudaStream_t s) {
-    static_assert(MAXT == 1, "single decode steps");
-    using Sh = MixedWarpShape<D, KHI, KDA, TI, kMixedWpt>;
-    auto kern = mixed_decode_kernel<D, KHI, KDA, TI, TO, kMixedWpt>;
+    using Sh = MixedWarpShape<D, KHI, KDA, TI, kMixedWpt, FUSED>;
+    auto kern = mixed_decode_kernel<D, KHI, KDA, TI, TO, kMixedWpt, FUSED>;
     const int header = Sh::kHeader + (P.Hv * D + 127) / 128 * 128;
     const int smax = device_max_smem_optin();
     // NSLOT tile slots and a ring of NS > NSLOT stages in the shared memory there is
@@ -43,18 +42,22 @@ cudaError_t run(StepParamsPi &P, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-template <bool KDA>
+template <bool KDA, bool FUSED>
 cudaError_t by_types(const StepLaunch &L, StepParamsPi &P, cudaStream_t s) {
-    if (L.in_dt == RS_BF16 && L.out_dt == RS_F32) return run<128, 16, KDA, 1, __nv_bfloat16, float>(P, s);
-    if (L.in_dt == RS_BF16 && L.out_dt == RS_BF16) return run<128, 16, KDA, 1, __nv_bfloat16, __nv_bfloat16>(P, s);
-    if (L.in_dt == RS_F32 && L.out_dt == RS_F32) return run<128, 16, KDA, 1, float, float>(P, s);
+    if (L.in_dt == RS_BF16 && L.out_dt == RS_F32) return run<128, 16, KDA, __nv_bfloat16, float, FUSED>(P, s);
+    if (L.in_dt == RS_BF16 && L.out_dt == RS_BF16)
+        return run<128, 16, KDA, __nv_bfloat16, __nv_bfloat16, FUSED>(P, s);
+    if (L.in_dt == RS_F32 && L.out_dt == RS_F32) return run<128, 16, KDA, float, float, FUSED>(P, s);
     return cudaErrorNotSupported;
 }
 
 }  // namespace
 
 cudaError_t launch_step_mixed_decode(const StepLaunch &L, StepParamsPi &P, cudaStream_t s) {
-    if (L.D == 128 && L.khi == 16) return L.kda ? by_types<true>(L, P, s) : by_types<false>(L, P, s);
+    if (L.D == 128 && L.khi == 16) {
+        if (L.fused) return L.kda ? by_types<true, true>(L, P, s) : by_types<false, true>(L, P, s);
+        return L.kda ? by_types<true, false>(L, P, s) : by_types<false, false>(L, P, s);
+    }
     return cudaErrorNotSupported;
 }
 

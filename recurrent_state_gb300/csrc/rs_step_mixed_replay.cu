@@ -7,10 +7,10 @@ namespace rs {
 
 namespace {
 
-template <int D, int KHI, bool KDA, int MAXT, typename TI, typename TO>
+template <int D, int KHI, bool KDA, int MAXT, typename TI, typename TO, bool FUSED>
 cudaError_t run(StepParamsPi &P, cudaStream_t s) {
     using Sh = StepShape<D, KHI, KDA, TI>;
-    auto kern = step_kernel<D, KHI, KDA, MAXT, TI, TO, StepParamsPi>;
+    auto kern = step_kernel<D, KHI, KDA, MAXT, TI, TO, StepParamsPi, FUSED>;
     const int region = Sh::region_bytes(P.T_max);
     const int header = 128 + (P.Hv * D + 127) / 128 * 128;
     const int smax = device_max_smem_optin();
@@ -30,18 +30,23 @@ cudaError_t run(StepParamsPi &P, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-template <bool KDA>
+template <bool KDA, bool FUSED>
 cudaError_t by_types(const StepLaunch &L, StepParamsPi &P, cudaStream_t s) {
-    if (L.in_dt == RS_BF16 && L.out_dt == RS_F32) return run<128, 16, KDA, kMaxTokens, __nv_bfloat16, float>(P, s);
-    if (L.in_dt == RS_BF16 && L.out_dt == RS_BF16) return run<128, 16, KDA, kMaxTokens, __nv_bfloat16, __nv_bfloat16>(P, s);
-    if (L.in_dt == RS_F32 && L.out_dt == RS_F32) return run<128, 16, KDA, kMaxTokens, float, float>(P, s);
+    if (L.in_dt == RS_BF16 && L.out_dt == RS_F32)
+        return run<128, 16, KDA, kMaxTokens, __nv_bfloat16, float, FUSED>(P, s);
+    if (L.in_dt == RS_BF16 && L.out_dt == RS_BF16)
+        return run<128, 16, KDA, kMaxTokens, __nv_bfloat16, __nv_bfloat16, FUSED>(P, s);
+    if (L.in_dt == RS_F32 && L.out_dt == RS_F32) return run<128, 16, KDA, kMaxTokens, float, float, FUSED>(P, s);
     return cudaErrorNotSupported;
 }
 
 }  // namespace
 
 cudaError_t launch_step_mixed_replay(const StepLaunch &L, StepParamsPi &P, cudaStream_t s) {
-    if (L.D == 128 && L.khi == 16) return L.kda ? by_types<true>(L, P, s) : by_types<false>(L, P, s);
+    if (L.D == 128 && L.khi == 16) {
+        if (L.fused) return L.kda ? by_types<true, true>(L, P, s) : by_types<false, true>(L, P, s);
+        return L.kda ? by_types<true, false>(L, P, s) : by_types<false, false>(L, P, s);
+    }
     return cudaErrorNotSupported;
 }
 
