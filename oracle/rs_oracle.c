@@ -154,7 +154,7 @@ void orc_dequantise_row(int n, const int8_t *codes, float s, float *x)
 /*     §3.1 Lambda applied to the dequantised state of §3.2 Eq. 6); FP16 rows */
 /*     are decayed as in mode 0, x = RN(h * a_u).                            */
 /* A mode-1 code differs from the mode-0 code only where x/s lies within a   */
-/* few units of 2^-24 |x/s| of a half-integer (the spec allowance is   */
+/* few units of 2^-24 |x/s| of a half-integer (the acceptance allowance is   */
 /* 1e-6 max(1, |x/s|)).                                                      */
 /* ------------------------------------------------------------------------ */
 int8_t orc_quant_code_rcp(float x, float y)

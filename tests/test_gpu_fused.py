@@ -7,7 +7,7 @@ Acceptance: the library and the oracle's mode 1 compute the same FP32
 values and the same one-rounding codes, so every byte of the packed tiles
 and every bit of o must match, step after step (NaN payloads excepted).  The
 oracle pins mode 1 against the IEEE-quotient definition separately: its
-codes differ only by one and only within the spec allowance of a
+codes differ only by one and only within the acceptance allowance of a
 rounding boundary.
 """
 import numpy as np

@@ -12,7 +12,7 @@ Pins, each independent of the oracle's own formulas:
   - the code against exact rational arithmetic (``fractions.Fraction``),
     including exact ties and a double-rounding trap;
   - mode-1 codes differ from mode-0 (IEEE quotient) codes by at most one and
-    only where the exact quotient lies within the spec allowance,
+    only where the exact quotient lies within the acceptance allowance,
     1e-6 max(1, |x/s|), of a half-integer; a constructed row where they do
     differ keeps the check from being vacuous;
   - the dequantise-and-decay against numpy's IEEE float32 arithmetic;
