@@ -535,38 +535,69 @@ __global__ void __launch_bounds__(step_threads(MAXT), 1)
                     issue(nxt, nxt_slot, nxt_n);  // the stage now belongs to the next tile
                 }
             }
+            // Token t's readout chain and token t + 1's decay and prediction chain
+            // read the same updated rows, so one pass over the registers carries
+            // both (two independent chains per thread); each chain keeps its
+            // ascending row order, so the result equals token-by-token steps.
+            auto decay4 = [&](const float *rv, int t, int j) -> float4 {
+                float4 aa;
+                if (KDA) aa = *reinterpret_cast<const float4 *>(rv + 4 * D + 2 * j);
+                else { const float a_s = decay_of(t); aa = make_float4(a_s, a_s, a_s, a_s); }
+                // fused arithmetic: token 0's decay of the INT8 rows is in their scales
+                if (MIXED && FUSED && t == 0 && 2 * j >= KH) aa = make_float4(1.0f, 1.0f, 1.0f, 1.0f);
+                return aa;
+            };
+            float p = 0.0f;
+#pragma unroll
+            for (int j = 0; j < DP; j += 2) {  // token 0: decay and prediction
+                const float4 kk = *reinterpret_cast<const float4 *>(rowv + 2 * j);
+                const float4 aa = decay4(rowv, 0, j);
+                x[j] = __fmul2_rn(x[j], make_float2(aa.x, aa.y));
+                x[j + 1] = __fmul2_rn(x[j + 1], make_float2(aa.z, aa.w));
+                p = __fmaf_rn(x[j].x, kk.x, p);
+                p = __fmaf_rn(x[j].y, kk.y, p);
+                p = __fmaf_rn(x[j + 1].x, kk.z, p);
+                p = __fmaf_rn(x[j + 1].y, kk.w, p);
+            }
             for (int t = 0; t < ntok; ++t) {
                 const float *rv = rowv + t * S::kRowVecs * D;
-                const float a_s = decay_of(t);
-                // fused arithmetic: token 0's decay of the INT8 rows is in their scales
-                const bool dec_lo = !(MIXED && FUSED) || t > 0;
-                float p = 0.0f;
-#pragma unroll
-                for (int j = 0; j < DP; j += 2) {
-                    const float4 kk = *reinterpret_cast<const float4 *>(rv + 2 * j);
-                    float4 aa;
-                    if (KDA) aa = *reinterpret_cast<const float4 *>(rv + 4 * D + 2 * j);
-                    else aa = make_float4(a_s, a_s, a_s, a_s);
-                    if (2 * j >= KH && !dec_lo) aa = make_float4(1.0f, 1.0f, 1.0f, 1.0f);  // x * 1 = x
-                    x[j] = __fmul2_rn(x[j], make_float2(aa.x, aa.y));
-                    x[j + 1] = __fmul2_rn(x[j + 1], make_float2(aa.z, aa.w));
-                    p = __fmaf_rn(x[j].x, kk.x, p);
-                    p = __fmaf_rn(x[j].y, kk.y, p);
-                    p = __fmaf_rn(x[j + 1].x, kk.z, p);
-                    p = __fmaf_rn(x[j + 1].y, kk.w, p);
-                }
                 const float e = __fsub_rn(rv[3 * D + tid], p);
                 float o = 0.0f;
+                if (t + 1 < ntok) {
+                    const float *rn = rv + S::kRowVecs * D;  // token t + 1
+                    float pn = 0.0f;
 #pragma unroll
-                for (int j = 0; j < DP; j += 2) {
-                    const float4 bk = *reinterpret_cast<const float4 *>(rv + D + 2 * j);
-                    const float4 qq = *reinterpret_cast<const float4 *>(rv + 2 * D + 2 * j);
-                    x[j] = __ffma2_rn(make_float2(bk.x, bk.y), make_float2(e, e), x[j]);
-                    x[j + 1] = __ffma2_rn(make_float2(bk.z, bk.w), make_float2(e, e), x[j + 1]);
-                    o = __fmaf_rn(x[j].x, qq.x, o);
-                    o = __fmaf_rn(x[j].y, qq.y, o);
-                    o = __fmaf_rn(x[j + 1].x, qq.z, o);
-                    o = __fmaf_rn(x[j + 1].y, qq.w, o);
+                    for (int j = 0; j < DP; j += 2) {
+                        const float4 bk = *reinterpret_cast<const float4 *>(rv + D + 2 * j);
+                        const float4 qq = *reinterpret_cast<const float4 *>(rv + 2 * D + 2 * j);
+                        const float4 kk = *reinterpret_cast<const float4 *>(rn + 2 * j);
+                        const float4 aa = decay4(rn, t + 1, j);
+                        x[j] = __ffma2_rn(make_float2(bk.x, bk.y), make_float2(e, e), x[j]);
+                        x[j + 1] = __ffma2_rn(make_float2(bk.z, bk.w), make_float2(e, e), x[j + 1]);
+                        o = __fmaf_rn(x[j].x, qq.x, o);
+                        o = __fmaf_rn(x[j].y, qq.y, o);
+                        o = __fmaf_rn(x[j + 1].x, qq.z, o);
+                        o = __fmaf_rn(x[j + 1].y, qq.w, o);
+                        x[j] = __fmul2_rn(x[j], make_float2(aa.x, aa.y));
+                        x[j + 1] = __fmul2_rn(x[j + 1], make_float2(aa.z, aa.w));
+                        pn = __fmaf_rn(x[j].x, kk.x, pn);
+                        pn = __fmaf_rn(x[j].y, kk.y, pn);
+                        pn = __fmaf_rn(x[j + 1].x, kk.z, pn);
+                        pn = __fmaf_rn(x[j + 1].y, kk.w, pn);
+                    }
+                    p = pn;
+                } else {
+#pragma unroll
+                    for (int j = 0; j < DP; j += 2) {
+                        const float4 bk = *reinterpret_cast<const float4 *>(rv + D + 2 * j);
+                        const float4 qq = *reinterpret_cast<const float4 *>(rv + 2 * D + 2 * j);
+                        x[j] = __ffma2_rn(make_float2(bk.x, bk.y), make_float2(e, e), x[j]);
+                        x[j + 1] = __ffma2_rn(make_float2(bk.z, bk.w), make_float2(e, e), x[j + 1]);
+                        o = __fmaf_rn(x[j].x, qq.x, o);
+                        o = __fmaf_rn(x[j].y, qq.y, o);
+                        o = __fmaf_rn(x[j + 1].x, qq.z, o);
+                        o = __fmaf_rn(x[j + 1].y, qq.w, o);
+                    }
                 }
                 if (og) store_from_f32<TO>(og + (((size_t)b * T + t) * Hv + h) * D + tid, o);
             }
