@@ -363,6 +363,7 @@ def _time(torch, fn, iters, warm=3):
 
 EXTRA = ("gdn_fp32", "kda_fp32", "kda_mixed", "gdn_mixed", "kda_damp", "replay_mixed", "replay_fp32",
          "kda_mixed_fused", "gdn_mixed_fused", "kda_damp_fused", "replay_mixed_fused",
+         "prefill_fp32", "prefill_mixed_fused",
          "pack_gdn", "restore_gdn", "pack_kda", "restore_kda", "pack_int8_gdn", "restore_int8_gdn",
          "pack_int8_kda", "restore_int8_kda", "pack_mixed", "restore_mixed")
 
@@ -498,6 +499,39 @@ def extra_kernels(args, rs, torch, dev, peak, world, only=None):
                 rec(f"kda_replay_fp32_b{B}_T8", sec, 2 * B * 32 * f32.head_bytes + tok * per_tok,
                     tok * 32, {"accepted_tokens": tok})
         del pool, mpool
+        torch.cuda.empty_cache()
+
+    # prefill chunks: KDA, 32 heads, a chunk of 32 tokens per sequence
+    if want & {"prefill_fp32", "prefill_mixed_fused"}:
+        Lc = 32
+        w = gen.decode_workload(steps=Lc, per_channel=True, in_dtype="bf16", seed=3,
+                                horizon=(2.0, 8192.0), **KDA_B)
+
+        def bt(x):
+            return np.ascontiguousarray(np.swapaxes(x, 0, 1))
+        pq, pk, pv = to_bf16(bt(w.q_bits)), to_bf16(bt(w.k_bits)), to_bf16(bt(w.v_bits))
+        pa, pb = to_dev(bt(w.alpha)), to_dev(bt(w.beta))
+        slots = to_dev(w.slot_idx)
+        po = torch.empty((B, Lc, 32, 128), device=dev)
+        f32 = rs.Layout("fp32", 128, KDA["Hv"], KDA["Hk"])
+        pool = to_dev(w.state0)
+        per_tok = 2 * 32 * 128 * 2 + 32 * 128 * 2 + 32 * 128 * 4 + 32 * 4 + 32 * 128 * 4
+        if "prefill_fp32" in want:
+            sec = _time(torch, lambda i: rs.prefill_update(f32, True, pool, slots, pq, pk, pv, pa, pb, o=po),
+                        max(3, iters // 10), warm)
+            rec(f"kda_prefill_fp32_b{B}_L{Lc}", sec, 2 * B * 32 * f32.head_bytes + B * Lc * per_tok,
+                B * 32 * Lc, {"chunk_tokens": Lc})
+        if "prefill_mixed_fused" in want:
+            hi = gen.hi_rows(KDA["Hv"], 128, 16, seed=3)
+            mixf = rs.Layout("mixed", 128, KDA["Hv"], KDA["Hk"], k_hi=16, hi_rows=hi, quant="fused")
+            mpool = mixf.empty_pool(B, device=dev)
+            rs.state_convert(f32, pool, mixf, mpool, torch.arange(B, dtype=torch.int32, device=dev))
+            sec = _time(torch, lambda i: rs.prefill_update(mixf, True, mpool, slots, pq, pk, pv, pa, pb, o=po),
+                        max(3, iters // 10), warm)
+            rec(f"kda_prefill_mixed_fused_b{B}_L{Lc}", sec, 2 * B * 32 * mixf.head_bytes + B * Lc * per_tok,
+                B * 32 * Lc, {"chunk_tokens": Lc, "quant": "fused"})
+            del mpool
+        del pool, pq, pk, pv, pa, pb, po
         torch.cuda.empty_cache()
 
     # dasc pack / restore: 36 layers, 64 checkpoints, 64 pool slots

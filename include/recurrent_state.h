@@ -256,6 +256,33 @@ rs_status rs_spec_replay_update(const rs_layout *l, int32_t per_channel_decay,
                                 void *o, int32_t out_dtype, int32_t *status,
                                 void *stream);
 
+/* Prefill chunk ([DAMP] Appendix A.4 "Prefill path": prefill uses FP32
+ * arithmetic within each chunk and writes its final state to the same
+ * packed cache, which later chunks and decoding steps read).  For each
+ * sequence b, the first n_tokens[b] tokens of its chunk of L tokens are
+ * applied to the state in order, each as one decode step (GDN or KDA, as
+ * per_channel_decay), with the state read (and dequantised) once, kept in
+ * FP32 on chip, and written (and requantised) once.  On the FP32 layout the
+ * result equals n_tokens[b] decode calls bit for bit; on a mixed layout it
+ * is the multi-token replay of the same tokens (one dequantisation and one
+ * requantisation, in the layout's RS_QUANT mode).
+ *   L         tokens per chunk (>= 0; 0 is a no-op)
+ *   n_tokens  device int32 [B], each in [0, L], or NULL for L tokens each;
+ *             an out-of-range count skips the sequence and sets
+ *             RS_DEV_BAD_ACCEPT
+ *   q, k      device in_dtype [B][L][Hk][dk]; v [B][L][Hv][dv]
+ *   alpha     device float [B][L][Hv] (GDN) or [B][L][Hv][dk] (KDA)
+ *   beta      device float [B][L][Hv]
+ *   o         device out_dtype [B][L][Hv][dv] or NULL; rows t >= n_tokens[b]
+ *             are not written.
+ * Built for dk = dv = 128, the FP32 layout and the one-scale-per-row mixed
+ * layout (k_hi = 16); other layouts return RS_ERR_UNSUPPORTED. */
+rs_status rs_prefill_update(const rs_layout *l, int32_t per_channel_decay, void *pool,
+                            int64_t n_slots, const int32_t *slot_idx, int32_t B, int32_t L,
+                            const int32_t *n_tokens, const void *q, const void *k, const void *v,
+                            int32_t in_dtype, const float *alpha, const float *beta, void *o,
+                            int32_t out_dtype, int32_t *status, void *stream);
+
 /* Convert n slots between two layouts of the same shape (FP32 -> mixed
  * quantises with the rules above; mixed -> FP32 dequantises and un-permutes
  * rows; same kind copies).  slots: device int32 [n], used as both source and

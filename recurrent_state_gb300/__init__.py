@@ -15,14 +15,14 @@ from __future__ import annotations
 import importlib
 
 __all__ = [
-    "Layout", "Plan", "gdn_decode_update", "kda_decode_update", "spec_replay_update",
+    "Layout", "Plan", "gdn_decode_update", "kda_decode_update", "spec_replay_update", "prefill_update",
     "state_convert", "ckpt_pack", "ckpt_restore", "ckpt_pack_int8", "ckpt_restore_int8", "RsError",
     "build", "inputs", "plans",
 ]
 
 _LAZY = {
     "Layout": "api", "Plan": "api", "gdn_decode_update": "api", "kda_decode_update": "api",
-    "spec_replay_update": "api", "state_convert": "api", "ckpt_pack": "api",
+    "spec_replay_update": "api", "prefill_update": "api", "state_convert": "api", "ckpt_pack": "api",
     "ckpt_restore": "api", "ckpt_pack_int8": "api", "ckpt_restore_int8": "api", "RsError": "_abi",
 }
 

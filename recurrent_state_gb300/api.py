@@ -177,6 +177,29 @@ def spec_replay_update(layout, per_channel_decay, pool, slot_idx, n_accept, q, k
     return o
 
 
+def prefill_update(layout, per_channel_decay, pool, slot_idx, q, k, v, alpha, beta, n_tokens=None,
+                   o=None, status=None, stream=None):
+    """Apply a prefill chunk of L tokens (inputs [B][L][...]) to each sequence's
+    state, read and written once; ``n_tokens`` [B] int32 limits each sequence
+    to its first n_tokens[b] tokens (default: all L)."""
+    n_slots = _pool_slots(layout, pool)
+    _dev(slot_idx, "slot_idx", torch.int32)
+    _dev(n_tokens, "n_tokens", torch.int32)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _dev(t, name)
+    _dev(alpha, "alpha", torch.float32)
+    _dev(beta, "beta", torch.float32)
+    _dev(o, "o")
+    _dev(status, "status", torch.int32)
+    B, L = q.shape[0], q.shape[1]
+    out_dt = _DT[o.dtype] if o is not None else _abi.RS_F32
+    check(_abi.lib().rs_prefill_update(
+        layout.handle, int(bool(per_channel_decay)), _ptr(pool), n_slots, _ptr(slot_idx), B, L,
+        _ptr(n_tokens), _ptr(q), _ptr(k), _ptr(v), _DT[q.dtype], _ptr(alpha), _ptr(beta), _ptr(o),
+        out_dt, _ptr(status), _stream(stream)), "rs_prefill_update")
+    return o
+
+
 def state_convert(src_layout, src_pool, dst_layout, dst_pool, slots, status=None, stream=None):
     """Convert the listed slots between two layouts of the same shape."""
     n_slots = _pool_slots(src_layout, src_pool)

@@ -308,6 +308,50 @@ rs_status rs_spec_replay_update(const rs_layout *l, int32_t per_channel_decay, v
                        q, k, v, in_dtype, alpha, beta, o, out_dtype, status, stream);
 }
 
+rs_status rs_prefill_update(const rs_layout *l, int32_t per_channel_decay, void *pool, int64_t n_slots,
+                            const int32_t *slot_idx, int32_t B, int32_t L, const int32_t *n_tokens,
+                            const void *q, const void *k, const void *v, int32_t in_dtype,
+                            const float *alpha, const float *beta, void *o, int32_t out_dtype,
+                            int32_t *status, void *stream) {
+    if (!l || (per_channel_decay != 0 && per_channel_decay != 1)) return RS_ERR_INVALID_ARG;
+    if (B < 0 || L < 0 || n_slots < 0 || n_slots > INT32_MAX) return RS_ERR_INVALID_ARG;
+    if (dtype_size(in_dtype) == 0 || (out_dtype != RS_F32 && out_dtype != RS_BF16)) return RS_ERR_INVALID_ARG;
+    const int Hv = l->p.num_v_heads, Hk = l->p.num_qk_heads, D = l->p.dk;
+    if ((int64_t)B * Hv > INT32_MAX / 2) return RS_ERR_INVALID_ARG;
+    if (B == 0 || L == 0) return RS_OK;
+    if (!pool || !slot_idx || !q || !k || !v || !alpha || !beta) return RS_ERR_INVALID_ARG;
+    if (!aligned16(pool) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(alpha))
+        return RS_ERR_MISALIGNED;
+    if (l->group) return RS_ERR_UNSUPPORTED;  // DAMP-exact layout: not built
+    rs::StepLaunch Ln;
+    Ln.D = D;
+    Ln.khi = l->p.kind == RS_LAYOUT_FP32 ? -1 : l->p.k_hi;
+    Ln.kda = per_channel_decay == 1;
+    Ln.in_dt = in_dtype;
+    Ln.out_dt = out_dtype;
+    Ln.fused = l->p.kind != RS_LAYOUT_FP32 && l->quant == RS_QUANT_FUSED;
+    static thread_local rs::PrefillParams P;
+    P.pool = pool;
+    P.n_slots = n_slots;
+    P.slot_idx = slot_idx;
+    P.n_tokens = n_tokens;
+    P.q = q;
+    P.k = k;
+    P.v = v;
+    P.alpha = alpha;
+    P.beta = beta;
+    P.o = o;
+    P.status = status;
+    P.B = B;
+    P.Hk = Hk;
+    P.Hv = Hv;
+    P.L = L;
+    for (size_t i = 0; i < l->pi.size() && i < (size_t)rs::kMaxRowMap; ++i) P.pi[i] = (uint8_t)l->pi[i];
+    const cudaError_t e = rs::launch_prefill(Ln, P, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return launch_fail(e);
+    return RS_OK;
+}
+
 // ---------------------------------------------------------------------------
 // conversion
 // ---------------------------------------------------------------------------

@@ -71,6 +71,24 @@ cudaError_t launch_step_f32_d128(const StepLaunch &L, StepParams &P, cudaStream_
 cudaError_t launch_step_mixed_decode(const StepLaunch &L, StepParamsPi &P, cudaStream_t s);
 cudaError_t launch_step_mixed_replay(const StepLaunch &L, StepParamsPi &P, cudaStream_t s);
 
+// rs_prefill.cu: prefill chunks (FP32 steps on chip, state read and written once)
+struct PrefillParams {
+    void *pool;
+    int64_t n_slots;
+    const int32_t *slot_idx;
+    const int32_t *n_tokens;   // [B] tokens of each sequence's chunk, or null: all L
+    const void *q;
+    const void *k;
+    const void *v;
+    const float *alpha;
+    const float *beta;
+    void *o;
+    int32_t *status;
+    int32_t B, Hk, Hv, L;
+    uint8_t pi[kMaxRowMap];    // mixed layout: physical row -> key channel
+};
+cudaError_t launch_prefill(const StepLaunch &L, PrefillParams &P, cudaStream_t s);
+
 // rs_convert.cu
 struct ConvertParams {
     const void *src;

@@ -147,12 +147,15 @@ __device__ __forceinline__ uint32_t quant_quad_cold(float2 x01, float2 x23, floa
 // Dequantise column tid of a mixed tile (shared or global memory) into row
 // pairs xs[j] = rows (2j, 2j+1).  int8 -> float is exact without a
 // conversion instruction: the code byte, offset by 128, becomes the low
-// mantissa byte of 2^23 and the bias is subtracted.
+// mantissa byte of 2^23 and the bias is subtracted.  `scales` (16-byte
+// aligned, D - KH floats) replaces the tile's own row scales when given.
 template <int D, int KH>
-__device__ __forceinline__ void mixed_dequant(const uint8_t *tile, int tid, float2 (&xs)[D / 2]) {
+__device__ __forceinline__ void mixed_dequant(const uint8_t *tile, int tid, float2 (&xs)[D / 2],
+                                              const float *scales = nullptr) {
     const __half2 *hi = reinterpret_cast<const __half2 *>(tile);
     const uint32_t *lo = reinterpret_cast<const uint32_t *>(tile + 2 * KH * D);
-    const float4 *sc4 = reinterpret_cast<const float4 *>(tile + 2 * KH * D + (D - KH) * D);
+    const float4 *sc4 = reinterpret_cast<const float4 *>(
+        scales ? scales : reinterpret_cast<const float *>(tile + 2 * KH * D + (D - KH) * D));
 #pragma unroll
     for (int j = 0; j < KH / 2; ++j) xs[j] = __half22float2(hi[j * D + tid]);
 #pragma unroll
