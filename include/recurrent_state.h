@@ -161,8 +161,8 @@ rs_status rs_layout_create(rs_layout **out, const rs_layout_params *p,
  * interleave), then scales [dk - k_hi][dv / group] f32 row-major: 20,224 B at
  * d = 128, k_hi = 16 (9.875 bits per value).  rs_state_convert converts FP32
  * states (S in logical rows) to and from it; checkpoint plans take its heads
- * as units.  Speculative replay on this layout is not built
- * (RS_ERR_UNSUPPORTED); Hv * dv <= 4096. */
+ * as units; speculative replay and prefill chunks run on it (one
+ * dequantisation and one requantisation per call).  Hv * dv <= 4096. */
 rs_status rs_layout_create_damp(rs_layout **out, const rs_layout_params *p, const int16_t *hi_rows,
                                 int32_t group, const float *value_scales);
 rs_status rs_layout_destroy(rs_layout *l);
@@ -275,8 +275,9 @@ rs_status rs_spec_replay_update(const rs_layout *l, int32_t per_channel_decay,
  *   beta      device float [B][L][Hv]
  *   o         device out_dtype [B][L][Hv][dv] or NULL; rows t >= n_tokens[b]
  *             are not written.
- * Built for dk = dv = 128, the FP32 layout and the one-scale-per-row mixed
- * layout (k_hi = 16); other layouts return RS_ERR_UNSUPPORTED. */
+ * Built for dk = dv = 128: the FP32 layout and the mixed layouts with
+ * k_hi = 16 (one scale per row, or DAMP-exact groups of 32 with value
+ * scaling); other shapes return RS_ERR_UNSUPPORTED. */
 rs_status rs_prefill_update(const rs_layout *l, int32_t per_channel_decay, void *pool,
                             int64_t n_slots, const int32_t *slot_idx, int32_t B, int32_t L,
                             const int32_t *n_tokens, const void *q, const void *k, const void *v,

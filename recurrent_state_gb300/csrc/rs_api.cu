@@ -207,6 +207,12 @@ rs_status rs_layout_bits_per_value(const rs_layout *l, double *bits) {
 // ---------------------------------------------------------------------------
 // decode / replay
 // ---------------------------------------------------------------------------
+static rs_status prefill_common(const rs_layout *l, int32_t per_channel_decay, void *pool, int64_t n_slots,
+                                const int32_t *slot_idx, int32_t B, int32_t L, const int32_t *n_tokens,
+                                const void *q, const void *k, const void *v, int32_t in_dtype,
+                                const float *alpha, const float *beta, void *o, int32_t out_dtype,
+                                int32_t *status, void *stream);
+
 static rs_status step_common(const rs_layout *l, bool kda, bool replay, void *pool, int64_t n_slots,
                              const int32_t *slot_idx, int32_t B, int32_t T_max,
                              const int32_t *n_accept, const void *q, const void *k, const void *v,
@@ -263,8 +269,12 @@ static rs_status step_common(const rs_layout *l, bool kda, bool replay, void *po
         fill(P);
         e = D == 128 ? rs::launch_step_f32_d128(L, P, s) : rs::launch_step_f32_d64(L, P, s);
     } else {
-        if (l->group) {  // DAMP-exact layout: single decode steps
-            if (replay || T_max > 1) return RS_ERR_UNSUPPORTED;
+        if (l->group) {  // DAMP-exact layout
+            // a multi-token replay is a prefill chunk of T_max tokens with
+            // n_accept[b] of them applied (same arithmetic, same status bits)
+            if (replay)
+                return prefill_common(l, kda ? 1 : 0, pool, n_slots, slot_idx, B, T_max, n_accept, q, k, v,
+                                      in_dtype, alpha, beta, o, out_dtype, status, stream);
             static thread_local rs::StepParamsDamp P;
             fill(P);
             for (size_t i = 0; i < l->pi.size(); ++i) P.pi[i] = (uint8_t)l->pi[i];
@@ -313,6 +323,15 @@ rs_status rs_prefill_update(const rs_layout *l, int32_t per_channel_decay, void 
                             const void *q, const void *k, const void *v, int32_t in_dtype,
                             const float *alpha, const float *beta, void *o, int32_t out_dtype,
                             int32_t *status, void *stream) {
+    return prefill_common(l, per_channel_decay, pool, n_slots, slot_idx, B, L, n_tokens, q, k, v, in_dtype,
+                          alpha, beta, o, out_dtype, status, stream);
+}
+
+static rs_status prefill_common(const rs_layout *l, int32_t per_channel_decay, void *pool, int64_t n_slots,
+                                const int32_t *slot_idx, int32_t B, int32_t L, const int32_t *n_tokens,
+                                const void *q, const void *k, const void *v, int32_t in_dtype,
+                                const float *alpha, const float *beta, void *o, int32_t out_dtype,
+                                int32_t *status, void *stream) {
     if (!l || (per_channel_decay != 0 && per_channel_decay != 1)) return RS_ERR_INVALID_ARG;
     if (B < 0 || L < 0 || n_slots < 0 || n_slots > INT32_MAX) return RS_ERR_INVALID_ARG;
     if (dtype_size(in_dtype) == 0 || (out_dtype != RS_F32 && out_dtype != RS_BF16)) return RS_ERR_INVALID_ARG;
@@ -322,7 +341,6 @@ rs_status rs_prefill_update(const rs_layout *l, int32_t per_channel_decay, void 
     if (!pool || !slot_idx || !q || !k || !v || !alpha || !beta) return RS_ERR_INVALID_ARG;
     if (!aligned16(pool) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(alpha))
         return RS_ERR_MISALIGNED;
-    if (l->group) return RS_ERR_UNSUPPORTED;  // DAMP-exact layout: not built
     rs::StepLaunch Ln;
     Ln.D = D;
     Ln.khi = l->p.kind == RS_LAYOUT_FP32 ? -1 : l->p.k_hi;
@@ -330,7 +348,7 @@ rs_status rs_prefill_update(const rs_layout *l, int32_t per_channel_decay, void 
     Ln.in_dt = in_dtype;
     Ln.out_dt = out_dtype;
     Ln.fused = l->p.kind != RS_LAYOUT_FP32 && l->quant == RS_QUANT_FUSED;
-    static thread_local rs::PrefillParams P;
+    auto fill = [&](rs::PrefillParams &P) {
     P.pool = pool;
     P.n_slots = n_slots;
     P.slot_idx = slot_idx;
@@ -347,7 +365,18 @@ rs_status rs_prefill_update(const rs_layout *l, int32_t per_channel_decay, void 
     P.Hv = Hv;
     P.L = L;
     for (size_t i = 0; i < l->pi.size() && i < (size_t)rs::kMaxRowMap; ++i) P.pi[i] = (uint8_t)l->pi[i];
-    const cudaError_t e = rs::launch_prefill(Ln, P, static_cast<cudaStream_t>(stream));
+    };
+    cudaError_t e;
+    if (l->group) {  // DAMP-exact layout: group scales and value-scaling factors
+        static thread_local rs::PrefillParamsDamp P;
+        fill(P);
+        std::copy(l->cs.begin(), l->cs.end(), P.cs);
+        e = rs::launch_prefill_damp(Ln, P, static_cast<cudaStream_t>(stream));
+    } else {
+        static thread_local rs::PrefillParams P;
+        fill(P);
+        e = rs::launch_prefill(Ln, P, static_cast<cudaStream_t>(stream));
+    }
     if (e != cudaSuccess) return launch_fail(e);
     return RS_OK;
 }

@@ -20,7 +20,12 @@ struct ConvertParamsDamp : ConvertParamsPi {
     float cs[kMaxValueScales];
 };
 
+struct PrefillParamsDamp : PrefillParams {
+    float cs[kMaxValueScales];
+};
+
 cudaError_t launch_step_damp_decode(const StepLaunch &L, StepParamsDamp &P, cudaStream_t s);
+cudaError_t launch_prefill_damp(const StepLaunch &L, PrefillParamsDamp &P, cudaStream_t s);
 cudaError_t launch_convert_damp(int D, int khi, ConvertParamsDamp &P, cudaStream_t s);
 
 }  // namespace rs

@@ -17,7 +17,15 @@
 // registers, so their global-load latency hides behind the current token's
 // two passes; they reach shared memory as per-row vectors in one of two
 // buffers, one group barrier per token.
-#include "rs_step.cuh"
+//
+// DAMP-exact layout (GRP: INT8 groups of 32 values along dv, value scaling;
+// DAMP Appendix A.1, A.3 Eq. 17-18): thread v's column lies in scale group
+// v / 32, which is the thread's warp, so a group's row maximum is one warp
+// max-reduction; the value v is divided by the column's factor c'_v before
+// the error and the readout is multiplied by it.  Multi-token replay on that
+// layout runs through this kernel too (it computes the same thing).
+#include "rs_damp.h"
+#include "rs_quant.cuh"
 #include "../../include/recurrent_state.h"
 
 namespace rs {
@@ -28,21 +36,84 @@ namespace {
 // requantisation scratch of the mixed layout (partial maxima [D/32][D], row
 // scales, their negations and reciprocals [D] each, a flag word) and the
 // requantised tile.
-template <int D, int KHI, bool KDA>
+template <int D, int KHI, bool KDA, bool GRP>
 struct PrefillShape {
     static constexpr bool kMixed = KHI >= 0;
     static constexpr int kKhi = KHI < 0 ? 0 : KHI;
     static constexpr int kNV = KDA ? 5 : 4;  // K, BK, Q, V (+ A)
+    static constexpr int kScales = GRP ? D / kDampGroup : 1;  // INT8 scales per row
     static constexpr int kStateBytes =
-        kMixed ? (2 * kKhi * D + (D - kKhi) * D + 4 * (D - kKhi)) : D * D * 4;
+        kMixed ? (2 * kKhi * D + (D - kKhi) * D + 4 * (D - kKhi) * kScales) : D * D * 4;
     static constexpr int kRowBytes = 2 * kNV * D * 4;
     static constexpr int kScratch = kMixed ? ((D / 32) * D * 4 + 3 * D * 4 + 128) : 0;
     static constexpr int kRegion = (kRowBytes + kScratch + (kMixed ? kStateBytes : 0) + 127) / 128 * 128;
 };
 
-template <int D, int KHI, bool KDA, typename TI, typename TO, bool FUSED>
-__global__ void __launch_bounds__(256, 1) prefill_kernel(const __grid_constant__ PrefillParams P) {
-    using S = PrefillShape<D, KHI, KDA>;
+// DAMP-exact tile: dequantise column tid (group tid / 32) into row pairs;
+// `scales` ([D - KH][D / 32] floats) replaces the tile's scales when given.
+template <int D, int KH>
+__device__ __forceinline__ void damp_dequant(const uint8_t *tile, int tid, float2 (&xs)[D / 2],
+                                             const float *scales) {
+    constexpr int NG = D / kDampGroup;
+    const __half2 *hi = reinterpret_cast<const __half2 *>(tile);
+    const uint32_t *lo = reinterpret_cast<const uint32_t *>(tile + 2 * KH * D);
+    const float *sc = scales ? scales : reinterpret_cast<const float *>(tile + 2 * KH * D + (D - KH) * D);
+    const int gi = tid / kDampGroup;
+#pragma unroll
+    for (int j = 0; j < KH / 2; ++j) xs[j] = __half22float2(hi[j * D + tid]);
+#pragma unroll
+    for (int qd = 0; qd < (D - KH) / 4; ++qd) {
+        const uint32_t w = lo[qd * D + tid] ^ 0x80808080u;
+        const float s0 = sc[(4 * qd) * NG + gi], s1 = sc[(4 * qd + 1) * NG + gi];
+        const float s2 = sc[(4 * qd + 2) * NG + gi], s3 = sc[(4 * qd + 3) * NG + gi];
+        const float f0 = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540));
+        const float f1 = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7541));
+        const float f2 = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7542));
+        const float f3 = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7543));
+        const float2 c01 = __fadd2_rn(make_float2(f0, f1), make_float2(-kCodeBias, -kCodeBias));
+        const float2 c23 = __fadd2_rn(make_float2(f2, f3), make_float2(-kCodeBias, -kCodeBias));
+        xs[KH / 2 + 2 * qd] = __fmul2_rn(c01, make_float2(s0, s1));
+        xs[KH / 2 + 2 * qd + 1] = __fmul2_rn(c23, make_float2(s2, s3));
+    }
+}
+
+// DAMP-exact tile: requantise column tid from its row pairs into `out`
+// (shared memory, the tile's byte layout).  The group of column tid is the
+// thread's warp: a row's group maximum is one warp max-reduction; every lane
+// forms the same scale, lane 0 stores it.  Codes: the IEEE quotient, or the
+// fused arithmetic's one-rounding product (groups with a non-finite maximum
+// keep the quotient).
+template <int D, int KH, bool FUSED>
+__device__ __forceinline__ void damp_requant(const float2 (&xs)[D / 2], uint8_t *out, int tid, int lane) {
+    constexpr int NG = D / kDampGroup;
+    __half2 *hi = reinterpret_cast<__half2 *>(out);
+    uint32_t *lo = reinterpret_cast<uint32_t *>(out + 2 * KH * D);
+    float *sc = reinterpret_cast<float *>(out + 2 * KH * D + (D - KH) * D);
+    const int gi = tid / kDampGroup;
+#pragma unroll
+    for (int j = 0; j < KH / 2; ++j) hi[j * D + tid] = __floats2half2_rn(xs[j].x, xs[j].y);
+#pragma unroll
+    for (int qd = 0; qd < (D - KH) / 4; ++qd) {
+        const float xr[4] = {xs[KH / 2 + 2 * qd].x, xs[KH / 2 + 2 * qd].y, xs[KH / 2 + 2 * qd + 1].x,
+                             xs[KH / 2 + 2 * qd + 1].y};
+        uint32_t word = 0u;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float a = warp_max_abs_nan(xr[i]);
+            const float sv = row_scale_from_absmax(a);
+            uint32_t c;
+            if constexpr (FUSED) c = quant_rcp_or_exact(xr[i], sv, a <= 3.402823466e38f ? __frcp_rn(sv) : 0.0f);
+            else c = quant_exact(xr[i], sv);
+            word |= c << (8 * i);
+            if (lane == 0) sc[(4 * qd + i) * NG + gi] = sv;
+        }
+        lo[qd * D + tid] = word;
+    }
+}
+
+template <int D, int KHI, bool KDA, typename TI, typename TO, bool FUSED, bool GRP, typename PT>
+__global__ void __launch_bounds__(256, 1) prefill_kernel(const __grid_constant__ PT P) {
+    using S = PrefillShape<D, KHI, KDA, GRP>;
     constexpr bool MIXED = S::kMixed;
     constexpr int KH = S::kKhi;
     constexpr int DP = D / 2;
@@ -87,6 +158,8 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const __grid_constant__
         }
         if (n == 0) continue;
         const int src = MIXED ? (int)P.pi[h * D + tid] : tid;  // key channel of physical row tid
+        float csv = 1.0f;  // DAMP-exact: the value-scaling factor c'_v of column tid
+        if constexpr (GRP) csv = P.cs[h * D + tid];
 
         // inputs of token t for row tid (key channel src) and value tid
         auto load_tok = [&](int t, float &kf, float &qf, float &vf, float &af, float &bt) {
@@ -102,7 +175,7 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const __grid_constant__
             rv[tid] = kf;
             rv[D + tid] = __fmul_rn(bt, kf);
             rv[2 * D + tid] = qf;
-            rv[3 * D + tid] = vf;
+            rv[3 * D + tid] = GRP ? __fdiv_rn(vf, csv) : vf;  // DAMP-exact: v' = v / c'
             if (KDA) rv[4 * D + tid] = af;
         };
 
@@ -120,6 +193,21 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const __grid_constant__
             const float *st = reinterpret_cast<const float *>(tile);
 #pragma unroll
             for (int j = 0; j < DP; ++j) x[j] = make_float2(st[(2 * j) * D + tid], st[(2 * j + 1) * D + tid]);
+        } else if constexpr (GRP) {
+            float *dsc = nullptr;
+            if constexpr (FUSED) {  // token 0's decay of INT8 row tid into its group scales
+                if (tid >= KH) {
+                    constexpr int NG = D / kDampGroup;
+                    const float *sc0 = reinterpret_cast<const float *>(tile + 2 * KH * D + (D - KH) * D);
+                    const float a_u = KDA ? rowv[4 * D + tid] : a_cur;
+#pragma unroll
+                    for (int gi = 0; gi < NG; ++gi)
+                        red[(tid - KH) * NG + gi] = __fmul_rn(sc0[(tid - KH) * NG + gi], a_u);
+                }
+                group_sync(bar_id, D);
+                dsc = red;
+            }
+            damp_dequant<D, KH>(tile, tid, x, dsc);
         } else if constexpr (FUSED) {
             // fused arithmetic: token 0's decay of INT8 row u goes into its
             // scale, RN(s_u a_u), so dequantising gives c * RN(s_u a_u) and
@@ -170,7 +258,7 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const __grid_constant__
                 o = __fmaf_rn(x[j + 1].x, qq.z, o);
                 o = __fmaf_rn(x[j + 1].y, qq.w, o);
             }
-            if (og) store_from_f32<TO>(og + (((size_t)b * L + t) * Hv + h) * D + tid, o);
+            if (og) store_from_f32<TO>(og + (((size_t)b * L + t) * Hv + h) * D + tid, GRP ? __fmul_rn(csv, o) : o);
             if (more) {
                 // buffer (t + 1) & 1 was last read by token t - 1, finished
                 // before the previous barrier
@@ -189,6 +277,12 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const __grid_constant__
                 st[(2 * j) * D + tid] = x[j].x;
                 st[(2 * j + 1) * D + tid] = x[j].y;
             }
+        } else if constexpr (GRP) {
+            damp_requant<D, KH, FUSED>(x, outt, tid, lane);
+            group_sync(bar_id, D);  // the requantised tile is complete
+            uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+            const uint4 *s4 = reinterpret_cast<const uint4 *>(outt);
+            for (int i = tid; i < S::kStateBytes / 16; i += D) d4[i] = s4[i];
         } else {
             float mine[D / 32];
 #pragma unroll
@@ -208,11 +302,11 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const __grid_constant__
     }
 }
 
-template <int D, int KHI, bool KDA, typename TI, typename TO, bool FUSED>
-cudaError_t run(PrefillParams &P, cudaStream_t s) {
-    using Sh = PrefillShape<D, KHI, KDA>;
+template <int D, int KHI, bool KDA, typename TI, typename TO, bool FUSED, bool GRP, typename PT>
+cudaError_t run(PT &P, cudaStream_t s) {
+    using Sh = PrefillShape<D, KHI, KDA, GRP>;
     static_assert(Sh::kStateBytes % 16 == 0, "16-byte tile copies");
-    auto kern = prefill_kernel<D, KHI, KDA, TI, TO, FUSED>;
+    auto kern = prefill_kernel<D, KHI, KDA, TI, TO, FUSED, GRP, PT>;
     constexpr int G = 256 / D;
     const int smem = G * Sh::kRegion;
     const int groups_needed = (P.B * P.Hv + G - 1) / G;
@@ -225,23 +319,35 @@ cudaError_t run(PrefillParams &P, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-template <int D, int KHI, bool KDA, bool FUSED>
-cudaError_t by_types(const StepLaunch &L, PrefillParams &P, cudaStream_t s) {
-    if (L.in_dt == RS_BF16 && L.out_dt == RS_F32) return run<D, KHI, KDA, __nv_bfloat16, float, FUSED>(P, s);
+template <int D, int KHI, bool KDA, bool FUSED, bool GRP, typename PT>
+cudaError_t by_types(const StepLaunch &L, PT &P, cudaStream_t s) {
+    if (L.in_dt == RS_BF16 && L.out_dt == RS_F32)
+        return run<D, KHI, KDA, __nv_bfloat16, float, FUSED, GRP>(P, s);
     if (L.in_dt == RS_BF16 && L.out_dt == RS_BF16)
-        return run<D, KHI, KDA, __nv_bfloat16, __nv_bfloat16, FUSED>(P, s);
-    if (L.in_dt == RS_F32 && L.out_dt == RS_F32) return run<D, KHI, KDA, float, float, FUSED>(P, s);
+        return run<D, KHI, KDA, __nv_bfloat16, __nv_bfloat16, FUSED, GRP>(P, s);
+    if (L.in_dt == RS_F32 && L.out_dt == RS_F32) return run<D, KHI, KDA, float, float, FUSED, GRP>(P, s);
     return cudaErrorNotSupported;
+}
+
+template <bool GRP, typename PT>
+cudaError_t by_mode(const StepLaunch &L, PT &P, cudaStream_t s) {
+    if (L.fused) return L.kda ? by_types<128, 16, true, true, GRP>(L, P, s) : by_types<128, 16, false, true, GRP>(L, P, s);
+    return L.kda ? by_types<128, 16, true, false, GRP>(L, P, s) : by_types<128, 16, false, false, GRP>(L, P, s);
 }
 
 }  // namespace
 
 cudaError_t launch_prefill(const StepLaunch &L, PrefillParams &P, cudaStream_t s) {
     if (L.D != 128) return cudaErrorNotSupported;
-    if (L.khi < 0) return L.kda ? by_types<128, -1, true, false>(L, P, s) : by_types<128, -1, false, false>(L, P, s);
+    if (L.khi < 0)
+        return L.kda ? by_types<128, -1, true, false, false>(L, P, s) : by_types<128, -1, false, false, false>(L, P, s);
     if (L.khi != 16) return cudaErrorNotSupported;
-    if (L.fused) return L.kda ? by_types<128, 16, true, true>(L, P, s) : by_types<128, 16, false, true>(L, P, s);
-    return L.kda ? by_types<128, 16, true, false>(L, P, s) : by_types<128, 16, false, false>(L, P, s);
+    return by_mode<false>(L, P, s);
+}
+
+cudaError_t launch_prefill_damp(const StepLaunch &L, PrefillParamsDamp &P, cudaStream_t s) {
+    if (L.D != 128 || L.khi != 16) return cudaErrorNotSupported;
+    return by_mode<true>(L, P, s);
 }
 
 }  // namespace rs

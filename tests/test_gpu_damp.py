@@ -134,12 +134,3 @@ def test_damp_small_batch_bad_slots_and_nonfinite():
     assert np.array_equal(np.isnan(og), np.isnan(orr))
     assert np.array_equal(og[~np.isnan(og)].view(np.uint32), orr[~np.isnan(orr)].view(np.uint32))
 
-
-def test_damp_replay_is_not_offered():
-    f32, damp, pi, cs = layouts(2, 2, seed=1)
-    pool = damp.empty_pool(1)
-    z = torch.zeros((1, 2, 2, D), dtype=torch.bfloat16, device="cuda")
-    with pytest.raises(rs.RsError):
-        rs.spec_replay_update(damp, True, pool, torch.zeros(1, dtype=torch.int32, device="cuda"),
-                              torch.ones(1, dtype=torch.int32, device="cuda"), z, z, z,
-                              torch.ones((1, 2, 2, D), device="cuda"), torch.ones((1, 2, 2), device="cuda"))

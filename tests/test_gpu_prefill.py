@@ -144,11 +144,45 @@ def test_prefill_bad_slot_and_count_reported():
     assert same_bits(after[w.slot_idx[0]], ref[w.slot_idx[0]])
 
 
-def test_prefill_on_damp_layout_is_unsupported():
-    hi = gen.hi_rows(4, D, KHI, seed=1)
-    lay = rs.Layout("damp", D, 4, 4, k_hi=KHI, hi_rows=hi)
-    w = gen.decode_workload(B=2, Hk=4, Hv=4, d=D, steps=2, per_channel=True, in_dtype="bf16", seed=53)
-    qd, kd, vd, ad, bd = replay_inputs(w, 2)
-    pool = lay.empty_pool(w.state0.shape[0])
-    with pytest.raises(rs.RsError):
-        rs.prefill_update(lay, True, pool, dev(w.slot_idx), qd, kd, vd, ad, bd)
+@pytest.mark.parametrize("quant", ["ieee", "fused"])
+@pytest.mark.parametrize("per_channel", [True, False])
+def test_prefill_and_replay_on_damp_layout(quant, per_channel):
+    """DAMP-exact layout (INT8 groups of 32, value scaling): a prefill chunk
+    and a speculative replay both match the oracle's DAMP replay bit for bit."""
+    B, Hk, Hv, L, G = 11, 2, 4, 19, 32
+    seed = 60 + (quant == "fused")
+    w = gen.decode_workload(B=B, Hk=Hk, Hv=Hv, d=D, steps=L, per_channel=per_channel,
+                            in_dtype="bf16", seed=seed, horizon=(2.0, 8192.0))
+    hi = gen.hi_rows(Hv, D, KHI, seed=seed)
+    pi = gen.row_map(hi, D)
+    cs = gen.value_scales(Hv, D, seed=seed)
+    lay = rs.Layout("damp", D, Hv, Hk, k_hi=KHI, hi_rows=hi, value_scales=cs, quant=quant)
+    f32 = rs.Layout("fp32", D, Hv, Hk)
+    mode = 1 if quant == "fused" else 0
+    n_tok = gen.rng(seed).integers(1, L + 1, B).astype(np.int32)
+    n_tok[0], n_tok[1] = 0, L
+    qd, kd, vd, ad, bd = replay_inputs(w, L)
+    q, k, v, a, b = gen.replay_view(w, L)
+    pool = to_mixed(f32, lay, w.state0)
+    o = torch.full((B, L, Hv, D), 2.0, device="cuda")
+    rs.prefill_update(lay, per_channel, pool, dev(w.slot_idx), qd, kd, vd, ad, bd, n_tokens=dev(n_tok), o=o)
+    ref = orc.convert_pool_f32_to_damp(w.state0, KHI, G, pi, cs, mode=mode)
+    o_r = np.full((B, L, Hv, D), 2.0, np.float32)
+    _, st = orc.replay_damp(ref, w.slot_idx, n_tok, pi, cs, KHI, G, D, D, q, k, v, a, b, o=o_r, mode=mode)
+    torch.cuda.synchronize()
+    assert st == 0
+    assert same_bits(host(o), o_r)
+    assert same_bits(host(pool), ref)
+    # replay of up to 8 logged tokens on the same layout
+    T = 8
+    n_acc = np.minimum(n_tok, T).astype(np.int32)
+    qd, kd, vd, ad, bd = replay_inputs(w, T)
+    q, k, v, a, b = gen.replay_view(w, T)
+    o2 = torch.full((B, T, Hv, D), 2.0, device="cuda")
+    rs.spec_replay_update(lay, per_channel, pool, dev(w.slot_idx), dev(n_acc), qd, kd, vd, ad, bd, o=o2)
+    o2_r = np.full((B, T, Hv, D), 2.0, np.float32)
+    _, st = orc.replay_damp(ref, w.slot_idx, n_acc, pi, cs, KHI, G, D, D, q, k, v, a, b, o=o2_r, mode=mode)
+    torch.cuda.synchronize()
+    assert st == 0
+    assert same_bits(host(o2), o2_r)
+    assert same_bits(host(pool), ref)
