@@ -198,8 +198,14 @@ def cpu_baseline(target_seconds=12.0):
     per_pass = max(n * s.per_item / s.threads, 1e-6)
     passes = max(1, int(round(target_seconds / per_pass)))
     dt = sum(s.run(n) for _ in range(passes))
+    # the same oracle on one host thread, about 2 s of work
+    n1 = int(min(s.items, max(1, 2.0 / max(s.per_item, 1e-9))))
+    t0 = time.perf_counter()
+    s.orc.decode_f32(s.pool, s.w.slot_idx, *s.args, o=s.o, items=(0, n1))
+    dt1 = time.perf_counter() - t0
     return {"value": n * passes / dt, "unit": UNIT, "cores": s.threads, "kind": "oracle",
-            "sample": f"{passes} pass(es) over " + s.describe(n), "seconds": dt}
+            "sample": f"{passes} pass(es) over " + s.describe(n), "seconds": dt,
+            "single_thread": {"value": n1 / dt1, "unit": UNIT, "items": n1, "seconds": dt1}}
 
 
 # --------------------------------------------------------------------------
