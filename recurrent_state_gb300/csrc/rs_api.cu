@@ -349,22 +349,22 @@ static rs_status prefill_common(const rs_layout *l, int32_t per_channel_decay, v
     Ln.out_dt = out_dtype;
     Ln.fused = l->p.kind != RS_LAYOUT_FP32 && l->quant == RS_QUANT_FUSED;
     auto fill = [&](rs::PrefillParams &P) {
-    P.pool = pool;
-    P.n_slots = n_slots;
-    P.slot_idx = slot_idx;
-    P.n_tokens = n_tokens;
-    P.q = q;
-    P.k = k;
-    P.v = v;
-    P.alpha = alpha;
-    P.beta = beta;
-    P.o = o;
-    P.status = status;
-    P.B = B;
-    P.Hk = Hk;
-    P.Hv = Hv;
-    P.L = L;
-    for (size_t i = 0; i < l->pi.size() && i < (size_t)rs::kMaxRowMap; ++i) P.pi[i] = (uint8_t)l->pi[i];
+        P.pool = pool;
+        P.n_slots = n_slots;
+        P.slot_idx = slot_idx;
+        P.n_tokens = n_tokens;
+        P.q = q;
+        P.k = k;
+        P.v = v;
+        P.alpha = alpha;
+        P.beta = beta;
+        P.o = o;
+        P.status = status;
+        P.B = B;
+        P.Hk = Hk;
+        P.Hv = Hv;
+        P.L = L;
+        for (size_t i = 0; i < l->pi.size() && i < (size_t)rs::kMaxRowMap; ++i) P.pi[i] = (uint8_t)l->pi[i];
     };
     cudaError_t e;
     if (l->group) {  // DAMP-exact layout: group scales and value-scaling factors

@@ -144,6 +144,24 @@ def test_host_validation_returns_before_launch(L):
              None) == _abi.RS_ERR_INVALID_ARG
     assert r(h, 2, fake, 4, fake, 4, 2, fake, fake, fake, fake, 0, fake, fake, None, 0, None,
              None) == _abi.RS_ERR_INVALID_ARG
+    # prefill: L = 0 or B = 0 is a no-op; negative L, a bad flag, NULL or
+    # misaligned inputs fail before any launch
+    p = L.rs_prefill_update
+    assert p(h, 0, None, 0, None, 4, 0, None, None, None, None, 0, None, None, None, 0, None, None) == 0
+    assert p(h, 0, None, 0, None, 0, 7, None, None, None, None, 0, None, None, None, 0, None, None) == 0
+    assert p(h, 0, fake, 4, fake, 4, -1, None, fake, fake, fake, 0, fake, fake, None, 0, None, None) == \
+        _abi.RS_ERR_INVALID_ARG
+    assert p(h, 3, fake, 4, fake, 4, 5, None, fake, fake, fake, 0, fake, fake, None, 0, None, None) == \
+        _abi.RS_ERR_INVALID_ARG
+    assert p(h, 1, fake, 4, fake, 4, 5, None, fake, None, fake, 0, fake, fake, None, 0, None, None) == \
+        _abi.RS_ERR_INVALID_ARG
+    assert p(h, 1, fake, 4, fake, 4, 5, None, fake, fake, fake, 0, odd, fake, None, 0, None, None) == \
+        _abi.RS_ERR_MISALIGNED
+    # quantisation mode: FP32 layouts take only the IEEE mode
+    assert L.rs_layout_set_quant(h, _abi.RS_QUANT_FUSED) == _abi.RS_ERR_INVALID_ARG
+    assert L.rs_layout_set_quant(h, 7) == _abi.RS_ERR_INVALID_ARG
+    mode = ctypes.c_int32(-1)
+    assert L.rs_layout_quant(h, ctypes.byref(mode)) == 0 and mode.value == _abi.RS_QUANT_IEEE
     L.rs_layout_destroy(h)
 
 
