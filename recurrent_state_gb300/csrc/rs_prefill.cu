@@ -111,8 +111,12 @@ __device__ __forceinline__ void damp_requant(const float2 (&xs)[D / 2], uint8_t 
     }
 }
 
+// Threads per CTA: three groups for the FP32 layout (its requantisation-free
+// code fits the 170 registers that allows), two for the mixed layouts.
+constexpr int prefill_threads(int khi) { return khi < 0 ? 384 : 256; }
+
 template <int D, int KHI, bool KDA, typename TI, typename TO, bool FUSED, bool GRP, typename PT>
-__global__ void __launch_bounds__(256, 1) prefill_kernel(const __grid_constant__ PT P) {
+__global__ void __launch_bounds__(prefill_threads(KHI), 1) prefill_kernel(const __grid_constant__ PT P) {
     using S = PrefillShape<D, KHI, KDA, GRP>;
     constexpr bool MIXED = S::kMixed;
     constexpr int KH = S::kKhi;
@@ -307,7 +311,7 @@ cudaError_t run(PT &P, cudaStream_t s) {
     using Sh = PrefillShape<D, KHI, KDA, GRP>;
     static_assert(Sh::kStateBytes % 16 == 0, "16-byte tile copies");
     auto kern = prefill_kernel<D, KHI, KDA, TI, TO, FUSED, GRP, PT>;
-    constexpr int G = 256 / D;
+    constexpr int G = prefill_threads(KHI) / D;
     const int smem = G * Sh::kRegion;
     const int groups_needed = (P.B * P.Hv + G - 1) / G;
     int grid = device_sm_count();
