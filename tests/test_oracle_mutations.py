@@ -21,6 +21,7 @@ from recurrent_state_gb300 import inputs as gen
 from . import test_oracle_ckpt as ck
 from . import test_oracle_ckpt_int8 as i8
 from . import test_oracle_damp as dm
+from . import test_oracle_error_propagation as ep
 from . import test_oracle_fused as fz
 from . import test_oracle_mixed as mx
 from . import test_oracle_quant as qt
@@ -64,6 +65,7 @@ CHECKS = [
     ("fused_bound", lambda: fz.test_fused_step_within_local_quantisation_error(True)),
     ("fused_replay", lambda: fz.test_fused_replay_one_equals_decode(True)),
     ("damp_fused_unpack", fz.test_damp_unpack_decayed_matches_numpy_float32),
+    ("error_recursion", lambda: ep.test_error_recursion_eq12_eq13(0)),
 ]
 
 READOUT_BLOCK = """    /* readout o = S^T q on the updated state */
