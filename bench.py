@@ -397,11 +397,23 @@ def _time(torch, fn, iters, warm=3):
     return e0.elapsed_time(e1) / 1e3 / iters
 
 
-EXTRA = ("gdn_fp32", "kda_fp32", "kda_mixed", "gdn_mixed", "kda_damp", "replay_mixed", "replay_fp32",
+EXTRA = ("gdn_tiny", "gdn_fp32", "kda_fp32", "kda_mixed", "gdn_mixed", "kda_damp", "replay_mixed", "replay_fp32",
          "kda_mixed_fused", "gdn_mixed_fused", "kda_damp_fused", "replay_mixed_fused",
          "prefill_fp32", "prefill_mixed_fused",
          "pack_gdn", "restore_gdn", "pack_kda", "restore_kda", "pack_int8_gdn", "restore_int8_gdn",
          "pack_int8_kda", "restore_int8_kda", "pack_mixed", "restore_mixed")
+
+
+# The five workload configurations as named presets of secondary kernels:
+# the small GDN case, GDN and KDA decode with FP32 state, KDA on the mixed
+# layout (decode and replay, both requantisation modes), dasc pack/restore.
+PRESETS = {
+    "tiny": ["gdn_tiny"],
+    "gdn": ["gdn_fp32"],
+    "kda": ["kda_fp32"],
+    "kda_mixed": ["kda_mixed", "kda_mixed_fused", "replay_mixed", "replay_mixed_fused"],
+    "ckpt": ["pack_gdn", "restore_gdn", "pack_kda", "restore_kda"],
+}
 
 
 def extra_kernels(args, rs, torch, dev, peak, world, only=None):
@@ -425,6 +437,18 @@ def extra_kernels(args, rs, torch, dev, peak, world, only=None):
             out[name].update(extra)
 
     B = getattr(args, "batch", None) or 256
+    if "gdn_tiny" in want:
+        # small GDN case: B=4, 4 heads, dk=dv=64, FP32 state and inputs (launch-bound; correctness size)
+        w = gen.decode_workload(B=4, Hk=4, Hv=4, d=64, steps=16, per_channel=False, in_dtype="f32", seed=0,
+                                tiny_gdn=True)
+        lay = rs.Layout("fp32", 64, 4, 4)
+        pool = to_dev(w.state0)
+        q, k, v = to_dev(w.q), to_dev(w.k), to_dev(w.v)
+        al, be, slots = to_dev(w.alpha), to_dev(w.beta), to_dev(w.slot_idx)
+        o = torch.empty((4, 4, 64), device=dev)
+        sec = _time(torch, lambda i: rs.gdn_decode_update(lay, pool, slots, q[i % 16], k[i % 16], v[i % 16],
+                                                          al[i % 16], be[i % 16], o=o), iters, warm)
+        rec("gdn_decode_fp32_tiny_b4_d64", sec, decode_bytes(4, 4, 4, 64, lay.head_bytes, 4, False), 16)
     if "gdn_fp32" in want:
         nsteps = 8
         g_cfg = dict(GDN, B=B)
@@ -682,7 +706,11 @@ def main():
                     help="pool slots and checkpoints of the pack/restore kernels (default 64)")
     ap.add_argument("--only", default=None,
                     help="comma list of secondary kernels to time alone (" + ",".join(EXTRA) + ")")
+    ap.add_argument("--config", choices=sorted(PRESETS), default=None,
+                    help="time one workload configuration's kernels alone (a named --only list)")
     args = ap.parse_args()
+    if args.config:
+        args.only = ",".join(PRESETS[args.config] + ([args.only] if args.only else []))
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
