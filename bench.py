@@ -449,6 +449,22 @@ def extra_kernels(args, rs, torch, dev, peak, world, only=None):
         sec = _time(torch, lambda i: rs.gdn_decode_update(lay, pool, slots, q[i % 16], k[i % 16], v[i % 16],
                                                           al[i % 16], be[i % 16], o=o), iters, warm)
         rec("gdn_decode_fp32_tiny_b4_d64", sec, decode_bytes(4, 4, 4, 64, lay.head_bytes, 4, False), 16)
+        # the same 16 steps captured once in a CUDA graph and replayed: launch cost without the
+        # host-side call path
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            for i in range(16):
+                rs.gdn_decode_update(lay, pool, slots, q[i], k[i], v[i], al[i], be[i], o=o)
+        torch.cuda.current_stream(dev).wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i in range(16):
+                rs.gdn_decode_update(lay, pool, slots, q[i], k[i], v[i], al[i], be[i], o=o)
+        sec = _time(torch, lambda i: graph.replay(), max(3, iters // 16), warm) / 16
+        rec("gdn_decode_fp32_tiny_b4_d64_graph", sec, decode_bytes(4, 4, 4, 64, lay.head_bytes, 4, False), 16,
+            {"launches_per_graph": 16})
     if "gdn_fp32" in want:
         nsteps = 8
         g_cfg = dict(GDN, B=B)

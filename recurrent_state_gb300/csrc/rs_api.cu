@@ -80,6 +80,29 @@ DevAttr &attr_for_current() {
 namespace rs {
 int device_sm_count() { return attr_for_current().sms; }
 int device_max_smem_optin() { return attr_for_current().smem; }
+
+cudaError_t set_dynamic_smem(const void *fn, int bytes) {
+    struct Entry {
+        const void *fn;
+        int dev, bytes;
+    };
+    static std::mutex mu;
+    static std::vector<Entry> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(mu);
+    for (Entry &x : done)
+        if (x.fn == fn && x.dev == dev) {
+            if (x.bytes >= bytes) return cudaSuccess;
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+            if (e == cudaSuccess) x.bytes = bytes;
+            return e;
+        }
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.push_back({fn, dev, bytes});
+    return e;
+}
 }  // namespace rs
 
 extern "C" {

@@ -134,4 +134,10 @@ cudaError_t launch_ckpt_restore(const CkptParams &P, cudaStream_t s);
 int device_sm_count();
 int device_max_smem_optin();
 
+// Raise kernel `fn`'s dynamic shared-memory limit to at least `bytes` on the
+// current device.  The attribute call is made only the first time a larger
+// size is needed for (fn, device), so steady-state launches -- including
+// launches recorded into a CUDA graph -- issue none.
+cudaError_t set_dynamic_smem(const void *fn, int bytes);
+
 }  // namespace rs

@@ -317,7 +317,7 @@ cudaError_t run(PT &P, cudaStream_t s) {
     int grid = device_sm_count();
     if (grid > groups_needed) grid = groups_needed;
     if (grid < 1) grid = 1;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = set_dynamic_smem(reinterpret_cast<const void *>(kern), smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, G * D, smem, s>>>(P);
     return cudaGetLastError();

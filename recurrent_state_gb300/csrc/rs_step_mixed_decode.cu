@@ -36,7 +36,7 @@ cudaError_t run(StepParamsPi &P, cudaStream_t s) {
     P.region_bytes = Sh::kStage;
     P.stages = NS;
     const int smem = header + NSLOT * Sh::kSlotBytes + NS * Sh::kStage;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = set_dynamic_smem(reinterpret_cast<const void *>(kern), smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, W * 32, smem, s>>>(P);
     return cudaGetLastError();

@@ -24,7 +24,7 @@ cudaError_t run(StepParamsPi &P, cudaStream_t s) {
     P.header_bytes = header;
     P.region_bytes = region;
     const int smem = header + G * region;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = set_dynamic_smem(reinterpret_cast<const void *>(kern), smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, G * D, smem, s>>>(P);
     return cudaGetLastError();
