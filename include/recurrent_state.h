@@ -213,7 +213,10 @@ rs_status rs_layout_bits_per_value(const rs_layout *l, double *bits);
  *   beta      device  float [B][Hv]               write strength
  *   o         device  out_dtype [B][Hv][dv]        readout (may be NULL)
  *   status    device  int32 (may be NULL)
- * in_dtype: RS_F32, RS_BF16 or RS_F16; out_dtype: RS_F32 or RS_BF16.
+ * in_dtype and out_dtype: built for bf16 -> f32, f32 -> f32 and, at
+ * dk = 128, bf16 -> bf16 (o rounded once from FP32, nearest even); other
+ * combinations (RS_F16 inputs among them) return RS_ERR_UNSUPPORTED before
+ * any launch.
  * B = 0 is a no-op. */
 rs_status rs_gdn_decode_update(const rs_layout *l, void *pool, int64_t n_slots,
                                const int32_t *slot_idx, int32_t B,

@@ -70,6 +70,7 @@ def test_tiny_gdn_all_steps():
 
 @pytest.mark.parametrize("per_channel,Hk,Hv,in_dtype,d", [
     (False, 4, 8, "bf16", 128),
+    (False, 2, 8, "bf16", 128),    # four value heads per key head
     (True, 8, 8, "bf16", 128),
     (False, 2, 4, "f32", 64),
     (True, 4, 4, "f32", 64),

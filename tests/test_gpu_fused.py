@@ -71,9 +71,9 @@ def test_fused_convert_matches_oracle_near_half_integers():
     assert not np.array_equal(ieee[..., hb:], ref[..., hb:])
 
 
-@pytest.mark.parametrize("per_channel", [True, False])
-def test_fused_decode_every_tile(per_channel):
-    B, Hk, Hv = 97, 4, 8
+@pytest.mark.parametrize("per_channel,Hk", [(True, 4), (False, 4), (False, 2)])
+def test_fused_decode_every_tile(per_channel, Hk):
+    B, Hv = 97, 8
     f32, lay, pi, _ = layouts(Hv, Hk, seed=5)
     w = gen.decode_workload(B=B, Hk=Hk, Hv=Hv, d=D, steps=6, per_channel=per_channel,
                             in_dtype="bf16", seed=5, horizon=(2.0, 8192.0))
