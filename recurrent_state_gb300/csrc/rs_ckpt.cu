@@ -11,8 +11,10 @@
 // of a unit possibly shorter: a mixed FP16/INT8 head of 18,880 B is 36
 // chunks and 448 B); a warp moves one chunk per step with one 16-byte load
 // and one 16-byte store per lane,
-// and each warp keeps kChunks chunks in flight so that enough bytes are
-// outstanding per SM to cover HBM latency.  Pack reads ragged source units
+// and each warp keeps several chunks in flight so that enough bytes are
+// outstanding per SM to cover HBM latency: four for pack, eight for restore,
+// whose chunks wait on an index-table lookup before their load (measured at
+// batch 64: restore 15% faster with eight, pack slower).  Pack reads ragged source units
 // and writes the checkpoint contiguously; restore walks the destination
 // contiguously, so its writes (the larger side) are fully sequential.
 #include "rs_internal.h"
@@ -23,7 +25,7 @@ namespace rs {
 namespace {
 
 constexpr int kChunkBytes = 512;
-constexpr int kChunks = 4;  // chunks in flight per warp
+__host__ __device__ constexpr int chunks_in_flight(bool pack) { return pack ? 4 : 8; }  // per warp
 
 struct Chunk {
     const uint4 *src;  // nullptr: write zeros
@@ -101,6 +103,7 @@ __device__ __forceinline__ Chunk restore_chunk(const CkptParams &P, int32_t s, i
 template <bool PACK>
 __global__ void __launch_bounds__(256) ckpt_kernel(const __grid_constant__ CkptParams P,
                                                    uint32_t chunks_per_pair, Split sp) {
+    constexpr int kChunks = chunks_in_flight(PACK);
     const int lane = threadIdx.x & 31;
     const int i = blockIdx.y;
     const int32_t ps = P.pool_slots[i], cs = P.ckpt_slots[i];
@@ -144,10 +147,11 @@ cudaError_t launch(const CkptParams &P, bool pack, cudaStream_t s) {
     const int64_t per_pair = units * cpu;
     if (per_pair >= (1ll << 31) || P.n > 65535) return cudaErrorNotSupported;
     if (per_pair == 0 || P.n == 0) return cudaSuccess;
+    const int kChunks = chunks_in_flight(pack);
     const int64_t warps_needed = (per_pair + kChunks - 1) / kChunks;
     int64_t bx = (warps_needed * 32 + 255) / 256;
-    // about 8 CTAs of 8 warps per SM over the whole grid
-    int64_t cap = ((int64_t)device_sm_count() * 8 + P.n - 1) / P.n;
+    // up to 16 CTAs of 8 warps per SM over the whole grid
+    int64_t cap = ((int64_t)device_sm_count() * 16 + P.n - 1) / P.n;
     if (cap < 1) cap = 1;
     if (bx > cap) bx = cap;
     dim3 grid((unsigned)bx, (unsigned)P.n);

@@ -196,7 +196,10 @@ template <bool PACK> cudaError_t launch(const Int8CkptParams &P, cudaStream_t s)
     if (rows == 0 || P.n == 0) return cudaSuccess;
     const int64_t warps_needed = (rows + kRows - 1) / kRows;
     int64_t bx = (warps_needed * 32 + 255) / 256;
-    int64_t cap = ((int64_t)device_sm_count() * 8 + P.n - 1) / P.n;  // ~8 CTAs of 8 warps per SM
+    // CTAs of 8 warps per SM over the whole grid: 8 for pack, 16 for restore
+    // (restore's writes are the larger side; measured faster with more warps)
+    const int64_t per_sm = PACK ? 8 : 16;
+    int64_t cap = ((int64_t)device_sm_count() * per_sm + P.n - 1) / P.n;
     if (cap < 1) cap = 1;
     if (bx > cap) bx = cap;
     dim3 grid((unsigned)bx, (unsigned)P.n);
