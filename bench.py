@@ -398,7 +398,7 @@ def _time(torch, fn, iters, warm=3):
 
 
 EXTRA = ("gdn_tiny", "gdn_fp32", "kda_fp32", "kda_mixed", "gdn_mixed", "kda_damp", "replay_mixed", "replay_fp32",
-         "kda_mixed_fused", "gdn_mixed_fused", "kda_damp_fused", "replay_mixed_fused",
+         "kda_mixed_fused", "gdn_mixed_fused", "kda_damp_fused", "replay_mixed_fused", "replay_sweep",
          "prefill_fp32", "prefill_mixed_fused",
          "pack_gdn", "restore_gdn", "pack_kda", "restore_kda", "pack_int8_gdn", "restore_int8_gdn",
          "pack_int8_kda", "restore_int8_kda", "pack_mixed", "restore_mixed")
@@ -411,7 +411,7 @@ PRESETS = {
     "tiny": ["gdn_tiny"],
     "gdn": ["gdn_fp32"],
     "kda": ["kda_fp32"],
-    "kda_mixed": ["kda_mixed", "kda_mixed_fused", "replay_mixed", "replay_mixed_fused"],
+    "kda_mixed": ["kda_mixed", "kda_mixed_fused", "replay_mixed", "replay_mixed_fused", "replay_sweep"],
     "ckpt": ["pack_gdn", "restore_gdn", "pack_kda", "restore_kda"],
 }
 
@@ -483,7 +483,7 @@ def extra_kernels(args, rs, torch, dev, peak, world, only=None):
         torch.cuda.empty_cache()
     KDA_B = dict(KDA, B=B)
     MIXED_KEYS = {"kda_fp32", "kda_mixed", "gdn_mixed", "kda_damp", "replay_mixed", "replay_fp32",
-                  "kda_mixed_fused", "gdn_mixed_fused", "kda_damp_fused", "replay_mixed_fused"}
+                  "kda_mixed_fused", "gdn_mixed_fused", "kda_damp_fused", "replay_mixed_fused", "replay_sweep"}
     if want & MIXED_KEYS:
         nsteps = 8
         w = gen.decode_workload(steps=nsteps, per_channel=True, in_dtype="bf16", seed=1,
@@ -547,7 +547,7 @@ def extra_kernels(args, rs, torch, dev, peak, world, only=None):
                 decode_bytes(B, 32, 32, 128, damp.head_bytes, 2, True), B * 32,
                 {"bits_per_value": damp.bits_per_value(), "quant": quant})
             del dpool
-        if want & {"replay_mixed", "replay_fp32", "replay_mixed_fused"}:
+        if want & {"replay_mixed", "replay_fp32", "replay_mixed_fused", "replay_sweep"}:
             T = 8
             n_acc = gen.n_accept(B, T, seed=1)
             tok = int(n_acc.sum())
@@ -574,6 +574,16 @@ def extra_kernels(args, rs, torch, dev, peak, world, only=None):
                     f32, True, pool, slots, nd, rq, rk, rv, ra, rb, o=ro), iters, warm)
                 rec(f"kda_replay_fp32_b{B}_T8", sec, 2 * B * 32 * f32.head_bytes + tok * per_tok,
                     tok * 32, {"accepted_tokens": tok})
+            if "replay_sweep" in want:
+                # every sequence accepts exactly Tn tokens of the 8-token window, both layouts' mixed modes
+                for Tn in (1, 2, 4, 8):
+                    nfix = torch.full((B,), Tn, dtype=torch.int32, device=dev)
+                    for lay, qname in ((mix, "ieee"), (mixf, "fused")):
+                        sec = _time(torch, lambda i: rs.spec_replay_update(
+                            lay, True, mpool, slots, nfix, rq, rk, rv, ra, rb, o=ro), iters, warm)
+                        rec(f"kda_replay_mixed_{qname}_b{B}_n{Tn}", sec,
+                            2 * B * 32 * mix.head_bytes + B * Tn * per_tok, B * Tn * 32,
+                            {"accepted_tokens": B * Tn, "n_accept": f"all {Tn}", "quant": qname})
         del pool, mpool
         torch.cuda.empty_cache()
 
