@@ -429,10 +429,19 @@ def extra_kernels(args, rs, torch, dev, peak, world, only=None):
     def to_bf16(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
 
-    def rec(name, sec, alg, updates, extra=None):
+    # FP32 pipe peak for the multi-token kernels, whose arithmetic per state byte is 4.5-32x a decode
+    # step's: every SM's 128 FP32 lanes retiring one FMA (2 FLOP) per cycle at the 2,070 MHz maximum
+    # SM clock.  Their FP32 work per state element and token is 7 FLOP (decay multiply, and the FMAs of
+    # the prediction, the write and the readout).
+    fp32_peak = torch.cuda.get_device_properties(dev).multi_processor_count * 128 * 2 * 2.07e9
+
+    def rec(name, sec, alg, updates, extra=None, tile_tokens=None):
         gbs = alg / sec / 1e9
         out[name] = {"ms": sec * 1e3, "GB/s": gbs, "frac_of_peak": gbs / peak,
                      "algorithmic_bytes": alg, "state_updates_per_s": updates / sec if updates else None}
+        if tile_tokens:
+            fl = tile_tokens * 128 * 128 * 7
+            out[name].update({"fp32_flops": fl, "TFLOP/s": fl / sec / 1e12, "frac_of_fp32_peak": fl / sec / fp32_peak})
         if extra:
             out[name].update(extra)
 
@@ -563,17 +572,18 @@ def extra_kernels(args, rs, torch, dev, peak, world, only=None):
                 sec = _time(torch, lambda i: rs.spec_replay_update(
                     mix, True, mpool, slots, nd, rq, rk, rv, ra, rb, o=ro), iters, warm)
                 rec(f"kda_replay_mixed_b{B}_T8", sec, 2 * B * 32 * mix.head_bytes + tok * per_tok,
-                    tok * 32, {"accepted_tokens": tok, "n_accept": "uniform 1..8"})
+                    tok * 32, {"accepted_tokens": tok, "n_accept": "uniform 1..8"}, tile_tokens=tok * 32)
             if "replay_mixed_fused" in want:
                 sec = _time(torch, lambda i: rs.spec_replay_update(
                     mixf, True, mpool, slots, nd, rq, rk, rv, ra, rb, o=ro), iters, warm)
                 rec(f"kda_replay_mixed_fused_b{B}_T8", sec, 2 * B * 32 * mix.head_bytes + tok * per_tok,
-                    tok * 32, {"accepted_tokens": tok, "n_accept": "uniform 1..8", "quant": "fused"})
+                    tok * 32, {"accepted_tokens": tok, "n_accept": "uniform 1..8", "quant": "fused"},
+                    tile_tokens=tok * 32)
             if "replay_fp32" in want:
                 sec = _time(torch, lambda i: rs.spec_replay_update(
                     f32, True, pool, slots, nd, rq, rk, rv, ra, rb, o=ro), iters, warm)
                 rec(f"kda_replay_fp32_b{B}_T8", sec, 2 * B * 32 * f32.head_bytes + tok * per_tok,
-                    tok * 32, {"accepted_tokens": tok})
+                    tok * 32, {"accepted_tokens": tok}, tile_tokens=tok * 32)
             if "replay_sweep" in want:
                 # every sequence accepts exactly Tn tokens of the 8-token window, both layouts' mixed modes
                 for Tn in (1, 2, 4, 8):
@@ -583,7 +593,8 @@ def extra_kernels(args, rs, torch, dev, peak, world, only=None):
                             lay, True, mpool, slots, nfix, rq, rk, rv, ra, rb, o=ro), iters, warm)
                         rec(f"kda_replay_mixed_{qname}_b{B}_n{Tn}", sec,
                             2 * B * 32 * mix.head_bytes + B * Tn * per_tok, B * Tn * 32,
-                            {"accepted_tokens": B * Tn, "n_accept": f"all {Tn}", "quant": qname})
+                            {"accepted_tokens": B * Tn, "n_accept": f"all {Tn}", "quant": qname},
+                            tile_tokens=B * Tn * 32)
         del pool, mpool
         torch.cuda.empty_cache()
 
@@ -606,7 +617,7 @@ def extra_kernels(args, rs, torch, dev, peak, world, only=None):
             sec = _time(torch, lambda i: rs.prefill_update(f32, True, pool, slots, pq, pk, pv, pa, pb, o=po),
                         max(3, iters // 10), warm)
             rec(f"kda_prefill_fp32_b{B}_L{Lc}", sec, 2 * B * 32 * f32.head_bytes + B * Lc * per_tok,
-                B * 32 * Lc, {"chunk_tokens": Lc})
+                B * 32 * Lc, {"chunk_tokens": Lc}, tile_tokens=B * 32 * Lc)
         if "prefill_mixed_fused" in want:
             hi = gen.hi_rows(KDA["Hv"], 128, 16, seed=3)
             mixf = rs.Layout("mixed", 128, KDA["Hv"], KDA["Hk"], k_hi=16, hi_rows=hi, quant="fused")
@@ -615,7 +626,7 @@ def extra_kernels(args, rs, torch, dev, peak, world, only=None):
             sec = _time(torch, lambda i: rs.prefill_update(mixf, True, mpool, slots, pq, pk, pv, pa, pb, o=po),
                         max(3, iters // 10), warm)
             rec(f"kda_prefill_mixed_fused_b{B}_L{Lc}", sec, 2 * B * 32 * mixf.head_bytes + B * Lc * per_tok,
-                B * 32 * Lc, {"chunk_tokens": Lc, "quant": "fused"})
+                B * 32 * Lc, {"chunk_tokens": Lc, "quant": "fused"}, tile_tokens=B * 32 * Lc)
             del mpool
         del pool, pq, pk, pv, pa, pb, po
         torch.cuda.empty_cache()
