@@ -9,11 +9,13 @@
 
 namespace rs {
 
-// Upper bound on polls of one mbarrier wait.  Each try_wait suspends the
-// thread for up to a hardware-chosen time slice, so this bounds a wait to
-// seconds; a wait that runs out reports RS_DEV_PIPE_TIMEOUT and the kernel
-// returns instead of spinning forever.
-constexpr uint32_t kWaitPollLimit = 1u << 24;
+// Upper bound on polls of one mbarrier wait.  Each try_wait that finds the
+// phase incomplete suspends the thread for a hardware-chosen time slice --
+// about 3.8 us on GB300 (7,800 cycles, measured by tests/c/wait_timeout.cu)
+// -- so this bounds a wait to about a second, while a stage's bulk copy
+// lands in microseconds; a wait that runs out reports RS_DEV_PIPE_TIMEOUT and
+// the kernel returns instead of spinning forever.
+constexpr uint32_t kWaitPollLimit = 1u << 18;
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -53,9 +55,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity to complete.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kWaitPollLimit; ++i)
+// Bounded wait for the phase with the given parity to complete: false once
+// `limit` polls have found it incomplete.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  uint32_t limit = kWaitPollLimit) {
+    for (uint32_t i = 0; i < limit; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     return false;
 }
