@@ -213,10 +213,10 @@ rs_status rs_layout_bits_per_value(const rs_layout *l, double *bits);
  *   beta      device  float [B][Hv]               write strength
  *   o         device  out_dtype [B][Hv][dv]        readout (may be NULL)
  *   status    device  int32 (may be NULL)
- * in_dtype and out_dtype: built for bf16 -> f32, f32 -> f32 and, at
- * dk = 128, bf16 -> bf16 (o rounded once from FP32, nearest even); other
- * combinations (RS_F16 inputs among them) return RS_ERR_UNSUPPORTED before
- * any launch.
+ * in_dtype and out_dtype: built for bf16 -> f32, f16 -> f32, f32 -> f32
+ * and, at dk = 128, bf16 -> bf16 (o rounded once from FP32, nearest even);
+ * bf16 and f16 inputs widen to FP32 exactly.  Other combinations (f16 -> bf16
+ * among them) return RS_ERR_UNSUPPORTED before any launch.
  * B = 0 is a no-op. */
 rs_status rs_gdn_decode_update(const rs_layout *l, void *pool, int64_t n_slots,
                                const int32_t *slot_idx, int32_t B,

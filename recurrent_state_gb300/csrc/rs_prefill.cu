@@ -330,6 +330,7 @@ cudaError_t by_types(const StepLaunch &L, PT &P, cudaStream_t s) {
     if (L.in_dt == RS_BF16 && L.out_dt == RS_BF16)
         return run<D, KHI, KDA, __nv_bfloat16, __nv_bfloat16, FUSED, GRP>(P, s);
     if (L.in_dt == RS_F32 && L.out_dt == RS_F32) return run<D, KHI, KDA, float, float, FUSED, GRP>(P, s);
+    if (L.in_dt == RS_F16 && L.out_dt == RS_F32) return run<D, KHI, KDA, __half, float, FUSED, GRP>(P, s);
     return cudaErrorNotSupported;
 }
 

@@ -33,6 +33,7 @@ template <int D, bool KDA, int MAXT>
 cudaError_t by_types(const StepLaunch &L, StepParams &P, cudaStream_t s) {
     if (L.in_dt == RS_BF16 && L.out_dt == RS_F32) return run<D, KDA, MAXT, __nv_bfloat16, float>(P, s);
     if (L.in_dt == RS_F32 && L.out_dt == RS_F32) return run<D, KDA, MAXT, float, float>(P, s);
+    if (L.in_dt == RS_F16 && L.out_dt == RS_F32) return run<D, KDA, MAXT, __half, float>(P, s);
     if (D == 128 && L.in_dt == RS_BF16 && L.out_dt == RS_BF16)
         return run<D, KDA, MAXT, __nv_bfloat16, __nv_bfloat16>(P, s);
     return cudaErrorNotSupported;

@@ -48,6 +48,7 @@ cudaError_t by_types(const StepLaunch &L, StepParamsPi &P, cudaStream_t s) {
     if (L.in_dt == RS_BF16 && L.out_dt == RS_BF16)
         return run<128, 16, KDA, __nv_bfloat16, __nv_bfloat16, FUSED>(P, s);
     if (L.in_dt == RS_F32 && L.out_dt == RS_F32) return run<128, 16, KDA, float, float, FUSED>(P, s);
+    if (L.in_dt == RS_F16 && L.out_dt == RS_F32) return run<128, 16, KDA, __half, float, FUSED>(P, s);
     return cudaErrorNotSupported;
 }
 

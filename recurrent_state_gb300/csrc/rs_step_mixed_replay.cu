@@ -37,6 +37,8 @@ cudaError_t by_types(const StepLaunch &L, StepParamsPi &P, cudaStream_t s) {
     if (L.in_dt == RS_BF16 && L.out_dt == RS_BF16)
         return run<128, 16, KDA, kMaxTokens, __nv_bfloat16, __nv_bfloat16, FUSED>(P, s);
     if (L.in_dt == RS_F32 && L.out_dt == RS_F32) return run<128, 16, KDA, kMaxTokens, float, float, FUSED>(P, s);
+    if (L.in_dt == RS_F16 && L.out_dt == RS_F32)
+        return run<128, 16, KDA, kMaxTokens, __half, float, FUSED>(P, s);
     return cudaErrorNotSupported;
 }
 

@@ -99,6 +99,10 @@ def _qkv(g, steps, B, Hk, Hv, dk, dv, in_dtype):
     if in_dtype == "bf16":
         qb, kb, vb = bf16_bits(q), bf16_bits(k), bf16_bits(v)
         return bf16_to_f32(qb), bf16_to_f32(kb), bf16_to_f32(vb), qb, kb, vb
+    if in_dtype == "f16":  # IEEE half, nearest even; the widened values are what both sides see
+        qh, kh, vh = (x.astype(np.float16) for x in (q, k, v))
+        return (qh.astype(np.float32), kh.astype(np.float32), vh.astype(np.float32),
+                qh.view(np.uint16), kh.view(np.uint16), vh.view(np.uint16))
     return q, k, v, None, None, None
 
 

@@ -28,14 +28,27 @@ def dev_bf16(bits: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
 
 
+def dev_f16(bits: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.float16)).cuda()
+
+
+def dev_in(w: gen.DecodeInputs, bits: np.ndarray, values: np.ndarray) -> torch.Tensor:
+    """A q, k or v tensor in the workload's input dtype."""
+    if w.in_dtype == "bf16":
+        return dev_bf16(bits)
+    if w.in_dtype == "f16":
+        return dev_f16(bits)
+    return dev(values)
+
+
 def host(t: torch.Tensor) -> np.ndarray:
     return t.detach().cpu().numpy()
 
 
 def step_inputs(w: gen.DecodeInputs, t: int):
     """Device tensors (q, k, v, alpha, beta) for decode step t."""
-    if w.in_dtype == "bf16":
-        q, k, v = dev_bf16(w.q_bits[t]), dev_bf16(w.k_bits[t]), dev_bf16(w.v_bits[t])
+    if w.in_dtype in ("bf16", "f16"):
+        q, k, v = (dev_in(w, b[t], None) for b in (w.q_bits, w.k_bits, w.v_bits))
     else:
         q, k, v = dev(w.q[t]), dev(w.k[t]), dev(w.v[t])
     return q, k, v, dev(w.alpha[t]), dev(w.beta[t])
@@ -45,8 +58,8 @@ def replay_inputs(w: gen.DecodeInputs, T_max: int):
     """Device tensors [B][T_max][...] from the first T_max steps."""
     def bt(x):
         return np.ascontiguousarray(np.swapaxes(x[:T_max], 0, 1))
-    if w.in_dtype == "bf16":
-        q, k, v = dev_bf16(bt(w.q_bits)), dev_bf16(bt(w.k_bits)), dev_bf16(bt(w.v_bits))
+    if w.in_dtype in ("bf16", "f16"):
+        q, k, v = (dev_in(w, bt(b), None) for b in (w.q_bits, w.k_bits, w.v_bits))
     else:
         q, k, v = dev(bt(w.q)), dev(bt(w.k)), dev(bt(w.v))
     return q, k, v, dev(bt(w.alpha)), dev(bt(w.beta))

@@ -157,8 +157,8 @@ def test_host_validation_returns_before_launch(L):
         _abi.RS_ERR_INVALID_ARG
     assert p(h, 1, fake, 4, fake, 4, 5, None, fake, fake, fake, 0, odd, fake, None, 0, None, None) == \
         _abi.RS_ERR_MISALIGNED
-    # fp16 inputs are declared in the enum but not built: refused before any launch
-    assert f(h, fake, 4, fake, 4, fake, fake, fake, _abi.RS_F16, fake, fake, None, 0, None, None) == \
+    # fp16 inputs with a bf16 readout are not built: refused before any launch
+    assert f(h, fake, 4, fake, 4, fake, fake, fake, _abi.RS_F16, fake, fake, None, _abi.RS_BF16, None, None) == \
         _abi.RS_ERR_UNSUPPORTED
     # quantisation mode: FP32 layouts take only the IEEE mode
     assert L.rs_layout_set_quant(h, _abi.RS_QUANT_FUSED) == _abi.RS_ERR_INVALID_ARG
