@@ -383,7 +383,14 @@ def job_value(world, steps, units_per_step, dt_max):
     return world * steps * units_per_step / dt_max
 
 
-def _time(torch, fn, iters, warm=3):
+# Median of the per-launch times of the last _time call (s) and its repeat count.
+_LAST_MEDIAN = {"s": None, "n": 0}
+
+
+def _time(torch, fn, iters, warm=3, repeats=20):
+    """Mean seconds per launch over ``iters`` back-to-back launches (CUDA events
+    around the window); also times ``max(repeats, 20)`` launches one by one,
+    each between its own pair of events, and keeps their median."""
     warm = max(3, warm)
     for i in range(warm):
         fn(i)
@@ -394,7 +401,17 @@ def _time(torch, fn, iters, warm=3):
         fn(warm + i)
     e1.record()
     torch.cuda.synchronize()
-    return e0.elapsed_time(e1) / 1e3 / iters
+    mean = e0.elapsed_time(e1) / 1e3 / iters
+    n = max(repeats, 20)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for i, (a, b) in enumerate(ev):
+        a.record()
+        fn(warm + iters + i)
+        b.record()
+    torch.cuda.synchronize()
+    per = sorted(a.elapsed_time(b) / 1e3 for a, b in ev)
+    _LAST_MEDIAN["s"], _LAST_MEDIAN["n"] = per[n // 2], n
+    return mean
 
 
 EXTRA = ("gdn_tiny", "gdn_fp32", "kda_fp32", "kda_mixed", "gdn_mixed", "kda_damp", "replay_mixed", "replay_fp32",
@@ -439,6 +456,9 @@ def extra_kernels(args, rs, torch, dev, peak, world, only=None):
         gbs = alg / sec / 1e9
         out[name] = {"ms": sec * 1e3, "GB/s": gbs, "frac_of_peak": gbs / peak,
                      "algorithmic_bytes": alg, "state_updates_per_s": updates / sec if updates else None}
+        if _LAST_MEDIAN["s"] is not None:
+            out[name].update({"ms_median": _LAST_MEDIAN["s"] * 1e3, "median_of": _LAST_MEDIAN["n"]})
+            _LAST_MEDIAN["s"] = None
         if tile_tokens:
             fl = tile_tokens * 128 * 128 * 7
             out[name].update({"fp32_flops": fl, "TFLOP/s": fl / sec / 1e12, "frac_of_fp32_peak": fl / sec / fp32_peak})
@@ -472,6 +492,7 @@ def extra_kernels(args, rs, torch, dev, peak, world, only=None):
             for i in range(16):
                 rs.gdn_decode_update(lay, pool, slots, q[i], k[i], v[i], al[i], be[i], o=o)
         sec = _time(torch, lambda i: graph.replay(), max(3, iters // 16), warm) / 16
+        _LAST_MEDIAN["s"] /= 16  # per launch, like the mean
         rec("gdn_decode_fp32_tiny_b4_d64_graph", sec, decode_bytes(4, 4, 4, 64, lay.head_bytes, 4, False), 16,
             {"launches_per_graph": 16})
     if "gdn_fp32" in want:
