@@ -121,6 +121,27 @@ def test_layout_validation(L, kw, expect):
     assert not h.value
 
 
+def test_layout_size_limits():
+    """The row map (8,192 bytes) and the value-scaling table (4,096 floats)
+    travel in the launch parameters: one head more than fits is refused at
+    layout creation; the largest that fits is accepted."""
+    import recurrent_state_gb300 as rs
+    for Hv, Hk, ok in ((64, 8, True), (72, 8, False)):
+        if ok:
+            rs.Layout("mixed", 128, Hv, Hk, k_hi=16, hi_rows=gen.hi_rows(Hv, 128, 16))
+        else:
+            with pytest.raises(_abi.RsError) as e:
+                rs.Layout("mixed", 128, Hv, Hk, k_hi=16, hi_rows=gen.hi_rows(Hv, 128, 16))
+            assert e.value.status == _abi.RS_ERR_UNSUPPORTED
+    for Hv, Hk, ok in ((32, 4, True), (36, 4, False)):
+        if ok:
+            rs.Layout("damp", 128, Hv, Hk, k_hi=16, hi_rows=gen.hi_rows(Hv, 128, 16))
+        else:
+            with pytest.raises(_abi.RsError) as e:
+                rs.Layout("damp", 128, Hv, Hk, k_hi=16, hi_rows=gen.hi_rows(Hv, 128, 16))
+            assert e.value.status == _abi.RS_ERR_UNSUPPORTED
+
+
 def test_host_validation_returns_before_launch(L):
     st, h = make_layout(L, _abi.RS_LAYOUT_FP32, dk=64, Hv=4, Hk=4)
     assert st == 0
