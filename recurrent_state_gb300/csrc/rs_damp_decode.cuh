@@ -3,7 +3,7 @@
 // and value scaling (DAMP Appendix A.1, A.3 Eq. 18, A.4 "Fused decoding").
 //
 // Same pipeline as rs_mixed_decode.cuh (two warps per tile, a ring of
-// shared-memory stages, the packed tile updated in place), with the columns
+// shared-memory stages, the new words stored from registers to HBM), with the columns
 // of a lane chosen so that a scale group is one warp: lane l of tile warp t
 // owns columns 64t + l and 64t + 32 + l, i.e. one column of group 2t and one
 // of group 2t + 1.  A group's row maximum is then one warp max-reduction
@@ -13,7 +13,7 @@
 // same order as the oracle's transformed step.
 // Fused arithmetic (FUSED): when the row vectors are built, each INT8 row's
 // group scales in the stage are multiplied by the row's decay in place
-// (RN(s_g a_u); the tile's new scales overwrite them in pass 2), so the
+// (RN(s_g a_u); the stage is not written back), so the
 // passes dequantise with c * RN(s_g a_u) and no decay multiply; each new code
 // is one fused multiply-add, the integer nearest to x * RN(1/s).
 #pragma once
@@ -136,10 +136,7 @@ __global__ void __launch_bounds__(512, 1) damp_decode_kernel(const __grid_consta
         ok = ok && (mbar_wait_bounded(&bars[s], (uint32_t)use & 1u) ||
                     mbar_wait_bounded(&bars[s], (uint32_t)use & 1u));
         if (group_sync_or(1 + ps, 32 * WPT, !ok)) {
-            if (tt == 0) {
-                report(P.status, 8);
-                bulk_store_wait_all();
-            }
+            if (tt == 0) report(P.status, 8);
             return;
         }
         const int b = it / Hv, h = it - b * Hv;
@@ -191,6 +188,10 @@ __global__ void __launch_bounds__(512, 1) damp_decode_kernel(const __grid_consta
         uint32_t *hiw = reinterpret_cast<uint32_t *>(st);               // FP16 pairs [KH/2][D]
         uint32_t *low = reinterpret_cast<uint32_t *>(st + 2 * KH * D);  // INT8 quads [(D-KH)/4][D]
         float *scales = reinterpret_cast<float *>(st + 2 * KH * D + (D - KH) * D);  // [(D-KH)][NG]
+        uint8_t *dst = pool + ((size_t)slot * Hv + h) * S::kStateBytes;  // the tile in HBM
+        uint32_t *hi_g = reinterpret_cast<uint32_t *>(dst);
+        uint32_t *lo_g = reinterpret_cast<uint32_t *>(dst + 2 * KH * D);
+        float *scales_g = reinterpret_cast<float *>(dst + 2 * KH * D + (D - KH) * D);
 
         // x[i] = columns (cA, cB) of row 4q + i
         auto decay = [&](int q, float2 (&x)[4]) {
@@ -268,8 +269,8 @@ __global__ void __launch_bounds__(512, 1) damp_decode_kernel(const __grid_consta
             for (int pr = 0; pr < 2; ++pr) {
                 const __half2 ha = __floats2half2_rn(x[2 * pr].x, x[2 * pr + 1].x);
                 const __half2 hb = __floats2half2_rn(x[2 * pr].y, x[2 * pr + 1].y);
-                hiw[(2 * q + pr) * D + cA] = *reinterpret_cast<const uint32_t *>(&ha);
-                hiw[(2 * q + pr) * D + cB] = *reinterpret_cast<const uint32_t *>(&hb);
+                hi_g[(2 * q + pr) * D + cA] = *reinterpret_cast<const uint32_t *>(&ha);
+                hi_g[(2 * q + pr) * D + cB] = *reinterpret_cast<const uint32_t *>(&hb);
             }
         }
         constexpr int QB = S::kBlock / 4;
@@ -302,7 +303,6 @@ __global__ void __launch_bounds__(512, 1) damp_decode_kernel(const __grid_consta
                 return l3 ? t2[1] : t2[0];
             };
             const float ma = pick(ra), mb = pick(rb);
-            __syncwarp();  // every lane has read the block's old scales
             bool nonfinite = false;
             if (lane < S::kBlock) {
                 const float sa = row_scale_from_absmax(ma), sb = row_scale_from_absmax(mb);
@@ -312,7 +312,7 @@ __global__ void __launch_bounds__(512, 1) damp_decode_kernel(const __grid_consta
                 // fused arithmetic: y = 0 marks a group whose absmax is inf or NaN
                 nsc[2 * S::kBlock + lane] = (FUSED && bad_a) ? 0.0f : __frcp_rn(sa);
                 nsc[3 * S::kBlock + lane] = (FUSED && bad_b) ? 0.0f : __frcp_rn(sb);
-                *reinterpret_cast<float2 *>(scales + (blk * S::kBlock + lane) * NG + 2 * wt) = make_float2(sa, sb);
+                *reinterpret_cast<float2 *>(scales_g + (blk * S::kBlock + lane) * NG + 2 * wt) = make_float2(sa, sb);
                 nonfinite = bad_a || bad_b;
             }
             __syncwarp();
@@ -344,10 +344,10 @@ __global__ void __launch_bounds__(512, 1) damp_decode_kernel(const __grid_consta
                         mA[i] = __float_as_uint(t.x);
                         mB[i] = __float_as_uint(t.y);
                     }
-                    low[(q0 + qq) * D + cA] = __byte_perm(__byte_perm(mA[0], mA[1], 0x0040),
-                                                          __byte_perm(mA[2], mA[3], 0x0040), 0x5410);
-                    low[(q0 + qq) * D + cB] = __byte_perm(__byte_perm(mB[0], mB[1], 0x0040),
-                                                          __byte_perm(mB[2], mB[3], 0x0040), 0x5410);
+                    lo_g[(q0 + qq) * D + cA] = __byte_perm(__byte_perm(mA[0], mA[1], 0x0040),
+                                                           __byte_perm(mA[2], mA[3], 0x0040), 0x5410);
+                    lo_g[(q0 + qq) * D + cB] = __byte_perm(__byte_perm(mB[0], mB[1], 0x0040),
+                                                           __byte_perm(mB[2], mB[3], 0x0040), 0x5410);
                 }
             } else {
 #pragma unroll
@@ -364,8 +364,8 @@ __global__ void __launch_bounds__(512, 1) damp_decode_kernel(const __grid_consta
                             wb |= quant_exact(X[qq][i].y, s_b) << (8 * i);
                         }
                     }
-                    low[(q0 + qq) * D + cA] = wa;
-                    low[(q0 + qq) * D + cB] = wb;
+                    lo_g[(q0 + qq) * D + cA] = wa;
+                    lo_g[(q0 + qq) * D + cB] = wb;
                 }
             }
             __syncwarp();
@@ -376,17 +376,14 @@ __global__ void __launch_bounds__(512, 1) damp_decode_kernel(const __grid_consta
             store_from_f32<TO>(og + cB, __fmul_rn(csB, o.y));
         }
 
-        fence_proxy_async_smem();
+        // the stage has been read by both warps: it takes tile j + NS
         tile_sync();
         if (tt == 0) {
-            bulk_s2g(pool + ((size_t)slot * Hv + h) * S::kStateBytes, st, S::kStateBytes);
-            bulk_store_commit();
-            bulk_store_wait_read();
+            fence_proxy_async_smem();
             issue(j + NS);
         }
         __syncwarp();
     }
-    if (tt == 0) bulk_store_wait_all();
 }
 
 }  // namespace rs

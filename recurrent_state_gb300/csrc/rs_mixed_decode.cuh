@@ -14,14 +14,16 @@
 //     values, one warp max-reduction (redux.sync) and, with two warps per
 //     tile, one exchange of the 16 partial maxima of a block through shared
 //     memory.
-// The packed tile (18,880 B at d = 128) is worked on in place in its
-// shared-memory stage: pass 1 dequantises and decays each row and runs the
-// prediction chain p = S^T k; pass 2 repeats the dequantisation and decay
-// from the same operands (so they round the same way), applies the write
+// The packed tile (18,880 B at d = 128) is read from its shared-memory
+// stage: pass 1 dequantises and decays each row and runs the prediction
+// chain p = S^T k; pass 2 repeats the dequantisation and decay from the same
+// operands (so they round the same way), applies the write
 // x += RN(beta k) e^T, runs the readout chain o = S^T q, and requantises in
 // blocks of 16 rows (FP16 rows round to nearest even; INT8 rows get a new
 // scale from the block's absmax and an exact RN(x/s) code, as in
-// rs_step.cuh).  One thread then bulk-stores the tile.
+// rs_step.cuh).  The new words go from registers straight to HBM (a lane
+// stores its 8 bytes of a word row, so a warp writes 256 contiguous bytes),
+// and the stage is free as soon as both warps have read it.
 // With the fused arithmetic (FUSED) the decay of INT8 row u is applied to
 // its scale when the row vectors are built (RN(s_u a_u), so dequantising is
 // c * RN(s_u a_u) and needs no decay multiply), and each new code is one
@@ -101,7 +103,8 @@ template <int N> __device__ __forceinline__ void lds_words(const uint32_t *p, ui
         w[0] = v.x, w[1] = v.y;
     }
 }
-template <int N> __device__ __forceinline__ void sts_words(uint32_t *p, const uint32_t (&w)[N]) {
+// ... and stored to a lane's 8 or 16 bytes of a word row in HBM.
+template <int N> __device__ __forceinline__ void st_words(uint32_t *p, const uint32_t (&w)[N]) {
     if constexpr (N == 4) *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
     else *reinterpret_cast<uint2 *>(p) = make_uint2(w[0], w[1]);
 }
@@ -136,7 +139,7 @@ __device__ __noinline__ void quant_rows_exact(Quad<CPL> X, float4 s, float4 y, u
                 wd[2 * k + 1] |= quant_exact(X.x[i][k].y, sr[i]) << (8 * i);
             }
         }
-    sts_words<CPL>(dst, wd);
+    st_words<CPL>(dst, wd);
 }
 
 template <int D, int KH, bool KDA, typename TI, typename TO, int WPT, bool FUSED>
@@ -249,10 +252,7 @@ __global__ void __launch_bounds__(256 * WPT, 1)
         if constexpr (WPT == 1) failed = !__all_sync(0xffffffffu, ok);
         else failed = group_sync_or(1 + ps, 32 * WPT, !ok);
         if (failed) {
-            if (tt == 0) {
-                report(P.status, 8);
-                bulk_store_wait_all();
-            }
+            if (tt == 0) report(P.status, 8);
             return;
         }
         const int b = it / Hv, h = it - b * Hv;
@@ -301,10 +301,13 @@ __global__ void __launch_bounds__(256 * WPT, 1)
         const float4 *BK4 = reinterpret_cast<const float4 *>(wv + D);
         const float4 *Q4 = reinterpret_cast<const float4 *>(wv + 2 * D);
         const float4 *A4 = reinterpret_cast<const float4 *>(wv + 3 * D);
-        uint32_t *hiw = reinterpret_cast<uint32_t *>(st);               // FP16 pairs [KH/2][D]
-        uint32_t *low = reinterpret_cast<uint32_t *>(st + 2 * KH * D);  // INT8 quads [(D-KH)/4][D]
-        float *scales = reinterpret_cast<float *>(st + 2 * KH * D + (D - KH) * D);
-        const float4 *sc4 = reinterpret_cast<const float4 *>(scales);
+        const uint32_t *hiw = reinterpret_cast<const uint32_t *>(st);               // FP16 pairs [KH/2][D]
+        const uint32_t *low = reinterpret_cast<const uint32_t *>(st + 2 * KH * D);  // INT8 quads [(D-KH)/4][D]
+        const float4 *sc4 = reinterpret_cast<const float4 *>(st + 2 * KH * D + (D - KH) * D);  // row scales
+        uint8_t *dst = pool + ((size_t)slot * Hv + h) * S::kStateBytes;  // the tile in HBM
+        uint32_t *hi_g = reinterpret_cast<uint32_t *>(dst);
+        uint32_t *lo_g = reinterpret_cast<uint32_t *>(dst + 2 * KH * D);
+        float *scales_g = reinterpret_cast<float *>(dst + 2 * KH * D + (D - KH) * D);
 
         auto decay = [&](int q, Quad<CPL> &X) {  // rows 4q..4q+3 times their decay
             const float4 a = (KDA || FUSED) ? A4[q] : make_float4(alpha0, alpha0, alpha0, alpha0);
@@ -397,7 +400,7 @@ __global__ void __launch_bounds__(256 * WPT, 1)
 
         // ---- pass 2: write, readout, requantise ---------------------------
 #pragma unroll
-        for (int q = 0; q < KH / 4; ++q) {  // FP16 rows: round to nearest even, in place
+        for (int q = 0; q < KH / 4; ++q) {  // FP16 rows: round to nearest even
             Quad<CPL> X;
             load_hi(q, X);
             write_read(q, X, e, o);
@@ -411,7 +414,7 @@ __global__ void __launch_bounds__(256 * WPT, 1)
                     wd[2 * k] = *reinterpret_cast<const uint32_t *>(&ha);
                     wd[2 * k + 1] = *reinterpret_cast<const uint32_t *>(&hb);
                 }
-                sts_words<CPL>(hiw + (2 * q + pr) * D + c0, wd);
+                st_words<CPL>(hi_g + (2 * q + pr) * D + c0, wd);
             }
         }
         constexpr int QB = S::kBlock / 4;  // quads per block
@@ -447,13 +450,13 @@ __global__ void __launch_bounds__(256 * WPT, 1)
             if constexpr (WPT > 1) {  // combine the tile's warps (every warp gets the same maxima)
                 float *pb = part + (blk & 1) * WPT * S::kBlock;
                 if (lane < S::kBlock) pb[wt * S::kBlock + lane] = mine;
-                tile_sync();  // also: every warp has read the block's old scales
+                tile_sync();
                 if (lane < S::kBlock)
 #pragma unroll
                     for (int u = 0; u < WPT; ++u)
                         if (u != wt) mine = max_nan(mine, pb[u * S::kBlock + lane]);
             } else {
-                __syncwarp();  // every lane has read the block's old scales
+                __syncwarp();
             }
             bool nonfinite = false;
             if (lane < S::kBlock) {
@@ -462,7 +465,7 @@ __global__ void __launch_bounds__(256 * WPT, 1)
                 nsc[lane] = -sv;
                 // fused arithmetic: y = 0 marks a row whose absmax is inf or NaN
                 nsc[S::kBlock + lane] = (FUSED && nonfinite) ? 0.0f : __frcp_rn(sv);
-                if (wt == 0) scales[blk * S::kBlock + lane] = sv;
+                if (wt == 0) scales_g[blk * S::kBlock + lane] = sv;
             }
             __syncwarp();
             nonfinite = __any_sync(0xffffffffu, nonfinite);
@@ -499,14 +502,14 @@ __global__ void __launch_bounds__(256 * WPT, 1)
                     for (int c = 0; c < CPL; ++c)
                         wd[c] = __byte_perm(__byte_perm(mb[0][c], mb[1][c], 0x0040),
                                             __byte_perm(mb[2][c], mb[3][c], 0x0040), 0x5410);
-                    sts_words<CPL>(low + (q0 + qq) * D + c0, wd);
+                    st_words<CPL>(lo_g + (q0 + qq) * D + c0, wd);
                 }
             } else {  // absmax inf or NaN somewhere in the block: literal IEEE division
 #pragma unroll
                 for (int qq = 0; qq < QB; ++qq)
                     quant_rows_exact<CPL, FUSED>(
                         X[qq], make_float4(-nsc[4 * qq], -nsc[4 * qq + 1], -nsc[4 * qq + 2], -nsc[4 * qq + 3]),
-                        reinterpret_cast<const float4 *>(nsc + S::kBlock)[qq], low + (q0 + qq) * D + c0);
+                        reinterpret_cast<const float4 *>(nsc + S::kBlock)[qq], lo_g + (q0 + qq) * D + c0);
             }
             __syncwarp();  // -s and 1/s are rewritten by the next block
         }
@@ -519,18 +522,14 @@ __global__ void __launch_bounds__(256 * WPT, 1)
             }
         }
 
-        // ---- store the tile; the stage then takes tile j + NS ---------------
-        fence_proxy_async_smem();
+        // ---- the stage has been read by both warps: it takes tile j + NS ----
         tile_sync();
         if (tt == 0) {
-            bulk_s2g(pool + ((size_t)slot * Hv + h) * S::kStateBytes, st, S::kStateBytes);
-            bulk_store_commit();
-            bulk_store_wait_read();
+            fence_proxy_async_smem();
             issue(j + NS);
         }
         __syncwarp();
     }
-    if (tt == 0) bulk_store_wait_all();
 }
 
 }  // namespace rs
