@@ -19,9 +19,10 @@
 // (cp.async.bulk + mbarrier) into the group's shared-memory stage; as soon as
 // the stage has been read into registers the group issues the copy of its
 // next tile, so HBM reads of tile i+1 overlap the arithmetic of tile i.
-// FP32 tiles go straight from registers to HBM with coalesced 16-byte stores
-// (four lanes transpose a 4 x 4 block by shuffles, so a lane writes four
-// consecutive columns of a row); mixed tiles are assembled in a
+// FP32 tiles go straight from registers to HBM with coalesced stores: 16-byte
+// stores for a single token (four lanes transpose a 4 x 4 block by shuffles,
+// so a lane writes four consecutive columns of a row), a warp's 32 columns of
+// a row for a replay; mixed tiles are assembled in a
 // shared-memory staging buffer and written with one bulk TMA store.
 //
 // Mixed layout (DAMP §5.2, Appendix A.4): FP16 rows and INT8 rows with one
@@ -613,11 +614,13 @@ __global__ void __launch_bounds__(step_threads(MAXT), 1)
 
         // ---- registers -> HBM ---------------------------------------------
         uint8_t *tile = pool + ((size_t)slot * Hv + h) * S::kStateBytes;
-        if constexpr (!MIXED) {
+        if constexpr (!MIXED && MAXT == 1) {
             // Rows 4r..4r+3 of the four columns of a lane quad are transposed
             // among its lanes (two exchanges), so lane i stores row 4r + i of
             // the quad's columns as one 16-byte store: a warp writes four
-            // whole 128-byte row segments per instruction.
+            // whole 128-byte row segments per instruction.  (Replay, whose
+            // threads hold more registers, keeps the column stores: the
+            // exchanges cost it more than the wider stores save.)
             float *st = reinterpret_cast<float *>(tile);
             const bool b0 = tid & 1, b1 = tid & 2;
 #pragma unroll
@@ -632,6 +635,13 @@ __global__ void __launch_bounds__(step_threads(MAXT), 1)
                 const float u1 = __shfl_xor_sync(0xffffffffu, b0 ? l2 : l3, 1);
                 const float4 w = b0 ? make_float4(u0, l1, u1, l3) : make_float4(l0, u0, l2, u1);
                 *reinterpret_cast<float4 *>(st + (4 * r + (tid & 3)) * D + (tid & ~3)) = w;
+            }
+        } else if constexpr (!MIXED) {
+            float *st = reinterpret_cast<float *>(tile);
+#pragma unroll
+            for (int j = 0; j < DP; ++j) {
+                st[(2 * j) * D + tid] = x[j].x;
+                st[(2 * j + 1) * D + tid] = x[j].y;
             }
         } else {
             mixed_requant_from_max<D, KH, FUSED>(x, mine, outt, red, scl, nscl, rcp, flag, tid, lane, wig,
