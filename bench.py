@@ -415,7 +415,7 @@ def _time(torch, fn, iters, warm=3, repeats=20):
 
 
 EXTRA = ("gdn_tiny", "gdn_fp32", "kda_fp32", "kda_mixed", "gdn_mixed", "kda_damp", "replay_mixed", "replay_fp32",
-         "kda_mixed_fused", "gdn_mixed_fused", "kda_damp_fused", "replay_mixed_fused", "replay_sweep",
+         "kda_mixed_fused", "kda_mixed_fused_wide", "gdn_mixed_fused", "kda_damp_fused", "replay_mixed_fused", "replay_sweep",
          "prefill_fp32", "prefill_mixed_fused",
          "pack_gdn", "restore_gdn", "pack_kda", "restore_kda", "pack_int8_gdn", "restore_int8_gdn",
          "pack_int8_kda", "restore_int8_kda", "pack_mixed", "restore_mixed")
@@ -428,7 +428,8 @@ PRESETS = {
     "tiny": ["gdn_tiny"],
     "gdn": ["gdn_fp32"],
     "kda": ["kda_fp32"],
-    "kda_mixed": ["kda_mixed", "kda_mixed_fused", "replay_mixed", "replay_mixed_fused", "replay_sweep"],
+    "kda_mixed": ["kda_mixed", "kda_mixed_fused", "kda_mixed_fused_wide", "replay_mixed", "replay_mixed_fused",
+                  "replay_sweep"],
     "ckpt": ["pack_gdn", "restore_gdn", "pack_kda", "restore_kda"],
 }
 
@@ -513,7 +514,8 @@ def extra_kernels(args, rs, torch, dev, peak, world, only=None):
         torch.cuda.empty_cache()
     KDA_B = dict(KDA, B=B)
     MIXED_KEYS = {"kda_fp32", "kda_mixed", "gdn_mixed", "kda_damp", "replay_mixed", "replay_fp32",
-                  "kda_mixed_fused", "gdn_mixed_fused", "kda_damp_fused", "replay_mixed_fused", "replay_sweep"}
+                  "kda_mixed_fused", "kda_mixed_fused_wide", "gdn_mixed_fused", "kda_damp_fused",
+                  "replay_mixed_fused", "replay_sweep"}
     if want & MIXED_KEYS:
         nsteps = 8
         w = gen.decode_workload(steps=nsteps, per_channel=True, in_dtype="bf16", seed=1,
@@ -548,6 +550,23 @@ def extra_kernels(args, rs, torch, dev, peak, world, only=None):
                 be[i % nsteps], o=o), iters, warm)
             rec(f"kda_decode_mixed_fused_b{B}", sec, decode_bytes(B, 32, 32, 128, mix.head_bytes, 2, True),
                 B * 32, {"quant": "fused"})
+        if "kda_mixed_fused_wide" in want:
+            # the same kernel on four copies of the batch (4 B sequences, built on the device): the
+            # per-launch fixed cost (pipeline fill and the last round of tiles) weighs a quarter as much
+            R = 4
+            wpool = mpool.repeat(R, 1, 1)
+            wq, wk, wv = q.repeat(1, R, 1, 1), k.repeat(1, R, 1, 1), v.repeat(1, R, 1, 1)
+            wal, wbe = al.repeat(1, R, 1, 1), be.repeat(1, R, 1)
+            wslots = torch.arange(R * B, dtype=torch.int32, device=dev)
+            wo = torch.empty((R * B, KDA["Hv"], KDA["d"]), device=dev)
+            sec = _time(torch, lambda i: rs.kda_decode_update(
+                mixf, wpool, wslots, wq[i % nsteps], wk[i % nsteps], wv[i % nsteps], wal[i % nsteps],
+                wbe[i % nsteps], o=wo), iters, warm)
+            rec(f"kda_decode_mixed_fused_b{R * B}", sec,
+                decode_bytes(R * B, 32, 32, 128, mix.head_bytes, 2, True), R * B * 32,
+                {"quant": "fused", "inputs": f"the batch-{B} workload repeated {R} times"})
+            del wpool, wq, wk, wv, wal, wbe, wo
+            torch.cuda.empty_cache()
         al_g = al[..., 0].contiguous()  # one decay per (sequence, head) for the GDN form
         if "gdn_mixed" in want:
             sec = _time(torch, lambda i: rs.gdn_decode_update(
