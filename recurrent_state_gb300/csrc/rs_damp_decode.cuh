@@ -192,6 +192,11 @@ __global__ void __launch_bounds__(512, 1) damp_decode_kernel(const __grid_consta
         uint32_t *hi_g = reinterpret_cast<uint32_t *>(dst);
         uint32_t *lo_g = reinterpret_cast<uint32_t *>(dst + 2 * KH * D);
         float *scales_g = reinterpret_cast<float *>(dst + 2 * KH * D + (D - KH) * D);
+        // this lane's column cA in each region (column cB is 32 words further);
+        // the warp's two group scales of a row are a float2 at 2 wt
+        const uint32_t *hiA = hiw + cA, *lowA = low + cA;
+        uint32_t *hiA_g = hi_g + cA, *loA_g = lo_g + cA;
+        const float *scW = scales + 2 * wt;
 
         // x[i] = columns (cA, cB) of row 4q + i
         auto decay = [&](int q, float2 (&x)[4]) {
@@ -203,7 +208,7 @@ __global__ void __launch_bounds__(512, 1) damp_decode_kernel(const __grid_consta
         auto load_hi = [&](int q, float2 (&x)[4]) {
 #pragma unroll
             for (int pr = 0; pr < 2; ++pr) {
-                const uint32_t wa = hiw[(2 * q + pr) * D + cA], wb = hiw[(2 * q + pr) * D + cB];
+                const uint32_t wa = hiA[(2 * q + pr) * D], wb = hiA[(2 * q + pr) * D + 32];
                 const __half2 ha = *reinterpret_cast<const __half2 *>(&wa);
                 const __half2 hb = *reinterpret_cast<const __half2 *>(&wb);
                 x[2 * pr] = make_float2(__low2float(ha), __low2float(hb));
@@ -212,11 +217,13 @@ __global__ void __launch_bounds__(512, 1) damp_decode_kernel(const __grid_consta
             decay(q, x);
         };
         auto load_lo = [&](int qd, float2 (&x)[4]) {
-            const uint32_t wa = low[qd * D + cA] ^ 0x80808080u, wb = low[qd * D + cB] ^ 0x80808080u;
+            const uint32_t *lw = lowA + qd * D;
+            const uint32_t wa = lw[0] ^ 0x80808080u, wb = lw[32] ^ 0x80808080u;
+            const float *sq = scW + 4 * qd * NG;
             const float2 nb = make_float2(-kCodeBias, -kCodeBias);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const float2 s2 = *reinterpret_cast<const float2 *>(scales + (4 * qd + i) * NG + 2 * wt);
+                const float2 s2 = *reinterpret_cast<const float2 *>(sq + i * NG);
                 const uint32_t sel = 0x7540u + (uint32_t)i;
                 const float fa = __uint_as_float(__byte_perm(wa, 0x4B000000u, sel));
                 const float fb = __uint_as_float(__byte_perm(wb, 0x4B000000u, sel));
@@ -269,8 +276,8 @@ __global__ void __launch_bounds__(512, 1) damp_decode_kernel(const __grid_consta
             for (int pr = 0; pr < 2; ++pr) {
                 const __half2 ha = __floats2half2_rn(x[2 * pr].x, x[2 * pr + 1].x);
                 const __half2 hb = __floats2half2_rn(x[2 * pr].y, x[2 * pr + 1].y);
-                hi_g[(2 * q + pr) * D + cA] = *reinterpret_cast<const uint32_t *>(&ha);
-                hi_g[(2 * q + pr) * D + cB] = *reinterpret_cast<const uint32_t *>(&hb);
+                hiA_g[(2 * q + pr) * D] = *reinterpret_cast<const uint32_t *>(&ha);
+                hiA_g[(2 * q + pr) * D + 32] = *reinterpret_cast<const uint32_t *>(&hb);
             }
         }
         constexpr int QB = S::kBlock / 4;
@@ -344,10 +351,9 @@ __global__ void __launch_bounds__(512, 1) damp_decode_kernel(const __grid_consta
                         mA[i] = __float_as_uint(t.x);
                         mB[i] = __float_as_uint(t.y);
                     }
-                    lo_g[(q0 + qq) * D + cA] = __byte_perm(__byte_perm(mA[0], mA[1], 0x0040),
-                                                           __byte_perm(mA[2], mA[3], 0x0040), 0x5410);
-                    lo_g[(q0 + qq) * D + cB] = __byte_perm(__byte_perm(mB[0], mB[1], 0x0040),
-                                                           __byte_perm(mB[2], mB[3], 0x0040), 0x5410);
+                    uint32_t *lg = loA_g + (q0 + qq) * D;
+                    lg[0] = __byte_perm(__byte_perm(mA[0], mA[1], 0x0040), __byte_perm(mA[2], mA[3], 0x0040), 0x5410);
+                    lg[32] = __byte_perm(__byte_perm(mB[0], mB[1], 0x0040), __byte_perm(mB[2], mB[3], 0x0040), 0x5410);
                 }
             } else {
 #pragma unroll
@@ -364,8 +370,8 @@ __global__ void __launch_bounds__(512, 1) damp_decode_kernel(const __grid_consta
                             wb |= quant_exact(X[qq][i].y, s_b) << (8 * i);
                         }
                     }
-                    lo_g[(q0 + qq) * D + cA] = wa;
-                    lo_g[(q0 + qq) * D + cB] = wb;
+                    loA_g[(q0 + qq) * D] = wa;
+                    loA_g[(q0 + qq) * D + 32] = wb;
                 }
             }
             __syncwarp();
