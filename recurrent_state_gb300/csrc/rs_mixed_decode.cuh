@@ -301,12 +301,13 @@ __global__ void __launch_bounds__(256 * WPT, 1)
         const float4 *BK4 = reinterpret_cast<const float4 *>(wv + D);
         const float4 *Q4 = reinterpret_cast<const float4 *>(wv + 2 * D);
         const float4 *A4 = reinterpret_cast<const float4 *>(wv + 3 * D);
-        const uint32_t *hiw = reinterpret_cast<const uint32_t *>(st);               // FP16 pairs [KH/2][D]
-        const uint32_t *low = reinterpret_cast<const uint32_t *>(st + 2 * KH * D);  // INT8 quads [(D-KH)/4][D]
+        // this lane's first column in each region: FP16 pairs [KH/2][D], INT8 quads [(D-KH)/4][D]
+        const uint32_t *hiw = reinterpret_cast<const uint32_t *>(st) + c0;
+        const uint32_t *low = reinterpret_cast<const uint32_t *>(st + 2 * KH * D) + c0;
         const float4 *sc4 = reinterpret_cast<const float4 *>(st + 2 * KH * D + (D - KH) * D);  // row scales
         uint8_t *dst = pool + ((size_t)slot * Hv + h) * S::kStateBytes;  // the tile in HBM
-        uint32_t *hi_g = reinterpret_cast<uint32_t *>(dst);
-        uint32_t *lo_g = reinterpret_cast<uint32_t *>(dst + 2 * KH * D);
+        uint32_t *hi_g = reinterpret_cast<uint32_t *>(dst) + c0;
+        uint32_t *lo_g = reinterpret_cast<uint32_t *>(dst + 2 * KH * D) + c0;
         float *scales_g = reinterpret_cast<float *>(dst + 2 * KH * D + (D - KH) * D);
 
         auto decay = [&](int q, Quad<CPL> &X) {  // rows 4q..4q+3 times their decay
@@ -321,7 +322,7 @@ __global__ void __launch_bounds__(256 * WPT, 1)
 #pragma unroll
             for (int pr = 0; pr < 2; ++pr) {
                 uint32_t wd[CPL];
-                lds_words<CPL>(hiw + (2 * q + pr) * D + c0, wd);
+                lds_words<CPL>(hiw + (2 * q + pr) * D, wd);
 #pragma unroll
                 for (int k = 0; k < NP; ++k) {
                     const __half2 ha = *reinterpret_cast<const __half2 *>(&wd[2 * k]);
@@ -334,7 +335,7 @@ __global__ void __launch_bounds__(256 * WPT, 1)
         };
         auto load_lo = [&](int qd, Quad<CPL> &X) {  // INT8 rows KH+4qd .. KH+4qd+3, decayed
             uint32_t wd[CPL];
-            lds_words<CPL>(low + qd * D + c0, wd);
+            lds_words<CPL>(low + qd * D, wd);
 #pragma unroll
             for (int t = 0; t < CPL; ++t) wd[t] ^= 0x80808080u;
             // fused: the decayed scales RN(s a) of the row vectors; otherwise the stored scales
@@ -414,7 +415,7 @@ __global__ void __launch_bounds__(256 * WPT, 1)
                     wd[2 * k] = *reinterpret_cast<const uint32_t *>(&ha);
                     wd[2 * k + 1] = *reinterpret_cast<const uint32_t *>(&hb);
                 }
-                st_words<CPL>(hi_g + (2 * q + pr) * D + c0, wd);
+                st_words<CPL>(hi_g + (2 * q + pr) * D, wd);
             }
         }
         constexpr int QB = S::kBlock / 4;  // quads per block
@@ -502,14 +503,14 @@ __global__ void __launch_bounds__(256 * WPT, 1)
                     for (int c = 0; c < CPL; ++c)
                         wd[c] = __byte_perm(__byte_perm(mb[0][c], mb[1][c], 0x0040),
                                             __byte_perm(mb[2][c], mb[3][c], 0x0040), 0x5410);
-                    st_words<CPL>(lo_g + (q0 + qq) * D + c0, wd);
+                    st_words<CPL>(lo_g + (q0 + qq) * D, wd);
                 }
             } else {  // absmax inf or NaN somewhere in the block: literal IEEE division
 #pragma unroll
                 for (int qq = 0; qq < QB; ++qq)
                     quant_rows_exact<CPL, FUSED>(
                         X[qq], make_float4(-nsc[4 * qq], -nsc[4 * qq + 1], -nsc[4 * qq + 2], -nsc[4 * qq + 3]),
-                        reinterpret_cast<const float4 *>(nsc + S::kBlock)[qq], lo_g + (q0 + qq) * D + c0);
+                        reinterpret_cast<const float4 *>(nsc + S::kBlock)[qq], lo_g + (q0 + qq) * D);
             }
             __syncwarp();  // -s and 1/s are rewritten by the next block
         }
