@@ -22,8 +22,8 @@
 // FP32 tiles go straight from registers to HBM with coalesced stores: 16-byte
 // stores for a single token (four lanes transpose a 4 x 4 block by shuffles,
 // so a lane writes four consecutive columns of a row), a warp's 32 columns of
-// a row for a replay; mixed tiles are assembled in a
-// shared-memory staging buffer and written with one bulk TMA store.
+// a row for a replay; mixed tiles are requantised from registers into the
+// pool tile directly (a thread writes its column of each word row).
 //
 // Mixed layout (DAMP §5.2, Appendix A.4): FP16 rows and INT8 rows with one
 // FP32 scale per row are dequantised into the registers, updated in FP32, and
@@ -67,7 +67,7 @@ struct StepShape {
     __host__ __device__ static constexpr int region_bytes(int T) {
         int r = stage_bytes(T);
         r += T * kRowVecs * D * 4 + 64;  // row vectors, per-token decays and strengths (replay)
-        if (kMixed) r += kWarps * D * 4 + D * 12 + 128 + kStatePad;  // partials, s/-s/1/s, flag, out tile
+        if (kMixed) r += kWarps * D * 4 + D * 12 + 128;  // partials, s/-s/1/s, flag
         return (r + 127) / 128 * 128;
     }
 };
@@ -326,7 +326,6 @@ __global__ void __launch_bounds__(step_threads(MAXT), 1)
     float *nscl = scl + D;                                          // [D] -scales
     float *rcp = nscl + D;                                          // [D] reciprocals
     int *flag = reinterpret_cast<int *>(rcp + D);                   // non-finite row seen
-    uint8_t *outt = reinterpret_cast<uint8_t *>(rcp + D + 32);      // out tile      (mixed)
 
     if (threadIdx.x < G) mbar_init(&bars[threadIdx.x], 1);
     if constexpr (MIXED)
@@ -423,10 +422,7 @@ __global__ void __launch_bounds__(step_threads(MAXT), 1)
         bool got = mbar_wait_bounded(bar, phase);
         if (!got) got = mbar_wait_bounded(bar, phase);  // copies still in flight get a second bound
         if (group_sync_or(bar_id, D, !got)) {
-            if (tid == 0) {
-                report(P.status, 8);
-                if constexpr (MIXED) bulk_store_wait_all();
-            }
+            if (tid == 0) report(P.status, 8);
             return;
         }
         phase ^= 1u;
@@ -644,24 +640,15 @@ __global__ void __launch_bounds__(step_threads(MAXT), 1)
                 st[(2 * j + 1) * D + tid] = x[j].y;
             }
         } else {
-            mixed_requant_from_max<D, KH, FUSED>(x, mine, outt, red, scl, nscl, rcp, flag, tid, lane, wig,
+            // the requantised words go from registers straight to the tile in HBM
+            // (thread tid writes column tid of each word row: 128 contiguous bytes a warp)
+            mixed_requant_from_max<D, KH, FUSED>(x, mine, tile, red, scl, nscl, rcp, flag, tid, lane, wig,
                                                  bar_id, [&] {
-                                              if (tid == 0) {
-                                                  bulk_store_wait_read();  // previous store has read `outt`
-                                                  *flag = 0;
-                                              }
-                                          });
-            fence_proxy_async_smem();  // this thread's writes to `outt` before the bulk store
-            group_sync(bar_id, D);
-            if (tid == 0) {
-                bulk_s2g(tile, outt, S::kStateBytes);
-                bulk_store_commit();
-            }
+                                                     if (tid == 0) *flag = 0;
+                                                 });
         }
         group_sync(bar_id, D);  // row vectors / partials free for the next item
     }
-    if constexpr (MIXED)
-        if (tid == 0) bulk_store_wait_all();
 }
 
 }  // namespace rs
