@@ -38,8 +38,8 @@ namespace {
 
 // Shared memory of one group: row vectors [2 buffers][NV][D] floats, then the
 // requantisation scratch of the mixed layout (partial maxima [D/32][D], row
-// scales, their negations and reciprocals [D] each, a flag word) and the
-// requantised tile.
+// scales, their negations and reciprocals [D] each, a flag word); the
+// requantised words go from registers straight to the pool tile.
 template <int D, int KHI, bool KDA, bool GRP>
 struct PrefillShape {
     static constexpr bool kMixed = KHI >= 0;
@@ -50,7 +50,7 @@ struct PrefillShape {
         kMixed ? (2 * kKhi * D + (D - kKhi) * D + 4 * (D - kKhi) * kScales) : D * D * 4;
     static constexpr int kRowBytes = 2 * kNV * D * 4;
     static constexpr int kScratch = kMixed ? ((D / 32) * D * 4 + 3 * D * 4 + 128) : 0;
-    static constexpr int kRegion = (kRowBytes + kScratch + (kMixed ? kStateBytes : 0) + 127) / 128 * 128;
+    static constexpr int kRegion = (kRowBytes + kScratch + 127) / 128 * 128;
 };
 
 // DAMP-exact tile: dequantise column tid (group tid / 32) into row pairs;
@@ -141,7 +141,6 @@ __global__ void __launch_bounds__(prefill_threads(KHI), 1) prefill_kernel(const 
     float *nscl = scl + D;
     float *rcp = nscl + D;
     int *flag = reinterpret_cast<int *>(rcp + D);
-    uint8_t *outt = reinterpret_cast<uint8_t *>(rcp + D + 32);
 
     const int Hv = P.Hv, Hk = P.Hk, L = P.L;
     const int items = P.B * Hv;
@@ -286,25 +285,18 @@ __global__ void __launch_bounds__(prefill_threads(KHI), 1) prefill_kernel(const 
                 st[(2 * j + 1) * D + tid] = x[j].y;
             }
         } else if constexpr (GRP) {
-            damp_requant<D, KH, FUSED>(x, outt, tid, lane);
-            group_sync(bar_id, D);  // the requantised tile is complete
-            uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-            const uint4 *s4 = reinterpret_cast<const uint4 *>(outt);
-            for (int i = tid; i < S::kStateBytes / 16; i += D) d4[i] = s4[i];
+            // the requantised words go from registers straight to the pool tile
+            damp_requant<D, KH, FUSED>(x, dst, tid, lane);
         } else {
             float mine[D / 32];
 #pragma unroll
             for (int k = 0; k < D / 32; ++k) mine[k] = 0.0f;
 #pragma unroll
             for (int j = KH / 2; j < DP; ++j) absmax_pair<D>(x[j], j, lane, mine);
-            mixed_requant_from_max<D, KH, FUSED>(x, mine, outt, red, scl, nscl, rcp, flag, tid, lane, wig,
+            mixed_requant_from_max<D, KH, FUSED>(x, mine, dst, red, scl, nscl, rcp, flag, tid, lane, wig,
                                                  bar_id, [&] {
                                                      if (tid == 0) *flag = 0;
                                                  });
-            group_sync(bar_id, D);  // the requantised tile is complete
-            uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-            const uint4 *s4 = reinterpret_cast<const uint4 *>(outt);
-            for (int i = tid; i < S::kStateBytes / 16; i += D) d4[i] = s4[i];
         }
         group_sync(bar_id, D);  // row vectors and scratch free for the next item
     }
@@ -313,7 +305,6 @@ __global__ void __launch_bounds__(prefill_threads(KHI), 1) prefill_kernel(const 
 template <int D, int KHI, bool KDA, typename TI, typename TO, bool FUSED, bool GRP, typename PT>
 cudaError_t run(PT &P, cudaStream_t s) {
     using Sh = PrefillShape<D, KHI, KDA, GRP>;
-    static_assert(Sh::kStateBytes % 16 == 0, "16-byte tile copies");
     auto kern = prefill_kernel<D, KHI, KDA, TI, TO, FUSED, GRP, PT>;
     constexpr int G = prefill_threads(KHI) / D;
     const int smem = G * Sh::kRegion;
