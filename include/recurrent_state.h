@@ -350,17 +350,27 @@ rs_status rs_ckpt_restore(const rs_plan *p, const void *ckpt_pool, int64_t n_ckp
  * that cannot afford the device-wide synchronisation of cudaFree.
  * Same arguments, layout and result as rs_ckpt_pack, but the plan needs no
  * rs_plan_upload: the plan's index table is copied (cudaMemcpyAsync on
- * `stream`) into a fixed array that the library holds in device memory, and
- * nothing is allocated or freed.  Limits and behaviour:
+ * `stream`, from a page-locked host copy that rs_plan_create made, so the
+ * call does not synchronise) into a fixed array that the library holds in
+ * device memory, and nothing is allocated or freed.  Limits and behaviour:
  *   - the plan may retain at most 262,144 units per checkpoint (o_L); a
  *     larger plan returns RS_ERR_UNSUPPORTED before any work;
+ *   - a plan created while no CUDA device was reachable has no page-locked
+ *     copy: RS_ERR_UNSUPPORTED;
+ *   - a shape rs_ckpt_pack would refuse (n > 65,535, too many 512-byte
+ *     chunks per checkpoint) returns RS_ERR_UNSUPPORTED before the array is
+ *     touched;
  *   - the array (1 MiB) lives on every GPU that loads the library until the
  *     process exits;
  *   - the first call on a device looks up the array's device address; make
- *     that first call before any stream capture begins;
+ *     that first call before any stream capture begins.  The address is kept
+ *     for the process: do not use this call on a device after
+ *     cudaDeviceReset.  Devices 0..63 only;
  *   - all calls share the one array, which keeps the last call's table:
  *     calls whose work overlaps on the GPU (on different streams) race and
- *     must be ordered by the caller. */
+ *     must be ordered by the caller;
+ *   - destroy the plan only after the call's copy has run (the copy reads
+ *     the plan's page-locked table). */
 rs_status rs_ckpt_pack_noalloc(const rs_plan *p, const void *pool, int64_t layer_stride_bytes,
                                int64_t n_pool_slots, const int32_t *src_slots,
                                const int32_t *dst_ckpt_slots, int32_t n, void *ckpt_pool,

@@ -42,6 +42,15 @@ rs_status launch_fail(cudaError_t e) {
     return cuda_fail(e);
 }
 
+}  // namespace
+
+namespace rs {
+int32_t fail_cuda(cudaError_t e) { return cuda_fail(e); }
+int32_t fail_launch(cudaError_t e) { return launch_fail(e); }
+}  // namespace rs
+
+namespace {
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 size_t mixed_head_bytes(int dk, int dv, int khi) {
@@ -495,6 +504,21 @@ rs_status rs_plan_create(rs_plan **out, const rs_layout *l, int32_t num_layers, 
         }
         p->offsets[lyr + 1] = p->offsets[lyr] + r;
     }
+    // Page-locked copy of the table for rs_ckpt_pack_noalloc, whose copy into
+    // its fixed device array must not stage through pageable memory (such a
+    // copy can synchronise with the stream).  Best effort: without a CUDA
+    // device (or for a plan beyond that call's limit) none is made, and that
+    // call then returns RS_ERR_UNSUPPORTED.
+    const size_t nk = p->kept_unit.size();
+    if (nk > 0 && (int64_t)nk <= rs::kNoallocTableEntries) {
+        void *h = nullptr;
+        if (cudaHostAlloc(&h, nk * sizeof(int32_t), cudaHostAllocPortable) == cudaSuccess) {
+            std::memcpy(h, p->kept_unit.data(), nk * sizeof(int32_t));
+            p->h_kept_pinned = static_cast<int32_t *>(h);
+        } else {
+            cudaGetLastError();  // leave no error behind for the caller's next CUDA call
+        }
+    }
     *out = p;
     return RS_OK;
 }
@@ -503,6 +527,7 @@ rs_status rs_plan_destroy(rs_plan *p) {
     if (!p) return RS_OK;
     if (p->d_kept) cudaFree(p->d_kept);
     if (p->d_all) cudaFree(p->d_all);
+    if (p->h_kept_pinned) cudaFreeHost(p->h_kept_pinned);
     delete p;
     return RS_OK;
 }

@@ -137,15 +137,25 @@ __global__ void __launch_bounds__(256) ckpt_kernel(const __grid_constant__ CkptP
     }
 }
 
-cudaError_t launch(const CkptParams &P, bool pack, cudaStream_t s) {
+// The shapes the kernel is built for: whole 16-byte lanes per unit, 32-bit
+// chunk indices within a (slot, checkpoint) pair, and n in grid.y.
+cudaError_t check(const CkptParams &P, bool pack) {
     if (P.unit_bytes <= 0 || (P.unit_bytes & 15)) return cudaErrorNotSupported;
+    const int64_t cpu = (P.unit_bytes + kChunkBytes - 1) / kChunkBytes;
+    const int64_t units = pack ? P.n_kept : P.n_all;
+    if (units * cpu >= (1ll << 31) || P.n > 65535) return cudaErrorNotSupported;
+    return cudaSuccess;
+}
+
+cudaError_t launch(const CkptParams &P, bool pack, cudaStream_t s) {
+    const cudaError_t ce = check(P, pack);
+    if (ce != cudaSuccess) return ce;
     const int64_t cpu = (P.unit_bytes + kChunkBytes - 1) / kChunkBytes;
     int log2cpu = 0;
     while ((1ll << log2cpu) < cpu) ++log2cpu;
     if ((1ll << log2cpu) != cpu) log2cpu = -1;
     const int64_t units = pack ? P.n_kept : P.n_all;
     const int64_t per_pair = units * cpu;
-    if (per_pair >= (1ll << 31) || P.n > 65535) return cudaErrorNotSupported;
     if (per_pair == 0 || P.n == 0) return cudaSuccess;
     const int kChunks = chunks_in_flight(pack);
     const int64_t warps_needed = (per_pair + kChunks - 1) / kChunks;
@@ -165,6 +175,7 @@ cudaError_t launch(const CkptParams &P, bool pack, cudaStream_t s) {
 
 }  // namespace
 
+cudaError_t check_ckpt_pack(const CkptParams &P) { return check(P, true); }
 cudaError_t launch_ckpt_pack(const CkptParams &P, cudaStream_t s) { return launch(P, true, s); }
 cudaError_t launch_ckpt_restore(const CkptParams &P, cudaStream_t s) { return launch(P, false, s); }
 

@@ -19,6 +19,11 @@ struct rs_plan {
     int device = -1;
     int32_t *d_kept = nullptr;
     int32_t *d_all = nullptr;
+    // Page-locked copy of kept_unit, made when the plan is created (null when
+    // no CUDA device could be reached then, or the plan is larger than the
+    // fixed table of rs_ckpt_pack_noalloc): the source of that call's
+    // asynchronous table copy.
+    int32_t *h_kept_pinned = nullptr;
 };
 
 namespace rs {
@@ -29,6 +34,9 @@ constexpr int kStepThreads = 384;    // threads per CTA of the step kernel (sing
 // leave it the registers it needs (255 per thread) without spilling.
 constexpr int step_threads(int max_tokens) { return max_tokens > 1 ? 256 : kStepThreads; }
 constexpr int kMaxRowMap = 8192;     // bytes of row maps carried in the launch params
+// Retained units per checkpoint that rs_ckpt_pack_noalloc's fixed device
+// table holds (int32 entries: 1 MiB).
+constexpr int64_t kNoallocTableEntries = int64_t(1) << 18;
 
 struct StepParams {
     void *pool;
@@ -128,7 +136,15 @@ struct CkptParams {
     int32_t units_per_layer;
 };
 cudaError_t launch_ckpt_pack(const CkptParams &P, cudaStream_t s);
+// cudaErrorNotSupported when launch_ckpt_pack would refuse P's shape (no launch).
+cudaError_t check_ckpt_pack(const CkptParams &P);
 cudaError_t launch_ckpt_restore(const CkptParams &P, cudaStream_t s);
+
+// Record e as the library's last CUDA error (rs_last_cuda_error) and return
+// RS_ERR_CUDA; fail_launch maps cudaErrorNotSupported (a combination that is
+// not built) to RS_ERR_UNSUPPORTED first.  Defined in rs_api.cu.
+int32_t fail_cuda(cudaError_t e);
+int32_t fail_launch(cudaError_t e);
 
 // Per-device cached attributes.
 int device_sm_count();

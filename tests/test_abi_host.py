@@ -92,7 +92,7 @@ def test_row_map_puts_selected_channels_first(L):
     assert st == 0
     pi = np.zeros((4, 64), np.int16)
     assert L.rs_layout_row_map(h, pi.ctypes.data) == 0
-    assert np.array_equal(pi, gen.row_map(hi, 64))
+    assert np.array_equal(pi, orc.row_map(hi, 64))
     L.rs_layout_destroy(h)
 
 
@@ -187,6 +187,24 @@ def test_host_validation_returns_before_launch(L):
     mode = ctypes.c_int32(-1)
     assert L.rs_layout_quant(h, ctypes.byref(mode)) == 0 and mode.value == _abi.RS_QUANT_IEEE
     L.rs_layout_destroy(h)
+
+
+def test_noalloc_pack_refuses_a_plan_one_unit_beyond_its_table(L):
+    """rs_ckpt_pack_noalloc holds at most 262,144 retained units; one more is
+    refused on the host, before any CUDA call (the pointers are never read)."""
+    st, lay = make_layout(L, _abi.RS_LAYOUT_FP32, dk=64, Hv=64, Hk=1)
+    assert st == 0
+    keep = np.zeros((65, 64 * 64), np.uint8)
+    keep[:64] = 1
+    keep[64, 17] = 1  # 262,145 retained units
+    plan = ctypes.c_void_p()
+    assert L.rs_plan_create(ctypes.byref(plan), lay, 65, _abi.RS_UNIT_CHANNEL,
+                            keep.ctypes.data) == 0
+    fake = ctypes.c_void_p(1 << 20)
+    assert L.rs_ckpt_pack_noalloc(plan, fake, 1 << 24, 1, fake, fake, 1, fake, 1, None,
+                                  None) == _abi.RS_ERR_UNSUPPORTED
+    L.rs_plan_destroy(plan)
+    L.rs_layout_destroy(lay)
 
 
 def test_plan_offsets_match_golden_and_oracle(L):

@@ -55,6 +55,30 @@ def test_noalloc_pack_matches_pack_on_two_calls():
         assert same_bits(host(out), host(ref)), f"call {call + 1} differs from rs_ckpt_pack"
 
 
+def test_noalloc_pack_at_exactly_the_table_size():
+    """A plan retaining exactly 262,144 units fills every entry of the fixed
+    table: the call is accepted and its bytes equal rs_ckpt_pack's."""
+    ensure_built()
+    L, slots, Hv, d, n = 64, 2, 64, 64, 2
+    lay = rs.Layout("fp32", d, Hv, 1)
+    keep = np.ones((L, Hv * d), np.uint8)  # 64 layers x 4,096 key channels = 262,144
+    g = torch.Generator(device="cuda").manual_seed(5)
+    pool = torch.randn((L, slots, Hv, d, d), device="cuda", generator=g)
+    src_d = dev(np.array([1, 0], np.int32))
+    dst_d = dev(np.array([0, 1], np.int32))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ref_plan = rs.Plan(lay, keep, "channel").upload()
+    assert ref_plan.ckpt_slot_bytes == 262144 * d * 4
+    ref = torch.zeros((n, ref_plan.ckpt_slot_bytes), dtype=torch.uint8, device="cuda")
+    rs.ckpt_pack(ref_plan, pool, src_d, dst_d, ref)
+    plan = rs.Plan(lay, keep, "channel")
+    out = torch.full((n, plan.ckpt_slot_bytes), 0xEE, dtype=torch.uint8, device="cuda")
+    assert _pack_noalloc(plan, pool, src_d, dst_d, out, status) == 0
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(out, ref)
+
+
 def test_noalloc_pack_rejects_plans_beyond_the_table():
     ensure_built()
     lay = rs.Layout("fp32", 128, 64, 1)
