@@ -96,6 +96,8 @@ _I64 = ctypes.c_int64
 
 
 def _declare(L):
+    L.orc_row_map.argtypes = [_I, _I, _P, _P]
+    L.orc_row_map.restype = _I
     L.orc_step_tile_f32.argtypes = [_I, _I, _P, _P, _P, _P, _P, _I, _F, _P]
     L.orc_step_tile_f32.restype = None
     L.orc_row_scale.argtypes = [_I, _P]
@@ -107,7 +109,6 @@ def _declare(L):
     L.orc_quant_code_rcp.restype = ctypes.c_int8
     L.orc_quantise_row_m.argtypes = [_I, _P, _I, _P, _P]
     L.orc_mixed_pack_m.argtypes = [_I, _I, _I, _I, _P, _P]
-    L.orc_mixed_unpack_decayed.argtypes = [_I, _I, _I, _P, _P, _P]
     L.orc_convert_f32_to_mixed_m.argtypes = [_I, _I, _I, _I, _P, _P, _P]
     L.orc_convert_f32_to_mixed_m.restype = _I
     L.orc_decode_mixed_m.argtypes = [_I, _I, _I, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P,
@@ -117,7 +118,6 @@ def _declare(L):
                                      _P, _P, _P, _P, _P, _P, _P, _I, _I]
     L.orc_replay_mixed_m.restype = _I
     L.orc_damp_pack_m.argtypes = [_I, _I, _I, _I, _I, _P, _P]
-    L.orc_damp_unpack_decayed.argtypes = [_I, _I, _I, _I, _P, _P, _P]
     L.orc_convert_f32_to_damp_m.argtypes = [_I, _I, _I, _I, _I, _P, _P, _P, _P]
     L.orc_convert_f32_to_damp_m.restype = _I
     L.orc_decode_damp_m.argtypes = [_I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P, _P,
@@ -195,6 +195,20 @@ def _ptr(a):
     return None if a is None else a.ctypes.data
 
 
+def row_map(hi, dk):
+    """Row map of every head: ``hi`` int [Hv][k_hi] selected key channels
+    (any order) -> int16 [Hv][dk], physical row r holding logical channel
+    pi[r] (the selected channels first, each region ascending)."""
+    hi = np.ascontiguousarray(np.asarray(hi).reshape(len(hi), -1), np.int16)
+    out = np.empty((hi.shape[0], dk), np.int16)
+    for h in range(hi.shape[0]):
+        row = np.ascontiguousarray(hi[h])
+        dst = out[h]
+        if lib().orc_row_map(dk, row.size, _ptr(row), _ptr(dst)) != 0:
+            raise ValueError(f"head {h}: selection must be distinct channels in [0, {dk})")
+    return out
+
+
 def step_tile(S, q, k, v, a, beta, want_o=True):
     """One decode step on one tile, in place on ``S`` [dk][dv] (float32).
     ``a`` is a float32 scalar array of shape () / (1,) for GDN or (dk,) for KDA."""
@@ -254,15 +268,6 @@ def mixed_pack(T, khi, mode=0):
     tile = np.zeros(mixed_tile_bytes(dk, dv, khi), np.uint8)
     lib().orc_mixed_pack_m(dk, dv, khi, int(mode), _ptr(T), _ptr(tile))
     return tile
-
-
-def mixed_unpack_decayed(tile, dk, dv, khi, a):
-    """Mode-1 dequantise-and-decay of a tile with per-row decays ``a`` [dk]."""
-    tile = _c(np.ascontiguousarray(tile), np.uint8)
-    a = np.ascontiguousarray(a, np.float32)
-    T = np.zeros((dk, dv), np.float32)
-    lib().orc_mixed_unpack_decayed(dk, dv, khi, _ptr(tile), _ptr(a), _ptr(T))
-    return T
 
 
 def convert_f32_to_mixed(S, khi, pi, mode=0):
@@ -485,14 +490,6 @@ def damp_pack(T, khi, group, mode=0):
     tile = np.zeros(damp_tile_bytes(dk, dv, khi, group), np.uint8)
     lib().orc_damp_pack_m(dk, dv, khi, group, int(mode), _ptr(T), _ptr(tile))
     return tile
-
-
-def damp_unpack_decayed(tile, dk, dv, khi, group, a):
-    tile = _c(np.ascontiguousarray(tile), np.uint8)
-    a = np.ascontiguousarray(a, np.float32)
-    T = np.zeros((dk, dv), np.float32)
-    lib().orc_damp_unpack_decayed(dk, dv, khi, group, _ptr(tile), _ptr(a), _ptr(T))
-    return T
 
 
 def convert_pool_f32_to_damp(pool, khi, group, pi, cs, mode=0):

@@ -149,10 +149,9 @@ void orc_dequantise_row(int n, const int8_t *codes, float s, float *x)
 /*   - code = the integer nearest to the exact product x * RN(1/s), ties to  */
 /*     even (the quotient through the correctly rounded reciprocal, rounded  */
 /*     once); rows whose absmax is inf or NaN keep the IEEE quotient;        */
-/*   - a step that decays a dequantised INT8 row multiplies the row's scale: */
-/*     x = c * RN(s * a_u), since diag(a) diag(s) C = diag(a s) C ([DAMP]    */
-/*     §3.1 Lambda applied to the dequantised state of §3.2 Eq. 6); FP16 rows */
-/*     are decayed as in mode 0, x = RN(h * a_u).                            */
+/*   - everything else is mode 0: the step dequantises, x = RN(c * s), and  */
+/*     then decays, RN(x * a_u), so the FP32 state before requantisation,    */
+/*     its row maxima and scales are those of mode 0 bit for bit.            */
 /* A mode-1 code differs from the mode-0 code only where x/s lies within a   */
 /* few units of 2^-24 |x/s| of a half-integer (the acceptance allowance is   */
 /* 1e-6 max(1, |x/s|)).                                                      */
@@ -279,28 +278,28 @@ void orc_mixed_pack(int dk, int dv, int khi, const float *T, uint8_t *tile)
     orc_mixed_pack_m(dk, dv, khi, 0, T, tile);
 }
 
-/* Mode 1: dequantise and decay in one (see above): FP16 row r gives
- * h * a[r], INT8 row r gives c * RN(s_r * a[r]). */
-void orc_mixed_unpack_decayed(int dk, int dv, int khi, const uint8_t *tile, const float *a, float *T)
+/* Row map of one head ([DAMP] Appendix A.2, Algorithm 1, last step: the
+ * selected high-risk key channels are moved to the front; Appendix A.3
+ * Eq. 17: the permutation P_K reorders the rows of S).  sel holds the khi
+ * selected channels in any order; pi[r] is the logical channel stored in
+ * physical row r.  Reading: the pages do not order the channels inside
+ * either region; here each region keeps ascending channel order.  Returns -1
+ * if sel repeats a channel or names one outside [0, dk). */
+int orc_row_map(int dk, int khi, const int16_t *sel, int16_t *pi)
 {
-    const uint8_t *hi = tile;
-    const uint8_t *lo = tile + (size_t)2 * khi * dv;
-    const uint8_t *sc = tile + (size_t)2 * khi * dv + (size_t)(dk - khi) * dv;
-    int8_t row[ORC_MAX_D];
-    int r, c;
-    for (r = 0; r < khi; ++r)
-        for (c = 0; c < dv; ++c) {
-            uint16_t b;
-            memcpy(&b, hi + hi_offset(dv, r, c), 2);
-            T[(size_t)r * dv + c] = f16_bits_to_f32(b) * a[r];
-        }
-    for (r = khi; r < dk; ++r) {
-        float s;
-        memcpy(&s, sc + (size_t)(r - khi) * 4, 4);
-        for (c = 0; c < dv; ++c)
-            row[c] = (int8_t)lo[lo_offset(dv, r - khi, c)];
-        orc_dequantise_row(dv, row, s * a[r], T + (size_t)r * dv);
+    unsigned char chosen[ORC_MAX_D];
+    int c, j, r = 0;
+    if (dk <= 0 || dk > ORC_MAX_D || khi < 0 || khi > dk) return -1;
+    memset(chosen, 0, sizeof chosen);
+    for (j = 0; j < khi; ++j) {
+        if (sel[j] < 0 || sel[j] >= dk || chosen[sel[j]]) return -1;
+        chosen[sel[j]] = 1;
     }
+    for (c = 0; c < dk; ++c)        /* the selected region, ascending */
+        if (chosen[c]) pi[r++] = (int16_t)c;
+    for (c = 0; c < dk; ++c)        /* then the rest, ascending */
+        if (!chosen[c]) pi[r++] = (int16_t)c;
+    return 0;
 }
 
 /* Logical FP32 head S (rows = key channels) <-> mixed tile with row map pi:
@@ -378,9 +377,8 @@ int orc_decode_f32(int B, int Hk, int Hv, int dk, int dv, int per_channel,
  * coordinates of [DAMP] Appendix A.3 Eq. 18 (inputs gathered by pi, the sums
  * over physical rows in ascending row order), requantise once and write back
  * ([DAMP] Appendix A.4 "Fused decoding").  pi: [Hv][dk].  mode: 0 or 1, the
- * requantisation arithmetic (see orc_quant_code_rcp); in mode 1 the decay is
- * applied while dequantising and the step itself decays by 1 (exact). */
-static const float k_one = 1.0f;
+ * requantisation arithmetic (see orc_quant_code_rcp): the modes differ only
+ * in how the new codes are rounded. */
 
 int orc_decode_mixed_m(int B, int Hk, int Hv, int dk, int dv, int khi, int per_channel, int mode,
                        uint8_t *pool, int n_slots, const int32_t *slot_idx,
@@ -408,17 +406,10 @@ int orc_decode_mixed_m(int B, int Hk, int Hv, int dk, int dv, int khi, int per_c
             ap[r] = per_channel ? alpha[((size_t)b * Hv + h) * dk + ph[r]]
                                 : alpha[(size_t)b * Hv + h];
         }
-        if (mode == 1) {
-            orc_mixed_unpack_decayed(dk, dv, khi, tile, ap, T);
-            orc_step_tile_f32(dk, dv, T, qp, kp, v + ((size_t)b * Hv + h) * dv, &k_one, 0,
-                              beta[(size_t)b * Hv + h],
-                              o ? o + ((size_t)b * Hv + h) * dv : NULL);
-        } else {
-            orc_mixed_unpack(dk, dv, khi, tile, T);
-            orc_step_tile_f32(dk, dv, T, qp, kp, v + ((size_t)b * Hv + h) * dv, ap, 1,
-                              beta[(size_t)b * Hv + h],
-                              o ? o + ((size_t)b * Hv + h) * dv : NULL);
-        }
+        orc_mixed_unpack(dk, dv, khi, tile, T);
+        orc_step_tile_f32(dk, dv, T, qp, kp, v + ((size_t)b * Hv + h) * dv, ap, 1,
+                          beta[(size_t)b * Hv + h],
+                          o ? o + ((size_t)b * Hv + h) * dv : NULL);
         orc_mixed_pack_m(dk, dv, khi, mode, T, tile);
     }
     free(T);
@@ -469,8 +460,7 @@ int orc_replay_f32(int B, int T_max, int Hk, int Hv, int dk, int dv, int per_cha
     return status;
 }
 
-/* mode as in orc_decode_mixed_m: in mode 1 the first token's decay is
- * applied while dequantising, so one replayed token equals one decode step. */
+/* mode as in orc_decode_mixed_m (the requantisation arithmetic only). */
 int orc_replay_mixed_m(int B, int T_max, int Hk, int Hv, int dk, int dv, int khi, int per_channel,
                        int mode, uint8_t *pool, int n_slots, const int32_t *slot_idx,
                        const int32_t *n_accept, const int16_t *pi, const float *q, const float *k,
@@ -499,12 +489,6 @@ int orc_replay_mixed_m(int B, int T_max, int Hk, int Hv, int dk, int dv, int khi
                 qp[r] = qh[ph[r]];
                 kp[r] = kh[ph[r]];
                 ap[r] = per_channel ? alpha[(bt * Hv + h) * dk + ph[r]] : alpha[bt * Hv + h];
-            }
-            if (t == 0 && mode == 1) {
-                orc_mixed_unpack_decayed(dk, dv, khi, tile, ap, T);
-                orc_step_tile_f32(dk, dv, T, qp, kp, v + (bt * Hv + h) * dv, &k_one, 0,
-                                  beta[bt * Hv + h], o ? o + (bt * Hv + h) * dv : NULL);
-                continue;
             }
             if (t == 0)
                 orc_mixed_unpack(dk, dv, khi, tile, T);
@@ -867,32 +851,6 @@ void orc_damp_pack(int dk, int dv, int khi, int group, const float *T, uint8_t *
     orc_damp_pack_m(dk, dv, khi, group, 0, T, tile);
 }
 
-/* Mode 1 (see orc_quant_code_rcp): dequantise and decay in one; the decay of
- * INT8 row r multiplies each of its group scales, c * RN(s_g * a[r]). */
-void orc_damp_unpack_decayed(int dk, int dv, int khi, int group, const uint8_t *tile, const float *a,
-                             float *T)
-{
-    const uint8_t *hi = tile;
-    const uint8_t *lo = tile + (size_t)2 * khi * dv;
-    const uint8_t *sc = tile + (size_t)2 * khi * dv + (size_t)(dk - khi) * dv;
-    int ng = dv / group, r, c, gi;
-    int8_t row[ORC_MAX_D];
-    for (r = 0; r < khi; ++r)
-        for (c = 0; c < dv; ++c) {
-            uint16_t b;
-            memcpy(&b, hi + hi_offset(dv, r, c), 2);
-            T[(size_t)r * dv + c] = f16_bits_to_f32(b) * a[r];
-        }
-    for (r = khi; r < dk; ++r) {
-        for (c = 0; c < dv; ++c)
-            row[c] = (int8_t)lo[lo_offset(dv, r - khi, c)];
-        for (gi = 0; gi < ng; ++gi) {
-            float s;
-            memcpy(&s, sc + ((size_t)(r - khi) * ng + gi) * 4, 4);
-            orc_dequantise_row(group, row + gi * group, s * a[r], T + (size_t)r * dv + gi * group);
-        }
-    }
-}
 
 /* S (logical rows, value order as produced) <-> tile: T[r][c] = S[pi[r]][c]
  * / cs[c] ([DAMP] Appendix A.3 Eq. 17), and back S[pi[r]][c] = T[r][c] * cs[c]. */
@@ -972,15 +930,9 @@ int orc_decode_damp_m(int B, int Hk, int Hv, int dk, int dv, int khi, int group,
             kp[r] = kh[ph[r]];
             ap[r] = per_channel ? alpha[((size_t)b * Hv + h) * dk + ph[r]] : alpha[(size_t)b * Hv + h];
         }
-        if (mode == 1) {
-            orc_damp_unpack_decayed(dk, dv, khi, group, tile, ap, T);
-            damp_step(dk, dv, T, qp, kp, v + ((size_t)b * Hv + h) * dv, cs + (size_t)h * dv, &k_one,
-                      0, beta[(size_t)b * Hv + h], o ? o + ((size_t)b * Hv + h) * dv : NULL);
-        } else {
-            orc_damp_unpack(dk, dv, khi, group, tile, T);
-            damp_step(dk, dv, T, qp, kp, v + ((size_t)b * Hv + h) * dv, cs + (size_t)h * dv, ap, 1,
-                      beta[(size_t)b * Hv + h], o ? o + ((size_t)b * Hv + h) * dv : NULL);
-        }
+        orc_damp_unpack(dk, dv, khi, group, tile, T);
+        damp_step(dk, dv, T, qp, kp, v + ((size_t)b * Hv + h) * dv, cs + (size_t)h * dv, ap, 1,
+                  beta[(size_t)b * Hv + h], o ? o + ((size_t)b * Hv + h) * dv : NULL);
         orc_damp_pack_m(dk, dv, khi, group, mode, T, tile);
     }
     free(T);
@@ -1024,12 +976,6 @@ int orc_replay_damp_m(int B, int T_max, int Hk, int Hv, int dk, int dv, int khi,
                 qp[r] = qh[ph[r]];
                 kp[r] = kh[ph[r]];
                 ap[r] = per_channel ? alpha[(bt * Hv + h) * dk + ph[r]] : alpha[bt * Hv + h];
-            }
-            if (t == 0 && mode == 1) {
-                orc_damp_unpack_decayed(dk, dv, khi, group, tile, ap, T);
-                damp_step(dk, dv, T, qp, kp, v + (bt * Hv + h) * dv, cs + (size_t)h * dv, &k_one, 0,
-                          beta[bt * Hv + h], o ? o + (bt * Hv + h) * dv : NULL);
-                continue;
             }
             if (t == 0)
                 orc_damp_unpack(dk, dv, khi, group, tile, T);

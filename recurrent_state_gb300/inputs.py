@@ -151,16 +151,6 @@ def hi_rows(Hv: int, dk: int, k_hi: int, seed: int = 0) -> np.ndarray:
     return np.stack([np.sort(g.permutation(dk)[:k_hi]) for _ in range(Hv)]).astype(np.int16)
 
 
-def row_map(hi: np.ndarray, dk: int) -> np.ndarray:
-    """Physical-row -> logical-channel map: the selected channels first, then
-    the rest, each region in ascending channel order.  int16 [Hv][dk]."""
-    out = []
-    for sel in hi:
-        s = set(int(x) for x in sel)
-        out.append(list(sorted(s)) + [c for c in range(dk) if c not in s])
-    return np.asarray(out, np.int16)
-
-
 def n_accept(B: int, T_max: int, seed: int = 0, lo: int = 1) -> np.ndarray:
     """Accepted draft tokens per sequence, uniform over {lo..T_max}."""
     return rng(seed + 104729).integers(lo, T_max + 1, size=B).astype(np.int32)

@@ -26,7 +26,7 @@ def layouts(Hv, Hk, seed=0):
     hi = gen.hi_rows(Hv, D, KHI, seed=seed)
     cs = gen.value_scales(Hv, D, seed=seed)
     return (rs.Layout("fp32", D, Hv, Hk), rs.Layout("damp", D, Hv, Hk, k_hi=KHI, hi_rows=hi, value_scales=cs),
-            gen.row_map(hi, D), cs)
+            orc.row_map(hi, D), cs)
 
 
 def to_damp_gpu(f32, damp, state0):

@@ -60,7 +60,7 @@ def test_packed_layout_decode_f16_inputs(kind, quant):
     w = gen.decode_workload(B=B, Hk=Hk, Hv=Hv, d=D, steps=steps, per_channel=True, in_dtype="f16", seed=seed,
                             horizon=(2.0, 8192.0))
     hi = gen.hi_rows(Hv, D, KHI, seed=seed)
-    pi = gen.row_map(hi, D)
+    pi = orc.row_map(hi, D)
     cs = gen.value_scales(Hv, D, seed=seed) if kind == "damp" else None
     lay = rs.Layout(kind, D, Hv, Hk, k_hi=KHI, hi_rows=hi, value_scales=cs, quant=quant)
     mode = 1 if quant == "fused" else 0
@@ -97,7 +97,7 @@ def test_multi_token_f16_inputs(path):
     o = torch.zeros((B, T, Hv, D), device="cuda")
     o_r = np.zeros((B, T, Hv, D), np.float32)
     hi = gen.hi_rows(Hv, D, KHI, seed=seed)
-    pi = gen.row_map(hi, D)
+    pi = orc.row_map(hi, D)
     if path.endswith("fp32"):
         lay = rs.Layout("fp32", D, Hv, Hk)
         pool, ref = dev(w.state0), w.state0.copy()

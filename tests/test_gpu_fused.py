@@ -36,7 +36,7 @@ def layouts(Hv, Hk, seed=0, kind="mixed"):
     hi = gen.hi_rows(Hv, D, KHI, seed=seed)
     cs = gen.value_scales(Hv, D, seed=seed) if kind == "damp" else None
     lay = rs.Layout(kind, D, Hv, Hk, k_hi=KHI, hi_rows=hi, value_scales=cs, quant="fused")
-    return rs.Layout("fp32", D, Hv, Hk), lay, gen.row_map(hi, D), cs
+    return rs.Layout("fp32", D, Hv, Hk), lay, orc.row_map(hi, D), cs
 
 
 def to_packed_gpu(f32, lay, state0):

@@ -40,7 +40,7 @@ def guarded(nbytes, fill):
 def test_packed_decode_touches_only_the_batch(kind, quant, per_channel):
     B, Hk, Hv, n_slots = 5, 2, 4, 9
     hi = gen.hi_rows(Hv, D, KHI, seed=21)
-    pi = gen.row_map(hi, D)
+    pi = orc.row_map(hi, D)
     cs = gen.value_scales(Hv, D, seed=21) if kind == "damp" else None
     f32 = rs.Layout("fp32", D, Hv, Hk)
     lay = rs.Layout(kind, D, Hv, Hk, k_hi=KHI, hi_rows=hi, value_scales=cs, quant=quant)

@@ -37,7 +37,7 @@ def to_packed(lay, state0, Hv, Hk):
 def layout(kind, Hv, Hk, seed, quant):
     hi = gen.hi_rows(Hv, D, KHI, seed=seed)
     cs = gen.value_scales(Hv, D, seed=seed) if kind == "damp" else None
-    return rs.Layout(kind, D, Hv, Hk, k_hi=KHI, hi_rows=hi, value_scales=cs, quant=quant), gen.row_map(hi, D), cs
+    return rs.Layout(kind, D, Hv, Hk, k_hi=KHI, hi_rows=hi, value_scales=cs, quant=quant), orc.row_map(hi, D), cs
 
 
 def oracle_pool(kind, state0, pi, cs, mode):

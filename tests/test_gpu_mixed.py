@@ -31,7 +31,7 @@ def _built():
 def layouts(Hv, Hk, seed=0):
     hi = gen.hi_rows(Hv, D, KHI, seed=seed)
     return (rs.Layout("fp32", D, Hv, Hk), rs.Layout("mixed", D, Hv, Hk, k_hi=KHI, hi_rows=hi),
-            gen.row_map(hi, D))
+            orc.row_map(hi, D))
 
 
 def to_mixed_gpu(f32_lay, mix_lay, state0):

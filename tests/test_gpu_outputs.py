@@ -37,7 +37,7 @@ def packed(kind, Hv, Hk, seed, quant):
     hi = gen.hi_rows(Hv, D, KHI, seed=seed)
     cs = gen.value_scales(Hv, D, seed=seed) if kind == "damp" else None
     lay = rs.Layout(kind, D, Hv, Hk, k_hi=KHI, hi_rows=hi, value_scales=cs, quant=quant)
-    return lay, gen.row_map(hi, D), cs
+    return lay, orc.row_map(hi, D), cs
 
 
 def to_packed(lay, state0, Hv, Hk):

@@ -30,7 +30,7 @@ def _built():
 
 def mixed_layout(Hv, Hk, seed, quant):
     hi = gen.hi_rows(Hv, D, KHI, seed=seed)
-    return rs.Layout("mixed", D, Hv, Hk, k_hi=KHI, hi_rows=hi, quant=quant), gen.row_map(hi, D)
+    return rs.Layout("mixed", D, Hv, Hk, k_hi=KHI, hi_rows=hi, quant=quant), orc.row_map(hi, D)
 
 
 def to_mixed(f32, lay, state0):
@@ -154,7 +154,7 @@ def test_prefill_and_replay_on_damp_layout(quant, per_channel):
     w = gen.decode_workload(B=B, Hk=Hk, Hv=Hv, d=D, steps=L, per_channel=per_channel,
                             in_dtype="bf16", seed=seed, horizon=(2.0, 8192.0))
     hi = gen.hi_rows(Hv, D, KHI, seed=seed)
-    pi = gen.row_map(hi, D)
+    pi = orc.row_map(hi, D)
     cs = gen.value_scales(Hv, D, seed=seed)
     lay = rs.Layout("damp", D, Hv, Hk, k_hi=KHI, hi_rows=hi, value_scales=cs, quant=quant)
     f32 = rs.Layout("fp32", D, Hv, Hk)

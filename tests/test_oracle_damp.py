@@ -40,7 +40,7 @@ def test_group_dv_unscaled_is_the_row_layout():
     assert np.array_equal(orc.damp_pack(T, 8, 64), orc.mixed_pack(T, 8))
     B, Hv, d = 3, 2, 32
     hi = gen.hi_rows(Hv, d, 4, seed=2)
-    pi = gen.row_map(hi, d)
+    pi = orc.row_map(hi, d)
     w = gen.decode_workload(B=B, Hk=Hv, Hv=Hv, d=d, steps=1, per_channel=True, in_dtype="f32", seed=3)
     a = orc.convert_pool_f32_to_mixed(w.state0, 4, pi)
     b = a.copy()
@@ -109,7 +109,7 @@ def test_pow2_value_scaling_equivariance(per_channel):
 def test_replay_one_token_equals_decode():
     B, Hv, d = 3, 2, D
     hi = gen.hi_rows(Hv, d, KHI, seed=8)
-    pi = gen.row_map(hi, d)
+    pi = orc.row_map(hi, d)
     w = gen.decode_workload(B=B, Hk=Hv, Hv=Hv, d=d, steps=2, per_channel=True, in_dtype="f32", seed=9)
     cs = gen.value_scales(Hv, d, seed=10)
     a = orc.convert_pool_f32_to_damp(w.state0, KHI, G, pi, cs)

@@ -31,7 +31,7 @@ def test_error_recursion_eq12_eq13(mode):
     w = gen.decode_workload(B=B, Hk=Hk, Hv=Hv, d=d, steps=T, per_channel=True, in_dtype="f32",
                             seed=90 + mode, horizon=(2.0, 64.0))
     hi = gen.hi_rows(Hv, d, khi, seed=90)
-    pi = gen.row_map(hi, d)
+    pi = orc.row_map(hi, d)
     pool = orc.convert_pool_f32_to_mixed(w.state0, khi, pi, mode=mode)
 
     def logical():

@@ -5,8 +5,8 @@ s = max(a, 1e-8)/127, code = clip(round(x/s), -127, 127), FP32) and the step
 (DAMP Appendix A.4: dequantise, decay and update in FP32, requantise), not how
 a kernel evaluates x/s or where the decay's rounding falls.  Mode 1 is the
 division-free reading: the code is the integer nearest to the exact product
-x * RN(1/s) (ties to even), and the decay of an INT8 row multiplies its scale,
-c * RN(s * a) (diag(a) diag(s) C = diag(a s) C).
+x * RN(1/s) (ties to even); the step itself (dequantise c * s, decay, update)
+is mode 0's, so only the rounding of the new codes differs.
 
 Pins, each independent of the oracle's own formulas:
   - the code against exact rational arithmetic (``fractions.Fraction``),
@@ -15,11 +15,11 @@ Pins, each independent of the oracle's own formulas:
     only where the exact quotient lies within the acceptance allowance,
     1e-6 max(1, |x/s|), of a half-integer; a constructed row where they do
     differ keeps the check from being vacuous;
-  - the dequantise-and-decay against numpy's IEEE float32 arithmetic;
   - one mode-1 step against the FP64 update of the dequantised input (DAMP
     §3.1 Eq. 2), within the local quantisation error of DAMP §3.3 Eq. 9;
   - replay of one token equals a decode step, replay requantises once;
-  - with unit decay the two modes agree on every byte but codes at a tie;
+  - with any decay the two modes agree on every byte but codes at a tie,
+    and a teacher-forced comparison of the two meets the acceptance rule;
   - the same for the DAMP-exact layout (INT8 groups of 32 along dv).
 """
 from fractions import Fraction
@@ -30,6 +30,7 @@ import pytest
 import oracle as orc
 from recurrent_state_gb300 import inputs as gen
 
+from .acceptance import Tally, compare_tile, reference_step_mixed
 from .test_oracle_mixed import damp_eq2_step, logical
 
 
@@ -169,26 +170,6 @@ def test_constructed_row_where_the_modes_differ():
     pytest.fail("no row found where the two quotients round differently")
 
 
-def test_unpack_decayed_matches_numpy_float32():
-    dk, dv, khi = 16, 32, 4
-    g = gen.rng(105)
-    T = (g.standard_normal((dk, dv)) * 0.3).astype(np.float32)
-    tile = orc.mixed_pack(T, khi)
-    a = g.uniform(0.2, 1.0, dk).astype(np.float32)
-    got = orc.mixed_unpack_decayed(tile, dk, dv, khi, a)
-    plain = orc.mixed_unpack(tile, dk, dv, khi)           # h and c * s
-    lo = tile[2 * khi * dv: 2 * khi * dv + (dk - khi) * dv].view(np.int8)
-    sc = tile[2 * khi * dv + (dk - khi) * dv:].view(np.float32)
-    for r in range(dk):
-        if r < khi:
-            exp = plain[r] * a[r]                           # float32 * float32
-        else:
-            q = r - khi
-            codes = np.array([lo[((q // 4) * dv + c) * 4 + q % 4] for c in range(dv)], np.int8)
-            exp = codes.astype(np.float32) * np.float32(sc[q] * a[r])
-        assert np.array_equal(got[r].view(np.uint32), exp.astype(np.float32).view(np.uint32)), r
-
-
 def make_strong(seed, per_channel, B=3, Hk=2, Hv=4, d=32, khi=4, steps=4, mode=1):
     w = gen.decode_workload(B=B, Hk=Hk, Hv=Hv, d=d, steps=steps, per_channel=per_channel,
                             in_dtype="bf16", seed=seed)
@@ -197,7 +178,7 @@ def make_strong(seed, per_channel, B=3, Hk=2, Hv=4, d=32, khi=4, steps=4, mode=1
     # outside the quantisation error
     w.alpha[...] = g.uniform(0.3, 0.9, w.alpha.shape).astype(np.float32)
     hi = gen.hi_rows(Hv, d, khi, seed=seed)
-    pi = gen.row_map(hi, d)
+    pi = orc.row_map(hi, d)
     pool = orc.convert_pool_f32_to_mixed(w.state0, khi, pi, mode=mode)
     return w, pi, pool
 
@@ -297,12 +278,11 @@ def split_tile(tile, d, khi):
 
 
 @pytest.mark.parametrize("per_channel", [False, True])
-def test_unit_decay_modes_agree_but_at_ties(per_channel):
-    """alpha = 1: c * RN(s * 1) = c * s, so both modes run the same FP32 step
-    and differ only in how the new codes are rounded."""
+def test_modes_agree_but_at_ties(per_channel):
+    """Both modes run the same FP32 step (strong decays here) and differ only
+    in how the new codes are rounded."""
     d, khi = 64, 8
     w, pi, pool = make_strong(113, per_channel, B=4, Hk=2, Hv=4, d=d, khi=khi, mode=0)
-    w.alpha[...] = 1.0
     p0, p1 = pool.copy(), pool.copy()
     o0, _ = orc.decode_mixed(p0, w.slot_idx, pi, khi, d, d, w.q[0], w.k[0], w.v[0], w.alpha[0],
                              w.beta[0], mode=0)
@@ -326,30 +306,10 @@ def make_damp(seed, per_channel, B=2, Hk=2, Hv=2, steps=3):
     g = gen.rng(seed + 2000)
     w.alpha[...] = g.uniform(0.3, 0.9, w.alpha.shape).astype(np.float32)
     hi = gen.hi_rows(Hv, DD, DKHI, seed=seed)
-    pi = gen.row_map(hi, DD)
+    pi = orc.row_map(hi, DD)
     cs = gen.value_scales(Hv, DD, seed=seed, group=DG)
     pool = orc.convert_pool_f32_to_damp(w.state0, DKHI, DG, pi, cs, mode=1)
     return w, pi, cs, pool
-
-
-def test_damp_unpack_decayed_matches_numpy_float32():
-    g = gen.rng(120)
-    T = (g.standard_normal((DD, DD)) * 0.2).astype(np.float32)
-    tile = orc.damp_pack(T, DKHI, DG, mode=1)
-    a = g.uniform(0.2, 1.0, DD).astype(np.float32)
-    got = orc.damp_unpack_decayed(tile, DD, DD, DKHI, DG, a)
-    plain = orc.damp_unpack(tile, DD, DD, DKHI, DG)
-    lo = tile[2 * DKHI * DD: 2 * DKHI * DD + (DD - DKHI) * DD].view(np.int8)
-    sc = tile[2 * DKHI * DD + (DD - DKHI) * DD:].view(np.float32).reshape(DD - DKHI, DD // DG)
-    for r in range(DD):
-        if r < DKHI:
-            exp = plain[r] * a[r]
-        else:
-            q = r - DKHI
-            codes = np.array([lo[((q // 4) * DD + c) * 4 + q % 4] for c in range(DD)], np.int8)
-            gs = np.repeat(np.float32(sc[q]) * a[r], DG).astype(np.float32)
-            exp = codes.astype(np.float32) * gs
-        assert np.array_equal(got[r].view(np.uint32), exp.astype(np.float32).view(np.uint32)), r
 
 
 @pytest.mark.parametrize("per_channel", [False, True])
@@ -393,3 +353,80 @@ def test_damp_fused_replay_one_equals_decode(per_channel):
                              q, k, v, a, b, mode=1)
     assert st == 0 and np.array_equal(p1, p2)
     assert np.array_equal(o1.view(np.uint32), o2[:, 0].view(np.uint32))
+
+
+# ---- mode 1 against the pages' quantiser under real decays ---------------
+@pytest.mark.parametrize("layout", ["mixed", "damp"])
+def test_reference_step_is_the_oracle_mode0_step(layout):
+    """The teacher-forced reference (unpack, one FP32 step, IEEE requantise)
+    is the oracle's batched mode-0 decode, byte for byte."""
+    d, khi, Hv = 128, 16, 4
+    group = DG if layout == "damp" else 0
+    w = gen.decode_workload(B=3, Hk=2, Hv=Hv, d=d, steps=1, per_channel=True, in_dtype="bf16",
+                            seed=41, horizon=(2.0, 8192.0))
+    pi = orc.row_map(gen.hi_rows(Hv, d, khi, seed=41), d)
+    cs = gen.value_scales(Hv, d, seed=41) if group else None
+    if group:
+        pool = orc.convert_pool_f32_to_damp(w.state0, khi, group, pi, cs)
+        before = pool.copy()
+        o, _ = orc.decode_damp(pool, w.slot_idx, pi, cs, khi, group, d, d, w.q[0], w.k[0], w.v[0],
+                               w.alpha[0], w.beta[0])
+    else:
+        pool = orc.convert_pool_f32_to_mixed(w.state0, khi, pi)
+        before = pool.copy()
+        o, _ = orc.decode_mixed(pool, w.slot_idx, pi, khi, d, d, w.q[0], w.k[0], w.v[0],
+                                w.alpha[0], w.beta[0])
+    for b in range(w.B):
+        s = w.slot_idx[b]
+        for h in range(Hv):
+            g_ = h // (Hv // w.Hk)
+            tile, _, o_r = reference_step_mixed(before[s, h], pi[h], w.q[0, b, g_], w.k[0, b, g_],
+                                                w.v[0, b, h], w.alpha[0, b, h], w.beta[0, b, h],
+                                                d, d, khi, group, None if cs is None else cs[h])
+            assert np.array_equal(tile, pool[s, h])
+            assert np.array_equal(o_r.view(np.uint32), o[b, h].view(np.uint32))
+
+
+@pytest.mark.parametrize("layout,per_channel", [("mixed", True), ("mixed", False), ("damp", True)])
+def test_fused_mode_meets_the_acceptance_rule_under_decay(layout, per_channel):
+    """Teacher-forced, with real decays (alpha != 1, so the two modes also
+    round the decay differently): every step, one mode-1 step and one step of
+    the pages' quantiser (mode 0) start from the same packed bytes; codes must
+    be equal except +-1 within 1e-6 max(1, |x/s|) of a rounding boundary,
+    scales and FP16 rows within one ulp, o within 1e-3 (dasc Appendix E.1
+    Eq. 8; DAMP §3.2 Eq. 5-6)."""
+    d, khi = 128, 16
+    group = DG if layout == "damp" else 0
+    Hk, Hv = (4, 4) if per_channel else (2, 4)
+    w = gen.decode_workload(B=12, Hk=Hk, Hv=Hv, d=d, steps=6, per_channel=per_channel,
+                            in_dtype="bf16", seed=43,
+                            horizon=(2.0, 8192.0) if per_channel else (4.0, 4096.0))
+    pi = orc.row_map(gen.hi_rows(Hv, d, khi, seed=43), d)
+    cs = gen.value_scales(Hv, d, seed=43) if group else None
+    if group:
+        pool = orc.convert_pool_f32_to_damp(w.state0, khi, group, pi, cs, mode=1)
+    else:
+        pool = orc.convert_pool_f32_to_mixed(w.state0, khi, pi, mode=1)
+    tally = Tally()
+    for t in range(w.steps):
+        before = pool.copy()
+        if group:
+            o1, st = orc.decode_damp(pool, w.slot_idx, pi, cs, khi, group, d, d, w.q[t], w.k[t],
+                                     w.v[t], w.alpha[t], w.beta[t], mode=1)
+        else:
+            o1, st = orc.decode_mixed(pool, w.slot_idx, pi, khi, d, d, w.q[t], w.k[t], w.v[t],
+                                      w.alpha[t], w.beta[t], mode=1)
+        assert st == 0
+        for b in range(w.B):
+            s = w.slot_idx[b]
+            for h in range(Hv):
+                g_ = h // (Hv // Hk)
+                ref, x, o_r = reference_step_mixed(before[s, h], pi[h], w.q[t, b, g_], w.k[t, b, g_],
+                                                   w.v[t, b, h], w.alpha[t, b, h], w.beta[t, b, h],
+                                                   d, d, khi, group, None if cs is None else cs[h])
+                compare_tile(tally, pool[s, h], ref, x, o1[b, h], o_r, d, d, khi, group,
+                             where=f"step {t} seq {b} head {h}")
+    assert tally.ok(), tally.failures[:5]
+    # the modes share the FP32 step: scales, FP16 rows and o agree exactly
+    assert tally.scale_ulp_max == 0 and tally.fp16_ulp_max == 0 and tally.o_rel_max == 0.0
+    assert tally.codes == w.steps * w.B * Hv * (d - khi) * d

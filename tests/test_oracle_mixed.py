@@ -30,7 +30,7 @@ def make(seed, per_channel, B=3, Hk=2, Hv=4, d=32, khi=4, steps=6):
     w = gen.decode_workload(B=B, Hk=Hk, Hv=Hv, d=d, steps=steps, per_channel=per_channel,
                             in_dtype="bf16", seed=seed, horizon=(2.0, 8192.0))
     hi = gen.hi_rows(Hv, d, khi, seed=seed)
-    pi = gen.row_map(hi, d)
+    pi = orc.row_map(hi, d)
     pool = orc.convert_pool_f32_to_mixed(w.state0, khi, pi)
     return w, pi, pool
 

@@ -26,6 +26,7 @@ from . import test_oracle_fused as fz
 from . import test_oracle_mixed as mx
 from . import test_oracle_quant as qt
 from . import test_oracle_recurrence as rc
+from . import test_oracle_row_map as rm
 
 
 def _tiny():
@@ -48,6 +49,7 @@ CHECKS = [
     ("ckpt_golden", ck.test_golden_offsets_and_order),
     ("ckpt_numpy", lambda: ck.test_pack_matches_numpy_statement(1, 0.45)),
     ("ckpt_restore", lambda: ck.test_restore_zero_fills_and_roundtrips(0, 0.5)),
+    ("row_map_golden", rm.test_hand_worked_row_maps),
     ("mixed_perm", mx.test_permutation_is_applied_to_inputs),
     ("mixed_bound", lambda: mx.test_mixed_step_within_local_quantisation_error(True)),
     ("mixed_replay", lambda: mx.test_mixed_replay_requantises_once(True)),
@@ -61,10 +63,9 @@ CHECKS = [
     ("fused_code", fz.test_rcp_code_is_nearest_integer_to_exact_product),
     ("fused_once", fz.test_rcp_code_rounds_the_exact_product_once),
     ("fused_constructed", fz.test_constructed_row_where_the_modes_differ),
-    ("fused_unpack", fz.test_unpack_decayed_matches_numpy_float32),
     ("fused_bound", lambda: fz.test_fused_step_within_local_quantisation_error(True)),
     ("fused_replay", lambda: fz.test_fused_replay_one_equals_decode(True)),
-    ("damp_fused_unpack", fz.test_damp_unpack_decayed_matches_numpy_float32),
+    ("fused_acceptance", lambda: fz.test_fused_mode_meets_the_acceptance_rule_under_decay("mixed", True)),
     ("error_recursion", lambda: ep.test_error_recursion_eq12_eq13(0)),
 ]
 
@@ -110,6 +111,16 @@ MUTATIONS = {
         ("memcpy(ckpt + ((size_t)d * off[L] + (size_t)(off[l] + j)) * ub,",
          "memcpy(ckpt + ((size_t)d * off[L] + (size_t)(off[l + 1] - 1 - j)) * ub,")],
     "restore_no_zero_fill": [("memset(dst, 0, ub);", "(void)dst;")],
+    "row_map_rest_descending": [("for (c = 0; c < dk; ++c)        /* then the rest, ascending */",
+                                 "for (c = dk - 1; c >= 0; --c)  /* then the rest, ascending */")],
+    "row_map_selection_last": [("    for (c = 0; c < dk; ++c)        /* the selected region, ascending */\n"
+                                "        if (chosen[c]) pi[r++] = (int16_t)c;\n"
+                                "    for (c = 0; c < dk; ++c)        /* then the rest, ascending */\n"
+                                "        if (!chosen[c]) pi[r++] = (int16_t)c;",
+                                "    for (c = 0; c < dk; ++c)        /* then the rest, ascending */\n"
+                                "        if (!chosen[c]) pi[r++] = (int16_t)c;\n"
+                                "    for (c = 0; c < dk; ++c)        /* the selected region, ascending */\n"
+                                "        if (chosen[c]) pi[r++] = (int16_t)c;")],
     "mixed_q_unpermuted": [("qp[r] = qh[ph[r]];", "qp[r] = qh[r];")],
     "mixed_alpha_unpermuted": [("? alpha[((size_t)b * Hv + h) * dk + ph[r]]",
                                 "? alpha[((size_t)b * Hv + h) * dk + r]")],
@@ -120,19 +131,9 @@ MUTATIONS = {
          "            orc_mixed_pack_m(dk, dv, khi, mode, T, tile);\n"
          "            orc_mixed_unpack(dk, dv, khi, tile, T);\n        }\n"
          "        orc_mixed_pack_m(dk, dv, khi, mode, T, tile);")],
-    "fused_decay_twice": [("&k_one, 0,\n                              beta[(size_t)b * Hv + h],",
-                           "ap, 1,\n                              beta[(size_t)b * Hv + h],")],
     "fused_double_rounding": [("double r = rint((double)x * (double)y);",
                                "double r = rint((double)(x * y));")],
     "fused_mode_ignored": [("if (mode == 1 && a <= FLT_MAX) {", "if (0) {")],
-    "fused_int8_decay_dropped": [("orc_dequantise_row(dv, row, s * a[r], T + (size_t)r * dv);",
-                                  "orc_dequantise_row(dv, row, s, T + (size_t)r * dv);")],
-    "fused_replay_first_decayed_twice": [
-        ("&k_one, 0,\n                                  beta[bt * Hv + h]",
-         "ap, 1,\n                                  beta[bt * Hv + h]")],
-    "damp_fused_group_decay_dropped": [
-        ("orc_dequantise_row(group, row + gi * group, s * a[r], T + (size_t)r * dv + gi * group);",
-         "orc_dequantise_row(group, row + gi * group, s, T + (size_t)r * dv + gi * group);")],
     "replay_skips_first": [("for (t = 0; t < n; ++t) {", "for (t = 1; t < n; ++t) {")],
     "int8_scale_per_unit": [
         ("memcpy(ckpt + (size_t)d * sb + (size_t)cb + (size_t)row * 4, &sc, 4);",

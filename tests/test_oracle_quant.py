@@ -136,7 +136,7 @@ def test_convert_places_logical_rows():
     dk = dv = 32
     khi = 4
     hi = gen.hi_rows(1, dk, khi, seed=3)
-    pi = gen.row_map(hi, dk)[0]
+    pi = orc.row_map(hi, dk)[0]
     assert list(pi[:khi]) == sorted(hi[0].tolist())
     assert sorted(pi.tolist()) == list(range(dk))
     assert list(pi[khi:]) == sorted(pi[khi:].tolist())
