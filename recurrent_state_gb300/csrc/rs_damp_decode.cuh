@@ -11,11 +11,8 @@
 // c'_v enter as v' = v / c' before the prediction error and o = c' o' after
 // the readout chain.  Every value is computed with the same operations in the
 // same order as the oracle's transformed step.
-// Fused arithmetic (FUSED): when the row vectors are built, each INT8 row's
-// group scales in the stage are multiplied by the row's decay in place
-// (RN(s_g a_u); the stage is not written back), so the
-// passes dequantise with c * RN(s_g a_u) and no decay multiply; each new code
-// is one fused multiply-add, the integer nearest to x * RN(1/s).
+// Fused arithmetic (FUSED): each new code is one fused multiply-add, the
+// integer nearest to x * RN(1/s); the step itself is the same.
 #pragma once
 
 #include "rs_damp.h"
@@ -164,15 +161,6 @@ __global__ void __launch_bounds__(512, 1) damp_decode_kernel(const __grid_consta
                 wv[2 * D + 2 * tt + i] = load_as_f32<TI>(reinterpret_cast<const TI *>(tb + S::kVecBytes) + src);
                 const float ar = KDA ? reinterpret_cast<const float *>(tb + 3 * S::kVecBytes)[src] : alpha0;
                 if (KDA) wv[3 * D + 2 * tt + i] = ar;
-                if constexpr (FUSED) {  // decay folded into the row's group scales
-                    const int r = 2 * tt + i;
-                    if (r >= KH) {
-                        float4 *g4 = reinterpret_cast<float4 *>(st + 2 * KH * D + (D - KH) * D) + (r - KH);
-                        const float4 sg = *g4;
-                        *g4 = make_float4(__fmul_rn(sg.x, ar), __fmul_rn(sg.y, ar), __fmul_rn(sg.z, ar),
-                                          __fmul_rn(sg.w, ar));
-                    }
-                }
             }
         }
         // value-scaling factors of this lane's columns; v' = v / c'
@@ -229,7 +217,7 @@ __global__ void __launch_bounds__(512, 1) damp_decode_kernel(const __grid_consta
                 const float fb = __uint_as_float(__byte_perm(wb, 0x4B000000u, sel));
                 x[i] = __fmul2_rn(__fadd2_rn(make_float2(fa, fb), nb), s2);
             }
-            if constexpr (!FUSED) decay(KH / 4 + qd, x);
+            decay(KH / 4 + qd, x);
         };
         auto predict = [&](int q, const float2 (&x)[4], float2 &p) {
             const float4 k4 = K4[q];

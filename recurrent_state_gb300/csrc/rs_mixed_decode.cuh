@@ -24,10 +24,8 @@
 // rs_step.cuh).  The new words go from registers straight to HBM (a lane
 // stores its 8 bytes of a word row, so a warp writes 256 contiguous bytes),
 // and the stage is free as soon as both warps have read it.
-// With the fused arithmetic (FUSED) the decay of INT8 row u is applied to
-// its scale when the row vectors are built (RN(s_u a_u), so dequantising is
-// c * RN(s_u a_u) and needs no decay multiply), and each new code is one
-// fused multiply-add, the integer nearest to x * RN(1/s).
+// With the fused arithmetic (FUSED) each new code is one fused multiply-add,
+// the integer nearest to x * RN(1/s); the step itself is the same.
 //
 // A CTA runs P = W / WPT tile slots over a ring of NS > P stages.  Its tiles
 // are numbered j = 0, 1, ... (tile blockIdx.x + j * gridDim.x of the
@@ -54,9 +52,8 @@ struct MixedWarpShape {
     static constexpr int kVecBytes = D * (int)sizeof(TI);
     static constexpr int kTokBytes = 3 * kVecBytes + (KDA ? D * 4 : 0);  // k, q, v (+ alpha)
     static constexpr int kStage = (kStatePad + kTokBytes + 127) / 128 * 128;
-    // K, BK, Q (+ A: the decay of each row; fused: RN(s_u a_u) for INT8 rows),
-    // floats in row order
-    static constexpr int kRowVecs = (KDA || FUSED) ? 4 : 3;
+    // K, BK, Q (+ A: the decay of each row), floats in row order
+    static constexpr int kRowVecs = KDA ? 4 : 3;
     static constexpr int kBlock = 16;             // rows per requantisation block
     // per tile slot: row vectors, partial row maxima [2][WPT][kBlock], and
     // per warp -s and 1/s of the current block
@@ -281,12 +278,7 @@ __global__ void __launch_bounds__(256 * WPT, 1)
                 wv[c0 + i] = kf;
                 wv[D + c0 + i] = __fmul_rn(beta0, kf);
                 wv[2 * D + c0 + i] = load_as_f32<TI>(reinterpret_cast<const TI *>(tb + S::kVecBytes) + src);
-                if constexpr (FUSED) {
-                    const float ar = KDA ? reinterpret_cast<const float *>(tb + 3 * S::kVecBytes)[src] : alpha0;
-                    const int r = c0 + i;
-                    const float *scl = reinterpret_cast<const float *>(st + 2 * KH * D + (D - KH) * D);
-                    wv[3 * D + r] = r < KH ? ar : __fmul_rn(scl[r - KH], ar);
-                } else if (KDA) {
+                if constexpr (KDA) {
                     wv[3 * D + c0 + i] = reinterpret_cast<const float *>(tb + 3 * S::kVecBytes)[src];
                 }
             }
@@ -311,7 +303,7 @@ __global__ void __launch_bounds__(256 * WPT, 1)
         float *scales_g = reinterpret_cast<float *>(dst + 2 * KH * D + (D - KH) * D);
 
         auto decay = [&](int q, Quad<CPL> &X) {  // rows 4q..4q+3 times their decay
-            const float4 a = (KDA || FUSED) ? A4[q] : make_float4(alpha0, alpha0, alpha0, alpha0);
+            const float4 a = KDA ? A4[q] : make_float4(alpha0, alpha0, alpha0, alpha0);
             const float ar[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i)
@@ -338,8 +330,7 @@ __global__ void __launch_bounds__(256 * WPT, 1)
             lds_words<CPL>(low + qd * D, wd);
 #pragma unroll
             for (int t = 0; t < CPL; ++t) wd[t] ^= 0x80808080u;
-            // fused: the decayed scales RN(s a) of the row vectors; otherwise the stored scales
-            const float4 s4 = FUSED ? A4[KH / 4 + qd] : sc4[qd];
+            const float4 s4 = sc4[qd];
             const float sr[4] = {s4.x, s4.y, s4.z, s4.w};
             const float2 nb = make_float2(-kCodeBias, -kCodeBias);
 #pragma unroll
@@ -352,7 +343,7 @@ __global__ void __launch_bounds__(256 * WPT, 1)
                     X.x[i][k] = __fmul2_rn(__fadd2_rn(make_float2(fa, fb), nb), make_float2(sr[i], sr[i]));
                 }
             }
-            if constexpr (!FUSED) decay(KH / 4 + qd, X);
+            decay(KH / 4 + qd, X);
         };
         auto predict = [&](int q, const Quad<CPL> &X, float2 (&p)[NP]) {
             const float4 k4 = K4[q];

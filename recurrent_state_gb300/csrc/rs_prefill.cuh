@@ -201,30 +201,7 @@ __global__ void __launch_bounds__(prefill_threads(KHI), 1) prefill_kernel(const 
 #pragma unroll
             for (int j = 0; j < DP; ++j) x[j] = make_float2(st[(2 * j) * D + tid], st[(2 * j + 1) * D + tid]);
         } else if constexpr (GRP) {
-            float *dsc = nullptr;
-            if constexpr (FUSED) {  // token 0's decay of INT8 row tid into its group scales
-                if (tid >= KH) {
-                    constexpr int NG = D / kDampGroup;
-                    const float *sc0 = reinterpret_cast<const float *>(tile + 2 * KH * D + (D - KH) * D);
-                    const float a_u = KDA ? rowv[4 * D + tid] : a_cur;
-#pragma unroll
-                    for (int gi = 0; gi < NG; ++gi)
-                        red[(tid - KH) * NG + gi] = __fmul_rn(sc0[(tid - KH) * NG + gi], a_u);
-                }
-                group_sync(bar_id, D);
-                dsc = red;
-            }
-            damp_dequant<D, KH>(tile, tid, x, dsc);
-        } else if constexpr (FUSED) {
-            // fused arithmetic: token 0's decay of INT8 row u goes into its
-            // scale, RN(s_u a_u), so dequantising gives c * RN(s_u a_u) and
-            // token 0 skips the decay of the INT8 rows
-            if (tid >= KH) {
-                const float s_u = reinterpret_cast<const float *>(tile + 2 * KH * D + (D - KH) * D)[tid - KH];
-                scl[tid - KH] = __fmul_rn(s_u, KDA ? rowv[4 * D + tid] : a_cur);
-            }
-            group_sync(bar_id, D);
-            mixed_dequant<D, KH>(tile, tid, x, scl);
+            damp_dequant<D, KH>(tile, tid, x, nullptr);
         } else {
             mixed_dequant<D, KH>(tile, tid, x);
         }
@@ -237,14 +214,12 @@ __global__ void __launch_bounds__(prefill_threads(KHI), 1) prefill_kernel(const 
             if (more) load_tok(t + 1, kn, qn, vn, an, bn);  // latency hidden by the passes below
 
             float p = 0.0f;
-            const bool dec_lo = !(MIXED && FUSED) || t > 0;  // fused: token 0's INT8 decay is in the scales
 #pragma unroll
             for (int j = 0; j < DP; j += 2) {
                 const float4 kk = *reinterpret_cast<const float4 *>(rv + 2 * j);
                 float4 aa;
                 if (KDA) aa = *reinterpret_cast<const float4 *>(rv + 4 * D + 2 * j);
                 else aa = make_float4(a_cur, a_cur, a_cur, a_cur);
-                if (2 * j >= KH && !dec_lo) aa = make_float4(1.0f, 1.0f, 1.0f, 1.0f);  // x * 1 = x
                 x[j] = __fmul2_rn(x[j], make_float2(aa.x, aa.y));
                 x[j + 1] = __fmul2_rn(x[j + 1], make_float2(aa.z, aa.w));
                 p = __fmaf_rn(x[j].x, kk.x, p);

@@ -456,15 +456,6 @@ __global__ void __launch_bounds__(step_threads(MAXT), 1)
                 rv[3 * D + tid] = load_as_f32<TI>(vt + tid);  // value coordinates: no row map
                 const float at = KDA ? reinterpret_cast<const float *>(tb + 3 * S::kVecBytes)[src] : decay_of(t);
                 if (KDA) rv[4 * D + tid] = at;
-                if constexpr (MIXED && FUSED && MAXT > 1) {
-                    // fused arithmetic: the first token's decay of INT8 row tid goes
-                    // into the row's scale in the stage, RN(s a); dequantising then
-                    // gives c * RN(s a) and token 0 skips that row's decay
-                    if (t == 0 && tid >= KH) {
-                        float *scl_st = reinterpret_cast<float *>(stage + 2 * KH * D + (D - KH) * D);
-                        scl_st[tid - KH] = __fmul_rn(scl_st[tid - KH], at);
-                    }
-                }
             }
         }
         group_sync(bar_id, D);  // row vectors visible (FP32: stage fully read)
@@ -544,8 +535,6 @@ __global__ void __launch_bounds__(step_threads(MAXT), 1)
                 float4 aa;
                 if (KDA) aa = *reinterpret_cast<const float4 *>(rv + 4 * D + 2 * j);
                 else { const float a_s = decay_of(t); aa = make_float4(a_s, a_s, a_s, a_s); }
-                // fused arithmetic: token 0's decay of the INT8 rows is in their scales
-                if (MIXED && FUSED && t == 0 && 2 * j >= KH) aa = make_float4(1.0f, 1.0f, 1.0f, 1.0f);
                 return aa;
             };
             float p = 0.0f;
