@@ -69,6 +69,8 @@ __global__ void __launch_bounds__(512, 1) damp_decode_kernel(const __grid_consta
     }
     for (int i = threadIdx.x; i < Hv * D; i += blockDim.x) pi_s[i] = P.pi[i];
     fence_mbar_init();
+    pdl_launch_next();
+    pdl_wait();  // the previous kernel's writes are visible from here on
     __syncthreads();
 
     auto tile_sync = [&]() { group_sync(1 + ps, 32 * WPT); };
@@ -110,15 +112,20 @@ __global__ void __launch_bounds__(512, 1) damp_decode_kernel(const __grid_consta
 
     auto tile_beta = [&](int it) -> float { return it < items ? P.beta[it] : 0.0f; };
     auto tile_alpha = [&](int it) -> float { return (!KDA && it < items) ? P.alpha[it] : 0.0f; };
+    // pool slot of a tile (for its stores), read one tile ahead too
+    auto tile_slot = [&](int it) -> int32_t { return it < items ? P.slot_idx[it / Hv] : -1; };
     float nbeta = tile_beta(item_of(ps)), nalpha = tile_alpha(item_of(ps));
+    int32_t nslot = tile_slot(item_of(ps));
     const bool l0 = lane & 1, l1 = lane & 2, l2 = lane & 4, l3 = lane & 8;
 
     for (int j = ps;; j += NSLOT) {
         const int it = item_of(j);
         if (it >= items) break;
         const float beta0 = nbeta, alpha0 = nalpha;
+        const int32_t slot = nslot;
         nbeta = tile_beta(item_of(j + NSLOT));
         nalpha = tile_alpha(item_of(j + NSLOT));
+        nslot = tile_slot(item_of(j + NSLOT));
         const int s = j % NS;
         const int32_t use = j / NS;
 
@@ -137,7 +144,6 @@ __global__ void __launch_bounds__(512, 1) damp_decode_kernel(const __grid_consta
             return;
         }
         const int b = it / Hv, h = it - b * Hv;
-        const int32_t slot = P.slot_idx[b];
         if (!slot_ok(slot)) {
             if (tt == 0) {
                 report(P.status, 1);

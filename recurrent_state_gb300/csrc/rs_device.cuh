@@ -31,6 +31,18 @@ __device__ __forceinline__ void fence_mbar_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
+// Programmatic dependent launch.  A kernel launched with the
+// programmatic-stream-serialization attribute (launch_pdl) may begin while
+// the kernel before it in the stream is still finishing; pdl_wait blocks
+// until that kernel has completed and its memory writes are visible, so a
+// kernel calls it before its first global-memory access.  Without the
+// attribute it returns at once.  pdl_launch_next lets the next such kernel
+// in the stream start launching (it still waits in its own pdl_wait).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_next() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Order this thread's earlier generic-proxy shared-memory accesses before
 // later async-proxy (TMA) accesses to the same memory.
 __device__ __forceinline__ void fence_proxy_async_smem() {

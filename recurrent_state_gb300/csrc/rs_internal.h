@@ -146,6 +146,26 @@ cudaError_t launch_ckpt_restore(const CkptParams &P, cudaStream_t s);
 int32_t fail_cuda(cudaError_t e);
 int32_t fail_launch(cudaError_t e);
 
+// Launch kern<<<grid, block, smem, s>>>(args...) with programmatic stream
+// serialization: its CTAs may be scheduled while the previous kernel in the
+// stream drains (kernels launched this way call pdl_wait before touching
+// global memory), which hides the launch gap between back-to-back steps.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
+
 // Per-device cached attributes.
 int device_sm_count();
 int device_max_smem_optin();

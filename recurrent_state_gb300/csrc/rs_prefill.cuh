@@ -148,6 +148,8 @@ __global__ void __launch_bounds__(prefill_threads(KHI), 1) prefill_kernel(const 
     const TI *k_g = static_cast<const TI *>(P.k);
     const TI *v_g = static_cast<const TI *>(P.v);
     TO *og = static_cast<TO *>(P.o);
+    pdl_launch_next();
+    pdl_wait();  // the previous kernel's writes are visible from here on
 
     for (int item = blockIdx.x * G + grp; item < items; item += gridDim.x * G) {
         const int b = item / Hv, h = item - (item / Hv) * Hv;
@@ -289,8 +291,7 @@ cudaError_t run(PT &P, cudaStream_t s) {
     if (grid < 1) grid = 1;
     cudaError_t e = set_dynamic_smem(reinterpret_cast<const void *>(kern), smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, G * D, smem, s>>>(P);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(G * D), smem, s, P);
 }
 
 template <int D, int KHI, bool KDA, bool FUSED, bool GRP, typename PT>

@@ -331,6 +331,8 @@ __global__ void __launch_bounds__(step_threads(MAXT), 1)
     if constexpr (MIXED)
         for (int i = threadIdx.x; i < Hv * D; i += blockDim.x) pi_s[i] = P.pi[i];
     fence_mbar_init();
+    pdl_launch_next();
+    pdl_wait();  // the previous kernel's writes are visible from here on
     __syncthreads();
 
     uint64_t *bar = &bars[grp];

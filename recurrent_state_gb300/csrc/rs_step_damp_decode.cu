@@ -34,8 +34,7 @@ cudaError_t run(StepParamsDamp &P, cudaStream_t s) {
     const int smem = header + NSLOT * Sh::kSlotBytes + NS * Sh::kStage;
     cudaError_t e = set_dynamic_smem(reinterpret_cast<const void *>(kern), smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, NSLOT * 64, smem, s>>>(P);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(NSLOT * 64), smem, s, P);
 }
 
 template <bool KDA, bool FUSED>

@@ -26,8 +26,7 @@ cudaError_t run(StepParamsPi &P, cudaStream_t s) {
     const int smem = header + G * region;
     cudaError_t e = set_dynamic_smem(reinterpret_cast<const void *>(kern), smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, G * D, smem, s>>>(P);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(G * D), smem, s, P);
 }
 
 template <bool KDA, bool FUSED>
