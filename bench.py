@@ -359,7 +359,7 @@ def run_ours(args, rank, world, local_rank):
     if "kernels" in result:
         # the packed-layout and multi-token lines in short, last in the line
         # (the most-read end of a long record), most important last
-        keep = [n for n in result["kernels"] if n.startswith(("ckpt_", "kda_prefill", "kda_replay"))]
+        keep = [n for n in result["kernels"] if n.startswith(("ckpt_", "kda_prefill", "gdn_prefill", "kda_replay"))]
         keep += [n for n in result["kernels"] if n.startswith(("kda_decode_damp", "gdn_decode_mixed",
                                                                 "kda_decode_mixed"))]
         result["packed_summary"] = {
@@ -440,7 +440,7 @@ def rot_info(pools):
 
 EXTRA = ("gdn_tiny", "gdn_fp32", "kda_fp32", "kda_mixed", "gdn_mixed", "kda_damp", "replay_mixed", "replay_fp32",
          "kda_mixed_fused", "kda_mixed_fused_wide", "gdn_mixed_fused", "kda_damp_fused", "replay_mixed_fused", "replay_sweep",
-         "prefill_fp32", "prefill_mixed_fused",
+         "prefill_fp32", "prefill_mixed_fused", "prefill_chunked",
          "pack_gdn", "restore_gdn", "pack_kda", "restore_kda", "pack_int8_gdn", "restore_int8_gdn",
          "pack_int8_kda", "restore_int8_kda", "pack_mixed", "restore_mixed")
 
@@ -701,6 +701,33 @@ def extra_kernels(args, rs, torch, dev, peak, world, only=None):
             del mpool, ppools
         del pool, pq, pk, pv, pa, pb, po
         torch.cuda.empty_cache()
+
+    # prefill in the chunk-parallel form on the tensor cores: FP32 state, KDA and GDN, 32 and 64 tokens
+    if "prefill_chunked" in want:
+        for kda, Lc in ((True, 32), (True, 64), (False, 32)):
+            cfg = dict(KDA_B) if kda else dict(GDN, B=B)
+            w = gen.decode_workload(steps=Lc, per_channel=kda, in_dtype="bf16", seed=4,
+                                    horizon=(2.0, 8192.0) if kda else (4.0, 4096.0), **cfg)
+
+            def bt(x):
+                return np.ascontiguousarray(np.swapaxes(x, 0, 1))
+            pq, pk, pv = to_bf16(bt(w.q_bits)), to_bf16(bt(w.k_bits)), to_bf16(bt(w.v_bits))
+            pa, pb = to_dev(bt(w.alpha)), to_dev(bt(w.beta))
+            slots = to_dev(w.slot_idx)
+            Hk, Hv = cfg["Hk"], cfg["Hv"]
+            po = torch.empty((B, Lc, Hv, 128), device=dev)
+            f32 = rs.Layout("fp32", 128, Hv, Hk)
+            pool = to_dev(w.state0)  # 512 MiB: larger than four L2 capacities
+            qk_tok = 2 * Hk * 128 * 2 / Hv          # q and k (bf16) per value head and token
+            per_tok = Hv * (qk_tok + 128 * 2 + (128 * 4 if kda else 4) + 4 + 128 * 4)
+            sec = _time(torch, lambda i: rs.prefill_update(f32, kda, pool, slots, pq, pk, pv, pa, pb, o=po,
+                                                           chunked=True), max(3, iters // 10), warm)
+            rec(f"{'kda' if kda else 'gdn'}_prefill_chunked_fp32_b{B}_L{Lc}", sec,
+                2 * B * Hv * f32.head_bytes + int(B * Lc * per_tok), B * Hv * Lc,
+                {"chunk_tokens": Lc, "form": "chunk-parallel, tcgen05 kind::tf32 (3 products per pair)"},
+                tile_tokens=B * Hv * Lc)
+            del pool, pq, pk, pv, pa, pb, po
+            torch.cuda.empty_cache()
 
     # dasc pack / restore: 36 layers, 64 checkpoints, 64 pool slots
     for unit, p, name in ((0, 0.5, "gdn"), (1, 0.45, "kda")):

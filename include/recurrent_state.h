@@ -287,6 +287,27 @@ rs_status rs_prefill_update(const rs_layout *l, int32_t per_channel_decay, void 
                             int32_t in_dtype, const float *alpha, const float *beta, void *o,
                             int32_t out_dtype, int32_t *status, void *stream);
 
+/* Prefill chunk in the chunk-parallel form, on the tensor cores.  Same
+ * arguments, layouts and status bits as rs_prefill_update, and the same map
+ * ([DAMP] Appendix A.4 "Prefill path"; [SRA] "Kernels follow the serving
+ * phase": prefill exposes parallel work across a chunk's tokens): the tokens
+ * are taken 16 at a time, and each group is applied as dense products on
+ * the tensor cores (the written rows W solve (I + diag(beta) A) W =
+ * diag(beta)(V - Khat S0), with A the decay-weighted key Gram matrix; the
+ * outputs and the new state follow from W).  The products use tf32 operands
+ * split into a high part and an exact remainder, with fp32 accumulation, so
+ * the result equals the token-by-token recurrence up to rounding (about
+ * 1e-6 relative), not bit for bit.  Built for the FP32 layout with
+ * dk = dv = 128; other layouts return RS_ERR_UNSUPPORTED before any launch.
+ * Use rs_prefill_update where bit-exactness with single decode steps is
+ * needed. */
+rs_status rs_prefill_chunked_update(const rs_layout *l, int32_t per_channel_decay, void *pool,
+                                    int64_t n_slots, const int32_t *slot_idx, int32_t B,
+                                    int32_t L, const int32_t *n_tokens, const void *q,
+                                    const void *k, const void *v, int32_t in_dtype,
+                                    const float *alpha, const float *beta, void *o,
+                                    int32_t out_dtype, int32_t *status, void *stream);
+
 /* Convert n slots between two layouts of the same shape (FP32 -> mixed
  * quantises with the rules above; mixed -> FP32 dequantises and un-permutes
  * rows; same kind copies).  slots: device int32 [n], used as both source and

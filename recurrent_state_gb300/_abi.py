@@ -34,7 +34,7 @@ EXPORTS = (
     "rs_status_string", "rs_last_cuda_error", "rs_version",
     "rs_layout_create", "rs_layout_create_damp", "rs_layout_destroy", "rs_layout_head_bytes", "rs_layout_row_map",
     "rs_layout_bits_per_value", "rs_layout_set_quant", "rs_layout_quant",
-    "rs_gdn_decode_update", "rs_kda_decode_update", "rs_spec_replay_update", "rs_prefill_update",
+    "rs_gdn_decode_update", "rs_kda_decode_update", "rs_spec_replay_update", "rs_prefill_update", "rs_prefill_chunked_update",
     "rs_state_convert",
     "rs_plan_create", "rs_plan_destroy", "rs_plan_offsets", "rs_plan_upload",
     "rs_ckpt_pack", "rs_ckpt_restore", "rs_ckpt_pack_noalloc",
@@ -103,6 +103,7 @@ def _declare(L):
                                         _P, _P, _P, _I32, _P, _P]
     L.rs_prefill_update.argtypes = [_P, _I32, _P, _I64, _P, _I32, _I32, _P, _P, _P, _P, _I32,
                                     _P, _P, _P, _I32, _P, _P]
+    L.rs_prefill_chunked_update.argtypes = L.rs_prefill_update.argtypes
     L.rs_state_convert.argtypes = [_P, _P, _P, _P, _I64, _P, _I32, _P, _P]
     L.rs_plan_create.argtypes = [ctypes.POINTER(_P), _P, _I32, _I32, _P]
     L.rs_plan_destroy.argtypes = [_P]

@@ -178,10 +178,12 @@ def spec_replay_update(layout, per_channel_decay, pool, slot_idx, n_accept, q, k
 
 
 def prefill_update(layout, per_channel_decay, pool, slot_idx, q, k, v, alpha, beta, n_tokens=None,
-                   o=None, status=None, stream=None):
+                   o=None, status=None, stream=None, chunked=False):
     """Apply a prefill chunk of L tokens (inputs [B][L][...]) to each sequence's
     state, read and written once; ``n_tokens`` [B] int32 limits each sequence
-    to its first n_tokens[b] tokens (default: all L)."""
+    to its first n_tokens[b] tokens (default: all L).  ``chunked``: the
+    chunk-parallel form on the tensor cores (rs_prefill_chunked_update; FP32
+    layout; equal to the recurrence up to rounding)."""
     n_slots = _pool_slots(layout, pool)
     _dev(slot_idx, "slot_idx", torch.int32)
     _dev(n_tokens, "n_tokens", torch.int32)
@@ -193,10 +195,11 @@ def prefill_update(layout, per_channel_decay, pool, slot_idx, q, k, v, alpha, be
     _dev(status, "status", torch.int32)
     B, L = q.shape[0], q.shape[1]
     out_dt = _DT[o.dtype] if o is not None else _abi.RS_F32
-    check(_abi.lib().rs_prefill_update(
+    fn = "rs_prefill_chunked_update" if chunked else "rs_prefill_update"
+    check(getattr(_abi.lib(), fn)(
         layout.handle, int(bool(per_channel_decay)), _ptr(pool), n_slots, _ptr(slot_idx), B, L,
         _ptr(n_tokens), _ptr(q), _ptr(k), _ptr(v), _DT[q.dtype], _ptr(alpha), _ptr(beta), _ptr(o),
-        out_dt, _ptr(status), _stream(stream)), "rs_prefill_update")
+        out_dt, _ptr(status), _stream(stream)), fn)
     return o
 
 

@@ -243,7 +243,7 @@ static rs_status prefill_common(const rs_layout *l, int32_t per_channel_decay, v
                                 const int32_t *slot_idx, int32_t B, int32_t L, const int32_t *n_tokens,
                                 const void *q, const void *k, const void *v, int32_t in_dtype,
                                 const float *alpha, const float *beta, void *o, int32_t out_dtype,
-                                int32_t *status, void *stream);
+                                int32_t *status, void *stream, bool chunked);
 
 static rs_status step_common(const rs_layout *l, bool kda, bool replay, void *pool, int64_t n_slots,
                              const int32_t *slot_idx, int32_t B, int32_t T_max,
@@ -306,7 +306,7 @@ static rs_status step_common(const rs_layout *l, bool kda, bool replay, void *po
             // n_accept[b] of them applied (same arithmetic, same status bits)
             if (replay)
                 return prefill_common(l, kda ? 1 : 0, pool, n_slots, slot_idx, B, T_max, n_accept, q, k, v,
-                                      in_dtype, alpha, beta, o, out_dtype, status, stream);
+                                      in_dtype, alpha, beta, o, out_dtype, status, stream, false);
             static thread_local rs::StepParamsDamp P;
             fill(P);
             for (size_t i = 0; i < l->pi.size(); ++i) P.pi[i] = (uint8_t)l->pi[i];
@@ -356,14 +356,23 @@ rs_status rs_prefill_update(const rs_layout *l, int32_t per_channel_decay, void 
                             const float *alpha, const float *beta, void *o, int32_t out_dtype,
                             int32_t *status, void *stream) {
     return prefill_common(l, per_channel_decay, pool, n_slots, slot_idx, B, L, n_tokens, q, k, v, in_dtype,
-                          alpha, beta, o, out_dtype, status, stream);
+                          alpha, beta, o, out_dtype, status, stream, false);
+}
+
+rs_status rs_prefill_chunked_update(const rs_layout *l, int32_t per_channel_decay, void *pool,
+                                    int64_t n_slots, const int32_t *slot_idx, int32_t B, int32_t L,
+                                    const int32_t *n_tokens, const void *q, const void *k, const void *v,
+                                    int32_t in_dtype, const float *alpha, const float *beta, void *o,
+                                    int32_t out_dtype, int32_t *status, void *stream) {
+    return prefill_common(l, per_channel_decay, pool, n_slots, slot_idx, B, L, n_tokens, q, k, v, in_dtype,
+                          alpha, beta, o, out_dtype, status, stream, true);
 }
 
 static rs_status prefill_common(const rs_layout *l, int32_t per_channel_decay, void *pool, int64_t n_slots,
                                 const int32_t *slot_idx, int32_t B, int32_t L, const int32_t *n_tokens,
                                 const void *q, const void *k, const void *v, int32_t in_dtype,
                                 const float *alpha, const float *beta, void *o, int32_t out_dtype,
-                                int32_t *status, void *stream) {
+                                int32_t *status, void *stream, bool chunked) {
     if (!l || (per_channel_decay != 0 && per_channel_decay != 1)) return RS_ERR_INVALID_ARG;
     if (B < 0 || L < 0 || n_slots < 0 || n_slots > INT32_MAX) return RS_ERR_INVALID_ARG;
     if (dtype_size(in_dtype) == 0 || (out_dtype != RS_F32 && out_dtype != RS_BF16)) return RS_ERR_INVALID_ARG;
@@ -399,7 +408,12 @@ static rs_status prefill_common(const rs_layout *l, int32_t per_channel_decay, v
         for (size_t i = 0; i < l->pi.size() && i < (size_t)rs::kMaxRowMap; ++i) P.pi[i] = (uint8_t)l->pi[i];
     };
     cudaError_t e;
-    if (l->group) {  // DAMP-exact layout: group scales and value-scaling factors
+    if (chunked) {  // the tensor-core form: FP32 layout only
+        if (l->p.kind != RS_LAYOUT_FP32 || D != 128) return RS_ERR_UNSUPPORTED;
+        static thread_local rs::PrefillParams P;
+        fill(P);
+        e = rs::launch_prefill_chunked(Ln, P, static_cast<cudaStream_t>(stream));
+    } else if (l->group) {  // DAMP-exact layout: group scales and value-scaling factors
         static thread_local rs::PrefillParamsDamp P;
         fill(P);
         std::copy(l->cs.begin(), l->cs.end(), P.cs);

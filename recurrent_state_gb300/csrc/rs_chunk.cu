@@ -1,0 +1,520 @@
+// rs_chunk.cu -- prefill chunks in the chunk-parallel form on the tensor
+// cores (sm_103a, FP32 state layout).
+//
+// DAMP Appendix A.4 "Prefill path" (prefill runs FP32 arithmetic within a
+// chunk) and "Serving recurrent attention", "Kernels follow the serving
+// phase" (prefill exposes parallel work across a chunk's tokens).  The
+// recurrence of DAMP §3.1 Eq. 1-2 over C tokens, started from state S0
+// (rows u = key channels, columns v = value dimensions), is evaluated as
+//     Gamma_t  = prod_{s<=t} diag(alpha_s)             (cumulative decay)
+//     A[t][i]  = sum_c k_t[c] k_i[c] prod_{s=i+1..t} alpha_s[c]     (i < t)
+//     Bm[t][i] = sum_c q_t[c] k_i[c] prod_{s=i+1..t} alpha_s[c]     (i <= t)
+//     R        = diag(beta) (V - Khat S0),   Khat[t] = Gamma_t k_t
+//     W        = (I + diag(beta) A)^{-1} R   (the rows the tokens write)
+//     O        = Qhat S0 + Bm W,             Qhat[t] = Gamma_t q_t
+//     S_C      = Gamma_C S0 + Ktil^T W,      Ktil[i] = k_i prod_{s=i+1..C} alpha_s
+// (the same map as C decode steps; tests/test_chunk_form.py checks the
+// algebra against the oracle's recurrence).  Every decay product is a
+// product of alphas in (0, 1], so nothing overflows whatever the decays.
+//
+// One CTA of 256 threads per SM takes (sequence, head) tiles in turn; the
+// two threads v and v + 128 share value column v, which is tensor-memory
+// lane v of every M = 128 product below (each takes half of the column's
+// key channels or tokens).  The state lives in tensor memory as S^T (lane v, columns
+// u) across the chunks of a tile.  Per chunk of C = 16 tokens:
+//   MMA 1   [P^T | Oq^T] = S0^T [Khat ; Qhat]^T      (K = 128, N = 2C)
+//   MMA 2   W^T = R^T T^T, T = (I + diag(beta) A)^{-1}  (K = C, N = C)
+//   MMA 3   O^T = Oq^T + W^T Bm^T                      (K = C, N = C)
+//   MMA 4   S_C^T = Gamma_C S0^T + W^T Ktil             (K = C, N = 128)
+// all of kind::tf32 with each fp32 operand split into a tf32 high part and
+// an exact remainder (three products: hi*hi + hi*lo + lo*hi, about 2^-21
+// relative), fp32 accumulation in tensor memory.  The C x C matrices A, Bm
+// and the unit lower triangular inverse T run on the CUDA cores while MMA 1
+// runs: A[t][i] = Khat_t . Kchk_i and Bm[t][i] = Qhat_t . Kchk_i with
+// Kchk_i = k_i / Gamma_i (the decay products factor through the cumulative
+// decay), unless some cumulative decay of the chunk falls below 1e-30, where
+// each pair takes the running product of its decays instead.  The result equals the token-by-token recurrence up to rounding (not
+// bit for bit: the order of the sums differs).
+#include "rs_internal.h"
+#include "rs_device.cuh"
+#include "rs_tc.cuh"
+#include "../../include/recurrent_state.h"
+
+namespace rs {
+
+namespace {
+
+__device__ __forceinline__ void report_bits(int32_t *status, int32_t bits) {
+    if (status) atomicOr(status, bits);
+}
+
+constexpr int D = 128;        // dk = dv
+constexpr int C = 16;         // tokens per chunk
+constexpr int kThreads = 256;  // two threads per value column
+constexpr uint32_t kTmemCols = 256;
+
+// shared memory (bytes): tf32 operands in the K-major core-matrix layout of
+// rs_tc.cuh, hi and lo parts; staged token inputs; small matrices
+constexpr int kSA = D * D * 4;      // S0^T (M = v, K = u)
+constexpr int kB1 = 2 * C * D * 4;  // [Khat ; Qhat] (N = 2C, K = u)
+constexpr int kCC = C * C * 4;      // T or Bm (N = t, K = i)
+constexpr int kKT = D * C * 4;      // Ktil^T (N = c, K = i)
+constexpr int kA2 = D * C * 4;      // R^T, then W^T (M = v, K = t)
+constexpr int DP = D + 4;           // padded row of the staged token vectors (bank spread)
+constexpr int kTok = C * DP * 4;    // k, q or alpha of the chunk, [t][c] fp32
+constexpr int oSAh = 0, oSAl = oSAh + kSA, oB1h = oSAl + kSA, oB1l = oB1h + kB1;
+constexpr int oTh = oB1l + kB1, oTl = oTh + kCC, oBh = oTl + kCC, oBl = oBh + kCC;
+constexpr int oKTh = oBl + kCC, oKTl = oKTh + kKT, oA2h = oKTl + kKT, oA2l = oA2h + kA2;
+constexpr int oK = oA2l + kA2, oQ = oK + kTok, oAl = oQ + kTok;
+constexpr int oBeta = oAl + kTok, oGc = oBeta + C * 4, oMA = oGc + D * 4, oMB = oMA + kCC;
+constexpr int oBar = oMB + kCC, oTslot = oBar + 3 * 8;
+constexpr int kSmem = oTslot + 16;
+static_assert(kSmem <= 232448, "fits the shared memory of one SM");
+static_assert(oBar % 8 == 0 && oSAl % 1024 == 0 && oB1h % 16 == 0, "alignment");
+
+// tensor-memory columns: S^T [0, 128), P^T [128, 128 + C), Oq^T [.., + C), W^T [.., + C)
+constexpr uint32_t cS = 0, cP = D, cOq = D + C, cW = D + 2 * C;
+
+// store x as a tf32 pair (hi, exact remainder) at byte offset off of the two buffers
+__device__ __forceinline__ void put_split(uint8_t *hi, uint8_t *lo, uint32_t off, float x) {
+    const float h = tc::tf32_hi(x);
+    *reinterpret_cast<float *>(hi + off) = h;
+    *reinterpret_cast<float *>(lo + off) = x - h;
+}
+// four consecutive K values of one row (16 bytes, off 16-aligned)
+__device__ __forceinline__ void put_split4(uint8_t *hi, uint8_t *lo, uint32_t off, float a, float b, float c,
+                                           float d) {
+    const float4 h = make_float4(tc::tf32_hi(a), tc::tf32_hi(b), tc::tf32_hi(c), tc::tf32_hi(d));
+    *reinterpret_cast<float4 *>(hi + off) = h;
+    *reinterpret_cast<float4 *>(lo + off) = make_float4(a - h.x, b - h.y, c - h.z, d - h.w);
+}
+
+template <bool KDA, typename TI, typename TO>
+__global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid_constant__ PrefillParams P) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int tid = threadIdx.x, w = tid >> 5;
+    const int v = tid & (D - 1);  // value column (and key channel c in the per-channel work)
+    const int hf = tid >> 7;      // which half of the column's channels / tokens
+    float *kS = reinterpret_cast<float *>(smem + oK);   // [t][DP]: k, then Khat (fast form)
+    float *qS = reinterpret_cast<float *>(smem + oQ);   // [t][DP]: q, then Qhat (fast form)
+    float *aS = reinterpret_cast<float *>(smem + oAl);  // [t][DP]: alpha, then Kchk (fast form)
+    float *betaS = reinterpret_cast<float *>(smem + oBeta);
+    float *gC = reinterpret_cast<float *>(smem + oGc);
+    float *mA = reinterpret_cast<float *>(smem + oMA);
+    float *mB = reinterpret_cast<float *>(smem + oMB);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + oBar);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + oTslot);
+
+    if (tid == 0)
+        for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
+    fence_mbar_init();
+    if (w == 0) {
+        tc::tmem_alloc(tslot, kTmemCols);
+        tc::tmem_relinquish();
+    }
+    pdl_launch_next();
+    pdl_wait();  // the previous kernel's writes are visible from here on
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tm = *tslot + ((uint32_t)(32 * (w & 3)) << 16);  // this warp's 32 lanes
+
+    const int Hv = P.Hv, Hk = P.Hk, L = P.L;
+    const int items = P.B * Hv;
+    const TI *q_g = static_cast<const TI *>(P.q);
+    const TI *k_g = static_cast<const TI *>(P.k);
+    const TI *v_g = static_cast<const TI *>(P.v);
+    TO *o_g = static_cast<TO *>(P.o);
+    uint32_t ph = 0;  // parity of the three barriers: each completes once per chunk
+    bool failed = false;
+
+    auto wait = [&](int k) -> bool {
+        const bool ok = mbar_wait_bounded(&bars[k], ph) || mbar_wait_bounded(&bars[k], ph);
+        return __syncthreads_and(ok);
+    };
+
+    for (int item = blockIdx.x; item < items && !failed; item += gridDim.x) {
+        const int b = item / Hv, h = item - b * Hv, g = h / (Hv / Hk);
+        const int32_t slot = P.slot_idx[b];
+        const int32_t n = P.n_tokens ? P.n_tokens[b] : L;
+        // every thread sees the same item: the skips are uniform
+        if (slot < 0 || (int64_t)slot >= P.n_slots) {
+            if (tid == 0) report_bits(P.status, 1);
+            continue;
+        }
+        if (n < 0 || n > L) {
+            if (tid == 0) report_bits(P.status, 2);
+            continue;
+        }
+        if (n == 0) continue;
+        float *Sg = static_cast<float *>(P.pool) + ((size_t)slot * Hv + h) * D * D;
+
+        for (int t0 = 0; t0 < n && !failed; t0 += C) {
+            const int nt = min(C, n - t0);
+            // ---- the chunk's inputs: thread (v, hf) loads channel v of tokens 8 hf .. 8 hf + 7
+            // (pads: k = q = 0, alpha = 1, beta = 0), and value v of the same tokens for R
+            float vt[C / 2];
+            {
+                float kv[C / 2], qv[C / 2], av[C / 2];
+#pragma unroll
+                for (int j = 0; j < C / 2; ++j) {
+                    const int t = (C / 2) * hf + j;
+                    kv[j] = 0.0f, qv[j] = 0.0f, av[j] = 1.0f, vt[j] = 0.0f;
+                    if (t < nt) {
+                        const size_t bt = (size_t)b * L + t0 + t;
+                        kv[j] = load_as_f32<TI>(k_g + (bt * Hk + g) * D + v);
+                        qv[j] = load_as_f32<TI>(q_g + (bt * Hk + g) * D + v);
+                        av[j] = KDA ? P.alpha[(bt * Hv + h) * D + v] : P.alpha[bt * Hv + h];
+                        vt[j] = load_as_f32<TI>(v_g + (bt * Hv + h) * D + v);
+                    }
+                }
+                const float bv = tid < nt ? P.beta[((size_t)b * L + t0 + tid) * Hv + h] : 0.0f;
+#pragma unroll
+                for (int j = 0; j < C / 2; ++j) {
+                    const int t = (C / 2) * hf + j;
+                    kS[t * DP + v] = kv[j];
+                    qS[t * DP + v] = qv[j];
+                    aS[t * DP + v] = av[j];
+                }
+                if (tid < C) betaS[tid] = bv;
+            }
+            __syncthreads();
+            // ---- channel c = v: cumulative decays Gamma_t[c]; the factored form if none is tiny
+            const int c = v;
+            float gam[C];
+            {
+                float pg = 1.0f;
+#pragma unroll
+                for (int t = 0; t < C; ++t) {
+                    pg = __fmul_rn(pg, aS[t * DP + c]);
+                    gam[t] = pg;
+                }
+            }
+            const bool fast = __syncthreads_and(gam[C - 1] >= 1e-30f);
+            if (hf == 0) {  // Khat rows, Kchk, Ktil^T row c, Gamma_C[c]
+#pragma unroll
+                for (int t = 0; t < C; ++t) {
+                    const float kr = kS[t * DP + c];
+                    const float kh = __fmul_rn(kr, gam[t]);
+                    put_split(smem + oB1h, smem + oB1l, tc::kmajor_offset(t, c, D), kh);
+                    if (fast) {
+                        kS[t * DP + c] = kh;
+                        const float kc = __fdiv_rn(kr, gam[t]);
+                        aS[t * DP + c] = kc;
+                        put_split(smem + oKTh, smem + oKTl, tc::kmajor_offset(c, t, C), __fmul_rn(kc, gam[C - 1]));
+                    }
+                }
+                if (!fast) {
+                    float tail = 1.0f;  // prod_{s=i+1..C-1} alpha_s[c]
+#pragma unroll
+                    for (int i = C - 1; i >= 0; --i) {
+                        put_split(smem + oKTh, smem + oKTl, tc::kmajor_offset(c, i, C),
+                                  __fmul_rn(kS[i * DP + c], tail));
+                        tail = __fmul_rn(tail, aS[i * DP + c]);
+                    }
+                }
+                gC[c] = gam[C - 1];
+            } else {  // Qhat rows
+#pragma unroll
+                for (int t = 0; t < C; ++t) {
+                    const float qh = __fmul_rn(qS[t * DP + c], gam[t]);
+                    put_split(smem + oB1h, smem + oB1l, tc::kmajor_offset(C + t, c, D), qh);
+                    if (fast) qS[t * DP + c] = qh;
+                }
+            }
+            __syncthreads();  // Gamma_C of every channel
+            // ---- S0^T (hi, lo) as the A operand, Gamma_C S0^T as MMA 4's accumulator:
+            // thread (v, hf) takes key channels 64 hf .. 64 hf + 63 of column v
+            {
+                const int ub = 64 * hf;
+                float x[64];
+                if (t0 == 0) {
+#pragma unroll
+                    for (int u = 0; u < 64; ++u) x[u] = Sg[(size_t)(ub + u) * D + v];
+                } else {
+#pragma unroll
+                    for (int u0 = 0; u0 < 64; u0 += 16) {
+                        float y[16];
+                        tc::ld16(tm + cS + ub + u0, y);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) x[u0 + j] = y[j];
+                    }
+                    tc::wait_ld();
+                }
+#pragma unroll
+                for (int u0 = 0; u0 < 64; u0 += 16) {
+                    float y[16];
+#pragma unroll
+                    for (int j = 0; j < 16; j += 4)
+                        put_split4(smem + oSAh, smem + oSAl, tc::kmajor_offset(v, ub + u0 + j, D), x[u0 + j],
+                                   x[u0 + j + 1], x[u0 + j + 2], x[u0 + j + 3]);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) y[j] = __fmul_rn(x[u0 + j], gC[ub + u0 + j]);
+                    tc::st16(tm + cS + ub + u0, y);
+                }
+                tc::wait_st();
+            }
+            fence_proxy_async_smem();
+            tc::fence_before_sync();
+            __syncthreads();
+            // ---- MMA 1: [P^T | Oq^T] = S0^T [Khat ; Qhat]^T
+            if (tid == 0) {
+                tc::fence_after_sync();
+                const uint32_t id = tc::idesc_tf32(128, 2 * C);
+#pragma unroll 1
+                for (int s = 0; s < D / 8; ++s) {
+                    const uint64_t ah = tc::smem_desc(smem + oSAh + 256 * s, 128, D * 32);
+                    const uint64_t al = tc::smem_desc(smem + oSAl + 256 * s, 128, D * 32);
+                    const uint64_t bh = tc::smem_desc(smem + oB1h + 256 * s, 128, D * 32);
+                    const uint64_t bl = tc::smem_desc(smem + oB1l + 256 * s, 128, D * 32);
+                    tc::mma_tf32(*tslot + cP, ah, bh, id, s > 0);
+                    tc::mma_tf32(*tslot + cP, ah, bl, id, true);
+                    tc::mma_tf32(*tslot + cP, al, bh, id, true);
+                }
+                tc::commit(&bars[0]);
+            }
+            // ---- meanwhile: A (scaled by beta) and Bm
+            {
+                const int e = tid;  // the parts above and on the diagonal that are zero
+                const int te = e / C, ie = e - te * C;
+                if (ie >= te) mA[te * C + ie] = 0.0f;
+                if (ie > te) mB[te * C + ie] = 0.0f;
+            }
+            if (fast) {
+                // pair p = (t, i), i <= t, in row order; thread pair (2p, 2p + 1) splits the
+                // channels.  Every lane runs both rounds (the shuffles need the whole warp);
+                // a lane without a pair in a round computes nothing and writes nothing.
+                constexpr int kPairs = C * (C + 1) / 2;
+#pragma unroll 1
+                for (int round = 0; round < (kPairs + kThreads / 2 - 1) / (kThreads / 2); ++round) {
+                    const int p = (tid >> 1) + round * (kThreads / 2);
+                    const bool active = p < kPairs;
+                    int t = 0;
+                    while (active && (t + 1) * (t + 2) / 2 <= p) ++t;
+                    const int i = active ? p - t * (t + 1) / 2 : 0;
+                    float da = 0.0f, db = 0.0f;
+                    if (active) {
+                        const int c0 = 64 * (tid & 1);
+                        const float4 *kt4 = reinterpret_cast<const float4 *>(kS + t * DP + c0);
+                        const float4 *qt4 = reinterpret_cast<const float4 *>(qS + t * DP + c0);
+                        const float4 *ki4 = reinterpret_cast<const float4 *>(aS + i * DP + c0);
+#pragma unroll 4
+                        for (int m = 0; m < 16; ++m) {
+                            const float4 a4 = kt4[m], q4 = qt4[m], k4 = ki4[m];
+                            da = __fmaf_rn(a4.x, k4.x, da);
+                            da = __fmaf_rn(a4.y, k4.y, da);
+                            da = __fmaf_rn(a4.z, k4.z, da);
+                            da = __fmaf_rn(a4.w, k4.w, da);
+                            db = __fmaf_rn(q4.x, k4.x, db);
+                            db = __fmaf_rn(q4.y, k4.y, db);
+                            db = __fmaf_rn(q4.z, k4.z, db);
+                            db = __fmaf_rn(q4.w, k4.w, db);
+                        }
+                    }
+                    da = __fadd_rn(da, __shfl_xor_sync(0xffffffffu, da, 1));
+                    db = __fadd_rn(db, __shfl_xor_sync(0xffffffffu, db, 1));
+                    if (active && (tid & 1) == 0) {
+                        if (i < t) mA[t * C + i] = __fmul_rn(betaS[t], da);
+                        mB[t * C + i] = db;
+                    }
+                }
+            } else {
+                // running products: thread (i, cq) takes channels cq + 16 m of row i
+                const int i = tid >> 4, cq = tid & 15;
+                float accA[C], accB[C];
+#pragma unroll
+                for (int t = 0; t < C; ++t) accA[t] = accB[t] = 0.0f;
+#pragma unroll 1
+                for (int m = 0; m < D / 16; ++m) {
+                    const int cc = cq + 16 * m;
+                    const float ki = kS[i * DP + cc];
+                    float rho = 1.0f;  // prod_{s=i+1..t} alpha_s[cc]
+#pragma unroll
+                    for (int t = 0; t < C; ++t) {
+                        if (t > i) rho = __fmul_rn(rho, aS[t * DP + cc]);
+                        const float kr = __fmul_rn(ki, rho);
+                        if (t > i) accA[t] = __fmaf_rn(kS[t * DP + cc], kr, accA[t]);
+                        if (t >= i) accB[t] = __fmaf_rn(qS[t * DP + cc], kr, accB[t]);
+                    }
+                }
+#pragma unroll
+                for (int t = 0; t < C; ++t) {
+#pragma unroll
+                    for (int s = 1; s < 16; s <<= 1) {
+                        accA[t] = __fadd_rn(accA[t], __shfl_xor_sync(0xffffffffu, accA[t], s));
+                        accB[t] = __fadd_rn(accB[t], __shfl_xor_sync(0xffffffffu, accB[t], s));
+                    }
+                }
+                if (cq == 0) {
+#pragma unroll
+                    for (int t = 0; t < C; ++t) {
+                        if (t > i) mA[t * C + i] = __fmul_rn(betaS[t], accA[t]);
+                        if (t >= i) mB[t * C + i] = accB[t];
+                    }
+                }
+            }
+            __syncthreads();
+            if (tid < C) {  // column j of T: T[t][j] = [t == j] - sum_{i<t} L[t][i] T[i][j]
+                const int j = tid;
+                float col[C];
+#pragma unroll
+                for (int t = 0; t < C; ++t) col[t] = t == j ? 1.0f : 0.0f;
+#pragma unroll
+                for (int t = 1; t < C; ++t) {
+                    float sum = 0.0f;
+#pragma unroll
+                    for (int i2 = 0; i2 < t; ++i2) sum = __fmaf_rn(mA[t * C + i2], col[i2], sum);
+                    if (t > j) col[t] = -sum;
+                }
+#pragma unroll
+                for (int t = 0; t < C; ++t) put_split(smem + oTh, smem + oTl, tc::kmajor_offset(t, j, C), col[t]);
+            }
+            put_split(smem + oBh, smem + oBl, tc::kmajor_offset(tid / C, tid % C, C), mB[tid]);  // C * C == kThreads
+            fence_proxy_async_smem();
+            // ---- MMA 1 done: R^T = diag(beta) (V^T - P^T) for tokens 8 hf .. 8 hf + 7
+            if (!wait(0)) {
+                failed = true;
+                break;
+            }
+            tc::fence_after_sync();
+            {
+                float pv[C], r[C / 2];
+                tc::ld16(tm + cP, pv);
+                tc::wait_ld();
+#pragma unroll
+                for (int j = 0; j < C / 2; ++j) {
+                    const int t = (C / 2) * hf + j;
+                    r[j] = __fmul_rn(betaS[t], __fsub_rn(vt[j], hf ? pv[C / 2 + j] : pv[j]));
+                }
+#pragma unroll
+                for (int j = 0; j < C / 2; j += 4)
+                    put_split4(smem + oA2h, smem + oA2l, tc::kmajor_offset(v, (C / 2) * hf + j, C), r[j], r[j + 1],
+                               r[j + 2], r[j + 3]);
+            }
+            fence_proxy_async_smem();
+            tc::fence_before_sync();
+            __syncthreads();
+            // ---- MMA 2: W^T = R^T T^T
+            if (tid == 0) {
+                tc::fence_after_sync();
+                const uint32_t id = tc::idesc_tf32(128, C);
+#pragma unroll
+                for (int s = 0; s < C / 8; ++s) {
+                    const uint64_t ah = tc::smem_desc(smem + oA2h + 256 * s, 128, C * 32);
+                    const uint64_t al = tc::smem_desc(smem + oA2l + 256 * s, 128, C * 32);
+                    const uint64_t bh = tc::smem_desc(smem + oTh + 256 * s, 128, C * 32);
+                    const uint64_t bl = tc::smem_desc(smem + oTl + 256 * s, 128, C * 32);
+                    tc::mma_tf32(*tslot + cW, ah, bh, id, s > 0);
+                    tc::mma_tf32(*tslot + cW, ah, bl, id, true);
+                    tc::mma_tf32(*tslot + cW, al, bh, id, true);
+                }
+                tc::commit(&bars[1]);
+            }
+            if (!wait(1)) {
+                failed = true;
+                break;
+            }
+            tc::fence_after_sync();
+            {
+                float wv[C];
+                tc::ld16(tm + cW, wv);
+                tc::wait_ld();
+#pragma unroll
+                for (int j = 0; j < C / 2; j += 4) {
+                    const int t = (C / 2) * hf + j;
+                    put_split4(smem + oA2h, smem + oA2l, tc::kmajor_offset(v, t, C),
+                               hf ? wv[C / 2 + j] : wv[j], hf ? wv[C / 2 + j + 1] : wv[j + 1],
+                               hf ? wv[C / 2 + j + 2] : wv[j + 2], hf ? wv[C / 2 + j + 3] : wv[j + 3]);
+                }
+            }
+            fence_proxy_async_smem();
+            tc::fence_before_sync();
+            __syncthreads();
+            // ---- MMA 3: O^T = Oq^T + W^T Bm^T;  MMA 4: S_C^T = Gamma_C S0^T + W^T Ktil
+            if (tid == 0) {
+                tc::fence_after_sync();
+                const uint32_t id16 = tc::idesc_tf32(128, C), id128 = tc::idesc_tf32(128, D);
+#pragma unroll
+                for (int s = 0; s < C / 8; ++s) {
+                    const uint64_t ah = tc::smem_desc(smem + oA2h + 256 * s, 128, C * 32);
+                    const uint64_t al = tc::smem_desc(smem + oA2l + 256 * s, 128, C * 32);
+                    const uint64_t bh = tc::smem_desc(smem + oBh + 256 * s, 128, C * 32);
+                    const uint64_t bl = tc::smem_desc(smem + oBl + 256 * s, 128, C * 32);
+                    tc::mma_tf32(*tslot + cOq, ah, bh, id16, true);
+                    tc::mma_tf32(*tslot + cOq, ah, bl, id16, true);
+                    tc::mma_tf32(*tslot + cOq, al, bh, id16, true);
+                    const uint64_t kh = tc::smem_desc(smem + oKTh + 256 * s, 128, C * 32);
+                    const uint64_t kl = tc::smem_desc(smem + oKTl + 256 * s, 128, C * 32);
+                    tc::mma_tf32(*tslot + cS, ah, kh, id128, true);
+                    tc::mma_tf32(*tslot + cS, ah, kl, id128, true);
+                    tc::mma_tf32(*tslot + cS, al, kh, id128, true);
+                }
+                tc::commit(&bars[2]);
+            }
+            if (!wait(2)) {
+                failed = true;
+                break;
+            }
+            tc::fence_after_sync();
+            if (o_g) {
+                float ov[C];
+                tc::ld16(tm + cOq, ov);
+                tc::wait_ld();
+#pragma unroll
+                for (int j = 0; j < C / 2; ++j) {
+                    const int t = (C / 2) * hf + j;
+                    if (t < nt)
+                        store_from_f32<TO>(o_g + (((size_t)b * L + t0 + t) * Hv + h) * D + v,
+                                           hf ? ov[C / 2 + j] : ov[j]);
+                }
+            }
+            ph ^= 1u;
+        }
+        if (failed) break;
+        // ---- the tile's final state back to HBM (thread (v, hf): key channels 64 hf ..)
+#pragma unroll
+        for (int u0 = 0; u0 < 64; u0 += 16) {
+            float y[16];
+            tc::ld16(tm + cS + 64 * hf + u0, y);
+            tc::wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) Sg[(size_t)(64 * hf + u0 + j) * D + v] = y[j];
+        }
+        __syncthreads();  // the next tile restages the inputs
+    }
+    if (failed && tid == 0) report_bits(P.status, RS_DEV_PIPE_TIMEOUT);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (w == 0) tc::tmem_dealloc(*tslot, kTmemCols);
+}
+
+template <bool KDA, typename TI, typename TO>
+cudaError_t run(PrefillParams &P, cudaStream_t s) {
+    auto kern = chunk_prefill_kernel<KDA, TI, TO>;
+    cudaError_t e = set_dynamic_smem(reinterpret_cast<const void *>(kern), kSmem);
+    if (e != cudaSuccess) return e;
+    const int items = P.B * P.Hv;
+    int grid = device_sm_count();
+    if (grid > items) grid = items;
+    if (grid < 1) grid = 1;
+    return launch_pdl(kern, dim3(grid), dim3(kThreads), kSmem, s, P);
+}
+
+template <bool KDA>
+cudaError_t by_types(const StepLaunch &L, PrefillParams &P, cudaStream_t s) {
+    if (L.in_dt == RS_BF16 && L.out_dt == RS_F32) return run<KDA, __nv_bfloat16, float>(P, s);
+    if (L.in_dt == RS_BF16 && L.out_dt == RS_BF16) return run<KDA, __nv_bfloat16, __nv_bfloat16>(P, s);
+    if (L.in_dt == RS_F32 && L.out_dt == RS_F32) return run<KDA, float, float>(P, s);
+    if (L.in_dt == RS_F16 && L.out_dt == RS_F32) return run<KDA, __half, float>(P, s);
+    return cudaErrorNotSupported;
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_chunked(const StepLaunch &L, PrefillParams &P, cudaStream_t s) {
+    if (L.D != 128 || L.khi >= 0) return cudaErrorNotSupported;  // FP32 layout, dk = dv = 128
+    return L.kda ? by_types<true>(L, P, s) : by_types<false>(L, P, s);
+}
+
+}  // namespace rs

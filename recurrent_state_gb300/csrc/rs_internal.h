@@ -96,6 +96,8 @@ struct PrefillParams {
     uint8_t pi[kMaxRowMap];    // mixed layout: physical row -> key channel
 };
 cudaError_t launch_prefill(const StepLaunch &L, PrefillParams &P, cudaStream_t s);
+// rs_chunk.cu: the chunk-parallel form on the tensor cores (FP32 layout)
+cudaError_t launch_prefill_chunked(const StepLaunch &L, PrefillParams &P, cudaStream_t s);
 
 // rs_convert.cu
 struct ConvertParams {

@@ -1,0 +1,122 @@
+// rs_tc.cuh -- the fifth-generation tensor-core pieces used by the chunked
+// prefill (sm_103a): tensor-memory allocation, tcgen05.mma of kind::tf32 with
+// both operands in shared memory, completion through an mbarrier, and the
+// tensor-memory <-> register moves of the epilogue.
+//
+// Operand layout (K-major, no swizzle): an R x K operand (R = M rows of A or
+// N rows of B, K the reduction) is stored as 8 x 16-byte core matrices, each
+// 128 contiguous bytes (8 rows of 4 fp32/tf32 values).  Core matrix
+// (r / 8, k / 4) sits at byte ((r / 8) * (K / 4) + k / 4) * 128, so along K
+// neighbouring core matrices are 128 bytes apart (the descriptor's leading
+// byte offset) and along R the 8-row groups are K * 32 bytes apart (its
+// stride byte offset).  One tf32 MMA reduces over 8 values of K (two core
+// matrices); the k-th step starts 256 * k bytes further in.
+//
+// Accumulators (M = 128, cta_group::1): row m of D is tensor-memory lane m,
+// column n is column (base + n), one fp32 value each.  Warp w of the CTA
+// reaches lanes 32 (w % 4) .. 32 (w % 4) + 31 with the 32x32b shapes.
+#pragma once
+
+#include <cstdint>
+
+#include "rs_device.cuh"
+
+namespace rs {
+namespace tc {
+
+// Byte offset of element (r, k) of an R x K operand in the layout above.
+__host__ __device__ constexpr uint32_t kmajor_offset(int r, int k, int K) {
+    return (uint32_t)(((r >> 3) * (K >> 2) + (k >> 2)) * 128 + (r & 7) * 16 + (k & 3) * 4);
+}
+
+// Shared-memory matrix descriptor: start address, leading (K) and stride (R)
+// byte offsets, all in 16-byte units; descriptor version 1; no swizzle.
+__device__ __forceinline__ uint64_t smem_desc(const void *base, uint32_t lead_bytes, uint32_t stride_bytes) {
+    const uint64_t addr = (uint64_t)(smem_addr(base) >> 4) & 0x3FFFull;
+    return addr | ((uint64_t)((lead_bytes >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((stride_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+}
+
+// Instruction descriptor of kind::tf32: fp32 accumulator, tf32 A and B, both
+// K-major, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
+    return (1u << 4)                      // D format: f32
+           | (2u << 7) | (2u << 10)       // A, B format: tf32
+           | ((uint32_t)(N >> 3) << 17)   // N / 8
+           | ((uint32_t)(M >> 4) << 24);  // M / 16
+}
+
+// Allocate `cols` tensor-memory columns (a power of two, >= 32); the whole
+// warp calls it; the base address is written to *slot (shared memory).
+__device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t cols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(slot)),
+                 "r"(cols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols) : "memory");
+}
+
+__device__ __forceinline__ void fence_before_sync() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after_sync() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D (+)= A B^T, one instruction (issued by one thread).
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
+        : "memory");
+}
+
+// Arrive on the mbarrier once every MMA this thread issued has completed.
+__device__ __forceinline__ void commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_addr(bar))
+                 : "memory");
+}
+
+// 32 lanes x 16 columns of 32-bit values: thread t of the warp gets lane
+// (lane base + t), columns col .. col + 15.
+__device__ __forceinline__ void ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void st16(uint32_t taddr, const float (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15]))
+        : "memory");
+}
+__device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// tf32 split of an fp32 value: hi keeps the 10 explicit mantissa bits the
+// tensor core reads (the low 13 bits cleared), lo = x - hi is exact.  Three
+// products hi*hi + hi*lo + lo*hi recover x*y to about 2^-21 relative.
+__device__ __forceinline__ float tf32_hi(float x) { return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u); }
+
+}  // namespace tc
+}  // namespace rs

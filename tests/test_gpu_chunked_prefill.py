@@ -1,0 +1,152 @@
+"""GPU parity of the chunk-parallel prefill on the tensor cores
+(rs_prefill_chunked_update; DAMP Appendix A.4 "Prefill path"; "Serving
+recurrent attention", "Kernels follow the serving phase").
+
+The oracle is the plain recurrence: every token one decode step in FP32
+(the oracle's multi-token replay).  The chunked form reorders the sums and
+runs the large products as tf32 pairs with fp32 accumulation, so the bar is
+a tolerance, not bit-exactness: per (sequence, head) tile, the final state
+and every output row within 1e-5 of the oracle's, normwise
+(||x - x_ref||_inf / ||x_ref||_inf), as for the FP32 state after 64 decode
+steps.  Cases: GDN and KDA, grouped key heads, ragged token counts (0, 1, L
+and between) over several 16-token groups with a partial last one, bf16 and
+fp32 inputs, strong decays, and the full batch-256 workload with 32 and 64
+tokens on sampled sequences.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+import recurrent_state_gb300 as rs
+from recurrent_state_gb300 import _abi
+from recurrent_state_gb300 import inputs as gen
+
+from .gpu_util import dev, ensure_built, host, replay_inputs, sub_batch
+
+pytestmark = pytest.mark.gpu
+
+D = 128
+TOL = 1e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+
+
+def tile_rel(x, ref):
+    """max over tiles of ||x - ref||_inf / ||ref||_inf (tiles: the last two axes)."""
+    x = x.astype(np.float64)
+    ref = ref.astype(np.float64)
+    num = np.max(np.abs(x - ref), axis=(-2, -1))
+    den = np.maximum(np.max(np.abs(ref), axis=(-2, -1)), 1e-30)
+    return float(np.max(num / den))
+
+
+def run_case(B, Hk, Hv, L, per_channel, in_dtype, seed, n_tok=None, decay_range=None):
+    w = gen.decode_workload(B=B, Hk=Hk, Hv=Hv, d=D, steps=L, per_channel=per_channel,
+                            in_dtype=in_dtype, seed=seed,
+                            horizon=(2.0, 8192.0) if per_channel else (4.0, 4096.0))
+    if decay_range is not None:  # decays far from 1
+        w.alpha[...] = gen.rng(seed + 5).uniform(*decay_range, w.alpha.shape).astype(np.float32)
+    if n_tok is None:
+        n_tok = np.full(B, L, np.int32)
+    qd, kd, vd, ad, bd = replay_inputs(w, L)
+    q, k, v, a, b = gen.replay_view(w, L)
+    lay = rs.Layout("fp32", D, Hv, Hk)
+    pool = dev(w.state0)
+    o = torch.full((B, L, Hv, D), 3.0, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rs.prefill_update(lay, per_channel, pool, dev(w.slot_idx), qd, kd, vd, ad, bd, n_tokens=dev(n_tok),
+                      o=o, status=status, chunked=True)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return w, n_tok, (q, k, v, a, b), host(pool), host(o)
+
+
+def check_against_oracle(w, n_tok, inputs, pool_g, o_g, bsel=None):
+    q, k, v, a, b = inputs
+    if bsel is None:
+        bsel = np.arange(w.B)
+    ws = sub_batch(w, bsel)
+    L = q.shape[1]
+    ref = ws.state0.copy()
+    o_r = np.full((len(bsel), L, w.Hv, D), 3.0, np.float32)
+    pick = lambda x: np.ascontiguousarray(x[bsel])
+    _, st = orc.replay_f32(ref, ws.slot_idx, np.ascontiguousarray(n_tok[bsel]), pick(q), pick(k), pick(v),
+                           pick(a), pick(b), o=o_r)
+    assert st == 0
+    s_err = tile_rel(pool_g[w.slot_idx[bsel]], ref)
+    assert s_err <= TOL, f"state {s_err:.3g}"
+    worst = 0.0
+    for i, bb in enumerate(bsel):
+        n = int(n_tok[bb])
+        if n:
+            got = np.swapaxes(o_g[bb, :n], 0, 1)     # [Hv][n][D]: tiles per head
+            exp = np.swapaxes(o_r[i, :n], 0, 1)
+            worst = max(worst, tile_rel(got, exp))
+        assert np.all(o_g[bb, n:] == 3.0), "rows past n_tokens must stay untouched"
+    assert worst <= TOL, f"o {worst:.3g}"
+    return s_err, worst
+
+
+@pytest.mark.parametrize("per_channel,Hk,Hv", [(True, 4, 4), (False, 2, 4), (False, 4, 4)])
+def test_chunked_prefill_ragged_counts(per_channel, Hk, Hv):
+    B, L = 11, 37
+    n_tok = gen.rng(3).integers(0, L + 1, B).astype(np.int32)
+    n_tok[0], n_tok[1], n_tok[2], n_tok[3] = 0, L, 1, 16
+    w, n_tok, inputs, pool_g, o_g = run_case(B, Hk, Hv, L, per_channel, "bf16", seed=61, n_tok=n_tok)
+    check_against_oracle(w, n_tok, inputs, pool_g, o_g)
+
+
+@pytest.mark.parametrize("per_channel", [True, False])
+@pytest.mark.parametrize("decay_range", [(0.02, 0.6), (0.001, 0.03)])
+def test_chunked_prefill_fp32_inputs_and_strong_decay(per_channel, decay_range):
+    """Strong decays: products over a 16-token group reach 1e-27 (the factored
+    form) and fall below 1e-30 (the running products the kernel then takes)."""
+    B, L = 6, 48
+    w, n_tok, inputs, pool_g, o_g = run_case(B, 2, 2, L, per_channel, "f32", seed=62,
+                                             decay_range=decay_range)
+    assert np.all(np.isfinite(pool_g)) and np.all(np.isfinite(o_g))
+    check_against_oracle(w, n_tok, inputs, pool_g, o_g)
+
+
+@pytest.mark.parametrize("L", [32, 64])
+def test_chunked_prefill_full_size_sampled(L):
+    """KDA, batch 256, 32 heads, chunks of 32 and 64 tokens; oracle on sampled
+    sequences (all heads)."""
+    w, n_tok, inputs, pool_g, o_g = run_case(256, 32, 32, L, True, "bf16", seed=63)
+    s_err, o_err = check_against_oracle(w, n_tok, inputs, pool_g, o_g, bsel=np.array([0, 97, 255]))
+    print(f"\nchunked prefill L={L}: state {s_err:.3g}, o {o_err:.3g} (normwise per tile)")
+
+
+def test_chunked_prefill_gdn_full_size_sampled():
+    """GDN, batch 256, 16 key heads shared by 32 value heads, 32 tokens."""
+    w, n_tok, inputs, pool_g, o_g = run_case(256, 16, 32, 32, False, "bf16", seed=64)
+    check_against_oracle(w, n_tok, inputs, pool_g, o_g, bsel=np.array([1, 128, 254]))
+
+
+def test_chunked_prefill_guards_and_layouts():
+    B, Hk, Hv, L = 4, 2, 2, 5
+    w = gen.decode_workload(B=B, Hk=Hk, Hv=Hv, d=D, steps=L, per_channel=True, in_dtype="bf16", seed=65)
+    qd, kd, vd, ad, bd = replay_inputs(w, L)
+    lay = rs.Layout("fp32", D, Hv, Hk)
+    pool = dev(w.state0)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    slots = w.slot_idx.copy()
+    slots[1] = 999                                 # out of range: skipped, bit 1
+    n_tok = np.array([L, L, L + 1, 2], np.int32)   # n > L: skipped, bit 2
+    rs.prefill_update(lay, True, pool, dev(slots), qd, kd, vd, ad, bd, n_tokens=dev(n_tok),
+                      status=status, chunked=True)
+    torch.cuda.synchronize()
+    assert int(status.item()) == (_abi.RS_DEV_BAD_SLOT | _abi.RS_DEV_BAD_ACCEPT)
+    got = host(pool)
+    for bb in (1, 2):  # skipped sequences keep their state
+        if slots[bb] < w.state0.shape[0]:
+            assert np.array_equal(got[slots[bb]], w.state0[slots[bb]])
+    hi = gen.hi_rows(Hv, D, 16, seed=1)
+    mix = rs.Layout("mixed", D, Hv, Hk, k_hi=16, hi_rows=hi)
+    with pytest.raises(rs.RsError) as e:
+        rs.prefill_update(mix, True, mix.empty_pool(B), dev(w.slot_idx), qd, kd, vd, ad, bd, chunked=True)
+    assert e.value.status == _abi.RS_ERR_UNSUPPORTED
