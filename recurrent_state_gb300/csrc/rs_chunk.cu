@@ -67,8 +67,9 @@ constexpr int oTh = oB1l + kB1, oTl = oTh + kCC, oBh = oTl + kCC, oBl = oBh + kC
 constexpr int oKTh = oBl + kCC, oKTl = oKTh + kKT, oA2h = oKTl + kKT, oA2l = oA2h + kA2;
 constexpr int oK = oA2l + kA2, oQ = oK + kTok, oAl = oQ + kTok;
 constexpr int oBeta = oAl + kTok, oGc = oBeta + C * 4, oMA = oGc + D * 4, oMB = oMA + kCC;
-constexpr int oBar = oMB + kCC, oTslot = oBar + 3 * 8;
-constexpr int kSmem = oTslot + 16;
+constexpr int oBar = oMB + kCC, oTslot = oBar + 5 * 8, oAlpS = oTslot + 16;
+constexpr int kSmemEnd = oAlpS + C * 4;
+constexpr int kSmem = kSmemEnd;
 static_assert(kSmem <= 232448, "fits the shared memory of one SM");
 static_assert(oBar % 8 == 0 && oSAl % 1024 == 0 && oB1h % 16 == 0, "alignment");
 
@@ -106,7 +107,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + oTslot);
 
     if (tid == 0)
-        for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < 5; ++i) mbar_init(&bars[i], 1);  // MMA 1, MMA 2, MMA 3+4, state, inputs
     fence_mbar_init();
     if (w == 0) {
         tc::tmem_alloc(tslot, kTmemCols);
@@ -132,9 +133,73 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
         const bool ok = mbar_wait_bounded(&bars[k], ph) || mbar_wait_bounded(&bars[k], ph);
         return __syncthreads_and(ok);
     };
+    // the first tile at or after `from` that this CTA processes (slot in range, 1 <= n <= L)
+    auto next_work = [&](int from) -> int {
+        for (int it = from; it < items; it += gridDim.x) {
+            const int bb = it / Hv;
+            const int32_t sl = P.slot_idx[bb];
+            const int32_t nn = P.n_tokens ? P.n_tokens[bb] : L;
+            if (sl >= 0 && (int64_t)sl < P.n_slots && nn >= 1 && nn <= L) return it;
+        }
+        return items;
+    };
+    // bulk copy of a tile's state ([u][v] row-major, 64 KB) into the lo operand buffer, staged
+    auto prefetch_state = [&](int it) {
+        if (tid != 0 || it >= items) return;
+        const int bb = it / Hv, hh = it - bb * Hv;
+        const float *src = static_cast<const float *>(P.pool) + ((size_t)P.slot_idx[bb] * Hv + hh) * D * D;
+        mbar_arrive_expect_tx(&bars[3], (uint32_t)(D * D * 4));
+        for (int part = 0; part < 4; ++part)
+            bulk_g2s(smem + oSAl + part * (D * D), src + part * (D * D / 4), D * D, &bars[3]);
+    };
+    // a group's token vectors by bulk copies into the [Khat ; Qhat] operand buffers (free from
+    // the end of MMA 1 to the next group's decays), raw: k, q, v [C][D] TI, then (KDA) alpha
+    // [C][D] fp32; the per-token scalars (beta, GDN alpha) into registers of threads t < C
+    constexpr uint32_t kVecTI = D * (uint32_t)sizeof(TI);
+    const uint8_t *rawK = smem + oB1h, *rawQ = rawK + C * kVecTI, *rawV = rawQ + C * kVecTI;
+    const float *rawA = reinterpret_cast<const float *>(rawV + C * kVecTI);
+    static_assert(3 * C * D * sizeof(TI) + (KDA ? C * D * 4 : 0) <= 2 * kB1, "raw inputs fit the operand buffers");
+    float fb = 0.0f, fga = 1.0f;  // beta and the GDN decay of token tid of the fetched group
+    int fnt = 0;                  // tokens in the fetched group
+    auto fetch = [&](int it, int tb) {
+        const int bb = it / Hv, hh = it - bb * Hv, gg = hh / (Hv / Hk);
+        const int nn = P.n_tokens ? P.n_tokens[bb] : L;
+        const int ntt = min(C, nn - tb);
+        fnt = ntt;
+        if (w == 0) {  // warp 0: lane l copies token l % C's k and q (l < C) or v and alpha
+            if (tid == 0)
+                mbar_arrive_expect_tx(&bars[4], (uint32_t)ntt * (3 * kVecTI + (KDA ? D * 4 : 0)));
+            __syncwarp();
+            const int t = tid & (C - 1);
+            if (t < ntt) {
+                const size_t bt = (size_t)bb * L + tb + t;
+                if (tid < C) {
+                    bulk_g2s(smem + oB1h + t * kVecTI, k_g + (bt * Hk + gg) * D, kVecTI, &bars[4]);
+                    bulk_g2s(smem + oB1h + (C + t) * kVecTI, q_g + (bt * Hk + gg) * D, kVecTI, &bars[4]);
+                } else {
+                    bulk_g2s(smem + oB1h + (2 * C + t) * kVecTI, v_g + (bt * Hv + hh) * D, kVecTI, &bars[4]);
+                    if (KDA)
+                        bulk_g2s(smem + oB1h + 3 * C * kVecTI + t * D * 4, P.alpha + (bt * Hv + hh) * D, D * 4,
+                                 &bars[4]);
+                }
+            }
+        }
+        fb = 0.0f, fga = 1.0f;
+        if (tid < ntt) {
+            const size_t bt = (size_t)bb * L + tb + tid;
+            fb = P.beta[bt * Hv + hh];
+            if (!KDA) fga = P.alpha[bt * Hv + hh];
+        }
+    };
+    uint32_t iph = 0;  // parity of the input-copy barrier
+    float *alpS = reinterpret_cast<float *>(smem + oAlpS);
+    uint32_t sph = 0;  // parity of the state-copy barrier
+    int staged = next_work(blockIdx.x);
+    prefetch_state(staged);
+    if (staged < items) fetch(staged, 0);
 
     for (int item = blockIdx.x; item < items && !failed; item += gridDim.x) {
-        const int b = item / Hv, h = item - b * Hv, g = h / (Hv / Hk);
+        const int b = item / Hv, h = item - b * Hv;
         const int32_t slot = P.slot_idx[b];
         const int32_t n = P.n_tokens ? P.n_tokens[b] : L;
         // every thread sees the same item: the skips are uniform
@@ -151,32 +216,30 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
 
         for (int t0 = 0; t0 < n && !failed; t0 += C) {
             const int nt = min(C, n - t0);
-            // ---- the chunk's inputs: thread (v, hf) loads channel v of tokens 8 hf .. 8 hf + 7
-            // (pads: k = q = 0, alpha = 1, beta = 0), and value v of the same tokens for R
+            // ---- the chunk's inputs, copied in during the previous group (or at start): raw
+            // vectors to padded fp32 rows (pads: k = q = 0, alpha = 1, v = 0, beta = 0)
             float vt[C / 2];
             {
-                float kv[C / 2], qv[C / 2], av[C / 2];
+                if (tid < C) {
+                    betaS[tid] = fb;
+                    alpS[tid] = fga;
+                }
+                const bool ok = mbar_wait_bounded(&bars[4], iph) || mbar_wait_bounded(&bars[4], iph);
+                if (!__syncthreads_and(ok)) {
+                    failed = true;
+                    break;
+                }
+                iph ^= 1u;
 #pragma unroll
                 for (int j = 0; j < C / 2; ++j) {
                     const int t = (C / 2) * hf + j;
-                    kv[j] = 0.0f, qv[j] = 0.0f, av[j] = 1.0f, vt[j] = 0.0f;
-                    if (t < nt) {
-                        const size_t bt = (size_t)b * L + t0 + t;
-                        kv[j] = load_as_f32<TI>(k_g + (bt * Hk + g) * D + v);
-                        qv[j] = load_as_f32<TI>(q_g + (bt * Hk + g) * D + v);
-                        av[j] = KDA ? P.alpha[(bt * Hv + h) * D + v] : P.alpha[bt * Hv + h];
-                        vt[j] = load_as_f32<TI>(v_g + (bt * Hv + h) * D + v);
-                    }
+                    const bool real = t < nt;
+                    kS[t * DP + v] = real ? load_as_f32<TI>(reinterpret_cast<const TI *>(rawK + t * kVecTI) + v) : 0.0f;
+                    qS[t * DP + v] = real ? load_as_f32<TI>(reinterpret_cast<const TI *>(rawQ + t * kVecTI) + v) : 0.0f;
+                    vt[j] = real ? load_as_f32<TI>(reinterpret_cast<const TI *>(rawV + t * kVecTI) + v) : 0.0f;
+                    if constexpr (KDA) aS[t * DP + v] = real ? rawA[t * D + v] : 1.0f;
+                    else aS[t * DP + v] = alpS[t];  // 1 for pads
                 }
-                const float bv = tid < nt ? P.beta[((size_t)b * L + t0 + tid) * Hv + h] : 0.0f;
-#pragma unroll
-                for (int j = 0; j < C / 2; ++j) {
-                    const int t = (C / 2) * hf + j;
-                    kS[t * DP + v] = kv[j];
-                    qS[t * DP + v] = qv[j];
-                    aS[t * DP + v] = av[j];
-                }
-                if (tid < C) betaS[tid] = bv;
             }
             __syncthreads();
             // ---- channel c = v: cumulative decays Gamma_t[c]; the factored form if none is tiny
@@ -199,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
                     put_split(smem + oB1h, smem + oB1l, tc::kmajor_offset(t, c, D), kh);
                     if (fast) {
                         kS[t * DP + c] = kh;
-                        const float kc = __fdiv_rn(kr, gam[t]);
+                        const float kc = __fmul_rn(kr, __frcp_rn(gam[t]));
                         aS[t * DP + c] = kc;
                         put_split(smem + oKTh, smem + oKTl, tc::kmajor_offset(c, t, C), __fmul_rn(kc, gam[C - 1]));
                     }
@@ -228,9 +291,17 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
             {
                 const int ub = 64 * hf;
                 float x[64];
-                if (t0 == 0) {
+                if (t0 == 0) {  // the staged copy ([u][v] row-major in the lo buffer)
+                    const bool ok = mbar_wait_bounded(&bars[3], sph) || mbar_wait_bounded(&bars[3], sph);
+                    if (!__syncthreads_and(ok)) {
+                        failed = true;
+                        break;
+                    }
+                    const float *st = reinterpret_cast<const float *>(smem + oSAl);
 #pragma unroll
-                    for (int u = 0; u < 64; ++u) x[u] = Sg[(size_t)(ub + u) * D + v];
+                    for (int u = 0; u < 64; ++u) x[u] = st[(ub + u) * D + v];
+                    sph ^= 1u;
+                    __syncthreads();  // every column read before the operands overwrite the copy
                 } else {
 #pragma unroll
                     for (int u0 = 0; u0 < 64; u0 += 16) {
@@ -354,20 +425,29 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
                 }
             }
             __syncthreads();
-            if (tid < C) {  // column j of T: T[t][j] = [t == j] - sum_{i<t} L[t][i] T[i][j]
-                const int j = tid;
-                float col[C];
+            {  // T = (I + L)^{-1} = (I - L)(I + L^2)(I + L^4)(I + L^8), L = diag(beta) A strictly
+               // lower (L^16 = 0); thread tid owns entry (r, cc); scratch in the R/W buffer
+                const int r = tid / C, cc = tid % C;
+                float *Tc = reinterpret_cast<float *>(smem + oA2h);
+                float *Pw = Tc + C * C, *Pn = Pw + C * C;
+                Tc[tid] = (r == cc ? 1.0f : 0.0f) - mA[tid];
+                Pw[tid] = mA[tid];
+#pragma unroll 1
+                for (int k = 0; k < 3; ++k) {
+                    __syncthreads();
+                    float acc = 0.0f;
 #pragma unroll
-                for (int t = 0; t < C; ++t) col[t] = t == j ? 1.0f : 0.0f;
+                    for (int i2 = 0; i2 < C; ++i2) acc = __fmaf_rn(Pw[r * C + i2], Pw[i2 * C + cc], acc);
+                    Pn[tid] = acc;  // L^(2^(k+1))
+                    __syncthreads();
+                    float t2 = Tc[tid];
 #pragma unroll
-                for (int t = 1; t < C; ++t) {
-                    float sum = 0.0f;
-#pragma unroll
-                    for (int i2 = 0; i2 < t; ++i2) sum = __fmaf_rn(mA[t * C + i2], col[i2], sum);
-                    if (t > j) col[t] = -sum;
+                    for (int i2 = 0; i2 < C; ++i2) t2 = __fmaf_rn(Tc[r * C + i2], Pn[i2 * C + cc], t2);
+                    __syncthreads();  // every thread has read Tc and Pw of this step
+                    Tc[tid] = t2;
+                    Pw[tid] = Pn[tid];
                 }
-#pragma unroll
-                for (int t = 0; t < C; ++t) put_split(smem + oTh, smem + oTl, tc::kmajor_offset(t, j, C), col[t]);
+                put_split(smem + oTh, smem + oTl, tc::kmajor_offset(r, cc, C), Tc[tid]);
             }
             put_split(smem + oBh, smem + oBl, tc::kmajor_offset(tid / C, tid % C, C), mB[tid]);  // C * C == kThreads
             fence_proxy_async_smem();
@@ -377,6 +457,15 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
                 break;
             }
             tc::fence_after_sync();
+            // the operand buffers are free: the next tile's state comes in now, and the
+            // next group's inputs are fetched while this group finishes
+            if (t0 + C < n) {
+                fetch(item, t0 + C);
+            } else {
+                staged = next_work(item + gridDim.x);
+                prefetch_state(staged);
+                if (staged < items) fetch(staged, 0);
+            }
             {
                 float pv[C], r[C / 2];
                 tc::ld16(tm + cP, pv);
