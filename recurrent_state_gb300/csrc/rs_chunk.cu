@@ -119,6 +119,13 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tm = *tslot + ((uint32_t)(32 * (w & 3)) << 16);  // this warp's 32 lanes
+    // operand descriptors at k-step 0; step s is 256 s bytes on, i.e. + 16 s in the address field
+    const uint64_t dSAh = tc::smem_desc(smem + oSAh, 128, D * 32), dSAl = tc::smem_desc(smem + oSAl, 128, D * 32);
+    const uint64_t dB1h = tc::smem_desc(smem + oB1h, 128, D * 32), dB1l = tc::smem_desc(smem + oB1l, 128, D * 32);
+    const uint64_t dA2h = tc::smem_desc(smem + oA2h, 128, C * 32), dA2l = tc::smem_desc(smem + oA2l, 128, C * 32);
+    const uint64_t dTh = tc::smem_desc(smem + oTh, 128, C * 32), dTl = tc::smem_desc(smem + oTl, 128, C * 32);
+    const uint64_t dBh = tc::smem_desc(smem + oBh, 128, C * 32), dBl = tc::smem_desc(smem + oBl, 128, C * 32);
+    const uint64_t dKTh = tc::smem_desc(smem + oKTh, 128, C * 32), dKTl = tc::smem_desc(smem + oKTl, 128, C * 32);
 
     const int Hv = P.Hv, Hk = P.Hk, L = P.L;
     const int items = P.B * Hv;
@@ -213,6 +220,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
         }
         if (n == 0) continue;
         float *Sg = static_cast<float *>(P.pool) + ((size_t)slot * Hv + h) * D * D;
+        // the following tile's slot and token count, read now (used by the last group)
+        const int nxi = item + gridDim.x;
+        const int32_t nx_slot = nxi < items ? P.slot_idx[nxi / Hv] : -1;
+        const int32_t nx_n = nxi < items ? (P.n_tokens ? P.n_tokens[nxi / Hv] : L) : 0;
 
         for (int t0 = 0; t0 < n && !failed; t0 += C) {
             const int nt = min(C, n - t0);
@@ -254,36 +265,55 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
                 }
             }
             const bool fast = __syncthreads_and(gam[C - 1] >= 1e-30f);
-            if (hf == 0) {  // Khat rows, Kchk, Ktil^T row c, Gamma_C[c]
+            if (fast) {
+                // the cumulative decays in place of alpha; then thread (t = tid % C, channels
+                // 8 (tid / C) .. + 7) forms Khat, Qhat, Kchk and Ktil^T with 16-byte accesses
+                // (a quarter warp covers 8 rows: no bank conflicts)
+                if (hf == 0) {
 #pragma unroll
-                for (int t = 0; t < C; ++t) {
-                    const float kr = kS[t * DP + c];
-                    const float kh = __fmul_rn(kr, gam[t]);
-                    put_split(smem + oB1h, smem + oB1l, tc::kmajor_offset(t, c, D), kh);
-                    if (fast) {
-                        kS[t * DP + c] = kh;
-                        const float kc = __fmul_rn(kr, __frcp_rn(gam[t]));
-                        aS[t * DP + c] = kc;
-                        put_split(smem + oKTh, smem + oKTl, tc::kmajor_offset(c, t, C), __fmul_rn(kc, gam[C - 1]));
-                    }
+                    for (int t = 0; t < C; ++t) aS[t * DP + c] = gam[t];
+                    gC[c] = gam[C - 1];
                 }
-                if (!fast) {
-                    float tail = 1.0f;  // prod_{s=i+1..C-1} alpha_s[c]
+                __syncthreads();
+                const int t = tid % C, c8 = 8 * (tid / C);
 #pragma unroll
-                    for (int i = C - 1; i >= 0; --i) {
-                        put_split(smem + oKTh, smem + oKTl, tc::kmajor_offset(c, i, C),
-                                  __fmul_rn(kS[i * DP + c], tail));
-                        tail = __fmul_rn(tail, aS[i * DP + c]);
-                    }
+                for (int half4 = 0; half4 < 2; ++half4) {
+                    const int cb = c8 + 4 * half4;
+                    const float4 k4 = *reinterpret_cast<const float4 *>(kS + t * DP + cb);
+                    const float4 q4 = *reinterpret_cast<const float4 *>(qS + t * DP + cb);
+                    const float4 g4 = *reinterpret_cast<const float4 *>(aS + t * DP + cb);
+                    const float4 gc4 = *reinterpret_cast<const float4 *>(gC + cb);
+                    const float4 kh = make_float4(__fmul_rn(k4.x, g4.x), __fmul_rn(k4.y, g4.y), __fmul_rn(k4.z, g4.z),
+                                                  __fmul_rn(k4.w, g4.w));
+                    const float4 qh = make_float4(__fmul_rn(q4.x, g4.x), __fmul_rn(q4.y, g4.y), __fmul_rn(q4.z, g4.z),
+                                                  __fmul_rn(q4.w, g4.w));
+                    const float4 kc = make_float4(__fmul_rn(k4.x, __frcp_rn(g4.x)), __fmul_rn(k4.y, __frcp_rn(g4.y)),
+                                                  __fmul_rn(k4.z, __frcp_rn(g4.z)), __fmul_rn(k4.w, __frcp_rn(g4.w)));
+                    put_split4(smem + oB1h, smem + oB1l, tc::kmajor_offset(t, cb, D), kh.x, kh.y, kh.z, kh.w);
+                    put_split4(smem + oB1h, smem + oB1l, tc::kmajor_offset(C + t, cb, D), qh.x, qh.y, qh.z, qh.w);
+                    put_split(smem + oKTh, smem + oKTl, tc::kmajor_offset(cb, t, C), __fmul_rn(kc.x, gc4.x));
+                    put_split(smem + oKTh, smem + oKTl, tc::kmajor_offset(cb + 1, t, C), __fmul_rn(kc.y, gc4.y));
+                    put_split(smem + oKTh, smem + oKTl, tc::kmajor_offset(cb + 2, t, C), __fmul_rn(kc.z, gc4.z));
+                    put_split(smem + oKTh, smem + oKTl, tc::kmajor_offset(cb + 3, t, C), __fmul_rn(kc.w, gc4.w));
+                    *reinterpret_cast<float4 *>(kS + t * DP + cb) = kh;
+                    *reinterpret_cast<float4 *>(qS + t * DP + cb) = qh;
+                    *reinterpret_cast<float4 *>(aS + t * DP + cb) = kc;
+                }
+            } else if (hf == 0) {  // tiny decays: Khat rows, Ktil^T row c by running products
+#pragma unroll
+                for (int t = 0; t < C; ++t)
+                    put_split(smem + oB1h, smem + oB1l, tc::kmajor_offset(t, c, D), __fmul_rn(kS[t * DP + c], gam[t]));
+                float tail = 1.0f;  // prod_{s=i+1..C-1} alpha_s[c]
+#pragma unroll
+                for (int i = C - 1; i >= 0; --i) {
+                    put_split(smem + oKTh, smem + oKTl, tc::kmajor_offset(c, i, C), __fmul_rn(kS[i * DP + c], tail));
+                    tail = __fmul_rn(tail, aS[i * DP + c]);
                 }
                 gC[c] = gam[C - 1];
-            } else {  // Qhat rows
+            } else {  // tiny decays: Qhat rows
 #pragma unroll
-                for (int t = 0; t < C; ++t) {
-                    const float qh = __fmul_rn(qS[t * DP + c], gam[t]);
-                    put_split(smem + oB1h, smem + oB1l, tc::kmajor_offset(C + t, c, D), qh);
-                    if (fast) qS[t * DP + c] = qh;
-                }
+                for (int t = 0; t < C; ++t)
+                    put_split(smem + oB1h, smem + oB1l, tc::kmajor_offset(C + t, c, D), __fmul_rn(qS[t * DP + c], gam[t]));
             }
             __syncthreads();  // Gamma_C of every channel
             // ---- S0^T (hi, lo) as the A operand, Gamma_C S0^T as MMA 4's accumulator:
@@ -334,10 +364,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
                 const uint32_t id = tc::idesc_tf32(128, 2 * C);
 #pragma unroll 1
                 for (int s = 0; s < D / 8; ++s) {
-                    const uint64_t ah = tc::smem_desc(smem + oSAh + 256 * s, 128, D * 32);
-                    const uint64_t al = tc::smem_desc(smem + oSAl + 256 * s, 128, D * 32);
-                    const uint64_t bh = tc::smem_desc(smem + oB1h + 256 * s, 128, D * 32);
-                    const uint64_t bl = tc::smem_desc(smem + oB1l + 256 * s, 128, D * 32);
+                    const uint64_t ah = dSAh + 16 * s, al = dSAl + 16 * s;
+                    const uint64_t bh = dB1h + 16 * s, bl = dB1l + 16 * s;
                     tc::mma_tf32(*tslot + cP, ah, bh, id, s > 0);
                     tc::mma_tf32(*tslot + cP, ah, bl, id, true);
                     tc::mma_tf32(*tslot + cP, al, bh, id, true);
@@ -462,7 +490,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
             if (t0 + C < n) {
                 fetch(item, t0 + C);
             } else {
-                staged = next_work(item + gridDim.x);
+                const bool nx_ok = nx_slot >= 0 && (int64_t)nx_slot < P.n_slots && nx_n >= 1 && nx_n <= L;
+                staged = nx_ok ? nxi : next_work(nxi);
                 prefetch_state(staged);
                 if (staged < items) fetch(staged, 0);
             }
@@ -489,10 +518,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
                 const uint32_t id = tc::idesc_tf32(128, C);
 #pragma unroll
                 for (int s = 0; s < C / 8; ++s) {
-                    const uint64_t ah = tc::smem_desc(smem + oA2h + 256 * s, 128, C * 32);
-                    const uint64_t al = tc::smem_desc(smem + oA2l + 256 * s, 128, C * 32);
-                    const uint64_t bh = tc::smem_desc(smem + oTh + 256 * s, 128, C * 32);
-                    const uint64_t bl = tc::smem_desc(smem + oTl + 256 * s, 128, C * 32);
+                    const uint64_t ah = dA2h + 16 * s, al = dA2l + 16 * s;
+                    const uint64_t bh = dTh + 16 * s, bl = dTl + 16 * s;
                     tc::mma_tf32(*tslot + cW, ah, bh, id, s > 0);
                     tc::mma_tf32(*tslot + cW, ah, bl, id, true);
                     tc::mma_tf32(*tslot + cW, al, bh, id, true);
@@ -525,15 +552,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
                 const uint32_t id16 = tc::idesc_tf32(128, C), id128 = tc::idesc_tf32(128, D);
 #pragma unroll
                 for (int s = 0; s < C / 8; ++s) {
-                    const uint64_t ah = tc::smem_desc(smem + oA2h + 256 * s, 128, C * 32);
-                    const uint64_t al = tc::smem_desc(smem + oA2l + 256 * s, 128, C * 32);
-                    const uint64_t bh = tc::smem_desc(smem + oBh + 256 * s, 128, C * 32);
-                    const uint64_t bl = tc::smem_desc(smem + oBl + 256 * s, 128, C * 32);
+                    const uint64_t ah = dA2h + 16 * s, al = dA2l + 16 * s;
+                    const uint64_t bh = dBh + 16 * s, bl = dBl + 16 * s;
                     tc::mma_tf32(*tslot + cOq, ah, bh, id16, true);
                     tc::mma_tf32(*tslot + cOq, ah, bl, id16, true);
                     tc::mma_tf32(*tslot + cOq, al, bh, id16, true);
-                    const uint64_t kh = tc::smem_desc(smem + oKTh + 256 * s, 128, C * 32);
-                    const uint64_t kl = tc::smem_desc(smem + oKTl + 256 * s, 128, C * 32);
+                    const uint64_t kh = dKTh + 16 * s, kl = dKTl + 16 * s;
                     tc::mma_tf32(*tslot + cS, ah, kh, id128, true);
                     tc::mma_tf32(*tslot + cS, ah, kl, id128, true);
                     tc::mma_tf32(*tslot + cS, al, kh, id128, true);
