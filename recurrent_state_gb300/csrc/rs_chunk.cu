@@ -173,22 +173,23 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
         const int nn = P.n_tokens ? P.n_tokens[bb] : L;
         const int ntt = min(C, nn - tb);
         fnt = ntt;
-        if (w == 0) {  // warp 0: lane l copies token l % C's k and q (l < C) or v and alpha
-            if (tid == 0)
-                mbar_arrive_expect_tx(&bars[4], (uint32_t)ntt * (3 * kVecTI + (KDA ? D * 4 : 0)));
-            __syncwarp();
-            const int t = tid & (C - 1);
-            if (t < ntt) {
+        // one copy per thread, spread over the warps (lanes 0..7 of each: the copies of one
+        // warp issue one after another): thread (warp x, lane y < 8) copies vector x / 2 of
+        // token 8 (x % 2) + y (0: k, 1: q, 2: v, 3: alpha)
+        if (tid == 0) mbar_arrive_expect_tx(&bars[4], (uint32_t)ntt * (3 * kVecTI + (KDA ? D * 4 : 0)));
+        __syncthreads();  // the expected bytes are set before any copy can complete
+        {
+            const int y = tid & 31, vec = w >> 1, t = 8 * (w & 1) + y;
+            if (y < 8 && t < ntt && (KDA || vec < 3)) {
                 const size_t bt = (size_t)bb * L + tb + t;
-                if (tid < C) {
-                    bulk_g2s(smem + oB1h + t * kVecTI, k_g + (bt * Hk + gg) * D, kVecTI, &bars[4]);
+                if (vec == 0) bulk_g2s(smem + oB1h + t * kVecTI, k_g + (bt * Hk + gg) * D, kVecTI, &bars[4]);
+                else if (vec == 1)
                     bulk_g2s(smem + oB1h + (C + t) * kVecTI, q_g + (bt * Hk + gg) * D, kVecTI, &bars[4]);
-                } else {
+                else if (vec == 2)
                     bulk_g2s(smem + oB1h + (2 * C + t) * kVecTI, v_g + (bt * Hv + hh) * D, kVecTI, &bars[4]);
-                    if (KDA)
-                        bulk_g2s(smem + oB1h + 3 * C * kVecTI + t * D * 4, P.alpha + (bt * Hv + hh) * D, D * 4,
-                                 &bars[4]);
-                }
+                else
+                    bulk_g2s(smem + oB1h + 3 * C * kVecTI + t * D * 4, P.alpha + (bt * Hv + hh) * D, D * 4,
+                             &bars[4]);
             }
         }
         fb = 0.0f, fga = 1.0f;
