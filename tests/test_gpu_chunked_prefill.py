@@ -8,10 +8,10 @@ runs the large products as tf32 pairs with fp32 accumulation, so the bar is
 a tolerance, not bit-exactness: per (sequence, head) tile, the final state
 and every output row within 1e-5 of the oracle's, normwise
 (||x - x_ref||_inf / ||x_ref||_inf), as for the FP32 state after 64 decode
-steps.  Cases: GDN and KDA, grouped key heads, ragged token counts (0, 1, L
-and between) over several 16-token groups with a partial last one, bf16 and
-fp32 inputs, strong decays, and the full batch-256 workload with 32 and 64
-tokens on sampled sequences.
+steps.  Cases: GDN and KDA, grouped key heads, ragged token counts (0, 1, 32,
+33, L and between) over two 32-token groups with a partial last one, bf16
+and fp32 inputs, strong decays, and the full batch-256 workload with 32 and
+64 tokens on sampled sequences.
 """
 import numpy as np
 import pytest
@@ -95,7 +95,7 @@ def check_against_oracle(w, n_tok, inputs, pool_g, o_g, bsel=None):
 def test_chunked_prefill_ragged_counts(per_channel, Hk, Hv):
     B, L = 11, 37
     n_tok = gen.rng(3).integers(0, L + 1, B).astype(np.int32)
-    n_tok[0], n_tok[1], n_tok[2], n_tok[3] = 0, L, 1, 16
+    n_tok[0], n_tok[1], n_tok[2], n_tok[3], n_tok[4], n_tok[5] = 0, L, 1, 16, 32, 33
     w, n_tok, inputs, pool_g, o_g = run_case(B, Hk, Hv, L, per_channel, "bf16", seed=61, n_tok=n_tok)
     check_against_oracle(w, n_tok, inputs, pool_g, o_g)
 
@@ -103,9 +103,10 @@ def test_chunked_prefill_ragged_counts(per_channel, Hk, Hv):
 @pytest.mark.parametrize("per_channel", [True, False])
 @pytest.mark.parametrize("decay_range", [(0.02, 0.6), (0.001, 0.03)])
 def test_chunked_prefill_fp32_inputs_and_strong_decay(per_channel, decay_range):
-    """Strong decays: products over a 16-token group reach 1e-27 (the factored
-    form) and fall below 1e-30 (the running products the kernel then takes)."""
-    B, L = 6, 48
+    """Strong decays: products over a 32-token group reach about 1e-26 (the
+    factored form) and fall far below 1e-30 (the running products the kernel
+    then takes)."""
+    B, L = 6, 80
     w, n_tok, inputs, pool_g, o_g = run_case(B, 2, 2, L, per_channel, "f32", seed=62,
                                              decay_range=decay_range)
     assert np.all(np.isfinite(pool_g)) and np.all(np.isfinite(o_g))
