@@ -75,7 +75,8 @@ constexpr int oTh = oA2l + kA2, oTl = oTh + kCC, oBh = oTl + kCC, oBl = oBh + kC
 constexpr int oK = oBl + kCC, oQ = oK + kTok, oAl = oQ + kTok;
 constexpr int oBeta = oAl + kTok, oAlpS = oBeta + C * 4, oGc = oAlpS + C * 4;
 constexpr int oMA = oGc + D * 4;
-constexpr int oBar = oMA + C * CA * 4, oTslot = oBar + 6 * 8;
+constexpr int kBars = 7;
+constexpr int oBar = oMA + C * CA * 4, oTslot = oBar + kBars * 8;
 // the Gram products' B operand Kchk (N = i, K = c; hi and lo parts, 16 KB each) over the k and
 // q rows, which the factored form no longer reads once Khat, Qhat and Kchk are formed
 constexpr int oKCh = oK, oKCl = oK + C * D * 4;
@@ -121,11 +122,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
     float *alpS = reinterpret_cast<float *>(smem + oAlpS);
     float *gC = reinterpret_cast<float *>(smem + oGc);
     float *mA = reinterpret_cast<float *>(smem + oMA);  // L = diag(beta) A, row stride CA
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + oBar);  // MMA 1, MMA 2, MMA 3+4, state, inputs, Gram
+    // mbarriers: MMA 1, MMA 2, MMA 3, state copy, input copy, Gram, MMA 4
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + oBar);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + oTslot);
 
     if (tid == 0)
-        for (int i = 0; i < 6; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < kBars; ++i) mbar_init(&bars[i], 1);
     fence_mbar_init();
     if (w == 0) {
         tc::tmem_alloc(tslot, kTmemCols);
@@ -156,9 +158,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
     TO *o_g = static_cast<TO *>(P.o);
     uint32_t ph = 0, sph = 0, iph = 0, gph = 0;  // barrier parities: MMAs, state copy, input copy, Gram
     bool failed = false;
-    // what is in flight (the same in every thread): input copy, state copy, the MMA barrier awaited
-    bool in_pend = false, st_pend = false;
-    int mma_pend = -1;
+    // the barriers with copies or MMAs in flight (bit k: bars[k]; the same in every thread)
+    uint32_t pendm = 0;
 
     auto wait_bar = [&](int k, uint32_t parity) -> bool {
         const bool ok = mbar_wait_bounded(&bars[k], parity) || mbar_wait_bounded(&bars[k], parity);
@@ -200,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
             else
                 bulk_g2s(smem + oB1h + 3 * C * kVecTI + t * D * 4, P.alpha + (bt * Hv + hh) * D, D * 4, &bars[4]);
         }
-        in_pend = true;
+        pendm |= 1u << 4;
         fb = 0.0f, fga = 1.0f;
         if (tid < ntt) {
             const size_t bt = (size_t)bb * L + tb + tid;
@@ -230,8 +231,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
         float *Sg = static_cast<float *>(P.pool) + ((size_t)slot * Hv + h) * D * D;
         // the tile's state by bulk copy into the KT / R-W operand buffers (free until this
         // tile's first group has read it); the following tile's slot and count, read now
-        st_pend = true;
+        pendm |= 1u << 3;
         if (tid == 0) {
+            bulk_store_wait_read();  // the previous tile's state has left the staging buffers
             mbar_arrive_expect_tx(&bars[3], (uint32_t)(D * D * 4));
             for (int part = 0; part < 4; ++part)
                 bulk_g2s(smem + oKTh + part * (D * D), Sg + part * (D * D / 4), D * D, &bars[3]);
@@ -255,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
                     break;
                 }
                 iph ^= 1u;
-                in_pend = false;
+                pendm &= ~(1u << 4);
 #pragma unroll
                 for (int j = 0; j < C / 2; ++j) {
                     const int t = (C / 2) * hf + j;
@@ -333,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
             }
             if (t0 == 0) {
                 sph ^= 1u;
-                st_pend = false;
+                pendm &= ~(1u << 3);
             }
 #pragma unroll
             for (int u0 = 0; u0 < 64; u0 += 16) {
@@ -364,18 +366,20 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
             // ---- the Gram products (factored form): G = [Khat_hi ; Qhat_hi ; Khat_lo ; Qhat_lo]
             // [Kchk_hi + Kchk_lo]^T, so that A = G[0..31] + G[64..95] and Bm = G[32..63] +
             // G[96..127] hold all four products of the split pairs; then MMA 1: [P^T | Oq^T] =
-            // S0^T [Khat ; Qhat]^T, A from tensor memory
-            if (tid == 0) {
+            // S0^T [Khat ; Qhat]^T, A from tensor memory.  Two warps issue (one thread each): the
+            // tensor pipe takes the two streams faster than one thread's back-to-back issue.
+            if (tid == 0 && fast) {
                 tc::fence_after_sync();
-                if (fast) {
-                    const uint32_t ig = tc::idesc_tf32(128, C);
+                const uint32_t ig = tc::idesc_tf32(128, C);
 #pragma unroll 1
-                    for (int s = 0; s < D / 8; ++s) {
-                        tc::mma_tf32(tbase + cG, dG + 16 * s, dKCh + 16 * s, ig, s > 0);
-                        tc::mma_tf32(tbase + cG, dG + 16 * s, dKCl + 16 * s, ig, true);
-                    }
-                    tc::commit(&bars[5]);
+                for (int s = 0; s < D / 8; ++s) {
+                    tc::mma_tf32(tbase + cG, dG + 16 * s, dKCh + 16 * s, ig, s > 0);
+                    tc::mma_tf32(tbase + cG, dG + 16 * s, dKCl + 16 * s, ig, true);
                 }
+                tc::commit(&bars[5]);
+            }
+            if (tid == 32) {
+                tc::fence_after_sync();
                 const uint32_t id = tc::idesc_tf32(128, 2 * C);
 #pragma unroll 1
                 for (int s = 0; s < D / 8; ++s) {
@@ -387,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
                 }
                 tc::commit(&bars[0]);
             }
-            mma_pend = 0;
+            pendm |= fast ? (1u | 1u << 5) : 1u;
             // ---- meanwhile: Ktil^T, then L = diag(beta) A, the Bm operand and T on the CUDA cores
             if (fast) {  // Ktil[i][c] = Kchk_i[c] Gamma_C[c]: thread (c, i = 16 hf ..), 4 i per store
                 const float gcc = gC[v];
@@ -414,6 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
                     break;
                 }
                 gph ^= 1u;
+                pendm &= ~(1u << 5);
                 tc::fence_after_sync();
                 float g[16];
                 tc::ld16(tm + cG + (C / 2) * hf, g);
@@ -507,6 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
                 failed = true;
                 break;
             }
+            pendm &= ~1u;
             tc::fence_after_sync();
             if (t0 + C < n) {
                 fetch(item, t0 + C);
@@ -547,11 +553,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
                 }
                 tc::commit(&bars[1]);
             }
-            mma_pend = 1;
+            pendm |= 1u << 1;
             if (!wait_bar(1, ph)) {
                 failed = true;
                 break;
             }
+            pendm &= ~(1u << 1);
             tc::fence_after_sync();
             {
                 float wv[16];
@@ -565,10 +572,11 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
             fence_proxy_async_smem();
             tc::fence_before_sync();
             __syncthreads();
-            // ---- MMA 3: O^T = Oq^T + W^T Bm^T;  MMA 4: S_C^T = Gamma_C S0^T + W^T Ktil
+            // ---- MMA 3: O^T = Oq^T + W^T Bm^T (thread 0);  MMA 4: S_C^T = Gamma_C S0^T + W^T Ktil
+            // (thread 32)
             if (tid == 0) {
                 tc::fence_after_sync();
-                const uint32_t idc = tc::idesc_tf32(128, C), idd = tc::idesc_tf32(128, D);
+                const uint32_t idc = tc::idesc_tf32(128, C);
 #pragma unroll
                 for (int s = 0; s < C / 8; ++s) {
                     const uint64_t ah = dA2h + 16 * s, al = dA2l + 16 * s;
@@ -576,18 +584,27 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
                     tc::mma_tf32(tbase + cOq, ah, bh, idc, true);
                     tc::mma_tf32(tbase + cOq, ah, bl, idc, true);
                     tc::mma_tf32(tbase + cOq, al, bh, idc, true);
+                }
+                tc::commit(&bars[2]);
+            } else if (tid == 32) {
+                tc::fence_after_sync();
+                const uint32_t idd = tc::idesc_tf32(128, D);
+#pragma unroll
+                for (int s = 0; s < C / 8; ++s) {
+                    const uint64_t ah = dA2h + 16 * s, al = dA2l + 16 * s;
                     const uint64_t kh = dKTh + 16 * s, kl = dKTl + 16 * s;
                     tc::mma_tf32(tbase + cS, ah, kh, idd, true);
                     tc::mma_tf32(tbase + cS, ah, kl, idd, true);
                     tc::mma_tf32(tbase + cS, al, kh, idd, true);
                 }
-                tc::commit(&bars[2]);
+                tc::commit(&bars[6]);
             }
-            mma_pend = 2;
-            if (!wait_bar(2, ph)) {
+            pendm |= 1u << 2 | 1u << 6;
+            if (!wait_bar(2, ph) || !wait_bar(6, ph)) {
                 failed = true;
                 break;
             }
+            pendm &= ~(1u << 2 | 1u << 6);
             tc::fence_after_sync();
             if (o_g) {
                 float ov[16];
@@ -600,27 +617,37 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
                 }
             }
             ph ^= 1u;
-            mma_pend = -1;
         }
         if (failed) break;
-        // ---- the tile's final state back to HBM (thread (v, hf): key channels 64 hf ..)
+        // ---- the tile's final state to the staging buffers (thread (v, hf): key channels 64 hf ..,
+        // rows of the pool's layout), then to HBM by bulk copies that run on while the next
+        // tile starts (the next state copy into these buffers waits until they have been read)
+        {
+            float *stg = reinterpret_cast<float *>(smem + oKTh);
 #pragma unroll
-        for (int u0 = 0; u0 < 64; u0 += 16) {
-            float y[16];
-            tc::ld16(tm + cS + 64 * hf + u0, y);
-            tc::wait_ld();
+            for (int u0 = 0; u0 < 64; u0 += 16) {
+                float y[16];
+                tc::ld16(tm + cS + 64 * hf + u0, y);
+                tc::wait_ld();
 #pragma unroll
-            for (int j = 0; j < 16; ++j) Sg[(size_t)(64 * hf + u0 + j) * D + v] = y[j];
+                for (int j = 0; j < 16; ++j) stg[(64 * hf + u0 + j) * D + v] = y[j];
+            }
+            fence_proxy_async_smem();
+            __syncthreads();
+            if (tid == 0) {
+                for (int part = 0; part < 4; ++part)
+                    bulk_s2g(Sg + part * (D * D / 4), smem + oKTh + part * (D * D), D * D);
+                bulk_store_commit();
+            }
         }
-        __syncthreads();  // the next tile's state copy lands in buffers read until here
     }
     if (failed) {
         // give what is still in flight a bounded time to land before the memory is released
-        if (in_pend) mbar_wait_bounded(&bars[4], iph);
-        if (st_pend) mbar_wait_bounded(&bars[3], sph);
-        if (mma_pend >= 0) mbar_wait_bounded(&bars[mma_pend], ph);  // a commit covers every earlier MMA
+        for (int k = 0; k < kBars; ++k)
+            if (pendm >> k & 1u) mbar_wait_bounded(&bars[k], k == 3 ? sph : k == 4 ? iph : k == 5 ? gph : ph);
         if (tid == 0) report_bits(P.status, RS_DEV_PIPE_TIMEOUT);
     }
+    if (tid == 0) bulk_store_wait_all();  // the last state copies out have landed
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
