@@ -41,6 +41,11 @@
 // copies, the vectors for the next group while the current one finishes.
 // The result equals the token-by-token recurrence up to rounding (not bit
 // for bit: the order of the sums differs).
+#include <cuda.h>  // CUtensorMap and the tiled-encode signature (called through the runtime)
+
+#include <cstring>
+#include <type_traits>
+
 #include "rs_internal.h"
 #include "rs_device.cuh"
 #include "rs_tc.cuh"
@@ -58,17 +63,19 @@ constexpr int D = 128;                 // dk = dv
 constexpr int C = 32;                  // tokens per group
 constexpr int kThreads = 256;          // two threads per value column
 constexpr uint32_t kTmemCols = 512;
-constexpr int DP = D + 4;              // padded row of the staged token vectors (bank spread)
+constexpr int DP = D + 4;              // padded fp32 row of alpha / Gamma / Kchk (bank spread)
 
 // shared memory (bytes): tf32 operands in the K-major core-matrix layout of
-// rs_tc.cuh, hi and lo parts; staged token inputs; small matrices
+// rs_tc.cuh, hi and lo parts; the group's token vectors as copied in (rows of
+// D values and 16 bytes of zeros, so that 16-byte reads by token stay clear of
+// bank conflicts); small matrices
 constexpr int kB1 = 2 * C * D * 4;     // [Khat ; Qhat] (N = 2C, K = u), per part
 constexpr int kCC = C * C * 4;         // T or Bm (N = t, K = i)
 constexpr int CA = C + 1;              // row of L = diag(beta) A in shared memory (bank spread)
 constexpr int kKT = D * C * 4;         // Ktil^T (N = c, K = i)
 constexpr int kA2 = D * C * 4;         // R^T, then W^T (M = v, K = t)
-constexpr int kTok = C * DP * 4;       // k, q or alpha of the group, [t][c] fp32
-constexpr int oB1h = 0, oB1l = oB1h + kB1;                   // also: the next group's raw vectors
+constexpr int kTok = C * DP * 4;       // [t][c] fp32 rows, or one token vector of the widest input type
+constexpr int oB1h = 0, oB1l = oB1h + kB1;
 constexpr int oKTh = oB1l + kB1, oKTl = oKTh + kKT;          // KT, A2: also a tile's staged state
 constexpr int oA2h = oKTl + kKT, oA2l = oA2h + kA2;
 constexpr int oTh = oA2l + kA2, oTl = oTh + kCC, oBh = oTl + kCC, oBl = oBh + kCC;
@@ -81,10 +88,48 @@ constexpr int oBar = oMA + C * CA * 4, oTslot = oBar + kBars * 8;
 // q rows, which the factored form no longer reads once Khat, Qhat and Kchk are formed
 constexpr int oKCh = oK, oKCl = oK + C * D * 4;
 static_assert(oKCl + C * D * 4 <= oAl, "Kchk operand fits the k and q rows");
-constexpr int kSmem = oTslot + 16;
+constexpr int oV = (oTslot + 16 + 127) / 128 * 128;  // the group's v rows
+constexpr int kSmem = oV + kTok;
 static_assert(kSmem <= 232448, "fits the shared memory of one SM");
 static_assert(oKTh + D * D * 4 == oTh, "the staged state fills KT and the R/W operand");
 static_assert(oBar % 8 == 0 && oKTh % 16 == 0 && oA2h % 16 == 0, "alignment");
+static_assert(oK % 128 == 0 && oAl % 128 == 0 && oV % 128 == 0, "tensor-copy destinations");
+
+// The group's token vectors come in by 3-D tensor copies: a tensor [rows][heads][D]
+// (rows = sequence x token) and a box of C rows of one head, D + 16 bytes wide
+// (the columns past D lie outside the tensor and arrive as zeros).
+struct ChunkMaps {
+    CUtensorMap k, q, v, a;  // a: per-channel decays (KDA)
+};
+__device__ __forceinline__ void tma_rows(void *dst, const CUtensorMap *map, int head, int row, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(head), "r"(row), "r"(smem_addr(bar))
+        : "memory");
+}
+// 16 consecutive input values (16-byte aligned) as fp32
+template <typename TI>
+__device__ __forceinline__ void load16(const uint8_t *p, float (&x)[16]) {
+    if constexpr (sizeof(TI) == 4) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float4 f = reinterpret_cast<const float4 *>(p)[j];
+            x[4 * j] = f.x, x[4 * j + 1] = f.y, x[4 * j + 2] = f.z, x[4 * j + 3] = f.w;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const uint4 u = reinterpret_cast<const uint4 *>(p)[j];
+            const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                x[8 * j + 2 * e] = load_as_f32<TI>(reinterpret_cast<const TI *>(&wd[e]));
+                x[8 * j + 2 * e + 1] = load_as_f32<TI>(reinterpret_cast<const TI *>(&wd[e]) + 1);
+            }
+        }
+    }
+}
 
 // tensor-memory columns: S^T, its tf32 high part and remainder, then P^T, Oq^T, W^T and the
 // Gram products G
@@ -110,13 +155,17 @@ __device__ __forceinline__ float4 mul4(float4 a, float4 b) {
 }
 
 template <bool KDA, typename TI, typename TO>
-__global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid_constant__ PrefillParams P) {
+__global__ void __launch_bounds__(kThreads, 1)
+    chunk_prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ ChunkMaps M) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, w = tid >> 5;
     const int v = tid & (D - 1);  // value column (and key channel c in the per-channel work)
     const int hf = tid >> 7;      // which half of the column's channels / tokens
-    float *kS = reinterpret_cast<float *>(smem + oK);   // [t][DP]: k, then Khat (factored form)
-    float *qS = reinterpret_cast<float *>(smem + oQ);   // [t][DP]: q, then Qhat (factored form)
+    // the group's vectors as copied in: k and q rows (then the Kchk operand), v rows; alpha
+    // rows (KDA) land in aS, which then holds Gamma and Kchk
+    constexpr int RP = D * (int)sizeof(TI) + 16;  // bytes per copied row
+    static_assert(2 * C * RP <= 2 * kTok && C * RP <= kTok, "copied rows fit");
+    const uint8_t *rawK = smem + oK, *rawQ = smem + oK + C * RP, *rawV = smem + oV;
     float *aS = reinterpret_cast<float *>(smem + oAl);  // [t][DP]: alpha, Gamma, then Kchk
     float *betaS = reinterpret_cast<float *>(smem + oBeta);
     float *alpS = reinterpret_cast<float *>(smem + oAlpS);
@@ -152,9 +201,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
 
     const int Hv = P.Hv, Hk = P.Hk, L = P.L;
     const int items = P.B * Hv;
-    const TI *q_g = static_cast<const TI *>(P.q);
-    const TI *k_g = static_cast<const TI *>(P.k);
-    const TI *v_g = static_cast<const TI *>(P.v);
     TO *o_g = static_cast<TO *>(P.o);
     uint32_t ph = 0, sph = 0, iph = 0, gph = 0;  // barrier parities: MMAs, state copy, input copy, Gram
     bool failed = false;
@@ -175,31 +221,22 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
         }
         return items;
     };
-    // a group's token vectors by bulk copies into the [Khat ; Qhat] operand buffers (free from
-    // the end of MMA 1 to the next group's decays), raw: k, q, v [C][D] TI, then (KDA) alpha
-    // [C][D] fp32, one copy per thread on lanes 0..15 of every warp (copies from one warp
-    // issue one after another); the per-token scalars (beta, GDN alpha) into registers
-    constexpr uint32_t kVecTI = D * (uint32_t)sizeof(TI);
-    const uint8_t *rawK = smem + oB1h, *rawQ = rawK + C * kVecTI, *rawV = rawQ + C * kVecTI;
-    const float *rawA = reinterpret_cast<const float *>(rawV + C * kVecTI);
-    static_assert(3 * C * D * sizeof(TI) + (KDA ? C * D * 4 : 0) <= 2 * kB1, "raw inputs fit the operand buffers");
+    // a group's token vectors by tensor copies (one thread issues them), the per-token scalars
+    // (beta, GDN alpha) into registers of threads 0..C-1; rows past the sequence's tokens are
+    // copied too and masked where read
+    constexpr uint32_t kInBytes = 3u * C * RP + (KDA ? (uint32_t)C * DP * 4 : 0u);
     float fb = 0.0f, fga = 1.0f;  // beta and the GDN decay of token tid of the fetched group
     auto fetch = [&](int it, int tb) {
         const int bb = it / Hv, hh = it - bb * Hv, gg = hh / (Hv / Hk);
         const int nn = P.n_tokens ? P.n_tokens[bb] : L;
         const int ntt = min(C, nn - tb);
-        if (tid == 0) mbar_arrive_expect_tx(&bars[4], (uint32_t)ntt * (3 * kVecTI + (KDA ? D * 4 : 0)));
-        __syncthreads();  // the expected bytes are set before any copy can complete
-        const int y = tid & 31, vec = w >> 1, t = 16 * (w & 1) + y;
-        if (y < 16 && t < ntt && (KDA || vec < 3)) {
-            const size_t bt = (size_t)bb * L + tb + t;
-            if (vec == 0) bulk_g2s(smem + oB1h + t * kVecTI, k_g + (bt * Hk + gg) * D, kVecTI, &bars[4]);
-            else if (vec == 1)
-                bulk_g2s(smem + oB1h + (C + t) * kVecTI, q_g + (bt * Hk + gg) * D, kVecTI, &bars[4]);
-            else if (vec == 2)
-                bulk_g2s(smem + oB1h + (2 * C + t) * kVecTI, v_g + (bt * Hv + hh) * D, kVecTI, &bars[4]);
-            else
-                bulk_g2s(smem + oB1h + 3 * C * kVecTI + t * D * 4, P.alpha + (bt * Hv + hh) * D, D * 4, &bars[4]);
+        if (tid == 0) {
+            const int row = bb * L + tb;
+            mbar_arrive_expect_tx(&bars[4], kInBytes);
+            tma_rows(smem + oK, &M.k, gg, row, &bars[4]);
+            tma_rows(smem + oK + C * RP, &M.q, gg, row, &bars[4]);
+            tma_rows(smem + oV, &M.v, hh, row, &bars[4]);
+            if (KDA) tma_rows(smem + oAl, &M.a, hh, row, &bars[4]);
         }
         pendm |= 1u << 4;
         fb = 0.0f, fga = 1.0f;
@@ -244,32 +281,24 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
 
         for (int t0 = 0; t0 < n && !failed; t0 += C) {
             const int nt = min(C, n - t0);
-            // ---- the group's vectors (copied in during the previous group, or at start) to
-            // padded fp32 rows; pads: k = q = 0, alpha = 1, v = 0, beta = 0
-            float vt[C / 2];  // value v of tokens 16 hf .. 16 hf + 15
-            {
-                if (tid < C) {
-                    betaS[tid] = fb;
-                    alpS[tid] = fga;
-                }
-                if (!wait_bar(4, iph)) {
-                    failed = true;
-                    break;
-                }
-                iph ^= 1u;
-                pendm &= ~(1u << 4);
-#pragma unroll
-                for (int j = 0; j < C / 2; ++j) {
-                    const int t = (C / 2) * hf + j;
-                    const bool real = t < nt;
-                    kS[t * DP + v] = real ? load_as_f32<TI>(reinterpret_cast<const TI *>(rawK + t * kVecTI) + v) : 0.0f;
-                    qS[t * DP + v] = real ? load_as_f32<TI>(reinterpret_cast<const TI *>(rawQ + t * kVecTI) + v) : 0.0f;
-                    vt[j] = real ? load_as_f32<TI>(reinterpret_cast<const TI *>(rawV + t * kVecTI) + v) : 0.0f;
-                    if constexpr (KDA) aS[t * DP + v] = real ? rawA[t * D + v] : 1.0f;
-                    else aS[t * DP + v] = alpS[t];  // 1 for pads
-                }
+            // ---- the group's vectors (copied in during the previous group, or at start); pads
+            // (t >= nt): k = q = v = 0, alpha = 1, beta = 0
+            if (tid < C) {
+                betaS[tid] = fb;
+                alpS[tid] = fga;
             }
-            __syncthreads();  // raw vectors consumed: the operand buffers may be rewritten
+            if (!wait_bar(4, iph)) {
+                failed = true;
+                break;
+            }
+            iph ^= 1u;
+            pendm &= ~(1u << 4);
+            auto kv = [&](int t, int cc) -> float {  // k and q of token t, channel cc (0 for pads)
+                return t < nt ? load_as_f32<TI>(reinterpret_cast<const TI *>(rawK + t * RP) + cc) : 0.0f;
+            };
+            auto qv = [&](int t, int cc) -> float {
+                return t < nt ? load_as_f32<TI>(reinterpret_cast<const TI *>(rawQ + t * RP) + cc) : 0.0f;
+            };
             // ---- cumulative decays Gamma_t[c] of channel c = v; the factored form if none is tiny
             const int c = v;
             float gam[C];
@@ -277,7 +306,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
                 float pg = 1.0f;
 #pragma unroll
                 for (int t = 0; t < C; ++t) {
-                    pg = __fmul_rn(pg, aS[t * DP + c]);
+                    const float a = KDA ? (t < nt ? aS[t * DP + c] : 1.0f) : alpS[t];
+                    pg = __fmul_rn(pg, a);
                     gam[t] = pg;
                 }
             }
@@ -293,11 +323,17 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
                 // and Kchk (fp32 rows now, its operand once every k and q row has been read),
                 // with 16-byte accesses (a quarter warp spans 8 rows)
                 const int t = tid % C, cb0 = 16 * (tid / C);
+                const bool real = t < nt;
+                float kx[16], qx[16];
+                load16<TI>(rawK + t * RP + cb0 * (int)sizeof(TI), kx);
+                load16<TI>(rawQ + t * RP + cb0 * (int)sizeof(TI), qx);
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
                     const int cb = cb0 + 4 * q4;
-                    const float4 k4 = *reinterpret_cast<const float4 *>(kS + t * DP + cb);
-                    const float4 qv4 = *reinterpret_cast<const float4 *>(qS + t * DP + cb);
+                    const float4 k4 = real ? make_float4(kx[4 * q4], kx[4 * q4 + 1], kx[4 * q4 + 2], kx[4 * q4 + 3])
+                                           : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                    const float4 qv4 = real ? make_float4(qx[4 * q4], qx[4 * q4 + 1], qx[4 * q4 + 2], qx[4 * q4 + 3])
+                                            : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
                     const float4 g4 = *reinterpret_cast<const float4 *>(aS + t * DP + cb);
                     const float4 kh = mul4(k4, g4), qh = mul4(qv4, g4);
                     const float4 kc = make_float4(__fmul_rn(k4.x, __frcp_rn(g4.x)), __fmul_rn(k4.y, __frcp_rn(g4.y)),
@@ -306,15 +342,18 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
                     put_split4(smem + oB1h, smem + oB1l, tc::kmajor_offset(C + t, cb, D), qh.x, qh.y, qh.z, qh.w);
                     *reinterpret_cast<float4 *>(aS + t * DP + cb) = kc;
                 }
-            } else if (hf == 0) {  // tiny decays: Khat rows of channel c
+            } else if (hf == 0) {  // tiny decays: Khat rows of channel c; alpha of the pads 1
 #pragma unroll
-                for (int t = 0; t < C; ++t)
-                    put_split(smem + oB1h, smem + oB1l, tc::kmajor_offset(t, c, D), __fmul_rn(kS[t * DP + c], gam[t]));
+                for (int t = 0; t < C; ++t) {
+                    put_split(smem + oB1h, smem + oB1l, tc::kmajor_offset(t, c, D), __fmul_rn(kv(t, c), gam[t]));
+                    if (!KDA) aS[t * DP + c] = alpS[t];
+                    else if (t >= nt) aS[t * DP + c] = 1.0f;
+                }
                 gC[c] = gam[C - 1];
             } else {  // tiny decays: Qhat rows of channel c
 #pragma unroll
                 for (int t = 0; t < C; ++t)
-                    put_split(smem + oB1h, smem + oB1l, tc::kmajor_offset(C + t, c, D), __fmul_rn(qS[t * DP + c], gam[t]));
+                    put_split(smem + oB1h, smem + oB1l, tc::kmajor_offset(C + t, c, D), __fmul_rn(qv(t, c), gam[t]));
             }
             __syncthreads();  // Gamma_C of every channel; every k and q row read
             if (fast) {
@@ -406,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
                 float tail = 1.0f;  // prod_{s=i+1..C-1} alpha_s[c]
 #pragma unroll
                 for (int i = C - 1; i >= 0; --i) {
-                    put_split(smem + oKTh, smem + oKTl, tc::kmajor_offset(c, i, C), __fmul_rn(kS[i * DP + c], tail));
+                    put_split(smem + oKTh, smem + oKTl, tc::kmajor_offset(c, i, C), __fmul_rn(kv(i, c), tail));
                     tail = __fmul_rn(tail, aS[i * DP + c]);
                 }
             }
@@ -459,14 +498,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
 #pragma unroll 1
                 for (int m = 0; m < D / 8; ++m) {
                     const int cc = cq + 8 * m;
-                    const float ki = kS[i * DP + cc];
+                    const float ki = kv(i, cc);
                     float rho = 1.0f;  // prod_{s=i+1..t} alpha_s[cc]
 #pragma unroll
                     for (int t = 0; t < C; ++t) {
                         if (t > i) rho = __fmul_rn(rho, aS[t * DP + cc]);
                         const float kr = __fmul_rn(ki, rho);
-                        if (t > i) accA[t] = __fmaf_rn(kS[t * DP + cc], kr, accA[t]);
-                        if (t >= i) accB[t] = __fmaf_rn(qS[t * DP + cc], kr, accB[t]);
+                        if (t > i) accA[t] = __fmaf_rn(kv(t, cc), kr, accA[t]);
+                        if (t >= i) accB[t] = __fmaf_rn(qv(t, cc), kr, accB[t]);
                     }
                 }
 #pragma unroll
@@ -507,24 +546,22 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
                     put_split(smem + oTh, smem + oTl, tc::kmajor_offset(r + 8 * m, j, C), x[m]);
             }
             fence_proxy_async_smem();
-            // ---- MMA 1 done: the next group's (or tile's) vectors come in now
+            // ---- MMA 1 done
             if (!wait_bar(0, ph)) {
                 failed = true;
                 break;
             }
             pendm &= ~1u;
             tc::fence_after_sync();
-            if (t0 + C < n) {
-                fetch(item, t0 + C);
-            } else {
-                const bool nx_ok = nx_slot >= 0 && (int64_t)nx_slot < P.n_slots && nx_n >= 1 && nx_n <= L;
-                const int nxt = nx_ok ? nxi : next_work(nxi);
-                if (nxt < items) fetch(nxt, 0);
-            }
             // ---- R^T = diag(beta) (V^T - P^T) for tokens 16 hf .. 16 hf + 15
             {
-                float pv[16];
+                float pv[16], vt[16];
                 tc::ld16(tm + cP + (C / 2) * hf, pv);
+#pragma unroll
+                for (int j = 0; j < C / 2; ++j) {
+                    const int t = (C / 2) * hf + j;
+                    vt[j] = t < nt ? load_as_f32<TI>(reinterpret_cast<const TI *>(rawV + t * RP) + v) : 0.0f;
+                }
                 tc::wait_ld();
 #pragma unroll
                 for (int j = 0; j < C / 2; j += 4) {
@@ -535,6 +572,15 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
                                __fmul_rn(betaS[t + 2], __fsub_rn(vt[j + 2], pv[j + 2])),
                                __fmul_rn(betaS[t + 3], __fsub_rn(vt[j + 3], pv[j + 3])));
                 }
+            }
+            __syncthreads();  // every copied row of the group has been read
+            // ---- the next group's (or tile's) vectors come in now
+            if (t0 + C < n) {
+                fetch(item, t0 + C);
+            } else {
+                const bool nx_ok = nx_slot >= 0 && (int64_t)nx_slot < P.n_slots && nx_n >= 1 && nx_n <= L;
+                const int nxt = nx_ok ? nxi : next_work(nxi);
+                if (nxt < items) fetch(nxt, 0);
             }
             fence_proxy_async_smem();
             tc::fence_before_sync();
@@ -654,16 +700,67 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
     if (w == 0) tc::tmem_dealloc(tbase, kTmemCols);
 }
 
+// The driver's tiled tensor-map encoder, reached through the runtime (no link to the driver
+// library); null if this driver does not offer it.
+using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                 const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiled encoder() {
+    static const EncodeTiled fn = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            return (EncodeTiled) nullptr;
+        }
+        return reinterpret_cast<EncodeTiled>(f);
+    }();
+    return fn;
+}
+
+// map of a [rows][heads][D] tensor of `esize`-byte elements, box (D + 16 bytes, 1, C)
+cudaError_t encode_rows(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esize, int heads,
+                        int64_t rows) {
+    const EncodeTiled fn = encoder();
+    if (!fn) return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)rows};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * esize, (cuuint64_t)heads * D * esize};
+    const cuuint32_t box[3] = {(cuuint32_t)((D * esize + 16) / esize), 1u, (cuuint32_t)C};
+    const cuuint32_t step[3] = {1u, 1u, 1u};
+    const CUresult r = fn(m, dt, 3, const_cast<void *>(base), dims, strides, box, step, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <typename TI>
+constexpr CUtensorMapDataType map_type() {
+    if constexpr (sizeof(TI) == 4) return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    else if constexpr (std::is_same_v<TI, __half>) return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    else return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+}
+
 template <bool KDA, typename TI, typename TO>
 cudaError_t run(PrefillParams &P, cudaStream_t s) {
     auto kern = chunk_prefill_kernel<KDA, TI, TO>;
-    cudaError_t e = set_dynamic_smem(reinterpret_cast<const void *>(kern), kSmem);
-    if (e != cudaSuccess) return e;
     const int items = P.B * P.Hv;
+    const int64_t rows = (int64_t)P.B * P.L;
+    if (items < 1 || rows < 1) return cudaSuccess;
+    if (rows > INT32_MAX - C) return cudaErrorNotSupported;  // tensor-copy row coordinates are 32-bit
+    ChunkMaps M;
+    std::memset(&M, 0, sizeof(M));
+    cudaError_t e = encode_rows(&M.k, P.k, map_type<TI>(), (int)sizeof(TI), P.Hk, rows);
+    if (e == cudaSuccess) e = encode_rows(&M.q, P.q, map_type<TI>(), (int)sizeof(TI), P.Hk, rows);
+    if (e == cudaSuccess) e = encode_rows(&M.v, P.v, map_type<TI>(), (int)sizeof(TI), P.Hv, rows);
+    if (e == cudaSuccess && KDA) e = encode_rows(&M.a, P.alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, P.Hv, rows);
+    if (e != cudaSuccess) return e;
+    e = set_dynamic_smem(reinterpret_cast<const void *>(kern), kSmem);
+    if (e != cudaSuccess) return e;
     int grid = device_sm_count();
     if (grid > items) grid = items;
-    if (grid < 1) grid = 1;
-    return launch_pdl(kern, dim3(grid), dim3(kThreads), kSmem, s, P);
+    return launch_pdl(kern, dim3(grid), dim3(kThreads), kSmem, s, P, M);
 }
 
 template <bool KDA>
