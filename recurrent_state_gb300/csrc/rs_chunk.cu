@@ -21,26 +21,33 @@
 // two threads v and v + 128 share value column v, which is tensor-memory
 // lane v of every M = 128 product below (each takes half of the column's key
 // channels or tokens).  The state lives in tensor memory as S^T (lane v,
-// columns u) across the groups of a tile, with its tf32 high part and exact
-// remainder beside it as the A operand of the first product.  Per group of
-// C = 32 tokens:
-//   MMA 1   [P^T | Oq^T] = S0^T [Khat ; Qhat]^T      (K = 128, N = 2C, A in tensor memory)
-//   MMA 2   W^T = R^T T^T, T = (I + diag(beta) A)^{-1}  (K = C, N = C)
-//   MMA 3   O^T = Oq^T + W^T Bm^T                      (K = C, N = C)
+// columns u) across the groups of a tile.  Per group of C = 32 tokens:
+//   G       [Khat ; Qhat] Kchk^T  (the C x C matrices A and Bm)   (K = 128)
+//   MMA 1   [P^T | Oq^T] = S0^T [Khat ; Qhat]^T      (K = 128, A in tensor memory)
+//   MMA 2   W^T = R^T T^T, T = (I + diag(beta) A)^{-1}  (K = C)
+//   MMA 3   O^T = Oq^T + W^T Bm^T                      (K = C)
 //   MMA 4   S_C^T = Gamma_C S0^T + W^T Ktil             (K = C, N = 128)
-// all of kind::tf32 with each fp32 operand split into a tf32 high part and
-// an exact remainder (three products: hi*hi + hi*lo + lo*hi, about 2^-21
-// relative), fp32 accumulation in tensor memory.  The C x C matrices A, Bm
-// and the unit lower triangular inverse T run on the CUDA cores while MMA 1
-// runs: A[t][i] = Khat_t . Kchk_i and Bm[t][i] = Qhat_t . Kchk_i with
-// Kchk_i = k_i / Gamma_i (the decay products factor through the cumulative
-// decay), unless some cumulative decay of the group falls below 1e-30, where
-// each pair takes the running product of its decays instead; T by forward
-// substitution through the unit lower triangular I + diag(beta) A.
-// A tile's state (64 KB) and each group's token vectors arrive by bulk
-// copies, the vectors for the next group while the current one finishes.
-// The result equals the token-by-token recurrence up to rounding (not bit
-// for bit: the order of the sums differs).
+// all of kind::tf32, which reads an fp32 operand as tf32 by dropping its low
+// 13 mantissa bits: each operand x is taken as hi = x (so read) plus the
+// exact remainder lo = x - hi, and the products hi*hi + hi*lo + lo*hi (about
+// 2^-21 relative) accumulate in fp32 in tensor memory.  Where one operand is
+// shared, its hi and lo parts stack along M or N so that one instruction
+// makes two of the three products (G: [hi ; lo] rows of Khat and Qhat; MMA 1
+// to 3: [hi ; lo] rows of the B operand), and the accumulator columns that
+// hold them are summed when read.  A[t][i] = Khat_t . Kchk_i and
+// Bm[t][i] = Qhat_t . Kchk_i with Kchk_i = k_i / Gamma_i (the decay products
+// factor through the cumulative decay), unless some cumulative decay of the
+// group falls below 1e-20, where the CUDA cores take the running product of
+// each pair's decays instead; T by forward substitution through the unit
+// lower triangular I + diag(beta) A.  In the factored form MMA 4 adds
+// W^T Kchk to the unscaled S0^T and the decay Gamma_C is applied when the
+// state is next read (the next group, or the tile's end): the same sum, with
+// Ktil = Gamma_C Kchk, whose rounding is relative to the result either way.
+// A tile's state (64 KB) arrives by bulk copies during the previous tile,
+// each group's token vectors by tensor copies during the previous group, and
+// the final state leaves by bulk copies while the next tile starts.  The
+// result equals the token-by-token recurrence up to rounding (not bit for
+// bit: the order of the sums differs).
 #include <cuda.h>  // CUtensorMap and the tiled-encode signature (called through the runtime)
 
 #include <cstring>
@@ -76,7 +83,7 @@ constexpr int kKT = D * C * 4;         // Ktil^T (N = c, K = i)
 constexpr int kA2 = D * C * 4;         // R^T, then W^T (M = v, K = t)
 constexpr int kTok = C * DP * 4;       // [t][c] fp32 rows, or one token vector of the widest input type
 constexpr int oB1h = 0, oB1l = oB1h + kB1;
-constexpr int oKTh = oB1l + kB1, oKTl = oKTh + kKT;          // KT, A2: also a tile's staged state
+constexpr int oKTh = oB1l + kB1, oKTl = oKTh + kKT;          // KT, A2: also a tile's final state
 constexpr int oA2h = oKTl + kKT, oA2l = oA2h + kA2;
 constexpr int oTh = oA2l + kA2, oTl = oTh + kCC, oBh = oTl + kCC, oBl = oBh + kCC;
 constexpr int oK = oBl + kCC, oQ = oK + kTok, oAl = oQ + kTok;
@@ -91,7 +98,9 @@ static_assert(oKCl + C * D * 4 <= oAl, "Kchk operand fits the k and q rows");
 constexpr int oV = (oTslot + 16 + 127) / 128 * 128;  // the group's v rows
 constexpr int kSmem = oV + kTok;
 static_assert(kSmem <= 232448, "fits the shared memory of one SM");
-static_assert(oKTh + D * D * 4 == oTh, "the staged state fills KT and the R/W operand");
+static_assert(oKTh + D * D * 4 == oTh, "the final state fills KT and the R/W operand");
+static_assert(2 * kB1 == D * D * 4, "a tile's incoming state fills the [Khat ; Qhat] operand buffers");
+static_assert(oTl == oTh + kCC && oBl == oBh + kCC, "T and Bm: remainder rows follow the high rows");
 static_assert(oBar % 8 == 0 && oKTh % 16 == 0 && oA2h % 16 == 0, "alignment");
 static_assert(oK % 128 == 0 && oAl % 128 == 0 && oV % 128 == 0, "tensor-copy destinations");
 
@@ -131,11 +140,12 @@ __device__ __forceinline__ void load16(const uint8_t *p, float (&x)[16]) {
     }
 }
 
-// tensor-memory columns: S^T, its tf32 high part and remainder, then P^T, Oq^T, W^T and the
-// Gram products G
-constexpr uint32_t cS = 0, cSh = D, cSl = 2 * D, cP = 3 * D, cOq = 3 * D + C, cW = 3 * D + 2 * C,
-                   cG = 3 * D + 3 * C;
-static_assert(cG + C <= kTmemCols, "tensor memory");
+// tensor-memory columns: S^T (also MMA 1's high part) and its remainder; MMA 1's accumulator
+// D1 = [hi*hi + lo*hi of P^T | of Oq^T | hi*lo of P^T | of Oq^T]; the Gram products G; W^T
+// (MMA 2: [hi*hi + lo*hi | hi*lo]), whose columns then take MMA 3's W^T Bm^T likewise
+constexpr uint32_t cS = 0, cSl = D, cD1 = 2 * D, cG = 3 * D, cW = 3 * D + C;
+static_assert(cW + 2 * C <= kTmemCols, "tensor memory");
+constexpr float kFastMin = 1e-20f;  // smallest cumulative decay of the factored form
 
 // store x as a tf32 pair (hi, exact remainder) at byte offset off of the two buffers
 __device__ __forceinline__ void put_split(uint8_t *hi, uint8_t *lo, uint32_t off, float x) {
@@ -200,6 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dKCh = tc::smem_desc(smem + oKCh, 128, D * 32), dKCl = tc::smem_desc(smem + oKCl, 128, D * 32);
 
     const int Hv = P.Hv, Hk = P.Hk, L = P.L;
+    float *pool = static_cast<float *>(P.pool);
     const int items = P.B * Hv;
     TO *o_g = static_cast<TO *>(P.o);
     uint32_t ph = 0, sph = 0, iph = 0, gph = 0;  // barrier parities: MMAs, state copy, input copy, Gram
@@ -246,15 +257,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!KDA) fga = P.alpha[bt * Hv + hh];
         }
     };
+    // a tile's state by bulk copies into the [Khat ; Qhat] operand buffers, free from the end of
+    // the previous tile's last MMA 1 until this tile's first group has read them
+    auto load_state = [&](int it) {
+        const int bb = it / Hv, hh = it - bb * Hv;
+        const float *src = pool + ((size_t)P.slot_idx[bb] * Hv + hh) * D * D;
+        if (tid == 0) {
+            mbar_arrive_expect_tx(&bars[3], (uint32_t)(D * D * 4));
+            for (int part = 0; part < 4; ++part)
+                bulk_g2s(smem + oB1h + part * (D * D), src + part * (D * D / 4), D * D, &bars[3]);
+        }
+        pendm |= 1u << 3;
+    };
     {
         const int first = next_work(blockIdx.x);
-        if (first < items) fetch(first, 0);
+        if (first < items) {
+            load_state(first);
+            fetch(first, 0);
+        }
+    }
+    // slot and token count of the current tile, read one tile ahead
+    int32_t c_slot = -1, c_n = 0;
+    if ((int)blockIdx.x < items) {
+        c_slot = P.slot_idx[blockIdx.x / Hv];
+        c_n = P.n_tokens ? P.n_tokens[blockIdx.x / Hv] : L;
     }
 
     for (int item = blockIdx.x; item < items && !failed; item += gridDim.x) {
         const int b = item / Hv, h = item - b * Hv;
-        const int32_t slot = P.slot_idx[b];
-        const int32_t n = P.n_tokens ? P.n_tokens[b] : L;
+        const int32_t slot = c_slot, n = c_n;
+        const int nxi = item + gridDim.x;
+        c_slot = nxi < items ? P.slot_idx[nxi / Hv] : -1;
+        c_n = nxi < items ? (P.n_tokens ? P.n_tokens[nxi / Hv] : L) : 0;
         // every thread sees the same item: the skips are uniform
         if (slot < 0 || (int64_t)slot >= P.n_slots) {
             if (tid == 0) report_bits(P.status, 1);
@@ -265,22 +299,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             continue;
         }
         if (n == 0) continue;
-        float *Sg = static_cast<float *>(P.pool) + ((size_t)slot * Hv + h) * D * D;
-        // the tile's state by bulk copy into the KT / R-W operand buffers (free until this
-        // tile's first group has read it); the following tile's slot and count, read now
-        pendm |= 1u << 3;
-        if (tid == 0) {
-            bulk_store_wait_read();  // the previous tile's state has left the staging buffers
-            mbar_arrive_expect_tx(&bars[3], (uint32_t)(D * D * 4));
-            for (int part = 0; part < 4; ++part)
-                bulk_g2s(smem + oKTh + part * (D * D), Sg + part * (D * D / 4), D * D, &bars[3]);
-        }
-        const int nxi = item + gridDim.x;
-        const int32_t nx_slot = nxi < items ? P.slot_idx[nxi / Hv] : -1;
-        const int32_t nx_n = nxi < items ? (P.n_tokens ? P.n_tokens[nxi / Hv] : L) : 0;
+        float *Sg = pool + ((size_t)slot * Hv + h) * D * D;
+        // the next tile this CTA processes (its state and first vectors come in during this
+        // tile's last group)
+        const bool nx_ok = c_slot >= 0 && (int64_t)c_slot < P.n_slots && c_n >= 1 && c_n <= L;
+        int nxt = items;
 
         for (int t0 = 0; t0 < n && !failed; t0 += C) {
             const int nt = min(C, n - t0);
+            const bool last = t0 + C >= n;
             // ---- the group's vectors (copied in during the previous group, or at start); pads
             // (t >= nt): k = q = v = 0, alpha = 1, beta = 0
             if (tid < C) {
@@ -293,12 +320,44 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             iph ^= 1u;
             pendm &= ~(1u << 4);
+            if (t0 == 0) {
+                if (!wait_bar(3, sph)) {
+                    failed = true;
+                    break;
+                }
+                sph ^= 1u;
+                pendm &= ~(1u << 3);
+            }
             auto kv = [&](int t, int cc) -> float {  // k and q of token t, channel cc (0 for pads)
                 return t < nt ? load_as_f32<TI>(reinterpret_cast<const TI *>(rawK + t * RP) + cc) : 0.0f;
             };
             auto qv = [&](int t, int cc) -> float {
                 return t < nt ? load_as_f32<TI>(reinterpret_cast<const TI *>(rawQ + t * RP) + cc) : 0.0f;
             };
+            // ---- S0^T and its tf32 remainder in tensor memory (MMA 1's A operand): thread (v, hf)
+            // takes key channels 64 hf .. 64 hf + 63 of column v, from the staged copy (a tile's
+            // first group) or from the state columns times the previous group's pending decay
+#pragma unroll
+            for (int u0 = 0; u0 < 64; u0 += 16) {
+                const int ub = 64 * hf + u0;
+                float x[16], lo[16];
+                if (t0 == 0) {
+                    const float *st = reinterpret_cast<const float *>(smem + oB1h);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) x[j] = st[(ub + j) * D + v];
+                } else {
+                    tc::ld16(tm + cS + ub, x);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) x[j] = __fmul_rn(x[j], gC[ub + j]);
+                }
+#pragma unroll
+                for (int j = 0; j < 16; ++j) lo[j] = x[j] - tc::tf32_hi(x[j]);
+                tc::st16(tm + cS + ub, x);
+                tc::st16(tm + cSl + ub, lo);
+            }
+            tc::wait_st();
+            tc::fence_before_sync();
             // ---- cumulative decays Gamma_t[c] of channel c = v; the factored form if none is tiny
             const int c = v;
             float gam[C];
@@ -311,7 +370,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     gam[t] = pg;
                 }
             }
-            const bool fast = __syncthreads_and(gam[C - 1] >= 1e-30f);
+            // (also: every thread's state columns are written and the staged state and the
+            // pending decays are read)
+            const bool fast = __syncthreads_and(gam[C - 1] >= kFastMin);
             if (fast) {
                 if (hf == 0) {
 #pragma unroll
@@ -364,49 +425,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     put_split4(smem + oKCh, smem + oKCl, tc::kmajor_offset(t, cb0 + 4 * q4, D), kc.x, kc.y, kc.z, kc.w);
                 }
             }
-            // ---- S0^T (tf32 high part and remainder) as MMA 1's A operand and Gamma_C S0^T as
-            // MMA 4's accumulator, all in tensor memory: thread (v, hf) takes key channels
-            // 64 hf .. 64 hf + 63 of column v, from the staged copy (a tile's first group) or from
-            // the state columns
-            if (t0 == 0 && !wait_bar(3, sph)) {
-                failed = true;
-                break;
-            }
-            if (t0 == 0) {
-                sph ^= 1u;
-                pendm &= ~(1u << 3);
-            }
-#pragma unroll
-            for (int u0 = 0; u0 < 64; u0 += 16) {
-                const int ub = 64 * hf + u0;
-                float x[16], hi[16], lo[16], y[16];
-                if (t0 == 0) {
-                    const float *st = reinterpret_cast<const float *>(smem + oKTh);
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) x[j] = st[(ub + j) * D + v];
-                } else {
-                    tc::ld16(tm + cS + ub, x);
-                    tc::wait_ld();
-                }
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    hi[j] = tc::tf32_hi(x[j]);
-                    lo[j] = x[j] - hi[j];
-                    y[j] = __fmul_rn(x[j], gC[ub + j]);
-                }
-                tc::st16(tm + cSh + ub, hi);
-                tc::st16(tm + cSl + ub, lo);
-                tc::st16(tm + cS + ub, y);
-            }
-            tc::wait_st();
+            if (tid == 0) bulk_store_wait_read();  // the previous tile's final state has left KT / A2
             fence_proxy_async_smem();
             tc::fence_before_sync();
-            __syncthreads();  // operands in place; the staged state is consumed
+            __syncthreads();  // operands in place
             // ---- the Gram products (factored form): G = [Khat_hi ; Qhat_hi ; Khat_lo ; Qhat_lo]
             // [Kchk_hi + Kchk_lo]^T, so that A = G[0..31] + G[64..95] and Bm = G[32..63] +
-            // G[96..127] hold all four products of the split pairs; then MMA 1: [P^T | Oq^T] =
-            // S0^T [Khat ; Qhat]^T, A from tensor memory.  Two warps issue (one thread each): the
-            // tensor pipe takes the two streams faster than one thread's back-to-back issue.
+            // G[96..127] hold all four products of the split pairs; then MMA 1: D1 = S0^T
+            // [Khat ; Qhat ; Khat_lo ; Qhat_lo]^T + S0_lo^T [Khat ; Qhat]^T.  Two warps issue (one
+            // thread each): the tensor pipe takes the two streams faster than one thread's
+            // back-to-back issue.
             if (tid == 0 && fast) {
                 tc::fence_after_sync();
                 const uint32_t ig = tc::idesc_tf32(128, C);
@@ -419,27 +447,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (tid == 32) {
                 tc::fence_after_sync();
-                const uint32_t id = tc::idesc_tf32(128, 2 * C);
+                const uint32_t i4 = tc::idesc_tf32(128, 4 * C), i2 = tc::idesc_tf32(128, 2 * C);
 #pragma unroll 1
                 for (int s = 0; s < D / 8; ++s) {
-                    const uint32_t ah = tbase + cSh + 8 * s, al = tbase + cSl + 8 * s;
-                    const uint64_t bh = dB1h + 16 * s, bl = dB1l + 16 * s;
-                    tc::mma_tf32_ta(tbase + cP, ah, bh, id, s > 0);
-                    tc::mma_tf32_ta(tbase + cP, ah, bl, id, true);
-                    tc::mma_tf32_ta(tbase + cP, al, bh, id, true);
+                    tc::mma_tf32_ta(tbase + cD1, tbase + cS + 8 * s, dB1h + 16 * s, i4, s > 0);
+                    tc::mma_tf32_ta(tbase + cD1, tbase + cSl + 8 * s, dB1h + 16 * s, i2, true);
                 }
                 tc::commit(&bars[0]);
             }
             pendm |= fast ? (1u | 1u << 5) : 1u;
-            // ---- meanwhile: Ktil^T, then L = diag(beta) A, the Bm operand and T on the CUDA cores
-            if (fast) {  // Ktil[i][c] = Kchk_i[c] Gamma_C[c]: thread (c, i = 16 hf ..), 4 i per store
-                const float gcc = gC[v];
+            // ---- meanwhile: Ktil^T (factored form: Kchk^T, the decay pending), then
+            // L = diag(beta) A, the Bm operand and T on the CUDA cores
+            if (fast) {  // thread (c, i = 16 hf ..), 4 i per store
 #pragma unroll
                 for (int i0 = 0; i0 < C / 2; i0 += 4) {
                     const int i = (C / 2) * hf + i0;
-                    put_split4(smem + oKTh, smem + oKTl, tc::kmajor_offset(v, i, C),
-                               __fmul_rn(aS[i * DP + v], gcc), __fmul_rn(aS[(i + 1) * DP + v], gcc),
-                               __fmul_rn(aS[(i + 2) * DP + v], gcc), __fmul_rn(aS[(i + 3) * DP + v], gcc));
+                    put_split4(smem + oKTh, smem + oKTl, tc::kmajor_offset(v, i, C), aS[i * DP + v],
+                               aS[(i + 1) * DP + v], aS[(i + 2) * DP + v], aS[(i + 3) * DP + v]);
                 }
             } else if (hf == 0) {  // running products of the decays
                 float tail = 1.0f;  // prod_{s=i+1..C-1} alpha_s[c]
@@ -553,10 +577,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             pendm &= ~1u;
             tc::fence_after_sync();
+            if (last) {  // the next tile's state into the operand buffers, free from here on
+                nxt = nx_ok ? nxi : next_work(nxi);
+                if (nxt < items) load_state(nxt);
+            }
+            if (!fast) {  // running products: MMA 4 adds Ktil^T W to Gamma_C S0^T, scaled now
+#pragma unroll
+                for (int u0 = 0; u0 < 64; u0 += 16) {
+                    const int ub = 64 * hf + u0;
+                    float x[16];
+                    tc::ld16(tm + cS + ub, x);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) x[j] = __fmul_rn(x[j], gC[ub + j]);
+                    tc::st16(tm + cS + ub, x);
+                }
+                tc::wait_st();
+                tc::fence_before_sync();
+            }
             // ---- R^T = diag(beta) (V^T - P^T) for tokens 16 hf .. 16 hf + 15
             {
-                float pv[16], vt[16];
-                tc::ld16(tm + cP + (C / 2) * hf, pv);
+                float pa[16], pb[16], vt[16];
+                tc::ld16(tm + cD1 + (C / 2) * hf, pa);
+                tc::ld16(tm + cD1 + 2 * C + (C / 2) * hf, pb);
 #pragma unroll
                 for (int j = 0; j < C / 2; ++j) {
                     const int t = (C / 2) * hf + j;
@@ -564,38 +607,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc::wait_ld();
 #pragma unroll
-                for (int j = 0; j < C / 2; j += 4) {
-                    const int t = (C / 2) * hf + j;
-                    put_split4(smem + oA2h, smem + oA2l, tc::kmajor_offset(v, t, C),
-                               __fmul_rn(betaS[t], __fsub_rn(vt[j], pv[j])),
-                               __fmul_rn(betaS[t + 1], __fsub_rn(vt[j + 1], pv[j + 1])),
-                               __fmul_rn(betaS[t + 2], __fsub_rn(vt[j + 2], pv[j + 2])),
-                               __fmul_rn(betaS[t + 3], __fsub_rn(vt[j + 3], pv[j + 3])));
-                }
+                for (int j = 0; j < C / 2; ++j) vt[j] = __fmul_rn(betaS[(C / 2) * hf + j], __fsub_rn(vt[j], __fadd_rn(pa[j], pb[j])));
+#pragma unroll
+                for (int j = 0; j < C / 2; j += 4)
+                    put_split4(smem + oA2h, smem + oA2l, tc::kmajor_offset(v, (C / 2) * hf + j, C), vt[j], vt[j + 1],
+                               vt[j + 2], vt[j + 3]);
             }
-            __syncthreads();  // every copied row of the group has been read
+            __syncthreads();  // every copied row of the group has been read (and the decays applied)
+            if (!fast && hf == 0) gC[v] = 1.0f;  // nothing pending
             // ---- the next group's (or tile's) vectors come in now
-            if (t0 + C < n) {
+            if (!last) {
                 fetch(item, t0 + C);
-            } else {
-                const bool nx_ok = nx_slot >= 0 && (int64_t)nx_slot < P.n_slots && nx_n >= 1 && nx_n <= L;
-                const int nxt = nx_ok ? nxi : next_work(nxi);
-                if (nxt < items) fetch(nxt, 0);
+            } else if (nxt < items) {
+                fetch(nxt, 0);
             }
             fence_proxy_async_smem();
             tc::fence_before_sync();
             __syncthreads();
-            // ---- MMA 2: W^T = R^T T^T
+            // ---- MMA 2: W^T = R^T [T ; T_lo]^T + R_lo^T T^T
             if (tid == 0) {
                 tc::fence_after_sync();
-                const uint32_t id = tc::idesc_tf32(128, C);
+                const uint32_t i2 = tc::idesc_tf32(128, 2 * C), i1 = tc::idesc_tf32(128, C);
 #pragma unroll
                 for (int s = 0; s < C / 8; ++s) {
-                    const uint64_t ah = dA2h + 16 * s, al = dA2l + 16 * s;
-                    const uint64_t bh = dTh + 16 * s, bl = dTl + 16 * s;
-                    tc::mma_tf32(tbase + cW, ah, bh, id, s > 0);
-                    tc::mma_tf32(tbase + cW, ah, bl, id, true);
-                    tc::mma_tf32(tbase + cW, al, bh, id, true);
+                    tc::mma_tf32(tbase + cW, dA2h + 16 * s, dTh + 16 * s, i2, s > 0);
+                    tc::mma_tf32(tbase + cW, dA2l + 16 * s, dTh + 16 * s, i1, true);
                 }
                 tc::commit(&bars[1]);
             }
@@ -607,29 +643,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             pendm &= ~(1u << 1);
             tc::fence_after_sync();
             {
-                float wv[16];
-                tc::ld16(tm + cW + (C / 2) * hf, wv);
+                float wa[16], wb[16];
+                tc::ld16(tm + cW + (C / 2) * hf, wa);
+                tc::ld16(tm + cW + C + (C / 2) * hf, wb);
                 tc::wait_ld();
 #pragma unroll
+                for (int j = 0; j < C / 2; ++j) wa[j] = __fadd_rn(wa[j], wb[j]);
+#pragma unroll
                 for (int j = 0; j < C / 2; j += 4)
-                    put_split4(smem + oA2h, smem + oA2l, tc::kmajor_offset(v, (C / 2) * hf + j, C), wv[j], wv[j + 1],
-                               wv[j + 2], wv[j + 3]);
+                    put_split4(smem + oA2h, smem + oA2l, tc::kmajor_offset(v, (C / 2) * hf + j, C), wa[j], wa[j + 1],
+                               wa[j + 2], wa[j + 3]);
             }
             fence_proxy_async_smem();
             tc::fence_before_sync();
             __syncthreads();
-            // ---- MMA 3: O^T = Oq^T + W^T Bm^T (thread 0);  MMA 4: S_C^T = Gamma_C S0^T + W^T Ktil
-            // (thread 32)
+            // ---- MMA 3 (thread 0): W^T Bm^T into the W^T columns, now free ([hi*hi + lo*hi |
+            // hi*lo]); MMA 4 (thread 32): S^T += W^T Ktil
             if (tid == 0) {
                 tc::fence_after_sync();
-                const uint32_t idc = tc::idesc_tf32(128, C);
+                const uint32_t i2 = tc::idesc_tf32(128, 2 * C), i1 = tc::idesc_tf32(128, C);
 #pragma unroll
                 for (int s = 0; s < C / 8; ++s) {
-                    const uint64_t ah = dA2h + 16 * s, al = dA2l + 16 * s;
-                    const uint64_t bh = dBh + 16 * s, bl = dBl + 16 * s;
-                    tc::mma_tf32(tbase + cOq, ah, bh, idc, true);
-                    tc::mma_tf32(tbase + cOq, ah, bl, idc, true);
-                    tc::mma_tf32(tbase + cOq, al, bh, idc, true);
+                    tc::mma_tf32(tbase + cW, dA2h + 16 * s, dBh + 16 * s, i2, s > 0);
+                    tc::mma_tf32(tbase + cW, dA2l + 16 * s, dBh + 16 * s, i1, true);
                 }
                 tc::commit(&bars[2]);
             } else if (tid == 32) {
@@ -652,22 +688,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             pendm &= ~(1u << 2 | 1u << 6);
             tc::fence_after_sync();
-            if (o_g) {
-                float ov[16];
-                tc::ld16(tm + cOq + (C / 2) * hf, ov);
+            if (o_g) {  // O^T = Oq^T (two parts) + W^T Bm^T (two parts)
+                float oa[16], ob[16], oc[16], od[16];
+                tc::ld16(tm + cD1 + C + (C / 2) * hf, oa);
+                tc::ld16(tm + cD1 + 3 * C + (C / 2) * hf, ob);
+                tc::ld16(tm + cW + (C / 2) * hf, oc);
+                tc::ld16(tm + cW + C + (C / 2) * hf, od);
                 tc::wait_ld();
 #pragma unroll
                 for (int j = 0; j < C / 2; ++j) {
                     const int t = (C / 2) * hf + j;
-                    if (t < nt) store_from_f32<TO>(o_g + (((size_t)b * L + t0 + t) * Hv + h) * D + v, ov[j]);
+                    const float o = __fadd_rn(__fadd_rn(oa[j], ob[j]), __fadd_rn(oc[j], od[j]));
+                    if (t < nt) store_from_f32<TO>(o_g + (((size_t)b * L + t0 + t) * Hv + h) * D + v, o);
                 }
             }
             ph ^= 1u;
         }
         if (failed) break;
-        // ---- the tile's final state to the staging buffers (thread (v, hf): key channels 64 hf ..,
-        // rows of the pool's layout), then to HBM by bulk copies that run on while the next
-        // tile starts (the next state copy into these buffers waits until they have been read)
+        // ---- the tile's final state (the pending decay applied) to the staging buffers (thread
+        // (v, hf): key channels 64 hf .., rows of the pool's layout), then to HBM by bulk copies
+        // that run on while the next tile starts (KT and A2 are next written once they are read)
         {
             float *stg = reinterpret_cast<float *>(smem + oKTh);
 #pragma unroll
@@ -676,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::ld16(tm + cS + 64 * hf + u0, y);
                 tc::wait_ld();
 #pragma unroll
-                for (int j = 0; j < 16; ++j) stg[(64 * hf + u0 + j) * D + v] = y[j];
+                for (int j = 0; j < 16; ++j) stg[(64 * hf + u0 + j) * D + v] = __fmul_rn(y[j], gC[64 * hf + u0 + j]);
             }
             fence_proxy_async_smem();
             __syncthreads();
