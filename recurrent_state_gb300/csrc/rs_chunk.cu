@@ -237,9 +237,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // copied too and masked where read
     constexpr uint32_t kInBytes = 3u * C * RP + (KDA ? (uint32_t)C * DP * 4 : 0u);
     float fb = 0.0f, fga = 1.0f;  // beta and the GDN decay of token tid of the fetched group
-    auto fetch = [&](int it, int tb) {
+    auto fetch = [&](int it, int tb, int nn) {  // nn: the sequence's token count
         const int bb = it / Hv, hh = it - bb * Hv, gg = hh / (Hv / Hk);
-        const int nn = P.n_tokens ? P.n_tokens[bb] : L;
         const int ntt = min(C, nn - tb);
         if (tid == 0) {
             const int row = bb * L + tb;
@@ -273,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int first = next_work(blockIdx.x);
         if (first < items) {
             load_state(first);
-            fetch(first, 0);
+            fetch(first, 0, P.n_tokens ? P.n_tokens[first / Hv] : L);
         }
     }
     // slot and token count of the current tile, read one tile ahead
@@ -303,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the next tile this CTA processes (its state and first vectors come in during this
         // tile's last group)
         const bool nx_ok = c_slot >= 0 && (int64_t)c_slot < P.n_slots && c_n >= 1 && c_n <= L;
-        int nxt = items;
+        int nxt = items, nxt_n = 0;
 
         for (int t0 = 0; t0 < n && !failed; t0 += C) {
             const int nt = min(C, n - t0);
@@ -338,33 +337,46 @@ __global__ void __launch_bounds__(kThreads, 1)
             // takes key channels 64 hf .. 64 hf + 63 of column v, from the staged copy (a tile's
             // first group) or from the state columns times the previous group's pending decay
 #pragma unroll
-            for (int u0 = 0; u0 < 64; u0 += 16) {
+            for (int u0 = 0; u0 < 64; u0 += 32) {
                 const int ub = 64 * hf + u0;
-                float x[16], lo[16];
+                float x[16], x2[16], lo[16];
                 if (t0 == 0) {
                     const float *st = reinterpret_cast<const float *>(smem + oB1h);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) x[j] = st[(ub + j) * D + v];
+                    for (int j = 0; j < 16; ++j) {
+                        x[j] = st[(ub + j) * D + v];
+                        x2[j] = st[(ub + 16 + j) * D + v];
+                    }
                 } else {
                     tc::ld16(tm + cS + ub, x);
+                    tc::ld16(tm + cS + ub + 16, x2);
                     tc::wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) x[j] = __fmul_rn(x[j], gC[ub + j]);
+                    for (int j = 0; j < 16; ++j) {
+                        x[j] = __fmul_rn(x[j], gC[ub + j]);
+                        x2[j] = __fmul_rn(x2[j], gC[ub + 16 + j]);
+                    }
                 }
 #pragma unroll
                 for (int j = 0; j < 16; ++j) lo[j] = x[j] - tc::tf32_hi(x[j]);
                 tc::st16(tm + cS + ub, x);
                 tc::st16(tm + cSl + ub, lo);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) lo[j] = x2[j] - tc::tf32_hi(x2[j]);
+                tc::st16(tm + cS + ub + 16, x2);
+                tc::st16(tm + cSl + ub + 16, lo);
             }
             tc::wait_st();
             tc::fence_before_sync();
             // ---- cumulative decays Gamma_t[c] of channel c = v; the factored form if none is tiny
+            // (thread (c, 0) needs tokens 0..15 of the fast form, thread (c, 1) all of them)
             const int c = v;
             float gam[C];
             {
                 float pg = 1.0f;
 #pragma unroll
                 for (int t = 0; t < C; ++t) {
+                    if (hf == 0 && t >= C / 2) break;
                     const float a = KDA ? (t < nt ? aS[t * DP + c] : 1.0f) : alpS[t];
                     pg = __fmul_rn(pg, a);
                     gam[t] = pg;
@@ -372,13 +384,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // (also: every thread's state columns are written and the staged state and the
             // pending decays are read)
-            const bool fast = __syncthreads_and(gam[C - 1] >= kFastMin);
+            const bool fast = __syncthreads_and(hf == 0 || gam[C - 1] >= kFastMin);
             if (fast) {
-                if (hf == 0) {
 #pragma unroll
-                    for (int t = 0; t < C; ++t) aS[t * DP + c] = gam[t];
-                    gC[c] = gam[C - 1];
-                }
+                for (int j = 0; j < C / 2; ++j) aS[((C / 2) * hf + j) * DP + c] = hf ? gam[C / 2 + j] : gam[j];
+                if (hf == 1) gC[c] = gam[C - 1];
                 __syncthreads();
                 // thread (t = tid % C, channels 16 (tid / C) .. + 15): the Khat and Qhat operands
                 // and Kchk (fp32 rows now, its operand once every k and q row has been read),
@@ -404,6 +414,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     *reinterpret_cast<float4 *>(aS + t * DP + cb) = kc;
                 }
             } else if (hf == 0) {  // tiny decays: Khat rows of channel c; alpha of the pads 1
+                float pg = gam[C / 2 - 1];
+#pragma unroll
+                for (int t = C / 2; t < C; ++t) {
+                    pg = __fmul_rn(pg, KDA ? (t < nt ? aS[t * DP + c] : 1.0f) : alpS[t]);
+                    gam[t] = pg;
+                }
 #pragma unroll
                 for (int t = 0; t < C; ++t) {
                     put_split(smem + oB1h, smem + oB1l, tc::kmajor_offset(t, c, D), __fmul_rn(kv(t, c), gam[t]));
@@ -553,16 +569,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                // (column j = tid / 8, r = tid % 8) holds T[r + 8 m][j], m = 0..3, and takes
                // T[i][j] from its owner by shuffle once row i is final
                 const int j = tid >> 3, r = tid & 7;
-                float x[4];
+                float x[4], lc[4], ln[4];  // L[r + 8 m][i] of this step and the next
 #pragma unroll
-                for (int m = 0; m < 4; ++m) x[m] = (r + 8 * m == j) ? 1.0f : 0.0f;
+                for (int m = 0; m < 4; ++m) {
+                    x[m] = (r + 8 * m == j) ? 1.0f : 0.0f;
+                    lc[m] = mA[(r + 8 * m) * CA];
+                }
 #pragma unroll
                 for (int i = 0; i < C - 1; ++i) {
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) ln[m] = i + 1 < C - 1 ? mA[(r + 8 * m) * CA + i + 1] : 0.0f;
                     const float xi = __shfl_sync(0xffffffffu, x[i >> 3], (tid & 24) | (i & 7));
 #pragma unroll
                     for (int m = 0; m < 4; ++m) {
                         const int t = r + 8 * m;
-                        if (t > i) x[m] = __fmaf_rn(-mA[t * CA + i], xi, x[m]);
+                        if (t > i) x[m] = __fmaf_rn(-lc[m], xi, x[m]);
+                        lc[m] = ln[m];
                     }
                 }
 #pragma unroll
@@ -579,6 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::fence_after_sync();
             if (last) {  // the next tile's state into the operand buffers, free from here on
                 nxt = nx_ok ? nxi : next_work(nxi);
+                nxt_n = nxt >= items ? 0 : nxt == nxi ? c_n : (P.n_tokens ? P.n_tokens[nxt / Hv] : L);
                 if (nxt < items) load_state(nxt);
             }
             if (!fast) {  // running products: MMA 4 adds Ktil^T W to Gamma_C S0^T, scaled now
@@ -617,9 +640,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!fast && hf == 0) gC[v] = 1.0f;  // nothing pending
             // ---- the next group's (or tile's) vectors come in now
             if (!last) {
-                fetch(item, t0 + C);
+                fetch(item, t0 + C, n);
             } else if (nxt < items) {
-                fetch(nxt, 0);
+                fetch(nxt, 0, nxt_n);
             }
             fence_proxy_async_smem();
             tc::fence_before_sync();
@@ -682,11 +705,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::commit(&bars[6]);
             }
             pendm |= 1u << 2 | 1u << 6;
-            if (!wait_bar(2, ph) || !wait_bar(6, ph)) {
+            if (!wait_bar(2, ph)) {
                 failed = true;
                 break;
             }
-            pendm &= ~(1u << 2 | 1u << 6);
+            pendm &= ~(1u << 2);
             tc::fence_after_sync();
             if (o_g) {  // O^T = Oq^T (two parts) + W^T Bm^T (two parts)
                 float oa[16], ob[16], oc[16], od[16];
@@ -702,6 +725,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (t < nt) store_from_f32<TO>(o_g + (((size_t)b * L + t0 + t) * Hv + h) * D + v, o);
                 }
             }
+            if (!wait_bar(6, ph)) {  // MMA 4: the state columns are current
+                failed = true;
+                break;
+            }
+            pendm &= ~(1u << 6);
+            tc::fence_after_sync();
             ph ^= 1u;
         }
         if (failed) break;
@@ -711,12 +740,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         {
             float *stg = reinterpret_cast<float *>(smem + oKTh);
 #pragma unroll
-            for (int u0 = 0; u0 < 64; u0 += 16) {
-                float y[16];
-                tc::ld16(tm + cS + 64 * hf + u0, y);
+            for (int u0 = 0; u0 < 64; u0 += 32) {
+                const int ub = 64 * hf + u0;
+                float y[16], y2[16];
+                tc::ld16(tm + cS + ub, y);
+                tc::ld16(tm + cS + ub + 16, y2);
                 tc::wait_ld();
 #pragma unroll
-                for (int j = 0; j < 16; ++j) stg[(64 * hf + u0 + j) * D + v] = __fmul_rn(y[j], gC[64 * hf + u0 + j]);
+                for (int j = 0; j < 16; ++j) {
+                    stg[(ub + j) * D + v] = __fmul_rn(y[j], gC[ub + j]);
+                    stg[(ub + 16 + j) * D + v] = __fmul_rn(y2[j], gC[ub + 16 + j]);
+                }
             }
             fence_proxy_async_smem();
             __syncthreads();
