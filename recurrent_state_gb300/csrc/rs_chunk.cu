@@ -350,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
                     tc::ld16(tm + cS + ub, x);
                     tc::ld16(tm + cS + ub + 16, x2);
-                    tc::wait_ld();
+                    tc::wait_ld_regs(x, x2);
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         x[j] = __fmul_rn(x[j], gC[ub + j]);
@@ -500,8 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pendm &= ~(1u << 5);
                 tc::fence_after_sync();
                 float g[16];
-                tc::ld16(tm + cG + (C / 2) * hf, g);
-                tc::wait_ld();
+                tc::ld16_wait(tm + cG + (C / 2) * hf, g);
                 float *G2 = reinterpret_cast<float *>(smem + oA2h);  // [64][CA]
                 if (v >= 2 * C) {
 #pragma unroll
@@ -609,8 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int u0 = 0; u0 < 64; u0 += 16) {
                     const int ub = 64 * hf + u0;
                     float x[16];
-                    tc::ld16(tm + cS + ub, x);
-                    tc::wait_ld();
+                    tc::ld16_wait(tm + cS + ub, x);
 #pragma unroll
                     for (int j = 0; j < 16; ++j) x[j] = __fmul_rn(x[j], gC[ub + j]);
                     tc::st16(tm + cS + ub, x);
@@ -628,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int t = (C / 2) * hf + j;
                     vt[j] = t < nt ? load_as_f32<TI>(reinterpret_cast<const TI *>(rawV + t * RP) + v) : 0.0f;
                 }
-                tc::wait_ld();
+                tc::wait_ld_regs(pa, pb);
 #pragma unroll
                 for (int j = 0; j < C / 2; ++j) vt[j] = __fmul_rn(betaS[(C / 2) * hf + j], __fsub_rn(vt[j], __fadd_rn(pa[j], pb[j])));
 #pragma unroll
@@ -669,7 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float wa[16], wb[16];
                 tc::ld16(tm + cW + (C / 2) * hf, wa);
                 tc::ld16(tm + cW + C + (C / 2) * hf, wb);
-                tc::wait_ld();
+                tc::wait_ld_regs(wa, wb);
 #pragma unroll
                 for (int j = 0; j < C / 2; ++j) wa[j] = __fadd_rn(wa[j], wb[j]);
 #pragma unroll
@@ -717,7 +715,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::ld16(tm + cD1 + 3 * C + (C / 2) * hf, ob);
                 tc::ld16(tm + cW + (C / 2) * hf, oc);
                 tc::ld16(tm + cW + C + (C / 2) * hf, od);
-                tc::wait_ld();
+                tc::wait_ld_regs(oa, ob);
+                tc::wait_ld_regs(oc, od);
 #pragma unroll
                 for (int j = 0; j < C / 2; ++j) {
                     const int t = (C / 2) * hf + j;
@@ -745,7 +744,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float y[16], y2[16];
                 tc::ld16(tm + cS + ub, y);
                 tc::ld16(tm + cS + ub + 16, y2);
-                tc::wait_ld();
+                tc::wait_ld_regs(y, y2);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     stg[(ub + j) * D + v] = __fmul_rn(y[j], gC[ub + j]);

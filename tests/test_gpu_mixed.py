@@ -169,6 +169,69 @@ def test_replay_full_size_sampled():
     assert same_bits(host(pool)[w.slot_idx[bsel]], ref)
 
 
+def test_replay_fp32_full_size_sampled():
+    """KDA FP32, batch 256 x 32 heads, n_accept uniform over 1..8: several tiles per CTA."""
+    B, H, T = 256, 32, 8
+    f32, mix, pi = layouts(H, H, seed=5)
+    w = gen.decode_workload(B=B, Hk=H, Hv=H, d=D, steps=T, per_channel=True, in_dtype="bf16",
+                            seed=5, horizon=(2.0, 8192.0))
+    n_acc = gen.n_accept(B, T, seed=5)
+    pool = dev(w.state0)
+    qd, kd, vd, ad, bd = replay_inputs(w, T)
+    o = torch.zeros((B, T, H, D), device="cuda")
+    rs.spec_replay_update(f32, True, pool, dev(w.slot_idx), dev(n_acc), qd, kd, vd, ad, bd, o=o)
+    torch.cuda.synchronize()
+    bsel = np.array([0, 100, 255])
+    ws = sub_batch(w, bsel)
+    q, k, v, a, b = gen.replay_view(ws, T)
+    ref = ws.state0.copy()
+    o_r = np.zeros((len(bsel), T, H, D), np.float32)
+    orc.replay_f32(ref, ws.slot_idx, np.ascontiguousarray(n_acc[bsel]), q, k, v, a, b, o=o_r)
+    assert same_bits(host(o)[bsel], o_r)
+    assert same_bits(host(pool)[w.slot_idx[bsel]], ref)
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_replay_nonfinite_state(fused):
+    """Replay on tiles holding a NaN in an FP16 row and an infinite INT8 row scale: the
+    requantisation takes the literal-division path for those tiles.  INT8 codes and scales
+    match every byte; FP16 rows and o match up to NaN payloads."""
+    B, Hv, T = 4, 4, 4
+    hi = gen.hi_rows(Hv, D, KHI, seed=10)
+    pi = orc.row_map(hi, D)
+    lay = rs.Layout("mixed", D, Hv, Hv, k_hi=KHI, hi_rows=hi, quant="fused" if fused else "ieee")
+    w = gen.decode_workload(B=B, Hk=Hv, Hv=Hv, d=D, steps=T, per_channel=True, in_dtype="bf16", seed=10)
+    n_acc = np.array([T, 2, 3, 1], np.int32)
+    ref = orc.convert_pool_f32_to_mixed(w.state0, KHI, pi)
+    s0, s1 = w.slot_idx[0], w.slot_idx[1]
+    r, c = 3, 10
+    off = 2 * (((r // 2) * D + c) * 2 + r % 2)
+    ref[s0, 1, off:off + 2] = np.array([0x7E00], np.uint16).view(np.uint8)
+    sc = 2 * KHI * D + (D - KHI) * D + 4 * 5
+    ref[s1, 0, sc:sc + 4] = np.array([np.inf], np.float32).view(np.uint8)
+    pool = dev(ref)
+    qd, kd, vd, ad, bd = replay_inputs(w, T)
+    q, k, v, a, b = gen.replay_view(w, T)
+    o = torch.full((B, T, Hv, D), 5.0, device="cuda")
+    rs.spec_replay_update(lay, True, pool, dev(w.slot_idx), dev(n_acc), qd, kd, vd, ad, bd, o=o)
+    o_r = np.full((B, T, Hv, D), 5.0, np.float32)
+    _, st = orc.replay_mixed(ref, w.slot_idx, n_acc, pi, KHI, D, D, q, k, v, a, b, o=o_r,
+                             mode=1 if fused else 0)
+    torch.cuda.synchronize()
+    assert st == 0
+    assert np.isnan(o_r).any()
+    assert nan_aware_same(host(o), o_r)
+    g = host(pool)
+    hb = 2 * KHI * D
+    assert same_bits(g[..., hb:], ref[..., hb:])
+    hg = g[..., :hb].copy().view(np.float16)
+    hr = ref[..., :hb].copy().view(np.float16)
+    nan = np.isnan(hr)
+    assert nan.sum() >= KHI
+    assert np.array_equal(np.isnan(hg), nan)
+    assert np.array_equal(hg.view(np.uint16)[~nan], hr.view(np.uint16)[~nan])
+
+
 def test_replay_bad_accept_count_reported():
     Hv, Hk, T = 4, 2, 4
     f32, mix, pi = layouts(Hv, Hk, seed=1)
