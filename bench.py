@@ -726,6 +726,21 @@ def extra_kernels(args, rs, torch, dev, peak, world, only=None):
                 2 * B * Hv * f32.head_bytes + int(B * Lc * per_tok), B * Hv * Lc,
                 {"chunk_tokens": Lc, "form": "chunk-parallel, tcgen05 kind::tf32 (3 products per pair)"},
                 tile_tokens=B * Hv * Lc)
+            if kda and Lc == 32:  # the same on the mixed FP16/INT8 state, fused arithmetic, rotated pools
+                hi = gen.hi_rows(Hv, 128, 16, seed=4)
+                mixf = rs.Layout("mixed", 128, Hv, Hk, k_hi=16, hi_rows=hi, quant="fused")
+                mpool = mixf.empty_pool(w.state0.shape[0], device=dev)
+                rs.state_convert(f32, pool, mixf, mpool,
+                                 torch.arange(w.state0.shape[0], dtype=torch.int32, device=dev))
+                ppools = rotation(torch, mpool, dev)
+                sec = _time(torch, lambda i: rs.prefill_update(mixf, kda, ppools[i % len(ppools)], slots, pq, pk,
+                                                               pv, pa, pb, o=po, chunked=True),
+                            max(3, iters // 10), warm)
+                rec(f"kda_prefill_chunked_mixed_fused_b{B}_L{Lc}", sec,
+                    2 * B * Hv * mixf.head_bytes + int(B * Lc * per_tok), B * Hv * Lc,
+                    {"chunk_tokens": Lc, "quant": "fused", "form": "chunk-parallel, tcgen05 kind::tf32",
+                     **rot_info(ppools)}, tile_tokens=B * Hv * Lc)
+                del mpool, ppools
             del pool, pq, pk, pv, pa, pb, po
             torch.cuda.empty_cache()
 

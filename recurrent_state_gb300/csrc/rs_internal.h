@@ -96,8 +96,9 @@ struct PrefillParams {
     uint8_t pi[kMaxRowMap];    // mixed layout: physical row -> key channel
 };
 cudaError_t launch_prefill(const StepLaunch &L, PrefillParams &P, cudaStream_t s);
-// rs_chunk.cu: the chunk-parallel form on the tensor cores (FP32 layout)
+// rs_chunk.cu / rs_chunk_mixed.cu: the chunk-parallel form on the tensor cores (FP32 and mixed layouts)
 cudaError_t launch_prefill_chunked(const StepLaunch &L, PrefillParams &P, cudaStream_t s);
+cudaError_t launch_prefill_chunked_mixed(const StepLaunch &L, PrefillParams &P, cudaStream_t s);
 
 // rs_convert.cu
 struct ConvertParams {

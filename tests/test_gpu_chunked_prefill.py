@@ -11,7 +11,12 @@ and every output row within 1e-5 of the oracle's, normwise
 steps.  Cases: GDN and KDA, grouped key heads, ragged token counts (0, 1, 32,
 33, L and between) over two 32-token groups with a partial last one, bf16
 and fp32 inputs, strong decays, and the full batch-256 workload with 32 and
-64 tokens on sampled sequences.
+64 tokens on sampled sequences.  On the mixed FP16/INT8 layout the oracle is its
+sequential mixed prefill from the same packed bytes (dequantise once, FP32
+steps, requantise once): outputs within the same tolerance, INT8 codes at
+most one step apart (and rarely), row scales within the state tolerance over
+127, and the dequantised state within the tolerance of the tile norm plus one
+quantisation step of the FP32 state the oracle requantises.
 """
 import numpy as np
 import pytest
@@ -128,6 +133,111 @@ def test_chunked_prefill_gdn_full_size_sampled():
     check_against_oracle(w, n_tok, inputs, pool_g, o_g, bsel=np.array([1, 128, 254]))
 
 
+KHI = 16
+
+
+def mixed_case(B, Hk, Hv, L, per_channel, seed, quant, n_tok=None, in_dtype="bf16"):
+    """Chunked prefill on the mixed FP16/INT8 layout from packed tiles the oracle wrote; returns
+    the GPU's packed pool and outputs beside the oracle's sequential mixed prefill from the same
+    bytes and the FP32 state it requantises."""
+    w = gen.decode_workload(B=B, Hk=Hk, Hv=Hv, d=D, steps=L, per_channel=per_channel, in_dtype=in_dtype,
+                            seed=seed, horizon=(2.0, 8192.0) if per_channel else (4.0, 4096.0))
+    if n_tok is None:
+        n_tok = np.full(B, L, np.int32)
+    hi = gen.hi_rows(Hv, D, KHI, seed=seed)
+    pi = orc.row_map(hi, D)
+    mode = 1 if quant == "fused" else 0
+    lay = rs.Layout("mixed", D, Hv, Hk, k_hi=KHI, hi_rows=hi, quant=quant)
+    packed0 = orc.convert_pool_f32_to_mixed(w.state0, KHI, pi, mode=mode)
+    qd, kd, vd, ad, bd = replay_inputs(w, L)
+    q, k, v, a, b = gen.replay_view(w, L)
+    pool = dev(packed0)
+    o = torch.full((B, L, Hv, D), 3.0, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rs.prefill_update(lay, per_channel, pool, dev(w.slot_idx), qd, kd, vd, ad, bd, n_tokens=dev(n_tok),
+                      o=o, status=status, chunked=True)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return w, n_tok, pi, mode, packed0, (q, k, v, a, b), host(pool), host(o)
+
+
+def check_mixed(w, n_tok, pi, mode, packed0, inputs, pool_g, o_g, bsel=None):
+    q, k, v, a, b = inputs
+    if bsel is None:
+        bsel = np.arange(w.B)
+    ws = sub_batch(w, bsel)
+    pick = lambda x: np.ascontiguousarray(x[bsel])
+    L = q.shape[1]
+    n_sel = np.ascontiguousarray(n_tok[bsel])
+    sel = w.slot_idx[bsel]                       # the sampled sequences' tiles, renumbered 0..
+    slots = ws.slot_idx
+    p0 = np.ascontiguousarray(packed0[sel])
+    # the oracle: sequential mixed prefill (dequantise once, FP32 steps, requantise once) ...
+    ref = p0.copy()
+    o_r = np.full((len(bsel), L, w.Hv, D), 3.0, np.float32)
+    _, st = orc.replay_mixed(ref, slots, n_sel, pi, KHI, D, D, pick(q), pick(k), pick(v), pick(a), pick(b),
+                             o=o_r, mode=mode)
+    assert st == 0
+    # ... and the FP32 state it requantises
+    s32 = orc.convert_pool_mixed_to_f32(p0, D, D, KHI, pi)
+    _, st = orc.replay_f32(s32, slots, n_sel, pick(q), pick(k), pick(v), pick(a), pick(b))
+    assert st == 0
+    worst = 0.0
+    for i, bb in enumerate(bsel):
+        n = int(n_tok[bb])
+        if n:
+            worst = max(worst, tile_rel(np.swapaxes(o_g[bb, :n], 0, 1), np.swapaxes(o_r[i, :n], 0, 1)))
+        assert np.all(o_g[bb, n:] == 3.0), "rows past n_tokens must stay untouched"
+    assert worst <= TOL, f"o {worst:.3g}"
+    g = pool_g[sel]
+    r = ref
+    S = s32.astype(np.float64)                                      # [n][Hv][u][v], key-channel order
+    norm = np.max(np.abs(S), axis=(-2, -1))                          # per tile
+    hb, lb = 2 * KHI * D, (D - KHI) * D
+    # INT8 codes: one step apart at most, and rarely
+    cg = g[..., hb:hb + lb].view(np.int8).astype(np.int32)
+    cr = r[..., hb:hb + lb].view(np.int8).astype(np.int32)
+    diff = np.abs(cg - cr)
+    assert diff.max() <= 1
+    frac = float(np.mean(diff != 0))
+    assert frac <= 5e-3, frac
+    # row scales: within the state's tolerance (absmax / 127) and a few ulps
+    sg = g[..., hb + lb:].copy().view(np.float32).astype(np.float64)  # [n][Hv][D - KHI]
+    sr = r[..., hb + lb:].copy().view(np.float32).astype(np.float64)
+    assert np.all(np.abs(sg - sr) <= TOL * norm[..., None] / 127.0 + 4 * np.spacing(sr.astype(np.float32)))
+    # dequantised states: within the tolerance of the tile norm plus one quantisation step
+    dg = orc.convert_pool_mixed_to_f32(np.ascontiguousarray(g), D, D, KHI, pi).astype(np.float64)
+    step = np.zeros_like(S)
+    rows = np.asarray(pi).reshape(w.Hv, D)                           # physical row -> key channel
+    for hh in range(w.Hv):
+        for rr in range(KHI, D):
+            step[:, hh, rows[hh, rr], :] = np.maximum(sg[:, hh, rr - KHI], sr[:, hh, rr - KHI])[:, None]
+        for rr in range(KHI):
+            step[:, hh, rows[hh, rr], :] = np.abs(S[:, hh, rows[hh, rr], :]) * 2.0 ** -10 + 2.0 ** -24
+    err = np.abs(dg - S) - step
+    assert np.all(err <= TOL * norm[..., None, None]), float(np.max(err / norm[..., None, None]))
+    return worst, frac
+
+
+@pytest.mark.parametrize("quant", ["ieee", "fused"])
+@pytest.mark.parametrize("per_channel,Hk,Hv", [(True, 4, 4), (False, 2, 4)])
+def test_chunked_prefill_mixed_ragged(quant, per_channel, Hk, Hv):
+    B, L = 9, 37
+    n_tok = gen.rng(5).integers(0, L + 1, B).astype(np.int32)
+    n_tok[0], n_tok[1], n_tok[2], n_tok[3] = 0, L, 1, 32
+    res = mixed_case(B, Hk, Hv, L, per_channel, 71, quant, n_tok=n_tok)
+    check_mixed(*res)
+
+
+@pytest.mark.parametrize("quant", ["ieee", "fused"])
+@pytest.mark.parametrize("L", [32, 64])
+def test_chunked_prefill_mixed_full_size_sampled(quant, L):
+    """KDA, batch 256, 32 heads, mixed FP16/INT8 state, sampled sequences (all heads)."""
+    res = mixed_case(256, 32, 32, L, True, 72, quant)
+    o_err, frac = check_mixed(*res, bsel=np.array([2, 130, 255]))
+    print(f"\nchunked prefill, mixed {quant}, L={L}: o {o_err:.3g}, codes off by one {frac:.2g}")
+
+
 def test_chunked_prefill_guards_and_layouts():
     B, Hk, Hv, L = 4, 2, 2, 5
     w = gen.decode_workload(B=B, Hk=Hk, Hv=Hv, d=D, steps=L, per_channel=True, in_dtype="bf16", seed=65)
@@ -147,7 +257,7 @@ def test_chunked_prefill_guards_and_layouts():
         if slots[bb] < w.state0.shape[0]:
             assert np.array_equal(got[slots[bb]], w.state0[slots[bb]])
     hi = gen.hi_rows(Hv, D, 16, seed=1)
-    mix = rs.Layout("mixed", D, Hv, Hk, k_hi=16, hi_rows=hi)
+    damp = rs.Layout("damp", D, Hv, Hk, k_hi=16, hi_rows=hi)  # DAMP-exact tiles: the sequential form only
     with pytest.raises(rs.RsError) as e:
-        rs.prefill_update(mix, True, mix.empty_pool(B), dev(w.slot_idx), qd, kd, vd, ad, bd, chunked=True)
+        rs.prefill_update(damp, True, damp.empty_pool(B), dev(w.slot_idx), qd, kd, vd, ad, bd, chunked=True)
     assert e.value.status == _abi.RS_ERR_UNSUPPORTED
