@@ -291,15 +291,21 @@ rs_status rs_prefill_update(const rs_layout *l, int32_t per_channel_decay, void 
  * arguments, layouts and status bits as rs_prefill_update, and the same map
  * ([DAMP] Appendix A.4 "Prefill path"; [SRA] "Kernels follow the serving
  * phase": prefill exposes parallel work across a chunk's tokens): the tokens
- * are taken 16 at a time, and each group is applied as dense products on
+ * are taken 32 at a time, and each group is applied as dense products on
  * the tensor cores (the written rows W solve (I + diag(beta) A) W =
  * diag(beta)(V - Khat S0), with A the decay-weighted key Gram matrix; the
  * outputs and the new state follow from W).  The products use tf32 operands
  * split into a high part and an exact remainder, with fp32 accumulation, so
  * the result equals the token-by-token recurrence up to rounding (about
- * 1e-6 relative), not bit for bit.  Built for the FP32 layout with
- * dk = dv = 128; other layouts return RS_ERR_UNSUPPORTED before any launch.
- * Use rs_prefill_update where bit-exactness with single decode steps is
+ * 1e-6 relative), not bit for bit.  A mixed tile is dequantised once when
+ * its chunk starts and requantised once at its end (its layout's
+ * arithmetic), so its INT8 codes can differ by one from those of
+ * rs_prefill_update where the FP32 state sits that close to a rounding
+ * boundary.  Built for dk = dv = 128 on the FP32 layout and on the mixed
+ * layout with k_hi = 16 and one scale per row; other layouts (DAMP-exact
+ * groups among them) return RS_ERR_UNSUPPORTED before any launch, as do
+ * in_dtype RS_F16 on the mixed layout and B * L >= 2^31 - 32.  Use
+ * rs_prefill_update where bit-exactness with single decode steps is
  * needed. */
 rs_status rs_prefill_chunked_update(const rs_layout *l, int32_t per_channel_decay, void *pool,
                                     int64_t n_slots, const int32_t *slot_idx, int32_t B,
