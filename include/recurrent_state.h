@@ -389,10 +389,10 @@ rs_status rs_ckpt_restore(const rs_plan *p, const void *ckpt_pool, int64_t n_ckp
  *     touched;
  *   - the array (1 MiB) lives on every GPU that loads the library until the
  *     process exits;
- *   - the first call on a device looks up the array's device address; make
- *     that first call before any stream capture begins.  The address is kept
- *     for the process: do not use this call on a device after
- *     cudaDeviceReset.  Devices 0..63 only;
+ *   - the first call on a device looks up the array's device address (a
+ *     host-side runtime query).  The address is kept for the process: do
+ *     not use this call on a device after cudaDeviceReset.  Devices 0..63
+ *     only;
  *   - all calls share the one array, which keeps the last call's table:
  *     calls whose work overlaps on the GPU (on different streams) race and
  *     must be ordered by the caller;

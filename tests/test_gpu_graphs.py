@@ -85,12 +85,12 @@ def test_decode_steps_in_a_graph(kind):
         assert same_bits(host(x), host(y))
 
 
-@pytest.mark.parametrize("path", ["replay", "prefill"])
+@pytest.mark.parametrize("path", ["replay", "prefill", "prefill_chunked", "prefill_chunked_fp32"])
 def test_multi_token_calls_in_a_graph(path):
     B, Hk, Hv, T = 13, 2, 4, 8
     w = gen.decode_workload(B=B, Hk=Hk, Hv=Hv, d=D, steps=T, per_channel=False, in_dtype="bf16", seed=81)
     f32, mix = layouts(Hv, Hk, 81)
-    base = packed(f32, mix, w.state0)
+    base = dev(w.state0) if path == "prefill_chunked_fp32" else packed(f32, mix, w.state0)
     qd, kd, vd, ad, bd = replay_inputs(w, T)
     n = dev(gen.n_accept(B, T, seed=81))
     slots = dev(w.slot_idx)
@@ -101,8 +101,11 @@ def test_multi_token_calls_in_a_graph(path):
     def calls(pool, outs):
         if path == "replay":
             rs.spec_replay_update(mix, False, pool, slots, n, qd, kd, vd, ad, bd, o=outs[0])
-        else:
+        elif path == "prefill":
             rs.prefill_update(mix, False, pool, slots, qd, kd, vd, ad, bd, n_tokens=n, o=outs[0])
+        else:  # the chunk-parallel form: tensor maps encoded on the host at each call, passed by value
+            rs.prefill_update(f32 if path == "prefill_chunked_fp32" else mix, False, pool, slots, qd, kd, vd, ad,
+                              bd, n_tokens=n, o=outs[0], chunked=True)
 
     (sd, od), (sg, og) = run_twice(calls, make_state)
     assert same_bits(host(sd), host(sg))
