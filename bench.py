@@ -741,6 +741,21 @@ def extra_kernels(args, rs, torch, dev, peak, world, only=None):
                     {"chunk_tokens": Lc, "quant": "fused", "form": "chunk-parallel, tcgen05 kind::tf32",
                      **rot_info(ppools)}, tile_tokens=B * Hv * Lc)
                 del mpool, ppools
+                # and on DAMP-exact tiles (INT8 groups of 32, value scaling)
+                cs = gen.value_scales(Hv, 128, seed=4)
+                dmp = rs.Layout("damp", 128, Hv, Hk, k_hi=16, hi_rows=hi, value_scales=cs, quant="fused")
+                dpool = dmp.empty_pool(w.state0.shape[0], device=dev)
+                rs.state_convert(f32, pool, dmp, dpool,
+                                 torch.arange(w.state0.shape[0], dtype=torch.int32, device=dev))
+                dpools = rotation(torch, dpool, dev)
+                sec = _time(torch, lambda i: rs.prefill_update(dmp, kda, dpools[i % len(dpools)], slots, pq, pk,
+                                                               pv, pa, pb, o=po, chunked=True),
+                            max(3, iters // 10), warm)
+                rec(f"kda_prefill_chunked_damp_fused_b{B}_L{Lc}", sec,
+                    2 * B * Hv * dmp.head_bytes + int(B * Lc * per_tok), B * Hv * Lc,
+                    {"chunk_tokens": Lc, "quant": "fused", "form": "chunk-parallel, tcgen05 kind::tf32",
+                     **rot_info(dpools)}, tile_tokens=B * Hv * Lc)
+                del dpool, dpools
             del pool, pq, pk, pv, pa, pb, po
             torch.cuda.empty_cache()
 

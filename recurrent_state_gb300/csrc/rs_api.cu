@@ -408,11 +408,19 @@ static rs_status prefill_common(const rs_layout *l, int32_t per_channel_decay, v
         for (size_t i = 0; i < l->pi.size() && i < (size_t)rs::kMaxRowMap; ++i) P.pi[i] = (uint8_t)l->pi[i];
     };
     cudaError_t e;
-    if (chunked) {  // the tensor-core form: FP32 layout, or the mixed one with 16 FP16 rows (not DAMP-exact)
-        if (D != 128 || l->group || (l->p.kind != RS_LAYOUT_FP32 && l->p.k_hi != 16)) return RS_ERR_UNSUPPORTED;
-        static thread_local rs::PrefillParams P;
-        fill(P);
-        e = rs::launch_prefill_chunked(Ln, P, static_cast<cudaStream_t>(stream));
+    if (chunked) {  // the tensor-core form: FP32 layout, or the mixed ones with 16 FP16 rows
+        if (D != 128 || (l->p.kind != RS_LAYOUT_FP32 && l->p.k_hi != 16)) return RS_ERR_UNSUPPORTED;
+        if (l->group) {  // DAMP-exact: groups of 32 and value scaling
+            if (l->group != rs::kDampGroup) return RS_ERR_UNSUPPORTED;
+            static thread_local rs::PrefillParamsDamp P;
+            fill(P);
+            std::copy(l->cs.begin(), l->cs.end(), P.cs);
+            e = rs::launch_prefill_chunked_damp(Ln, P, static_cast<cudaStream_t>(stream));
+        } else {
+            static thread_local rs::PrefillParams P;
+            fill(P);
+            e = rs::launch_prefill_chunked(Ln, P, static_cast<cudaStream_t>(stream));
+        }
     } else if (l->group) {  // DAMP-exact layout: group scales and value-scaling factors
         static thread_local rs::PrefillParamsDamp P;
         fill(P);

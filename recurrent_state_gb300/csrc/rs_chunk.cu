@@ -8,10 +8,10 @@ namespace {
 
 template <bool KDA>
 cudaError_t by_types(const StepLaunch &L, PrefillParams &P, cudaStream_t s) {
-    if (L.in_dt == RS_BF16 && L.out_dt == RS_F32) return run<KDA, false, false, __nv_bfloat16, float>(P, s);
-    if (L.in_dt == RS_BF16 && L.out_dt == RS_BF16) return run<KDA, false, false, __nv_bfloat16, __nv_bfloat16>(P, s);
-    if (L.in_dt == RS_F32 && L.out_dt == RS_F32) return run<KDA, false, false, float, float>(P, s);
-    if (L.in_dt == RS_F16 && L.out_dt == RS_F32) return run<KDA, false, false, __half, float>(P, s);
+    if (L.in_dt == RS_BF16 && L.out_dt == RS_F32) return run<KDA, false, false, false, __nv_bfloat16, float>(P, s);
+    if (L.in_dt == RS_BF16 && L.out_dt == RS_BF16) return run<KDA, false, false, false, __nv_bfloat16, __nv_bfloat16>(P, s);
+    if (L.in_dt == RS_F32 && L.out_dt == RS_F32) return run<KDA, false, false, false, float, float>(P, s);
+    if (L.in_dt == RS_F16 && L.out_dt == RS_F32) return run<KDA, false, false, false, __half, float>(P, s);
     return cudaErrorNotSupported;
 }
 

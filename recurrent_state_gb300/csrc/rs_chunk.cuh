@@ -57,6 +57,7 @@
 #include <type_traits>
 
 #include "rs_internal.h"
+#include "rs_damp.h"
 #include "rs_device.cuh"
 #include "rs_step.cuh"  // the mixed layout's quantiser (quant_quad*) and its constants
 #include "rs_tc.cuh"
@@ -102,11 +103,16 @@ static_assert(oKCl + C * D * 4 <= oAl, "Kchk operand fits the k and q rows");
 constexpr int oV = (oTslot + 16 + 127) / 128 * 128;  // the group's v rows
 // mixed layout: key channel -> physical row of the tile's head, and the requantisation's row
 // scales, their negations and reciprocals (by physical row), and the non-finite flag
-constexpr int oPinv = oV + kTok, oQs = oPinv + D, oQns = oQs + D * 4, oQrc = oQns + D * 4, oQflag = oQrc + D * 4;
-constexpr int kSmem = oQflag + 16;
+// (DAMP-exact tiles: one scale per group of 32 columns, [group][row]; and the value-scaling factors)
+constexpr int NGM = D / kDampGroup;
+constexpr int oPinv = oV + kTok, oQs = oPinv + D, oQns = oQs + NGM * D * 4, oQrc = oQns + NGM * D * 4,
+              oQflag = oQrc + NGM * D * 4, oCs = oQflag + 16;
+constexpr int kSmem = oCs + D * 4;
 constexpr int KHM = 16;  // FP16 rows of the mixed layout the chunked form takes
 constexpr int kMixBytes = 2 * KHM * D + (D - KHM) * D + 4 * (D - KHM);  // 18,880 B
-static_assert(kMixBytes % 16 == 0 && kMixBytes <= 2 * kB1, "a packed tile fits the staging buffers");
+constexpr int kDampBytes = 2 * KHM * D + (D - KHM) * D + 4 * (D - KHM) * NGM;  // 20,224 B
+static_assert(kMixBytes % 16 == 0 && kDampBytes % 16 == 0 && kDampBytes <= 2 * kB1,
+              "a packed tile fits the staging buffers");
 static_assert(kSmem <= 232448, "fits the shared memory of one SM");
 static_assert(oKTh + D * D * 4 == oTh, "the final state fills KT and the R/W operand");
 static_assert(2 * kB1 == D * D * 4, "a tile's incoming state fills the [Khat ; Qhat] operand buffers");
@@ -175,10 +181,13 @@ __device__ __forceinline__ float4 mul4(float4 a, float4 b) {
 }
 
 // MIX: the pool holds mixed FP16/INT8 tiles (16 FP16 rows, one INT8 scale per row, row map pi);
+// GRP: DAMP-exact ones (INT8 scales per group of 32 columns, value scaling c': the state is
+// T = S diag(c')^{-1}, the values v' = v / c' and the outputs c' o'; PT carries c');
 // FUSED: their requantisation arithmetic is the fused one
-template <bool KDA, bool MIX, bool FUSED, typename TI, typename TO>
+template <bool KDA, bool MIX, bool GRP, bool FUSED, typename TI, typename TO, typename PT>
 __global__ void __launch_bounds__(kThreads, 1)
-    chunk_prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ ChunkMaps M) {
+    chunk_prefill_kernel(const __grid_constant__ PT P, const __grid_constant__ ChunkMaps M) {
+    static_assert(MIX || !GRP, "DAMP-exact tiles are mixed tiles");
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, w = tid >> 5;
     const int v = tid & (D - 1);  // value column (and key channel c in the per-channel work)
@@ -222,7 +231,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dKCh = tc::smem_desc(smem + oKCh, 128, D * 32), dKCl = tc::smem_desc(smem + oKCl, 128, D * 32);
 
     const int Hv = P.Hv, Hk = P.Hk, L = P.L;
-    constexpr int kStateBytes = MIX ? kMixBytes : D * D * 4;
+    constexpr int kStateBytes = MIX ? (GRP ? kDampBytes : kMixBytes) : D * D * 4;
+    float *csS = reinterpret_cast<float *>(smem + oCs);  // DAMP-exact: c' of the tile's head
     uint8_t *pool = static_cast<uint8_t *>(P.pool);
     uint8_t *pinv = smem + oPinv;
     const int items = P.B * Hv;
@@ -320,6 +330,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         float *Sg = reinterpret_cast<float *>(tile_g);
         if constexpr (MIX) {  // this head's inverse row map (read at the tile's end)
             if (tid < D) pinv[P.pi[h * D + tid]] = (uint8_t)tid;
+            if constexpr (GRP) {
+                if (tid < D) csS[tid] = P.cs[h * D + tid];
+            }
         }
         // the next tile this CTA processes (its state and first vectors come in during this
         // tile's last group)
@@ -369,7 +382,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         } else {
                             const int qd = j - KHM / 2, r0 = KHM + 4 * qd;
                             const uint32_t wd = lw[qd * D + v];
-                            const float4 s4 = *reinterpret_cast<const float4 *>(sc + 4 * qd);
+                            // the scales of rows r0 .. r0 + 3 (DAMP-exact: of column v's group)
+                            const float4 s4 = GRP ? make_float4(sc[(4 * qd) * NGM + (v >> 5)], sc[(4 * qd + 1) * NGM + (v >> 5)],
+                                                                sc[(4 * qd + 2) * NGM + (v >> 5)], sc[(4 * qd + 3) * NGM + (v >> 5)])
+                                                  : *reinterpret_cast<const float4 *>(sc + 4 * qd);
                             stg[pih[r0] * D + v] = __fmul_rn((float)(int8_t)(wd & 0xffu), s4.x);
                             stg[pih[r0 + 1] * D + v] = __fmul_rn((float)(int8_t)((wd >> 8) & 0xffu), s4.y);
                             stg[pih[r0 + 2] * D + v] = __fmul_rn((float)(int8_t)((wd >> 16) & 0xffu), s4.z);
@@ -680,6 +696,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc::wait_ld_regs(pa, pb);
 #pragma unroll
+                if constexpr (GRP) {  // v' = v / c' (IEEE division)
+#pragma unroll
+                    for (int j = 0; j < C / 2; ++j) vt[j] = __fdiv_rn(vt[j], csS[v]);
+                }
+#pragma unroll
                 for (int j = 0; j < C / 2; ++j) vt[j] = __fmul_rn(betaS[(C / 2) * hf + j], __fsub_rn(vt[j], __fadd_rn(pa[j], pb[j])));
 #pragma unroll
                 for (int j = 0; j < C / 2; j += 4)
@@ -772,7 +793,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int j = 0; j < C / 2; ++j) {
                     const int t = (C / 2) * hf + j;
-                    const float o = __fadd_rn(__fadd_rn(oa[j], ob[j]), __fadd_rn(oc[j], od[j]));
+                    float o = __fadd_rn(__fadd_rn(oa[j], ob[j]), __fadd_rn(oc[j], od[j]));
+                    if constexpr (GRP) o = __fmul_rn(csS[v], o);  // o = c' o'
                     if (t < nt) store_from_f32<TO>(o_g + (((size_t)b * L + t0 + t) * Hv + h) * D + v, o);
                 }
             }
@@ -821,34 +843,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float *qns = reinterpret_cast<float *>(smem + oQns);
                 float *qrc = reinterpret_cast<float *>(smem + oQrc);
                 const int lane = tid & 31;
-                float amax = 0.0f;  // lane i: the absmax of row 16 w + i
+                auto max_nan = [](float a, float b) {
+                    float r;
+                    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+                    return r;
+                };
+                float amax = 0.0f;  // lane i: the absmax of row 16 w + i (one scale per row)
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const int u = 16 * w + i;
                     const float4 x4 = reinterpret_cast<const float4 *>(stg + u * D)[lane];
-                    float m;
-                    asm("{\n\t.reg .f32 t0, t1;\n\t"
-                        "max.NaN.f32 t0, %1, %2;\n\t"
-                        "max.NaN.f32 t1, %3, %4;\n\t"
-                        "max.NaN.f32 %0, t0, t1;\n\t}"
-                        : "=f"(m)
-                        : "f"(fabsf(x4.x)), "f"(fabsf(x4.y)), "f"(fabsf(x4.z)), "f"(fabsf(x4.w)));
-                    const float a = warp_max_abs_nan(m);
-                    amax = lane == i ? a : amax;
-                }
-                {
-                    const int r = lane < 16 ? (int)pinv[16 * w + lane] : 0;
-                    const float a = amax;
-                    if (lane < 16 && r >= KHM) {
-                        const uint32_t ab = __float_as_uint(a);
-                        const float sv = __fdiv_rn(fmaxf(a, 1e-8f), 127.0f);
-                        qs[r] = sv;
-                        qns[r] = -sv;
-                        // fused arithmetic: y = 0 marks a row whose absmax is inf or NaN
-                        qrc[r] = (FUSED && ab >= 0x7f800000u) ? 0.0f : __frcp_rn(sv);
-                        if (ab >= 0x7f800000u) *qflag = 1;  // the exact path for the tile
-                        reinterpret_cast<float *>(tile_g + 2 * KHM * D + (D - KHM) * D)[r - KHM] = sv;
+                    float m = max_nan(max_nan(fabsf(x4.x), fabsf(x4.y)), max_nan(fabsf(x4.z), fabsf(x4.w)));
+                    if constexpr (GRP) {  // the lane's group (lanes 8 g .. 8 g + 7: columns 32 g ..)
+                        m = max_nan(m, __shfl_xor_sync(0xffffffffu, m, 1));
+                        m = max_nan(m, __shfl_xor_sync(0xffffffffu, m, 2));
+                        m = max_nan(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                        const int r = pinv[u];
+                        if ((lane & 7) == 0 && r >= KHM) qs[(lane >> 3) * D + r] = m;
+                    } else {
+                        const float a = warp_max_abs_nan(m);  // every lane takes part in the reduction
+                        amax = lane == i ? a : amax;
                     }
+                }
+                if constexpr (!GRP) {
+                    const int r = lane < 16 ? (int)pinv[16 * w + lane] : 0;
+                    if (lane < 16 && r >= KHM) qs[r] = amax;
+                }
+                __syncthreads();
+                // the scales of every (group, INT8 row) from the maxima
+                constexpr int NGc = GRP ? NGM : 1;
+                for (int pq = tid; pq < NGc * (D - KHM); pq += kThreads) {
+                    const int g = pq / (D - KHM), r = KHM + pq % (D - KHM);
+                    const float a = qs[g * D + r];
+                    const uint32_t ab = __float_as_uint(a);
+                    const float sv = __fdiv_rn(fmaxf(a, 1e-8f), 127.0f);
+                    qs[g * D + r] = sv;
+                    qns[g * D + r] = -sv;
+                    // fused arithmetic: y = 0 marks a row (group) whose absmax is inf or NaN
+                    qrc[g * D + r] = (FUSED && ab >= 0x7f800000u) ? 0.0f : __frcp_rn(sv);
+                    if (ab >= 0x7f800000u) *qflag = 1;  // the exact path for the tile
+                    reinterpret_cast<float *>(tile_g + 2 * KHM * D + (D - KHM) * D)[GRP ? (r - KHM) * NGM + g : r - KHM] = sv;
                 }
                 __syncthreads();
                 const bool exact = *qflag != 0;
@@ -865,13 +899,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int qd = j - KHM / 2, r0 = KHM + 4 * qd;
                         const float2 x01 = make_float2(stg[pih[r0] * D + v], stg[pih[r0 + 1] * D + v]);
                         const float2 x23 = make_float2(stg[pih[r0 + 2] * D + v], stg[pih[r0 + 3] * D + v]);
-                        const float4 rc4 = *reinterpret_cast<const float4 *>(qrc + r0);
+                        const int go = GRP ? (v >> 5) * D : 0;  // column v's scale group
+                        const float4 rc4 = *reinterpret_cast<const float4 *>(qrc + go + r0);
                         uint32_t wd;
                         if (!exact) {
                             if constexpr (FUSED) wd = quant_quad_rcp(x01, x23, rc4);
-                            else wd = quant_quad(x01, x23, *reinterpret_cast<const float4 *>(qns + r0), rc4);
+                            else wd = quant_quad(x01, x23, *reinterpret_cast<const float4 *>(qns + go + r0), rc4);
                         } else {
-                            wd = quant_quad_cold<FUSED>(x01, x23, *reinterpret_cast<const float4 *>(qs + r0), rc4);
+                            wd = quant_quad_cold<FUSED>(x01, x23, *reinterpret_cast<const float4 *>(qs + go + r0), rc4);
                         }
                         lw[qd * D + v] = wd;
                     }
@@ -934,9 +969,9 @@ constexpr CUtensorMapDataType map_type() {
     else return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
 }
 
-template <bool KDA, bool MIX, bool FUSED, typename TI, typename TO>
-cudaError_t run(PrefillParams &P, cudaStream_t s) {
-    auto kern = chunk_prefill_kernel<KDA, MIX, FUSED, TI, TO>;
+template <bool KDA, bool MIX, bool GRP, bool FUSED, typename TI, typename TO, typename PT>
+cudaError_t run(PT &P, cudaStream_t s) {
+    auto kern = chunk_prefill_kernel<KDA, MIX, GRP, FUSED, TI, TO, PT>;
     const int items = P.B * P.Hv;
     const int64_t rows = (int64_t)P.B * P.L;
     if (items < 1 || rows < 1) return cudaSuccess;

@@ -9,9 +9,9 @@ namespace {
 
 template <bool KDA, bool FUSED>
 cudaError_t by_types(const StepLaunch &L, PrefillParams &P, cudaStream_t s) {
-    if (L.in_dt == RS_BF16 && L.out_dt == RS_F32) return run<KDA, true, FUSED, __nv_bfloat16, float>(P, s);
-    if (L.in_dt == RS_BF16 && L.out_dt == RS_BF16) return run<KDA, true, FUSED, __nv_bfloat16, __nv_bfloat16>(P, s);
-    if (L.in_dt == RS_F32 && L.out_dt == RS_F32) return run<KDA, true, FUSED, float, float>(P, s);
+    if (L.in_dt == RS_BF16 && L.out_dt == RS_F32) return run<KDA, true, false, FUSED, __nv_bfloat16, float>(P, s);
+    if (L.in_dt == RS_BF16 && L.out_dt == RS_BF16) return run<KDA, true, false, FUSED, __nv_bfloat16, __nv_bfloat16>(P, s);
+    if (L.in_dt == RS_F32 && L.out_dt == RS_F32) return run<KDA, true, false, FUSED, float, float>(P, s);
     return cudaErrorNotSupported;
 }
 

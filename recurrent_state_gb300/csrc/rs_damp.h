@@ -26,6 +26,8 @@ struct PrefillParamsDamp : PrefillParams {
 
 cudaError_t launch_step_damp_decode(const StepLaunch &L, StepParamsDamp &P, cudaStream_t s);
 cudaError_t launch_prefill_damp(const StepLaunch &L, PrefillParamsDamp &P, cudaStream_t s);
+// rs_chunk_damp.cu: the chunk-parallel prefill on the tensor cores, DAMP-exact tiles (groups of 32)
+cudaError_t launch_prefill_chunked_damp(const StepLaunch &L, PrefillParamsDamp &P, cudaStream_t s);
 cudaError_t launch_convert_damp(int D, int khi, ConvertParamsDamp &P, cudaStream_t s);
 
 }  // namespace rs

@@ -238,6 +238,102 @@ def test_chunked_prefill_mixed_full_size_sampled(quant, L):
     print(f"\nchunked prefill, mixed {quant}, L={L}: o {o_err:.3g}, codes off by one {frac:.2g}")
 
 
+def check_damp(w, n_tok, pi, cs, mode, packed0, inputs, pool_g, o_g, bsel=None):
+    """DAMP-exact tiles (INT8 groups of 32 columns, value scaling): the rule of the mixed layout, on
+    the stored state T = S diag(c')^-1 of each tile (physical rows), scales per (row, group)."""
+    q, k, v, a, b = inputs
+    if bsel is None:
+        bsel = np.arange(w.B)
+    ws = sub_batch(w, bsel)
+    pick = lambda x: np.ascontiguousarray(x[bsel])
+    L = q.shape[1]
+    n_sel = np.ascontiguousarray(n_tok[bsel])
+    sel = w.slot_idx[bsel]
+    slots = ws.slot_idx
+    p0 = np.ascontiguousarray(packed0[sel])
+    ref = p0.copy()
+    o_r = np.full((len(bsel), L, w.Hv, D), 3.0, np.float32)
+    _, st = orc.replay_damp(ref, slots, n_sel, pi, cs, KHI, 32, D, D, pick(q), pick(k), pick(v), pick(a), pick(b),
+                            o=o_r, mode=mode)
+    assert st == 0
+    s32 = orc.convert_pool_damp_to_f32(p0, D, D, KHI, 32, pi, cs)    # S, key-channel order
+    _, st = orc.replay_f32(s32, slots, n_sel, pick(q), pick(k), pick(v), pick(a), pick(b))
+    assert st == 0
+    worst = 0.0
+    for i, bb in enumerate(bsel):
+        n = int(n_tok[bb])
+        if n:
+            worst = max(worst, tile_rel(np.swapaxes(o_g[bb, :n], 0, 1), np.swapaxes(o_r[i, :n], 0, 1)))
+        assert np.all(o_g[bb, n:] == 3.0), "rows past n_tokens must stay untouched"
+    assert worst <= TOL, f"o {worst:.3g}"
+    g = pool_g[sel]
+    hb, lb = 2 * KHI * D, (D - KHI) * D
+    cg = g[..., hb:hb + lb].view(np.int8).astype(np.int32)
+    cr = ref[..., hb:hb + lb].view(np.int8).astype(np.int32)
+    diff = np.abs(cg - cr)
+    assert diff.max() <= 1
+    frac = float(np.mean(diff != 0))
+    assert frac <= 5e-3, frac
+    rows = np.asarray(pi).reshape(w.Hv, D)                           # physical row -> key channel
+    csa = np.asarray(cs, np.float64).reshape(w.Hv, D)
+    n_t = len(bsel)
+    sg = g[..., hb + lb:].copy().view(np.float32).astype(np.float64).reshape(n_t, w.Hv, D - KHI, D // 32)
+    sr = ref[..., hb + lb:].copy().view(np.float32).astype(np.float64).reshape(n_t, w.Hv, D - KHI, D // 32)
+    for hh in range(w.Hv):
+        T = s32[:, hh].astype(np.float64) / csa[hh][None, None, :]   # [n][u][v], key-channel order
+        Tp = T[:, rows[hh], :]                                       # physical rows
+        norm = np.max(np.abs(Tp), axis=(-2, -1))
+        assert np.all(np.abs(sg[:, hh] - sr[:, hh]) <=
+                      TOL * norm[:, None, None] / 127.0 + 4 * np.spacing(sr[:, hh].astype(np.float32)))
+        dq = np.stack([orc.damp_unpack(g[i, hh], D, D, KHI, 32) for i in range(n_t)]).astype(np.float64)
+        step = np.empty_like(Tp)
+        step[:, :KHI, :] = np.abs(Tp[:, :KHI, :]) * 2.0 ** -10 + 2.0 ** -24
+        grp = np.repeat(np.maximum(sg[:, hh], sr[:, hh]), 32, axis=-1)  # [n][row - KHI][v]
+        step[:, KHI:, :] = grp
+        err = np.abs(dq - Tp) - step
+        assert np.all(err <= TOL * norm[:, None, None]), float(np.max(err / norm[:, None, None]))
+    return worst, frac
+
+
+def damp_case(B, Hk, Hv, L, per_channel, seed, quant, n_tok=None):
+    w = gen.decode_workload(B=B, Hk=Hk, Hv=Hv, d=D, steps=L, per_channel=per_channel, in_dtype="bf16",
+                            seed=seed, horizon=(2.0, 8192.0) if per_channel else (4.0, 4096.0))
+    if n_tok is None:
+        n_tok = np.full(B, L, np.int32)
+    hi = gen.hi_rows(Hv, D, KHI, seed=seed)
+    pi = orc.row_map(hi, D)
+    cs = gen.value_scales(Hv, D, seed=seed)
+    mode = 1 if quant == "fused" else 0
+    lay = rs.Layout("damp", D, Hv, Hk, k_hi=KHI, hi_rows=hi, value_scales=cs, quant=quant)
+    packed0 = orc.convert_pool_f32_to_damp(w.state0, KHI, 32, pi, cs, mode=mode)
+    qd, kd, vd, ad, bd = replay_inputs(w, L)
+    q, k, v, a, b = gen.replay_view(w, L)
+    pool = dev(packed0)
+    o = torch.full((B, L, Hv, D), 3.0, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rs.prefill_update(lay, per_channel, pool, dev(w.slot_idx), qd, kd, vd, ad, bd, n_tokens=dev(n_tok),
+                      o=o, status=status, chunked=True)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return w, n_tok, pi, cs, mode, packed0, (q, k, v, a, b), host(pool), host(o)
+
+
+@pytest.mark.parametrize("quant", ["ieee", "fused"])
+@pytest.mark.parametrize("per_channel,Hk,Hv", [(True, 4, 4), (False, 2, 4)])
+def test_chunked_prefill_damp_ragged(quant, per_channel, Hk, Hv):
+    B, L = 9, 37
+    n_tok = gen.rng(6).integers(0, L + 1, B).astype(np.int32)
+    n_tok[0], n_tok[1], n_tok[2], n_tok[3] = 0, L, 1, 32
+    check_damp(*damp_case(B, Hk, Hv, L, per_channel, 73, quant, n_tok=n_tok))
+
+
+@pytest.mark.parametrize("quant", ["ieee", "fused"])
+def test_chunked_prefill_damp_full_size_sampled(quant):
+    """KDA, batch 256, 32 heads, DAMP-exact state, 32 tokens, sampled sequences (all heads)."""
+    o_err, frac = check_damp(*damp_case(256, 32, 32, 32, True, 74, quant), bsel=np.array([5, 199]))
+    print(f"\nchunked prefill, DAMP-exact {quant}, L=32: o {o_err:.3g}, codes off by one {frac:.2g}")
+
+
 def test_chunked_prefill_guards_and_layouts():
     B, Hk, Hv, L = 4, 2, 2, 5
     w = gen.decode_workload(B=B, Hk=Hk, Hv=Hv, d=D, steps=L, per_channel=True, in_dtype="bf16", seed=65)
@@ -257,7 +353,8 @@ def test_chunked_prefill_guards_and_layouts():
         if slots[bb] < w.state0.shape[0]:
             assert np.array_equal(got[slots[bb]], w.state0[slots[bb]])
     hi = gen.hi_rows(Hv, D, 16, seed=1)
-    damp = rs.Layout("damp", D, Hv, Hk, k_hi=16, hi_rows=hi)  # DAMP-exact tiles: the sequential form only
+    hi32 = gen.hi_rows(Hv, D, 32, seed=1)
+    wide = rs.Layout("mixed", D, Hv, Hk, k_hi=32, hi_rows=hi32)  # 32 FP16 rows: the chunked form is not built
     with pytest.raises(rs.RsError) as e:
-        rs.prefill_update(damp, True, damp.empty_pool(B), dev(w.slot_idx), qd, kd, vd, ad, bd, chunked=True)
+        rs.prefill_update(wide, True, wide.empty_pool(B), dev(w.slot_idx), qd, kd, vd, ad, bd, chunked=True)
     assert e.value.status == _abi.RS_ERR_UNSUPPORTED
