@@ -302,10 +302,10 @@ rs_status rs_prefill_update(const rs_layout *l, int32_t per_channel_decay, void 
  * arithmetic), so its INT8 codes can differ by one from those of
  * rs_prefill_update where the FP32 state sits that close to a rounding
  * boundary.  Built for dk = dv = 128 on the FP32 layout and on the mixed
- * layout with k_hi = 16 and one scale per row; other layouts (DAMP-exact
- * groups among them) return RS_ERR_UNSUPPORTED before any launch, as do
- * in_dtype RS_F16 on the mixed layout and B * L >= 2^31 - 32.  Use
- * rs_prefill_update where bit-exactness with single decode steps is
+ * layouts with k_hi = 16 (one scale per row, or DAMP-exact groups of 32
+ * with value scaling); other layouts return RS_ERR_UNSUPPORTED before any
+ * launch, as do in_dtype RS_F16 on a mixed layout and B * L >= 2^31 - 32.
+ * Use rs_prefill_update where bit-exactness with single decode steps is
  * needed. */
 rs_status rs_prefill_chunked_update(const rs_layout *l, int32_t per_channel_decay, void *pool,
                                     int64_t n_slots, const int32_t *slot_idx, int32_t B,

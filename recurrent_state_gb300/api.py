@@ -183,8 +183,8 @@ def prefill_update(layout, per_channel_decay, pool, slot_idx, q, k, v, alpha, be
     state, read and written once; ``n_tokens`` [B] int32 limits each sequence
     to its first n_tokens[b] tokens (default: all L).  ``chunked``: the
     chunk-parallel form on the tensor cores (rs_prefill_chunked_update; FP32
-    layout and the mixed one with one scale per row; equal to the recurrence
-    up to rounding)."""
+    layout and the mixed ones with 16 FP16 rows; equal to the recurrence up
+    to rounding)."""
     n_slots = _pool_slots(layout, pool)
     _dev(slot_idx, "slot_idx", torch.int32)
     _dev(n_tokens, "n_tokens", torch.int32)
