@@ -33,9 +33,10 @@
 // exact remainder lo = x - hi, and the products hi*hi + hi*lo + lo*hi (about
 // 2^-21 relative) accumulate in fp32 in tensor memory.  Where one operand is
 // shared, its hi and lo parts stack along M or N so that one instruction
-// makes two of the three products (G: [hi ; lo] rows of Khat and Qhat; MMA 1
-// to 3: [hi ; lo] rows of the B operand), and the accumulator columns that
-// hold them are summed when read.  A[t][i] = Khat_t . Kchk_i and
+// makes two of the three products (G: [hi ; lo] rows of Khat and Qhat along
+// M and of Kchk along N, all four products in one instruction; MMA 1 to 3:
+// [hi ; lo] rows of the B operand), and the accumulator columns that hold
+// them are summed when read.  A[t][i] = Khat_t . Kchk_i and
 // Bm[t][i] = Qhat_t . Kchk_i with Kchk_i = k_i / Gamma_i (the decay products
 // factor through the cumulative decay), unless some cumulative decay of the
 // group falls below 1e-20, where the CUDA cores take the running product of
@@ -157,9 +158,10 @@ __device__ __forceinline__ void load16(const uint8_t *p, float (&x)[16]) {
 }
 
 // tensor-memory columns: S^T (also MMA 1's high part) and its remainder; MMA 1's accumulator
-// D1 = [hi*hi + lo*hi of P^T | of Oq^T | hi*lo of P^T | of Oq^T]; the Gram products G; W^T
+// D1 = [hi*hi + lo*hi of P^T | of Oq^T | hi*lo of P^T | of Oq^T]; the Gram products G (Kchk's high
+// parts | remainders); W^T
 // (MMA 2: [hi*hi + lo*hi | hi*lo]), whose columns then take MMA 3's W^T Bm^T likewise
-constexpr uint32_t cS = 0, cSl = D, cD1 = 2 * D, cG = 3 * D, cW = 3 * D + C;
+constexpr uint32_t cS = 0, cSl = D, cD1 = 2 * D, cG = 3 * D, cW = 3 * D + 2 * C;
 static_assert(cW + 2 * C <= kTmemCols, "tensor memory");
 constexpr float kFastMin = 1e-20f;  // smallest cumulative decay of the factored form
 
@@ -514,19 +516,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::fence_before_sync();
             __syncthreads();  // operands in place
             // ---- the Gram products (factored form): G = [Khat_hi ; Qhat_hi ; Khat_lo ; Qhat_lo]
-            // [Kchk_hi + Kchk_lo]^T, so that A = G[0..31] + G[64..95] and Bm = G[32..63] +
-            // G[96..127] hold all four products of the split pairs; then MMA 1: D1 = S0^T
+            // [Kchk_hi ; Kchk_lo]^T, so that A = G[0..31] + G[64..95] and Bm = G[32..63] +
+            // G[96..127] (each the sum of its two column halves) hold all four products of the
+            // split pairs; then MMA 1: D1 = S0^T
             // [Khat ; Qhat ; Khat_lo ; Qhat_lo]^T + S0_lo^T [Khat ; Qhat]^T.  Two warps issue (one
             // thread each): the tensor pipe takes the two streams faster than one thread's
             // back-to-back issue.
             if (tid == 0 && fast) {
                 tc::fence_after_sync();
-                const uint32_t ig = tc::idesc_tf32(128, C);
+                // B = [Kchk_hi ; Kchk_lo] (64 rows): columns 0..31 of G take the high parts, 32..63 the
+                // remainders
+                const uint32_t ig = tc::idesc_tf32(128, 2 * C);
 #pragma unroll 1
-                for (int s = 0; s < D / 8; ++s) {
-                    tc::mma_tf32(tbase + cG, dG + 16 * s, dKCh + 16 * s, ig, s > 0);
-                    tc::mma_tf32(tbase + cG, dG + 16 * s, dKCl + 16 * s, ig, true);
-                }
+                for (int s = 0; s < D / 8; ++s) tc::mma_tf32(tbase + cG, dG + 16 * s, dKCh + 16 * s, ig, s > 0);
                 tc::commit(&bars[5]);
             }
             if (tid == 32) {
@@ -568,7 +570,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pendm &= ~(1u << 5);
                 tc::fence_after_sync();
                 float g[16];
-                tc::ld16_wait(tm + cG + (C / 2) * hf, g);
+                {
+                    float g2[16];
+                    tc::ld16(tm + cG + (C / 2) * hf, g);
+                    tc::ld16(tm + cG + C + (C / 2) * hf, g2);
+                    tc::wait_ld_regs(g, g2);
+#pragma unroll
+                    for (int j = 0; j < C / 2; ++j) g[j] = __fadd_rn(g[j], g2[j]);
+                }
                 float *G2 = reinterpret_cast<float *>(smem + oA2h);  // [64][CA]
                 if (v >= 2 * C) {
 #pragma unroll
