@@ -126,7 +126,17 @@ static_assert(oK % 128 == 0 && oAl % 128 == 0 && oV % 128 == 0, "tensor-copy des
 // (the columns past D lie outside the tensor and arrive as zeros).
 struct ChunkMaps {
     CUtensorMap k, q, v, a;  // a: per-channel decays (KDA)
+    CUtensorMap o;           // the outputs, box of C rows by D (used when o_rows != 0)
+    int o_rows;              // 1: a full group's outputs leave by one tensor copy
 };
+// C rows of one head from shared memory to a [rows][heads][D] tensor (a bulk group of this thread)
+__device__ __forceinline__ void tma_store_rows(const CUtensorMap *map, const void *src, int head, int row) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(0), "r"(head), "r"(row), "r"(smem_addr(src))
+        : "memory");
+}
 __device__ __forceinline__ void tma_rows(void *dst, const CUtensorMap *map, int head, int row, uint64_t *bar) {
     asm volatile(
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
@@ -704,7 +714,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     vt[j] = t < nt ? load_as_f32<TI>(reinterpret_cast<const TI *>(rawV + t * RP) + v) : 0.0f;
                 }
                 tc::wait_ld_regs(pa, pb);
-#pragma unroll
                 if constexpr (GRP) {  // v' = v / c' (IEEE division)
 #pragma unroll
                     for (int j = 0; j < C / 2; ++j) vt[j] = __fdiv_rn(vt[j], csS[v]);
@@ -801,10 +810,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::wait_ld_regs(oc, od);
 #pragma unroll
                 for (int j = 0; j < C / 2; ++j) {
-                    const int t = (C / 2) * hf + j;
-                    float o = __fadd_rn(__fadd_rn(oa[j], ob[j]), __fadd_rn(oc[j], od[j]));
-                    if constexpr (GRP) o = __fmul_rn(csS[v], o);  // o = c' o'
-                    if (t < nt) store_from_f32<TO>(o_g + (((size_t)b * L + t0 + t) * Hv + h) * D + v, o);
+                    oa[j] = __fadd_rn(__fadd_rn(oa[j], ob[j]), __fadd_rn(oc[j], od[j]));
+                    if constexpr (GRP) oa[j] = __fmul_rn(csS[v], oa[j]);  // o = c' o'
+                }
+                if (M.o_rows && nt == C) {
+                    // a full group: rows [t][v] in the T / Bm operand buffers (free until the next
+                    // group's operands, which wait until this copy has read them), one tensor copy out
+                    TO *ost = reinterpret_cast<TO *>(smem + oTh);
+#pragma unroll
+                    for (int j = 0; j < C / 2; ++j) store_from_f32<TO>(ost + ((C / 2) * hf + j) * D + v, oa[j]);
+                    fence_proxy_async_smem();
+                    __syncthreads();
+                    if (tid == 0) {
+                        tma_store_rows(&M.o, smem + oTh, h, b * L + t0);
+                        bulk_store_commit();
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < C / 2; ++j) {
+                        const int t = (C / 2) * hf + j;
+                        if (t < nt) store_from_f32<TO>(o_g + (((size_t)b * L + t0 + t) * Hv + h) * D + v, oa[j]);
+                    }
                 }
             }
             if (!wait_bar(6, ph)) {  // MMA 4: the state columns are current
@@ -957,13 +983,14 @@ EncodeTiled encoder() {
 }
 
 // map of a [rows][heads][D] tensor of `esize`-byte elements, box (D + 16 bytes, 1, C)
+// (pad: the box is D + 16 bytes wide, the columns past D reading as zeros)
 cudaError_t encode_rows(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esize, int heads,
-                        int64_t rows) {
+                        int64_t rows, bool pad = true) {
     const EncodeTiled fn = encoder();
     if (!fn) return cudaErrorNotSupported;
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)rows};
     const cuuint64_t strides[2] = {(cuuint64_t)D * esize, (cuuint64_t)heads * D * esize};
-    const cuuint32_t box[3] = {(cuuint32_t)((D * esize + 16) / esize), 1u, (cuuint32_t)C};
+    const cuuint32_t box[3] = {(cuuint32_t)((D * esize + (pad ? 16 : 0)) / esize), 1u, (cuuint32_t)C};
     const cuuint32_t step[3] = {1u, 1u, 1u};
     const CUresult r = fn(m, dt, 3, const_cast<void *>(base), dims, strides, box, step, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
@@ -992,6 +1019,9 @@ cudaError_t run(PT &P, cudaStream_t s) {
     if (e == cudaSuccess) e = encode_rows(&M.v, P.v, map_type<TI>(), (int)sizeof(TI), P.Hv, rows);
     if (e == cudaSuccess && KDA) e = encode_rows(&M.a, P.alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, P.Hv, rows);
     if (e != cudaSuccess) return e;
+    if (P.o && (reinterpret_cast<uintptr_t>(P.o) & 15u) == 0 &&
+        encode_rows(&M.o, P.o, map_type<TO>(), (int)sizeof(TO), P.Hv, rows, false) == cudaSuccess)
+        M.o_rows = 1;  // else each thread stores its outputs
     e = set_dynamic_smem(reinterpret_cast<const void *>(kern), kSmem);
     if (e != cudaSuccess) return e;
     int grid = device_sm_count();

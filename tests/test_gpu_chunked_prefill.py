@@ -133,6 +133,45 @@ def test_chunked_prefill_gdn_full_size_sampled():
     check_against_oracle(w, n_tok, inputs, pool_g, o_g, bsel=np.array([1, 128, 254]))
 
 
+def test_chunked_prefill_f16_inputs():
+    """fp16 q, k, v (widened exactly), FP32 state: the same bar."""
+    w, n_tok, inputs, pool_g, o_g = run_case(5, 2, 2, 40, True, "f16", seed=66)
+    check_against_oracle(w, n_tok, inputs, pool_g, o_g)
+
+
+@pytest.mark.parametrize("kind", ["fp32", "mixed"])
+def test_chunked_prefill_bf16_outputs(kind):
+    """bf16 outputs: the FP32 readout rounded to nearest even -- within half a bf16 ulp (2^-8 of the
+    value: bf16 keeps 7 explicit mantissa bits) of the oracle's readout, plus the chunked form's
+    tolerance."""
+    B, Hk, Hv, L = 6, 2, 4, 33
+    w = gen.decode_workload(B=B, Hk=Hk, Hv=Hv, d=D, steps=L, per_channel=False, in_dtype="bf16", seed=67,
+                            horizon=(4.0, 4096.0))
+    qd, kd, vd, ad, bd = replay_inputs(w, L)
+    q, k, v, a, b = gen.replay_view(w, L)
+    hi = gen.hi_rows(Hv, D, 16, seed=67)
+    pi = orc.row_map(hi, D)
+    if kind == "fp32":
+        lay, pool = rs.Layout("fp32", D, Hv, Hk), dev(w.state0)
+    else:
+        lay = rs.Layout("mixed", D, Hv, Hk, k_hi=16, hi_rows=hi)
+        pool = dev(orc.convert_pool_f32_to_mixed(w.state0, 16, pi))
+    n_tok = np.full(B, L, np.int32)
+    o = torch.full((B, L, Hv, D), 3.0, dtype=torch.bfloat16, device="cuda")
+    rs.prefill_update(lay, False, pool, dev(w.slot_idx), qd, kd, vd, ad, bd, o=o, chunked=True)
+    torch.cuda.synchronize()
+    s0 = w.state0 if kind == "fp32" else orc.convert_pool_mixed_to_f32(
+        orc.convert_pool_f32_to_mixed(w.state0, 16, pi), D, D, 16, pi)
+    ref = s0.copy()
+    o_r = np.zeros((B, L, Hv, D), np.float32)
+    _, st = orc.replay_f32(ref, w.slot_idx, n_tok, q, k, v, a, b, o=o_r)
+    assert st == 0
+    og = o.float().cpu().numpy()
+    for bb in range(B):
+        err = tile_rel(np.swapaxes(og[bb], 0, 1), np.swapaxes(o_r[bb], 0, 1))
+        assert err <= 2.0 ** -8 + TOL, err
+
+
 KHI = 16
 
 
