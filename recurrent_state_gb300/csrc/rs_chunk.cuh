@@ -1,6 +1,7 @@
 // rs_chunk.cuh -- prefill chunks in the chunk-parallel form on the tensor
-// cores (sm_103a; FP32 state layout, and the mixed FP16/INT8 layout
-// dequantised at a tile's start and requantised at its end).
+// cores (sm_103a; the FP32 state layout, and the mixed FP16/INT8 layouts --
+// one INT8 scale per row, or DAMP-exact groups of 32 with value scaling --
+// dequantised at a tile's start and requantised once at its end).
 //
 // DAMP Appendix A.4 "Prefill path" (prefill runs FP32 arithmetic within a
 // chunk) and "Serving recurrent attention", "Kernels follow the serving
@@ -45,11 +46,15 @@
 // W^T Kchk to the unscaled S0^T and the decay Gamma_C is applied when the
 // state is next read (the next group, or the tile's end): the same sum, with
 // Ktil = Gamma_C Kchk, whose rounding is relative to the result either way.
-// A tile's state (64 KB) arrives by bulk copies during the previous tile,
-// each group's token vectors by tensor copies during the previous group, and
-// the final state leaves by bulk copies while the next tile starts.  The
-// result equals the token-by-token recurrence up to rounding (not bit for
-// bit: the order of the sums differs).
+// A tile's state (64 KB FP32, or its packed tile) arrives by bulk copies
+// during the previous tile, each group's token vectors by tensor copies
+// during the previous group, a full group's outputs leave by one tensor
+// copy, and the final FP32 state by bulk copies while the next tile starts
+// (a packed tile is requantised from shared memory and its words stored by
+// every thread).  On the DAMP-exact layout the state is T = S diag(c')^{-1}:
+// the values enter as v / c' and the outputs leave as c' o.  The result
+// equals the token-by-token recurrence up to rounding (not bit for bit: the
+// order of the sums differs).
 #pragma once
 
 #include <cuda.h>  // CUtensorMap and the tiled-encode signature (called through the runtime)
@@ -88,10 +93,11 @@ constexpr int CA = C + 1;              // row of L = diag(beta) A in shared memo
 constexpr int kKT = D * C * 4;         // Ktil^T (N = c, K = i)
 constexpr int kA2 = D * C * 4;         // R^T, then W^T (M = v, K = t)
 constexpr int kTok = C * DP * 4;       // [t][c] fp32 rows, or one token vector of the widest input type
-constexpr int oB1h = 0, oB1l = oB1h + kB1;
-constexpr int oKTh = oB1l + kB1, oKTl = oKTh + kKT;          // KT, A2: also a tile's final state
+constexpr int oB1h = 0, oB1l = oB1h + kB1;                   // also: the next tile's incoming state
+constexpr int oKTh = oB1l + kB1, oKTl = oKTh + kKT;          // KT, A2: also a tile's final state and a
+                                                             // packed tile's dequantised rows
 constexpr int oA2h = oKTl + kKT, oA2l = oA2h + kA2;
-constexpr int oTh = oA2l + kA2, oTl = oTh + kCC, oBh = oTl + kCC, oBl = oBh + kCC;
+constexpr int oTh = oA2l + kA2, oTl = oTh + kCC, oBh = oTl + kCC, oBl = oBh + kCC;  // also: a group's outputs
 constexpr int oK = oBl + kCC, oQ = oK + kTok, oAl = oQ + kTok;
 constexpr int oBeta = oAl + kTok, oAlpS = oBeta + C * 4, oGc = oAlpS + C * 4;
 constexpr int oMA = oGc + D * 4;
