@@ -373,12 +373,23 @@ def test_chunked_prefill_damp_full_size_sampled(quant):
     print(f"\nchunked prefill, DAMP-exact {quant}, L=32: o {o_err:.3g}, codes off by one {frac:.2g}")
 
 
-def test_chunked_prefill_guards_and_layouts():
+@pytest.mark.parametrize("kind", ["fp32", "mixed", "damp"])
+def test_chunked_prefill_guards_and_layouts(kind):
     B, Hk, Hv, L = 4, 2, 2, 5
     w = gen.decode_workload(B=B, Hk=Hk, Hv=Hv, d=D, steps=L, per_channel=True, in_dtype="bf16", seed=65)
     qd, kd, vd, ad, bd = replay_inputs(w, L)
-    lay = rs.Layout("fp32", D, Hv, Hk)
-    pool = dev(w.state0)
+    hi = gen.hi_rows(Hv, D, 16, seed=1)
+    pi = orc.row_map(hi, D)
+    if kind == "fp32":
+        lay, start = rs.Layout("fp32", D, Hv, Hk), w.state0
+    elif kind == "mixed":
+        lay = rs.Layout("mixed", D, Hv, Hk, k_hi=16, hi_rows=hi)
+        start = orc.convert_pool_f32_to_mixed(w.state0, 16, pi)
+    else:
+        cs = gen.value_scales(Hv, D, seed=1)
+        lay = rs.Layout("damp", D, Hv, Hk, k_hi=16, hi_rows=hi, value_scales=cs)
+        start = orc.convert_pool_f32_to_damp(w.state0, 16, 32, pi, cs)
+    pool = dev(start)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     slots = w.slot_idx.copy()
     slots[1] = 999                                 # out of range: skipped, bit 1
@@ -389,9 +400,10 @@ def test_chunked_prefill_guards_and_layouts():
     assert int(status.item()) == (_abi.RS_DEV_BAD_SLOT | _abi.RS_DEV_BAD_ACCEPT)
     got = host(pool)
     for bb in (1, 2):  # skipped sequences keep their state
-        if slots[bb] < w.state0.shape[0]:
-            assert np.array_equal(got[slots[bb]], w.state0[slots[bb]])
-    hi = gen.hi_rows(Hv, D, 16, seed=1)
+        if slots[bb] < start.shape[0]:
+            assert np.array_equal(got[slots[bb]], start[slots[bb]])
+    for bb in (0, 3):  # the others changed
+        assert not np.array_equal(got[slots[bb]], start[slots[bb]])
     hi32 = gen.hi_rows(Hv, D, 32, seed=1)
     wide = rs.Layout("mixed", D, Hv, Hk, k_hi=32, hi_rows=hi32)  # 32 FP16 rows: the chunked form is not built
     with pytest.raises(rs.RsError) as e:
