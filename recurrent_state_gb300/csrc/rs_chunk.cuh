@@ -194,6 +194,13 @@ __device__ __forceinline__ void put_split4(uint8_t *hi, uint8_t *lo, uint32_t of
     *reinterpret_cast<float4 *>(hi + off) = h;
     *reinterpret_cast<float4 *>(lo + off) = make_float4(a - h.x, b - h.y, c - h.z, d - h.w);
 }
+// 1 / x by the hardware's approximate reciprocal (about 1 ulp; x a normal number here): Kchk only enters
+// products held to the FP32 state's tolerance, so a correctly rounded quotient is not needed
+__device__ __forceinline__ float rcp_fast(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
 __device__ __forceinline__ float4 mul4(float4 a, float4 b) {
     return make_float4(__fmul_rn(a.x, b.x), __fmul_rn(a.y, b.y), __fmul_rn(a.z, b.z), __fmul_rn(a.w, b.w));
 }
@@ -493,8 +500,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                             : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
                     const float4 g4 = *reinterpret_cast<const float4 *>(aS + t * DP + cb);
                     const float4 kh = mul4(k4, g4), qh = mul4(qv4, g4);
-                    const float4 kc = make_float4(__fmul_rn(k4.x, __frcp_rn(g4.x)), __fmul_rn(k4.y, __frcp_rn(g4.y)),
-                                                  __fmul_rn(k4.z, __frcp_rn(g4.z)), __fmul_rn(k4.w, __frcp_rn(g4.w)));
+                    const float4 kc = make_float4(__fmul_rn(k4.x, rcp_fast(g4.x)), __fmul_rn(k4.y, rcp_fast(g4.y)),
+                                                  __fmul_rn(k4.z, rcp_fast(g4.z)), __fmul_rn(k4.w, rcp_fast(g4.w)));
                     put_split4(smem + oB1h, smem + oB1l, tc::kmajor_offset(t, cb, D), kh.x, kh.y, kh.z, kh.w);
                     put_split4(smem + oB1h, smem + oB1l, tc::kmajor_offset(C + t, cb, D), qh.x, qh.y, qh.z, qh.w);
                     *reinterpret_cast<float4 *>(aS + t * DP + cb) = kc;
