@@ -727,9 +727,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     vt[j] = t < nt ? load_as_f32<TI>(reinterpret_cast<const TI *>(rawV + t * RP) + v) : 0.0f;
                 }
                 tc::wait_ld_regs(pa, pb);
-                if constexpr (GRP) {  // v' = v / c' (IEEE division)
+                if constexpr (GRP) {  // v' = v / c', by one correctly rounded reciprocal of the column's c'
+                    const float rc = __frcp_rn(csS[v]);
 #pragma unroll
-                    for (int j = 0; j < C / 2; ++j) vt[j] = __fdiv_rn(vt[j], csS[v]);
+                    for (int j = 0; j < C / 2; ++j) vt[j] = __fmul_rn(vt[j], rc);
                 }
 #pragma unroll
                 for (int j = 0; j < C / 2; ++j) vt[j] = __fmul_rn(betaS[(C / 2) * hf + j], __fsub_rn(vt[j], __fadd_rn(pa[j], pb[j])));
