@@ -227,12 +227,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *alpS = reinterpret_cast<float *>(smem + oAlpS);
     float *gC = reinterpret_cast<float *>(smem + oGc);
     float *mA = reinterpret_cast<float *>(smem + oMA);  // L = diag(beta) A, row stride CA
-    // mbarriers: MMA 1, MMA 2, MMA 3, state copy, input copy, Gram, MMA 4
+    // mbarriers: MMA 1, MMA 2, MMA 3, state copy, input copy, Gram, MMA 4 (MMA 1 and the Gram
+    // products are issued by four warps, MMA 2 by two, each committing once)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + oBar);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + oTslot);
 
     if (tid == 0)
-        for (int i = 0; i < kBars; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < kBars; ++i) mbar_init(&bars[i], i == 0 || i == 5 ? 4 : i == 1 ? 2 : 1);
     fence_mbar_init();
     if (w == 0) {
         tc::tmem_alloc(tslot, kTmemCols);
@@ -245,6 +246,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_after_sync();
     const uint32_t tbase = *tslot;
     const uint32_t tm = tbase + ((uint32_t)(32 * (w & 3)) << 16);  // this warp's 32 lanes
+    // the accumulators of MMA 1, MMA 2 and the Gram products start from zero in every group:
+    // their instructions come from several warps in no fixed order, so all of them accumulate
+    // (zeroed again after each group's last read of them; the first group's split waits for
+    // these stores)
+    auto zero_acc = [&]() {
+        float z[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) z[j] = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) tc::st16(tm + cD1 + k * C + (C / 2) * hf, z);
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            tc::st16(tm + cW + k * C + (C / 2) * hf, z);
+            tc::st16(tm + cG + k * C + (C / 2) * hf, z);
+        }
+    };
+    zero_acc();
     // operand descriptors at k-step 0; step s is 256 s bytes on, i.e. + 16 s in the address field
     const uint64_t dB1h = tc::smem_desc(smem + oB1h, 128, D * 32), dB1l = tc::smem_desc(smem + oB1l, 128, D * 32);
     const uint64_t dA2h = tc::smem_desc(smem + oA2h, 128, C * 32), dA2l = tc::smem_desc(smem + oA2l, 128, C * 32);
@@ -281,15 +299,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return items;
     };
-    // a group's token vectors by tensor copies (one thread issues them), the per-token scalars
+    // a group's token vectors by tensor copies (thread `issuer` issues them), the per-token scalars
     // (beta, GDN alpha) into registers of threads 0..C-1; rows past the sequence's tokens are
     // copied too and masked where read
     constexpr uint32_t kInBytes = 3u * C * RP + (KDA ? (uint32_t)C * DP * 4 : 0u);
     float fb = 0.0f, fga = 1.0f;  // beta and the GDN decay of token tid of the fetched group
-    auto fetch = [&](int it, int tb, int nn) {  // nn: the sequence's token count
+    auto fetch = [&](int it, int tb, int nn, int issuer) {  // nn: the sequence's token count
         const int bb = it / Hv, hh = it - bb * Hv, gg = hh / (Hv / Hk);
         const int ntt = min(C, nn - tb);
-        if (tid == 0) {
+        if (tid == issuer) {
             const int row = bb * L + tb;
             mbar_arrive_expect_tx(&bars[4], kInBytes);
             tma_rows(smem + oK, &M.k, gg, row, &bars[4]);
@@ -325,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int first = next_work(blockIdx.x);
         if (first < items) {
             load_state(first);
-            fetch(first, 0, P.n_tokens ? P.n_tokens[first / Hv] : L);
+            fetch(first, 0, P.n_tokens ? P.n_tokens[first / Hv] : L, 0);
         }
     }
     // slot and token count of the current tile, read one tile ahead
@@ -541,30 +559,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---- the Gram products (factored form): G = [Khat_hi ; Qhat_hi ; Khat_lo ; Qhat_lo]
             // [Kchk_hi ; Kchk_lo]^T, so that A = G[0..31] + G[64..95] and Bm = G[32..63] +
             // G[96..127] (each the sum of its two column halves) hold all four products of the
-            // split pairs; then MMA 1: D1 = S0^T
-            // [Khat ; Qhat ; Khat_lo ; Qhat_lo]^T + S0_lo^T [Khat ; Qhat]^T.  Two warps issue (one
-            // thread each): the tensor pipe takes the two streams faster than one thread's
-            // back-to-back issue.
-            if (tid == 0 && fast) {
+            // split pairs.  One thread in each of warps 0..3 issues a quarter of the k-steps: one
+            // thread issues a tensor-core instruction only about every hundred cycles, and the
+            // pipe takes several streams at once.  MMA 1 waits until the solve for T, so that the
+            // Gram products have the pipe to themselves.
+            if (fast && w < 4 && (tid & 31) == 0) {
                 tc::fence_after_sync();
                 // B = [Kchk_hi ; Kchk_lo] (64 rows): columns 0..31 of G take the high parts, 32..63 the
                 // remainders
                 const uint32_t ig = tc::idesc_tf32(128, 2 * C);
 #pragma unroll 1
-                for (int s = 0; s < D / 8; ++s) tc::mma_tf32(tbase + cG, dG + 16 * s, dKCh + 16 * s, ig, s > 0);
+                for (int s = w * (D / 32); s < (w + 1) * (D / 32); ++s)
+                    tc::mma_tf32(tbase + cG, dG + 16 * s, dKCh + 16 * s, ig, true);
                 tc::commit(&bars[5]);
             }
-            if (tid == 32) {
-                tc::fence_after_sync();
-                const uint32_t i4 = tc::idesc_tf32(128, 4 * C), i2 = tc::idesc_tf32(128, 2 * C);
-#pragma unroll 1
-                for (int s = 0; s < D / 8; ++s) {
-                    tc::mma_tf32_ta(tbase + cD1, tbase + cS + 8 * s, dB1h + 16 * s, i4, s > 0);
-                    tc::mma_tf32_ta(tbase + cD1, tbase + cSl + 8 * s, dB1h + 16 * s, i2, true);
-                }
-                tc::commit(&bars[0]);
-            }
-            pendm |= fast ? (1u | 1u << 5) : 1u;
+            if (fast) pendm |= 1u << 5;
             // ---- meanwhile: Ktil^T (factored form: Kchk^T, the decay pending), then
             // L = diag(beta) A, the Bm operand and T on the CUDA cores
             if (fast) {  // thread (c, i = 16 hf ..), 4 i per store
@@ -664,32 +673,49 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             __syncthreads();
-            {  // T = (I + L)^{-1} by forward substitution, L = diag(beta) A strictly lower: thread
-               // (column j = tid / 8, r = tid % 8) holds T[r + 8 m][j], m = 0..3, and takes
-               // T[i][j] from its owner by shuffle once row i is final
-                const int j = tid >> 3, r = tid & 7;
-                float x[4], lc[4], ln[4];  // L[r + 8 m][i] of this step and the next
+            if (w < 4) {
+                // ---- MMA 1: D1 = S0^T [Khat ; Qhat ; Khat_lo ; Qhat_lo]^T + S0_lo^T [Khat ; Qhat]^T,
+                // a quarter of it from one thread of each of warps 0..3 (S0^T, N = 128, by warps 0
+                // and 1; S0_lo^T, N = 64, by warps 2 and 3; half the k-steps each)
+                if ((tid & 31) == 0) {
+                    tc::fence_after_sync();
+                    const bool hi = w < 2;
+                    const uint32_t ia = tc::idesc_tf32(128, hi ? 4 * C : 2 * C);
+                    const uint32_t ta = tbase + (hi ? cS : cSl);
+                    const int s0 = (w & 1) * (D / 16);
+#pragma unroll 1
+                    for (int s = s0; s < s0 + D / 16; ++s)
+                        tc::mma_tf32_ta(tbase + cD1, ta + 8 * s, dB1h + 16 * s, ia, true);
+                    tc::commit(&bars[0]);
+                }
+            } else {
+                // ---- T = (I + L)^{-1} by forward substitution, L = diag(beta) A strictly lower:
+                // thread (column j = (tid - 128) / 4, r = tid % 4) of warps 4..7 holds T[r + 4 m][j],
+                // m = 0..7, and takes T[i][j] from its owner by shuffle once row i is final
+                const int j = (tid - kThreads / 2) >> 2, r = tid & 3;
+                float x[8], lc[8], ln[8];  // L[r + 4 m][i] of this step and the next
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    x[m] = (r + 8 * m == j) ? 1.0f : 0.0f;
-                    lc[m] = mA[(r + 8 * m) * CA];
+                for (int m = 0; m < 8; ++m) {
+                    x[m] = (r + 4 * m == j) ? 1.0f : 0.0f;
+                    lc[m] = mA[(r + 4 * m) * CA];
                 }
 #pragma unroll
                 for (int i = 0; i < C - 1; ++i) {
 #pragma unroll
-                    for (int m = 0; m < 4; ++m) ln[m] = i + 1 < C - 1 ? mA[(r + 8 * m) * CA + i + 1] : 0.0f;
-                    const float xi = __shfl_sync(0xffffffffu, x[i >> 3], (tid & 24) | (i & 7));
+                    for (int m = 0; m < 8; ++m) ln[m] = i + 1 < C - 1 ? mA[(r + 4 * m) * CA + i + 1] : 0.0f;
+                    const float xi = __shfl_sync(0xffffffffu, x[i >> 2], (tid & 28) | (i & 3));
 #pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        const int t = r + 8 * m;
+                    for (int m = 0; m < 8; ++m) {
+                        const int t = r + 4 * m;
                         if (t > i) x[m] = __fmaf_rn(-lc[m], xi, x[m]);
                         lc[m] = ln[m];
                     }
                 }
 #pragma unroll
-                for (int m = 0; m < 4; ++m)  // T as a B operand: row t, K = j
-                    put_split(smem + oTh, smem + oTl, tc::kmajor_offset(r + 8 * m, j, C), x[m]);
+                for (int m = 0; m < 8; ++m)  // T as a B operand: row t, K = j
+                    put_split(smem + oTh, smem + oTl, tc::kmajor_offset(r + 4 * m, j, C), x[m]);
             }
+            pendm |= 1u;
             fence_proxy_async_smem();
             // ---- MMA 1 done
             if (!wait_bar(0, ph)) {
@@ -739,27 +765,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     put_split4(smem + oA2h, smem + oA2l, tc::kmajor_offset(v, (C / 2) * hf + j, C), vt[j], vt[j + 1],
                                vt[j + 2], vt[j + 3]);
             }
-            __syncthreads();  // every copied row of the group has been read (and the decays applied)
-            if (!fast && hf == 0) gC[v] = 1.0f;  // nothing pending
-            // ---- the next group's (or tile's) vectors come in now
-            if (!last) {
-                fetch(item, t0 + C, n);
-            } else if (nxt < items) {
-                fetch(nxt, 0, nxt_n);
-            }
             fence_proxy_async_smem();
             tc::fence_before_sync();
-            __syncthreads();
-            // ---- MMA 2: W^T = R^T [T ; T_lo]^T + R_lo^T T^T
-            if (tid == 0) {
+            __syncthreads();  // R^T in place; every copied row of the group has been read (and the decays applied)
+            if (!fast && hf == 0) gC[v] = 1.0f;  // nothing pending
+            // ---- MMA 2: W^T = R^T [T ; T_lo]^T (thread 0) + R_lo^T T^T (thread 32), while thread 64
+            // issues the copies of the next group's (or tile's) vectors
+            if (tid == 0 || tid == 32) {
                 tc::fence_after_sync();
-                const uint32_t i2 = tc::idesc_tf32(128, 2 * C), i1 = tc::idesc_tf32(128, C);
+                const bool hi = tid == 0;
+                const uint32_t ia = tc::idesc_tf32(128, hi ? 2 * C : C);
+                const uint64_t da = hi ? dA2h : dA2l;
 #pragma unroll
-                for (int s = 0; s < C / 8; ++s) {
-                    tc::mma_tf32(tbase + cW, dA2h + 16 * s, dTh + 16 * s, i2, s > 0);
-                    tc::mma_tf32(tbase + cW, dA2l + 16 * s, dTh + 16 * s, i1, true);
-                }
+                for (int s = 0; s < C / 8; ++s) tc::mma_tf32(tbase + cW, da + 16 * s, dTh + 16 * s, ia, true);
                 tc::commit(&bars[1]);
+            }
+            if (!last) {
+                fetch(item, t0 + C, n, 64);
+            } else if (nxt < items) {
+                fetch(nxt, 0, nxt_n, 64);
             }
             pendm |= 1u << 1;
             if (!wait_bar(1, ph)) {
@@ -847,6 +871,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            zero_acc();  // D1 and the W^T columns have been read
             if (!wait_bar(6, ph)) {  // MMA 4: the state columns are current
                 failed = true;
                 break;
