@@ -227,13 +227,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *alpS = reinterpret_cast<float *>(smem + oAlpS);
     float *gC = reinterpret_cast<float *>(smem + oGc);
     float *mA = reinterpret_cast<float *>(smem + oMA);  // L = diag(beta) A, row stride CA
-    // mbarriers: MMA 1, MMA 2, MMA 3, state copy, input copy, Gram, MMA 4 (MMA 1 and the Gram
-    // products are issued by four warps, MMA 2 by two, each committing once)
+    // mbarriers: MMA 1, MMA 2, MMA 3, state copy, input copy, Gram, MMA 4 (the Gram products are
+    // issued by four warps, MMA 1 and MMA 2 by two, each committing once)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + oBar);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + oTslot);
 
     if (tid == 0)
-        for (int i = 0; i < kBars; ++i) mbar_init(&bars[i], i == 0 || i == 5 ? 4 : i == 1 ? 2 : 1);
+        for (int i = 0; i < kBars; ++i) mbar_init(&bars[i], i == 5 ? 4 : i < 2 ? 2 : 1);
     fence_mbar_init();
     if (w == 0) {
         tc::tmem_alloc(tslot, kTmemCols);
@@ -246,23 +246,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_after_sync();
     const uint32_t tbase = *tslot;
     const uint32_t tm = tbase + ((uint32_t)(32 * (w & 3)) << 16);  // this warp's 32 lanes
-    // the accumulators of MMA 1, MMA 2 and the Gram products start from zero in every group:
-    // their instructions come from several warps in no fixed order, so all of them accumulate
-    // (zeroed again after each group's last read of them; the first group's split waits for
-    // these stores)
-    auto zero_acc = [&]() {
-        float z[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) z[j] = 0.0f;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) tc::st16(tm + cD1 + k * C + (C / 2) * hf, z);
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            tc::st16(tm + cW + k * C + (C / 2) * hf, z);
-            tc::st16(tm + cG + k * C + (C / 2) * hf, z);
-        }
-    };
-    zero_acc();
+    // Several warps issue tensor-core instructions at once (one thread issues one only about
+    // every hundred cycles).  Each issuing thread accumulates into columns of its own, and the
+    // parts are summed in a fixed order when read, so results do not depend on the order in
+    // which the pipe takes the warps' instructions.
     // operand descriptors at k-step 0; step s is 256 s bytes on, i.e. + 16 s in the address field
     const uint64_t dB1h = tc::smem_desc(smem + oB1h, 128, D * 32), dB1l = tc::smem_desc(smem + oB1l, 128, D * 32);
     const uint64_t dA2h = tc::smem_desc(smem + oA2h, 128, C * 32), dA2l = tc::smem_desc(smem + oA2l, 128, C * 32);
@@ -272,6 +259,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the Gram products' A operand: [Khat ; Qhat] high parts (rows 0..63) then remainders (rows 64..127)
     const uint64_t dG = tc::smem_desc(smem + oB1h, 128, D * 32);
     const uint64_t dKCh = tc::smem_desc(smem + oKCh, 128, D * 32), dKCl = tc::smem_desc(smem + oKCl, 128, D * 32);
+    // MMA 1: D1 = S0^T [Khat ; Qhat ; Khat_lo ; Qhat_lo]^T + S0_lo^T [Khat ; Qhat]^T, issued by one
+    // thread of warp 2 (k-steps 0..15, into the D1 columns) and of warp 3 (k-steps 16..31, into
+    // the Gram and W^T columns, then free); R and the outputs add the two parts
+    auto issue_mma1 = [&]() {
+        if ((tid & 31) == 0) {
+            tc::fence_after_sync();
+            const uint32_t i4 = tc::idesc_tf32(128, 4 * C), i2 = tc::idesc_tf32(128, 2 * C);
+            const uint32_t acc = tbase + (w == 2 ? cD1 : cG);
+            const int s0 = (w - 2) * (D / 16);
+#pragma unroll 1
+            for (int s = s0; s < s0 + D / 16; ++s) {
+                tc::mma_tf32_ta(acc, tbase + cS + 8 * s, dB1h + 16 * s, i4, s > s0);
+                tc::mma_tf32_ta(acc, tbase + cSl + 8 * s, dB1h + 16 * s, i2, true);
+            }
+            tc::commit(&bars[0]);
+        }
+    };
 
     const int Hv = P.Hv, Hk = P.Hk, L = P.L;
     constexpr int kStateBytes = MIX ? (GRP ? kDampBytes : kMixBytes) : D * D * 4;
@@ -330,12 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint8_t *src = pool + ((size_t)P.slot_idx[bb] * Hv + hh) * kStateBytes;
         if (tid == 0) {
             mbar_arrive_expect_tx(&bars[3], (uint32_t)kStateBytes);
-            if constexpr (MIX) {
-                bulk_g2s(smem + oB1h, src, kStateBytes, &bars[3]);
-            } else {
-                for (int part = 0; part < 4; ++part)
-                    bulk_g2s(smem + oB1h + part * (D * D), src + part * (D * D), D * D, &bars[3]);
-            }
+            bulk_g2s(smem + oB1h, src, kStateBytes, &bars[3]);  // one copy: each issue costs thread 0 time
         }
         pendm |= 1u << 3;
     };
@@ -559,18 +558,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---- the Gram products (factored form): G = [Khat_hi ; Qhat_hi ; Khat_lo ; Qhat_lo]
             // [Kchk_hi ; Kchk_lo]^T, so that A = G[0..31] + G[64..95] and Bm = G[32..63] +
             // G[96..127] (each the sum of its two column halves) hold all four products of the
-            // split pairs.  One thread in each of warps 0..3 issues a quarter of the k-steps: one
-            // thread issues a tensor-core instruction only about every hundred cycles, and the
-            // pipe takes several streams at once.  MMA 1 waits until the solve for T, so that the
-            // Gram products have the pipe to themselves.
+            // split pairs.  One thread in each of warps 0..3 issues a quarter of the k-steps into
+            // 64 columns of its own (the MMA 1 and W^T columns are free until the parts are read);
+            // MMA 1 waits until then, so that the Gram products have the pipe to themselves.
             if (fast && w < 4 && (tid & 31) == 0) {
                 tc::fence_after_sync();
                 // B = [Kchk_hi ; Kchk_lo] (64 rows): columns 0..31 of G take the high parts, 32..63 the
                 // remainders
                 const uint32_t ig = tc::idesc_tf32(128, 2 * C);
+                const uint32_t acc = tbase + (w == 0 ? cG : w == 1 ? cW : cD1 + (w - 2) * 2 * C);
+                const int s0 = w * (D / 32);
 #pragma unroll 1
-                for (int s = w * (D / 32); s < (w + 1) * (D / 32); ++s)
-                    tc::mma_tf32(tbase + cG, dG + 16 * s, dKCh + 16 * s, ig, true);
+                for (int s = s0; s < s0 + D / 32; ++s) tc::mma_tf32(acc, dG + 16 * s, dKCh + 16 * s, ig, s > s0);
                 tc::commit(&bars[5]);
             }
             if (fast) pendm |= 1u << 5;
@@ -602,21 +601,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pendm &= ~(1u << 5);
                 tc::fence_after_sync();
                 float g[16];
-                {
-                    float g2[16];
-                    tc::ld16(tm + cG + (C / 2) * hf, g);
-                    tc::ld16(tm + cG + C + (C / 2) * hf, g2);
-                    tc::wait_ld_regs(g, g2);
 #pragma unroll
-                    for (int j = 0; j < C / 2; ++j) g[j] = __fadd_rn(g[j], g2[j]);
+                for (int half = 0; half < 2; ++half) {  // the high-part columns, then the remainders'
+                    const uint32_t off = half * C + (C / 2) * hf;
+                    float a0[16], a1[16], a2[16], a3[16];
+                    tc::ld16(tm + cG + off, a0);
+                    tc::ld16(tm + cW + off, a1);
+                    tc::ld16(tm + cD1 + off, a2);
+                    tc::ld16(tm + cD1 + 2 * C + off, a3);
+                    tc::wait_ld_regs(a0, a1);
+                    tc::wait_ld_regs(a2, a3);
+#pragma unroll
+                    for (int j = 0; j < C / 2; ++j) {
+                        const float sj = __fadd_rn(__fadd_rn(__fadd_rn(a0[j], a1[j]), a2[j]), a3[j]);
+                        g[j] = half ? __fadd_rn(g[j], sj) : sj;
+                    }
                 }
                 float *G2 = reinterpret_cast<float *>(smem + oA2h);  // [64][CA]
                 if (v >= 2 * C) {
 #pragma unroll
                     for (int j = 0; j < C / 2; ++j) G2[(v - 2 * C) * CA + (C / 2) * hf + j] = g[j];
                 }
-                __syncthreads();
-                if (v < 2 * C) {
+                tc::fence_before_sync();
+                __syncthreads();  // the Gram parts are read: MMA 1 may overwrite them
+                if (w == 2 || w == 3) {
+                    issue_mma1();
+                } else if (v < 2 * C) {
 #pragma unroll
                     for (int j = 0; j < C / 2; ++j) g[j] = __fadd_rn(g[j], G2[v * CA + (C / 2) * hf + j]);
                     if (v < C) {  // row t = v of A
@@ -672,23 +682,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            __syncthreads();
-            if (w < 4) {
-                // ---- MMA 1: D1 = S0^T [Khat ; Qhat ; Khat_lo ; Qhat_lo]^T + S0_lo^T [Khat ; Qhat]^T,
-                // a quarter of it from one thread of each of warps 0..3 (S0^T, N = 128, by warps 0
-                // and 1; S0_lo^T, N = 64, by warps 2 and 3; half the k-steps each)
-                if ((tid & 31) == 0) {
-                    tc::fence_after_sync();
-                    const bool hi = w < 2;
-                    const uint32_t ia = tc::idesc_tf32(128, hi ? 4 * C : 2 * C);
-                    const uint32_t ta = tbase + (hi ? cS : cSl);
-                    const int s0 = (w & 1) * (D / 16);
-#pragma unroll 1
-                    for (int s = s0; s < s0 + D / 16; ++s)
-                        tc::mma_tf32_ta(tbase + cD1, ta + 8 * s, dB1h + 16 * s, ia, true);
-                    tc::commit(&bars[0]);
-                }
+            if (fast) {  // warps 2 and 3 are issuing MMA 1; L and Bm are in place for the others
+                if (w != 2 && w != 3) group_sync(1, kThreads - 64);
             } else {
+                __syncthreads();
+                if (w == 2 || w == 3) issue_mma1();
+            }
+            if (w >= 4) {
                 // ---- T = (I + L)^{-1} by forward substitution, L = diag(beta) A strictly lower:
                 // thread (column j = (tid - 128) / 4, r = tid % 4) of warps 4..7 holds T[r + 4 m][j],
                 // m = 0..7, and takes T[i][j] from its owner by shuffle once row i is final
@@ -742,17 +742,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::wait_st();
                 tc::fence_before_sync();
             }
-            // ---- R^T = diag(beta) (V^T - P^T) for tokens 16 hf .. 16 hf + 15
+            // ---- R^T = diag(beta) (V^T - P^T) for tokens 16 hf .. 16 hf + 15; and the two parts of
+            // Oq^T summed into the D1 columns (MMA 2 and 3 reuse the other part's columns)
             {
-                float pa[16], pb[16], vt[16];
-                tc::ld16(tm + cD1 + (C / 2) * hf, pa);
-                tc::ld16(tm + cD1 + 2 * C + (C / 2) * hf, pb);
+                const uint32_t tok = (C / 2) * hf;
+                {
+                    float a0[16], a1[16], a2[16], a3[16];
+                    tc::ld16(tm + cD1 + C + tok, a0);
+                    tc::ld16(tm + cD1 + 3 * C + tok, a1);
+                    tc::ld16(tm + cG + C + tok, a2);
+                    tc::ld16(tm + cG + 3 * C + tok, a3);
+                    tc::wait_ld_regs(a0, a1);
+                    tc::wait_ld_regs(a2, a3);
 #pragma unroll
-                for (int j = 0; j < C / 2; ++j) {
-                    const int t = (C / 2) * hf + j;
-                    vt[j] = t < nt ? load_as_f32<TI>(reinterpret_cast<const TI *>(rawV + t * RP) + v) : 0.0f;
+                    for (int j = 0; j < C / 2; ++j)
+                        a0[j] = __fadd_rn(__fadd_rn(__fadd_rn(a0[j], a1[j]), a2[j]), a3[j]);
+                    tc::st16(tm + cD1 + C + tok, a0);
                 }
-                tc::wait_ld_regs(pa, pb);
+                float pa[16], pb[16], vt[16];
+                {
+                    float pc[16], pd[16];
+                    tc::ld16(tm + cD1 + tok, pa);
+                    tc::ld16(tm + cD1 + 2 * C + tok, pb);
+                    tc::ld16(tm + cG + tok, pc);
+                    tc::ld16(tm + cG + 2 * C + tok, pd);
+#pragma unroll
+                    for (int j = 0; j < C / 2; ++j) {
+                        const int t = (C / 2) * hf + j;
+                        vt[j] = t < nt ? load_as_f32<TI>(reinterpret_cast<const TI *>(rawV + t * RP) + v) : 0.0f;
+                    }
+                    tc::wait_ld_regs(pa, pb);
+                    tc::wait_ld_regs(pc, pd);
+#pragma unroll
+                    for (int j = 0; j < C / 2; ++j) pa[j] = __fadd_rn(__fadd_rn(pa[j], pc[j]), pd[j]);
+                }
                 if constexpr (GRP) {  // v' = v / c', by one correctly rounded reciprocal of the column's c'
                     const float rc = __frcp_rn(csS[v]);
 #pragma unroll
@@ -769,15 +792,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::fence_before_sync();
             __syncthreads();  // R^T in place; every copied row of the group has been read (and the decays applied)
             if (!fast && hf == 0) gC[v] = 1.0f;  // nothing pending
-            // ---- MMA 2: W^T = R^T [T ; T_lo]^T (thread 0) + R_lo^T T^T (thread 32), while thread 64
-            // issues the copies of the next group's (or tile's) vectors
+            // ---- MMA 2: W^T = R^T [T ; T_lo]^T (thread 0, into the W^T columns) + R_lo^T T^T (thread
+            // 32, into the Gram columns), while thread 64 issues the copies of the next group's (or
+            // tile's) vectors
             if (tid == 0 || tid == 32) {
                 tc::fence_after_sync();
                 const bool hi = tid == 0;
                 const uint32_t ia = tc::idesc_tf32(128, hi ? 2 * C : C);
                 const uint64_t da = hi ? dA2h : dA2l;
+                const uint32_t acc = tbase + (hi ? cW : cG);
 #pragma unroll
-                for (int s = 0; s < C / 8; ++s) tc::mma_tf32(tbase + cW, da + 16 * s, dTh + 16 * s, ia, true);
+                for (int s = 0; s < C / 8; ++s) tc::mma_tf32(acc, da + 16 * s, dTh + 16 * s, ia, s > 0);
                 tc::commit(&bars[1]);
             }
             if (!last) {
@@ -793,12 +818,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             pendm &= ~(1u << 1);
             tc::fence_after_sync();
             {
-                float wa[16], wb[16];
+                float wa[16], wb[16], wc[16];
                 tc::ld16(tm + cW + (C / 2) * hf, wa);
                 tc::ld16(tm + cW + C + (C / 2) * hf, wb);
+                tc::ld16(tm + cG + (C / 2) * hf, wc);
                 tc::wait_ld_regs(wa, wb);
+                tc::wait_ld_regs(wc);
 #pragma unroll
-                for (int j = 0; j < C / 2; ++j) wa[j] = __fadd_rn(wa[j], wb[j]);
+                for (int j = 0; j < C / 2; ++j) wa[j] = __fadd_rn(__fadd_rn(wa[j], wb[j]), wc[j]);
 #pragma unroll
                 for (int j = 0; j < C / 2; j += 4)
                     put_split4(smem + oA2h, smem + oA2l, tc::kmajor_offset(v, (C / 2) * hf + j, C), wa[j], wa[j + 1],
@@ -838,17 +865,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             pendm &= ~(1u << 2);
             tc::fence_after_sync();
-            if (o_g) {  // O^T = Oq^T (two parts) + W^T Bm^T (two parts)
-                float oa[16], ob[16], oc[16], od[16];
+            if (o_g) {  // O^T = Oq^T (summed when R was formed) + W^T Bm^T (two parts)
+                float oa[16], oc[16], od[16];
+                tc::wait_st();  // this thread's Oq^T sums have landed
                 tc::ld16(tm + cD1 + C + (C / 2) * hf, oa);
-                tc::ld16(tm + cD1 + 3 * C + (C / 2) * hf, ob);
                 tc::ld16(tm + cW + (C / 2) * hf, oc);
                 tc::ld16(tm + cW + C + (C / 2) * hf, od);
-                tc::wait_ld_regs(oa, ob);
-                tc::wait_ld_regs(oc, od);
+                tc::wait_ld_regs(oa, oc);
+                tc::wait_ld_regs(od);
 #pragma unroll
                 for (int j = 0; j < C / 2; ++j) {
-                    oa[j] = __fadd_rn(__fadd_rn(oa[j], ob[j]), __fadd_rn(oc[j], od[j]));
+                    oa[j] = __fadd_rn(oa[j], __fadd_rn(oc[j], od[j]));
                     if constexpr (GRP) oa[j] = __fmul_rn(csS[v], oa[j]);  // o = c' o'
                 }
                 if (M.o_rows && nt == C) {
@@ -871,7 +898,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            zero_acc();  // D1 and the W^T columns have been read
             if (!wait_bar(6, ph)) {  // MMA 4: the state columns are current
                 failed = true;
                 break;
@@ -905,8 +931,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncthreads();
             if constexpr (!MIX) {
                 if (tid == 0) {
-                    for (int part = 0; part < 4; ++part)
-                        bulk_s2g(Sg + part * (D * D / 4), smem + oKTh + part * (D * D), D * D);
+                    bulk_s2g(Sg, smem + oKTh, D * D * 4);
                     bulk_store_commit();
                 }
             } else {

@@ -409,3 +409,30 @@ def test_chunked_prefill_guards_and_layouts(kind):
     with pytest.raises(rs.RsError) as e:
         rs.prefill_update(wide, True, wide.empty_pool(B), dev(w.slot_idx), qd, kd, vd, ad, bd, chunked=True)
     assert e.value.status == _abi.RS_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("kind", ["fp32", "mixed"])
+def test_chunked_prefill_repeats_bit_for_bit(kind):
+    """The tensor-core products are issued by several warps at once; each issuing thread has
+    accumulator columns of its own and the parts are summed in a fixed order, so the same call on
+    the same state gives the same bits every time (KDA, 64 sequences, 32 heads, 64 tokens)."""
+    B, Hk, Hv, L = 64, 32, 32, 64
+    w = gen.decode_workload(B=B, Hk=Hk, Hv=Hv, d=D, steps=L, per_channel=True, in_dtype="bf16", seed=91,
+                            horizon=(2.0, 8192.0))
+    qd, kd, vd, ad, bd = replay_inputs(w, L)
+    if kind == "fp32":
+        lay, start = rs.Layout("fp32", D, Hv, Hk), w.state0
+    else:
+        hi = gen.hi_rows(Hv, D, KHI, seed=91)
+        lay = rs.Layout("mixed", D, Hv, Hk, k_hi=KHI, hi_rows=hi, quant="fused")
+        start = orc.convert_pool_f32_to_mixed(w.state0, KHI, orc.row_map(hi, D), mode=1)
+    runs = []
+    for _ in range(3):
+        pool = dev(start)
+        o = torch.zeros((B, L, Hv, D), device="cuda")
+        rs.prefill_update(lay, True, pool, dev(w.slot_idx), qd, kd, vd, ad, bd, o=o, chunked=True)
+        torch.cuda.synchronize()
+        runs.append((host(pool), host(o)))
+    for pool_r, o_r in runs[1:]:
+        assert np.array_equal(pool_r.view(np.uint8), runs[0][0].view(np.uint8))
+        assert np.array_equal(o_r.view(np.uint32), runs[0][1].view(np.uint32))
