@@ -297,7 +297,8 @@ rs_status rs_prefill_update(const rs_layout *l, int32_t per_channel_decay, void 
  * outputs and the new state follow from W).  The products use tf32 operands
  * split into a high part and an exact remainder, with fp32 accumulation, so
  * the result equals the token-by-token recurrence up to rounding (about
- * 1e-6 relative), not bit for bit.  A mixed tile is dequantised once when
+ * 1e-6 relative), not bit for bit; the same call on the same state gives
+ * the same bits every time.  A mixed tile is dequantised once when
  * its chunk starts and requantised once at its end (its layout's
  * arithmetic), so its INT8 codes can differ by one from those of
  * rs_prefill_update where the FP32 state sits that close to a rounding

@@ -46,15 +46,19 @@
 // W^T Kchk to the unscaled S0^T and the decay Gamma_C is applied when the
 // state is next read (the next group, or the tile's end): the same sum, with
 // Ktil = Gamma_C Kchk, whose rounding is relative to the result either way.
-// A tile's state (64 KB FP32, or its packed tile) arrives by bulk copies
+// One thread issues a tensor-core instruction only about every hundred
+// cycles, so the instructions of G, MMA 1 and MMA 2 come from several warps
+// at once, each accumulating into tensor-memory columns of its own that are
+// free at that moment; the parts are summed in a fixed order when read.
+// A tile's state (64 KB FP32, or its packed tile) arrives by a bulk copy
 // during the previous tile, each group's token vectors by tensor copies
 // during the previous group, a full group's outputs leave by one tensor
-// copy, and the final FP32 state by bulk copies while the next tile starts
+// copy, and the final FP32 state by a bulk copy while the next tile starts
 // (a packed tile is requantised from shared memory and its words stored by
 // every thread).  On the DAMP-exact layout the state is T = S diag(c')^{-1}:
 // the values enter as v / c' and the outputs leave as c' o.  The result
 // equals the token-by-token recurrence up to rounding (not bit for bit: the
-// order of the sums differs).
+// order of the sums differs), and is the same on every call.
 #pragma once
 
 #include <cuda.h>  // CUtensorMap and the tiled-encode signature (called through the runtime)
