@@ -112,11 +112,12 @@ constexpr int oBar = oMA + C * CA * 4, oTslot = oBar + kBars * 8;
 constexpr int oKCh = oK, oKCl = oK + C * D * 4;
 static_assert(oKCl + C * D * 4 <= oAl, "Kchk operand fits the k and q rows");
 constexpr int oV = (oTslot + 16 + 127) / 128 * 128;  // the group's v rows
-// mixed layout: key channel -> physical row of the tile's head, and the requantisation's row
-// scales, their negations and reciprocals (by physical row), and the non-finite flag
-// (DAMP-exact tiles: one scale per group of 32 columns, [group][row]; and the value-scaling factors)
+// mixed layout: key channel -> physical row of the tile's head and the reverse map, the
+// requantisation's row scales, their negations and reciprocals (by physical row), and the
+// non-finite flag (DAMP-exact tiles: one scale per group of 32 columns, [group][row]; and the
+// value-scaling factors)
 constexpr int NGM = D / kDampGroup;
-constexpr int oPinv = oV + kTok, oQs = oPinv + D, oQns = oQs + NGM * D * 4, oQrc = oQns + NGM * D * 4,
+constexpr int oPinv = oV + kTok, oPiS = oPinv + D, oQs = oPiS + D, oQns = oQs + NGM * D * 4, oQrc = oQns + NGM * D * 4,
               oQflag = oQrc + NGM * D * 4, oCs = oQflag + 16;
 constexpr int kSmem = oCs + D * 4;
 constexpr int KHM = 16;  // FP16 rows of the mixed layout the chunked form takes
@@ -285,7 +286,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kStateBytes = MIX ? (GRP ? kDampBytes : kMixBytes) : D * D * 4;
     float *csS = reinterpret_cast<float *>(smem + oCs);  // DAMP-exact: c' of the tile's head
     uint8_t *pool = static_cast<uint8_t *>(P.pool);
-    uint8_t *pinv = smem + oPinv;
+    uint8_t *pinv = smem + oPinv;  // key channel -> physical row
+    uint8_t *piS = smem + oPiS;    // physical row -> key channel
+    const uint32_t *pi4 = reinterpret_cast<const uint32_t *>(piS);  // the key channels of four physical rows
     const int items = P.B * Hv;
     TO *o_g = static_cast<TO *>(P.o);
     uint32_t ph = 0, sph = 0, iph = 0, gph = 0;  // barrier parities: MMAs, state copy, input copy, Gram
@@ -355,6 +358,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         c_slot = P.slot_idx[blockIdx.x / Hv];
         c_n = P.n_tokens ? P.n_tokens[blockIdx.x / Hv] : L;
     }
+    // mixed layouts: thread tid < D holds pi[tid] of the current tile's head, read one tile ahead
+    int c_pi = (MIX && tid < D && (int)blockIdx.x < items) ? P.pi[((int)blockIdx.x % Hv) * D + tid] : 0;
 
     for (int item = blockIdx.x; item < items && !failed; item += gridDim.x) {
         const int b = item / Hv, h = item - b * Hv;
@@ -362,6 +367,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nxi = item + gridDim.x;
         c_slot = nxi < items ? P.slot_idx[nxi / Hv] : -1;
         c_n = nxi < items ? (P.n_tokens ? P.n_tokens[nxi / Hv] : L) : 0;
+        const int pi_t = c_pi;
+        if (MIX && tid < D && nxi < items) c_pi = P.pi[(nxi % Hv) * D + tid];
         // every thread sees the same item: the skips are uniform
         if (slot < 0 || (int64_t)slot >= P.n_slots) {
             if (tid == 0) report_bits(P.status, 1);
@@ -374,11 +381,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (n == 0) continue;
         uint8_t *tile_g = pool + ((size_t)slot * Hv + h) * kStateBytes;
         float *Sg = reinterpret_cast<float *>(tile_g);
-        if constexpr (MIX) {  // this head's inverse row map (read at the tile's end)
-            if (tid < D) pinv[P.pi[h * D + tid]] = (uint8_t)tid;
-            if constexpr (GRP) {
-                if (tid < D) csS[tid] = P.cs[h * D + tid];
-            }
+        if constexpr (GRP) {  // this head's value-scaling factors
+            if (tid < D) csS[tid] = P.cs[h * D + tid];
         }
         // the next tile this CTA processes (its state and first vectors come in during this
         // tile's last group)
@@ -401,6 +405,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             iph ^= 1u;
             pendm &= ~(1u << 4);
             if (t0 == 0) {
+                // this head's row map both ways (every thread has left the previous tile, whose
+                // requantisation read them; the state-copy barrier orders them before use)
+                if (MIX && tid < D) {
+                    piS[tid] = (uint8_t)pi_t;
+                    pinv[pi_t] = (uint8_t)tid;
+                }
                 if (!wait_bar(3, sph)) {
                     failed = true;
                     break;
@@ -409,34 +419,54 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pendm &= ~(1u << 3);
                 if constexpr (MIX) {
                     // the packed tile dequantised into FP32 rows of key-channel order in the staging
-                    // buffers: thread (v, hf) takes 18 of column v's 36 word rows (FP16 pairs, INT8
-                    // quads) and writes physical row r to row pi[r]
+                    // buffers: thread (v, hf) takes column v of 18 of the 36 word rows (hf = 0: the 8
+                    // FP16 pair rows and INT8 quads 0..9; hf = 1: quads 10..27) and writes physical
+                    // row r to row pi[r]; each batch's loads go ahead of its stores
                     const uint8_t *stt = smem + oB1h;
                     float *stg = reinterpret_cast<float *>(smem + oKTh);
-                    const uint8_t *pih = P.pi + h * D;
                     const uint32_t *hw = reinterpret_cast<const uint32_t *>(stt);
                     const uint32_t *lw = reinterpret_cast<const uint32_t *>(stt + 2 * KHM * D);
                     const float *sc = reinterpret_cast<const float *>(stt + 2 * KHM * D + (D - KHM) * D);
-                    constexpr int kWordRows = KHM / 2 + (D - KHM) / 4;
-#pragma unroll 2
-                    for (int j = hf * (kWordRows / 2); j < (hf + 1) * (kWordRows / 2); ++j) {
-                        if (j < KHM / 2) {
-                            const uint32_t wd = hw[j * D + v];
-                            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&wd));
-                            stg[pih[2 * j] * D + v] = f.x;
-                            stg[pih[2 * j + 1] * D + v] = f.y;
-                        } else {
-                            const int qd = j - KHM / 2, r0 = KHM + 4 * qd;
-                            const uint32_t wd = lw[qd * D + v];
-                            // the scales of rows r0 .. r0 + 3 (DAMP-exact: of column v's group)
-                            const float4 s4 = GRP ? make_float4(sc[(4 * qd) * NGM + (v >> 5)], sc[(4 * qd + 1) * NGM + (v >> 5)],
-                                                                sc[(4 * qd + 2) * NGM + (v >> 5)], sc[(4 * qd + 3) * NGM + (v >> 5)])
-                                                  : *reinterpret_cast<const float4 *>(sc + 4 * qd);
-                            stg[pih[r0] * D + v] = __fmul_rn((float)(int8_t)(wd & 0xffu), s4.x);
-                            stg[pih[r0 + 1] * D + v] = __fmul_rn((float)(int8_t)((wd >> 8) & 0xffu), s4.y);
-                            stg[pih[r0 + 2] * D + v] = __fmul_rn((float)(int8_t)((wd >> 16) & 0xffu), s4.z);
-                            stg[pih[r0 + 3] * D + v] = __fmul_rn((float)(int8_t)(wd >> 24), s4.w);
+                    constexpr int kQuads = (D - KHM) / 4, kQB = 6;
+                    auto quads = [&](int q0, int q1) {  // INT8 quads q0 .. q1 - 1
+                        for (int b0 = q0; b0 < q1; b0 += kQB) {
+                            uint32_t wd[kQB], pr[kQB];
+                            float4 s4[kQB];
+#pragma unroll
+                            for (int i = 0; i < kQB; ++i) {
+                                const int qd = min(b0 + i, q1 - 1);  // (a batch's tail repeats the last quad)
+                                wd[i] = lw[qd * D + v];
+                                pr[i] = pi4[KHM / 4 + qd];
+                                // the scales of rows KHM + 4 qd .. + 3 (DAMP-exact: of column v's group)
+                                s4[i] = GRP ? make_float4(sc[(4 * qd) * NGM + (v >> 5)], sc[(4 * qd + 1) * NGM + (v >> 5)],
+                                                          sc[(4 * qd + 2) * NGM + (v >> 5)], sc[(4 * qd + 3) * NGM + (v >> 5)])
+                                            : *reinterpret_cast<const float4 *>(sc + 4 * qd);
+                            }
+#pragma unroll
+                            for (int i = 0; i < kQB; ++i) {
+                                stg[(pr[i] & 0xffu) * D + v] = __fmul_rn((float)(int8_t)(wd[i] & 0xffu), s4[i].x);
+                                stg[((pr[i] >> 8) & 0xffu) * D + v] = __fmul_rn((float)(int8_t)((wd[i] >> 8) & 0xffu), s4[i].y);
+                                stg[((pr[i] >> 16) & 0xffu) * D + v] = __fmul_rn((float)(int8_t)((wd[i] >> 16) & 0xffu), s4[i].z);
+                                stg[(pr[i] >> 24) * D + v] = __fmul_rn((float)(int8_t)(wd[i] >> 24), s4[i].w);
+                            }
                         }
+                    };
+                    if (hf == 0) {
+                        uint32_t wh[KHM / 2], ph[KHM / 4];
+#pragma unroll
+                        for (int j = 0; j < KHM / 2; ++j) wh[j] = hw[j * D + v];
+#pragma unroll
+                        for (int j = 0; j < KHM / 4; ++j) ph[j] = pi4[j];
+#pragma unroll
+                        for (int j = 0; j < KHM / 2; ++j) {  // FP16 rows 2 j, 2 j + 1
+                            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&wh[j]));
+                            const uint32_t p2 = ph[j >> 1] >> (16 * (j & 1));
+                            stg[(p2 & 0xffu) * D + v] = f.x;
+                            stg[((p2 >> 8) & 0xffu) * D + v] = f.y;
+                        }
+                        quads(0, (kQuads - KHM / 2) / 2);
+                    } else {
+                        quads((kQuads - KHM / 2) / 2, kQuads);
                     }
                     __syncthreads();
                 }
@@ -952,6 +982,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     return r;
                 };
                 float amax = 0.0f;  // lane i: the absmax of row 16 w + i (one scale per row)
+                float mg[16];       // DAMP-exact: the maxima of the lane's column group, row 16 w + i
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const int u = 16 * w + i;
@@ -961,11 +992,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         m = max_nan(m, __shfl_xor_sync(0xffffffffu, m, 1));
                         m = max_nan(m, __shfl_xor_sync(0xffffffffu, m, 2));
                         m = max_nan(m, __shfl_xor_sync(0xffffffffu, m, 4));
-                        const int r = pinv[u];
-                        if ((lane & 7) == 0 && r >= KHM) qs[(lane >> 3) * D + r] = m;
+                        mg[i] = m;
                     } else {
                         const float a = warp_max_abs_nan(m);  // every lane takes part in the reduction
                         amax = lane == i ? a : amax;
+                    }
+                }
+                if constexpr (GRP) {  // stored after all sixteen rows are read
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int r = pinv[16 * w + i];
+                        if ((lane & 7) == 0 && r >= KHM) qs[(lane >> 3) * D + r] = mg[i];
                     }
                 }
                 if constexpr (!GRP) {
@@ -989,30 +1026,58 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 __syncthreads();
                 const bool exact = *qflag != 0;
-                const uint8_t *pih = P.pi + h * D;  // physical row -> key channel
                 uint32_t *hw = reinterpret_cast<uint32_t *>(tile_g);
                 uint32_t *lw = reinterpret_cast<uint32_t *>(tile_g + 2 * KHM * D);
-                constexpr int kWordRows = KHM / 2 + (D - KHM) / 4;  // 8 FP16 + 28 INT8 word rows
-#pragma unroll 1
-                for (int j = hf * (kWordRows / 2); j < (hf + 1) * (kWordRows / 2); ++j) {
-                    if (j < KHM / 2) {  // FP16 rows 2j, 2j + 1: round to nearest even
-                        const __half2 hh = __floats2half2_rn(stg[pih[2 * j] * D + v], stg[pih[2 * j + 1] * D + v]);
-                        hw[j * D + v] = *reinterpret_cast<const uint32_t *>(&hh);
-                    } else {            // INT8 rows r0 .. r0 + 3
-                        const int qd = j - KHM / 2, r0 = KHM + 4 * qd;
-                        const float2 x01 = make_float2(stg[pih[r0] * D + v], stg[pih[r0 + 1] * D + v]);
-                        const float2 x23 = make_float2(stg[pih[r0 + 2] * D + v], stg[pih[r0 + 3] * D + v]);
-                        const int go = GRP ? (v >> 5) * D : 0;  // column v's scale group
-                        const float4 rc4 = *reinterpret_cast<const float4 *>(qrc + go + r0);
-                        uint32_t wd;
-                        if (!exact) {
-                            if constexpr (FUSED) wd = quant_quad_rcp(x01, x23, rc4);
-                            else wd = quant_quad(x01, x23, *reinterpret_cast<const float4 *>(qns + go + r0), rc4);
-                        } else {
-                            wd = quant_quad_cold<FUSED>(x01, x23, *reinterpret_cast<const float4 *>(qs + go + r0), rc4);
+                const int go = GRP ? (v >> 5) * D : 0;  // column v's scale group
+                // thread (v, hf) writes column v of 18 of the 36 word rows (hf = 0: the 8 FP16 pair
+                // rows and INT8 quads 0..9; hf = 1: quads 10..27); each batch's loads go ahead of its
+                // quantisation and stores
+                constexpr int kQuads = (D - KHM) / 4, kQB = 6;
+                auto quads = [&](int q0, int q1) {
+                    for (int b0 = q0; b0 < q1; b0 += kQB) {
+                        float2 x01[kQB], x23[kQB];
+                        float4 rc4[kQB], s4[kQB];  // reciprocals; negated scales (IEEE), or scales (exact path)
+#pragma unroll
+                        for (int i = 0; i < kQB; ++i) {
+                            const int qd = min(b0 + i, q1 - 1), r0 = KHM + 4 * qd;
+                            const uint32_t pr = pi4[r0 / 4];
+                            x01[i] = make_float2(stg[(pr & 0xffu) * D + v], stg[((pr >> 8) & 0xffu) * D + v]);
+                            x23[i] = make_float2(stg[((pr >> 16) & 0xffu) * D + v], stg[(pr >> 24) * D + v]);
+                            rc4[i] = *reinterpret_cast<const float4 *>(qrc + go + r0);
+                            if (exact || !FUSED) s4[i] = *reinterpret_cast<const float4 *>((exact ? qs : qns) + go + r0);
                         }
-                        lw[qd * D + v] = wd;
+#pragma unroll
+                        for (int i = 0; i < kQB; ++i) {
+                            if (b0 + i >= q1) break;
+                            uint32_t wd;
+                            if (!exact) {
+                                if constexpr (FUSED) wd = quant_quad_rcp(x01[i], x23[i], rc4[i]);
+                                else wd = quant_quad(x01[i], x23[i], s4[i], rc4[i]);
+                            } else {
+                                wd = quant_quad_cold<FUSED>(x01[i], x23[i], s4[i], rc4[i]);
+                            }
+                            lw[(b0 + i) * D + v] = wd;
+                        }
                     }
+                };
+                if (hf == 0) {  // FP16 rows 2 j, 2 j + 1: round to nearest even
+                    uint32_t ph[KHM / 4];
+#pragma unroll
+                    for (int j = 0; j < KHM / 4; ++j) ph[j] = pi4[j];
+                    float2 xh[KHM / 2];
+#pragma unroll
+                    for (int j = 0; j < KHM / 2; ++j) {
+                        const uint32_t p2 = ph[j >> 1] >> (16 * (j & 1));
+                        xh[j] = make_float2(stg[(p2 & 0xffu) * D + v], stg[((p2 >> 8) & 0xffu) * D + v]);
+                    }
+#pragma unroll
+                    for (int j = 0; j < KHM / 2; ++j) {
+                        const __half2 hh = __floats2half2_rn(xh[j].x, xh[j].y);
+                        hw[j * D + v] = *reinterpret_cast<const uint32_t *>(&hh);
+                    }
+                    quads(0, (kQuads - KHM / 2) / 2);
+                } else {
+                    quads((kQuads - KHM / 2) / 2, kQuads);
                 }
             }
         }
