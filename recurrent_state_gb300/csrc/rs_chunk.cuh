@@ -982,27 +982,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                     return r;
                 };
                 float amax = 0.0f;  // lane i: the absmax of row 16 w + i (one scale per row)
-                float mg[16];       // DAMP-exact: the maxima of the lane's column group, row 16 w + i
+                float mg[16];       // DAMP-exact: the lane's maximum of its four columns, row 16 w + i
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const int u = 16 * w + i;
                     const float4 x4 = reinterpret_cast<const float4 *>(stg + u * D)[lane];
-                    float m = max_nan(max_nan(fabsf(x4.x), fabsf(x4.y)), max_nan(fabsf(x4.z), fabsf(x4.w)));
-                    if constexpr (GRP) {  // the lane's group (lanes 8 g .. 8 g + 7: columns 32 g ..)
-                        m = max_nan(m, __shfl_xor_sync(0xffffffffu, m, 1));
-                        m = max_nan(m, __shfl_xor_sync(0xffffffffu, m, 2));
-                        m = max_nan(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                    const float m = max_nan(max_nan(fabsf(x4.x), fabsf(x4.y)), max_nan(fabsf(x4.z), fabsf(x4.w)));
+                    if constexpr (GRP) {
                         mg[i] = m;
                     } else {
                         const float a = warp_max_abs_nan(m);  // every lane takes part in the reduction
                         amax = lane == i ? a : amax;
                     }
                 }
-                if constexpr (GRP) {  // stored after all sixteen rows are read
+                if constexpr (GRP) {
+                    // the maxima over each group's eight lanes (lanes 8 g .. 8 g + 7: columns 32 g ..),
+                    // halving the rows at each exchange: at the level of lane bit b the lane keeps the
+                    // rows whose bit 3 - b equals its own bit b and sends the others, so that 14
+                    // exchanges leave it the group maxima of rows 8 b0 + 4 b1 + 2 b2 + {0, 1}
+                    const bool b0 = lane & 1, b1 = lane & 2, b2 = lane & 4;
+                    float n8[8], n4[4], n2[2];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
+                    for (int k = 0; k < 8; ++k) {
+                        const float keep = b0 ? mg[k + 8] : mg[k], send = b0 ? mg[k] : mg[k + 8];
+                        n8[k] = max_nan(keep, __shfl_xor_sync(0xffffffffu, send, 1));
+                    }
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float keep = b1 ? n8[k + 4] : n8[k], send = b1 ? n8[k] : n8[k + 4];
+                        n4[k] = max_nan(keep, __shfl_xor_sync(0xffffffffu, send, 2));
+                    }
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        const float keep = b2 ? n4[k + 2] : n4[k], send = b2 ? n4[k] : n4[k + 2];
+                        n2[k] = max_nan(keep, __shfl_xor_sync(0xffffffffu, send, 4));
+                    }
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        const int i = 8 * b0 + 4 * b1 + 2 * b2 + k;
                         const int r = pinv[16 * w + i];
-                        if ((lane & 7) == 0 && r >= KHM) qs[(lane >> 3) * D + r] = mg[i];
+                        if (r >= KHM) qs[(lane >> 3) * D + r] = n2[k];
                     }
                 }
                 if constexpr (!GRP) {
