@@ -265,8 +265,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dG = tc::smem_desc(smem + oB1h, 128, D * 32);
     const uint64_t dKCh = tc::smem_desc(smem + oKCh, 128, D * 32), dKCl = tc::smem_desc(smem + oKCl, 128, D * 32);
     // MMA 1: D1 = S0^T [Khat ; Qhat ; Khat_lo ; Qhat_lo]^T + S0_lo^T [Khat ; Qhat]^T, issued by one
-    // thread of warp 2 (k-steps 0..15, into the D1 columns) and of warp 3 (k-steps 16..31, into
-    // the Gram and W^T columns, then free); R and the outputs add the two parts
+    // thread of warp 2 (k-steps 0..7 of the 16, both terms, into the D1 columns) and of warp 3
+    // (k-steps 8..15, into the Gram and W^T columns, then free); R and the outputs add the two parts
     auto issue_mma1 = [&]() {
         if ((tid & 31) == 0) {
             tc::fence_after_sync();
@@ -341,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint8_t *src = pool + ((size_t)P.slot_idx[bb] * Hv + hh) * kStateBytes;
         if (tid == 0) {
             mbar_arrive_expect_tx(&bars[3], (uint32_t)kStateBytes);
-            bulk_g2s(smem + oB1h, src, kStateBytes, &bars[3]);  // one copy: each issue costs thread 0 time
+            bulk_g2s(smem + oB1h, src, kStateBytes, &bars[3]);  // the whole tile in one copy
         }
         pendm |= 1u << 3;
     };
