@@ -397,25 +397,33 @@ _LAST_MEDIAN = {"s": None, "n": 0}
 
 
 def _time(torch, fn, iters, warm=3, repeats=20):
-    """Mean seconds per launch over ``iters`` back-to-back launches (CUDA events
-    around the window); also times ``max(repeats, 20)`` launches one by one,
-    each between its own pair of events, and keeps their median."""
+    """Seconds per launch: ``iters`` launches split into up to five windows of
+    back-to-back launches (CUDA events around each window), and the median of
+    the windows' means, so that one stall of the host between two launches
+    cannot move the figure; also times ``max(repeats, 20)`` launches one by
+    one, each between its own pair of events, and keeps their median."""
     warm = max(3, warm)
     for i in range(warm):
         fn(i)
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for i in range(iters):
-        fn(warm + i)
-    e1.record()
-    torch.cuda.synchronize()
-    mean = e0.elapsed_time(e1) / 1e3 / iters
+    nw = max(1, min(5, iters))
+    per_w = max(1, iters // nw)
+    means, k = [], warm
+    for _ in range(nw):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(per_w):
+            fn(k)
+            k += 1
+        e1.record()
+        torch.cuda.synchronize()
+        means.append(e0.elapsed_time(e1) / 1e3 / per_w)
+    mean = sorted(means)[nw // 2]
     n = max(repeats, 20)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
     for i, (a, b) in enumerate(ev):
         a.record()
-        fn(warm + iters + i)
+        fn(k + i)
         b.record()
     torch.cuda.synchronize()
     per = sorted(a.elapsed_time(b) / 1e3 for a, b in ev)
